@@ -1,0 +1,219 @@
+"""Seeded synthetic inputs for the routed-expert MoE layer.
+
+This module is shared by the CUDA path's tests/bench and by the oracle's tests.
+It draws random numbers and stores them in the layer's storage formats; it
+holds none of the layer's arithmetic (no dequantisation, no router, no top-k,
+no FFN, no combine).  Everything is numpy on the host.
+
+Layer shapes follow the qwen3_5_moe routed-expert layer described on the page
+"Qwen3.6-35B-A3B (qwen3_5_moe) on the native Metal engine: proposal and gate"
+(section "What it is": 256 experts, 8 picked, plus a shared expert) and on
+"r9700-vllm-blogs part 13" (hidden size 2048, moe_intermediate 512).  The
+storage format is the MLX affine rule quoted in the same proposal (experts at
+4 bits in groups of 64, router at 8 bits): a group of 64 consecutive inputs of
+one output row shares one bf16 scale and one bf16 bias.
+
+Storage layout (all little-endian, rows dense):
+  x        bf16 bits, uint16 [T, H]
+  router   codes uint8 [E, H], scales/biases bf16 bits uint16 [E, H/64]
+  v        shared-expert gate vector, bf16 bits uint16 [H]
+  gate, up codes uint8 [E, I, H/2] (4-bit: element j of a row is byte j//2,
+           low nibble for even j), scales/biases uint16 [E, I, H/64]
+  down     codes uint8 [E, H, I/2], scales/biases uint16 [E, H, I/64]
+  s_gate, s_up, s_down: the shared expert, same layouts with a leading dim of 1
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+GROUP = 64
+
+
+@dataclasses.dataclass(frozen=True)
+class LayerShape:
+    hidden: int
+    inter: int
+    n_experts: int
+    top_k: int
+    has_shared: int = 1
+    bits: int = 4
+    router_bits: int = 8
+    group: int = GROUP
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One named workload: a layer shape, a token count and the input recipe."""
+    name: str
+    shape: LayerShape
+    tokens: int
+    seed: int
+    zipf_s: float = 0.0        # > 0: per-expert log-Zipf logit bias
+    tie_every: int = 0         # > 0: every n-th row of supplied logits is snapped to 1/8
+
+
+QWEN_SHAPE = LayerShape(hidden=2048, inter=512, n_experts=256, top_k=8)
+TINY_SHAPE = LayerShape(hidden=256, inter=64, n_experts=16, top_k=2)
+
+WORKLOADS = [
+    Workload("tiny_T4_H256_E16_k2", TINY_SHAPE, 4, seed=0),
+    Workload("decode_T1_H2048_E256_k8", QWEN_SHAPE, 1, seed=1),
+    Workload("decode_T16_H2048_E256_k8", QWEN_SHAPE, 16, seed=2),
+    Workload("prefill_T512_H2048_E256_k8", QWEN_SHAPE, 512, seed=3),
+    Workload("prefill_T4096_zipf1.1_H2048_E256_k8", QWEN_SHAPE, 4096, seed=4,
+             zipf_s=1.1, tie_every=20),
+]
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even); returns uint16 bits."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclasses.dataclass
+class QMat:
+    codes: np.ndarray    # uint8 [..., rows, in*bits/8]
+    scales: np.ndarray   # uint16 [..., rows, in/64]
+    biases: np.ndarray   # uint16 [..., rows, in/64]
+
+
+@dataclasses.dataclass
+class LayerWeights:
+    shape: LayerShape
+    router: QMat
+    gate: QMat
+    up: QMat
+    down: QMat
+    s_gate: QMat
+    s_up: QMat
+    s_down: QMat
+    shared_gate_vec: np.ndarray   # uint16 [H]
+
+    def nbytes(self) -> int:
+        tot = self.shared_gate_vec.nbytes
+        for m in (self.router, self.gate, self.up, self.down, self.s_gate, self.s_up, self.s_down):
+            tot += m.codes.nbytes + m.scales.nbytes + m.biases.nbytes
+        return tot
+
+
+def _expert_qmat(rng: np.random.Generator, n: int, rows: int, cols: int) -> QMat:
+    """4-bit codes uniform in 0..15, scale ~ U(0.005, 0.02) rounded to bf16, bias = -8*scale."""
+    codes = rng.integers(0, 256, size=(n, rows, cols // 2), dtype=np.uint8)
+    s = f32_to_bf16_bits(rng.uniform(0.005, 0.02, size=(n, rows, cols // GROUP)).astype(np.float32))
+    # -8 * s is exact in bf16 (power-of-two scaling of a bf16 value).
+    b = f32_to_bf16_bits(-8.0 * bf16_bits_to_f32(s))
+    return QMat(codes, s, b)
+
+
+def _quantise_8bit(w: np.ndarray) -> QMat:
+    """Generator-side 8-bit affine quantiser for the router (group 64 along the input dim).
+
+    Per group: bias = min, scale = (max - min) / 255, both rounded to bf16;
+    code = clamp(rint((w - bias) / scale), 0, 255).  Only the code
+    distribution depends on this rule: both the kernels and the oracle read
+    the stored codes, scales and biases.
+    """
+    rows, cols = w.shape
+    g = w.reshape(rows, cols // GROUP, GROUP).astype(np.float32)
+    lo = g.min(axis=2)
+    hi = g.max(axis=2)
+    b_bits = f32_to_bf16_bits(lo)
+    s_bits = f32_to_bf16_bits((hi - lo) / 255.0)
+    b = bf16_bits_to_f32(b_bits)[..., None]
+    s = bf16_bits_to_f32(s_bits)[..., None]
+    s_safe = np.where(s > 0, s, 1.0)
+    q = np.clip(np.rint((g - b) / s_safe), 0, 255).astype(np.uint8)
+    return QMat(q.reshape(rows, cols), s_bits, b_bits)
+
+
+def make_weights(shape: LayerShape, seed: int) -> LayerWeights:
+    """Draw one layer's weights.  Draw order: router, v, gate, up, down, shared gate/up/down."""
+    assert shape.bits == 4 and shape.router_bits == 8 and shape.group == GROUP
+    H, I, E = shape.hidden, shape.inter, shape.n_experts
+    rng = np.random.default_rng([seed, 1])
+    router = _quantise_8bit(rng.normal(0.0, 0.02, size=(E, H)).astype(np.float32))
+    v = f32_to_bf16_bits(rng.normal(0.0, 0.02, size=(H,)).astype(np.float32))
+    gate = _expert_qmat(rng, E, I, H)
+    up = _expert_qmat(rng, E, I, H)
+    down = _expert_qmat(rng, E, H, I)
+    ns = 1 if shape.has_shared else 0
+    s_gate = _expert_qmat(rng, ns, I, H)
+    s_up = _expert_qmat(rng, ns, I, H)
+    s_down = _expert_qmat(rng, ns, H, I)
+    return LayerWeights(shape, router, gate, up, down, s_gate, s_up, s_down, v)
+
+
+def make_x(shape: LayerShape, tokens: int, seed: int, stream: int = 0) -> np.ndarray:
+    """x ~ N(0, 1) rounded to bf16, [T, H] uint16 bits."""
+    rng = np.random.default_rng([seed, 2, stream])
+    return f32_to_bf16_bits(rng.normal(0.0, 1.0, size=(tokens, shape.hidden)).astype(np.float32))
+
+
+def zipf_bias(shape: LayerShape, s: float, seed: int) -> np.ndarray:
+    """Per-expert logit bias -s*ln(r_e), r_e = 1 + pi(e) for a seeded permutation pi.
+
+    Adding ln of a Zipf(s) prior to the logits makes expert popularity follow
+    that prior: a few experts take most tokens.
+    """
+    rng = np.random.default_rng([seed, 3])
+    ranks = 1 + rng.permutation(shape.n_experts)
+    return (-s * np.log(ranks.astype(np.float64))).astype(np.float32)
+
+
+def snap_rows_to_eighths(logits: np.ndarray, every: int) -> np.ndarray:
+    """Return a copy of fp32 logits with rows t % every == 0 snapped to multiples of 1/8.
+
+    Snapping to a coarse grid makes exact equal logits common, which exercises
+    the lower-id tie rule of the top-k.
+    """
+    out = np.array(logits, dtype=np.float32, copy=True)
+    rows = np.arange(0, out.shape[0], every)
+    out[rows] = (np.rint(out[rows].astype(np.float64) * 8.0) / 8.0).astype(np.float32)
+    return out
+
+
+def workload_inputs(wl: Workload, stream: int = 0):
+    """(weights, x, router_bias or None) for a named workload."""
+    w = make_weights(wl.shape, wl.seed)
+    x = make_x(wl.shape, wl.tokens, wl.seed, stream)
+    bias = zipf_bias(wl.shape, wl.zipf_s, wl.seed) if wl.zipf_s > 0 else None
+    return w, x, bias
+
+
+def active_expert_bytes(shape: LayerShape) -> int:
+    """Bytes of one expert's gate+up+down codes, scales and biases."""
+    H, I = shape.hidden, shape.inter
+    per = lambda rows, cols: rows * cols * shape.bits // 8 + 2 * 2 * rows * (cols // GROUP)
+    return 2 * per(I, H) + per(H, I)
+
+
+def router_bytes(shape: LayerShape) -> int:
+    H, E = shape.hidden, shape.n_experts
+    return E * H * shape.router_bits // 8 + 2 * 2 * E * (H // GROUP) + 2 * H
+
+
+def expert_flops_per_token(shape: LayerShape) -> int:
+    """Multiply-adds x2 of the k routed + shared expert FFNs for one token."""
+    slots = shape.top_k + (1 if shape.has_shared else 0)
+    return slots * 3 * 2 * shape.hidden * shape.inter
+
+
+def nominal_tokens_per_expert(wl: Workload) -> float:
+    return wl.tokens * wl.shape.top_k / wl.shape.n_experts
+
+
+if __name__ == "__main__":
+    for wl in WORKLOADS:
+        print(wl.name, active_expert_bytes(wl.shape), router_bytes(wl.shape),
+              expert_flops_per_token(wl.shape), math.ceil(nominal_tokens_per_expert(wl)))
