@@ -1,0 +1,202 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) routed-expert MoE layer library (libmoe.so).
+ *
+ * The layer is the qwen3_5_moe routed-expert MLP with the routing and combine
+ * contract set out on the page "Qwen3.6-35B-A3B (qwen3_5_moe) on the native
+ * Metal engine: proposal and gate", section "What I'd build, in slices",
+ * slice "The family, plain decode":
+ *   1. fp32 router logits over the E experts, and the shared expert's fp32 gate
+ *      logit gamma = x . v;
+ *   2. top-k experts by logit, ties going to the lower expert id;
+ *   3. pick weights exp(l - l_top) over the k picks, normalised over the picks
+ *      (the "softmax top-8" of the "Qwen-3.6-35B-A3B-SIQ-K6-K4K3" model card,
+ *      section "Reproduction"), rounded to bf16;
+ *   4. the shared expert is one more slot with weight bf16(sigmoid(bf16(gamma)));
+ *   5. each expert is a SwiGLU MLP, y_e = W_down (silu(W_gate x) * (W_up x))
+ *      (the Gate section's "expert gate/up pair, expert down");
+ *   6. y = bf16( sum_j p_j y_{e_j} + w_s y_shared ), rounded once.
+ * Weights are MLX affine quantised (same slice): experts 4-bit, router 8-bit,
+ * groups of 64 consecutive inputs of one output row sharing a bf16 scale s
+ * and bias b, w = s * q + b.
+ *
+ * Conventions shared by every entry point
+ *   - Every function returns an int status (enum moe_status).  Argument,
+ *     shape and format errors are found on the host, before anything is
+ *     enqueued, and leave every buffer untouched.
+ *   - Pointers to tensors are caller-owned DEVICE memory unless a parameter
+ *     says otherwise.  The library never allocates, frees or synchronises,
+ *     except moe_get_device_status, which synchronises the given stream.
+ *   - Every tensor pointer must be 16-byte aligned; rows are dense (no
+ *     padding between rows).  bf16 tensors are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All work is enqueued asynchronously on it, in order.
+ *   - `ws`/`ws_bytes` is caller-owned device scratch of at least
+ *     moe_workspace_size() bytes for the call's T; it must not be shared by
+ *     calls that may run concurrently.  Its contents between calls are
+ *     meaningless, except that moe_get_device_status reads the status word
+ *     that kernels running on it set.
+ *   - Device-side failures (a bounded wait that ran out, an index out of
+ *     range) never trap: the kernel writes a nonzero code into the workspace
+ *     status word and returns; the host reads it with moe_get_device_status.
+ *
+ * Storage formats (MLX layout, [out, in] with quantisation along `in`)
+ *   codes   4-bit: uint8 [rows, in/2], element j of a row in byte j/2, low
+ *           nibble for even j.  8-bit: uint8 [rows, in].
+ *   scales, biases: bf16 [rows, in/group].
+ *   Stacked expert matrices add a leading expert dimension:
+ *     gate, up   [E, inter, hidden]     down  [E, hidden, inter]
+ *     s_gate, s_up [inter, hidden]      s_down [hidden, inter]   (shared expert)
+ *     router     [E, hidden] (8-bit)    shared_gate_vec bf16 [hidden]
+ */
+#ifndef QMOE_GB300_MOE_H
+#define QMOE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative or oversized size */
+    MOE_ERR_UNSUPPORTED = 2,  /* a format or shape the kernels do not implement */
+    MOE_ERR_WORKSPACE = 3,    /* ws_bytes below moe_workspace_size() */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute query) */
+    MOE_ERR_TIMEOUT = 5,      /* device status: a bounded wait inside a kernel ran out */
+    MOE_ERR_DEVICE = 6        /* device status: a kernel found an index out of range */
+};
+
+enum moe_path {
+    MOE_PATH_AUTO = 0,     /* decode for T <= 16, prefill above */
+    MOE_PATH_DECODE = 1,   /* weight-streaming dequant-GEMV kernels (any T, meant for small T) */
+    MOE_PATH_PREFILL = 2   /* tcgen05 grouped GEMM kernels (any T >= 1) */
+};
+
+/* Layer shape.  Supported: group == 64, bits == 4, router_bits == 8,
+ * hidden and inter multiples of 64 (hidden <= 8192, inter <= 4096),
+ * 1 <= top_k <= min(n_experts, 16), 1 <= n_experts <= 256, has_shared in {0,1}.
+ * Anything else returns MOE_ERR_UNSUPPORTED. */
+typedef struct moe_config {
+    int hidden;       /* H */
+    int inter;        /* I, intermediate size of every expert, shared included */
+    int n_experts;    /* E routed experts */
+    int top_k;        /* k picks per token */
+    int group;        /* quantisation group along the input dimension */
+    int bits;         /* expert code width */
+    int router_bits;  /* router code width */
+    int has_shared;   /* 1: the layer has a shared expert slot */
+} moe_config;
+
+/* One affine-quantised matrix (or a stack of them), device pointers. */
+typedef struct moe_qmat {
+    const uint8_t *codes;
+    const uint16_t *scales;  /* bf16 */
+    const uint16_t *biases;  /* bf16 */
+} moe_qmat;
+
+/* All weights of one layer, device pointers.  s_* and shared_gate_vec may be
+ * NULL when has_shared == 0. */
+typedef struct moe_weights {
+    moe_qmat router;   /* [E, H], router_bits */
+    moe_qmat gate;     /* [E, I, H] */
+    moe_qmat up;       /* [E, I, H] */
+    moe_qmat down;     /* [E, H, I] */
+    moe_qmat s_gate;   /* [I, H] */
+    moe_qmat s_up;     /* [I, H] */
+    moe_qmat s_down;   /* [H, I] */
+    const uint16_t *shared_gate_vec;  /* bf16 [H] */
+} moe_weights;
+
+/* Human-readable name of a status code; never NULL, static storage. */
+MOE_API const char *moe_status_string(int status);
+
+/* Checks a configuration against the supported set (see moe_config). */
+MOE_API int moe_check_config(const moe_config *cfg);
+
+/* Bytes of workspace every entry point below needs for T tokens (0 <= T <= 65536).
+ * *bytes receives the size; the same workspace serves every entry point. */
+MOE_API int moe_workspace_size(const moe_config *cfg, int T, size_t *bytes);
+
+/* Steps 1-4: router logits, top-k, pick weights, shared weight.
+ *   x           bf16 [T, H]
+ *   router_bias fp32 [E] added to every computed logit with one fp32 rounding
+ *               (l = fp32(l + bias_e)); NULL for none.  Ignored with logits_in.
+ *   logits_in   fp32 [T, E] logits to route on instead of the router GEMV; NULL
+ *               to compute them.  Lets a caller with its own router use the layer.
+ *   logits_out  fp32 [T, E] or NULL: the logits the top-k ran on.
+ *   ids         int32 [T, k] expert ids in rank order (descending logit, ties
+ *               to the lower id).
+ *   p           bf16 [T, k] pick weights in the same order.
+ *   w_shared    bf16 [T] shared-slot weight; NULL allowed; all zero when
+ *               has_shared == 0.
+ * T == 0 is valid and enqueues nothing. */
+MOE_API int moe_route(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T,
+              const float *router_bias, const float *logits_in, float *logits_out,
+              int32_t *ids, uint16_t *p, uint16_t *w_shared,
+              void *ws, size_t ws_bytes, void *stream);
+
+/* Groups the T*k routed slots by expert: a stable counting sort of the flat
+ * slot index f = t*k + j by ids[f] (so slots of one expert are in increasing t).
+ *   counts   int32 [E]      slots routed to each expert
+ *   offsets  int32 [E + 1]  exclusive prefix sum of counts
+ *   perm     int32 [T*k]    perm[offsets[e] + r] = r-th slot routed to e
+ *   inv_perm int32 [T*k]    inv_perm[f] = position of slot f in perm
+ * ids entries outside [0, E) set MOE_ERR_DEVICE in the status word and the
+ * outputs are then unspecified. */
+MOE_API int moe_permute(const moe_config *cfg, const int32_t *ids, int T, int32_t *counts,
+                int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                void *ws, size_t ws_bytes, void *stream);
+
+/* Step 5 and the weighted sum of step 6 without its rounding:
+ *   acc[t, :] += sum_j p[t,j] * y_{ids[t,j]}(x_t) + w_shared[t] * y_shared(x_t)
+ * acc is fp32 [T, H], caller-initialised (zero for a plain layer).
+ * ids/p/w_shared as produced by moe_route; counts/offsets/perm as produced by
+ * moe_permute from the same ids.  w_shared may be NULL when has_shared == 0.
+ * path selects the kernels (enum moe_path).  On the decode path every acc
+ * element receives one fixed-order sum (bit-reproducible for a given input,
+ * independent of the other tokens in the batch); the prefill path adds slot
+ * contributions with fp32 atomics, so the order of additions (and the last
+ * bits of acc) may vary between runs. */
+MOE_API int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T,
+                   const int32_t *ids, const uint16_t *p, const uint16_t *w_shared,
+                   const int32_t *counts, const int32_t *offsets, const int32_t *perm,
+                   float *acc, int path, void *ws, size_t ws_bytes, void *stream);
+
+/* The single rounding of step 6: y = bf16_rne(acc), acc fp32 [T, H], y bf16 [T, H]. */
+MOE_API int moe_combine(const moe_config *cfg, int T, const float *acc, uint16_t *y, void *stream);
+
+/* The whole layer: route, permute, expert FFNs and combine.
+ *   y        bf16 [T, H] output.
+ *   ids_out  int32 [T, k], p_out bf16 [T, k], w_shared_out bf16 [T]: optional
+ *            copies of the routing (NULL to skip).
+ * Other arguments as in moe_route / moe_expert_ffn.  With MOE_PATH_DECODE
+ * (or AUTO with T <= 16) row t of y, ids_out, p_out and w_shared_out is
+ * bit-identical to the result of a T = 1 call on row t alone. */
+MOE_API int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T,
+                const float *router_bias, const float *logits_in, uint16_t *y,
+                int32_t *ids_out, uint16_t *p_out, uint16_t *w_shared_out, int path,
+                void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of `ws`.
+ * *device_status receives MOE_OK or the first error code a kernel recorded. */
+MOE_API int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_status);
+
+/* Upper bound on the polls of every bounded wait inside the kernels (mbarrier
+ * waits of the tensor-core pipeline).  A wait that reaches it records
+ * MOE_ERR_TIMEOUT and the kernel returns early.  Default 1 << 26 polls
+ * (about a second); values <= 0 restore the default.  Affects launches
+ * enqueued after the call; meant for fault-handling tests. */
+MOE_API int moe_set_wait_limit(long long polls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMOE_GB300_MOE_H */

@@ -1,0 +1,413 @@
+// Decode path: weight-streaming dequant-GEMV over the selected experts.
+//
+// Meant for small token counts (the "gemv MoE path" at batch size 1 of the page
+// "POC for qwen3.5 / qwen3.6 support optimized for AGX Orin", Phase 1-4): the
+// cost is the bytes of the experts the batch selected, each streamed from HBM
+// exactly once, whatever number of the batch's tokens picked it.
+//
+// Arithmetic.  A weight of group g of a row is w = s_g * q + b_g (MLX affine,
+// 4-bit codes, group 64).  Over one group of 64 inputs
+//     sum_j w_j x_j = s_g * sum_j (128 + q_j) x_j + (b_g - 128 s_g) * sum_j x_j.
+// 128 + q is exact in bf16 (OR of the nibble into the mantissa of 128.0), and
+// the products with a bf16 x are exact, so the two sums are computed on the
+// tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate): one MMA chain
+// with the codes as A, and one with an all-ones A that yields sum_j x_j.  The
+// per-group scale and bias are then applied in fp32 per row.  The down
+// projection works the same way in fp16: 1024 + q is exact in fp16 and the
+// intermediate h is stored as fp16.  Nothing of a weight is rounded; the only
+// rounding before fp32 accumulation is the fp16 storage of h (11 significant
+// bits: bf16's 8 would put the layer output outside the parity tolerance).
+//
+// Fragment layout.  Thread (g = lane/4, t = lane%4) loads 8 bytes (16 codes) of
+// rows g and g+8 of a group: bytes 8t..8t+7.  A u32 of 8 nibbles splits into
+// four bf16x2 registers holding elements (0,4) (1,5) (2,6) (3,7); MMA m of the
+// group's four takes registers 2m, 2m+1.  The MMA's k order is therefore a
+// permutation of the group's inputs; the B fragment (x or h) is permuted the
+// same way with byte permutes, so each product still pairs w_j with x_j.
+// Every output element is one column of the MMA and never mixes tokens, so a
+// token's result does not depend on the batch it is in.
+#include "kernels.cuh"
+
+namespace qmoe {
+namespace {
+
+// D += A B, m16n8k16, fp32 accumulate; F16 selects fp16 operands, else bf16.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    if constexpr (F16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// 8 nibbles -> four 16-bit pairs of (OFF + q), elements (0,4), (1,5), (2,6), (3,7).
+// bf16: OR into the mantissa of 128.0 (0x4300) gives 128 + q exactly; fp16: OR
+// into the mantissa of 1024.0 (0x6400) gives 1024 + q exactly.
+template <bool F16>
+__device__ __forceinline__ void nib8(uint32_t u, uint32_t *r)
+{
+    constexpr uint32_t base = F16 ? 0x64006400u : 0x43004300u;
+    r[0] = (u & 0x000F000Fu) | base;
+    r[1] = ((u >> 4) & 0x000F000Fu) | base;
+    r[2] = ((u >> 8) & 0x000F000Fu) | base;
+    r[3] = ((u >> 12) & 0x000F000Fu) | base;
+}
+
+// 16 consecutive bf16 (two uint4) -> eight bf16x2 in the codes' element order.
+__device__ __forceinline__ void permute_b(const uint4 &lo, const uint4 &hi, uint32_t *b)
+{
+    b[0] = prmt(lo.x, lo.z, 0x5410u);
+    b[1] = prmt(lo.x, lo.z, 0x7632u);
+    b[2] = prmt(lo.y, lo.w, 0x5410u);
+    b[3] = prmt(lo.y, lo.w, 0x7632u);
+    b[4] = prmt(hi.x, hi.z, 0x5410u);
+    b[5] = prmt(hi.x, hi.z, 0x7632u);
+    b[6] = prmt(hi.y, hi.w, 0x5410u);
+    b[7] = prmt(hi.y, hi.w, 0x7632u);
+}
+
+// One group (64 inputs) of a 16-row block against one n8 tile of B:
+// codes u64 of rows g / g+8, B registers bp[8]; accumulates the code chain
+// sum (OFF + q) b and, with do_ones, the ones chain sum b over the group.
+template <bool F16>
+__device__ __forceinline__ void group_mma(uint2 c_lo, uint2 c_hi, const uint32_t *bp, float (&dq)[4],
+                                          float (&dx)[4], bool do_ones)
+{
+    constexpr uint32_t ones = F16 ? 0x3C003C00u : 0x3F803F80u;   // {1, 1}
+    uint32_t ra[8], rb[8];
+    nib8<F16>(c_lo.x, ra);
+    nib8<F16>(c_lo.y, ra + 4);
+    nib8<F16>(c_hi.x, rb);
+    nib8<F16>(c_hi.y, rb + 4);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        mma16816<F16>(dq, ra[2 * m], rb[2 * m], ra[2 * m + 1], rb[2 * m + 1], bp[2 * m], bp[2 * m + 1]);
+        if (do_ones) mma16816<F16>(dx, ones, ones, ones, ones, bp[2 * m], bp[2 * m + 1]);
+    }
+}
+
+struct ExpertView {
+    const uint8_t *codes;
+    const uint16_t *scales;
+    const uint16_t *biases;
+};
+
+__device__ __forceinline__ ExpertView expert_view(const QMatDev &m, int e, int rows, int cols)
+{
+    ExpertView v;
+    const size_t eo = (size_t)e * rows;
+    v.codes = m.codes + eo * (cols / 2);
+    v.scales = m.scales + eo * (cols / kGroup);
+    v.biases = m.biases + eo * (cols / kGroup);
+    return v;
+}
+
+// Columns (tokens) of a work item: token index and slot index f.
+__device__ __forceinline__ void item_columns(const ExpertArgs &a, const WorkItem &it, int *s_tok, int *s_slot)
+{
+    const int c = threadIdx.x;
+    if (c < kDecodeMaxTok) {
+        int t = -1, f = -1;
+        if (c < it.ntok) {
+            if (it.expert == a.E) {
+                t = it.tok0 + c;
+                f = a.T * a.k + t;
+            } else {
+                const int pos = __ldg(a.offsets + it.expert) + it.tok0 + c;
+                f = (pos >= 0 && pos < a.T * a.k) ? __ldg(a.perm + pos) : -1;
+                if (f < 0 || f >= a.T * a.k) {      // offsets/perm inconsistent with the work list
+                    record_status(a.status, MOE_ERR_DEVICE);
+                    f = -1;
+                }
+                t = f < 0 ? -1 : f / a.k;
+            }
+        }
+        s_tok[c] = t;
+        s_slot[c] = f;
+    }
+}
+
+// ------------------------------------------------------------ gate/up + SwiGLU
+//
+// grid (I/16, max items); 128 threads.  Block (rb, item) computes rows
+// [16 rb, 16 rb + 16) of gate and up for the item's <= 16 tokens; warp w takes
+// a quarter of the hidden groups and the quarters are added in warp order.
+template <int NT>
+__global__ void __launch_bounds__(128) decode_gateup_kernel(ExpertArgs a)
+{
+    extern __shared__ uint4 s_x[];                 // [NT*8][H/8 + 1] (one uint4 of padding per row)
+    __shared__ float s_red[4][2][16][NT * 8];      // [warp][gate/up][row][col]
+    __shared__ int s_tok[kDecodeMaxTok], s_slot[kDecodeMaxTok];
+    if ((int)blockIdx.y >= __ldg(a.nwork + 0)) return;
+    const WorkItem it = a.work[blockIdx.y];
+    const int H = a.H, I = a.I, G = H / kGroup, rowu4 = H / 8 + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const bool is_shared = it.expert == a.E;
+
+    item_columns(a, it, s_tok, s_slot);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < NT * 8 * (H / 8); idx += blockDim.x) {
+        const int c = idx / (H / 8), col = idx - c * (H / 8);
+        const int tok = c < kDecodeMaxTok ? s_tok[c] : -1;
+        s_x[c * rowu4 + col] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * H) + col)
+                                        : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+
+    const ExpertView vg = is_shared ? expert_view(a.s_gate, 0, I, H) : expert_view(a.gate, it.expert, I, H);
+    const ExpertView vu = is_shared ? expert_view(a.s_up, 0, I, H) : expert_view(a.up, it.expert, I, H);
+    const int r0 = blockIdx.x * 16 + g, r1 = r0 + 8;
+    const int gbeg = (warp * G) / 4, gend = ((warp + 1) * G) / 4;
+
+    float acc_g[NT][4], acc_u[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc_g[j][q] = acc_u[j][q] = 0.f;
+
+    constexpr int GB = 4;   // groups whose loads are issued together
+    for (int gb = gbeg; gb < gend; gb += GB) {
+        uint2 cg0[GB], cg1[GB], cu0[GB], cu1[GB];
+        uint16_t sg[GB][2], bg[GB][2], su[GB][2], bu[GB][2];
+#pragma unroll
+        for (int i = 0; i < GB; ++i) {
+            const int grp = gb + i;
+            if (grp < gend) {
+                const size_t co = (size_t)grp * 32 + 8 * t;
+                cg0[i] = __ldg(reinterpret_cast<const uint2 *>(vg.codes + (size_t)r0 * (H / 2) + co));
+                cg1[i] = __ldg(reinterpret_cast<const uint2 *>(vg.codes + (size_t)r1 * (H / 2) + co));
+                cu0[i] = __ldg(reinterpret_cast<const uint2 *>(vu.codes + (size_t)r0 * (H / 2) + co));
+                cu1[i] = __ldg(reinterpret_cast<const uint2 *>(vu.codes + (size_t)r1 * (H / 2) + co));
+                sg[i][0] = __ldg(vg.scales + (size_t)r0 * G + grp);
+                sg[i][1] = __ldg(vg.scales + (size_t)r1 * G + grp);
+                bg[i][0] = __ldg(vg.biases + (size_t)r0 * G + grp);
+                bg[i][1] = __ldg(vg.biases + (size_t)r1 * G + grp);
+                su[i][0] = __ldg(vu.scales + (size_t)r0 * G + grp);
+                su[i][1] = __ldg(vu.scales + (size_t)r1 * G + grp);
+                bu[i][0] = __ldg(vu.biases + (size_t)r0 * G + grp);
+                bu[i][1] = __ldg(vu.biases + (size_t)r1 * G + grp);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < GB; ++i) {
+            const int grp = gb + i;
+            if (grp >= gend) break;
+            const float s_g0 = bf16_bits_to_float(sg[i][0]), s_g1 = bf16_bits_to_float(sg[i][1]);
+            const float s_u0 = bf16_bits_to_float(su[i][0]), s_u1 = bf16_bits_to_float(su[i][1]);
+            const float c_g0 = fmaf(-128.f, s_g0, bf16_bits_to_float(bg[i][0]));   // b - 128 s, exact
+            const float c_g1 = fmaf(-128.f, s_g1, bf16_bits_to_float(bg[i][1]));
+            const float c_u0 = fmaf(-128.f, s_u0, bf16_bits_to_float(bu[i][0]));
+            const float c_u1 = fmaf(-128.f, s_u1, bf16_bits_to_float(bu[i][1]));
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const uint4 *xr = s_x + (j * 8 + g) * rowu4 + grp * 8 + 2 * t;
+                uint32_t bp[8];
+                permute_b(xr[0], xr[1], bp);
+                float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
+                group_mma<false>(cg0[i], cg1[i], bp, dg, dx, true);
+                group_mma<false>(cu0[i], cu1[i], bp, du, dx, false);
+                // rows: d[0], d[1] -> row g; d[2], d[3] -> row g+8
+                acc_g[j][0] = fmaf(s_g0, dg[0], fmaf(c_g0, dx[0], acc_g[j][0]));
+                acc_g[j][1] = fmaf(s_g0, dg[1], fmaf(c_g0, dx[1], acc_g[j][1]));
+                acc_g[j][2] = fmaf(s_g1, dg[2], fmaf(c_g1, dx[2], acc_g[j][2]));
+                acc_g[j][3] = fmaf(s_g1, dg[3], fmaf(c_g1, dx[3], acc_g[j][3]));
+                acc_u[j][0] = fmaf(s_u0, du[0], fmaf(c_u0, dx[0], acc_u[j][0]));
+                acc_u[j][1] = fmaf(s_u0, du[1], fmaf(c_u0, dx[1], acc_u[j][1]));
+                acc_u[j][2] = fmaf(s_u1, du[2], fmaf(c_u1, dx[2], acc_u[j][2]));
+                acc_u[j][3] = fmaf(s_u1, du[3], fmaf(c_u1, dx[3], acc_u[j][3]));
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int c0 = j * 8 + 2 * t;
+        s_red[warp][0][g][c0] = acc_g[j][0];
+        s_red[warp][0][g][c0 + 1] = acc_g[j][1];
+        s_red[warp][0][g + 8][c0] = acc_g[j][2];
+        s_red[warp][0][g + 8][c0 + 1] = acc_g[j][3];
+        s_red[warp][1][g][c0] = acc_u[j][0];
+        s_red[warp][1][g][c0 + 1] = acc_u[j][1];
+        s_red[warp][1][g + 8][c0] = acc_u[j][2];
+        s_red[warp][1][g + 8][c0 + 1] = acc_u[j][3];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < 16 * NT * 8; idx += blockDim.x) {
+        const int c = idx >> 4, row = idx & 15;
+        const int f = c < kDecodeMaxTok ? s_slot[c] : -1;
+        if (f < 0) continue;
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            gs += s_red[w][0][row][c];
+            us += s_red[w][1][row][c];
+        }
+        const float hv = gs / (1.f + __expf(-gs)) * us;
+        a.h[(size_t)f * I + blockIdx.x * 16 + row] = __half_as_ushort(__float2half_rn(hv));
+    }
+}
+
+// ------------------------------------------------------------ down projection
+//
+// grid (H/64, max items); 128 threads, warp w owns rows [64 bx + 16 w, +16) of
+// the down matrix over all of the intermediate dimension; writes the raw
+// expert output y_e for each of the item's slots.
+template <int NT>
+__global__ void __launch_bounds__(128) decode_down_kernel(ExpertArgs a)
+{
+    extern __shared__ uint4 s_h[];                 // [NT*8][I/8 + 1]
+    __shared__ int s_tok[kDecodeMaxTok], s_slot[kDecodeMaxTok];
+    if ((int)blockIdx.y >= __ldg(a.nwork + 0)) return;
+    const WorkItem it = a.work[blockIdx.y];
+    const int H = a.H, I = a.I, GI = I / kGroup, rowu4 = I / 8 + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const bool is_shared = it.expert == a.E;
+
+    item_columns(a, it, s_tok, s_slot);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < NT * 8 * (I / 8); idx += blockDim.x) {
+        const int c = idx / (I / 8), col = idx - c * (I / 8);
+        const int f = c < kDecodeMaxTok ? s_slot[c] : -1;
+        s_h[c * rowu4 + col] = f >= 0 ? *(reinterpret_cast<const uint4 *>(a.h + (size_t)f * I) + col)
+                                      : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+
+    const ExpertView vd = is_shared ? expert_view(a.s_down, 0, H, I) : expert_view(a.down, it.expert, H, I);
+    const int rbase = blockIdx.x * 64 + warp * 16;
+    const int r0 = rbase + g, r1 = r0 + 8;
+    float acc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+
+    constexpr int GB = 8;
+    for (int gb = 0; gb < GI; gb += GB) {
+        uint2 c0[GB], c1[GB];
+        uint16_t sv[GB][2], bv[GB][2];
+#pragma unroll
+        for (int i = 0; i < GB; ++i) {
+            const int grp = gb + i;
+            if (grp < GI) {
+                const size_t co = (size_t)grp * 32 + 8 * t;
+                c0[i] = __ldg(reinterpret_cast<const uint2 *>(vd.codes + (size_t)r0 * (I / 2) + co));
+                c1[i] = __ldg(reinterpret_cast<const uint2 *>(vd.codes + (size_t)r1 * (I / 2) + co));
+                sv[i][0] = __ldg(vd.scales + (size_t)r0 * GI + grp);
+                sv[i][1] = __ldg(vd.scales + (size_t)r1 * GI + grp);
+                bv[i][0] = __ldg(vd.biases + (size_t)r0 * GI + grp);
+                bv[i][1] = __ldg(vd.biases + (size_t)r1 * GI + grp);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < GB; ++i) {
+            const int grp = gb + i;
+            if (grp >= GI) break;
+            const float s0 = bf16_bits_to_float(sv[i][0]), s1 = bf16_bits_to_float(sv[i][1]);
+            const float k0 = fmaf(-1024.f, s0, bf16_bits_to_float(bv[i][0]));   // b - 1024 s
+            const float k1 = fmaf(-1024.f, s1, bf16_bits_to_float(bv[i][1]));
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const uint4 *hr = s_h + (j * 8 + g) * rowu4 + grp * 8 + 2 * t;
+                uint32_t bp[8];
+                permute_b(hr[0], hr[1], bp);
+                float d[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
+                group_mma<true>(c0[i], c1[i], bp, d, dx, true);
+                acc[j][0] = fmaf(s0, d[0], fmaf(k0, dx[0], acc[j][0]));
+                acc[j][1] = fmaf(s0, d[1], fmaf(k0, dx[1], acc[j][1]));
+                acc[j][2] = fmaf(s1, d[2], fmaf(k1, dx[2], acc[j][2]));
+                acc[j][3] = fmaf(s1, d[3], fmaf(k1, dx[3], acc[j][3]));
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int cA = j * 8 + 2 * t, cB = cA + 1;
+        const int fA = cA < kDecodeMaxTok ? s_slot[cA] : -1, fB = cB < kDecodeMaxTok ? s_slot[cB] : -1;
+        if (fA >= 0) {
+            a.yslot[(size_t)fA * H + r0] = acc[j][0];
+            a.yslot[(size_t)fA * H + r1] = acc[j][2];
+        }
+        if (fB >= 0) {
+            a.yslot[(size_t)fB * H + r0] = acc[j][1];
+            a.yslot[(size_t)fB * H + r1] = acc[j][3];
+        }
+    }
+}
+
+// ------------------------------------------------------------ fixed-order combine
+//
+// sum[t, n] = sum_{j < k} p[t,j] * y_slot[t*k + j, n] + w_s[t] * y_slot[T*k + t, n],
+// added in slot order; y = bf16(sum) or acc += sum.
+__global__ void decode_reduce_kernel(ReduceArgs a)
+{
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)a.T * a.H) return;
+    const int t = (int)(idx / a.H), n = (int)(idx - (size_t)t * a.H);
+    float s = 0.f;
+    for (int j = 0; j < a.k; ++j)
+        s = fmaf(bf16_bits_to_float(a.p[(size_t)t * a.k + j]), a.yslot[((size_t)t * a.k + j) * a.H + n], s);
+    if (a.has_shared)
+        s = fmaf(bf16_bits_to_float(a.w_s[t]), a.yslot[((size_t)a.T * a.k + t) * a.H + n], s);
+    if (a.y)
+        a.y[idx] = float_to_bf16_bits(s);
+    else
+        a.acc[idx] += s;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_gateup(const ExpertArgs &a, cudaStream_t st)
+{
+    const int ncol = a.T >= 9 ? 16 : 8;
+    const size_t smem = (size_t)ncol * (a.H / 8 + 1) * 16;
+    dim3 grid(a.I / 16, a.max_items);
+    if (ncol == 16) {
+        cudaFuncSetAttribute(decode_gateup_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_gateup_kernel<2><<<grid, 128, smem, st>>>(a);
+    } else {
+        cudaFuncSetAttribute(decode_gateup_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_gateup_kernel<1><<<grid, 128, smem, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_down(const ExpertArgs &a, cudaStream_t st)
+{
+    const int ncol = a.T >= 9 ? 16 : 8;
+    const size_t smem = (size_t)ncol * (a.I / 8 + 1) * 16;
+    dim3 grid(a.H / 64, a.max_items);
+    if (ncol == 16) {
+        cudaFuncSetAttribute(decode_down_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_down_kernel<2><<<grid, 128, smem, st>>>(a);
+    } else {
+        cudaFuncSetAttribute(decode_down_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_down_kernel<1><<<grid, 128, smem, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_reduce(const ReduceArgs &a, cudaStream_t st)
+{
+    const size_t n = (size_t)a.T * a.H;
+    decode_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace qmoe

@@ -1,0 +1,105 @@
+// Kernel argument blocks and launchers of the MoE layer library.
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace qmoe {
+
+struct RouteArgs {
+    const uint16_t *x;            // bf16 [T, H]
+    const uint8_t *r_codes;       // u8 [E, H]
+    const uint16_t *r_scales;     // bf16 [E, H/64]
+    const uint16_t *r_biases;
+    const uint16_t *v;            // bf16 [H] shared gate vector (may be null)
+    const float *router_bias;     // f32 [E] or null
+    float *logits;                // f32 [T, E]
+    float *gamma;                 // f32 [T]
+    int *status_reset;            // non-null: cleared by the first thread (first kernel of a call)
+    int T, H, E;
+    int n_expert_tiles;           // 0: only the gamma column runs
+};
+
+struct TopkArgs {
+    const float *logits;          // f32 [T, E]
+    const float *gamma;           // f32 [T]
+    int32_t *ids;                 // [T, k]
+    uint16_t *p;                  // bf16 [T, k]
+    uint16_t *w_s;                // bf16 [T] (may be null)
+    int32_t *hist;                // [nblk, E]
+    int T, E, k, has_shared;
+};
+
+struct PermuteArgs {
+    const int32_t *ids;
+    const int32_t *hist;
+    int32_t *counts, *offsets, *perm, *inv_perm;
+    int32_t *nwork;               // [3]: decode items, gemm1 tiles, gemm2 tiles
+    WorkItem *work_dec, *work_g1, *work_g2;
+    int *status;
+    int T, E, k, nblk, has_shared;
+    int build_work;               // block 0 also writes the expert kernels' work lists
+    int max_items[3];             // capacity of each work list
+};
+
+struct HistArgs {
+    const int32_t *ids;
+    int32_t *hist;
+    int *status;
+    int T, E, k, nblk;
+};
+
+struct WorklistArgs {
+    const int32_t *counts;
+    int32_t *nwork;
+    WorkItem *work_dec, *work_g1, *work_g2;
+    int *status;
+    int T, E, has_shared;
+    int max_items[3];
+};
+
+// One expert matrix stack as the expert kernels see it.
+struct QMatDev {
+    const uint8_t *codes;
+    const uint16_t *scales;
+    const uint16_t *biases;
+};
+
+struct ExpertArgs {
+    const uint16_t *x;            // bf16 [T, H]
+    QMatDev gate, up, down;       // stacked [E, ...]
+    QMatDev s_gate, s_up, s_down; // shared expert
+    const int32_t *offsets;       // [E + 1]
+    const int32_t *perm;          // [T*k]
+    const int32_t *nwork;         // [3]
+    const WorkItem *work;         // decode items or GEMM tiles
+    uint16_t *h;                  // bf16 [T*k + T, I], slot-major (f = t*k + j; shared f = T*k + t)
+    float *yslot;                 // f32 [T*k + T, H] (decode)
+    const uint16_t *p;            // bf16 [T, k]
+    const uint16_t *w_s;          // bf16 [T]
+    float *acc;                   // f32 [T, H]
+    int *status;
+    int T, H, I, E, k, has_shared;
+    int max_items;
+};
+
+struct ReduceArgs {
+    const float *yslot;
+    const uint16_t *p;
+    const uint16_t *w_s;
+    float *acc;                   // acc += sum (when y == null)
+    uint16_t *y;                  // y = bf16(sum) (when non-null)
+    int T, H, k, has_shared;
+};
+
+cudaError_t launch_route_gemv(const RouteArgs &a, cudaStream_t st);
+cudaError_t launch_topk(const TopkArgs &a, cudaStream_t st);
+cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t st);
+cudaError_t launch_hist(const HistArgs &a, cudaStream_t st);
+cudaError_t launch_worklist(const WorklistArgs &a, cudaStream_t st);
+cudaError_t launch_decode_gateup(const ExpertArgs &a, cudaStream_t st);
+cudaError_t launch_decode_down(const ExpertArgs &a, cudaStream_t st);
+cudaError_t launch_decode_reduce(const ReduceArgs &a, cudaStream_t st);
+cudaError_t launch_combine(const float *acc, uint16_t *y, size_t n, cudaStream_t st);
+cudaError_t launch_zero(float *p, size_t n, cudaStream_t st);
+
+}  // namespace qmoe

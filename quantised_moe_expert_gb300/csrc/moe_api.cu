@@ -1,0 +1,373 @@
+// C ABI of the MoE layer library: argument checks, workspace carving, launches.
+// The operations and their contract are stated in include/moe.h.
+#include <atomic>
+
+#include "kernels.cuh"
+
+using namespace qmoe;
+
+namespace {
+
+std::atomic<long long> g_wait_limit{1ll << 26};
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned16_or_null(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool qmat_ok(const moe_qmat &m)
+{
+    return aligned16(m.codes) && aligned16(m.scales) && aligned16(m.biases);
+}
+
+template <typename T>
+T *ws_at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
+
+QMatDev dev(const moe_qmat &m) { return QMatDev{m.codes, m.scales, m.biases}; }
+
+int check_common(const moe_config *cfg, int T)
+{
+    if (!cfg) return MOE_ERR_INVALID_ARG;
+    const int rc = moe_check_config(cfg);
+    if (rc != MOE_OK) return rc;
+    if (T < 0 || T > kMaxTokens) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+int check_ws(const moe_config *cfg, int T, void *ws, size_t ws_bytes, WsLayout *L)
+{
+    *L = ws_layout(*cfg, T);
+    if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int resolve_path(int path, int T)
+{
+    if (path == MOE_PATH_AUTO) return T <= kDecodeMaxTok ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+    return path;
+}
+
+// Router GEMV (or pass-through of supplied logits) and top-k into the given buffers.
+int enqueue_route(const moe_config &c, const moe_weights &w, const uint16_t *x, int T, const float *router_bias,
+                  const float *logits_in, float *logits, int32_t *ids, uint16_t *p, uint16_t *w_s,
+                  const WsLayout &L, void *ws, cudaStream_t st)
+{
+    RouteArgs ra{};
+    ra.x = x;
+    ra.r_codes = w.router.codes;
+    ra.r_scales = w.router.scales;
+    ra.r_biases = w.router.biases;
+    ra.v = c.has_shared ? w.shared_gate_vec : nullptr;
+    ra.router_bias = router_bias;
+    ra.logits = logits;
+    ra.gamma = ws_at<float>(ws, L.gamma);
+    ra.status_reset = ws_at<int>(ws, L.status);
+    ra.T = T;
+    ra.H = c.hidden;
+    ra.E = c.n_experts;
+    ra.n_expert_tiles = logits_in ? 0 : (c.n_experts + 7) / 8;
+    int rc = cuda_rc(launch_route_gemv(ra, st));
+    if (rc) return rc;
+    if (logits_in && logits && logits != logits_in) {
+        rc = cuda_rc(cudaMemcpyAsync(logits, logits_in, sizeof(float) * (size_t)T * c.n_experts,
+                                     cudaMemcpyDeviceToDevice, st));
+        if (rc) return rc;
+    }
+    TopkArgs ta{};
+    ta.logits = logits_in ? logits_in : logits;
+    ta.gamma = ra.gamma;
+    ta.ids = ids;
+    ta.p = p;
+    ta.w_s = w_s;
+    ta.hist = ws_at<int32_t>(ws, L.hist);
+    ta.T = T;
+    ta.E = c.n_experts;
+    ta.k = c.top_k;
+    ta.has_shared = c.has_shared;
+    return cuda_rc(launch_topk(ta, st));
+}
+
+PermuteArgs permute_args(const moe_config &c, const int32_t *ids, int T, int32_t *counts, int32_t *offsets,
+                         int32_t *perm, int32_t *inv_perm, const WsLayout &L, void *ws)
+{
+    PermuteArgs pa{};
+    pa.ids = ids;
+    pa.hist = ws_at<int32_t>(ws, L.hist);
+    pa.counts = counts;
+    pa.offsets = offsets;
+    pa.perm = perm;
+    pa.inv_perm = inv_perm;
+    pa.nwork = ws_at<int32_t>(ws, L.nwork);
+    pa.work_dec = ws_at<WorkItem>(ws, L.work_dec);
+    pa.work_g1 = ws_at<WorkItem>(ws, L.work_g1);
+    pa.work_g2 = ws_at<WorkItem>(ws, L.work_g2);
+    pa.status = ws_at<int>(ws, L.status);
+    pa.T = T;
+    pa.E = c.n_experts;
+    pa.k = c.top_k;
+    pa.nblk = L.nblk;
+    pa.has_shared = c.has_shared;
+    pa.build_work = 1;
+    pa.max_items[0] = L.max_wd;
+    pa.max_items[1] = L.max_w1;
+    pa.max_items[2] = L.max_w2;
+    return pa;
+}
+
+ExpertArgs expert_args(const moe_config &c, const moe_weights &w, const uint16_t *x, int T, const uint16_t *p,
+                       const uint16_t *w_s, const int32_t *offsets, const int32_t *perm, float *acc,
+                       const WsLayout &L, void *ws)
+{
+    ExpertArgs ea{};
+    ea.x = x;
+    ea.gate = dev(w.gate);
+    ea.up = dev(w.up);
+    ea.down = dev(w.down);
+    if (c.has_shared) {
+        ea.s_gate = dev(w.s_gate);
+        ea.s_up = dev(w.s_up);
+        ea.s_down = dev(w.s_down);
+    }
+    ea.offsets = offsets;
+    ea.perm = perm;
+    ea.nwork = ws_at<int32_t>(ws, L.nwork);
+    ea.h = ws_at<uint16_t>(ws, L.h);
+    ea.yslot = ws_at<float>(ws, L.yslot);
+    ea.p = p;
+    ea.w_s = w_s;
+    ea.acc = acc;
+    ea.status = ws_at<int>(ws, L.status);
+    ea.T = T;
+    ea.H = c.hidden;
+    ea.I = c.inter;
+    ea.E = c.n_experts;
+    ea.k = c.top_k;
+    ea.has_shared = c.has_shared;
+    return ea;
+}
+
+// Decode expert kernels; the sum lands in y (rounded) or is added to acc.
+int enqueue_decode_experts(const moe_config &c, ExpertArgs ea, const WsLayout &L, void *ws, uint16_t *y,
+                           cudaStream_t st)
+{
+    ea.work = ws_at<WorkItem>(ws, L.work_dec);
+    ea.max_items = L.max_wd;
+    int rc = cuda_rc(launch_decode_gateup(ea, st));
+    if (rc) return rc;
+    rc = cuda_rc(launch_decode_down(ea, st));
+    if (rc) return rc;
+    ReduceArgs r{};
+    r.yslot = ea.yslot;
+    r.p = ea.p;
+    r.w_s = ea.w_s;
+    r.acc = ea.acc;
+    r.y = y;
+    r.T = ea.T;
+    r.H = c.hidden;
+    r.k = c.top_k;
+    r.has_shared = c.has_shared;
+    return cuda_rc(launch_decode_reduce(r, st));
+}
+
+int enqueue_prefill_experts(const moe_config &, ExpertArgs, const WsLayout &, void *, cudaStream_t)
+{
+    return MOE_ERR_UNSUPPORTED;
+}
+
+bool weights_ok(const moe_config &c, const moe_weights *w, bool need_router, bool need_experts)
+{
+    if (!w) return false;
+    if (need_router && !qmat_ok(w->router)) return false;
+    if (need_experts) {
+        if (!qmat_ok(w->gate) || !qmat_ok(w->up) || !qmat_ok(w->down)) return false;
+        if (c.has_shared && (!qmat_ok(w->s_gate) || !qmat_ok(w->s_up) || !qmat_ok(w->s_down))) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(int status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE: return "device-side index out of range";
+    default: return "unknown status";
+    }
+}
+
+int moe_check_config(const moe_config *c)
+{
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->hidden <= 0 || c->inter <= 0 || c->n_experts <= 0 || c->top_k <= 0) return MOE_ERR_INVALID_ARG;
+    if (c->group != kGroup || c->bits != 4 || c->router_bits != 8) return MOE_ERR_UNSUPPORTED;
+    if (c->hidden % 64 || c->inter % 64 || c->hidden > 8192 || c->inter > 4096) return MOE_ERR_UNSUPPORTED;
+    if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->top_k > c->n_experts) return MOE_ERR_UNSUPPORTED;
+    if (c->has_shared != 0 && c->has_shared != 1) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int moe_workspace_size(const moe_config *cfg, int T, size_t *bytes)
+{
+    const int rc = check_common(cfg, T);
+    if (rc) return rc;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(*cfg, T).total;
+    return MOE_OK;
+}
+
+int moe_route(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T, const float *router_bias,
+              const float *logits_in, float *logits_out, int32_t *ids, uint16_t *p, uint16_t *w_shared, void *ws,
+              size_t ws_bytes, void *stream)
+{
+    int rc = check_common(cfg, T);
+    if (rc) return rc;
+    if (!w || !aligned16(x) || !aligned16(ids) || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16_or_null(router_bias) || !aligned16_or_null(logits_in) || !aligned16_or_null(logits_out) ||
+        !aligned16_or_null(w_shared))
+        return MOE_ERR_INVALID_ARG;
+    if (!logits_in && !weights_ok(*cfg, w, true, false)) return MOE_ERR_INVALID_ARG;
+    if (cfg->has_shared && w_shared && !aligned16(w->shared_gate_vec)) return MOE_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
+    if (T == 0) return MOE_OK;
+    auto st = static_cast<cudaStream_t>(stream);
+    float *logits = logits_out ? logits_out : ws_at<float>(ws, L.logits);
+    return enqueue_route(*cfg, *w, x, T, router_bias, logits_in, logits, ids, p, w_shared, L, ws, st);
+}
+
+int moe_permute(const moe_config *cfg, const int32_t *ids, int T, int32_t *counts, int32_t *offsets,
+                int32_t *perm, int32_t *inv_perm, void *ws, size_t ws_bytes, void *stream)
+{
+    int rc = check_common(cfg, T);
+    if (rc) return rc;
+    if (!aligned16(ids) || !aligned16(counts) || !aligned16(offsets) || !aligned16(perm) || !aligned16(inv_perm))
+        return MOE_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
+    auto st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        rc = cuda_rc(cudaMemsetAsync(counts, 0, sizeof(int32_t) * cfg->n_experts, st));
+        if (!rc) rc = cuda_rc(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (cfg->n_experts + 1), st));
+        return rc;
+    }
+    HistArgs ha{};
+    ha.ids = ids;
+    ha.hist = ws_at<int32_t>(ws, L.hist);
+    ha.status = ws_at<int>(ws, L.status);
+    ha.T = T;
+    ha.E = cfg->n_experts;
+    ha.k = cfg->top_k;
+    ha.nblk = L.nblk;
+    if ((rc = cuda_rc(launch_hist(ha, st)))) return rc;
+    return cuda_rc(launch_permute(permute_args(*cfg, ids, T, counts, offsets, perm, inv_perm, L, ws), st));
+}
+
+int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T, const int32_t *ids,
+                   const uint16_t *p, const uint16_t *w_shared, const int32_t *counts, const int32_t *offsets,
+                   const int32_t *perm, float *acc, int path, void *ws, size_t ws_bytes, void *stream)
+{
+    int rc = check_common(cfg, T);
+    if (rc) return rc;
+    if (!weights_ok(*cfg, w, false, true) || !aligned16(x) || !aligned16(ids) || !aligned16(p) ||
+        !aligned16(counts) || !aligned16(offsets) || !aligned16(perm) || !aligned16(acc))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->has_shared && !aligned16(w_shared)) return MOE_ERR_INVALID_ARG;
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_PREFILL) return MOE_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
+    if (T == 0) return MOE_OK;
+    auto st = static_cast<cudaStream_t>(stream);
+    WorklistArgs wa{};
+    wa.counts = counts;
+    wa.nwork = ws_at<int32_t>(ws, L.nwork);
+    wa.work_dec = ws_at<WorkItem>(ws, L.work_dec);
+    wa.work_g1 = ws_at<WorkItem>(ws, L.work_g1);
+    wa.work_g2 = ws_at<WorkItem>(ws, L.work_g2);
+    wa.status = ws_at<int>(ws, L.status);
+    wa.T = T;
+    wa.E = cfg->n_experts;
+    wa.has_shared = cfg->has_shared;
+    wa.max_items[0] = L.max_wd;
+    wa.max_items[1] = L.max_w1;
+    wa.max_items[2] = L.max_w2;
+    if ((rc = cuda_rc(launch_worklist(wa, st)))) return rc;
+    ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_shared, offsets, perm, acc, L, ws);
+    if (resolve_path(path, T) == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, nullptr, st);
+    return enqueue_prefill_experts(*cfg, ea, L, ws, st);
+}
+
+int moe_combine(const moe_config *cfg, int T, const float *acc, uint16_t *y, void *stream)
+{
+    int rc = check_common(cfg, T);
+    if (rc) return rc;
+    if (!aligned16(acc) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    return cuda_rc(launch_combine(acc, y, (size_t)T * cfg->hidden, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T, const float *router_bias,
+                const float *logits_in, uint16_t *y, int32_t *ids_out, uint16_t *p_out, uint16_t *w_shared_out,
+                int path, void *ws, size_t ws_bytes, void *stream)
+{
+    int rc = check_common(cfg, T);
+    if (rc) return rc;
+    if (!weights_ok(*cfg, w, logits_in == nullptr, true) || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    if (cfg->has_shared && !aligned16(w->shared_gate_vec)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16_or_null(router_bias) || !aligned16_or_null(logits_in) || !aligned16_or_null(ids_out) ||
+        !aligned16_or_null(p_out) || !aligned16_or_null(w_shared_out))
+        return MOE_ERR_INVALID_ARG;
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_PREFILL) return MOE_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
+    if (T == 0) return MOE_OK;
+    const int rp = resolve_path(path, T);
+    if (rp == MOE_PATH_PREFILL) {
+        // the prefill GEMMs are checked before anything is enqueued
+        if ((rc = enqueue_prefill_experts(*cfg, ExpertArgs{}, L, nullptr, nullptr)) == MOE_ERR_UNSUPPORTED) return rc;
+    }
+    auto st = static_cast<cudaStream_t>(stream);
+    int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.ids);
+    uint16_t *p = p_out ? p_out : ws_at<uint16_t>(ws, L.p);
+    uint16_t *w_s = w_shared_out ? w_shared_out : ws_at<uint16_t>(ws, L.w_s);
+    float *logits = ws_at<float>(ws, L.logits);
+    if ((rc = enqueue_route(*cfg, *w, x, T, router_bias, logits_in, logits_in ? nullptr : logits, ids, p, w_s, L,
+                            ws, st)))
+        return rc;
+    int32_t *counts = ws_at<int32_t>(ws, L.counts), *offsets = ws_at<int32_t>(ws, L.offsets);
+    int32_t *perm = ws_at<int32_t>(ws, L.perm), *inv_perm = ws_at<int32_t>(ws, L.inv_perm);
+    if ((rc = cuda_rc(launch_permute(permute_args(*cfg, ids, T, counts, offsets, perm, inv_perm, L, ws), st))))
+        return rc;
+    ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_s, offsets, perm, ws_at<float>(ws, L.acc), L, ws);
+    if (rp == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, y, st);
+    return enqueue_prefill_experts(*cfg, ea, L, ws, st);
+}
+
+int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_status)
+{
+    if (!aligned16(ws) || ws_bytes < 256 || !device_status) return MOE_ERR_INVALID_ARG;
+    auto st = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    int rc = cuda_rc(cudaStreamSynchronize(st));
+    if (!rc) rc = cuda_rc(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost));
+    if (!rc) rc = cuda_rc(cudaMemset(ws, 0, sizeof(int)));
+    if (rc) return rc;
+    *device_status = v;
+    return MOE_OK;
+}
+
+int moe_set_wait_limit(long long polls)
+{
+    g_wait_limit.store(polls > 0 ? polls : (1ll << 26));
+    return MOE_OK;
+}
+
+}  // extern "C"

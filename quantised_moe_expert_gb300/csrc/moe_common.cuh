@@ -1,0 +1,134 @@
+// Shared device/host definitions of the MoE layer kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace qmoe {
+
+constexpr int kGroup = 64;          // quantisation group along the input dimension
+constexpr int kMaxExperts = 256;    // top-k kernel keeps E/32 logits per lane
+constexpr int kMaxTopK = 16;
+constexpr int kMaxTokens = 65536;
+constexpr int kTokBlock = 128;      // tokens per block of the histogram / stable scatter
+constexpr int kDecodeMaxTok = 16;   // decode GEMV handles up to 16 tokens per expert per pass
+
+// Tile of the prefill grouped GEMMs: 128 weight rows x up to kTileN tokens.
+constexpr int kTileM = 128;
+constexpr int kTileN1 = 128;        // tokens per tile, gate/up GEMM (two accumulators)
+constexpr int kTileN2 = 256;        // tokens per tile, down GEMM
+
+// One unit of work of a grouped kernel: an expert (E = shared) and a token range
+// [tok0, tok0 + ntok) of its permuted slot list.
+struct WorkItem {
+    int expert;
+    int tok0;
+    int ntok;
+    int pad;
+};
+
+// Offsets (bytes) of every scratch array inside the caller's workspace.
+struct WsLayout {
+    size_t status;     // int32 status word + counters (256 B)
+    size_t logits;     // f32 [T, E]
+    size_t ids;        // i32 [T, k]
+    size_t p;          // u16 [T, k]
+    size_t w_s;        // u16 [T]
+    size_t gamma;      // f32 [T] shared gate logit
+    size_t hist;       // i32 [nblk, E]
+    size_t counts;     // i32 [E]
+    size_t offsets;    // i32 [E + 1]
+    size_t perm;       // i32 [T*k]
+    size_t inv_perm;   // i32 [T*k]
+    size_t nwork;      // i32 [4]: decode active experts, gemm1 tiles, gemm2 tiles
+    size_t work_dec;   // WorkItem [E + 1]
+    size_t work_g1;    // WorkItem [max tiles gemm1]
+    size_t work_g2;    // WorkItem [max tiles gemm2]
+    size_t h;          // bf16 [T*k + T, I]
+    size_t yslot;      // f32 [T*k + T, H] (decode)
+    size_t acc;        // f32 [T, H] (prefill accumulation)
+    size_t total;
+    int nblk;
+    int max_wd;
+    int max_w1;
+    int max_w2;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int max_tiles(int T, int k, int E, int has_shared, int tile_n)
+{
+    // sum_e ceil(c_e / n) <= (T*k) / n + E, plus the shared expert's ceil(T / n).
+    long long t = (long long)T * k / tile_n + E + (has_shared ? (T + tile_n - 1) / tile_n : 0) + 1;
+    return (int)t;
+}
+
+inline WsLayout ws_layout(const moe_config &c, int T)
+{
+    WsLayout L{};
+    const size_t H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k;
+    const size_t Tz = T > 0 ? T : 1;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+    L.nblk = (int)((Tz + kTokBlock - 1) / kTokBlock);
+    L.max_w1 = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kTileN1);
+    L.max_w2 = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kTileN2);
+    L.status = take(256);
+    L.logits = take(4 * Tz * E);
+    L.ids = take(4 * Tz * k);
+    L.p = take(2 * Tz * k);
+    L.w_s = take(2 * Tz);
+    L.gamma = take(4 * Tz);
+    L.hist = take(4 * (size_t)L.nblk * E);
+    L.counts = take(4 * E);
+    L.offsets = take(4 * (E + 1));
+    L.perm = take(4 * Tz * k);
+    L.inv_perm = take(4 * Tz * k);
+    L.nwork = take(16);
+    L.max_wd = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kDecodeMaxTok);
+    L.work_dec = take(sizeof(WorkItem) * (size_t)L.max_wd);
+    L.work_g1 = take(sizeof(WorkItem) * (size_t)L.max_w1);
+    L.work_g2 = take(sizeof(WorkItem) * (size_t)L.max_w2);
+    L.h = take(2 * Tz * (k + 1) * I);
+    L.yslot = take(4 * Tz * (k + 1) * H);
+    L.acc = take(4 * Tz * H);
+    L.total = o;
+    return L;
+}
+
+// Device-side status recording: first error wins, never traps.
+__device__ __forceinline__ void record_status(int *status, int code)
+{
+    atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
+{
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
+// Round a float to bf16 bits, nearest-even (finite inputs).
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Round a double to bf16 bits, nearest-even, with a single rounding (normal range).
+// Drops the low 45 of the 52 fraction bits with round-half-even on the bit
+// pattern, then the 7-bit-fraction double is exactly representable in fp32.
+__device__ __forceinline__ uint16_t double_to_bf16_bits(double d)
+{
+    unsigned long long u = (unsigned long long)__double_as_longlong(d);
+    unsigned long long lsb = (u >> 45) & 1ull;
+    u += 0x0FFFFFFFFFFFull + lsb;     // 2^44 - 1 + lsb
+    u &= ~((1ull << 45) - 1ull);
+    float f = (float)__longlong_as_double((long long)u);
+    return (uint16_t)(__float_as_uint(f) >> 16);
+}
+
+}  // namespace qmoe

@@ -1,0 +1,401 @@
+// Router GEMV, top-k / pick weights / shared weight, and the stable permutation.
+//
+// Follows the routing contract of the page "Qwen3.6-35B-A3B (qwen3_5_moe) on the
+// native Metal engine: proposal and gate", slice "The family, plain decode":
+// fp32 logits, top-k by logit with ties to the lower id, weights exp(l - l_top)
+// normalised over the picks and rounded to bf16, shared slot weight
+// bf16(sigmoid(bf16(gate))).  The router is MLX affine 8-bit in groups of 64.
+#include "kernels.cuh"
+
+namespace qmoe {
+
+// ---------------------------------------------------------------- router GEMV
+//
+// grid.x: ceil(E / 8) expert tiles plus one extra column that computes the
+// shared gate logit gamma; grid.y: ceil(T / 8) token tiles.  256 threads: warp
+// w owns expert (tile*8 + w) for the tile's 8 tokens.  Lane l owns the groups
+// g = l, l + 32, ... of the hidden dimension; per group
+//     partial += s_g * sum_j(q_j * x_j) + b_g * sum_j(x_j)
+// in fp32, then a fixed shuffle tree adds the 32 lane partials.  The
+// arithmetic of one token never depends on the other tokens of the tile, so a
+// token's logits are the same bits at every batch size.
+__global__ void __launch_bounds__(256) route_gemv_kernel(RouteArgs a)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.y * 8;
+    const int H = a.H, E = a.E, G = a.H / kGroup;
+    const int ntok = min(8, a.T - t0);
+    const bool gamma_col = (int)blockIdx.x == a.n_expert_tiles;
+    if (a.status_reset && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.status_reset = 0;
+
+    if (gamma_col) {
+        // gamma[t] = sum_h x[t,h] * v[h] in fp32, warp w -> token t0 + w.
+        if (warp >= ntok || a.v == nullptr) return;
+        const int t = t0 + warp;
+        float part = 0.f;
+        for (int g = lane; g < G; g += 32) {
+            const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + g * kGroup);
+            const uint4 *vp = reinterpret_cast<const uint4 *>(a.v + g * kGroup);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 xv = __ldg(xp + c), vv = __ldg(vp + c);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    part = fmaf(__uint_as_float(xw[q] << 16), __uint_as_float(vw[q] << 16), part);
+                    part = fmaf(__uint_as_float(xw[q] & 0xFFFF0000u), __uint_as_float(vw[q] & 0xFFFF0000u), part);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) a.gamma[t] = part;
+        return;
+    }
+
+    const int e = blockIdx.x * 8 + warp;
+    if (e >= E) return;
+    float part[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part[i] = 0.f;
+
+    const uint8_t *crow = a.r_codes + (size_t)e * H;
+    for (int g = lane; g < G; g += 32) {
+        uint4 cq[4];
+        const uint4 *cp = reinterpret_cast<const uint4 *>(crow + g * kGroup);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cq[c] = __ldg(cp + c);
+        const float s = bf16_bits_to_float(__ldg(a.r_scales + (size_t)e * G + g));
+        const float b = bf16_bits_to_float(__ldg(a.r_biases + (size_t)e * G + g));
+        const uint32_t cw[16] = {cq[0].x, cq[0].y, cq[0].z, cq[0].w, cq[1].x, cq[1].y, cq[1].z, cq[1].w,
+                                 cq[2].x, cq[2].y, cq[2].z, cq[2].w, cq[3].x, cq[3].y, cq[3].z, cq[3].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < ntok) {
+                const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)(t0 + i) * H + g * kGroup);
+                float dq = 0.f, sx = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 xv = __ldg(xp + c);
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = c * 8 + q * 2;                  // element index within the group
+                        const uint32_t codes4 = cw[j >> 2];
+                        const float q0 = (float)((codes4 >> ((j & 3) * 8)) & 0xFFu);
+                        const float q1 = (float)((codes4 >> (((j & 3) + 1) * 8)) & 0xFFu);
+                        const float x0 = __uint_as_float(xw[q] << 16);
+                        const float x1 = __uint_as_float(xw[q] & 0xFFFF0000u);
+                        dq = fmaf(q0, x0, dq);
+                        dq = fmaf(q1, x1, dq);
+                        sx += x0;
+                        sx += x1;
+                    }
+                }
+                part[i] = fmaf(s, dq, fmaf(b, sx, part[i]));
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part[i] += __shfl_xor_sync(0xffffffffu, part[i], o);
+    }
+    if (lane < ntok) {
+        float l = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i == lane) l = part[i];
+        if (a.router_bias) l = l + __ldg(a.router_bias + e);   // one fp32 rounding
+        a.logits[(size_t)(t0 + lane) * E + e] = l;
+    }
+}
+
+// ---------------------------------------------------------------- top-k
+//
+// One warp per token (32 warps per block, 4 tokens per warp: a block owns
+// kTokBlock = 128 consecutive tokens).  Lane l holds logits e = l + 32 r.  A
+// logit maps to an order-preserving unsigned key (+0 and -0 map to the same
+// key); the pair (key, 0xFFFF - id) is maximised, so equal logits resolve to
+// the lower id.  k rounds of a warp max give the ids in rank order.  Weights
+// are computed in fp64 and rounded once to bf16.  The block also counts its
+// slots per expert into hist[block][E] for the stable scatter.
+__device__ __forceinline__ uint32_t logit_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7FFFFFFFu) == 0) u = 0;                  // -0 == +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(1024) topk_kernel(TopkArgs a)
+{
+    __shared__ int sh_hist[kMaxExperts];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E, k = a.k;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sh_hist[e] = 0;
+    __syncthreads();
+
+    const int R = (E + 31) / 32;
+    for (int i = 0; i < kTokBlock / 32; ++i) {
+        const int t = blockIdx.x * kTokBlock + i * 32 + warp;
+        if (t >= a.T) break;
+        const float *lrow = a.logits + (size_t)t * E;
+        uint32_t key[kMaxExperts / 32];
+        float val[kMaxExperts / 32];
+#pragma unroll
+        for (int r = 0; r < kMaxExperts / 32; ++r) {
+            const int e = lane + 32 * r;
+            if (r < R && e < E) {
+                val[r] = lrow[e];
+                key[r] = logit_key(val[r]);
+            } else {
+                val[r] = 0.f;
+                key[r] = 0;     // below every real key
+            }
+        }
+        unsigned taken = 0;     // bit r: logit lane+32r already picked
+        int my_id = -1;         // lane j < k ends with the id of rank j
+        float my_l = 0.f;
+        float top_l = 0.f;
+        for (int j = 0; j < k; ++j) {
+            unsigned long long best = 0;
+#pragma unroll
+            for (int r = 0; r < kMaxExperts / 32; ++r) {
+                const int e = lane + 32 * r;
+                if (r < R && e < E && !(taken & (1u << r))) {
+                    unsigned long long c = ((unsigned long long)key[r] << 32) | (unsigned)(0xFFFF - e);
+                    best = c > best ? c : best;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+                best = other > best ? other : best;
+            }
+            const int id = 0xFFFF - (int)(best & 0xFFFFu);
+            if ((id & 31) == lane) taken |= 1u << (id >> 5);
+            // logit value of the winner, broadcast from its owner lane
+            float v = 0.f;
+#pragma unroll
+            for (int r = 0; r < kMaxExperts / 32; ++r)
+                if ((id >> 5) == r) v = val[r];
+            v = __shfl_sync(0xffffffffu, v, id & 31);
+            if (j == 0) top_l = v;
+            if (lane == j) { my_id = id; my_l = v; }
+        }
+        // pick weights in fp64: p_j = exp(l_j - l_top) / sum_i exp(l_i - l_top)
+        double ex = 0.0;
+        if (lane < k) ex = exp((double)my_l - (double)top_l);
+        double den = 0.0;
+        for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order j = 0..k-1
+        if (lane < k) {
+            a.ids[(size_t)t * k + lane] = my_id;
+            a.p[(size_t)t * k + lane] = double_to_bf16_bits(ex / den);
+            atomicAdd(&sh_hist[my_id], 1);
+        }
+        if (lane == 0 && a.w_s) {
+            uint16_t ws = 0;
+            if (a.has_shared) {
+                const float gb = bf16_bits_to_float(float_to_bf16_bits(a.gamma[t]));
+                ws = double_to_bf16_bits(1.0 / (1.0 + exp(-(double)gb)));
+            }
+            a.w_s[t] = ws;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) a.hist[(size_t)blockIdx.x * E + e] = sh_hist[e];
+}
+
+// Work lists of the expert kernels from the per-expert slot counts: expert e
+// (in increasing id, the shared expert last as id E) contributes
+// ceil(count_e / n) items of at most n tokens, for n = 16 (decode GEMV),
+// kTileN1 (gate/up GEMM) and kTileN2 (down GEMM).  Called by a whole block.
+__device__ void build_work_lists(const int *s_cnt, int E, int T, int has_shared, int32_t *nwork,
+                                 WorkItem *work_dec, WorkItem *work_g1, WorkItem *work_g2, const int *max_items,
+                                 int *status)
+{
+    __shared__ int s_items[3][kMaxExperts + 2];
+    const int tid = threadIdx.x;
+    const int tile_n[3] = {kDecodeMaxTok, kTileN1, kTileN2};
+    for (int w = 0; w < 3; ++w)
+        for (int e = tid; e <= E; e += blockDim.x) {
+            const int c = e < E ? s_cnt[e] : (has_shared ? T : 0);
+            s_items[w][e] = (c + tile_n[w] - 1) / tile_n[w];
+        }
+    __syncthreads();
+    if (tid < 3) {
+        int run = 0;
+        for (int e = 0; e <= E; ++e) { const int n = s_items[tid][e]; s_items[tid][e] = run; run += n; }
+        if (run > max_items[tid]) {          // counts inconsistent with T*k: build nothing
+            record_status(status, MOE_ERR_DEVICE);
+            run = -1;
+        }
+        s_items[tid][E + 1] = run;
+        nwork[tid] = run < 0 ? 0 : run;
+    }
+    __syncthreads();
+    WorkItem *lists[3] = {work_dec, work_g1, work_g2};
+    for (int w = 0; w < 3; ++w)
+        for (int e = tid; e <= E && s_items[w][E + 1] >= 0; e += blockDim.x) {
+            const int c = e < E ? s_cnt[e] : (has_shared ? T : 0);
+            int pos = s_items[w][e];
+            for (int t0 = 0; t0 < c; t0 += tile_n[w]) {
+                WorkItem it;
+                it.expert = e;
+                it.tok0 = t0;
+                it.ntok = min(tile_n[w], c - t0);
+                it.pad = 0;
+                lists[w][pos++] = it;
+            }
+        }
+}
+
+// Work lists alone, from caller-supplied counts (standalone expert FFN call).
+// Also clears the status word: it is the first kernel of that call.
+__global__ void __launch_bounds__(256) worklist_kernel(WorklistArgs a)
+{
+    __shared__ int s_cnt[kMaxExperts];
+    if (threadIdx.x == 0) *a.status = 0;
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        int c = a.counts[e];
+        if (c < 0 || c > a.T) {
+            record_status(a.status, MOE_ERR_DEVICE);
+            c = 0;
+        }
+        s_cnt[e] = c;
+    }
+    __syncthreads();
+    build_work_lists(s_cnt, a.E, a.T, a.has_shared, a.nwork, a.work_dec, a.work_g1, a.work_g2, a.max_items,
+                     a.status);
+}
+
+// Per-block histogram of the slots' expert ids (standalone permute call);
+// clears the status word first (first kernel of that call).
+__global__ void __launch_bounds__(1024) hist_kernel(HistArgs a)
+{
+    __shared__ int sh[kMaxExperts];
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) sh[e] = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0;
+    __syncthreads();
+    const int f_begin = blockIdx.x * kTokBlock * a.k;
+    const int f_end = min(a.T, (int)(blockIdx.x + 1) * kTokBlock) * a.k;
+    for (int f = f_begin + threadIdx.x; f < f_end; f += blockDim.x) {
+        const int e = a.ids[f];
+        if (e >= 0 && e < a.E) atomicAdd(&sh[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.hist[(size_t)blockIdx.x * a.E + e] = sh[e];
+}
+
+// ---------------------------------------------------------------- permutation
+//
+// Block b owns the slots of tokens [128 b, 128 b + 128).  Every block sums the
+// histogram column of each expert over all blocks (counts) and over the blocks
+// before it (its base inside each expert's segment), scans counts into
+// offsets, then scatters its own slots in increasing flat index: within a
+// warp, lanes holding the same expert are ranked by __match_any_sync; across
+// warps, by per-warp per-expert counts in shared memory.  Block 0 also writes
+// counts/offsets and the work lists of the expert kernels.
+__global__ void __launch_bounds__(1024) permute_kernel(PermuteArgs a)
+{
+    __shared__ int s_base[kMaxExperts];     // offsets[e] + slots of e in earlier blocks
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_wcnt[32][kMaxExperts]; // per-warp counts of the current chunk
+    const int E = a.E, k = a.k, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    for (int e = tid; e < E; e += blockDim.x) {
+        int tot = 0, before = 0;
+        for (int b = 0; b < a.nblk; ++b) {
+            const int h = a.hist[(size_t)b * E + e];
+            tot += h;
+            if (b < (int)blockIdx.x) before += h;
+        }
+        s_cnt[e] = tot;
+        s_base[e] = before;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) { s_off[e] = run; run += s_cnt[e]; }
+        s_off[E] = run;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) s_base[e] += s_off[e];
+
+    if (blockIdx.x == 0) {
+        for (int e = tid; e < E; e += blockDim.x) a.counts[e] = s_cnt[e];
+        for (int e = tid; e <= E; e += blockDim.x) a.offsets[e] = s_off[e];
+        if (a.build_work)
+            build_work_lists(s_cnt, E, a.T, a.has_shared, a.nwork, a.work_dec, a.work_g1, a.work_g2, a.max_items,
+                             a.status);
+    }
+
+    // stable scatter of this block's slots, 1024 at a time
+    const int f_begin = blockIdx.x * kTokBlock * k;
+    const int f_end = min(a.T, (int)(blockIdx.x + 1) * kTokBlock) * k;
+    for (int c0 = f_begin; c0 < f_end; c0 += blockDim.x) {
+        for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&s_wcnt[0][0])[i] = 0;
+        __syncthreads();
+        const int f = c0 + tid;
+        const bool valid = f < f_end;
+        int e = valid ? a.ids[f] : -1;
+        if (valid && (e < 0 || e >= E)) {
+            record_status(a.status, MOE_ERR_DEVICE);
+            e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank_in_warp == 0) s_wcnt[warp][e] = __popc(peers);
+        __syncthreads();
+        if (e >= 0) {
+            int before = 0;
+            for (int w = 0; w < warp; ++w) before += s_wcnt[w][e];
+            const int pos = s_base[e] + before + rank_in_warp;
+            a.perm[pos] = f;
+            a.inv_perm[f] = pos;
+        }
+        __syncthreads();
+        for (int ee = tid; ee < E; ee += blockDim.x) {
+            int tot = 0;
+            for (int w = 0; w < 32; ++w) tot += s_wcnt[w][ee];
+            s_base[ee] += tot;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- launchers
+
+cudaError_t launch_route_gemv(const RouteArgs &a, cudaStream_t st)
+{
+    dim3 grid(a.n_expert_tiles + 1, (a.T + 7) / 8);
+    route_gemv_kernel<<<grid, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const TopkArgs &a, cudaStream_t st)
+{
+    topk_kernel<<<(a.T + kTokBlock - 1) / kTokBlock, 1024, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_hist(const HistArgs &a, cudaStream_t st)
+{
+    hist_kernel<<<a.nblk, 1024, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_worklist(const WorklistArgs &a, cudaStream_t st)
+{
+    worklist_kernel<<<1, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t st)
+{
+    permute_kernel<<<a.nblk, 1024, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace qmoe
