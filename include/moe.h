@@ -191,7 +191,7 @@ MOE_API int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *
 
 /* Upper bound on the polls of every bounded wait inside the kernels (mbarrier
  * waits of the tensor-core pipeline).  A wait that reaches it records
- * MOE_ERR_TIMEOUT and the kernel returns early.  Default 1 << 26 polls
+ * MOE_ERR_TIMEOUT and the kernel returns early.  Default 1 << 24 polls
  * (about a second); values <= 0 restore the default.  Affects launches
  * enqueued after the call; meant for fault-handling tests. */
 MOE_API int moe_set_wait_limit(long long polls);

@@ -91,6 +91,22 @@ struct ReduceArgs {
     int T, H, k, has_shared;
 };
 
+struct PrefillArgs {
+    const uint16_t *x;            // bf16 [T, H]
+    uint16_t *x16;                // fp16 [T, H] scratch (K-permuted)
+    uint16_t *hs;                 // fp16 [T*k + T, I] scratch, expert-sorted rows
+    QMatDev gate, up, down, s_gate, s_up, s_down;
+    const int32_t *nwork, *offsets, *perm;
+    const WorkItem *work_g1, *work_g2;
+    const uint16_t *p, *w_s;
+    float *acc;                   // f32 [T, H]
+    int acc_zero;                 // 1: zero acc first
+    int *status;
+    int T, H, I, E, k, has_shared, max_w1, max_w2;
+    long long wait_limit;
+};
+
+cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st);
 cudaError_t launch_route_gemv(const RouteArgs &a, cudaStream_t st);
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t st);
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t st);

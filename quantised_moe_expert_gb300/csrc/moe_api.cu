@@ -8,7 +8,7 @@ using namespace qmoe;
 
 namespace {
 
-std::atomic<long long> g_wait_limit{1ll << 26};
+std::atomic<long long> g_wait_limit{1ll << 24};
 
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned16_or_null(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -170,9 +170,40 @@ int enqueue_decode_experts(const moe_config &c, ExpertArgs ea, const WsLayout &L
     return cuda_rc(launch_decode_reduce(r, st));
 }
 
-int enqueue_prefill_experts(const moe_config &, ExpertArgs, const WsLayout &, void *, cudaStream_t)
+// Prefill expert GEMMs; acc is zeroed first when acc_zero (the fused forward).
+int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsLayout &L, void *ws, int acc_zero,
+                            cudaStream_t st)
 {
-    return MOE_ERR_UNSUPPORTED;
+    PrefillArgs a{};
+    a.x = ea.x;
+    a.x16 = ws_at<uint16_t>(ws, L.x16);
+    a.hs = ws_at<uint16_t>(ws, L.h);
+    a.gate = ea.gate;
+    a.up = ea.up;
+    a.down = ea.down;
+    a.s_gate = ea.s_gate;
+    a.s_up = ea.s_up;
+    a.s_down = ea.s_down;
+    a.nwork = ea.nwork;
+    a.offsets = ea.offsets;
+    a.perm = ea.perm;
+    a.work_g1 = ws_at<WorkItem>(ws, L.work_g1);
+    a.work_g2 = ws_at<WorkItem>(ws, L.work_g2);
+    a.p = ea.p;
+    a.w_s = ea.w_s;
+    a.acc = ea.acc;
+    a.acc_zero = acc_zero;
+    a.status = ea.status;
+    a.T = ea.T;
+    a.H = c.hidden;
+    a.I = c.inter;
+    a.E = c.n_experts;
+    a.k = c.top_k;
+    a.has_shared = c.has_shared;
+    a.max_w1 = L.max_w1;
+    a.max_w2 = L.max_w2;
+    a.wait_limit = g_wait_limit.load();
+    return cuda_rc(launch_prefill_experts(a, st));
 }
 
 bool weights_ok(const moe_config &c, const moe_weights *w, bool need_router, bool need_experts)
@@ -302,7 +333,7 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     if ((rc = cuda_rc(launch_worklist(wa, st)))) return rc;
     ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_shared, offsets, perm, acc, L, ws);
     if (resolve_path(path, T) == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, nullptr, st);
-    return enqueue_prefill_experts(*cfg, ea, L, ws, st);
+    return enqueue_prefill_experts(*cfg, ea, L, ws, 0, st);
 }
 
 int moe_combine(const moe_config *cfg, int T, const float *acc, uint16_t *y, void *stream)
@@ -330,10 +361,6 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
     if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
     if (T == 0) return MOE_OK;
     const int rp = resolve_path(path, T);
-    if (rp == MOE_PATH_PREFILL) {
-        // the prefill GEMMs are checked before anything is enqueued
-        if ((rc = enqueue_prefill_experts(*cfg, ExpertArgs{}, L, nullptr, nullptr)) == MOE_ERR_UNSUPPORTED) return rc;
-    }
     auto st = static_cast<cudaStream_t>(stream);
     int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.ids);
     uint16_t *p = p_out ? p_out : ws_at<uint16_t>(ws, L.p);
@@ -348,7 +375,8 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
         return rc;
     ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_s, offsets, perm, ws_at<float>(ws, L.acc), L, ws);
     if (rp == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, y, st);
-    return enqueue_prefill_experts(*cfg, ea, L, ws, st);
+    if ((rc = enqueue_prefill_experts(*cfg, ea, L, ws, 1, st))) return rc;
+    return cuda_rc(launch_combine(ea.acc, y, (size_t)T * cfg->hidden, st));
 }
 
 int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_status)
@@ -366,7 +394,7 @@ int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_s
 
 int moe_set_wait_limit(long long polls)
 {
-    g_wait_limit.store(polls > 0 ? polls : (1ll << 26));
+    g_wait_limit.store(polls > 0 ? polls : (1ll << 24));
     return MOE_OK;
 }
 

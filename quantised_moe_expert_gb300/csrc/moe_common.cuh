@@ -49,7 +49,8 @@ struct WsLayout {
     size_t work_dec;   // WorkItem [E + 1]
     size_t work_g1;    // WorkItem [max tiles gemm1]
     size_t work_g2;    // WorkItem [max tiles gemm2]
-    size_t h;          // bf16 [T*k + T, I]
+    size_t x16;        // fp16 [T, H] (prefill B operand)
+    size_t h;          // fp16 [T*k + T, I] (decode: slot order; prefill: expert-sorted, K-permuted)
     size_t yslot;      // f32 [T*k + T, H] (decode)
     size_t acc;        // f32 [T, H] (prefill accumulation)
     size_t total;
@@ -94,6 +95,7 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.work_dec = take(sizeof(WorkItem) * (size_t)L.max_wd);
     L.work_g1 = take(sizeof(WorkItem) * (size_t)L.max_w1);
     L.work_g2 = take(sizeof(WorkItem) * (size_t)L.max_w2);
+    L.x16 = take(2 * Tz * H);
     L.h = take(2 * Tz * (k + 1) * I);
     L.yslot = take(4 * Tz * (k + 1) * H);
     L.acc = take(4 * Tz * H);

@@ -1,0 +1,156 @@
+"""GPU parity of the prefill (tcgen05 grouped GEMM) path against the FP64 oracle.
+
+Small cases are compared element by element on every row; the T = 512 and
+T = 4096 layers on sampled rows (the oracle's rows are independent), and
+routing (ids, permutation) on every row.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantised_moe_expert_gb300 as qm
+from quantised_moe_expert_gb300 import synth
+
+from . import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    qm.load()
+    oracle.build()
+
+
+def _compare_rows(wl, w, x, got, rows, bias=None, logits_in=None):
+    ref = oracle.forward(wl.shape, w, x, bias=bias, logits_in=logits_in, rows=rows)
+    g = {key: got[key][rows] for key in ("y", "ids", "p", "w_s")}
+    gap = H.oracle_gap(ref["logits"], wl.shape.top_k)
+    clear = gap >= (0 if logits_in is not None else H.AMBIGUOUS_GAP)
+    assert np.array_equal(g["ids"][clear], ref["ids"][clear])
+    same = np.nonzero(np.all(g["ids"] == ref["ids"], axis=1))[0]
+    assert len(same) >= len(rows) - 2
+    assert H.ulp_diff_bf16(g["p"][same], ref["p"][same]).max(initial=0) <= 1
+    return H.check_y(g["y"], ref["y"], rows=same)
+
+
+def test_prefill_tiny_all_rows():
+    wl, w, layer = H.device_layer(0)
+    x = synth.make_x(wl.shape, wl.tokens, wl.seed)
+    got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
+    assert got["status"] == 0
+    stats = _compare_rows(wl, w, x, got, np.arange(wl.tokens))
+    assert stats["max_abs"] <= 2e-2, stats
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 40, 129])
+def test_prefill_ragged_token_counts_small_layer(T):
+    """Token counts that leave ragged N tiles, several tiles per expert and tiny experts."""
+    wl, w, layer = H.device_layer(0)
+    x = synth.make_x(wl.shape, T, wl.seed, stream=T)
+    got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
+    assert got["status"] == 0
+    _compare_rows(wl, w, x, got, np.arange(T))
+
+
+def test_prefill_t512_sampled_rows():
+    wl, w, layer = H.device_layer(3)
+    x = synth.make_x(wl.shape, wl.tokens, wl.seed)
+    got = H.run_forward(layer, x, path=qm.MOE_PATH_AUTO)
+    assert got["status"] == 0
+    rows = np.random.default_rng(0).choice(wl.tokens, 24, replace=False)
+    rows = np.concatenate([rows, [0, wl.tokens - 1]])
+    _compare_rows(wl, w, x, got, rows)
+
+
+def test_prefill_t4096_zipf_sampled_rows_and_full_routing():
+    wl, w, layer = H.device_layer(4)
+    x = synth.make_x(wl.shape, wl.tokens, wl.seed)
+    bias = synth.zipf_bias(wl.shape, wl.zipf_s, wl.seed)
+    got = H.run_forward(layer, x, path=qm.MOE_PATH_AUTO, router_bias=bias)
+    assert got["status"] == 0
+    rows = np.random.default_rng(1).choice(wl.tokens, 24, replace=False)
+    _compare_rows(wl, w, x, got, np.concatenate([rows, [wl.tokens - 1]]), bias=bias)
+    # every row's routing against the oracle's router and top-k
+    ref_logits = oracle.router_logits(wl.shape, w, x, bias)
+    ref_ids = oracle.topk(ref_logits, wl.shape.top_k)
+    clear = H.oracle_gap(ref_logits, wl.shape.top_k) >= H.AMBIGUOUS_GAP
+    assert np.array_equal(got["ids"][clear], ref_ids[clear])
+    counts = np.bincount(ref_ids.ravel(), minlength=wl.shape.n_experts)
+    assert counts.max() > 8 * wl.tokens * wl.shape.top_k / wl.shape.n_experts   # the skew is real
+
+
+def test_prefill_t4096_forced_ties_bit_exact_routing():
+    """Supplied logits with 5% of rows snapped to 1/8: ids, p, w_s, permutation bit-exact on all rows."""
+    wl, w, layer = H.device_layer(4)
+    x = synth.make_x(wl.shape, wl.tokens, wl.seed)
+    bias = synth.zipf_bias(wl.shape, wl.zipf_s, wl.seed)
+    lg = synth.snap_rows_to_eighths(oracle.router_logits(wl.shape, w, x, bias), wl.tie_every)
+    gaps = H.oracle_gap(lg, wl.shape.top_k)
+    assert (gaps == 0).sum() >= 1
+    r = H.run_route(layer, x, logits_in=lg)
+    ref_ids = oracle.topk(lg, wl.shape.top_k)
+    assert np.array_equal(r["ids"], ref_ids)
+    _, ref_p = oracle.pick_weights(lg, ref_ids)
+    assert np.array_equal(r["p"], ref_p)
+    _, ref_ws = oracle.shared_weight(x, w.shared_gate_vec)
+    assert H.ulp_diff_bf16(r["w_s"], ref_ws).max() <= 1
+    # permutation of the full batch
+    T, k = wl.tokens, wl.shape.top_k
+    ws = qm.workspace(layer.cfg, T)
+    counts = torch.empty(256, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(257, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    qm.moe_permute(layer.cfg, torch.from_numpy(ref_ids).cuda(), T, counts, offsets, perm, inv, ws)
+    torch.cuda.synchronize()
+    rc, ro, rp, ri = oracle.permute(ref_ids, 256)
+    assert np.array_equal(perm.cpu().numpy(), rp) and np.array_equal(inv.cpu().numpy(), ri)
+    assert np.array_equal(counts.cpu().numpy(), rc) and np.array_equal(offsets.cpu().numpy(), ro)
+    # the whole layer on the forced-tie logits, sampled rows (tie rows included)
+    got = H.run_forward(layer, x, logits_in=lg)
+    rows = np.concatenate([np.arange(0, T, 20)[:12], np.random.default_rng(2).choice(T, 12, replace=False)])
+    _compare_rows(wl, w, x, got, rows, logits_in=lg)
+
+
+def test_decode_and_prefill_paths_agree():
+    wl, w, layer = H.device_layer(2)
+    x = synth.make_x(wl.shape, 16, wl.seed, stream=3)
+    a = H.run_forward(layer, x, path=qm.MOE_PATH_DECODE)
+    b = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
+    assert np.array_equal(a["ids"], b["ids"]) and np.array_equal(a["p"], b["p"])
+    H.check_y(b["y"], a["y"])
+
+
+def test_staged_prefill_expert_ffn_accumulates():
+    """moe_expert_ffn on the prefill path adds into a caller accumulator (twice = 2x)."""
+    wl, w, layer = H.device_layer(0)
+    T = 40
+    sh = wl.shape
+    x_bits = synth.make_x(sh, T, wl.seed, stream=5)
+    x = H.to_dev_u16(x_bits)
+    ws = qm.workspace(layer.cfg, T)
+    ids = torch.empty((T, sh.top_k), dtype=torch.int32, device="cuda")
+    p = torch.empty((T, sh.top_k), dtype=torch.int16, device="cuda")
+    w_s = torch.empty((T,), dtype=torch.int16, device="cuda")
+    qm.moe_route(layer.cfg, layer.w, x, T, None, None, None, ids, p, w_s, ws)
+    counts = torch.empty(sh.n_experts, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(sh.n_experts + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * sh.top_k, dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * sh.top_k, dtype=torch.int32, device="cuda")
+    qm.moe_permute(layer.cfg, ids, T, counts, offsets, perm, inv, ws)
+    acc = torch.zeros((T, sh.hidden), dtype=torch.float32, device="cuda")
+    qm.moe_expert_ffn(layer.cfg, layer.w, x, T, ids, p, w_s, counts, offsets, perm, acc, qm.MOE_PATH_PREFILL, ws)
+    once = acc.clone()
+    qm.moe_expert_ffn(layer.cfg, layer.w, x, T, ids, p, w_s, counts, offsets, perm, acc, qm.MOE_PATH_PREFILL, ws)
+    torch.cuda.synchronize()
+    assert qm.moe_get_device_status(ws) == 0
+    assert torch.allclose(acc, 2 * once, rtol=1e-5, atol=1e-5)
+    y = torch.empty((T, sh.hidden), dtype=torch.int16, device="cuda")
+    qm.moe_combine(layer.cfg, T, once, y)
+    torch.cuda.synchronize()
+    ref = oracle.forward(sh, w, x_bits)
+    H.check_y(H.u16(y), ref["y"])
