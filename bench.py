@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="warm-up and timed steps only (for a profiler's launch list): no clocks, stage, e2e, "
+                         "CPU baseline or sweep")
     return ap.parse_args()
 
 
@@ -93,16 +96,24 @@ def barrier(pg):
     import torch
     if pg is not None:
         pg.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(pg, v):
+    """Largest value over all ranks (the slowest rank's time); identity without a process group."""
     import torch
     if pg is None:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     pg.all_reduce(t, op=pg.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tokens_per_s(world, steps, tokens, max_ms):
+    """Weak scaling: every rank processes `steps` batches of `tokens`; the job takes the slowest rank's time."""
+    return world * steps * tokens / (max_ms / 1e3)
 
 
 # ----------------------------------------------------------------- clocks
@@ -259,33 +270,39 @@ def run_ours(args, wl, rank, world, pg, steps, warmup, want_extras):
 
     g_warm = capture(lambda i: W.step(i, stream), max(warmup, 1), stream)
     g_timed = capture(lambda i: W.step(i, stream), steps, stream)
+
+    def replay(g):
+        # CUDAGraph.replay() launches on the current stream: make it the timed stream
+        with torch.cuda.stream(stream):
+            g.replay()
+
     for _ in range(2):
-        g_warm.replay()
+        replay(g_warm)
     torch.cuda.synchronize()
     st = qm.moe_get_device_status(W.ws[0], stream)
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
 
-    clocks = ClockSampler(torch.cuda.current_device()) if want_extras else None
+    clocks = ClockSampler(torch.cuda.current_device()) if want_extras and not args.profile else None
     if clocks:
         clocks.start()
         time.sleep(0.3)
         clocks.mark(True)
         t_end = time.time() + 1.0          # keep the GPU busy so clocks settle under load
         while time.time() < t_end:
-            g_warm.replay()
-        torch.cuda.synchronize()
+            replay(g_warm)
+            torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(pg)
     ev0.record(stream)
-    g_timed.replay()
+    replay(g_timed)
     ev1.record(stream)
     barrier(pg)
     if clocks:
         t_end = time.time() + 0.5
         while time.time() < t_end:
-            g_warm.replay()
-        torch.cuda.synchronize()
+            replay(g_warm)
+            torch.cuda.synchronize()
         clocks.mark(False)
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(pg, ms)
@@ -293,15 +310,14 @@ def run_ours(args, wl, rank, world, pg, steps, warmup, want_extras):
         if qm.moe_get_device_status(W.ws[c], stream) != 0:
             raise RuntimeError("device status set during the timed steps")
     distinct = W.distinct_experts()
-    total_tokens = world * steps * wl.tokens
-    value = total_tokens / (ms / 1e3)
+    value = whole_job_tokens_per_s(world, steps, wl.tokens, ms)
     res = dict(value=value, ms_per_step=ms / steps, copies=copies, distinct=distinct)
     bytes_step, expert_bytes, flops = algorithmic(wl, W, distinct)
     res["bytes_step"] = bytes_step
     res["flops_step"] = flops
     res["kernels"] = steps * W.kernels_per_step()
     res["clocks"] = clocks.stop() if clocks else None
-    if want_extras:
+    if want_extras and not args.profile:
         res["stage"] = stage_timing(W, stream, steps, expert_bytes, flops)
         res["e2e"] = e2e_timing(W, stream, steps, warmup)
     del g_warm, g_timed
@@ -343,8 +359,9 @@ def stage_timing(W, stream, steps, expert_bytes, flops):
         qm.moe_combine(L.cfg, T, b["acc"], W.y[c], stream)
 
     g = capture(step, n, stream)
-    g.replay()
-    g.replay()
+    with torch.cuda.stream(stream):
+        g.replay()
+        g.replay()
     torch.cuda.synchronize()
     times = [a.elapsed_time(b) for a, b in evs]
     ms = float(np.mean(times))
@@ -466,6 +483,10 @@ def main():
     rank, world, local, pg = dist_setup(args.gpus)
     hbm, tc, tc_sus, peak_src = peaks()
     r = run_ours(args, wl, rank, world, pg, steps, warmup, want_extras=True)
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile_run": wl.name, "ms_per_step": r["ms_per_step"], "steps": steps}), flush=True)
+        return
     st = r["stage"]
     decode = wl.tokens <= 16
     if decode:

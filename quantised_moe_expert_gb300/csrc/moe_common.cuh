@@ -64,8 +64,10 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 inline int max_tiles(int T, int k, int E, int has_shared, int tile_n)
 {
-    // sum_e ceil(c_e / n) <= (T*k) / n + E, plus the shared expert's ceil(T / n).
-    long long t = (long long)T * k / tile_n + E + (has_shared ? (T + tile_n - 1) / tile_n : 0) + 1;
+    // sum over active experts of ceil(c_e / n) <= (T*k) / n + (number of active experts),
+    // and at most min(E, T*k) experts are active; plus the shared expert's ceil(T / n).
+    const long long active = (long long)T * k < E ? (long long)T * k : E;
+    long long t = (long long)T * k / tile_n + active + (has_shared ? (T + tile_n - 1) / tile_n : 0) + 1;
     return (int)t;
 }
 

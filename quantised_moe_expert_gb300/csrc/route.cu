@@ -206,6 +206,30 @@ __global__ void __launch_bounds__(1024) topk_kernel(TopkArgs a)
     for (int e = threadIdx.x; e < E; e += blockDim.x) a.hist[(size_t)blockIdx.x * E + e] = sh_hist[e];
 }
 
+// Exclusive prefix sum of a[0..n) in place, by one full warp; returns the total.
+// Lane l scans a contiguous chunk, the chunk sums are scanned with shuffles.
+__device__ int warp_exclusive_scan(int *a, int n)
+{
+    const int lane = threadIdx.x & 31;
+    const int per = (n + 31) / 32;
+    const int b = lane * per, e = min(n, b + per);
+    int local = 0;
+    for (int i = b; i < e; ++i) local += a[i];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int i = b; i < e; ++i) {
+        const int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    return __shfl_sync(0xffffffffu, incl, 31);
+}
+
 // Work lists of the expert kernels from the per-expert slot counts: expert e
 // (in increasing id, the shared expert last as id E) contributes
 // ceil(count_e / n) items of at most n tokens, for n = 16 (decode GEMV),
@@ -223,15 +247,17 @@ __device__ void build_work_lists(const int *s_cnt, int E, int T, int has_shared,
             s_items[w][e] = (c + tile_n[w] - 1) / tile_n[w];
         }
     __syncthreads();
-    if (tid < 3) {
-        int run = 0;
-        for (int e = 0; e <= E; ++e) { const int n = s_items[tid][e]; s_items[tid][e] = run; run += n; }
-        if (run > max_items[tid]) {          // counts inconsistent with T*k: build nothing
-            record_status(status, MOE_ERR_DEVICE);
-            run = -1;
+    if (tid < 3 * 32) {
+        const int w = tid >> 5;
+        int run = warp_exclusive_scan(s_items[w], E + 1);
+        if ((tid & 31) == 0) {
+            if (run > max_items[w]) {        // counts inconsistent with T*k: build nothing
+                record_status(status, MOE_ERR_DEVICE);
+                run = -1;
+            }
+            s_items[w][E + 1] = run;
+            nwork[w] = run < 0 ? 0 : run;
         }
-        s_items[tid][E + 1] = run;
-        nwork[tid] = run < 0 ? 0 : run;
     }
     __syncthreads();
     WorkItem *lists[3] = {work_dec, work_g1, work_g2};
@@ -315,10 +341,11 @@ __global__ void __launch_bounds__(1024) permute_kernel(PermuteArgs a)
         s_base[e] = before;
     }
     __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int e = 0; e < E; ++e) { s_off[e] = run; run += s_cnt[e]; }
-        s_off[E] = run;
+    if (tid < 32) {
+        for (int e = tid; e < E; e += 32) s_off[e] = s_cnt[e];
+        __syncwarp();
+        const int total = warp_exclusive_scan(s_off, E);
+        if (tid == 0) s_off[E] = total;
     }
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) s_base[e] += s_off[e];
