@@ -146,14 +146,15 @@ __device__ __forceinline__ void item_columns(const ExpertArgs &a, const WorkItem
 
 // ------------------------------------------------------------ gate/up + SwiGLU
 //
-// grid (I/16, max items); 128 threads.  Block (rb, item) computes rows
+// grid (I/16, max items); 256 threads.  Block (rb, item) computes rows
 // [16 rb, 16 rb + 16) of gate and up for the item's <= 16 tokens; warp w takes
-// a quarter of the hidden groups and the quarters are added in warp order.
+// an eighth of the hidden groups and the eighths are added in warp order (the
+// same split and order as the fused decode kernel, so both give the same bits).
 template <int NT>
-__global__ void __launch_bounds__(128) decode_gateup_kernel(ExpertArgs a)
+__global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
 {
     extern __shared__ uint4 s_x[];                 // [NT*8][H/8 + 1] (one uint4 of padding per row)
-    __shared__ float s_red[4][2][16][NT * 8];      // [warp][gate/up][row][col]
+    __shared__ float s_red[8][2][16][NT * 8];      // [warp][gate/up][row][col]
     __shared__ int s_tok[kDecodeMaxTok], s_slot[kDecodeMaxTok];
     if ((int)blockIdx.y >= __ldg(a.nwork + 0)) return;
     const WorkItem it = a.work[blockIdx.y];
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(128) decode_gateup_kernel(ExpertArgs a)
     const ExpertView vg = is_shared ? expert_view(a.s_gate, 0, I, H) : expert_view(a.gate, it.expert, I, H);
     const ExpertView vu = is_shared ? expert_view(a.s_up, 0, I, H) : expert_view(a.up, it.expert, I, H);
     const int r0 = blockIdx.x * 16 + g, r1 = r0 + 8;
-    const int gbeg = (warp * G) / 4, gend = ((warp + 1) * G) / 4;
+    const int gbeg = (warp * G) / 8, gend = ((warp + 1) * G) / 8;
 
     float acc_g[NT][4], acc_u[NT][4];
 #pragma unroll
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(128) decode_gateup_kernel(ExpertArgs a)
         if (f < 0) continue;
         float gs = 0.f, us = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+        for (int w = 0; w < 8; ++w) {
             gs += s_red[w][0][row][c];
             us += s_red[w][1][row][c];
         }
@@ -380,10 +381,10 @@ cudaError_t launch_decode_gateup(const ExpertArgs &a, cudaStream_t st)
     dim3 grid(a.I / 16, a.max_items);
     if (ncol == 16) {
         cudaFuncSetAttribute(decode_gateup_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        decode_gateup_kernel<2><<<grid, 128, smem, st>>>(a);
+        decode_gateup_kernel<2><<<grid, 256, smem, st>>>(a);
     } else {
         cudaFuncSetAttribute(decode_gateup_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        decode_gateup_kernel<1><<<grid, 128, smem, st>>>(a);
+        decode_gateup_kernel<1><<<grid, 256, smem, st>>>(a);
     }
     return cudaGetLastError();
 }

@@ -15,6 +15,8 @@ struct RouteArgs {
     float *logits;                // f32 [T, E]
     float *gamma;                 // f32 [T]
     int *status_reset;            // non-null: cleared by the first thread (first kernel of a call)
+    int *zero;                    // non-null: block (0,0) zeroes zero[0, nzero) (counters of the next kernel)
+    int nzero;
     int T, H, E;
     int n_expert_tiles;           // 0: only the gamma column runs
 };
@@ -107,6 +109,26 @@ struct PrefillArgs {
 };
 
 cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st);
+
+struct FusedDecodeArgs {
+    const uint16_t *x;            // bf16 [T, H]
+    QMatDev gate, up, down, s_gate, s_up, s_down;
+    const float *logits;          // f32 [T, E]
+    const float *gamma;           // f32 [T]
+    int32_t *ids_out;             // [T, k] or null
+    uint16_t *p_out;              // bf16 [T, k] or null
+    uint16_t *ws_out;             // bf16 [T] or null
+    uint16_t *h;                  // fp16 [T*k + T, I], slot order
+    float *yslot;                 // f32 [T*k + T, H]
+    uint16_t *y;                  // bf16 [T, H]
+    int *cnt_expert;              // [E + 1] gate/up units done, per expert-list entry (zeroed before launch)
+    int *cnt_rows;                // [H / 16] down units done, per 16-row block (zeroed before launch)
+    int *status;
+    int T, H, I, E, k, has_shared;
+    long long wait_limit;
+};
+
+cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t st);
 cudaError_t launch_route_gemv(const RouteArgs &a, cudaStream_t st);
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t st);
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t st);

@@ -49,9 +49,9 @@ int resolve_path(int path, int T)
 }
 
 // Router GEMV (or pass-through of supplied logits) and top-k into the given buffers.
-int enqueue_route(const moe_config &c, const moe_weights &w, const uint16_t *x, int T, const float *router_bias,
-                  const float *logits_in, float *logits, int32_t *ids, uint16_t *p, uint16_t *w_s,
-                  const WsLayout &L, void *ws, cudaStream_t st)
+// Router GEMV (and gamma) only; zeroes the fused decode counters.
+RouteArgs route_args(const moe_config &c, const moe_weights &w, const uint16_t *x, int T, const float *router_bias,
+                     const float *logits_in, float *logits, const WsLayout &L, void *ws)
 {
     RouteArgs ra{};
     ra.x = x;
@@ -67,6 +67,14 @@ int enqueue_route(const moe_config &c, const moe_weights &w, const uint16_t *x, 
     ra.H = c.hidden;
     ra.E = c.n_experts;
     ra.n_expert_tiles = logits_in ? 0 : (c.n_experts + 7) / 8;
+    return ra;
+}
+
+int enqueue_route(const moe_config &c, const moe_weights &w, const uint16_t *x, int T, const float *router_bias,
+                  const float *logits_in, float *logits, int32_t *ids, uint16_t *p, uint16_t *w_s,
+                  const WsLayout &L, void *ws, cudaStream_t st)
+{
+    RouteArgs ra = route_args(c, w, x, T, router_bias, logits_in, logits, L, ws);
     int rc = cuda_rc(launch_route_gemv(ra, st));
     if (rc) return rc;
     if (logits_in && logits && logits != logits_in) {
@@ -362,6 +370,43 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
     if (T == 0) return MOE_OK;
     const int rp = resolve_path(path, T);
     auto st = static_cast<cudaStream_t>(stream);
+    if (rp == MOE_PATH_DECODE && T <= kDecodeMaxTok) {
+        // router GEMV (zeroing the counters), then one cooperative launch for the rest of the layer
+        float *lg = logits_in ? const_cast<float *>(logits_in) : ws_at<float>(ws, L.logits);
+        RouteArgs ra = route_args(*cfg, *w, x, T, router_bias, logits_in, lg, L, ws);
+        ra.zero = ws_at<int>(ws, L.counters);
+        ra.nzero = cfg->n_experts + 1 + cfg->hidden / 16;
+        if ((rc = cuda_rc(launch_route_gemv(ra, st)))) return rc;
+        FusedDecodeArgs fa{};
+        fa.x = x;
+        fa.gate = dev(w->gate);
+        fa.up = dev(w->up);
+        fa.down = dev(w->down);
+        if (cfg->has_shared) {
+            fa.s_gate = dev(w->s_gate);
+            fa.s_up = dev(w->s_up);
+            fa.s_down = dev(w->s_down);
+        }
+        fa.logits = lg;
+        fa.gamma = ra.gamma;
+        fa.ids_out = ids_out;
+        fa.p_out = p_out;
+        fa.ws_out = w_shared_out;
+        fa.h = ws_at<uint16_t>(ws, L.h);
+        fa.yslot = ws_at<float>(ws, L.yslot);
+        fa.y = y;
+        fa.cnt_expert = ra.zero;
+        fa.cnt_rows = ra.zero + cfg->n_experts + 1;
+        fa.status = ws_at<int>(ws, L.status);
+        fa.T = T;
+        fa.H = cfg->hidden;
+        fa.I = cfg->inter;
+        fa.E = cfg->n_experts;
+        fa.k = cfg->top_k;
+        fa.has_shared = cfg->has_shared;
+        fa.wait_limit = g_wait_limit.load();
+        return cuda_rc(launch_decode_fused(fa, st));
+    }
     int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.ids);
     uint16_t *p = p_out ? p_out : ws_at<uint16_t>(ws, L.p);
     uint16_t *w_s = w_shared_out ? w_shared_out : ws_at<uint16_t>(ws, L.w_s);

@@ -246,12 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(smem_u32(empty + st));
             }
-            if (ok) {
-                mma_commit(smem_u32(accf));
-            } else {
-                mma_commit(smem_u32(drain));
-                mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
-            }
+            if (ok) mma_commit(smem_u32(accf));
+            // every MMA this thread issued completes before TMEM is freed, on every path
+            mma_commit(smem_u32(drain));
+            mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
     } else {
         // ------------------------------------------------ dequant (thread = weight row) + token rows
@@ -469,12 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16(tmem, desc_sw128(aa + kk * 32), desc_sw128(bb + kk * 32), idesc, (s | kk) != 0);
                 mma_commit(smem_u32(empty + st));
             }
-            if (ok) {
-                mma_commit(smem_u32(accf));
-            } else {
-                mma_commit(smem_u32(drain));
-                mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
-            }
+            if (ok) mma_commit(smem_u32(accf));
+            // every MMA this thread issued completes before TMEM is freed, on every path
+            mma_commit(smem_u32(drain));
+            mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
     } else {
         const int r = tid;

@@ -26,7 +26,10 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(RouteArgs a)
     const int H = a.H, E = a.E, G = a.H / kGroup;
     const int ntok = min(8, a.T - t0);
     const bool gamma_col = (int)blockIdx.x == a.n_expert_tiles;
-    if (a.status_reset && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.status_reset = 0;
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        if (a.status_reset && threadIdx.x == 0) *a.status_reset = 0;
+        for (int i = threadIdx.x; i < a.nzero; i += blockDim.x) a.zero[i] = 0;
+    }
 
     if (gamma_col) {
         // gamma[t] = sum_h x[t,h] * v[h] in fp32, warp w -> token t0 + w.

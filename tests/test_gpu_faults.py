@@ -1,0 +1,81 @@
+"""Device-side failure handling without a GPU fault.
+
+Every wait inside the kernels is bounded.  Setting the bound to one poll makes
+the tensor-core pipeline's waits run out before any copy can land: the kernels
+must record MOE_ERR_TIMEOUT in the workspace status word, drain what they
+issued, free their TMEM and return, leaving the context usable.  Nothing here
+traps, faults or hangs the GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantised_moe_expert_gb300 as qm
+from quantised_moe_expert_gb300 import synth
+
+from . import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    qm.load()
+    yield
+    qm.moe_set_wait_limit(0)
+
+
+def test_prefill_wait_limit_runs_out_then_recovers():
+    wl, w, layer = H.device_layer(0)
+    x = synth.make_x(wl.shape, 40, wl.seed, stream=9)
+    qm.moe_set_wait_limit(1)
+    try:
+        got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
+    finally:
+        qm.moe_set_wait_limit(0)
+    assert got["status"] == qm.MOE_ERR_TIMEOUT
+    again = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
+    assert again["status"] == 0
+    ref = oracle.forward(wl.shape, w, x)
+    assert np.array_equal(again["ids"], ref["ids"])
+    H.check_y(again["y"], ref["y"])
+
+
+def test_decode_wait_limit_is_bounded_then_recovers():
+    wl, w, layer = H.device_layer(2)
+    x = synth.make_x(wl.shape, 16, wl.seed, stream=9)
+    qm.moe_set_wait_limit(1)
+    try:
+        got = H.run_forward(layer, x, path=qm.MOE_PATH_DECODE)
+    finally:
+        qm.moe_set_wait_limit(0)
+    assert got["status"] in (0, qm.MOE_ERR_TIMEOUT)
+    again = H.run_forward(layer, x, path=qm.MOE_PATH_DECODE)
+    assert again["status"] == 0
+    ref = oracle.forward(wl.shape, w, x)
+    same = np.all(again["ids"] == ref["ids"], axis=1)
+    H.check_y(again["y"], ref["y"], rows=np.nonzero(same)[0])
+
+
+def test_bad_expert_ids_are_reported_not_trapped():
+    """Out-of-range ids given to moe_permute set MOE_ERR_DEVICE; nothing is written out of bounds."""
+    wl, w, layer = H.device_layer(0)
+    T, k, E = 8, wl.shape.top_k, wl.shape.n_experts
+    ids = np.tile(np.arange(k, dtype=np.int32), (T, 1))
+    ids[3, 1] = E + 5
+    ids[5, 0] = -2
+    ws = qm.workspace(layer.cfg, T)
+    guard = 1024
+    buf = torch.full((T * k + 2 * guard,), -7, dtype=torch.int32, device="cuda")
+    perm = buf[guard:guard + T * k]
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    qm.moe_permute(layer.cfg, torch.from_numpy(ids).cuda(), T, counts, offsets, perm, inv, ws)
+    torch.cuda.synchronize()
+    assert qm.moe_get_device_status(ws) == qm.MOE_ERR_DEVICE
+    b = buf.cpu()
+    assert torch.all(b[:guard] == -7) and torch.all(b[guard + T * k:] == -7)
