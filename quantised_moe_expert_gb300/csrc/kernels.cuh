@@ -21,13 +21,25 @@ struct RouteArgs {
     int n_expert_tiles;           // 0: only the gamma column runs
 };
 
+struct RouterMmaArgs {
+    const uint16_t *x;            // bf16 [T, H]
+    const uint8_t *codes;         // u8 [E, H]
+    const uint16_t *scales;       // bf16 [E, H/64]
+    const uint16_t *biases;
+    const float *router_bias;     // f32 [E] or null
+    float *logits;                // f32 [T, E]
+    int T, H, E;
+};
+
+cudaError_t launch_router_mma(const RouterMmaArgs &a, cudaStream_t st);
+
 struct TopkArgs {
     const float *logits;          // f32 [T, E]
     const float *gamma;           // f32 [T]
     int32_t *ids;                 // [T, k]
     uint16_t *p;                  // bf16 [T, k]
     uint16_t *w_s;                // bf16 [T] (may be null)
-    int32_t *hist;                // [nblk, E]
+    int32_t *hist;                // [nblk, E], zeroed beforehand; slots of tokens [128 b, 128 b + 128) count into row b
     int T, E, k, has_shared;
 };
 

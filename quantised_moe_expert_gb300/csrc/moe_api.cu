@@ -75,8 +75,25 @@ int enqueue_route(const moe_config &c, const moe_weights &w, const uint16_t *x, 
                   const WsLayout &L, void *ws, cudaStream_t st)
 {
     RouteArgs ra = route_args(c, w, x, T, router_bias, logits_in, logits, L, ws);
+    const bool mma_router = !logits_in && T > kDecodeMaxTok;
+    if (mma_router) ra.n_expert_tiles = 0;                  // gamma (and zeroing) only
+    ra.zero = ws_at<int>(ws, L.hist);                       // the top-k counts into a zeroed histogram
+    ra.nzero = L.nblk * c.n_experts;
     int rc = cuda_rc(launch_route_gemv(ra, st));
     if (rc) return rc;
+    if (mma_router) {
+        RouterMmaArgs rm{};
+        rm.x = x;
+        rm.codes = w.router.codes;
+        rm.scales = w.router.scales;
+        rm.biases = w.router.biases;
+        rm.router_bias = router_bias;
+        rm.logits = logits;
+        rm.T = T;
+        rm.H = c.hidden;
+        rm.E = c.n_experts;
+        if ((rc = cuda_rc(launch_router_mma(rm, st)))) return rc;
+    }
     if (logits_in && logits && logits != logits_in) {
         rc = cuda_rc(cudaMemcpyAsync(logits, logits_in, sizeof(float) * (size_t)T * c.n_experts,
                                      cudaMemcpyDeviceToDevice, st));

@@ -116,13 +116,13 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(RouteArgs a)
 
 // ---------------------------------------------------------------- top-k
 //
-// One warp per token (32 warps per block, 4 tokens per warp: a block owns
-// kTokBlock = 128 consecutive tokens).  Lane l holds logits e = l + 32 r.  A
-// logit maps to an order-preserving unsigned key (+0 and -0 map to the same
+// One warp per token, 8 tokens per block.  Lane l holds logits e = l + 32 r.
+// A logit maps to an order-preserving unsigned key (+0 and -0 map to the same
 // key); the pair (key, 0xFFFF - id) is maximised, so equal logits resolve to
 // the lower id.  k rounds of a warp max give the ids in rank order.  Weights
-// are computed in fp64 and rounded once to bf16.  The block also counts its
-// slots per expert into hist[block][E] for the stable scatter.
+// are computed in fp64 and rounded once to bf16 (fp64 is scarce on this GPU,
+// hence few tokens per block so the work spreads over every SM).  Each pick
+// is counted into the histogram row of its 128-token block (global atomics).
 __device__ __forceinline__ uint32_t logit_key(float f)
 {
     uint32_t u = __float_as_uint(f);
@@ -130,18 +130,14 @@ __device__ __forceinline__ uint32_t logit_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(1024) topk_kernel(TopkArgs a)
+__global__ void __launch_bounds__(256) topk_kernel(TopkArgs a)
 {
-    __shared__ int sh_hist[kMaxExperts];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.E, k = a.k;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) sh_hist[e] = 0;
-    __syncthreads();
-
     const int R = (E + 31) / 32;
-    for (int i = 0; i < kTokBlock / 32; ++i) {
-        const int t = blockIdx.x * kTokBlock + i * 32 + warp;
-        if (t >= a.T) break;
+    {
+        const int t = blockIdx.x * 8 + warp;
+        if (t >= a.T) return;
         const float *lrow = a.logits + (size_t)t * E;
         uint32_t key[kMaxExperts / 32];
         float val[kMaxExperts / 32];
@@ -194,7 +190,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(TopkArgs a)
         if (lane < k) {
             a.ids[(size_t)t * k + lane] = my_id;
             a.p[(size_t)t * k + lane] = double_to_bf16_bits(ex / den);
-            atomicAdd(&sh_hist[my_id], 1);
+            atomicAdd(a.hist + (size_t)(t / kTokBlock) * E + my_id, 1);
         }
         if (lane == 0 && a.w_s) {
             uint16_t ws = 0;
@@ -205,8 +201,6 @@ __global__ void __launch_bounds__(1024) topk_kernel(TopkArgs a)
             a.w_s[t] = ws;
         }
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) a.hist[(size_t)blockIdx.x * E + e] = sh_hist[e];
 }
 
 // Exclusive prefix sum of a[0..n) in place, by one full warp; returns the total.
@@ -406,7 +400,7 @@ cudaError_t launch_route_gemv(const RouteArgs &a, cudaStream_t st)
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t st)
 {
-    topk_kernel<<<(a.T + kTokBlock - 1) / kTokBlock, 1024, 0, st>>>(a);
+    topk_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

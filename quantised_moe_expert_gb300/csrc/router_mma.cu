@@ -1,0 +1,138 @@
+// Router GEMV of many tokens on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+//
+// The router is MLX affine 8-bit in groups of 64 (page "Qwen3.6-35B-A3B
+// (qwen3_5_moe) on the native Metal engine: proposal and gate", slice "The
+// family, plain decode": "the routers at 8 bits"), and the logits are fp32.
+// At prefill sizes the router is a small GEMM, [E x H] x [H x T]; with CUDA
+// cores it dominated the layer.  No weight is rounded here: an 8-bit code
+// q = 16 q_hi + q_lo is split into two nibbles, each made exact in bf16 as
+// 128 + nibble, and per group of 64 inputs
+//   sum_j w_j x_j = s (16 sum (128+q_hi) x + sum (128+q_lo) x - 2176 sum x) + b sum x
+// with sum x from an all-ones MMA chain; scale and bias apply in fp32.
+//
+// K order: a 32-bit word holds inputs 0..3 of a chunk; the bit operations
+// yield pairs (0,2) and (1,3), and the x fragment is permuted the same way.
+#include "kernels.cuh"
+
+namespace qmoe {
+namespace {
+
+constexpr int kRWarps = 8;                 // 8 warps x 16 experts per block
+constexpr int kRTok = 32;                  // tokens per block (4 n8 tiles)
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// grid (ceil(E/128), ceil(T/32)), 256 threads.  Warp w: experts e0 + 16 w .. +15, all 32 tokens.
+__global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaArgs a)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int H = a.H, E = a.E, T = a.T, G = H / kGroup;
+    const int ebase = blockIdx.x * (kRWarps * 16) + warp * 16;
+    const int tbase = blockIdx.y * kRTok;
+    if (ebase >= E) return;
+    const int r0 = min(ebase + g, E - 1), r1 = min(ebase + g + 8, E - 1);   // clamped rows are not stored
+    int tok[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tok[j] = tbase + j * 8 + g;
+
+    float acc[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+
+    for (int grp = 0; grp < G; ++grp) {
+        // 16 codes (bytes 16t..16t+15 of the group) of rows g and g+8
+        const uint4 c0 = __ldg(reinterpret_cast<const uint4 *>(a.codes + (size_t)r0 * H + grp * 64 + 16 * t));
+        const uint4 c1 = __ldg(reinterpret_cast<const uint4 *>(a.codes + (size_t)r1 * H + grp * 64 + 16 * t));
+        const float s0 = bf16_bits_to_float(__ldg(a.scales + (size_t)r0 * G + grp));
+        const float s1 = bf16_bits_to_float(__ldg(a.scales + (size_t)r1 * G + grp));
+        const float k0 = fmaf(-2176.f, s0, bf16_bits_to_float(__ldg(a.biases + (size_t)r0 * G + grp)));
+        const float k1 = fmaf(-2176.f, s1, bf16_bits_to_float(__ldg(a.biases + (size_t)r1 * G + grp)));
+        const uint32_t w0[4] = {c0.x, c0.y, c0.z, c0.w}, w1[4] = {c1.x, c1.y, c1.z, c1.w};
+        // lo / hi nibble pairs: word m -> {(0,2), (1,3)} of inputs 16t + 4m .. +3
+        uint32_t lo0[8], lo1[8], hi0[8], hi1[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            lo0[2 * m] = (w0[m] & 0x000F000Fu) | 0x43004300u;
+            lo0[2 * m + 1] = ((w0[m] >> 8) & 0x000F000Fu) | 0x43004300u;
+            hi0[2 * m] = ((w0[m] >> 4) & 0x000F000Fu) | 0x43004300u;
+            hi0[2 * m + 1] = ((w0[m] >> 12) & 0x000F000Fu) | 0x43004300u;
+            lo1[2 * m] = (w1[m] & 0x000F000Fu) | 0x43004300u;
+            lo1[2 * m + 1] = ((w1[m] >> 8) & 0x000F000Fu) | 0x43004300u;
+            hi1[2 * m] = ((w1[m] >> 4) & 0x000F000Fu) | 0x43004300u;
+            hi1[2 * m + 1] = ((w1[m] >> 12) & 0x000F000Fu) | 0x43004300u;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t b[8];
+            if (tok[j] < T) {
+                const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)tok[j] * H + grp * 64 + 16 * t);
+                const uint4 xa = __ldg(xp), xb = __ldg(xp + 1);
+                const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    b[2 * m] = prmt(xw[2 * m], xw[2 * m + 1], 0x5410u);       // inputs (0, 2)
+                    b[2 * m + 1] = prmt(xw[2 * m], xw[2 * m + 1], 0x7632u);   // inputs (1, 3)
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) b[q] = 0;
+            }
+            float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
+            constexpr uint32_t ones = 0x3F803F80u;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                mma_bf16(dl, lo0[2 * m], lo1[2 * m], lo0[2 * m + 1], lo1[2 * m + 1], b[2 * m], b[2 * m + 1]);
+                mma_bf16(dh, hi0[2 * m], hi1[2 * m], hi0[2 * m + 1], hi1[2 * m + 1], b[2 * m], b[2 * m + 1]);
+                mma_bf16(dx, ones, ones, ones, ones, b[2 * m], b[2 * m + 1]);
+            }
+            // rows: d[0], d[1] -> expert g; d[2], d[3] -> expert g+8
+            acc[j][0] = fmaf(s0, fmaf(16.f, dh[0], dl[0]), fmaf(k0, dx[0], acc[j][0]));
+            acc[j][1] = fmaf(s0, fmaf(16.f, dh[1], dl[1]), fmaf(k0, dx[1], acc[j][1]));
+            acc[j][2] = fmaf(s1, fmaf(16.f, dh[2], dl[2]), fmaf(k1, dx[2], acc[j][2]));
+            acc[j][3] = fmaf(s1, fmaf(16.f, dh[3], dl[3]), fmaf(k1, dx[3], acc[j][3]));
+        }
+    }
+    const int e0 = ebase + g, e1 = e0 + 8;
+    const float bias0 = (a.router_bias && e0 < E) ? __ldg(a.router_bias + e0) : 0.f;
+    const float bias1 = (a.router_bias && e1 < E) ? __ldg(a.router_bias + e1) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int tA = tbase + j * 8 + 2 * t, tB = tA + 1;
+        if (tA < T) {
+            if (e0 < E) a.logits[(size_t)tA * E + e0] = a.router_bias ? acc[j][0] + bias0 : acc[j][0];
+            if (e1 < E) a.logits[(size_t)tA * E + e1] = a.router_bias ? acc[j][2] + bias1 : acc[j][2];
+        }
+        if (tB < T) {
+            if (e0 < E) a.logits[(size_t)tB * E + e0] = a.router_bias ? acc[j][1] + bias0 : acc[j][1];
+            if (e1 < E) a.logits[(size_t)tB * E + e1] = a.router_bias ? acc[j][3] + bias1 : acc[j][3];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_router_mma(const RouterMmaArgs &a, cudaStream_t st)
+{
+    dim3 grid((a.E + kRWarps * 16 - 1) / (kRWarps * 16), (a.T + kRTok - 1) / kRTok);
+    router_mma_kernel<<<grid, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace qmoe
