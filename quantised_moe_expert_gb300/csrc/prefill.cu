@@ -46,9 +46,11 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 3;
-constexpr int kThreads = 192;        // warps 0-3 dequant + epilogue, warp 4 TMA, warp 5 MMA
-constexpr int kScaleChunk = 32;      // groups of scales staged in shared memory at a time
+constexpr int kStages = 3;          // A/B operand stages
+constexpr int kCodeStages1 = 6;     // code-tile stages, gate/up GEMM (8 KB each)
+constexpr int kCodeStages2 = 8;     // code-tile stages, down GEMM (4 KB each)
+constexpr int kThreads = 320;       // warps 0-3 dequant, 4 TMA, 5 MMA, 6-9 epilogue
+constexpr int kScaleChunk = 16;     // groups of scales staged in shared memory at a time
 constexpr long long kDrainLimit = 1ll << 22;
 
 struct G1Params {
@@ -118,7 +120,7 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *status)
     record_status(status, MOE_ERR_TIMEOUT);
 }
 
-// Stage one chunk of a row's scales and biases (groups [g0, g0 + 32)) into the
+// Stage one chunk of a row's scales and biases (groups [g0, g0 + kScaleChunk)) into the
 // thread-private columns of the shared staging arrays.
 __device__ __forceinline__ void stage_scales(uint16_t *dst, const uint16_t *const *src, int nsrc, int row_ok,
                                              size_t row_off, int G, int g0, int r)
@@ -130,61 +132,90 @@ __device__ __forceinline__ void stage_scales(uint16_t *dst, const uint16_t *cons
         }
 }
 
+// Named barrier of the four dequantising warps (threads 0..127).
+__device__ __forceinline__ void dequant_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named barrier `id` over `count` threads that also ORs a predicate: every
+// participant gets the same answer, so a group of warps stops together.
+__device__ __forceinline__ bool bar_any(int id, int count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Tile tau of a grouped GEMM: work item tau / MB, weight-row block tau % MB.
+struct TileInfo {
+    int expert, tok0, ntok, mb, pbase;
+    bool shared_e;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const WorkItem *work, const int32_t *offsets, int tau, int MB, int E,
+                                              int Tk)
+{
+    const WorkItem it = work[tau / MB];
+    TileInfo ti;
+    ti.expert = it.expert;
+    ti.tok0 = it.tok0;
+    ti.ntok = it.ntok;
+    ti.mb = tau % MB;
+    ti.shared_e = it.expert == E;
+    ti.pbase = ti.shared_e ? Tk + it.tok0 : __ldg(offsets + it.expert) + it.tok0;
+    return ti;
+}
+
 // --------------------------------------------------------------- gate/up GEMM
-template <int S>
+//
+// Persistent: one CTA per SM loops over tiles tau = blockIdx.x + i * gridDim.x.
+// Roles: warps 0-3 dequantise the code tiles and gather the token rows; warp 4
+// (one thread) streams code tiles with TMA through a ring of CS stages; warp 5
+// (one thread) issues the MMAs; warps 6-9 run the epilogue of the previous tile
+// from the other TMEM buffer while the next tile's MMAs accumulate.
+template <int S, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_gateup_kernel(const __grid_constant__ CUtensorMap map_gc, const __grid_constant__ CUtensorMap map_uc,
                        const __grid_constant__ CUtensorMap map_sgc, const __grid_constant__ CUtensorMap map_suc,
                        const G1Params P)
 {
-    if ((int)blockIdx.y >= __ldg(P.nwork + 1)) return;
+    const int H = P.H, I = P.I, G = H / kGroup, nk = G, MB = (I + 127) / 128, Tk = P.T * P.k;
+    const int ntiles = __ldg(P.nwork + 1) * MB;
+    if ((int)blockIdx.x >= ntiles) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA_g = smem;                         // S x 16 KB
     uint8_t *sA_u = sA_g + S * 16384;             // S x 16 KB
-    uint8_t *sB = sA_u + S * 16384;               // S x 16 KB (128 rows x 128 B)
-    uint8_t *sC = sB + S * 16384;                 // S x 8 KB (gate codes 4 KB | up codes 4 KB)
-    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + S * 8192);   // [4][32][128]
+    uint8_t *sB = sA_u + S * 16384;               // S x 16 KB (128 token rows x 128 B)
+    uint8_t *sC = sB + S * 16384;                 // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
+    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [4][kScaleChunk][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 4 * kScaleChunk * 128);
-    uint64_t *full = bars, *afull = bars + S, *empty = bars + 2 * S, *accf = bars + 3 * S, *drain = accf + 1;
-    int *s_rows = reinterpret_cast<int *>(drain + 1);     // [128]
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_rows + 128);
+    uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *empty = afull + S;
+    uint64_t *tfull = empty + S, *tempty = tfull + 2, *drain = tempty + 2;
+    int *s_rows = reinterpret_cast<int *>(drain + 1);     // [2][128]
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_rows + 256);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const WorkItem it = P.work[blockIdx.y];
-    const bool shared_e = it.expert == P.E;
-    const int i0 = blockIdx.x * 128;
-    const int ntok = it.ntok;
-    const int N = (ntok + 15) & ~15;
-    const int H = P.H, I = P.I, G = H / kGroup, nk = G;
-    const int pbase = shared_e ? P.T * P.k + it.tok0 : __ldg(P.offsets + it.expert) + it.tok0;
-
-    if (tid < 128) {
-        int row = 0;                              // rows past ntok are never read
-        if (tid < ntok) {
-            if (shared_e) {
-                row = it.tok0 + tid;
-            } else {
-                const int pos = pbase + tid;
-                const int f = (pos >= 0 && pos < P.T * P.k) ? __ldg(P.perm + pos) : -1;
-                if (f < 0 || f >= P.T * P.k) record_status(P.status, MOE_ERR_DEVICE);
-                else row = f / P.k;
-            }
-        }
-        s_rows[tid] = row;
-    }
     if (warp == 5) {
-        tmem_alloc(smem_u32(s_tmem), 256);
+        tmem_alloc(smem_u32(s_tmem), 512);
         tmem_relinquish();
     }
     if (tid == 0) {
+        for (int s = 0; s < CS; ++s) {
+            mbar_init(smem_u32(cfull + s), 1);
+            mbar_init(smem_u32(cempty + s), 128);
+        }
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(full + s), 1);
             mbar_init(smem_u32(afull + s), 128);
             mbar_init(smem_u32(empty + s), 1);
         }
-        mbar_init(smem_u32(accf), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(tfull + b), 1);
+            mbar_init(smem_u32(tempty + b), 128);
+        }
         mbar_init(smem_u32(drain), 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -196,223 +227,265 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long limit = P.wait_limit;
 
     if (warp == 4) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ code tiles (TMA)
         if (lane == 0) {
-            const CUtensorMap *mg = shared_e ? &map_sgc : &map_gc;
-            const CUtensorMap *mu = shared_e ? &map_suc : &map_uc;
-            prefetch_map(mg);
-            prefetch_map(mu);
-            const int wrow = (shared_e ? 0 : it.expert * I) + i0;
-            const uint32_t bytes = 8192;
-            int issued = 0;
-            for (int s = 0; s < nk; ++s) {
-                const int st = s % S, rnd = s / S;
-                if (s >= S && !mbar_wait(smem_u32(empty + st), (rnd - 1) & 1, limit, s_abort)) {
-                    set_abort(s_abort, P.status);
-                    break;
+            prefetch_map(&map_gc);
+            prefetch_map(&map_uc);
+            prefetch_map(&map_sgc);
+            prefetch_map(&map_suc);
+            int q = 0;
+            bool ok = true;
+            for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
+                const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+                const CUtensorMap *mg = ti.shared_e ? &map_sgc : &map_gc;
+                const CUtensorMap *mu = ti.shared_e ? &map_suc : &map_uc;
+                const int wrow = (ti.shared_e ? 0 : ti.expert * I) + ti.mb * 128;
+                for (int s = 0; s < nk; ++s, ++q) {
+                    const int cs = q % CS;
+                    if (q >= CS && !mbar_wait(smem_u32(cempty + cs), (q / CS - 1) & 1, limit, s_abort)) {
+                        set_abort(s_abort, P.status);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(cfull + cs);
+                    mbar_arrive_expect_tx(fb, 8192);
+                    tma_load_2d(smem_u32(sC + cs * 8192), mg, s * 32, wrow, fb);
+                    tma_load_2d(smem_u32(sC + cs * 8192 + 4096), mu, s * 32, wrow, fb);
                 }
-                const uint32_t fb = smem_u32(full + st);
-                mbar_arrive_expect_tx(fb, bytes);
-                tma_load_2d(smem_u32(sC + st * 8192), mg, s * 32, wrow, fb);
-                tma_load_2d(smem_u32(sC + st * 8192 + 4096), mu, s * 32, wrow, fb);
-                issued = s + 1;
             }
-            if (*s_abort) {
-                // drain: every issued stage's copies must land before the CTA exits
-                for (int s = (issued > S ? issued - S : 0); s < issued; ++s)
-                    mbar_wait(smem_u32(full + s % S), (s / S) & 1, kDrainLimit, nullptr);
-            }
+            if (!ok || *s_abort)   // every issued copy lands before the CTA exits
+                for (int d = (q > CS ? q - CS : 0); d < q; ++d)
+                    mbar_wait(smem_u32(cfull + d % CS), (d / CS) & 1, kDrainLimit, nullptr);
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_m128((uint32_t)N);
+            int q = 0, i = 0;
             bool ok = true;
-            for (int s = 0; s < nk && ok; ++s) {
-                const int st = s % S, rnd = s / S;
-                if (!mbar_wait(smem_u32(afull + st), rnd & 1, limit, s_abort)) {
+            for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x, ++i) {
+                const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+                const int N = (ti.ntok + 15) & ~15;
+                const uint32_t idesc = idesc_f16_m128((uint32_t)N);
+                const int buf = i & 1;
+                if (i >= 2 && !mbar_wait(smem_u32(tempty + buf), ((i >> 1) - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ag = smem_u32(sA_g + st * 16384), au = smem_u32(sA_u + st * 16384);
-                const uint32_t bb = smem_u32(sB + st * 16384);
+                const uint32_t d0 = tmem + (uint32_t)buf * 256;
+                for (int s = 0; s < nk; ++s, ++q) {
+                    const int st = q % S;
+                    if (!mbar_wait(smem_u32(afull + st), (q / S) & 1, limit, s_abort)) {
+                        set_abort(s_abort, P.status);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ag = smem_u32(sA_g + st * 16384), au = smem_u32(sA_u + st * 16384);
+                    const uint32_t bb = smem_u32(sB + st * 16384);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t acc = (s | kk) != 0;
-                    mma_f16(tmem, desc_sw128(ag + kk * 32), desc_sw128(bb + kk * 32), idesc, acc);
-                    mma_f16(tmem + 128, desc_sw128(au + kk * 32), desc_sw128(bb + kk * 32), idesc, acc);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t acc = (s | kk) != 0;
+                        mma_f16(d0, desc_sw128(ag + kk * 32), desc_sw128(bb + kk * 32), idesc, acc);
+                        mma_f16(d0 + 128, desc_sw128(au + kk * 32), desc_sw128(bb + kk * 32), idesc, acc);
+                    }
+                    mma_commit(smem_u32(empty + st));
                 }
-                mma_commit(smem_u32(empty + st));
+                if (ok) mma_commit(smem_u32(tfull + buf));
             }
-            if (ok) mma_commit(smem_u32(accf));
-            // every MMA this thread issued completes before TMEM is freed, on every path
-            mma_commit(smem_u32(drain));
+            mma_commit(smem_u32(drain));   // every issued MMA completes before TMEM is freed
             mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------ dequant (thread = weight row) + token rows
         const int r = tid;
-        const int row = i0 + r;
-        const bool row_ok = row < I;
-        const size_t soff = (size_t)(shared_e ? 0 : it.expert) * I * G + (size_t)row * G;
-        const uint16_t *srcs[4] = {shared_e ? P.sgs : P.gs, shared_e ? P.sgb : P.gb, shared_e ? P.sus : P.us,
-                                   shared_e ? P.sub : P.ub};
-        // token rows: thread copies 16-byte chunk (tid & 7) of tile rows (tid >> 3) + 16 i
         const int bchunk = tid & 7, brow0 = tid >> 3;
-        auto issue_b = [&](int ks) {
-            uint8_t *dst = sB + (ks % S) * 16384;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int n = brow0 + 16 * i;
-                if (n < ntok) {
-                    const uint16_t *src = P.x16 + (size_t)s_rows[n] * H + ks * 64 + bchunk * 8;
-                    cp_async16(smem_u32(dst + swz128(n, bchunk)), src);
-                }
-            }
-            cp_async_commit();
-        };
+        int q = 0, i = 0;
         bool ok = true;
-        issue_b(0);
-        for (int s = 0; s < nk; ++s) {
-            const int st = s % S, rnd = s / S;
-            if (s % kScaleChunk == 0) stage_scales(sScale, srcs, 4, row_ok, soff, G, s, r);
-            if (s + 1 < nk) {
-                const int sn = s + 1;
-                if (sn >= S && !mbar_wait(smem_u32(empty + sn % S), (sn / S - 1) & 1, limit, s_abort)) {
+        for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
+            const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+            const int par = i & 1;
+            int *rows = s_rows + par * 128;
+            {
+                int row = 0;                          // rows past ntok are never read
+                if (tid < ti.ntok) {
+                    if (ti.shared_e) {
+                        row = ti.tok0 + tid;
+                    } else {
+                        const int pos = ti.pbase + tid;
+                        const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                        if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
+                        else row = f / P.k;
+                    }
+                }
+                rows[tid] = row;
+            }
+            dequant_bar();
+            const int row = ti.mb * 128 + r;
+            const bool row_ok = row < I;
+            const int ee = ti.shared_e ? 0 : ti.expert;
+            const size_t soff = (size_t)ee * I * G + (size_t)row * G;
+            const uint16_t *srcs[4] = {ti.shared_e ? P.sgs : P.gs, ti.shared_e ? P.sgb : P.gb,
+                                       ti.shared_e ? P.sus : P.us, ti.shared_e ? P.sub : P.ub};
+            auto issue_b = [&](int ks, int st) {
+                uint8_t *dst = sB + st * 16384;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int n = brow0 + 16 * j;
+                    if (n < ti.ntok) {
+                        const uint16_t *src = P.x16 + (size_t)rows[n] * H + ks * 64 + bchunk * 8;
+                        cp_async16(smem_u32(dst + swz128(n, bchunk)), src);
+                    }
+                }
+                cp_async_commit();
+            };
+            // stage of step q must be free (MMA of step q - S done) before its B and A are written
+            if (q >= S && !mbar_wait(smem_u32(empty + q % S), (q / S - 1) & 1, limit, s_abort)) {
+                set_abort(s_abort, P.status);
+                ok = false;
+            }
+            if (ok) issue_b(0, q % S);
+            for (int s = 0; s < nk && ok; ++s, ++q) {
+                const int st = q % S;
+                if (s % kScaleChunk == 0) stage_scales(sScale, srcs, 4, row_ok, soff, G, s, r);
+                if (s + 1 < nk) {
+                    const int qn = q + 1;
+                    if (qn >= S && !mbar_wait(smem_u32(empty + qn % S), (qn / S - 1) & 1, limit, s_abort)) {
+                        set_abort(s_abort, P.status);
+                        ok = false;
+                        break;
+                    }
+                    issue_b(s + 1, qn % S);
+                } else {
+                    cp_async_commit();
+                }
+                const int cs = q % CS;
+                if (!mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
                 }
-                issue_b(sn);
-            } else {
-                cp_async_commit();
-            }
-            if (!mbar_wait(smem_u32(full + st), rnd & 1, limit, s_abort)) {
-                set_abort(s_abort, P.status);
-                ok = false;
-                break;
-            }
-            const int gi = s % kScaleChunk;
-            const __half2 sg = bf16_to_h2(sScale[(0 * kScaleChunk + gi) * 128 + r]);
-            const __half2 bg = bf16_to_h2(sScale[(1 * kScaleChunk + gi) * 128 + r]);
-            const __half2 su = bf16_to_h2(sScale[(2 * kScaleChunk + gi) * 128 + r]);
-            const __half2 bu = bf16_to_h2(sScale[(3 * kScaleChunk + gi) * 128 + r]);
-            const uint4 *cg = reinterpret_cast<const uint4 *>(sC + st * 8192 + r * 32);
-            const uint4 *cu = reinterpret_cast<const uint4 *>(sC + st * 8192 + 4096 + r * 32);
-            const uint4 g0 = cg[0], g1 = cg[1], u0 = cu[0], u1 = cu[1];
-            const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-            uint8_t *ag = sA_g + st * 16384;
-            uint8_t *au = sA_u + st * 16384;
+                const int gi = s % kScaleChunk;
+                const __half2 sg = bf16_to_h2(sScale[(0 * kScaleChunk + gi) * 128 + r]);
+                const __half2 bg = bf16_to_h2(sScale[(1 * kScaleChunk + gi) * 128 + r]);
+                const __half2 su = bf16_to_h2(sScale[(2 * kScaleChunk + gi) * 128 + r]);
+                const __half2 bu = bf16_to_h2(sScale[(3 * kScaleChunk + gi) * 128 + r]);
+                const uint4 *cg = reinterpret_cast<const uint4 *>(sC + cs * 8192 + r * 32);
+                const uint4 *cu = reinterpret_cast<const uint4 *>(sC + cs * 8192 + 4096 + r * 32);
+                const uint4 g0 = cg[0], g1 = cg[1], u0 = cu[0], u1 = cu[1];
+                const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                mbar_arrive(smem_u32(cempty + cs));          // the code words are in registers
+                uint8_t *ag = sA_g + st * 16384;
+                uint8_t *au = sA_u + st * 16384;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                *reinterpret_cast<uint4 *>(ag + swz128(r, c)) = dequant8(gw[c], sg, bg);
-                *reinterpret_cast<uint4 *>(au + swz128(r, c)) = dequant8(uw[c], su, bu);
+                for (int c = 0; c < 8; ++c) {
+                    *reinterpret_cast<uint4 *>(ag + swz128(r, c)) = dequant8(gw[c], sg, bg);
+                    *reinterpret_cast<uint4 *>(au + swz128(r, c)) = dequant8(uw[c], su, bu);
+                }
+                cp_async_wait_1();               // this K-step's token rows have landed
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(afull + st));
             }
-            cp_async_wait_1();               // this K-step's token rows have landed
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(afull + st));
+            cp_async_wait_all();
+            if (bar_any(1, 128, !ok || *s_abort)) break;     // the four warps stop together
         }
         cp_async_wait_all();
+    } else {
         // ------------------------------------------------ epilogue: h = silu(g) * u
-        if (ok && mbar_wait(smem_u32(accf), 0, limit, s_abort)) {
+        const int quad = warp & 3;                        // TMEM lanes 32 quad .. 32 quad + 31
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        int i = 0;
+        for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
+            const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+            const int N = (ti.ntok + 15) & ~15;
+            const int buf = i & 1;
+            bool got = mbar_wait(smem_u32(tfull + buf), (i >> 1) & 1, limit, s_abort);
+            got = __all_sync(0xffffffffu, got);              // tcgen05.ld needs the whole warp
+            if (!got) {
+                set_abort(s_abort, P.status);
+                break;
+            }
             tc_fence_after();
-            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-            const int erow = i0 + warp * 32 + lane;
+            const int erow = ti.mb * 128 + quad * 32 + lane;
             const int hcol = kperm_pos(erow);
+            const uint32_t d0 = tmem + lane_base + (uint32_t)buf * 256;
             for (int n0 = 0; n0 < N; n0 += 16) {
                 uint32_t gv[16], uv[16];
-                tmem_ld16(tmem + lane_base + n0, gv);
-                tmem_ld16(tmem + lane_base + 128 + n0, uv);
+                tmem_ld16(d0 + n0, gv);
+                tmem_ld16(d0 + 128 + n0, uv);
                 tmem_ld_wait();
                 if (erow < I) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int n = n0 + j;
-                        if (n < ntok) {
+                        if (n < ti.ntok) {
                             const float g = __uint_as_float(gv[j]), u = __uint_as_float(uv[j]);
                             const float hv = g / (1.f + __expf(-g)) * u;
-                            P.hs[(size_t)(pbase + n) * I + hcol] = __half_as_ushort(__float2half_rn(hv));
+                            P.hs[(size_t)(ti.pbase + n) * I + hcol] = __half_as_ushort(__float2half_rn(hv));
                         }
                     }
                 }
             }
-        } else if (ok) {
-            set_abort(s_abort, P.status);
+            tc_fence_before();
+            mbar_arrive(smem_u32(tempty + buf));
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 5) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
 // --------------------------------------------------------------- down GEMM
-template <int S>
+//
+// Same structure; the token operand is the h tile of the expert's rows (TMA,
+// issued by dequant thread 0 once the stage is free), and the epilogue adds
+// p * y into the fp32 layer accumulator.
+template <int S, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_down_kernel(const __grid_constant__ CUtensorMap map_dc, const __grid_constant__ CUtensorMap map_sdc,
                      const __grid_constant__ CUtensorMap map_h, const G2Params P)
 {
-    if ((int)blockIdx.y >= __ldg(P.nwork + 2)) return;
+    const int H = P.H, I = P.I, GI = I / kGroup, nk = GI, MB = (H + 127) / 128, Tk = P.T * P.k;
+    const int ntiles = __ldg(P.nwork + 2) * MB;
+    if ((int)blockIdx.x >= ntiles) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;                           // S x 16 KB
     uint8_t *sB = sA + S * 16384;                 // S x 32 KB (256 rows x 128 B)
-    uint8_t *sC = sB + S * 32768;                 // S x 4 KB
-    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + S * 4096);   // [2][32][128]
+    uint8_t *sC = sB + S * 32768;                 // CS x 4 KB
+    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 4096);   // [2][kScaleChunk][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 2 * kScaleChunk * 128);
-    uint64_t *full = bars, *afull = bars + S, *empty = bars + 2 * S, *accf = bars + 3 * S, *drain = accf + 1;
-    int *s_tok = reinterpret_cast<int *>(drain + 1);           // [256]
-    float *s_w = reinterpret_cast<float *>(s_tok + 256);       // [256]
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_w + 256);
+    uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *bfull = afull + S, *empty = bfull + S;
+    uint64_t *tfull = empty + S, *tempty = tfull + 2, *drain = tempty + 2;
+    int *s_tok = reinterpret_cast<int *>(drain + 1);           // [2][256]
+    float *s_w = reinterpret_cast<float *>(s_tok + 512);       // [2][256]
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_w + 512);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const WorkItem it = P.work[blockIdx.y];
-    const bool shared_e = it.expert == P.E;
-    const int h0 = blockIdx.x * 128;
-    const int ntok = it.ntok;
-    const int N = (ntok + 15) & ~15;
-    const int nbox = (N + 31) / 32;
-    const int H = P.H, I = P.I, GI = I / kGroup, nk = GI;
-    const int pbase = shared_e ? P.T * P.k + it.tok0 : __ldg(P.offsets + it.expert) + it.tok0;
-
-    for (int n = tid; n < 256; n += blockDim.x) {
-        int t = -1;
-        float wgt = 0.f;
-        if (n < ntok) {
-            if (shared_e) {
-                t = it.tok0 + n;
-                wgt = bf16_bits_to_float(P.w_s[t]);
-            } else {
-                const int pos = pbase + n;
-                const int f = (pos >= 0 && pos < P.T * P.k) ? __ldg(P.perm + pos) : -1;
-                if (f < 0 || f >= P.T * P.k) {
-                    record_status(P.status, MOE_ERR_DEVICE);
-                } else {
-                    t = f / P.k;
-                    wgt = bf16_bits_to_float(P.p[f]);
-                }
-            }
-        }
-        s_tok[n] = t;
-        s_w[n] = wgt;
-    }
     if (warp == 5) {
-        tmem_alloc(smem_u32(s_tmem), 256);
+        tmem_alloc(smem_u32(s_tmem), 512);
         tmem_relinquish();
     }
     if (tid == 0) {
+        for (int s = 0; s < CS; ++s) {
+            mbar_init(smem_u32(cfull + s), 1);
+            mbar_init(smem_u32(cempty + s), 128);
+        }
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(full + s), 1);
             mbar_init(smem_u32(afull + s), 128);
+            mbar_init(smem_u32(bfull + s), 1);
             mbar_init(smem_u32(empty + s), 1);
         }
-        mbar_init(smem_u32(accf), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(tfull + b), 1);
+            mbar_init(smem_u32(tempty + b), 128);
+        }
         mbar_init(smem_u32(drain), 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -425,107 +498,183 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 4) {
         if (lane == 0) {
-            const CUtensorMap *md = shared_e ? &map_sdc : &map_dc;
-            prefetch_map(md);
-            prefetch_map(&map_h);
-            const int wrow = (shared_e ? 0 : it.expert * H) + h0;
-            const uint32_t bytes = 4096 + (uint32_t)nbox * 32 * 128;
-            int issued = 0;
-            for (int s = 0; s < nk; ++s) {
-                const int st = s % S, rnd = s / S;
-                if (s >= S && !mbar_wait(smem_u32(empty + st), (rnd - 1) & 1, limit, s_abort)) {
-                    set_abort(s_abort, P.status);
-                    break;
+            prefetch_map(&map_dc);
+            prefetch_map(&map_sdc);
+            int q = 0;
+            bool ok = true;
+            for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
+                const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+                const CUtensorMap *md = ti.shared_e ? &map_sdc : &map_dc;
+                const int wrow = (ti.shared_e ? 0 : ti.expert * H) + ti.mb * 128;
+                for (int s = 0; s < nk; ++s, ++q) {
+                    const int cs = q % CS;
+                    if (q >= CS && !mbar_wait(smem_u32(cempty + cs), (q / CS - 1) & 1, limit, s_abort)) {
+                        set_abort(s_abort, P.status);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(cfull + cs);
+                    mbar_arrive_expect_tx(fb, 4096);
+                    tma_load_2d(smem_u32(sC + cs * 4096), md, s * 32, wrow, fb);
                 }
-                const uint32_t fb = smem_u32(full + st);
-                mbar_arrive_expect_tx(fb, bytes);
-                tma_load_2d(smem_u32(sC + st * 4096), md, s * 32, wrow, fb);
-                for (int q = 0; q < nbox; ++q)
-                    tma_load_2d(smem_u32(sB + st * 32768 + q * 4096), &map_h, s * 64, pbase + q * 32, fb);
-                issued = s + 1;
             }
-            if (*s_abort)
-                for (int s = (issued > S ? issued - S : 0); s < issued; ++s)
-                    mbar_wait(smem_u32(full + s % S), (s / S) & 1, kDrainLimit, nullptr);
+            if (!ok || *s_abort)
+                for (int d = (q > CS ? q - CS : 0); d < q; ++d)
+                    mbar_wait(smem_u32(cfull + d % CS), (d / CS) & 1, kDrainLimit, nullptr);
         }
     } else if (warp == 5) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_m128((uint32_t)N);
+            int q = 0, i = 0;
             bool ok = true;
-            for (int s = 0; s < nk; ++s) {
-                const int st = s % S, rnd = s / S;
-                if (!mbar_wait(smem_u32(full + st), rnd & 1, limit, s_abort) ||
-                    !mbar_wait(smem_u32(afull + st), rnd & 1, limit, s_abort)) {
+            for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x, ++i) {
+                const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+                const int N = (ti.ntok + 15) & ~15;
+                const uint32_t idesc = idesc_f16_m128((uint32_t)N);
+                const int buf = i & 1;
+                if (i >= 2 && !mbar_wait(smem_u32(tempty + buf), ((i >> 1) - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t aa = smem_u32(sA + st * 16384), bb = smem_u32(sB + st * 32768);
+                const uint32_t d0 = tmem + (uint32_t)buf * 256;
+                for (int s = 0; s < nk; ++s, ++q) {
+                    const int st = q % S;
+                    if (!mbar_wait(smem_u32(bfull + st), (q / S) & 1, limit, s_abort) ||
+                        !mbar_wait(smem_u32(afull + st), (q / S) & 1, limit, s_abort)) {
+                        set_abort(s_abort, P.status);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t aa = smem_u32(sA + st * 16384), bb = smem_u32(sB + st * 32768);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(tmem, desc_sw128(aa + kk * 32), desc_sw128(bb + kk * 32), idesc, (s | kk) != 0);
-                mma_commit(smem_u32(empty + st));
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(d0, desc_sw128(aa + kk * 32), desc_sw128(bb + kk * 32), idesc, (s | kk) != 0);
+                    mma_commit(smem_u32(empty + st));
+                }
+                if (ok) mma_commit(smem_u32(tfull + buf));
             }
-            if (ok) mma_commit(smem_u32(accf));
-            // every MMA this thread issued completes before TMEM is freed, on every path
             mma_commit(smem_u32(drain));
             mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
-    } else {
+    } else if (warp < 4) {
         const int r = tid;
-        const int row = h0 + r;
-        const bool row_ok = row < H;
-        const size_t soff = (size_t)(shared_e ? 0 : it.expert) * H * GI + (size_t)row * GI;
-        const uint16_t *srcs[2] = {shared_e ? P.sds : P.ds, shared_e ? P.sdb : P.db};
+        int q = 0;
         bool ok = true;
-        for (int s = 0; s < nk; ++s) {
-            const int st = s % S, rnd = s / S;
-            if (s % kScaleChunk == 0) stage_scales(sScale, srcs, 2, row_ok, soff, GI, s, r);
-            if (!mbar_wait(smem_u32(full + st), rnd & 1, limit, s_abort)) {
-                set_abort(s_abort, P.status);
-                ok = false;
-                break;
-            }
-            const int gi = s % kScaleChunk;
-            const __half2 sd = bf16_to_h2(sScale[(0 * kScaleChunk + gi) * 128 + r]);
-            const __half2 bd = bf16_to_h2(sScale[(1 * kScaleChunk + gi) * 128 + r]);
-            const uint4 *cd = reinterpret_cast<const uint4 *>(sC + st * 4096 + r * 32);
-            const uint4 c0 = cd[0], c1 = cd[1];
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            uint8_t *aa = sA + st * 16384;
+        int b_issued = 0;                       // h-tile loads issued by thread 0 (for the drain)
+        for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
+            const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+            const int N = (ti.ntok + 15) & ~15;
+            const int nbox = (N + 31) / 32;
+            const int row = ti.mb * 128 + r;
+            const bool row_ok = row < H;
+            const int ee = ti.shared_e ? 0 : ti.expert;
+            const size_t soff = (size_t)ee * H * GI + (size_t)row * GI;
+            const uint16_t *srcs[2] = {ti.shared_e ? P.sds : P.ds, ti.shared_e ? P.sdb : P.db};
+            for (int s = 0; s < nk && ok; ++s, ++q) {
+                const int st = q % S;
+                if (s % kScaleChunk == 0) stage_scales(sScale, srcs, 2, row_ok, soff, GI, s, r);
+                if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
+                    set_abort(s_abort, P.status);
+                    ok = false;
+                    break;
+                }
+                if (tid == 0) {
+                    const uint32_t fb = smem_u32(bfull + st);
+                    mbar_arrive_expect_tx(fb, (uint32_t)nbox * 4096);
+                    for (int b = 0; b < nbox; ++b)
+                        tma_load_2d(smem_u32(sB + st * 32768 + b * 4096), &map_h, s * 64, ti.pbase + b * 32, fb);
+                    b_issued = q + 1;
+                }
+                const int cs = q % CS;
+                if (!mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort)) {
+                    set_abort(s_abort, P.status);
+                    ok = false;
+                    break;
+                }
+                const int gi = s % kScaleChunk;
+                const __half2 sd = bf16_to_h2(sScale[(0 * kScaleChunk + gi) * 128 + r]);
+                const __half2 bd = bf16_to_h2(sScale[(1 * kScaleChunk + gi) * 128 + r]);
+                const uint4 *cd = reinterpret_cast<const uint4 *>(sC + cs * 4096 + r * 32);
+                const uint4 c0 = cd[0], c1 = cd[1];
+                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                mbar_arrive(smem_u32(cempty + cs));
+                uint8_t *aa = sA + st * 16384;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(aa + swz128(r, c)) = dequant8(cw[c], sd, bd);
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(afull + st));
+                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(aa + swz128(r, c)) = dequant8(cw[c], sd, bd);
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(afull + st));
+            }
+            if (bar_any(1, 128, !ok || *s_abort)) break;     // the four warps stop together
         }
+        if (tid == 0 && (!ok || *s_abort))     // issued h tiles land before the CTA exits
+            for (int d = (b_issued > S ? b_issued - S : 0); d < b_issued; ++d)
+                mbar_wait(smem_u32(bfull + d % S), (d / S) & 1, kDrainLimit, nullptr);
+    } else {
         // ------------------------------------------------ epilogue: acc[t, row] += w * y
-        if (ok && mbar_wait(smem_u32(accf), 0, limit, s_abort)) {
+        const int quad = warp & 3;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        int i = 0;
+        for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
+            const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+            const int N = (ti.ntok + 15) & ~15;
+            const int buf = i & 1;
+            int *tok = s_tok + buf * 256;
+            float *wv = s_w + buf * 256;
+            // token and weight of each column (epilogue threads 192..319 fill them)
+            for (int n = tid - 192; n < 256; n += 128) {
+                int t = -1;
+                float wgt = 0.f;
+                if (n < ti.ntok) {
+                    if (ti.shared_e) {
+                        t = ti.tok0 + n;
+                        wgt = bf16_bits_to_float(P.w_s[t]);
+                    } else {
+                        const int pos = ti.pbase + n;
+                        const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                        if (f < 0 || f >= Tk) {
+                            record_status(P.status, MOE_ERR_DEVICE);
+                        } else {
+                            t = f / P.k;
+                            wgt = bf16_bits_to_float(P.p[f]);
+                        }
+                    }
+                }
+                tok[n] = t;
+                wv[n] = wgt;
+            }
+            if (bar_any(2, 128, *s_abort)) break;
+            bool got = mbar_wait(smem_u32(tfull + buf), (i >> 1) & 1, limit, s_abort);
+            got = __all_sync(0xffffffffu, got);              // tcgen05.ld needs the whole warp
+            if (!got) set_abort(s_abort, P.status);
+            if (bar_any(2, 128, !got)) break;                // the four warps stop together
             tc_fence_after();
-            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-            const int erow = h0 + warp * 32 + lane;
+            const int erow = ti.mb * 128 + quad * 32 + lane;
+            const uint32_t d0 = tmem + lane_base + (uint32_t)buf * 256;
             for (int n0 = 0; n0 < N; n0 += 16) {
                 uint32_t v[16];
-                tmem_ld16(tmem + lane_base + n0, v);
+                tmem_ld16(d0 + n0, v);
                 tmem_ld_wait();
                 if (erow < H) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int n = n0 + j;
-                        const int t = n < ntok ? s_tok[n] : -1;
-                        if (t >= 0) atomicAdd(P.acc + (size_t)t * H + erow, s_w[n] * __uint_as_float(v[j]));
+                        const int t = n < ti.ntok ? tok[n] : -1;
+                        if (t >= 0) atomicAdd(P.acc + (size_t)t * H + erow, wv[n] * __uint_as_float(v[j]));
                     }
                 }
             }
-        } else if (ok) {
-            set_abort(s_abort, P.status);
+            tc_fence_before();
+            mbar_arrive(smem_u32(tempty + buf));
+            if (bar_any(2, 128, *s_abort)) break;           // tok/wv of this buffer are reused two tiles later
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 5) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -581,8 +730,25 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t g1_smem() { return 1024 + kStages * (16384 * 3 + 8192) + 4 * kScaleChunk * 128 * 2 + 8 * (3 * kStages + 2) + 128 * 4 + 16; }
-size_t g2_smem() { return 1024 + kStages * (16384 + 32768 + 4096) + 2 * kScaleChunk * 128 * 2 + 8 * (3 * kStages + 2) + 512 * 4 + 16; }
+size_t g1_smem()
+{
+    return 1024 + kStages * 16384 * 3 + kCodeStages1 * 8192 + 4 * kScaleChunk * 128 * 2 +
+           8 * (2 * kCodeStages1 + 2 * kStages + 5) + 256 * 4 + 16;
+}
+size_t g2_smem()
+{
+    return 1024 + kStages * (16384 + 32768) + kCodeStages2 * 4096 + 2 * kScaleChunk * 128 * 2 +
+           8 * (2 * kCodeStages2 + 3 * kStages + 5) + 1024 * 4 + 16;
+}
+
+int sm_count()
+{
+    static int n[16] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!n[dev & 15]) cudaDeviceGetAttribute(&n[dev & 15], cudaDevAttrMultiProcessorCount, dev);
+    return n[dev & 15] > 0 ? n[dev & 15] : 1;
+}
 
 }  // namespace
 
@@ -643,8 +809,10 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p1.k = k;
     p1.wait_limit = a.wait_limit;
     const size_t s1 = g1_smem();
-    cudaFuncSetAttribute(gemm_gateup_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
-    gemm_gateup_kernel<kStages><<<dim3((I + 127) / 128, a.max_w1), kThreads, s1, st>>>(mgc, muc, msgc, msuc, p1);
+    auto k1 = gemm_gateup_kernel<kStages, kCodeStages1>;
+    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+    const int tiles1 = a.max_w1 * ((I + 127) / 128);
+    k1<<<std::min(sm_count(), tiles1), kThreads, s1, st>>>(mgc, muc, msgc, msuc, p1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     G2Params p2{};
@@ -667,8 +835,10 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p2.k = k;
     p2.wait_limit = a.wait_limit;
     const size_t s2 = g2_smem();
-    cudaFuncSetAttribute(gemm_down_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
-    gemm_down_kernel<kStages><<<dim3((H + 127) / 128, a.max_w2), kThreads, s2, st>>>(mdc, msdc, mh, p2);
+    auto k2 = gemm_down_kernel<kStages, kCodeStages2>;
+    cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+    const int tiles2 = a.max_w2 * ((H + 127) / 128);
+    k2<<<std::min(sm_count(), tiles2), kThreads, s2, st>>>(mdc, msdc, mh, p2);
     return cudaGetLastError();
 }
 

@@ -5,10 +5,14 @@
 // family, plain decode": "the routers at 8 bits"), and the logits are fp32.
 // At prefill sizes the router is a small GEMM, [E x H] x [H x T]; with CUDA
 // cores it dominated the layer.  No weight is rounded here: an 8-bit code
-// q = 16 q_hi + q_lo is split into two nibbles, each made exact in bf16 as
-// 128 + nibble, and per group of 64 inputs
-//   sum_j w_j x_j = s (16 sum (128+q_hi) x + sum (128+q_lo) x - 2176 sum x) + b sum x
-// with sum x from an all-ones MMA chain; scale and bias apply in fp32.
+// q = 16 q_hi + q_lo is split into two nibbles, each made an exact bf16
+// integer (OR into the mantissa of 128.0, then subtract 128 exactly), and per
+// group of 64 inputs
+//   sum_j w_j x_j = s (16 sum q_hi x + sum q_lo x) + b sum x
+// with sum x from an all-ones MMA chain; scale and bias apply in fp32.  (Keeping
+// the 128 offset inside the MMA sums would cancel ~4 bits of the fp32
+// accumulation afterwards; the logits must stay within ~1e-6 of the exact
+// sum so the top-k agrees with an exact router away from near-ties.)
 //
 // K order: a 32-bit word holds inputs 0..3 of a chunk; the bit operations
 // yield pairs (0,2) and (1,3), and the x fragment is permuted the same way.
@@ -28,6 +32,14 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16x2 (128 + n0, 128 + n1) -> (n0, n1), exact.
+__device__ __forceinline__ uint32_t sub128(uint32_t v)
+{
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&v);
+    h = __hsub2(h, __floats2bfloat162_rn(128.f, 128.f));
+    return *reinterpret_cast<uint32_t *>(&h);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
@@ -62,21 +74,21 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaArgs a)
         const uint4 c1 = __ldg(reinterpret_cast<const uint4 *>(a.codes + (size_t)r1 * H + grp * 64 + 16 * t));
         const float s0 = bf16_bits_to_float(__ldg(a.scales + (size_t)r0 * G + grp));
         const float s1 = bf16_bits_to_float(__ldg(a.scales + (size_t)r1 * G + grp));
-        const float k0 = fmaf(-2176.f, s0, bf16_bits_to_float(__ldg(a.biases + (size_t)r0 * G + grp)));
-        const float k1 = fmaf(-2176.f, s1, bf16_bits_to_float(__ldg(a.biases + (size_t)r1 * G + grp)));
+        const float k0 = bf16_bits_to_float(__ldg(a.biases + (size_t)r0 * G + grp));
+        const float k1 = bf16_bits_to_float(__ldg(a.biases + (size_t)r1 * G + grp));
         const uint32_t w0[4] = {c0.x, c0.y, c0.z, c0.w}, w1[4] = {c1.x, c1.y, c1.z, c1.w};
         // lo / hi nibble pairs: word m -> {(0,2), (1,3)} of inputs 16t + 4m .. +3
         uint32_t lo0[8], lo1[8], hi0[8], hi1[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            lo0[2 * m] = (w0[m] & 0x000F000Fu) | 0x43004300u;
-            lo0[2 * m + 1] = ((w0[m] >> 8) & 0x000F000Fu) | 0x43004300u;
-            hi0[2 * m] = ((w0[m] >> 4) & 0x000F000Fu) | 0x43004300u;
-            hi0[2 * m + 1] = ((w0[m] >> 12) & 0x000F000Fu) | 0x43004300u;
-            lo1[2 * m] = (w1[m] & 0x000F000Fu) | 0x43004300u;
-            lo1[2 * m + 1] = ((w1[m] >> 8) & 0x000F000Fu) | 0x43004300u;
-            hi1[2 * m] = ((w1[m] >> 4) & 0x000F000Fu) | 0x43004300u;
-            hi1[2 * m + 1] = ((w1[m] >> 12) & 0x000F000Fu) | 0x43004300u;
+            lo0[2 * m] = sub128((w0[m] & 0x000F000Fu) | 0x43004300u);
+            lo0[2 * m + 1] = sub128(((w0[m] >> 8) & 0x000F000Fu) | 0x43004300u);
+            hi0[2 * m] = sub128(((w0[m] >> 4) & 0x000F000Fu) | 0x43004300u);
+            hi0[2 * m + 1] = sub128(((w0[m] >> 12) & 0x000F000Fu) | 0x43004300u);
+            lo1[2 * m] = sub128((w1[m] & 0x000F000Fu) | 0x43004300u);
+            lo1[2 * m + 1] = sub128(((w1[m] >> 8) & 0x000F000Fu) | 0x43004300u);
+            hi1[2 * m] = sub128(((w1[m] >> 4) & 0x000F000Fu) | 0x43004300u);
+            hi1[2 * m + 1] = sub128(((w1[m] >> 12) & 0x000F000Fu) | 0x43004300u);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -61,6 +61,9 @@ def test_prefill_t512_sampled_rows():
     x = synth.make_x(wl.shape, wl.tokens, wl.seed)
     got = H.run_forward(layer, x, path=qm.MOE_PATH_AUTO)
     assert got["status"] == 0
+    r = H.run_route(layer, x)
+    ref_logits = oracle.router_logits(wl.shape, w, x)
+    assert np.abs(r["logits"].astype(np.float64) - ref_logits).max() <= H.LOGIT_TOL
     rows = np.random.default_rng(0).choice(wl.tokens, 24, replace=False)
     rows = np.concatenate([rows, [0, wl.tokens - 1]])
     _compare_rows(wl, w, x, got, rows)
@@ -77,8 +80,13 @@ def test_prefill_t4096_zipf_sampled_rows_and_full_routing():
     # every row's routing against the oracle's router and top-k
     ref_logits = oracle.router_logits(wl.shape, w, x, bias)
     ref_ids = oracle.topk(ref_logits, wl.shape.top_k)
+    r = H.run_route(layer, x, router_bias=bias)
+    err = np.abs(r["logits"].astype(np.float64) - ref_logits)
+    assert err.max() <= H.LOGIT_TOL, (err.max(), np.unravel_index(err.argmax(), err.shape))
+    assert np.array_equal(r["ids"], got["ids"])
     clear = H.oracle_gap(ref_logits, wl.shape.top_k) >= H.AMBIGUOUS_GAP
-    assert np.array_equal(got["ids"][clear], ref_ids[clear])
+    bad = np.nonzero(np.any(got["ids"] != ref_ids, axis=1) & clear)[0]
+    assert len(bad) == 0, (len(bad), bad[:8], err.max())
     counts = np.bincount(ref_ids.ravel(), minlength=wl.shape.n_experts)
     assert counts.max() > 8 * wl.tokens * wl.shape.top_k / wl.shape.n_experts   # the skew is real
 
