@@ -185,6 +185,25 @@ MOE_API int moe_forward(const moe_config *cfg, const moe_weights *w, const uint1
                 int32_t *ids_out, uint16_t *p_out, uint16_t *w_shared_out, int path,
                 void *ws, size_t ws_bytes, void *stream);
 
+/* The decode layer (T <= 16) for callers that cannot allocate device memory.
+ * The pages describe nothing like it: it exists for callers such as code that
+ * runs inside another engine's enqueue callback (that engine owns all device
+ * memory) or a process that must not allocate after start-up.
+ * Same arguments and results as moe_forward with MOE_PATH_DECODE, but no
+ * workspace: the scratch is a fixed 4 MiB array in the library's own device
+ * memory, held on every GPU that loads the library until the process exits.
+ * Layers whose decode scratch exceeds 4 MiB are refused with
+ * MOE_ERR_WORKSPACE; T outside 0..16 with MOE_ERR_INVALID_ARG.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array, which keeps the last call's
+ * contents: calls that overlap on the GPU (other streams, other threads)
+ * race and give wrong results, so keep them ordered.  Device-side status is
+ * recorded in the array and cannot be read back.  Allocates nothing. */
+MOE_API int moe_forward_decode_static(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T,
+                                      const float *router_bias, const float *logits_in, uint16_t *y,
+                                      int32_t *ids_out, uint16_t *p_out, uint16_t *w_shared_out, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of `ws`.
  * *device_status receives MOE_OK or the first error code a kernel recorded. */
 MOE_API int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_status);

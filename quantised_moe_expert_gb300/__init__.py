@@ -31,7 +31,8 @@ MOE_PATH_DECODE = 1
 MOE_PATH_PREFILL = 2
 
 EXPORTED = ("moe_status_string", "moe_check_config", "moe_workspace_size", "moe_route", "moe_permute",
-            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status", "moe_set_wait_limit")
+            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status", "moe_set_wait_limit",
+            "moe_forward_decode_static")
 
 
 class MoeError(RuntimeError):
@@ -91,6 +92,8 @@ def load(build: bool = True):
                                     _SZ, _VP]
         lib.moe_get_device_status.argtypes = [_VP, _SZ, _VP, P(ctypes.c_int)]
         lib.moe_set_wait_limit.argtypes = [ctypes.c_longlong]
+        lib.moe_forward_decode_static.argtypes = [P(moe_config), P(moe_weights), _VP, _I, _VP, _VP, _VP, _VP, _VP,
+                                                  _VP, _VP]
         for name in EXPORTED:
             if name != "moe_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -210,6 +213,19 @@ def moe_forward(cfg, w, x, T, router_bias, logits_in, y, ids_out, p_out, w_share
                             _ptr(y), _ptr(ids_out), _ptr(p_out), _ptr(w_shared_out), path, _ptr(ws),
                             ws.numel() * ws.element_size(), _stream(stream))
     _check("moe_forward", rc)
+
+
+def moe_forward_decode_static(cfg, w, x, T, router_bias, logits_in, y, ids_out, p_out, w_shared_out, stream=None):
+    """Decode layer (T <= 16) without a workspace, for callers that cannot allocate device memory.
+
+    The scratch is a fixed array inside libmoe.so's device memory, shared by
+    every call: keep calls ordered on the GPU (overlapping calls race).  The
+    first call on a device must come before any stream capture.
+    """
+    rc = load().moe_forward_decode_static(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), T, _ptr(router_bias),
+                                          _ptr(logits_in), _ptr(y), _ptr(ids_out), _ptr(p_out), _ptr(w_shared_out),
+                                          _stream(stream))
+    _check("moe_forward_decode_static", rc)
 
 
 def moe_get_device_status(ws, stream=None) -> int:
