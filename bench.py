@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0: enough to defeat L2)")
     ap.add_argument("--profile", action="store_true",
                     help="warm-up and timed steps only (for a profiler's launch list): no clocks, stage, e2e, "
                          "CPU baseline or sweep")
@@ -264,6 +265,8 @@ def run_ours(args, wl, rank, world, pg, steps, warmup, want_extras):
     act = synth.active_expert_bytes(sh) * (min(sh.n_experts, wl.tokens * sh.top_k) + 1)
     l2 = 129 * 2 ** 20
     copies = int(max(2, min(64, np.ceil(3 * l2 / max(act, 1)) + 1)))
+    if getattr(args, "copies", 0):
+        copies = args.copies
     W = Workload(wl, copies)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()

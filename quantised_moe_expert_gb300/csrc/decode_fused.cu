@@ -14,11 +14,11 @@
 //   phase 1  gate/up units (expert, 16 rows of I): split-K over the 8 warps,
 //            fixed-order reduction, h = silu(g) * u stored as fp16; each unit
 //            then increments its expert's counter;
-//   phase 2  down units (expert, 16 rows of H), one per warp, wait (bounded)
-//            for their expert's gate/up units, write the raw expert output per
-//            slot; the last unit of each 16-row block (a per-block counter)
-//            combines that block for every token in slot order and rounds once
-//            to bf16.
+//   phase 2  down units (expert, 128 rows of H), one per CTA, wait (one
+//            polling thread, bounded, with backoff) for their expert's gate/up
+//            units, write the raw expert output per slot; the last unit of each
+//            128-row block (a per-block counter) combines that block for every
+//            token in slot order and rounds once to bf16.
 // The GEMV arithmetic (exact codes on mma.sync, per-group scale in fp32) is
 // the one of the multi-kernel decode path; a token's result does not depend on
 // the other tokens of the batch.  Counters are zeroed by the router kernel that
@@ -31,6 +31,7 @@ namespace qmoe {
 namespace {
 
 constexpr int kFThreads = 256;
+constexpr int kCounterStride = 32;   // counters 128 bytes apart: pollers and writers do not share a line
 constexpr int kMaxList = kMaxExperts + 1;
 
 template <bool F16>
@@ -146,6 +147,25 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
     const int G = H / kGroup, GI = I / kGroup;
 
     // ---------------------------------------------------------------- phase 0: routing
+    if (a.ids_in) {
+        // routing given by the caller (the staged expert-FFN entry point)
+        for (int i = tid; i < T * k; i += kFThreads) {
+            const int tt = i / k, j = i - tt * k;
+            int e = a.ids_in[i];
+            if (e < 0 || e >= E) {
+                record_status(a.status, MOE_ERR_DEVICE);
+                e = 0;
+            }
+            S.ids[tt][j] = e;
+            S.pbits[tt][j] = a.p_in[i];
+            S.p[tt][j] = bf16_bits_to_float(a.p_in[i]);
+        }
+        for (int tt = tid; tt < T; tt += kFThreads) {
+            const uint16_t wsb = (a.has_shared && a.ws_in) ? a.ws_in[tt] : (uint16_t)0;
+            S.wsbits[tt] = wsb;
+            S.ws[tt] = bf16_bits_to_float(wsb);
+        }
+    } else
     for (int tt = warp; tt < T; tt += 8) {
         const float *lrow = a.logits + (size_t)tt * E;
         uint32_t key[kMaxExperts / 32];
@@ -205,7 +225,7 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
         }
     }
     __syncthreads();
-    if (blockIdx.x == 0) {
+    if (blockIdx.x == 0 && !a.ids_in) {
         for (int i = tid; i < T * k; i += kFThreads) {
             const int tt = i / k, j = i - tt * k;
             if (a.ids_out) a.ids_out[i] = S.ids[tt][j];
@@ -249,7 +269,10 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
         } else {
             for (int tt = 0; tt < T; ++tt)
                 for (int j = 0; j < k; ++j)
-                    if (S.ids[tt][j] == e) S.cols[d][n++] = tt * k + j;
+                    if (S.ids[tt][j] == e) {
+                        if (n < kDecodeMaxTok) S.cols[d][n++] = tt * k + j;
+                        else record_status(a.status, MOE_ERR_DEVICE);   // an id repeated within a token
+                    }
         }
         S.ncols[d] = n;
     }
@@ -384,15 +407,20 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
                 a.h[(size_t)S.cols[d][c] * I + rb * 16 + row] = __half_as_ushort(__float2half_rn(hv));
             }
         }
-        __threadfence();
         __syncthreads();
-        if (tid == 0) atomicAdd(a.cnt_expert + d, 1);
+        if (tid == 0) {
+            __threadfence();                 // cumulative: every h store of this unit is visible first
+            atomicAdd(a.cnt_expert + d * kCounterStride, 1);
+        }
     }
 
     // ---------------------------------------------------------------- phase 2: down units + combine
-    const int rb_h = H / 16;
+    // Unit = (expert d, 128-row block of H); warp w owns rows 16 w .. 16 w + 15 of it.
+    // Thread 0 alone waits (with backoff) for the expert's gate/up units.
+    const int rb_h = (H + 127) / 128;
     const int U2 = D * rb_h;
-    for (int v = blockIdx.x * 8 + warp; v < U2; v += gridDim.x * 8) {
+    __shared__ int s_ready;
+    for (int v = blockIdx.x; v < U2; v += gridDim.x) {
         const int d = v / rb_h, rb = v - d * rb_h;
         const int e = S.list[d];
         const bool shr = e == E;
@@ -400,16 +428,16 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
         const QMatDev &md = shr ? a.s_down : a.down;
         const uint8_t *cd = codes_of(md, ee, H, I);
         const size_t so = sb_off(ee, H, I);
-        const int r0 = rb * 16 + g, r1 = r0 + 8;
+        const int rbase = rb * 128 + warp * 16;
+        const bool wactive = rbase < H;
+        const int r0 = min(rbase + g, H - 1), r1 = min(rbase + g + 8, H - 1);
         const int ncol = S.ncols[d];
-        // load this unit's codes and scales before waiting for h
         constexpr int GBD = 8;
         float acc[NT][4];
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
-        bool ready = false;
         for (int gb = 0; gb < GI; gb += GBD) {
             uint2 c0[GBD], c1[GBD];
             uint16_t sv[GBD][2], bv[GBD][2];
@@ -426,17 +454,23 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
                     bv[i][1] = __ldg(md.biases + so + (size_t)r1 * GI + grp);
                 }
             }
-            if (!ready) {
-                long long n = 0;
-                while (ld_acquire(a.cnt_expert + d) < rb_i) {
-                    if (++n > a.wait_limit) break;
-                    __nanosleep(64);
+            if (gb == 0) {
+                // the codes above are in flight; now wait for this expert's h
+                if (tid == 0) {
+                    const int *cnt = a.cnt_expert + d * kCounterStride;
+                    long long n = 0;
+                    unsigned ns = 64;
+                    while (ld_acquire(cnt) < rb_i && n <= a.wait_limit) {
+                        ++n;
+                        __nanosleep(ns);
+                        ns = ns < 1024 ? ns * 2 : 1024;
+                    }
+                    const int ok = n <= a.wait_limit;
+                    if (!ok) record_status(a.status, MOE_ERR_TIMEOUT);
+                    s_ready = ok;
                 }
-                if (n > a.wait_limit) {
-                    record_status(a.status, MOE_ERR_TIMEOUT);
-                    break;
-                }
-                ready = true;
+                __syncthreads();
+                if (!s_ready) break;
             }
 #pragma unroll
             for (int i = 0; i < GBD; ++i) {
@@ -466,37 +500,49 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
                 }
             }
         }
-        if (!ready) continue;
+        if (!s_ready) {
+            __syncthreads();
+            continue;
+        }
+        if (wactive) {
+            const int w0 = rbase + g, w1 = w0 + 8;
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int cA = j * 8 + 2 * t4, cB = cA + 1;
-            if (cA < ncol) {
-                const int f = S.cols[d][cA];
-                a.yslot[(size_t)f * H + r0] = acc[j][0];
-                a.yslot[(size_t)f * H + r1] = acc[j][2];
-            }
-            if (cB < ncol) {
-                const int f = S.cols[d][cB];
-                a.yslot[(size_t)f * H + r0] = acc[j][1];
-                a.yslot[(size_t)f * H + r1] = acc[j][3];
+            for (int j = 0; j < NT; ++j) {
+                const int cA = j * 8 + 2 * t4, cB = cA + 1;
+                if (cA < ncol) {
+                    const int f = S.cols[d][cA];
+                    a.yslot[(size_t)f * H + w0] = acc[j][0];
+                    a.yslot[(size_t)f * H + w1] = acc[j][2];
+                }
+                if (cB < ncol) {
+                    const int f = S.cols[d][cB];
+                    a.yslot[(size_t)f * H + w0] = acc[j][1];
+                    a.yslot[(size_t)f * H + w1] = acc[j][3];
+                }
             }
         }
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(a.cnt_rows + rb, 1) == D - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
+        __syncthreads();
+        if (tid == 0) {
             __threadfence();
-            // y[t, rows of block rb] = bf16(sum_j p_j y_slot[t*k+j] + w_s y_slot[T*k+t]), slot order
-            for (int q = lane; q < 16 * T; q += 32) {
-                const int tt = q >> 4, row = rb * 16 + (q & 15);
+            s_ready = atomicAdd(a.cnt_rows + rb * kCounterStride, 1) == D - 1 ? 2 : 1;
+        }
+        __syncthreads();
+        if (s_ready == 2) {
+            __threadfence();
+            // last unit of this row block: y = bf16(sum_j p_j y_slot[t*k+j] + w_s y_slot[T*k+t]), slot order
+            const int nrow = min(128, H - rb * 128);
+            for (int q = tid; q < nrow * T; q += kFThreads) {
+                const int tt = q / nrow, row = rb * 128 + (q - tt * nrow);
                 float s = 0.f;
                 for (int j = 0; j < k; ++j) s = fmaf(S.p[tt][j], __ldcg(a.yslot + ((size_t)tt * k + j) * H + row), s);
                 if (a.has_shared) s = fmaf(S.ws[tt], __ldcg(a.yslot + ((size_t)T * k + tt) * H + row), s);
-                a.y[(size_t)tt * H + row] = float_to_bf16_bits(s);
+                if (a.y)
+                    a.y[(size_t)tt * H + row] = float_to_bf16_bits(s);
+                else
+                    a.acc[(size_t)tt * H + row] += s;
             }
         }
+        __syncthreads();
     }
 }
 

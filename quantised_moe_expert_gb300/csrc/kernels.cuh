@@ -67,6 +67,8 @@ struct WorklistArgs {
     int32_t *nwork;
     WorkItem *work_dec, *work_g1, *work_g2;
     int *status;
+    int *zero;                    // non-null: zero[0, nzero) (counters of the fused decode kernel)
+    int nzero;
     int T, E, has_shared;
     int max_items[3];
 };
@@ -125,16 +127,20 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st);
 struct FusedDecodeArgs {
     const uint16_t *x;            // bf16 [T, H]
     QMatDev gate, up, down, s_gate, s_up, s_down;
-    const float *logits;          // f32 [T, E]
+    const float *logits;          // f32 [T, E] (routing source unless ids_in is given)
     const float *gamma;           // f32 [T]
+    const int32_t *ids_in;        // [T, k] given routing (then p_in / ws_in too), or null
+    const uint16_t *p_in;         // bf16 [T, k]
+    const uint16_t *ws_in;        // bf16 [T] or null
     int32_t *ids_out;             // [T, k] or null
     uint16_t *p_out;              // bf16 [T, k] or null
     uint16_t *ws_out;             // bf16 [T] or null
     uint16_t *h;                  // fp16 [T*k + T, I], slot order
     float *yslot;                 // f32 [T*k + T, H]
-    uint16_t *y;                  // bf16 [T, H]
-    int *cnt_expert;              // [E + 1] gate/up units done, per expert-list entry (zeroed before launch)
-    int *cnt_rows;                // [H / 16] down units done, per 16-row block (zeroed before launch)
+    uint16_t *y;                  // bf16 [T, H] = bf16(sum), or null
+    float *acc;                   // f32 [T, H] += sum (when y is null)
+    int *cnt_expert;              // [(E + 1) * 32] gate/up units done per expert-list entry, stride 32 (zeroed before launch)
+    int *cnt_rows;                // [(H / 128) * 32] down units done per 128-row block, stride 32 (zeroed before launch)
     int *status;
     int T, H, I, E, k, has_shared;
     long long wait_limit;

@@ -231,6 +231,35 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     return cuda_rc(launch_prefill_experts(a, st));
 }
 
+// Arguments of the fused decode kernel common to both of its callers.
+FusedDecodeArgs fused_args(const moe_config &c, const moe_weights &w, const uint16_t *x, int T, const WsLayout &L,
+                           void *ws)
+{
+    FusedDecodeArgs fa{};
+    fa.x = x;
+    fa.gate = dev(w.gate);
+    fa.up = dev(w.up);
+    fa.down = dev(w.down);
+    if (c.has_shared) {
+        fa.s_gate = dev(w.s_gate);
+        fa.s_up = dev(w.s_up);
+        fa.s_down = dev(w.s_down);
+    }
+    fa.h = ws_at<uint16_t>(ws, L.h);
+    fa.yslot = ws_at<float>(ws, L.yslot);
+    fa.cnt_expert = ws_at<int>(ws, L.counters);
+    fa.cnt_rows = fa.cnt_expert + 32 * (c.n_experts + 1);
+    fa.status = ws_at<int>(ws, L.status);
+    fa.T = T;
+    fa.H = c.hidden;
+    fa.I = c.inter;
+    fa.E = c.n_experts;
+    fa.k = c.top_k;
+    fa.has_shared = c.has_shared;
+    fa.wait_limit = g_wait_limit.load();
+    return fa;
+}
+
 bool weights_ok(const moe_config &c, const moe_weights *w, bool need_router, bool need_experts)
 {
     if (!w) return false;
@@ -355,9 +384,23 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     wa.max_items[0] = L.max_wd;
     wa.max_items[1] = L.max_w1;
     wa.max_items[2] = L.max_w2;
+    const int rp = resolve_path(path, T);
+    const bool fused = rp == MOE_PATH_DECODE && T <= kDecodeMaxTok;
+    if (fused) {
+        wa.zero = ws_at<int>(ws, L.counters);
+        wa.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128);
+    }
     if ((rc = cuda_rc(launch_worklist(wa, st)))) return rc;
+    if (fused) {
+        FusedDecodeArgs fa = fused_args(*cfg, *w, x, T, L, ws);
+        fa.ids_in = ids;
+        fa.p_in = p;
+        fa.ws_in = w_shared;
+        fa.acc = acc;
+        return cuda_rc(launch_decode_fused(fa, st));
+    }
     ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_shared, offsets, perm, acc, L, ws);
-    if (resolve_path(path, T) == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, nullptr, st);
+    if (rp == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, nullptr, st);
     return enqueue_prefill_experts(*cfg, ea, L, ws, 0, st);
 }
 
@@ -392,36 +435,15 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
         float *lg = logits_in ? const_cast<float *>(logits_in) : ws_at<float>(ws, L.logits);
         RouteArgs ra = route_args(*cfg, *w, x, T, router_bias, logits_in, lg, L, ws);
         ra.zero = ws_at<int>(ws, L.counters);
-        ra.nzero = cfg->n_experts + 1 + cfg->hidden / 16;
+        ra.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128);
         if ((rc = cuda_rc(launch_route_gemv(ra, st)))) return rc;
-        FusedDecodeArgs fa{};
-        fa.x = x;
-        fa.gate = dev(w->gate);
-        fa.up = dev(w->up);
-        fa.down = dev(w->down);
-        if (cfg->has_shared) {
-            fa.s_gate = dev(w->s_gate);
-            fa.s_up = dev(w->s_up);
-            fa.s_down = dev(w->s_down);
-        }
+        FusedDecodeArgs fa = fused_args(*cfg, *w, x, T, L, ws);
         fa.logits = lg;
         fa.gamma = ra.gamma;
         fa.ids_out = ids_out;
         fa.p_out = p_out;
         fa.ws_out = w_shared_out;
-        fa.h = ws_at<uint16_t>(ws, L.h);
-        fa.yslot = ws_at<float>(ws, L.yslot);
         fa.y = y;
-        fa.cnt_expert = ra.zero;
-        fa.cnt_rows = ra.zero + cfg->n_experts + 1;
-        fa.status = ws_at<int>(ws, L.status);
-        fa.T = T;
-        fa.H = cfg->hidden;
-        fa.I = cfg->inter;
-        fa.E = cfg->n_experts;
-        fa.k = cfg->top_k;
-        fa.has_shared = cfg->has_shared;
-        fa.wait_limit = g_wait_limit.load();
         return cuda_rc(launch_decode_fused(fa, st));
     }
     int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.ids);

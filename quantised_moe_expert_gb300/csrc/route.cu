@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(256) worklist_kernel(WorklistArgs a)
 {
     __shared__ int s_cnt[kMaxExperts];
     if (threadIdx.x == 0) *a.status = 0;
+    for (int i = threadIdx.x; i < a.nzero; i += blockDim.x) a.zero[i] = 0;
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
         int c = a.counts[e];
         if (c < 0 || c > a.T) {
