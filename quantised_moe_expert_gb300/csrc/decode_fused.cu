@@ -6,11 +6,15 @@
 // a few microseconds of HBM time, so launch gaps and grid-wide barriers would
 // dominate.  This kernel therefore keeps the whole expert stage in one grid of
 // co-resident CTAs (cooperative launch) and replaces barriers by counters:
-//   phase 0  every CTA recomputes the top-k of the <= 16 tokens from the fp32
-//            logits (the same arithmetic as the top-k kernel, so the same bits)
-//            and builds the list of distinct experts (increasing id, shared
-//            expert last) with their token columns; it also asks L2 to
-//            prefetch its share of the selected experts' down matrices;
+//   phase 0  every CTA stages x in shared memory, recomputes the top-k ids of
+//            the <= 16 tokens from the fp32 logits (the same comparisons as the
+//            top-k kernel) and builds the list of distinct experts (increasing
+//            id, shared expert last) with their token columns; it also asks L2
+//            to prefetch its share of the selected experts' down matrices.  The
+//            pick weights and shared weight need fp64 (a long dependent chain
+//            on this GPU), so only the first ceil(T/8) CTAs compute them, one
+//            warp per token, publish them and skip phase 1; nothing but the
+//            final combine waits for them;
 //   phase 1  gate/up units (expert, 16 rows of I): split-K over the 8 warps,
 //            fixed-order reduction, h = silu(g) * u stored as fp16; each unit
 //            then increments its expert's counter;
@@ -119,6 +123,7 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
 
 struct Smem {
     int ids[kDecodeMaxTok][kMaxTopK];
+    float lg[kDecodeMaxTok][kMaxTopK];     // fp32 logit of each pick
     float p[kDecodeMaxTok][kMaxTopK];
     uint16_t pbits[kDecodeMaxTok][kMaxTopK];
     float ws[kDecodeMaxTok];
@@ -138,13 +143,21 @@ __device__ __forceinline__ const uint8_t *codes_of(const QMatDev &m, int e, int 
 __device__ __forceinline__ size_t sb_off(int e, int rows, int cols) { return (size_t)e * rows * (cols / kGroup); }
 
 // ------------------------------------------------------------------ kernel
-template <int NT>
+template <int NT, bool XS>
 __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeArgs a)
 {
     __shared__ Smem S;
+    extern __shared__ uint4 s_x[];         // XS: x rows [T][H/8 + 1] (one uint4 of padding per row)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k;
-    const int G = H / kGroup, GI = I / kGroup;
+    const int G = H / kGroup, GI = I / kGroup, rowu4 = H / 8 + 1;
+    // CTAs [0, npc) compute the fp64 pick weights (one warp per token) and skip phase 1
+    const int npc = a.ids_in ? 0 : (T + 7) / 8;
+    if (XS)
+        for (int i = tid; i < T * (H / 8); i += kFThreads) {
+            const int tt = i / (H / 8), col = i - tt * (H / 8);
+            s_x[tt * rowu4 + col] = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)tt * H) + col);
+        }
 
     // ---------------------------------------------------------------- phase 0: routing
     if (a.ids_in) {
@@ -204,35 +217,44 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
             if (j == 0) top_l = v;
             if (lane == j) { my_id = id; my_l = v; }
         }
-        double ex = 0.0;
-        if (lane < k) ex = exp((double)my_l - (double)top_l);
-        double den = 0.0;
-        for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);
+        (void)top_l;
         if (lane < k) {
-            const uint16_t pb = double_to_bf16_bits(ex / den);
             S.ids[tt][lane] = my_id;
-            S.pbits[tt][lane] = pb;
-            S.p[tt][lane] = bf16_bits_to_float(pb);
-        }
-        if (lane == 0) {
-            uint16_t wsb = 0;
-            if (a.has_shared) {
-                const float gb = bf16_bits_to_float(float_to_bf16_bits(a.gamma[tt]));
-                wsb = double_to_bf16_bits(1.0 / (1.0 + exp(-(double)gb)));
-            }
-            S.wsbits[tt] = wsb;
-            S.ws[tt] = bf16_bits_to_float(wsb);
+            S.lg[tt][lane] = my_l;
         }
     }
     __syncthreads();
-    if (blockIdx.x == 0 && !a.ids_in) {
-        for (int i = tid; i < T * k; i += kFThreads) {
-            const int tt = i / k, j = i - tt * k;
-            if (a.ids_out) a.ids_out[i] = S.ids[tt][j];
-            if (a.p_out) a.p_out[i] = S.pbits[tt][j];
+    if (blockIdx.x == 0 && !a.ids_in && a.ids_out)
+        for (int i = tid; i < T * k; i += kFThreads) a.ids_out[i] = S.ids[i / k][i % k];
+    if ((int)blockIdx.x < npc) {
+        // pick weights p = exp(l - l_top) / sum over the picks and w_s = sigmoid(bf16(gamma)),
+        // in fp64 with one rounding to bf16; published for the combining CTAs
+        const int tt = blockIdx.x * 8 + warp;
+        if (tt < T) {
+            double ex = 0.0;
+            if (lane < k) ex = exp((double)S.lg[tt][lane] - (double)S.lg[tt][0]);
+            double den = 0.0;
+            for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);
+            if (lane < k) {
+                const uint16_t pb = double_to_bf16_bits(ex / den);
+                a.p_glob[tt * k + lane] = pb;
+                if (a.p_out) a.p_out[tt * k + lane] = pb;
+            }
+            if (lane == 0) {
+                uint16_t wsb = 0;
+                if (a.has_shared) {
+                    const float gb = bf16_bits_to_float(float_to_bf16_bits(a.gamma[tt]));
+                    wsb = double_to_bf16_bits(1.0 / (1.0 + exp(-(double)gb)));
+                }
+                a.ws_glob[tt] = wsb;
+                if (a.ws_out) a.ws_out[tt] = wsb;
+            }
         }
-        for (int tt = tid; tt < T; tt += kFThreads)
-            if (a.ws_out) a.ws_out[tt] = S.wsbits[tt];
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            atomicAdd(a.cnt_pick, 1);
+        }
     }
     // distinct experts in increasing id, then the shared expert
     for (int e = tid; e < E; e += kFThreads) {
@@ -282,7 +304,7 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
     {
         const size_t dcode = (size_t)H * (I / 2), dsb = (size_t)H * GI * 2;
         const int pieces = (int)((dcode + 65535) / 65536) + 2;
-        for (int q = blockIdx.x * kFThreads + tid; q < D * pieces; q += gridDim.x * kFThreads) {
+        for (int q = blockIdx.x + tid * gridDim.x; q < D * pieces; q += gridDim.x * kFThreads) {   // one piece per CTA first
             const int d = q / pieces, piece = q - d * pieces;
             const int e = S.list[d];
             const QMatDev &m = e == E ? a.s_down : a.down;
@@ -301,7 +323,8 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
     // ---------------------------------------------------------------- phase 1: gate/up units
     const int rb_i = I / 16;
     const int U1 = D * rb_i;
-    for (int u = blockIdx.x; u < U1; u += gridDim.x) {
+    const int p1_cta = (int)blockIdx.x - npc, p1_grid = (int)gridDim.x - npc;
+    for (int u = p1_cta; p1_cta >= 0 && u < U1; u += p1_grid) {
         const int d = u / rb_i, rb = u - d * rb_i;
         const int e = S.list[d];
         const bool shr = e == E;
@@ -361,8 +384,14 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
                 for (int j = 0; j < NT; ++j) {
                     uint32_t bp[8];
                     if (xrow[j] >= 0) {
-                        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)xrow[j] * H) + grp * 8 + 2 * t4;
-                        permute_b(__ldg(xr), __ldg(xr + 1), bp);
+                        if (XS) {
+                            const uint4 *xr = s_x + xrow[j] * rowu4 + grp * 8 + 2 * t4;
+                            permute_b(xr[0], xr[1], bp);
+                        } else {
+                            const uint4 *xr =
+                                reinterpret_cast<const uint4 *>(a.x + (size_t)xrow[j] * H) + grp * 8 + 2 * t4;
+                            permute_b(__ldg(xr), __ldg(xr + 1), bp);
+                        }
                     } else {
 #pragma unroll
                         for (int q = 0; q < 8; ++q) bp[q] = 0;
@@ -527,6 +556,28 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
             s_ready = atomicAdd(a.cnt_rows + rb * kCounterStride, 1) == D - 1 ? 2 : 1;
         }
         __syncthreads();
+        if (s_ready == 2 && !a.ids_in) {
+            // wait (bounded) for the published pick weights, then take them into shared memory
+            if (tid == 0) {
+                long long n = 0;
+                unsigned ns = 64;
+                while (ld_acquire(a.cnt_pick) < npc && n <= a.wait_limit) {
+                    ++n;
+                    __nanosleep(ns);
+                    ns = ns < 1024 ? ns * 2 : 1024;
+                }
+                if (n > a.wait_limit) {
+                    record_status(a.status, MOE_ERR_TIMEOUT);
+                    s_ready = 1;
+                }
+            }
+            __syncthreads();
+            if (s_ready == 2) {
+                for (int i = tid; i < T * k; i += kFThreads) S.p[i / k][i % k] = bf16_bits_to_float(__ldcg(a.p_glob + i));
+                for (int tt = tid; tt < T; tt += kFThreads) S.ws[tt] = bf16_bits_to_float(__ldcg(a.ws_glob + tt));
+            }
+            __syncthreads();
+        }
         if (s_ready == 2) {
             __threadfence();
             // last unit of this row block: y = bf16(sum_j p_j y_slot[t*k+j] + w_s y_slot[T*k+t]), slot order
@@ -548,43 +599,52 @@ __global__ void __launch_bounds__(kFThreads, 2) decode_fused_kernel(FusedDecodeA
 
 struct Occupancy {
     int device = -1;
+    size_t smem = 0;
     int sms = 0;
-    int per_sm[2] = {0, 0};
+    int per_sm = 0;
 };
 
 }  // namespace
 
 cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t st)
 {
-    static Occupancy occ[16];
+    static Occupancy occ[16][4];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    Occupancy &o = occ[dev & 15];
-    if (o.device != dev) {
+    const int nt = a.T > 8 ? 1 : 0;
+    const size_t xs_bytes = (size_t)a.T * (a.H / 8 + 1) * 16;
+    const bool xs = xs_bytes <= 100 * 1024;
+    const int variant = nt * 2 + (xs ? 1 : 0);
+    auto kern = variant == 0 ? decode_fused_kernel<1, false>
+              : variant == 1 ? decode_fused_kernel<1, true>
+              : variant == 2 ? decode_fused_kernel<2, false>
+                             : decode_fused_kernel<2, true>;
+    const size_t smem = xs ? xs_bytes : 0;
+    Occupancy &o = occ[dev & 15][variant];
+    if (o.device != dev || o.smem != smem) {
         if ((e = cudaDeviceGetAttribute(&o.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o.per_sm[0], decode_fused_kernel<1>, kFThreads, 0)) !=
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(100 * 1024 + 1024))) !=
             cudaSuccess)
             return e;
-        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o.per_sm[1], decode_fused_kernel<2>, kFThreads, 0)) !=
-            cudaSuccess)
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o.per_sm, kern, kFThreads, smem)) != cudaSuccess)
             return e;
         o.device = dev;
+        o.smem = smem;
     }
-    const int nt = a.T > 8 ? 1 : 0;
-    const int grid = o.sms * std::max(1, std::min(2, o.per_sm[nt]));
+    if (o.per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int grid = o.sms * std::min(2, o.per_sm);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kFThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (nt) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<2>, a);
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<1>, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace qmoe

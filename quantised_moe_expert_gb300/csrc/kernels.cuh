@@ -141,6 +141,9 @@ struct FusedDecodeArgs {
     float *acc;                   // f32 [T, H] += sum (when y is null)
     int *cnt_expert;              // [(E + 1) * 32] gate/up units done per expert-list entry, stride 32 (zeroed before launch)
     int *cnt_rows;                // [(H / 128) * 32] down units done per 128-row block, stride 32 (zeroed before launch)
+    int *cnt_pick;                // CTAs that published pick weights (zeroed before launch)
+    uint16_t *p_glob;             // bf16 [T, k] published pick weights
+    uint16_t *ws_glob;            // bf16 [T] published shared weights
     int *status;
     int T, H, I, E, k, has_shared;
     long long wait_limit;

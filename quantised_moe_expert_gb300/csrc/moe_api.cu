@@ -249,6 +249,9 @@ FusedDecodeArgs fused_args(const moe_config &c, const moe_weights &w, const uint
     fa.yslot = ws_at<float>(ws, L.yslot);
     fa.cnt_expert = ws_at<int>(ws, L.counters);
     fa.cnt_rows = fa.cnt_expert + 32 * (c.n_experts + 1);
+    fa.cnt_pick = fa.cnt_rows + 32 * ((c.hidden + 127) / 128);
+    fa.p_glob = ws_at<uint16_t>(ws, L.p);
+    fa.ws_glob = ws_at<uint16_t>(ws, L.w_s);
     fa.status = ws_at<int>(ws, L.status);
     fa.T = T;
     fa.H = c.hidden;
@@ -388,7 +391,7 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     const bool fused = rp == MOE_PATH_DECODE && T <= kDecodeMaxTok;
     if (fused) {
         wa.zero = ws_at<int>(ws, L.counters);
-        wa.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128);
+        wa.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128 + 1);
     }
     if ((rc = cuda_rc(launch_worklist(wa, st)))) return rc;
     if (fused) {
@@ -435,7 +438,7 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
         float *lg = logits_in ? const_cast<float *>(logits_in) : ws_at<float>(ws, L.logits);
         RouteArgs ra = route_args(*cfg, *w, x, T, router_bias, logits_in, lg, L, ws);
         ra.zero = ws_at<int>(ws, L.counters);
-        ra.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128);
+        ra.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128 + 1);
         if ((rc = cuda_rc(launch_route_gemv(ra, st)))) return rc;
         FusedDecodeArgs fa = fused_args(*cfg, *w, x, T, L, ws);
         fa.logits = lg;

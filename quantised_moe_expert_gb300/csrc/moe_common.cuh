@@ -46,7 +46,7 @@ struct WsLayout {
     size_t perm;       // i32 [T*k]
     size_t inv_perm;   // i32 [T*k]
     size_t nwork;      // i32 [4]: decode active experts, gemm1 tiles, gemm2 tiles
-    size_t counters;   // i32 [(E + 1 + H/128) * 32]: fused decode readiness counters, 128 B apart
+    size_t counters;   // i32 [(E + 1 + H/128 + 1) * 32]: fused decode counters, 128 B apart
     size_t work_dec;   // WorkItem [E + 1]
     size_t work_g1;    // WorkItem [max tiles gemm1]
     size_t work_g2;    // WorkItem [max tiles gemm2]
@@ -94,7 +94,7 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.perm = take(4 * Tz * k);
     L.inv_perm = take(4 * Tz * k);
     L.nwork = take(16);
-    L.counters = take(4 * 32 * (E + 1 + (H + 127) / 128));
+    L.counters = take(4 * 32 * (E + 1 + (H + 127) / 128 + 1));
     L.max_wd = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kDecodeMaxTok);
     L.work_dec = take(sizeof(WorkItem) * (size_t)L.max_wd);
     L.work_g1 = take(sizeof(WorkItem) * (size_t)L.max_w1);
