@@ -121,22 +121,15 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *status)
 }
 
 // Stage one chunk of a row's scales and biases (groups [g0, g0 + kScaleChunk)) into the
-// thread-private columns of the shared staging arrays.  Every load is issued
-// before the first store, so the chunk costs one memory round trip.
-template <int NSRC>
-__device__ __forceinline__ void stage_scales(uint16_t *dst, const uint16_t *const *src, int row_ok, size_t row_off,
-                                             int G, int g0, int r)
+// thread-private columns of the shared staging arrays.
+__device__ __forceinline__ void stage_scales(uint16_t *dst, const uint16_t *const *src, int nsrc, int row_ok,
+                                             size_t row_off, int G, int g0, int r)
 {
-    uint16_t v[NSRC][kScaleChunk];
-#pragma unroll
-    for (int a = 0; a < NSRC; ++a)
-#pragma unroll
-        for (int g = 0; g < kScaleChunk; ++g)
-            v[a][g] = (row_ok && g0 + g < G) ? __ldg(src[a] + row_off + g0 + g) : (uint16_t)0;
-#pragma unroll
-    for (int a = 0; a < NSRC; ++a)
-#pragma unroll
-        for (int g = 0; g < kScaleChunk; ++g) dst[(a * kScaleChunk + g) * 128 + r] = v[a][g];
+    for (int a = 0; a < nsrc; ++a)
+        for (int g = 0; g < kScaleChunk; ++g) {
+            const int gg = g0 + g;
+            dst[(a * kScaleChunk + g) * 128 + r] = (row_ok && gg < G) ? src[a][row_off + gg] : (uint16_t)0;
+        }
 }
 
 // Named barrier of the four dequantising warps (threads 0..127).
@@ -355,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) issue_b(0, q % S);
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
-                if (s % kScaleChunk == 0) stage_scales<4>(sScale, srcs, row_ok, soff, G, s, r);
+                if (s % kScaleChunk == 0) stage_scales(sScale, srcs, 4, row_ok, soff, G, s, r);
                 if (s + 1 < nk) {
                     const int qn = q + 1;
                     if (qn >= S && !mbar_wait(smem_u32(empty + qn % S), (qn / S - 1) & 1, limit, s_abort)) {
@@ -581,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint16_t *srcs[2] = {ti.shared_e ? P.sds : P.ds, ti.shared_e ? P.sdb : P.db};
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
-                if (s % kScaleChunk == 0) stage_scales<2>(sScale, srcs, row_ok, soff, GI, s, r);
+                if (s % kScaleChunk == 0) stage_scales(sScale, srcs, 2, row_ok, soff, GI, s, r);
                 if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
