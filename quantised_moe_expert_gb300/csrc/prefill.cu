@@ -121,15 +121,22 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *status)
 }
 
 // Stage one chunk of a row's scales and biases (groups [g0, g0 + kScaleChunk)) into the
-// thread-private columns of the shared staging arrays.
-__device__ __forceinline__ void stage_scales(uint16_t *dst, const uint16_t *const *src, int nsrc, int row_ok,
-                                             size_t row_off, int G, int g0, int r)
+// thread-private columns of the shared staging arrays.  Every load is issued
+// before the first store, so the chunk costs one memory round trip.
+template <int NSRC>
+__device__ __forceinline__ void stage_scales(uint16_t *dst, const uint16_t *const *src, int row_ok, size_t row_off,
+                                             int G, int g0, int r)
 {
-    for (int a = 0; a < nsrc; ++a)
-        for (int g = 0; g < kScaleChunk; ++g) {
-            const int gg = g0 + g;
-            dst[(a * kScaleChunk + g) * 128 + r] = (row_ok && gg < G) ? src[a][row_off + gg] : (uint16_t)0;
-        }
+    uint16_t v[NSRC][kScaleChunk];
+#pragma unroll
+    for (int a = 0; a < NSRC; ++a)
+#pragma unroll
+        for (int g = 0; g < kScaleChunk; ++g)
+            v[a][g] = (row_ok && g0 + g < G) ? src[a][row_off + g0 + g] : (uint16_t)0;
+#pragma unroll
+    for (int a = 0; a < NSRC; ++a)
+#pragma unroll
+        for (int g = 0; g < kScaleChunk; ++g) dst[(a * kScaleChunk + g) * 128 + r] = v[a][g];
 }
 
 // Named barrier of the four dequantising warps (threads 0..127).
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) issue_b(0, q % S);
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
-                if (s % kScaleChunk == 0) stage_scales(sScale, srcs, 4, row_ok, soff, G, s, r);
+                if (s % kScaleChunk == 0) stage_scales<4>(sScale, srcs, row_ok, soff, G, s, r);
                 if (s + 1 < nk) {
                     const int qn = q + 1;
                     if (qn >= S && !mbar_wait(smem_u32(empty + qn % S), (qn / S - 1) & 1, limit, s_abort)) {
@@ -376,7 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 g0 = cg[0], g1 = cg[1], u0 = cu[0], u1 = cu[1];
                 const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
                 const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                mbar_arrive(smem_u32(cempty + cs));          // the code words are in registers
                 uint8_t *ag = sA_g + st * 16384;
                 uint8_t *au = sA_u + st * 16384;
 #pragma unroll
@@ -384,6 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(ag + swz128(r, c)) = dequant8(gw[c], sg, bg);
                     *reinterpret_cast<uint4 *>(au + swz128(r, c)) = dequant8(uw[c], su, bu);
                 }
+                // Release the code slot only after its words have been consumed: the
+                // arrive does not wait for shared loads still in flight, and the TMA
+                // refill of the slot would race them.
+                mbar_arrive(smem_u32(cempty + cs));
                 cp_async_wait_1();               // this K-step's token rows have landed
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(afull + st));
@@ -574,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint16_t *srcs[2] = {ti.shared_e ? P.sds : P.ds, ti.shared_e ? P.sdb : P.db};
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
-                if (s % kScaleChunk == 0) stage_scales(sScale, srcs, 2, row_ok, soff, GI, s, r);
+                if (s % kScaleChunk == 0) stage_scales<2>(sScale, srcs, row_ok, soff, GI, s, r);
                 if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
@@ -599,10 +609,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 *cd = reinterpret_cast<const uint4 *>(sC + cs * 4096 + r * 32);
                 const uint4 c0 = cd[0], c1 = cd[1];
                 const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                mbar_arrive(smem_u32(cempty + cs));
                 uint8_t *aa = sA + st * 16384;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(aa + swz128(r, c)) = dequant8(cw[c], sd, bd);
+                mbar_arrive(smem_u32(cempty + cs));
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(afull + st));
             }
