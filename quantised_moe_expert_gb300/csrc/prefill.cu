@@ -49,7 +49,8 @@ using namespace tc;
 constexpr int kStages = 3;          // A/B operand stages
 constexpr int kCodeStages1 = 6;     // code-tile stages, gate/up GEMM (8 KB each)
 constexpr int kCodeStages2 = 8;     // code-tile stages, down GEMM (4 KB each)
-constexpr int kThreads = 320;       // warps 0-3 dequant, 4 TMA, 5 MMA, 6-9 epilogue
+constexpr int kThreads = 320;       // warps 0-3 dequant, 4 TMA, 5 MMA, 6-9 epilogue (down GEMM)
+constexpr int kThreads1 = 352;      // gate/up GEMM: the same plus warp 10, the token-row loader
 constexpr int kScaleChunk = 16;     // groups of scales staged in shared memory at a time
 constexpr long long kDrainLimit = 1ll << 22;
 
@@ -178,12 +179,13 @@ __device__ __forceinline__ TileInfo tile_info(const WorkItem *work, const int32_
 // --------------------------------------------------------------- gate/up GEMM
 //
 // Persistent: one CTA per SM loops over tiles tau = blockIdx.x + i * gridDim.x.
-// Roles: warps 0-3 dequantise the code tiles and gather the token rows; warp 4
-// (one thread) streams code tiles with TMA through a ring of CS stages; warp 5
-// (one thread) issues the MMAs; warps 6-9 run the epilogue of the previous tile
-// from the other TMEM buffer while the next tile's MMAs accumulate.
+// Roles: warps 0-3 dequantise the code tiles; warp 4 (one thread) streams code
+// tiles with TMA through a ring of CS stages; warp 5 (one thread) issues the
+// MMAs; warps 6-9 run the epilogue of the previous tile from the other TMEM
+// buffer while the next tile's MMAs accumulate; warp 10 gathers the token rows
+// of x with cp.async, up to S - 1 K-steps ahead.
 template <int S, int CS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads1, 1)
     gemm_gateup_kernel(const __grid_constant__ CUtensorMap map_gc, const __grid_constant__ CUtensorMap map_uc,
                        const __grid_constant__ CUtensorMap map_sgc, const __grid_constant__ CUtensorMap map_suc,
                        const G1Params P)
@@ -199,9 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sC = sB + S * 16384;                 // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [4][kScaleChunk][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 4 * kScaleChunk * 128);
-    uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *empty = afull + S;
+    uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *bfull = afull + S, *empty = bfull + S;
     uint64_t *tfull = empty + S, *tempty = tfull + 2, *drain = tempty + 2;
-    int *s_rows = reinterpret_cast<int *>(drain + 1);     // [2][128]
+    int *s_rows = reinterpret_cast<int *>(drain + 1);     // [2][128], written and read by the loader warp
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_rows + 256);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
@@ -217,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(afull + s), 128);
+            mbar_init(smem_u32(bfull + s), 32);
             mbar_init(smem_u32(empty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -233,7 +236,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *s_tmem;
     const long long limit = P.wait_limit;
 
-    if (warp == 4) {
+    if (warp == 10) {
+        // ------------------------------------------------ token rows of x (cp.async gather)
+        // Runs ahead of the dequant warps, bounded only by free stages: step q's rows go
+        // into stage q % S once the MMAs of step q - S are done; the arrive for step q is
+        // made when its copies have landed, one step later.
+        int q = 0, i = 0, pending = -1;
+        bool ok = true;
+        for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x, ++i) {
+            const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+            int *rows = s_rows + (i & 1) * 128;
+            for (int n = lane; n < 128; n += 32) {
+                int row = 0;                                  // rows past ntok are never read
+                if (n < ti.ntok) {
+                    if (ti.shared_e) {
+                        row = ti.tok0 + n;
+                    } else {
+                        const int pos = ti.pbase + n;
+                        const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                        if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
+                        else row = f / P.k;
+                    }
+                }
+                rows[n] = row;
+            }
+            __syncwarp();
+            const int nchunks = ti.ntok * 8;
+            for (int s = 0; s < nk; ++s, ++q) {
+                const int st = q % S;
+                if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
+                    set_abort(s_abort, P.status);
+                    ok = false;
+                    break;
+                }
+                uint8_t *dst = sB + st * 16384;
+                for (int idx = lane; idx < nchunks; idx += 32) {
+                    const int n = idx >> 3, c = idx & 7;
+                    cp_async16(smem_u32(dst + swz128(n, c)), P.x16 + (size_t)rows[n] * H + s * 64 + c * 8);
+                }
+                cp_async_commit();
+                if (pending >= 0) {
+                    cp_async_wait_1();                        // the previous step's rows have landed
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_u32(bfull + pending % S));
+                }
+                pending = q;
+            }
+            __syncwarp();
+        }
+        cp_async_wait_all();
+        if (pending >= 0) {
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(bfull + pending % S));
+        }
+    } else if (warp == 4) {
         // ------------------------------------------------ code tiles (TMA)
         if (lane == 0) {
             prefetch_map(&map_gc);
@@ -283,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d0 = tmem + (uint32_t)buf * 256;
                 for (int s = 0; s < nk; ++s, ++q) {
                     const int st = q % S;
-                    if (!mbar_wait(smem_u32(afull + st), (q / S) & 1, limit, s_abort)) {
+                    if (!mbar_wait(smem_u32(bfull + st), (q / S) & 1, limit, s_abort) ||
+                        !mbar_wait(smem_u32(afull + st), (q / S) & 1, limit, s_abort)) {
                         set_abort(s_abort, P.status);
                         ok = false;
                         break;
@@ -305,67 +362,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
     } else if (warp < 4) {
-        // ------------------------------------------------ dequant (thread = weight row) + token rows
+        // ------------------------------------------------ dequant (thread = weight row)
         const int r = tid;
-        const int bchunk = tid & 7, brow0 = tid >> 3;
-        int q = 0, i = 0;
+        int q = 0;
         bool ok = true;
-        for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
+        for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
-            const int par = i & 1;
-            int *rows = s_rows + par * 128;
-            {
-                int row = 0;                          // rows past ntok are never read
-                if (tid < ti.ntok) {
-                    if (ti.shared_e) {
-                        row = ti.tok0 + tid;
-                    } else {
-                        const int pos = ti.pbase + tid;
-                        const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
-                        if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
-                        else row = f / P.k;
-                    }
-                }
-                rows[tid] = row;
-            }
-            dequant_bar();
             const int row = ti.mb * 128 + r;
             const bool row_ok = row < I;
             const int ee = ti.shared_e ? 0 : ti.expert;
             const size_t soff = (size_t)ee * I * G + (size_t)row * G;
             const uint16_t *srcs[4] = {ti.shared_e ? P.sgs : P.gs, ti.shared_e ? P.sgb : P.gb,
                                        ti.shared_e ? P.sus : P.us, ti.shared_e ? P.sub : P.ub};
-            auto issue_b = [&](int ks, int st) {
-                uint8_t *dst = sB + st * 16384;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int n = brow0 + 16 * j;
-                    if (n < ti.ntok) {
-                        const uint16_t *src = P.x16 + (size_t)rows[n] * H + ks * 64 + bchunk * 8;
-                        cp_async16(smem_u32(dst + swz128(n, bchunk)), src);
-                    }
-                }
-                cp_async_commit();
-            };
-            // stage of step q must be free (MMA of step q - S done) before its B and A are written
-            if (q >= S && !mbar_wait(smem_u32(empty + q % S), (q / S - 1) & 1, limit, s_abort)) {
-                set_abort(s_abort, P.status);
-                ok = false;
-            }
-            if (ok) issue_b(0, q % S);
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
                 if (s % kScaleChunk == 0) stage_scales<4>(sScale, srcs, row_ok, soff, G, s, r);
-                if (s + 1 < nk) {
-                    const int qn = q + 1;
-                    if (qn >= S && !mbar_wait(smem_u32(empty + qn % S), (qn / S - 1) & 1, limit, s_abort)) {
-                        set_abort(s_abort, P.status);
-                        ok = false;
-                        break;
-                    }
-                    issue_b(s + 1, qn % S);
-                } else {
-                    cp_async_commit();
+                // the A stage of step q is free once the MMAs of step q - S are done
+                if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
+                    set_abort(s_abort, P.status);
+                    ok = false;
+                    break;
                 }
                 const int cs = q % CS;
                 if (!mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort)) {
@@ -394,14 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // arrive does not wait for shared loads still in flight, and the TMA
                 // refill of the slot would race them.
                 mbar_arrive(smem_u32(cempty + cs));
-                cp_async_wait_1();               // this K-step's token rows have landed
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(afull + st));
             }
-            cp_async_wait_all();
             if (bar_any(1, 128, !ok || *s_abort)) break;     // the four warps stop together
         }
-        cp_async_wait_all();
     } else {
         // ------------------------------------------------ epilogue: h = silu(g) * u
         const int quad = warp & 3;                        // TMEM lanes 32 quad .. 32 quad + 31
@@ -452,9 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // --------------------------------------------------------------- down GEMM
 //
-// Same structure; the token operand is the h tile of the expert's rows (TMA,
-// issued by dequant thread 0 once the stage is free), and the epilogue adds
-// p * y into the fp32 layer accumulator.
+// Same structure; the token operand is the h tile of the expert's rows, loaded
+// with TMA by a second thread of warp 4 as soon as each stage is free, and the
+// epilogue adds p * y into the fp32 layer accumulator.
 template <int S, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_down_kernel(const __grid_constant__ CUtensorMap map_dc, const __grid_constant__ CUtensorMap map_sdc,
@@ -531,6 +544,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok || *s_abort)
                 for (int d = (q > CS ? q - CS : 0); d < q; ++d)
                     mbar_wait(smem_u32(cfull + d % CS), (d / CS) & 1, kDrainLimit, nullptr);
+        } else if (lane == 1) {
+            // h tiles of the expert's rows (TMA), as soon as each stage is free
+            prefetch_map(&map_h);
+            int q = 0;
+            bool ok = true;
+            for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
+                const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+                const int nbox = (((ti.ntok + 15) & ~15) + 31) / 32;
+                for (int s = 0; s < nk; ++s, ++q) {
+                    const int st = q % S;
+                    if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
+                        set_abort(s_abort, P.status);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(bfull + st);
+                    mbar_arrive_expect_tx(fb, (uint32_t)nbox * 4096);
+                    for (int b = 0; b < nbox; ++b)
+                        tma_load_2d(smem_u32(sB + st * 32768 + b * 4096), &map_h, s * 64, ti.pbase + b * 32, fb);
+                }
+            }
+            if (!ok || *s_abort)   // issued h tiles land before the CTA exits
+                for (int d = (q > S ? q - S : 0); d < q; ++d)
+                    mbar_wait(smem_u32(bfull + d % S), (d / S) & 1, kDrainLimit, nullptr);
         }
     } else if (warp == 5) {
         if (lane == 0) {
@@ -572,11 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = tid;
         int q = 0;
         bool ok = true;
-        int b_issued = 0;                       // h-tile loads issued by thread 0 (for the drain)
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
-            const int N = (ti.ntok + 15) & ~15;
-            const int nbox = (N + 31) / 32;
             const int row = ti.mb * 128 + r;
             const bool row_ok = row < H;
             const int ee = ti.shared_e ? 0 : ti.expert;
@@ -589,13 +623,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
-                }
-                if (tid == 0) {
-                    const uint32_t fb = smem_u32(bfull + st);
-                    mbar_arrive_expect_tx(fb, (uint32_t)nbox * 4096);
-                    for (int b = 0; b < nbox; ++b)
-                        tma_load_2d(smem_u32(sB + st * 32768 + b * 4096), &map_h, s * 64, ti.pbase + b * 32, fb);
-                    b_issued = q + 1;
                 }
                 const int cs = q % CS;
                 if (!mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort)) {
@@ -618,9 +645,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (bar_any(1, 128, !ok || *s_abort)) break;     // the four warps stop together
         }
-        if (tid == 0 && (!ok || *s_abort))     // issued h tiles land before the CTA exits
-            for (int d = (b_issued > S ? b_issued - S : 0); d < b_issued; ++d)
-                mbar_wait(smem_u32(bfull + d % S), (d / S) & 1, kDrainLimit, nullptr);
     } else {
         // ------------------------------------------------ epilogue: acc[t, row] += w * y
         const int quad = warp & 3;
@@ -743,7 +767,7 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
 size_t g1_smem()
 {
     return 1024 + kStages * 16384 * 3 + kCodeStages1 * 8192 + 4 * kScaleChunk * 128 * 2 +
-           8 * (2 * kCodeStages1 + 2 * kStages + 5) + 256 * 4 + 16;
+           8 * (2 * kCodeStages1 + 3 * kStages + 5) + 256 * 4 + 16;
 }
 size_t g2_smem()
 {
@@ -822,7 +846,7 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     auto k1 = gemm_gateup_kernel<kStages, kCodeStages1>;
     cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     const int tiles1 = a.max_w1 * ((I + 127) / 128);
-    k1<<<std::min(sm_count(), tiles1), kThreads, s1, st>>>(mgc, muc, msgc, msuc, p1);
+    k1<<<std::min(sm_count(), tiles1), kThreads1, s1, st>>>(mgc, muc, msgc, msuc, p1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     G2Params p2{};
