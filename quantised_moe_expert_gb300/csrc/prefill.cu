@@ -46,9 +46,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 3;          // A/B operand stages
-constexpr int kCodeStages1 = 6;     // code-tile stages, gate/up GEMM (8 KB each)
-constexpr int kCodeStages2 = 8;     // code-tile stages, down GEMM (4 KB each)
+// Stage counts of the three rings of each GEMM: dequantised weights (A), token
+// operand (B) and int4 code tiles.  B runs deepest: its loads come from L2 /
+// HBM with a latency of several K-steps of MMA.
+constexpr int kStagesA1 = 2, kStagesB1 = 5, kCodeStages1 = 4;   // gate/up: 32 KB, 16 KB, 8 KB per stage
+constexpr int kStagesA2 = 3, kStagesB2 = 4, kCodeStages2 = 6;   // down:    16 KB, 32 KB, 4 KB per stage
+constexpr int kLoaderLag = kStagesB1 - 2;                       // token-row groups in flight beyond the newest
 constexpr int kThreads = 320;       // warps 0-3 dequant, 4 TMA, 5 MMA, 6-9 epilogue (down GEMM)
 constexpr int kThreads1 = 352;      // gate/up GEMM: the same plus warp 10, the token-row loader
 constexpr int kScaleChunk = 16;     // groups of scales staged in shared memory at a time
@@ -184,7 +187,7 @@ __device__ __forceinline__ TileInfo tile_info(const WorkItem *work, const int32_
 // MMAs; warps 6-9 run the epilogue of the previous tile from the other TMEM
 // buffer while the next tile's MMAs accumulate; warp 10 gathers the token rows
 // of x with cp.async, up to S - 1 K-steps ahead.
-template <int S, int CS>
+template <int S, int SB, int CS>
 __global__ void __launch_bounds__(kThreads1, 1)
     gemm_gateup_kernel(const __grid_constant__ CUtensorMap map_gc, const __grid_constant__ CUtensorMap map_uc,
                        const __grid_constant__ CUtensorMap map_sgc, const __grid_constant__ CUtensorMap map_suc,
@@ -197,12 +200,13 @@ __global__ void __launch_bounds__(kThreads1, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA_g = smem;                         // S x 16 KB
     uint8_t *sA_u = sA_g + S * 16384;             // S x 16 KB
-    uint8_t *sB = sA_u + S * 16384;               // S x 16 KB (128 token rows x 128 B)
-    uint8_t *sC = sB + S * 16384;                 // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
+    uint8_t *sB = sA_u + S * 16384;               // SB x 16 KB (128 token rows x 128 B)
+    uint8_t *sC = sB + SB * 16384;                // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [4][kScaleChunk][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 4 * kScaleChunk * 128);
-    uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *bfull = afull + S, *empty = bfull + S;
-    uint64_t *tfull = empty + S, *tempty = tfull + 2, *drain = tempty + 2;
+    uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
+    uint64_t *bfull = aempty + S, *bempty = bfull + SB;
+    uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
     int *s_rows = reinterpret_cast<int *>(drain + 1);     // [2][128], written and read by the loader warp
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_rows + 256);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
@@ -219,8 +223,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(afull + s), 128);
+            mbar_init(smem_u32(aempty + s), 1);
+        }
+        for (int s = 0; s < SB; ++s) {
             mbar_init(smem_u32(bfull + s), 32);
-            mbar_init(smem_u32(empty + s), 1);
+            mbar_init(smem_u32(bempty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(tfull + b), 1);
@@ -238,10 +245,10 @@ __global__ void __launch_bounds__(kThreads1, 1)
 
     if (warp == 10) {
         // ------------------------------------------------ token rows of x (cp.async gather)
-        // Runs ahead of the dequant warps, bounded only by free stages: step q's rows go
-        // into stage q % S once the MMAs of step q - S are done; the arrive for step q is
-        // made when its copies have landed, one step later.
-        int q = 0, i = 0, pending = -1;
+        // Runs ahead of the dequant warps, bounded only by free B stages: step q's rows go
+        // into stage q % SB once the MMAs of step q - SB are done; the arrive for step q is
+        // made when its copies have landed, kLoaderLag steps later.
+        int q = 0, i = 0, done = 0;                           // steps [done, q) issued, not yet arrived
         bool ok = true;
         for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x, ++i) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
@@ -263,8 +270,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
             __syncwarp();
             const int nchunks = ti.ntok * 8;
             for (int s = 0; s < nk; ++s, ++q) {
-                const int st = q % S;
-                if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
+                const int st = q % SB;
+                if (q >= SB && !mbar_wait(smem_u32(bempty + st), (q / SB - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
@@ -275,20 +282,18 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     cp_async16(smem_u32(dst + swz128(n, c)), P.x16 + (size_t)rows[n] * H + s * 64 + c * 8);
                 }
                 cp_async_commit();
-                if (pending >= 0) {
-                    cp_async_wait_1();                        // the previous step's rows have landed
+                if (q - done >= kLoaderLag) {
+                    cp_async_wait_group<kLoaderLag>();        // step `done`'s rows have landed
                     fence_proxy_async_smem();
-                    mbar_arrive(smem_u32(bfull + pending % S));
+                    mbar_arrive(smem_u32(bfull + done % SB));
+                    ++done;
                 }
-                pending = q;
             }
             __syncwarp();
         }
         cp_async_wait_all();
-        if (pending >= 0) {
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(bfull + pending % S));
-        }
+        fence_proxy_async_smem();
+        for (; done < q; ++done) mbar_arrive(smem_u32(bfull + done % SB));
     } else if (warp == 4) {
         // ------------------------------------------------ code tiles (TMA)
         if (lane == 0) {
@@ -338,8 +343,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 tc_fence_after();
                 const uint32_t d0 = tmem + (uint32_t)buf * 256;
                 for (int s = 0; s < nk; ++s, ++q) {
-                    const int st = q % S;
-                    if (!mbar_wait(smem_u32(bfull + st), (q / S) & 1, limit, s_abort) ||
+                    const int st = q % S, sb = q % SB;
+                    if (!mbar_wait(smem_u32(bfull + sb), (q / SB) & 1, limit, s_abort) ||
                         !mbar_wait(smem_u32(afull + st), (q / S) & 1, limit, s_abort)) {
                         set_abort(s_abort, P.status);
                         ok = false;
@@ -347,14 +352,15 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     }
                     tc_fence_after();
                     const uint32_t ag = smem_u32(sA_g + st * 16384), au = smem_u32(sA_u + st * 16384);
-                    const uint32_t bb = smem_u32(sB + st * 16384);
+                    const uint32_t bb = smem_u32(sB + sb * 16384);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t acc = (s | kk) != 0;
                         mma_f16(d0, desc_sw128(ag + kk * 32), desc_sw128(bb + kk * 32), idesc, acc);
                         mma_f16(d0 + 128, desc_sw128(au + kk * 32), desc_sw128(bb + kk * 32), idesc, acc);
                     }
-                    mma_commit(smem_u32(empty + st));
+                    mma_commit(smem_u32(aempty + st));
+                    mma_commit(smem_u32(bempty + sb));
                 }
                 if (ok) mma_commit(smem_u32(tfull + buf));
             }
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 const int st = q % S;
                 if (s % kScaleChunk == 0) stage_scales<4>(sScale, srcs, row_ok, soff, G, s, r);
                 // the A stage of step q is free once the MMAs of step q - S are done
-                if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
+                if (q >= S && !mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
@@ -468,7 +474,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
 // Same structure; the token operand is the h tile of the expert's rows, loaded
 // with TMA by a second thread of warp 4 as soon as each stage is free, and the
 // epilogue adds p * y into the fp32 layer accumulator.
-template <int S, int CS>
+template <int S, int SB, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_down_kernel(const __grid_constant__ CUtensorMap map_dc, const __grid_constant__ CUtensorMap map_sdc,
                      const __grid_constant__ CUtensorMap map_h, const G2Params P)
@@ -479,12 +485,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;                           // S x 16 KB
-    uint8_t *sB = sA + S * 16384;                 // S x 32 KB (256 rows x 128 B)
-    uint8_t *sC = sB + S * 32768;                 // CS x 4 KB
+    uint8_t *sB = sA + S * 16384;                 // SB x 32 KB (256 rows x 128 B)
+    uint8_t *sC = sB + SB * 32768;                // CS x 4 KB
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 4096);   // [2][kScaleChunk][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 2 * kScaleChunk * 128);
-    uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *bfull = afull + S, *empty = bfull + S;
-    uint64_t *tfull = empty + S, *tempty = tfull + 2, *drain = tempty + 2;
+    uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
+    uint64_t *bfull = aempty + S, *bempty = bfull + SB;
+    uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
     int *s_tok = reinterpret_cast<int *>(drain + 1);           // [2][256]
     float *s_w = reinterpret_cast<float *>(s_tok + 512);       // [2][256]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_w + 512);
@@ -502,8 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(afull + s), 128);
+            mbar_init(smem_u32(aempty + s), 1);
+        }
+        for (int s = 0; s < SB; ++s) {
             mbar_init(smem_u32(bfull + s), 1);
-            mbar_init(smem_u32(empty + s), 1);
+            mbar_init(smem_u32(bempty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(tfull + b), 1);
@@ -553,21 +563,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
                 const int nbox = (((ti.ntok + 15) & ~15) + 31) / 32;
                 for (int s = 0; s < nk; ++s, ++q) {
-                    const int st = q % S;
-                    if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
+                    const int sb = q % SB;
+                    if (q >= SB && !mbar_wait(smem_u32(bempty + sb), (q / SB - 1) & 1, limit, s_abort)) {
                         set_abort(s_abort, P.status);
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(bfull + st);
+                    const uint32_t fb = smem_u32(bfull + sb);
                     mbar_arrive_expect_tx(fb, (uint32_t)nbox * 4096);
                     for (int b = 0; b < nbox; ++b)
-                        tma_load_2d(smem_u32(sB + st * 32768 + b * 4096), &map_h, s * 64, ti.pbase + b * 32, fb);
+                        tma_load_2d(smem_u32(sB + sb * 32768 + b * 4096), &map_h, s * 64, ti.pbase + b * 32, fb);
                 }
             }
             if (!ok || *s_abort)   // issued h tiles land before the CTA exits
-                for (int d = (q > S ? q - S : 0); d < q; ++d)
-                    mbar_wait(smem_u32(bfull + d % S), (d / S) & 1, kDrainLimit, nullptr);
+                for (int d = (q > SB ? q - SB : 0); d < q; ++d)
+                    mbar_wait(smem_u32(bfull + d % SB), (d / SB) & 1, kDrainLimit, nullptr);
         }
     } else if (warp == 5) {
         if (lane == 0) {
@@ -586,19 +596,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d0 = tmem + (uint32_t)buf * 256;
                 for (int s = 0; s < nk; ++s, ++q) {
-                    const int st = q % S;
-                    if (!mbar_wait(smem_u32(bfull + st), (q / S) & 1, limit, s_abort) ||
+                    const int st = q % S, sb = q % SB;
+                    if (!mbar_wait(smem_u32(bfull + sb), (q / SB) & 1, limit, s_abort) ||
                         !mbar_wait(smem_u32(afull + st), (q / S) & 1, limit, s_abort)) {
                         set_abort(s_abort, P.status);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t aa = smem_u32(sA + st * 16384), bb = smem_u32(sB + st * 32768);
+                    const uint32_t aa = smem_u32(sA + st * 16384), bb = smem_u32(sB + sb * 32768);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_f16(d0, desc_sw128(aa + kk * 32), desc_sw128(bb + kk * 32), idesc, (s | kk) != 0);
-                    mma_commit(smem_u32(empty + st));
+                    mma_commit(smem_u32(aempty + st));
+                    mma_commit(smem_u32(bempty + sb));
                 }
                 if (ok) mma_commit(smem_u32(tfull + buf));
             }
@@ -619,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
                 if (s % kScaleChunk == 0) stage_scales<2>(sScale, srcs, row_ok, soff, GI, s, r);
-                if (q >= S && !mbar_wait(smem_u32(empty + st), (q / S - 1) & 1, limit, s_abort)) {
+                if (q >= S && !mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
@@ -766,13 +777,13 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
 
 size_t g1_smem()
 {
-    return 1024 + kStages * 16384 * 3 + kCodeStages1 * 8192 + 4 * kScaleChunk * 128 * 2 +
-           8 * (2 * kCodeStages1 + 3 * kStages + 5) + 256 * 4 + 16;
+    return 1024 + kStagesA1 * 32768 + kStagesB1 * 16384 + kCodeStages1 * 8192 + 4 * kScaleChunk * 128 * 2 +
+           8 * (2 * kCodeStages1 + 2 * kStagesA1 + 2 * kStagesB1 + 5) + 256 * 4 + 16;
 }
 size_t g2_smem()
 {
-    return 1024 + kStages * (16384 + 32768) + kCodeStages2 * 4096 + 2 * kScaleChunk * 128 * 2 +
-           8 * (2 * kCodeStages2 + 3 * kStages + 5) + 1024 * 4 + 16;
+    return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + kCodeStages2 * 4096 + 2 * kScaleChunk * 128 * 2 +
+           8 * (2 * kCodeStages2 + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 1024 * 4 + 16;
 }
 
 int sm_count()
@@ -843,7 +854,7 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p1.k = k;
     p1.wait_limit = a.wait_limit;
     const size_t s1 = g1_smem();
-    auto k1 = gemm_gateup_kernel<kStages, kCodeStages1>;
+    auto k1 = gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1>;
     cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     const int tiles1 = a.max_w1 * ((I + 127) / 128);
     k1<<<std::min(sm_count(), tiles1), kThreads1, s1, st>>>(mgc, muc, msgc, msuc, p1);
@@ -869,7 +880,7 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p2.k = k;
     p2.wait_limit = a.wait_limit;
     const size_t s2 = g2_smem();
-    auto k2 = gemm_down_kernel<kStages, kCodeStages2>;
+    auto k2 = gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2>;
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
     const int tiles2 = a.max_w2 * ((H + 127) / 128);
     k2<<<std::min(sm_count(), tiles2), kThreads, s2, st>>>(mdc, msdc, mh, p2);
