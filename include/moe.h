@@ -209,10 +209,13 @@ MOE_API int moe_forward_decode_static(const moe_config *cfg, const moe_weights *
 MOE_API int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_status);
 
 /* Upper bound on the polls of every bounded wait inside the kernels (mbarrier
- * waits of the tensor-core pipeline).  A wait that reaches it records
- * MOE_ERR_TIMEOUT and the kernel returns early.  Default 1 << 24 polls
- * (about a second); values <= 0 restore the default.  Affects launches
- * enqueued after the call; meant for fault-handling tests. */
+ * waits of the tensor-core pipeline, readiness counters of the fused decode
+ * kernel).  The first poll does not block; later polls suspend for up to about
+ * a microsecond.  A wait that reaches the bound records MOE_ERR_TIMEOUT and
+ * the kernel returns early.  Default 1 << 20 polls (about a second); values
+ * <= 0 restore the default.  Affects launches enqueued after the call; meant
+ * for fault-handling tests (a limit of 1 makes any wait that is not already
+ * satisfied run out). */
 MOE_API int moe_set_wait_limit(long long polls);
 
 #ifdef __cplusplus

@@ -8,7 +8,7 @@ using namespace qmoe;
 
 namespace {
 
-std::atomic<long long> g_wait_limit{1ll << 24};
+std::atomic<long long> g_wait_limit{1ll << 20};
 
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned16_or_null(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -481,7 +481,7 @@ int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_s
 
 int moe_set_wait_limit(long long polls)
 {
-    g_wait_limit.store(polls > 0 ? polls : (1ll << 24));
+    g_wait_limit.store(polls > 0 ? polls : (1ll << 20));
     return MOE_OK;
 }
 

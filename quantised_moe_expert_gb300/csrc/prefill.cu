@@ -8,19 +8,22 @@
 // operand, tokens the N operand, so an expert with few tokens still fills the
 // MMA's M dimension.
 //
-// Per K-step (one quantisation group of 64 inputs):
-//   - a TMA thread loads the int4 code tile of the weights (128 rows x 32 B),
-//     and for the down GEMM the h tile (128-byte swizzle), on an mbarrier;
-//   - four dequantising warps turn codes into fp16 w = s*q + b (one rounding)
-//     and store them in the 128-byte-swizzled K-major layout the MMA reads;
-//     for the gate/up GEMM they also gather the expert's token rows of x
-//     with cp.async (16-byte chunks placed at their swizzled positions), one
-//     K-step ahead;
+// Both kernels are persistent (one CTA per SM looping over tiles) and warp
+// specialised.  Per K-step (one quantisation group of 64 inputs):
+//   - a TMA thread streams the int4 code tile of the weights (128 rows x 32 B)
+//     through a ring of code stages;
+//   - the token operand arrives in its own, deeper ring: for the gate/up GEMM a
+//     loader warp gathers the expert's rows of x with cp.async (16-byte chunks
+//     placed at their 128-byte-swizzled positions), for the down GEMM a second
+//     TMA thread loads the h tile;
+//   - eight dequantising warps turn codes into fp16 w = s*q + b (one rounding)
+//     and store them in the swizzled K-major layout the MMA reads;
 //   - one thread issues tcgen05.mma (fp16 in, fp32 accumulate in TMEM) and
-//     releases the stage with tcgen05.commit.
-// The epilogue reads the accumulators with tcgen05.ld: the gate/up GEMM writes
-// h = silu(g) * u as fp16 in expert-sorted row order, the down GEMM adds
-// p * y into the fp32 layer accumulator with atomics.
+//     releases each stage with tcgen05.commit.
+// Four epilogue warps read the previous tile's accumulators with tcgen05.ld
+// from the other half of TMEM while the next tile accumulates: the gate/up
+// GEMM writes h = silu(g) * u as fp16 in expert-sorted row order, the down
+// GEMM adds p * y into the fp32 layer accumulator with atomics.
 //
 // Operand type.  MMA operands are fp16: dequantised weights and the
 // intermediate h keep 11 significant bits (bf16 would keep 8, which puts the
@@ -52,8 +55,12 @@ using namespace tc;
 constexpr int kStagesA1 = 2, kStagesB1 = 5, kCodeStages1 = 4;   // gate/up: 32 KB, 16 KB, 8 KB per stage
 constexpr int kStagesA2 = 3, kStagesB2 = 4, kCodeStages2 = 6;   // down:    16 KB, 32 KB, 4 KB per stage
 constexpr int kLoaderLag = kStagesB1 - 2;                       // token-row groups in flight beyond the newest
-constexpr int kThreads = 320;       // warps 0-3 dequant, 4 TMA, 5 MMA, 6-9 epilogue (down GEMM)
-constexpr int kThreads1 = 352;      // gate/up GEMM: the same plus warp 10, the token-row loader
+// Warp roles (both GEMMs): 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue; the
+// gate/up GEMM adds warp 14, the token-row loader.
+constexpr int kDequantThreads = 256;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10, kWarpLoader = 14;
+constexpr int kThreads = 448;       // down GEMM
+constexpr int kThreads1 = 480;      // gate/up GEMM
 constexpr int kScaleChunk = 16;     // groups of scales staged in shared memory at a time
 constexpr long long kDrainLimit = 1ll << 22;
 
@@ -212,17 +219,17 @@ __global__ void __launch_bounds__(kThreads1, 1)
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(s_tmem), 512);
         tmem_relinquish();
     }
     if (tid == 0) {
         for (int s = 0; s < CS; ++s) {
             mbar_init(smem_u32(cfull + s), 1);
-            mbar_init(smem_u32(cempty + s), 128);
+            mbar_init(smem_u32(cempty + s), kDequantThreads);
         }
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(afull + s), 128);
+            mbar_init(smem_u32(afull + s), kDequantThreads);
             mbar_init(smem_u32(aempty + s), 1);
         }
         for (int s = 0; s < SB; ++s) {
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
     const uint32_t tmem = *s_tmem;
     const long long limit = P.wait_limit;
 
-    if (warp == 10) {
+    if (warp == kWarpLoader) {
         // ------------------------------------------------ token rows of x (cp.async gather)
         // Runs ahead of the dequant warps, bounded only by free B stages: step q's rows go
         // into stage q % SB once the MMAs of step q - SB are done; the arrive for step q is
@@ -294,7 +301,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
         cp_async_wait_all();
         fence_proxy_async_smem();
         for (; done < q; ++done) mbar_arrive(smem_u32(bfull + done % SB));
-    } else if (warp == 4) {
+    } else if (warp == kWarpTma) {
         // ------------------------------------------------ code tiles (TMA)
         if (lane == 0) {
             prefetch_map(&map_gc);
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 for (int d = (q > CS ? q - CS : 0); d < q; ++d)
                     mbar_wait(smem_u32(cfull + d % CS), (d / CS) & 1, kDrainLimit, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             int q = 0, i = 0;
@@ -367,9 +374,9 @@ __global__ void __launch_bounds__(kThreads1, 1)
             mma_commit(smem_u32(drain));   // every issued MMA completes before TMEM is freed
             mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------ dequant (thread = weight row)
-        const int r = tid;
+    } else if (warp < 8) {
+        // ------------------------------------------------ dequant: warps 0-3 gate rows, 4-7 up rows
+        const int m = tid >> 7, r = tid & 127;
         int q = 0;
         bool ok = true;
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
@@ -378,11 +385,12 @@ __global__ void __launch_bounds__(kThreads1, 1)
             const bool row_ok = row < I;
             const int ee = ti.shared_e ? 0 : ti.expert;
             const size_t soff = (size_t)ee * I * G + (size_t)row * G;
-            const uint16_t *srcs[4] = {ti.shared_e ? P.sgs : P.gs, ti.shared_e ? P.sgb : P.gb,
-                                       ti.shared_e ? P.sus : P.us, ti.shared_e ? P.sub : P.ub};
+            const uint16_t *srcs[2] = {m == 0 ? (ti.shared_e ? P.sgs : P.gs) : (ti.shared_e ? P.sus : P.us),
+                                       m == 0 ? (ti.shared_e ? P.sgb : P.gb) : (ti.shared_e ? P.sub : P.ub)};
+            uint16_t *myscale = sScale + m * 2 * kScaleChunk * 128;
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
-                if (s % kScaleChunk == 0) stage_scales<4>(sScale, srcs, row_ok, soff, G, s, r);
+                if (s % kScaleChunk == 0) stage_scales<2>(myscale, srcs, row_ok, soff, G, s, r);
                 // the A stage of step q is free once the MMAs of step q - S are done
                 if (q >= S && !mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
@@ -396,22 +404,14 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     break;
                 }
                 const int gi = s % kScaleChunk;
-                const __half2 sg = bf16_to_h2(sScale[(0 * kScaleChunk + gi) * 128 + r]);
-                const __half2 bg = bf16_to_h2(sScale[(1 * kScaleChunk + gi) * 128 + r]);
-                const __half2 su = bf16_to_h2(sScale[(2 * kScaleChunk + gi) * 128 + r]);
-                const __half2 bu = bf16_to_h2(sScale[(3 * kScaleChunk + gi) * 128 + r]);
-                const uint4 *cg = reinterpret_cast<const uint4 *>(sC + cs * 8192 + r * 32);
-                const uint4 *cu = reinterpret_cast<const uint4 *>(sC + cs * 8192 + 4096 + r * 32);
-                const uint4 g0 = cg[0], g1 = cg[1], u0 = cu[0], u1 = cu[1];
-                const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-                const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                uint8_t *ag = sA_g + st * 16384;
-                uint8_t *au = sA_u + st * 16384;
+                const __half2 sc = bf16_to_h2(myscale[(0 * kScaleChunk + gi) * 128 + r]);
+                const __half2 bc = bf16_to_h2(myscale[(1 * kScaleChunk + gi) * 128 + r]);
+                const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
+                const uint4 w0 = cp[0], w1 = cp[1];
+                const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint8_t *aa = (m == 0 ? sA_g : sA_u) + st * 16384;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    *reinterpret_cast<uint4 *>(ag + swz128(r, c)) = dequant8(gw[c], sg, bg);
-                    *reinterpret_cast<uint4 *>(au + swz128(r, c)) = dequant8(uw[c], su, bu);
-                }
+                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(aa + swz128(r, c)) = dequant8(cw[c], sc, bc);
                 // Release the code slot only after its words have been consumed: the
                 // arrive does not wait for shared loads still in flight, and the TMA
                 // refill of the slot would race them.
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(afull + st));
             }
-            if (bar_any(1, 128, !ok || *s_abort)) break;     // the four warps stop together
+            if (bar_any(1, kDequantThreads, !ok || *s_abort)) break;   // the eight warps stop together
         }
     } else {
         // ------------------------------------------------ epilogue: h = silu(g) * u
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -487,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sA = smem;                           // S x 16 KB
     uint8_t *sB = sA + S * 16384;                 // SB x 32 KB (256 rows x 128 B)
     uint8_t *sC = sB + SB * 32768;                // CS x 4 KB
-    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 4096);   // [2][kScaleChunk][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 2 * kScaleChunk * 128);
+    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 4096);   // [2 halves][2][kScaleChunk][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 4 * kScaleChunk * 128);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
@@ -498,17 +498,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(s_tmem), 512);
         tmem_relinquish();
     }
     if (tid == 0) {
         for (int s = 0; s < CS; ++s) {
             mbar_init(smem_u32(cfull + s), 1);
-            mbar_init(smem_u32(cempty + s), 128);
+            mbar_init(smem_u32(cempty + s), kDequantThreads);
         }
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(afull + s), 128);
+            mbar_init(smem_u32(afull + s), kDequantThreads);
             mbar_init(smem_u32(aempty + s), 1);
         }
         for (int s = 0; s < SB; ++s) {
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *s_tmem;
     const long long limit = P.wait_limit;
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         if (lane == 0) {
             prefetch_map(&map_dc);
             prefetch_map(&map_sdc);
@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int d = (q > SB ? q - SB : 0); d < q; ++d)
                     mbar_wait(smem_u32(bfull + d % SB), (d / SB) & 1, kDrainLimit, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         if (lane == 0) {
             int q = 0, i = 0;
             bool ok = true;
@@ -616,8 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(drain));
             mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
-    } else if (warp < 4) {
-        const int r = tid;
+    } else if (warp < 8) {
+        // ------------------------------------------------ dequant: thread = half a row (4 chunks)
+        const int r = tid & 127, half = tid >> 7;
         int q = 0;
         bool ok = true;
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
@@ -627,9 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ee = ti.shared_e ? 0 : ti.expert;
             const size_t soff = (size_t)ee * H * GI + (size_t)row * GI;
             const uint16_t *srcs[2] = {ti.shared_e ? P.sds : P.ds, ti.shared_e ? P.sdb : P.db};
+            uint16_t *myscale = sScale + half * 2 * kScaleChunk * 128;   // each half keeps its own copy
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
-                if (s % kScaleChunk == 0) stage_scales<2>(sScale, srcs, row_ok, soff, GI, s, r);
+                if (s % kScaleChunk == 0) stage_scales<2>(myscale, srcs, row_ok, soff, GI, s, r);
                 if (q >= S && !mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
@@ -642,19 +644,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int gi = s % kScaleChunk;
-                const __half2 sd = bf16_to_h2(sScale[(0 * kScaleChunk + gi) * 128 + r]);
-                const __half2 bd = bf16_to_h2(sScale[(1 * kScaleChunk + gi) * 128 + r]);
-                const uint4 *cd = reinterpret_cast<const uint4 *>(sC + cs * 4096 + r * 32);
-                const uint4 c0 = cd[0], c1 = cd[1];
-                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                const __half2 sd = bf16_to_h2(myscale[(0 * kScaleChunk + gi) * 128 + r]);
+                const __half2 bd = bf16_to_h2(myscale[(1 * kScaleChunk + gi) * 128 + r]);
+                const uint4 w = *reinterpret_cast<const uint4 *>(sC + cs * 4096 + r * 32 + half * 16);
+                const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
                 uint8_t *aa = sA + st * 16384;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(aa + swz128(r, c)) = dequant8(cw[c], sd, bd);
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(aa + swz128(r, half * 4 + c)) = dequant8(cw[c], sd, bd);
                 mbar_arrive(smem_u32(cempty + cs));
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(afull + st));
             }
-            if (bar_any(1, 128, !ok || *s_abort)) break;     // the four warps stop together
+            if (bar_any(1, kDequantThreads, !ok || *s_abort)) break;   // the eight warps stop together
         }
     } else {
         // ------------------------------------------------ epilogue: acc[t, row] += w * y
@@ -668,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int *tok = s_tok + buf * 256;
             float *wv = s_w + buf * 256;
             // token and weight of each column (epilogue threads 192..319 fill them)
-            for (int n = tid - 192; n < 256; n += 128) {
+            for (int n = tid - kWarpEpi * 32; n < 256; n += 128) {
                 int t = -1;
                 float wgt = 0.f;
                 if (n < ti.ntok) {
@@ -717,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -782,7 +784,7 @@ size_t g1_smem()
 }
 size_t g2_smem()
 {
-    return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + kCodeStages2 * 4096 + 2 * kScaleChunk * 128 * 2 +
+    return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + kCodeStages2 * 4096 + 4 * kScaleChunk * 128 * 2 +
            8 * (2 * kCodeStages2 + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 1024 * 4 + 16;
 }
 

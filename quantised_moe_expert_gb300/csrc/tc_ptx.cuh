@@ -49,14 +49,29 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
-// Bounded wait for the phase with the given parity.  Gives up (returns false)
-// after `limit` polls or as soon as *abort is set by another thread.
+// Suspending poll: the thread sleeps in hardware until the phase completes or
+// about a microsecond passes, so waiting warps take no issue slots.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, "
+        "p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(1000u)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase with the given parity: one non-blocking poll, then
+// suspending polls.  Gives up (returns false) after `limit` polls in all, or as
+// soon as *abort is set by another thread.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit, volatile int *abort)
 {
-    for (long long i = 0;; ++i) {
-        if (mbar_test(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;
+    for (long long i = 1;; ++i) {
         if (i >= limit || (abort != nullptr && *abort)) return false;
-        if (i > 256) __nanosleep(32);
+        if (mbar_try(bar, parity)) return true;
     }
 }
 
