@@ -1,0 +1,986 @@
+// Streaming decode layer for T <= 16: one cooperative launch after the router GEMV.
+//
+// The decode cost is the bytes of the selected experts (page "POC for qwen3.5 /
+// qwen3.6 support optimized for AGX Orin", Phase 1-4: the batch-1 "gemv MoE
+// path"; "both stacks are now weight-BW bound").  At T = 1 those are ~16 MB,
+// a few microseconds of HBM time, so the whole expert stage stays in one grid
+// of co-resident CTAs (one per SM) and the data movement is the TMA engine's:
+//   - the work is a list of units: gate/up units (expert, 16 rows of I, both
+//     matrices, all of H) followed by down units (expert, 128 rows of H, all
+//     of I); CTA c takes units c, c + grid, c + 2 grid, ...;
+//   - a producer thread streams each unit's int4 codes with 2D TMA (128-byte
+//     swizzled boxes, so the MMA fragment reads below hit no bank twice) and
+//     its scales and biases with bulk copies into a ring of shared-memory
+//     slots, as far ahead as the ring allows, and asks L2 for the unit one ring
+//     length further; down units are loaded before their inputs exist;
+//   - eight consumer warps compute each unit from shared memory, write its
+//     result to global memory, release the slot and publish the unit in
+//     shared memory;
+//   - a signal thread makes the published units visible GPU-wide (one fence
+//     per batch) and counts them: gate/up units per expert, down units per
+//     128-row block; the last down unit of a row block queues that block's
+//     combine for this CTA's consumers.  Before that, in CTAs assigned a
+//     token, its warp computes the token's pick weights and shared weight in
+//     fp64 (a long dependent chain on this GPU); only the combine waits for
+//     them.
+// Phase 0 (every CTA): stage x (in the codes' k order) and its per-group sums
+// in shared memory, redo the top-k from the fp32 logits (same comparisons as
+// the top-k kernel), list the distinct experts (increasing id, shared expert
+// last) and their columns.
+// Gate/up unit: split-K over the eight warps, fixed-order reduction, h =
+// silu(g) * u stored as fp16 in the codes' k order.  Down unit: one thread
+// waits (bounded, with backoff) for the expert's gate/up units, the expert's
+// h columns are staged in shared memory, the raw expert output is written per
+// slot.  Combine: y = bf16(sum_j p_j y_slot[t k + j] + w_s y_slot[T k + t]) in
+// slot order, one rounding.
+//
+// Arithmetic (the GEMV of the decode path): over one group of 64 inputs
+//     sum_j w_j x_j = s (sum_j (OFF + q_j) x_j) + (b - OFF s) sum_j x_j,
+// OFF + q exact in the MMA operand type (bf16 128 + q for x, fp16 1024 + q for
+// h), products on mma.sync m16n8k16 with fp32 accumulation, per-group scale and
+// bias in fp32.  Every output element is one MMA column: a token's result does
+// not depend on the other tokens of the batch.
+//
+// Code size matters here as much as arithmetic: at T = 1 every SM runs each
+// code path two or three times, so instruction fetch is part of the critical
+// path.  The hot loops are therefore not unrolled across groups, and the rarely
+// run parts (routing, lists, producer, signals, combine) are separate
+// functions.  Counters are zeroed by the kernel that precedes this launch.
+#include <algorithm>
+
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+#include "tma_host.cuh"
+
+namespace qmoe {
+namespace {
+
+using namespace tc;
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kWarpProd = 8, kWarpSig = 9;
+constexpr int kSThreads = 320;
+constexpr int kCounterStride = 32;       // counters 128 bytes apart: pollers and writers do not share a line
+constexpr int kMaxList = kMaxExperts + 1;
+constexpr int kMaxSlots = 6;
+constexpr int kRows1 = 16;               // rows of a gate/up unit
+constexpr int kRows2 = 128;              // rows of a down unit
+constexpr int kBox1 = kRows1 * 128;      // bytes of one 128-byte-wide code box of a gate/up unit
+constexpr int kBox2 = kRows2 * 128;      // same, down unit
+constexpr int kMaxRowBlocks = 64;        // H / 128 for H <= 8192
+constexpr long long kDrainLimit = 1ll << 22;
+
+struct StreamMaps {
+    CUtensorMap g, u, d, sg, su, sd;     // int4 codes of gate, up, down (routed stacks, then the shared expert)
+};
+
+// Shared-memory geometry (bytes), fixed per (T, H, I) on the host.
+struct StreamGeom {
+    int R;                 // ring slots
+    uint32_t slot;         // bytes per slot (multiple of 1024)
+    int nb1;               // 128-byte boxes per gate/up code row (H / 256)
+    uint32_t up_off, sc1_off, sb1, bytes1;
+    int nb2;               // 128-byte boxes per down code row (I / 256)
+    uint32_t sc2_off;
+    uint32_t x_off, sumx_off, h_off, red_off, dyn;
+    int x_stride;          // uint4 per staged x row
+    int h_stride;          // fp16 per staged h column
+};
+
+struct SSmem {
+    int ids[kDecodeMaxTok][kMaxTopK];
+    float lg[kDecodeMaxTok][kMaxTopK];     // fp32 logit of each pick
+    float p[kDecodeMaxTok][kMaxTopK];
+    float ws[kDecodeMaxTok];
+    int lpos[kMaxList];                    // list position of each used expert, -1 if unused
+    int cfill[kMaxList];
+    int list[kMaxList];
+    int ncols[kMaxList];
+    int colptr[kMaxList + 1];
+    int colf[kDecodeMaxTok * (kMaxTopK + 1)];   // slot index f of each column, expert after expert
+    int nlist;
+    int ready;
+    int abort;
+    int sig;                               // units finished by the consumers (the signal thread reads it)
+    int sig_done;                          // the signal thread has counted every unit
+    int ncomb, ncomb_snap;                 // combines queued for the consumers, and their snapshot
+    int combq[kMaxRowBlocks];
+    uint64_t full[kMaxSlots], empty[kMaxSlots];
+};
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    if constexpr (F16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// 8 nibbles -> four 16-bit pairs of (OFF + q), elements (0,4), (1,5), (2,6), (3,7).
+template <bool F16>
+__device__ __forceinline__ void nib8(uint32_t u, uint32_t *r)
+{
+    constexpr uint32_t base = F16 ? 0x64006400u : 0x43004300u;
+    r[0] = (u & 0x000F000Fu) | base;
+    r[1] = ((u >> 4) & 0x000F000Fu) | base;
+    r[2] = ((u >> 8) & 0x000F000Fu) | base;
+    r[3] = ((u >> 12) & 0x000F000Fu) | base;
+}
+
+// 8 consecutive 16-bit values -> the codes' k order (0,4,1,5,2,6,3,7).
+__device__ __forceinline__ uint4 kperm8(uint4 v)
+{
+    uint4 o;
+    o.x = prmt(v.x, v.z, 0x5410u);
+    o.y = prmt(v.x, v.z, 0x7632u);
+    o.z = prmt(v.y, v.w, 0x5410u);
+    o.w = prmt(v.y, v.w, 0x7632u);
+    return o;
+}
+
+// Position of input i in the k order of its chunk of 8.
+__device__ __forceinline__ int kperm_pos(int i) { return (i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1); }
+
+// Byte offset, inside a row's 128-byte box, of the 8 code bytes that lane (g, t4) reads for group
+// grp: 16-byte chunk 2 (grp % 4) + t4 / 2 of row r (r % 8 == g), stored at chunk index (chunk ^ g).
+__device__ __forceinline__ uint32_t swz_chunk(int grp, int g, int t4)
+{
+    return (uint32_t)((((((grp & 3) << 1) | (t4 >> 1)) ^ g) << 4) | ((t4 & 1) << 3));
+}
+
+__device__ __forceinline__ uint32_t logit_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7FFFFFFFu) == 0) u = 0;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded poll (backoff) until *cnt >= target; false when the limit ran out.
+__device__ __forceinline__ bool poll_at_least(const int *cnt, int target, long long limit)
+{
+    long long n = 0;
+    unsigned ns = 32;
+    while (ld_acquire(cnt) < target) {
+        if (++n > limit) return false;
+        __nanosleep(ns);
+        ns = ns < 512 ? ns * 2 : 512;
+    }
+    return true;
+}
+
+// Shared-memory flag accesses with CTA-scope acquire / release.
+__device__ __forceinline__ int ld_acquire_cta(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_cta(int *p, int v)
+{
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Named barrier 1 over the consumer warps that also ORs a predicate (uniform stop decisions).
+__device__ __forceinline__ bool consumer_any(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ int col_token(int f, int T, int k) { return f < 0 ? -1 : (f >= T * k ? f - T * k : f / k); }
+
+// ------------------------------------------------------------------ phase 0 (all threads)
+//
+// x rows into shared memory in the codes' k order, their per-group sums, the routing
+// (top-k of the fp32 logits, or the caller's ids), the list of distinct experts and
+// their columns.
+__device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4 *s_x, float *s_sumx, int xs)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = a.T, H = a.H, E = a.E, k = a.k, G = H / kGroup, cpr = H / 8;
+    for (int i = tid; i < T * cpr; i += kSThreads) {
+        const int tt = i / cpr, col = i - tt * cpr;
+        cp_async16(smem_u32(s_x + tt * xs + col), reinterpret_cast<const uint4 *>(a.x + (size_t)tt * H) + col);
+    }
+    cp_async_commit();
+    if (a.ids_in) {
+        for (int i = tid; i < T * k; i += kSThreads) {
+            const int tt = i / k, j = i - tt * k;
+            int e = a.ids_in[i];
+            if (e < 0 || e >= E) {
+                record_status(a.status, MOE_ERR_DEVICE);
+                e = 0;
+            }
+            S.ids[tt][j] = e;
+            S.p[tt][j] = bf16_bits_to_float(a.p_in[i]);
+        }
+        for (int tt = tid; tt < T; tt += kSThreads)
+            S.ws[tt] = bf16_bits_to_float((a.has_shared && a.ws_in) ? a.ws_in[tt] : (uint16_t)0);
+    } else if (warp < kConsumerWarps) {
+        // one warp per token: lane l holds logits e = l + 32 r; k rounds of a warp max over
+        // (key, 0xFFFF - id) give the ids in rank order (equal logits: lower id first)
+        constexpr int RW = kMaxExperts / 32;
+        for (int tt = warp; tt < T; tt += kConsumerWarps) {
+            float val[RW];
+            uint32_t key[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int e = lane + 32 * r;
+                val[r] = e < E ? __ldg(a.logits + (size_t)tt * E + e) : 0.f;
+                key[r] = e < E ? logit_key(val[r]) : 0u;
+            }
+            unsigned taken = 0;
+            for (int j = 0; j < k; ++j) {
+                unsigned long long best = 0;
+#pragma unroll
+                for (int r = 0; r < RW; ++r) {
+                    const int e = lane + 32 * r;
+                    const unsigned long long c = ((unsigned long long)key[r] << 32) | (unsigned)(0xFFFF - e);
+                    if (e < E && !(taken & (1u << r)) && c > best) best = c;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+                    best = other > best ? other : best;
+                }
+                const int id = 0xFFFF - (int)(best & 0xFFFFu);
+                if ((id & 31) == lane) {
+                    taken |= 1u << (id >> 5);
+                    float v = 0.f;
+#pragma unroll
+                    for (int r = 0; r < RW; ++r)
+                        if ((id >> 5) == r) v = val[r];
+                    S.ids[tt][j] = id;
+                    S.lg[tt][j] = v;
+                }
+            }
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    for (int i = tid; i < T * cpr; i += kSThreads) {
+        const int tt = i / cpr, col = i - tt * cpr;
+        s_x[tt * xs + col] = kperm8(s_x[tt * xs + col]);   // each chunk read and written by one thread
+    }
+    if (blockIdx.x == 0 && !a.ids_in && a.ids_out)
+        for (int i = tid; i < T * k; i += kSThreads) a.ids_out[i] = S.ids[i / k][i % k];
+    __syncthreads();
+    // per-token sums of x over each group (fixed order; the bias term of the gate/up GEMV)
+    for (int i = tid; i < T * G; i += kSThreads) {
+        const int tt = i / G, grp = i - tt * G;
+        const uint4 *xr = s_x + tt * xs + grp * 8;
+        float s = 0.f;
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = xr[c];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                s += __uint_as_float(w4[q] << 16);
+                s += __uint_as_float(w4[q] & 0xFFFF0000u);
+            }
+        }
+        s_sumx[i] = s;
+    }
+    for (int i = tid; i < T * k; i += kSThreads) S.lpos[S.ids[i / k][i % k]] = 0;   // mark the used experts
+    __syncthreads();
+    // distinct experts in increasing id (lpos[e] = list position), then the shared expert
+    if (warp == 0) {
+        const int per = (E + 31) / 32, b0 = lane * per, b1 = min(E, b0 + per);
+        int local = 0;
+        for (int e = b0; e < b1; ++e) local += S.lpos[e] == 0;
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int pos = incl - local;
+        for (int e = b0; e < b1; ++e)
+            if (S.lpos[e] == 0) {
+                S.list[pos] = e;
+                S.lpos[e] = pos++;
+            }
+        if (lane == 31) {
+            S.nlist = incl + (a.has_shared ? 1 : 0);
+            if (a.has_shared) {
+                S.list[incl] = E;
+                S.ncols[incl] = T;
+            }
+        }
+    }
+    __syncthreads();
+    const int D = S.nlist;
+    for (int i = tid; i < T * k; i += kSThreads) atomicAdd(&S.ncols[S.lpos[S.ids[i / k][i % k]]], 1);
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (D + 31) / 32, b0 = lane * per, b1 = min(D, b0 + per);
+        int local = 0;
+        for (int d = b0; d < b1; ++d) local += S.ncols[d];
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int d = b0; d < b1; ++d) {
+            S.colptr[d] = run;
+            run += S.ncols[d];
+            if (S.ncols[d] > T) record_status(a.status, MOE_ERR_DEVICE);   // an id repeated within a token
+        }
+        if (lane == 31) S.colptr[D] = incl;
+    }
+    __syncthreads();
+    // columns of each expert: its slots (in no particular order: every column is computed on
+    // its own), the shared expert's in token order
+    for (int i = tid; i < T * k; i += kSThreads) {
+        const int d = S.lpos[S.ids[i / k][i % k]];
+        S.colf[S.colptr[d] + atomicAdd(&S.cfill[d], 1)] = i;
+    }
+    if (a.has_shared)
+        for (int tt = tid; tt < T; tt += kSThreads) S.colf[S.colptr[D - 1] + tt] = T * k + tt;
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ producer (one thread)
+__device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const FusedDecodeArgs &a,
+                                      const StreamGeom &geo, uint8_t *ring, int U1, int U)
+{
+    const int H = a.H, I = a.I, E = a.E, G = H / kGroup, GI = I / kGroup, R = geo.R;
+    const int RBI = I / kRows1, RBH = (H + kRows2 - 1) / kRows2;
+    prefetch_map(&maps.g);
+    prefetch_map(&maps.u);
+    prefetch_map(&maps.d);
+    if (a.has_shared) {
+        prefetch_map(&maps.sg);
+        prefetch_map(&maps.su);
+        prefetch_map(&maps.sd);
+    }
+    int issued = 0;
+    for (int w = blockIdx.x, i = 0; w < U; w += gridDim.x, ++i) {
+        const int slot = i % R;
+        if (i >= R && !mbar_wait_sleepy(smem_u32(&S.empty[slot]), ((i / R) - 1) & 1, a.wait_limit, &S.abort)) {
+            S.abort = 1;
+            record_status(a.status, MOE_ERR_TIMEOUT);
+            break;
+        }
+        uint8_t *base = ring + (size_t)slot * geo.slot;
+        const uint32_t fb = smem_u32(&S.full[slot]);
+        // this unit into the slot, and the unit one ring length ahead into L2
+        for (int pass = 0; pass < 2; ++pass) {
+            const int wu = pass == 0 ? w : w + R * (int)gridDim.x;
+            if (wu >= U) break;
+            if (wu < U1) {
+                const int d = wu / RBI, rb = wu - d * RBI, e = S.list[d];
+                const bool shr = e == E;
+                const int row0 = (shr ? 0 : e * I) + rb * kRows1;
+                const QMatDev &qg = shr ? a.s_gate : a.gate, &qu = shr ? a.s_up : a.up;
+                const size_t so = (size_t)row0 * G;
+                if (pass == 0) {
+                    const CUtensorMap *mg = shr ? &maps.sg : &maps.g, *mu = shr ? &maps.su : &maps.u;
+                    mbar_arrive_expect_tx(fb, geo.bytes1);
+                    for (int j = 0; j < geo.nb1; ++j) {
+                        tma_load_2d(smem_u32(base + j * kBox1), mg, j * 128, row0, fb);
+                        tma_load_2d(smem_u32(base + geo.up_off + j * kBox1), mu, j * 128, row0, fb);
+                    }
+                    bulk_load(smem_u32(base + geo.sc1_off), qg.scales + so, geo.sb1, fb);
+                    bulk_load(smem_u32(base + geo.sc1_off + geo.sb1), qg.biases + so, geo.sb1, fb);
+                    bulk_load(smem_u32(base + geo.sc1_off + 2 * geo.sb1), qu.scales + so, geo.sb1, fb);
+                    bulk_load(smem_u32(base + geo.sc1_off + 3 * geo.sb1), qu.biases + so, geo.sb1, fb);
+                } else {
+                    const uint32_t cb = (uint32_t)kRows1 * (H / 2);
+                    prefetch_l2_bulk(qg.codes + (size_t)row0 * (H / 2), cb);
+                    prefetch_l2_bulk(qu.codes + (size_t)row0 * (H / 2), cb);
+                    prefetch_l2_bulk(qg.scales + so, geo.sb1);
+                    prefetch_l2_bulk(qg.biases + so, geo.sb1);
+                    prefetch_l2_bulk(qu.scales + so, geo.sb1);
+                    prefetch_l2_bulk(qu.biases + so, geo.sb1);
+                }
+            } else {
+                const int v = wu - U1, d = v / RBH, rb = v - d * RBH, e = S.list[d];
+                const bool shr = e == E;
+                const int row0 = (shr ? 0 : e * H) + rb * kRows2;
+                const int nrows = min(kRows2, H - rb * kRows2);
+                const uint32_t sb2 = (uint32_t)nrows * GI * 2;
+                const QMatDev &qd = shr ? a.s_down : a.down;
+                const size_t so = (size_t)row0 * GI;
+                if (pass == 0) {
+                    const CUtensorMap *md = shr ? &maps.sd : &maps.d;
+                    mbar_arrive_expect_tx(fb, (uint32_t)geo.nb2 * kBox2 + 2 * sb2);
+                    for (int j = 0; j < geo.nb2; ++j) tma_load_2d(smem_u32(base + j * kBox2), md, j * 128, row0, fb);
+                    bulk_load(smem_u32(base + geo.sc2_off), qd.scales + so, sb2, fb);
+                    bulk_load(smem_u32(base + geo.sc2_off + kRows2 * GI * 2), qd.biases + so, sb2, fb);
+                } else {
+                    prefetch_l2_bulk(qd.codes + (size_t)row0 * (I / 2), (uint32_t)nrows * (I / 2));
+                    prefetch_l2_bulk(qd.scales + so, sb2);
+                    prefetch_l2_bulk(qd.biases + so, sb2);
+                }
+            }
+        }
+        issued = i + 1;
+    }
+    // every issued copy lands before the CTA may exit
+    for (int q = issued > R ? issued - R : 0; q < issued; ++q)
+        mbar_wait(smem_u32(&S.full[q % R]), (q / R) & 1, kDrainLimit, nullptr);
+}
+
+// ------------------------------------------------------------------ signal warp
+//
+// First, in the CTA assigned token grid - 1 - blockIdx, the token's pick weights p =
+// exp(l - l_top) / sum over the picks and w_s = sigmoid(bf16(gamma)) in fp64, one rounding
+// to bf16, published for the combining CTAs.  Then (lane 0) the completion signals of
+// this CTA's units.
+__device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U1, int U, int D)
+{
+    const int lane = threadIdx.x & 31, T = a.T, k = a.k, H = a.H, I = a.I;
+    const int RBI = I / kRows1, RBH = (H + kRows2 - 1) / kRows2;
+    const int tt = (int)gridDim.x - 1 - (int)blockIdx.x;
+    if (!a.ids_in && tt >= 0 && tt < T) {
+        double ex = 0.0;
+        if (lane < k) ex = exp((double)S.lg[tt][lane] - (double)S.lg[tt][0]);
+        double den = 0.0;
+        for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order j = 0..k-1
+        if (lane < k) {
+            const uint16_t pb = double_to_bf16_bits(ex / den);
+            a.p_glob[tt * k + lane] = pb;
+            if (a.p_out) a.p_out[tt * k + lane] = pb;
+        }
+        if (lane == 0) {
+            uint16_t wsb = 0;
+            if (a.has_shared) {
+                const float gb = bf16_bits_to_float(float_to_bf16_bits(a.gamma[tt]));
+                wsb = double_to_bf16_bits(1.0 / (1.0 + exp(-(double)gb)));
+            }
+            a.ws_glob[tt] = wsb;
+            if (a.ws_out) a.ws_out[tt] = wsb;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();
+            atomicAdd(a.cnt_pick, 1);
+        }
+    }
+    if (lane != 0) return;
+    // The consumers publish every finished unit in S.sig (release at CTA scope).  One fence
+    // makes a batch of units' global stores visible GPU-wide, then each unit is counted.
+    const int nmine = (int)blockIdx.x < U ? (U - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    int done = 0, nq = 0;
+    bool picks = a.ids_in != nullptr;       // given routing: S.p and S.ws were filled in phase 0
+    // the published pick weights into shared memory (once every token's are out), for the combines
+    auto take_picks = [&]() {
+#pragma unroll 8
+        for (int q = 0; q < T * k; ++q) S.p[q / k][q % k] = bf16_bits_to_float(__ldcg(a.p_glob + q));
+        for (int q = 0; q < T; ++q) S.ws[q] = bf16_bits_to_float(__ldcg(a.ws_glob + q));
+    };
+    long long polls = 0;
+    while (done < nmine) {
+        const int avail = ld_acquire_cta(&S.sig);
+        if (avail <= done) {
+            if (S.abort || ++polls > a.wait_limit) break;
+            if (!picks && ld_acquire(a.cnt_pick) >= T) {   // idle: fetch the pick weights ahead of any combine
+                take_picks();
+                picks = true;
+            }
+            __nanosleep(64);
+            continue;
+        }
+        polls = 0;
+        __threadfence();
+        for (; done < avail; ++done) {
+            const int w = (int)blockIdx.x + done * (int)gridDim.x;
+            if (w < U1) {
+                atomicAdd(a.cnt_expert + (w / RBI) * kCounterStride, 1);
+                continue;
+            }
+            const int rb = (w - U1) % RBH;
+            if (atomicAdd(a.cnt_rows + rb * kCounterStride, 1) != D - 1) continue;
+            __threadfence();                  // every unit's slot outputs, before the combine reads them
+            if (!picks) {
+                picks = poll_at_least(a.cnt_pick, T, a.wait_limit);
+                if (picks) take_picks();
+                else record_status(a.status, MOE_ERR_TIMEOUT);
+            }
+            if (picks && nq < kMaxRowBlocks) {
+                S.combq[nq] = rb;
+                st_release_cta(&S.ncomb, ++nq);
+            }
+        }
+    }
+    if (done < nmine) record_status(a.status, MOE_ERR_TIMEOUT);
+    st_release_cta(&S.sig_done, 1);
+}
+
+// ------------------------------------------------------------------ combine (consumer warps)
+//
+// Row block rb of y (or acc): sum over the token's slots in slot order, one rounding.  The
+// pick weights are in shared memory: the signal thread filled them before queueing the block.
+__device__ __noinline__ void combine_block(SSmem &S, const FusedDecodeArgs &a, int rb)
+{
+    const int tid = threadIdx.x, T = a.T, H = a.H, k = a.k;
+    const int nrow = min(kRows2, H - rb * kRows2);
+    for (int q = tid; q < nrow * T; q += kConsumers) {
+        const int tt = q / nrow, row = rb * kRows2 + (q - tt * nrow);
+        float ys[kMaxTopK + 1];                     // every load in flight before the first add
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) ys[j] = j < k ? __ldcg(a.yslot + ((size_t)tt * k + j) * H + row) : 0.f;
+        ys[kMaxTopK] = a.has_shared ? __ldcg(a.yslot + ((size_t)T * k + tt) * H + row) : 0.f;
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < k) s = fmaf(S.p[tt][j], ys[j], s);
+        if (a.has_shared) s = fmaf(S.ws[tt], ys[kMaxTopK], s);
+        if (a.y)
+            a.y[(size_t)tt * H + row] = float_to_bf16_bits(s);
+        else
+            a.acc[(size_t)tt * H + row] += s;
+    }
+    consumer_bar();
+}
+
+// ------------------------------------------------------------------ kernel
+template <int NT, int MINB>
+__global__ void __launch_bounds__(kSThreads, MINB)
+    decode_stream_kernel(const __grid_constant__ StreamMaps maps, const __grid_constant__ FusedDecodeArgs a,
+                         const __grid_constant__ StreamGeom geo)
+{
+    __shared__ SSmem S;
+    extern __shared__ uint8_t dyn_raw[];
+    uint8_t *dyn = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ring = dyn;
+    uint4 *s_x = reinterpret_cast<uint4 *>(dyn + geo.x_off);          // [T][x_stride] bf16 rows, k order
+    float *s_sumx = reinterpret_cast<float *>(dyn + geo.sumx_off);    // [T][G]
+    uint16_t *s_h = reinterpret_cast<uint16_t *>(dyn + geo.h_off);    // [NT * 8][h_stride] fp16 columns, k order
+    float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);      // [8][2][16][NT * 8]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+    const int T = a.T, H = a.H, I = a.I, k = a.k;
+    const int G = H / kGroup, GI = I / kGroup, xs = geo.x_stride, R = geo.R;
+    const long long limit = a.wait_limit;
+
+    if (tid == 0) {
+        for (int s = 0; s < R; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 1);
+            mbar_init(smem_u32(&S.empty[s]), kConsumers);
+        }
+        S.abort = 0;
+        S.sig = 0;
+        S.sig_done = 0;
+        S.ncomb = 0;
+        fence_mbar_init();
+    }
+    for (int e = tid; e < kMaxList; e += kSThreads) {
+        S.lpos[e] = -1;
+        S.ncols[e] = 0;
+        S.cfill[e] = 0;
+    }
+    phase0(S, a, s_x, s_sumx, xs);
+
+    const int D = S.nlist;
+    const int RBI = I / kRows1, RBH = (H + kRows2 - 1) / kRows2;
+    const int U1 = D * RBI, U = U1 + D * RBH;
+
+    if (warp == kWarpProd) {
+        if (lane == 0) producer(S, maps, a, geo, ring, U1, U);
+        return;
+    }
+    if (warp == kWarpSig) {
+        signaller(S, a, U1, U, D);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers (warps 0-7)
+    constexpr int NC = NT * 8;
+    const int gbeg = (warp * G) / kConsumerWarps, gend = ((warp + 1) * G) / kConsumerWarps;
+    int ncomb_done = 0;
+
+    for (int w = blockIdx.x, i = 0; w < U; w += gridDim.x, ++i) {
+        const int slot = i % R;
+        const bool got = mbar_wait(smem_u32(&S.full[slot]), (i / R) & 1, limit, &S.abort);
+        if (!got) {
+            S.abort = 1;
+            record_status(a.status, MOE_ERR_TIMEOUT);
+        }
+        if (tid == 0) S.ncomb_snap = ld_acquire_cta(&S.ncomb);
+        if (consumer_any(!got)) break;
+        for (const int snap = S.ncomb_snap; ncomb_done < snap; ++ncomb_done) combine_block(S, a, S.combq[ncomb_done]);
+        const uint8_t *base = ring + (size_t)slot * geo.slot;
+        const uint32_t eb = smem_u32(&S.empty[slot]);
+
+        if (w < U1) {
+            // ------------------------------------------------ gate/up unit: 16 rows, split-K over the warps
+            const int d = w / RBI, rb = w - d * RBI;
+            const int ncol = min(S.ncols[d], T);
+            const int *colf = S.colf + S.colptr[d];
+            int xrow[NT], tA[NT], tB[NT];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c = j * 8 + g, cA = j * 8 + 2 * t4;
+                xrow[j] = col_token(c < ncol ? colf[c] : -1, T, k);
+                tA[j] = col_token(cA < ncol ? colf[cA] : -1, T, k);
+                tB[j] = col_token(cA + 1 < ncol ? colf[cA + 1] : -1, T, k);
+            }
+            const uint16_t *gs = reinterpret_cast<const uint16_t *>(base + geo.sc1_off) + g * G;
+            const uint16_t *gbi = gs + kRows1 * G, *us = gbi + kRows1 * G, *ubi = us + kRows1 * G;
+            const uint8_t *cb = base + g * 128;          // row g of box 0; row g + 8 is 1024 bytes further
+            float acc_g[NT][4], acc_u[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc_g[j][q] = acc_u[j][q] = 0.f;
+#pragma unroll 1
+            for (int grp = gbeg; grp < gend; ++grp) {
+                const uint32_t o = (uint32_t)(grp >> 2) * kBox1 + swz_chunk(grp, g, t4);
+                const uint2 cg0 = *reinterpret_cast<const uint2 *>(cb + o);
+                const uint2 cg1 = *reinterpret_cast<const uint2 *>(cb + o + 1024);
+                const uint2 cu0 = *reinterpret_cast<const uint2 *>(cb + geo.up_off + o);
+                const uint2 cu1 = *reinterpret_cast<const uint2 *>(cb + geo.up_off + o + 1024);
+                const float s_g0 = bf16_bits_to_float(gs[grp]), s_g1 = bf16_bits_to_float(gs[8 * G + grp]);
+                const float s_u0 = bf16_bits_to_float(us[grp]), s_u1 = bf16_bits_to_float(us[8 * G + grp]);
+                const float c_g0 = fmaf(-128.f, s_g0, bf16_bits_to_float(gbi[grp]));
+                const float c_g1 = fmaf(-128.f, s_g1, bf16_bits_to_float(gbi[8 * G + grp]));
+                const float c_u0 = fmaf(-128.f, s_u0, bf16_bits_to_float(ubi[grp]));
+                const float c_u1 = fmaf(-128.f, s_u1, bf16_bits_to_float(ubi[8 * G + grp]));
+                uint32_t ag[2][8], au[2][8];
+                nib8<false>(cg0.x, ag[0]);
+                nib8<false>(cg0.y, ag[0] + 4);
+                nib8<false>(cg1.x, ag[1]);
+                nib8<false>(cg1.y, ag[1] + 4);
+                nib8<false>(cu0.x, au[0]);
+                nib8<false>(cu0.y, au[0] + 4);
+                nib8<false>(cu1.x, au[1]);
+                nib8<false>(cu1.y, au[1] + 4);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    if (j * 8 >= ncol) break;
+                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                    if (xrow[j] >= 0) {
+                        const uint4 *xr = s_x + xrow[j] * xs + grp * 8 + 2 * t4;
+                        lo = xr[0];
+                        hi = xr[1];
+                    }
+                    const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        mma16816<false>(dg, ag[0][2 * m], ag[1][2 * m], ag[0][2 * m + 1], ag[1][2 * m + 1], bp[2 * m],
+                                        bp[2 * m + 1]);
+                        mma16816<false>(du, au[0][2 * m], au[1][2 * m], au[0][2 * m + 1], au[1][2 * m + 1], bp[2 * m],
+                                        bp[2 * m + 1]);
+                    }
+                    const float sxA = tA[j] >= 0 ? s_sumx[tA[j] * G + grp] : 0.f;
+                    const float sxB = tB[j] >= 0 ? s_sumx[tB[j] * G + grp] : 0.f;
+                    acc_g[j][0] = fmaf(s_g0, dg[0], fmaf(c_g0, sxA, acc_g[j][0]));
+                    acc_g[j][1] = fmaf(s_g0, dg[1], fmaf(c_g0, sxB, acc_g[j][1]));
+                    acc_g[j][2] = fmaf(s_g1, dg[2], fmaf(c_g1, sxA, acc_g[j][2]));
+                    acc_g[j][3] = fmaf(s_g1, dg[3], fmaf(c_g1, sxB, acc_g[j][3]));
+                    acc_u[j][0] = fmaf(s_u0, du[0], fmaf(c_u0, sxA, acc_u[j][0]));
+                    acc_u[j][1] = fmaf(s_u0, du[1], fmaf(c_u0, sxB, acc_u[j][1]));
+                    acc_u[j][2] = fmaf(s_u1, du[2], fmaf(c_u1, sxA, acc_u[j][2]));
+                    acc_u[j][3] = fmaf(s_u1, du[3], fmaf(c_u1, sxB, acc_u[j][3]));
+                }
+            }
+            mbar_arrive_after(eb, acc_g[0][0], acc_g[0][2], acc_u[0][0], acc_u[0][2]);
+            float *rg = s_red + (warp * 2 + 0) * 16 * NC, *ru = rg + 16 * NC;
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c0 = j * 8 + 2 * t4;
+                rg[g * NC + c0] = acc_g[j][0];
+                rg[g * NC + c0 + 1] = acc_g[j][1];
+                rg[(g + 8) * NC + c0] = acc_g[j][2];
+                rg[(g + 8) * NC + c0 + 1] = acc_g[j][3];
+                ru[g * NC + c0] = acc_u[j][0];
+                ru[g * NC + c0 + 1] = acc_u[j][1];
+                ru[(g + 8) * NC + c0] = acc_u[j][2];
+                ru[(g + 8) * NC + c0 + 1] = acc_u[j][3];
+            }
+            consumer_bar();
+            {
+                const int row = tid & 15, c = tid >> 4;   // 256 threads = 16 rows x 16 columns
+                if (c < ncol) {
+                    float gsum = 0.f, usum = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < kConsumerWarps; ++ww) {
+                        gsum += s_red[((ww * 2 + 0) * 16 + row) * NC + c];
+                        usum += s_red[((ww * 2 + 1) * 16 + row) * NC + c];
+                    }
+                    const float hv = gsum / (1.f + __expf(-gsum)) * usum;
+                    // h in the codes' k order: the down unit's fragments are plain loads
+                    a.h[(size_t)colf[c] * I + kperm_pos(rb * kRows1 + row)] = __half_as_ushort(__float2half_rn(hv));
+                }
+            }
+            consumer_bar();
+            if (tid == 0) st_release_cta(&S.sig, i + 1);
+        } else {
+            // ------------------------------------------------ down unit: 128 rows, warp w rows 16 w .. 16 w + 15
+            const int v = w - U1, d = v / RBH, rb = v - d * RBH;
+            const int ncol = min(S.ncols[d], T);
+            const int *colf = S.colf + S.colptr[d];
+            if (tid == 0) {
+                const bool ok = poll_at_least(a.cnt_expert + d * kCounterStride, RBI, limit);
+                if (!ok) {
+                    S.abort = 1;
+                    record_status(a.status, MOE_ERR_TIMEOUT);
+                }
+                S.ready = ok;
+            }
+            consumer_bar();
+            if (!S.ready) {
+                mbar_arrive(eb);
+                break;
+            }
+            // the expert's h columns into shared memory (L2 reads, after the acquire above)
+            for (int idx = tid, cpr = I / 8; idx < ncol * cpr; idx += kConsumers) {
+                const int c = idx / cpr, ch = idx - c * cpr;
+                *reinterpret_cast<uint4 *>(s_h + c * geo.h_stride + ch * 8) =
+                    __ldcg(reinterpret_cast<const uint4 *>(a.h + (size_t)colf[c] * I) + ch);
+            }
+            consumer_bar();
+            const int r0 = warp * 16 + g;                        // rows r0 and r0 + 8 of the unit
+            const bool wactive = rb * kRows2 + warp * 16 < H;   // H is a multiple of 64: warps are all in or out
+            const uint16_t *dsc = reinterpret_cast<const uint16_t *>(base + geo.sc2_off) + r0 * GI;
+            const uint16_t *dbi = dsc + kRows2 * GI;
+            const uint8_t *cb = base + r0 * 128;
+            float acc[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+            if (wactive) {
+#pragma unroll 1
+                for (int grp = 0; grp < GI; ++grp) {
+                    const uint32_t o = (uint32_t)(grp >> 2) * kBox2 + swz_chunk(grp, g, t4);
+                    const uint2 c0 = *reinterpret_cast<const uint2 *>(cb + o);
+                    const uint2 c1 = *reinterpret_cast<const uint2 *>(cb + o + 1024);
+                    const float s0 = bf16_bits_to_float(dsc[grp]), s1 = bf16_bits_to_float(dsc[8 * GI + grp]);
+                    const float k0 = fmaf(-1024.f, s0, bf16_bits_to_float(dbi[grp]));
+                    const float k1 = fmaf(-1024.f, s1, bf16_bits_to_float(dbi[8 * GI + grp]));
+                    uint32_t ad[2][8];
+                    nib8<true>(c0.x, ad[0]);
+                    nib8<true>(c0.y, ad[0] + 4);
+                    nib8<true>(c1.x, ad[1]);
+                    nib8<true>(c1.y, ad[1] + 4);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        if (j * 8 >= ncol) break;
+                        const int c = j * 8 + g;
+                        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                        if (c < ncol) {
+                            const uint4 *hr = reinterpret_cast<const uint4 *>(s_h + c * geo.h_stride + grp * 64 + 16 * t4);
+                            lo = hr[0];
+                            hi = hr[1];
+                        }
+                        const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                        constexpr uint32_t ones = 0x3C003C00u;
+                        float dd[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            mma16816<true>(dd, ad[0][2 * m], ad[1][2 * m], ad[0][2 * m + 1], ad[1][2 * m + 1], bp[2 * m],
+                                           bp[2 * m + 1]);
+                            mma16816<true>(dx, ones, ones, ones, ones, bp[2 * m], bp[2 * m + 1]);
+                        }
+                        acc[j][0] = fmaf(s0, dd[0], fmaf(k0, dx[0], acc[j][0]));
+                        acc[j][1] = fmaf(s0, dd[1], fmaf(k0, dx[1], acc[j][1]));
+                        acc[j][2] = fmaf(s1, dd[2], fmaf(k1, dx[2], acc[j][2]));
+                        acc[j][3] = fmaf(s1, dd[3], fmaf(k1, dx[3], acc[j][3]));
+                    }
+                }
+            }
+            mbar_arrive_after(eb, acc[0][0], acc[0][2], acc[0][1], acc[0][3]);
+            if (wactive) {
+                const int w0 = rb * kRows2 + r0, w1 = w0 + 8;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const int cA = j * 8 + 2 * t4, cB = cA + 1;
+                    if (cA < ncol) {
+                        const int f = colf[cA];
+                        a.yslot[(size_t)f * H + w0] = acc[j][0];
+                        a.yslot[(size_t)f * H + w1] = acc[j][2];
+                    }
+                    if (cB < ncol) {
+                        const int f = colf[cB];
+                        a.yslot[(size_t)f * H + w0] = acc[j][1];
+                        a.yslot[(size_t)f * H + w1] = acc[j][3];
+                    }
+                }
+            }
+            consumer_bar();
+            if (tid == 0) st_release_cta(&S.sig, i + 1);
+        }
+    }
+    // the remaining combines of this CTA, each as soon as the signal thread queues it, until it has
+    // counted every unit (bounded)
+    for (long long polls = 0;; ++polls) {
+        if (tid == 0) {
+            const int done = ld_acquire_cta(&S.sig_done);
+            S.ncomb_snap = ld_acquire_cta(&S.ncomb);
+            S.ready = done || polls > limit;
+            if (!done && polls > limit) record_status(a.status, MOE_ERR_TIMEOUT);
+        }
+        consumer_bar();
+        const bool last = S.ready;
+        for (const int snap = S.ncomb_snap; ncomb_done < snap; ++ncomb_done) combine_block(S, a, S.combq[ncomb_done]);
+        if (last) break;
+        if (tid == 0) __nanosleep(64);
+        consumer_bar();
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+// The ring layout needs 128-byte code boxes: H and I multiples of 256.
+bool stream_geometry(int T, int H, int I, size_t smem_budget, StreamGeom *out)
+{
+    if (T < 1 || T > kDecodeMaxTok || H % 256 || I % 256 || H > 8192) return false;
+    StreamGeom g{};
+    const int G = H / kGroup, GI = I / kGroup, NT = T > 8 ? 2 : 1;
+    g.nb1 = H / 256;
+    g.up_off = (uint32_t)g.nb1 * kBox1;
+    g.sc1_off = 2 * g.up_off;
+    g.sb1 = (uint32_t)kRows1 * G * 2;
+    g.bytes1 = 2 * g.up_off + 4 * g.sb1;
+    const uint32_t size1 = g.sc1_off + 4 * g.sb1;
+    g.nb2 = I / 256;
+    g.sc2_off = (uint32_t)g.nb2 * kBox2;
+    const uint32_t size2 = g.sc2_off + 2u * kRows2 * GI * 2;
+    g.slot = (uint32_t)align_up(size1 > size2 ? size1 : size2, 1024);
+    g.x_stride = H / 8 + 1;
+    g.h_stride = I + 8;
+    const size_t xb = (size_t)T * g.x_stride * 16, sumb = (size_t)T * G * 4;
+    const size_t hb = (size_t)NT * 8 * g.h_stride * 2, redb = (size_t)kConsumerWarps * 2 * 16 * NT * 8 * 4;
+    const size_t fixed = align_up(xb, 16) + align_up(sumb, 16) + align_up(hb, 16) + redb + 1024;
+    const size_t budget = smem_budget - sizeof(SSmem) - 256;
+    if (budget <= fixed) return false;
+    size_t R = (budget - fixed) / g.slot;
+    if (R > kMaxSlots) R = kMaxSlots;
+    if (R < 2) return false;
+    g.R = (int)R;
+    size_t o = R * g.slot;
+    g.x_off = (uint32_t)o;
+    o += align_up(xb, 16);
+    g.sumx_off = (uint32_t)o;
+    o += align_up(sumb, 16);
+    g.h_off = (uint32_t)o;
+    o += align_up(hb, 16);
+    g.red_off = (uint32_t)o;
+    o += redb;
+    g.dyn = (uint32_t)(o + 1024);      // slack for aligning the base to 1024 bytes
+    *out = g;
+    return true;
+}
+
+int dev_attr(int dev, cudaDeviceAttr attr, int slot)
+{
+    static int v[16][3] = {};
+    int &r = v[dev & 15][slot];
+    if (!r) cudaDeviceGetAttribute(&r, attr, dev);
+    return r;
+}
+int optin_smem(int dev) { return dev_attr(dev, cudaDevAttrMaxSharedMemoryPerBlockOptin, 0); }
+int sm_smem(int dev) { return dev_attr(dev, cudaDevAttrMaxSharedMemoryPerMultiprocessor, 1); }
+int sm_count(int dev) { return dev_attr(dev, cudaDevAttrMultiProcessorCount, 2); }
+
+// CTAs per SM and the matching geometry: two per SM when T <= 2 and half of the SM's
+// shared memory still holds a ring of two slots (twice the warps on the few units
+// of a one- or two-token batch), else one.
+bool plan_launch(int T, int H, int I, int dev, StreamGeom *geo, int *per_sm)
+{
+    const size_t reserved = 1024;                  // per CTA, kept by the runtime
+    if (T <= 2 && stream_geometry(T, H, I, (size_t)sm_smem(dev) / 2 - reserved, geo)) {
+        *per_sm = 2;
+        return true;
+    }
+    *per_sm = 1;
+    return stream_geometry(T, H, I, (size_t)optin_smem(dev), geo);
+}
+
+bool code_map(CUtensorMap *m, const uint8_t *codes, int row_bytes, uint64_t rows, int box_rows)
+{
+    return make_map_2d(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)row_bytes, rows, 128u, (uint32_t)box_rows,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+bool decode_stream_fits(int T, int H, int I)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    StreamGeom g;
+    int per_sm = 0;
+    return plan_launch(T, H, I, dev, &g, &per_sm);
+}
+
+cudaError_t launch_decode_stream(const FusedDecodeArgs &a, cudaStream_t st)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    StreamGeom geo;
+    int want = 1;
+    if (!plan_launch(a.T, a.H, a.I, dev, &geo, &want)) return cudaErrorInvalidValue;
+    StreamMaps maps;
+    const uint64_t E = (uint64_t)a.E;
+    bool ok = code_map(&maps.g, a.gate.codes, a.H / 2, E * a.I, kRows1) &&
+              code_map(&maps.u, a.up.codes, a.H / 2, E * a.I, kRows1) &&
+              code_map(&maps.d, a.down.codes, a.I / 2, E * a.H, kRows2);
+    if (ok && a.has_shared)
+        ok = code_map(&maps.sg, a.s_gate.codes, a.H / 2, a.I, kRows1) &&
+             code_map(&maps.su, a.s_up.codes, a.H / 2, a.I, kRows1) &&
+             code_map(&maps.sd, a.s_down.codes, a.I / 2, a.H, kRows2);
+    else if (ok) {
+        maps.sg = maps.g;
+        maps.su = maps.u;
+        maps.sd = maps.d;
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    auto kern = a.T > 8 ? decode_stream_kernel<2, 1> : (want == 2 ? decode_stream_kernel<1, 2> : decode_stream_kernel<1, 1>);
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.dyn)) != cudaSuccess)
+        return e;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, geo.dyn)) != cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sm_count(dev) * (per_sm < want ? per_sm : want));
+    cfg.blockDim = dim3(kSThreads);
+    cfg.dynamicSmemBytes = geo.dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, maps, a, geo);
+}
+
+}  // namespace qmoe

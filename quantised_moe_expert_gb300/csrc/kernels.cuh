@@ -141,7 +141,7 @@ struct FusedDecodeArgs {
     float *acc;                   // f32 [T, H] += sum (when y is null)
     int *cnt_expert;              // [(E + 1) * 32] gate/up units done per expert-list entry, stride 32 (zeroed before launch)
     int *cnt_rows;                // [(H / 128) * 32] down units done per 128-row block, stride 32 (zeroed before launch)
-    int *cnt_pick;                // CTAs that published pick weights (zeroed before launch)
+    int *cnt_pick;                // tokens whose pick weights are published (zeroed before launch)
     uint16_t *p_glob;             // bf16 [T, k] published pick weights
     uint16_t *ws_glob;            // bf16 [T] published shared weights
     int *status;
@@ -149,7 +149,10 @@ struct FusedDecodeArgs {
     long long wait_limit;
 };
 
-cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t st);
+// Streaming decode kernel (T <= 16): whether the layer shape fits its shared-memory
+// ring on the current device, and the cooperative launch (one CTA per SM).
+bool decode_stream_fits(int T, int H, int I);
+cudaError_t launch_decode_stream(const FusedDecodeArgs &a, cudaStream_t st);
 cudaError_t launch_route_gemv(const RouteArgs &a, cudaStream_t st);
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t st);
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t st);

@@ -388,7 +388,7 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     wa.max_items[1] = L.max_w1;
     wa.max_items[2] = L.max_w2;
     const int rp = resolve_path(path, T);
-    const bool fused = rp == MOE_PATH_DECODE && T <= kDecodeMaxTok;
+    const bool fused = rp == MOE_PATH_DECODE && T <= kDecodeMaxTok && decode_stream_fits(T, cfg->hidden, cfg->inter);
     if (fused) {
         wa.zero = ws_at<int>(ws, L.counters);
         wa.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128 + 1);
@@ -400,7 +400,7 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
         fa.p_in = p;
         fa.ws_in = w_shared;
         fa.acc = acc;
-        return cuda_rc(launch_decode_fused(fa, st));
+        return cuda_rc(launch_decode_stream(fa, st));
     }
     ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_shared, offsets, perm, acc, L, ws);
     if (rp == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, nullptr, st);
@@ -433,7 +433,7 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
     if (T == 0) return MOE_OK;
     const int rp = resolve_path(path, T);
     auto st = static_cast<cudaStream_t>(stream);
-    if (rp == MOE_PATH_DECODE && T <= kDecodeMaxTok) {
+    if (rp == MOE_PATH_DECODE && T <= kDecodeMaxTok && decode_stream_fits(T, cfg->hidden, cfg->inter)) {
         // router GEMV (zeroing the counters), then one cooperative launch for the rest of the layer
         float *lg = logits_in ? const_cast<float *>(logits_in) : ws_at<float>(ws, L.logits);
         RouteArgs ra = route_args(*cfg, *w, x, T, router_bias, logits_in, lg, L, ws);
@@ -447,7 +447,7 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
         fa.p_out = p_out;
         fa.ws_out = w_shared_out;
         fa.y = y;
-        return cuda_rc(launch_decode_fused(fa, st));
+        return cuda_rc(launch_decode_stream(fa, st));
     }
     int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.ids);
     uint16_t *p = p_out ? p_out : ws_at<uint16_t>(ws, L.p);

@@ -37,12 +37,11 @@
 //
 // Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT, the
 // CTA drains its in-flight copies and MMAs, frees its TMEM and returns.
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 
 #include "kernels.cuh"
 #include "tc_ptx.cuh"
+#include "tma_host.cuh"
 
 namespace qmoe {
 namespace {
@@ -149,9 +148,6 @@ __device__ __forceinline__ void stage_scales(uint16_t *dst, const uint16_t *cons
 #pragma unroll
         for (int g = 0; g < kScaleChunk; ++g) dst[(a * kScaleChunk + g) * 128 + r] = v[a][g];
 }
-
-// Named barrier of the four dequantising warps (threads 0..127).
-__device__ __forceinline__ void dequant_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Named barrier `id` over `count` threads that also ORs a predicate: every
 // participant gets the same answer, so a group of warps stops together.
@@ -748,35 +744,6 @@ __global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict_
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 2D row-major map: inner extent `cols` elements, `rows` rows, box {bc, br}.
-bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, uint64_t cols, uint64_t rows,
-              uint32_t bc, uint32_t br, CUtensorMapSwizzle swz)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * (uint64_t)esize};
-    cuuint32_t box[2] = {bc, br};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 size_t g1_smem()
 {
     return 1024 + kStagesA1 * 32768 + kStagesB1 * 16384 + kCodeStages1 * 8192 + 4 * kScaleChunk * 128 * 2 +
@@ -818,14 +785,14 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE, sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int ns = a.has_shared ? 1 : 0;
-    bool ok = make_map(&mgc, a.gate.codes, u8, 1, H / 2, (uint64_t)E * I, 32, 128, none) &&
-              make_map(&muc, a.up.codes, u8, 1, H / 2, (uint64_t)E * I, 32, 128, none) &&
-              make_map(&mdc, a.down.codes, u8, 1, I / 2, (uint64_t)E * H, 32, 128, none) &&
-              make_map(&mh, a.hs, f16, 2, I, (uint64_t)T * k + (uint64_t)T, 64, 32, sw128);
+    bool ok = make_map_2d(&mgc, a.gate.codes, u8, 1, H / 2, (uint64_t)E * I, 32, 128, none) &&
+              make_map_2d(&muc, a.up.codes, u8, 1, H / 2, (uint64_t)E * I, 32, 128, none) &&
+              make_map_2d(&mdc, a.down.codes, u8, 1, I / 2, (uint64_t)E * H, 32, 128, none) &&
+              make_map_2d(&mh, a.hs, f16, 2, I, (uint64_t)T * k + (uint64_t)T, 64, 32, sw128);
     if (ns)
-        ok = ok && make_map(&msgc, a.s_gate.codes, u8, 1, H / 2, I, 32, 128, none) &&
-             make_map(&msuc, a.s_up.codes, u8, 1, H / 2, I, 32, 128, none) &&
-             make_map(&msdc, a.s_down.codes, u8, 1, I / 2, H, 32, 128, none);
+        ok = ok && make_map_2d(&msgc, a.s_gate.codes, u8, 1, H / 2, I, 32, 128, none) &&
+             make_map_2d(&msuc, a.s_up.codes, u8, 1, H / 2, I, 32, 128, none) &&
+             make_map_2d(&msdc, a.s_down.codes, u8, 1, I / 2, H, 32, 128, none);
     else {
         msgc = mgc;
         msuc = muc;

@@ -75,6 +75,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
     }
 }
 
+// The same wait for a thread whose wait does not hold up others' work (a producer
+// waiting for a free slot): the polls are spaced by a short sleep, so the waiting
+// thread takes neither issue slots nor shared-memory bandwidth from the SM.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, long long limit, volatile int *abort)
+{
+    if (mbar_test(bar, parity)) return true;
+    for (long long i = 1;; ++i) {
+        if (i >= limit || (abort != nullptr && *abort)) return false;
+        __nanosleep(128);
+        if (mbar_test(bar, parity)) return true;
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
@@ -84,6 +97,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "[%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Contiguous global -> shared copy (async proxy); size and both addresses multiples of 16 bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Asks L2 to fetch a contiguous range (16-byte aligned address and size); no completion signal.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Arrive on `bar` only once the four values are available: they are computed
+// from every shared-memory word the thread read from a ring slot, so the slot
+// cannot be refilled while one of those reads is still in flight.
+__device__ __forceinline__ void mbar_arrive_after(uint32_t bar, float v0, float v1, float v2, float v3)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar), "f"(v0), "f"(v1),
+                 "f"(v2), "f"(v3)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map)
