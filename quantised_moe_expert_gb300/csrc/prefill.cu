@@ -51,17 +51,18 @@ using namespace tc;
 // Stage counts of the three rings of each GEMM: dequantised weights (A), token
 // operand (B) and int4 code tiles.  B runs deepest: its loads come from L2 /
 // HBM with a latency of several K-steps of MMA.
-constexpr int kStagesA1 = 2, kStagesB1 = 5, kCodeStages1 = 4;   // gate/up: 32 KB, 16 KB, 8 KB per stage
+constexpr int kStagesA1 = 4, kStagesB1 = 6, kCodeStages1 = 6;   // gate/up: A in TMEM (64 columns), 16 KB, 8 KB per stage
 constexpr int kStagesA2 = 3, kStagesB2 = 4, kCodeStages2 = 6;   // down:    16 KB, 32 KB, 4 KB per stage
 constexpr int kLoaderLag = kStagesB1 - 2;                       // token-row groups in flight beyond the newest
 // Warp roles (both GEMMs): 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue; the
 // gate/up GEMM adds warp 14, the token-row loader.
 constexpr int kDequantThreads = 256;
-constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10, kWarpLoader = 14;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10, kWarpLoader = 14, kLoaderWarps = 4;
 constexpr int kThreads = 448;       // down GEMM
-constexpr int kThreads1 = 480;      // gate/up GEMM
+constexpr int kThreads1 = 576;      // gate/up GEMM
 constexpr int kScaleChunk = 16;     // groups of scales staged in shared memory at a time
 constexpr long long kDrainLimit = 1ll << 22;
+constexpr uint32_t kTmemA1 = 256;   // gate/up GEMM: accumulators in TMEM columns [0, 256), A stages from 256
 
 struct G1Params {
     const int32_t *nwork;
@@ -70,6 +71,7 @@ struct G1Params {
     const int32_t *perm;
     uint16_t *hs;                      // fp16 [T*k + T, I] (K-permuted), expert-sorted rows
     const uint16_t *x16;               // fp16 [T, H] (K-permuted)
+    const uint8_t *gc, *uc, *sgc, *suc;    // int4 codes (routed [E, I, H/2], shared [I, H/2]), for L2 prefetch
     const uint16_t *gs, *gb, *us, *ub;     // routed gate/up scales, biases [E, I, H/64]
     const uint16_t *sgs, *sgb, *sus, *sub; // shared expert [I, H/64]
     int *status;
@@ -85,6 +87,7 @@ struct G2Params {
     const uint16_t *p;                 // bf16 [T, k]
     const uint16_t *w_s;               // bf16 [T]
     float *acc;                        // f32 [T, H]
+    const uint8_t *dc, *sdc;           // int4 codes (routed [E, H, I/2], shared [H, I/2]), for L2 prefetch
     const uint16_t *ds, *db;           // routed down scales, biases [E, H, I/64]
     const uint16_t *sds, *sdb;         // shared [H, I/64]
     int *status;
@@ -182,14 +185,23 @@ __device__ __forceinline__ TileInfo tile_info(const WorkItem *work, const int32_
     return ti;
 }
 
+// Asks L2 for `bytes` contiguous bytes in 32 KB pieces (16-byte multiples, 16-byte aligned).
+__device__ __forceinline__ void prefetch_rows(const void *p, uint32_t bytes)
+{
+    const uint8_t *b = static_cast<const uint8_t *>(p);
+    for (uint32_t off = 0; off < bytes; off += 32768u) prefetch_l2_bulk(b + off, bytes - off < 32768u ? bytes - off : 32768u);
+}
+
 // --------------------------------------------------------------- gate/up GEMM
 //
 // Persistent: one CTA per SM loops over tiles tau = blockIdx.x + i * gridDim.x.
-// Roles: warps 0-3 dequantise the code tiles; warp 4 (one thread) streams code
-// tiles with TMA through a ring of CS stages; warp 5 (one thread) issues the
-// MMAs; warps 6-9 run the epilogue of the previous tile from the other TMEM
-// buffer while the next tile's MMAs accumulate; warp 10 gathers the token rows
-// of x with cp.async, up to S - 1 K-steps ahead.
+// Roles: warps 0-7 dequantise the code tiles (0-3 gate rows, 4-7 up rows) into A
+// stages in tensor memory; warp 8 (one thread) streams code tiles with TMA through a
+// ring of CS stages and asks L2 for the next tile in bulk; warp 9 (one thread)
+// issues the MMAs (A from tensor memory, B from shared memory); warps 10-13 run the
+// epilogue; warps 14-17 gather the token rows of x with cp.async, SB - 2 steps ahead.
+// Tensor memory: gate and up accumulators in columns [0, 256) (one buffer, so a tile's
+// first MMAs wait for the previous epilogue's reads), A stages from column 256.
 template <int S, int SB, int CS>
 __global__ void __launch_bounds__(kThreads1, 1)
     gemm_gateup_kernel(const __grid_constant__ CUtensorMap map_gc, const __grid_constant__ CUtensorMap map_uc,
@@ -201,17 +213,14 @@ __global__ void __launch_bounds__(kThreads1, 1)
     if ((int)blockIdx.x >= ntiles) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA_g = smem;                         // S x 16 KB
-    uint8_t *sA_u = sA_g + S * 16384;             // S x 16 KB
-    uint8_t *sB = sA_u + S * 16384;               // SB x 16 KB (128 token rows x 128 B)
+    uint8_t *sB = smem;                           // SB x 16 KB (128 token rows x 128 B)
     uint8_t *sC = sB + SB * 16384;                // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [4][kScaleChunk][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 4 * kScaleChunk * 128);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
-    int *s_rows = reinterpret_cast<int *>(drain + 1);     // [2][128], written and read by the loader warp
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_rows + 256);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -222,20 +231,18 @@ __global__ void __launch_bounds__(kThreads1, 1)
     if (tid == 0) {
         for (int s = 0; s < CS; ++s) {
             mbar_init(smem_u32(cfull + s), 1);
-            mbar_init(smem_u32(cempty + s), kDequantThreads);
+            mbar_init(smem_u32(cempty + s), 1);
         }
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(afull + s), kDequantThreads);
+            mbar_init(smem_u32(afull + s), 1);
             mbar_init(smem_u32(aempty + s), 1);
         }
         for (int s = 0; s < SB; ++s) {
-            mbar_init(smem_u32(bfull + s), 32);
+            mbar_init(smem_u32(bfull + s), 32 * kLoaderWarps);
             mbar_init(smem_u32(bempty + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(tfull + b), 1);
-            mbar_init(smem_u32(tempty + b), 128);
-        }
+        mbar_init(smem_u32(tfull), 1);
+        mbar_init(smem_u32(tempty), 128);
         mbar_init(smem_u32(drain), 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -246,32 +253,30 @@ __global__ void __launch_bounds__(kThreads1, 1)
     const uint32_t tmem = *s_tmem;
     const long long limit = P.wait_limit;
 
-    if (warp == kWarpLoader) {
+    if (warp >= kWarpLoader) {
         // ------------------------------------------------ token rows of x (cp.async gather)
-        // Runs ahead of the dequant warps, bounded only by free B stages: step q's rows go
-        // into stage q % SB once the MMAs of step q - SB are done; the arrive for step q is
-        // made when its copies have landed, kLoaderLag steps later.
-        int q = 0, i = 0, done = 0;                           // steps [done, q) issued, not yet arrived
+        // Four loader warps, one token row of the tile per lane.  They run ahead of the
+        // dequant warps, bounded only by free B stages: step q's rows go into stage q % SB
+        // once the MMAs of step q - SB are done; a lane's arrive for step q is made when its
+        // copies have landed, kLoaderLag steps later.
+        const int n = (warp - kWarpLoader) * 32 + lane;      // row of the B tile
+        int q = 0, done = 0;                                  // steps [done, q) issued, not yet arrived
         bool ok = true;
-        for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x, ++i) {
+        for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
-            int *rows = s_rows + (i & 1) * 128;
-            for (int n = lane; n < 128; n += 32) {
-                int row = 0;                                  // rows past ntok are never read
-                if (n < ti.ntok) {
-                    if (ti.shared_e) {
-                        row = ti.tok0 + n;
-                    } else {
-                        const int pos = ti.pbase + n;
-                        const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
-                        if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
-                        else row = f / P.k;
-                    }
+            const uint16_t *src = nullptr;                    // rows past ntok are never read
+            if (n < ti.ntok) {
+                int row = -1;
+                if (ti.shared_e) {
+                    row = ti.tok0 + n;
+                } else {
+                    const int pos = ti.pbase + n;
+                    const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                    if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
+                    else row = f / P.k;
                 }
-                rows[n] = row;
+                if (row >= 0) src = P.x16 + (size_t)row * H;
             }
-            __syncwarp();
-            const int nchunks = ti.ntok * 8;
             for (int s = 0; s < nk; ++s, ++q) {
                 const int st = q % SB;
                 if (q >= SB && !mbar_wait(smem_u32(bempty + st), (q / SB - 1) & 1, limit, s_abort)) {
@@ -279,10 +284,10 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     ok = false;
                     break;
                 }
-                uint8_t *dst = sB + st * 16384;
-                for (int idx = lane; idx < nchunks; idx += 32) {
-                    const int n = idx >> 3, c = idx & 7;
-                    cp_async16(smem_u32(dst + swz128(n, c)), P.x16 + (size_t)rows[n] * H + s * 64 + c * 8);
+                if (src) {
+                    uint8_t *dst = sB + st * 16384;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) cp_async16(smem_u32(dst + swz128(n, c)), src + s * 64 + c * 8);
                 }
                 cp_async_commit();
                 if (q - done >= kLoaderLag) {
@@ -292,7 +297,6 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     ++done;
                 }
             }
-            __syncwarp();
         }
         cp_async_wait_all();
         fence_proxy_async_smem();
@@ -304,10 +308,28 @@ __global__ void __launch_bounds__(kThreads1, 1)
             prefetch_map(&map_uc);
             prefetch_map(&map_sgc);
             prefetch_map(&map_suc);
+            // The code boxes are 32 bytes of 128 rows 1 KB apart: fetched from DRAM piece by
+            // piece they would cost a DRAM burst each.  A tile's rows are contiguous, so the
+            // whole tile (codes, scales, biases) is requested from L2 in bulk one tile ahead.
+            auto prefetch_tile = [&](int tp) {
+                if (tp >= ntiles) return;
+                const TileInfo t2 = tile_info(P.work, P.offsets, tp, MB, P.E, Tk);
+                const int rows = min(128, I - t2.mb * 128);
+                const size_t wrow = (size_t)(t2.shared_e ? 0 : t2.expert * I) + t2.mb * 128;
+                prefetch_rows((t2.shared_e ? P.sgc : P.gc) + wrow * (H / 2), (uint32_t)rows * (H / 2));
+                prefetch_rows((t2.shared_e ? P.suc : P.uc) + wrow * (H / 2), (uint32_t)rows * (H / 2));
+                const uint32_t sb = (uint32_t)rows * G * 2;
+                prefetch_rows((t2.shared_e ? P.sgs : P.gs) + wrow * G, sb);
+                prefetch_rows((t2.shared_e ? P.sgb : P.gb) + wrow * G, sb);
+                prefetch_rows((t2.shared_e ? P.sus : P.us) + wrow * G, sb);
+                prefetch_rows((t2.shared_e ? P.sub : P.ub) + wrow * G, sb);
+            };
+            prefetch_tile(blockIdx.x);
             int q = 0;
             bool ok = true;
             for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
                 const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+                prefetch_tile(tau + gridDim.x);
                 const CUtensorMap *mg = ti.shared_e ? &map_sgc : &map_gc;
                 const CUtensorMap *mu = ti.shared_e ? &map_suc : &map_uc;
                 const int wrow = (ti.shared_e ? 0 : ti.expert * I) + ti.mb * 128;
@@ -337,14 +359,13 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
                 const int N = (ti.ntok + 15) & ~15;
                 const uint32_t idesc = idesc_f16_m128((uint32_t)N);
-                const int buf = i & 1;
-                if (i >= 2 && !mbar_wait(smem_u32(tempty + buf), ((i >> 1) - 1) & 1, limit, s_abort)) {
+                // one accumulator pair: the epilogue of the previous tile has read it
+                if (i >= 1 && !mbar_wait(smem_u32(tempty), (i - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d0 = tmem + (uint32_t)buf * 256;
                 for (int s = 0; s < nk; ++s, ++q) {
                     const int st = q % S, sb = q % SB;
                     if (!mbar_wait(smem_u32(bfull + sb), (q / SB) & 1, limit, s_abort) ||
@@ -354,25 +375,28 @@ __global__ void __launch_bounds__(kThreads1, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t ag = smem_u32(sA_g + st * 16384), au = smem_u32(sA_u + st * 16384);
+                    const uint32_t a0 = tmem + kTmemA1 + (uint32_t)st * 64;   // gate A | up A (32 columns each)
                     const uint32_t bb = smem_u32(sB + sb * 16384);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t acc = (s | kk) != 0;
-                        mma_f16(d0, desc_sw128(ag + kk * 32), desc_sw128(bb + kk * 32), idesc, acc);
-                        mma_f16(d0 + 128, desc_sw128(au + kk * 32), desc_sw128(bb + kk * 32), idesc, acc);
+                        mma_f16_ts(tmem, a0 + kk * 8, desc_sw128(bb + kk * 32), idesc, acc);
+                        mma_f16_ts(tmem + 128, a0 + 32 + kk * 8, desc_sw128(bb + kk * 32), idesc, acc);
                     }
                     mma_commit(smem_u32(aempty + st));
                     mma_commit(smem_u32(bempty + sb));
                 }
-                if (ok) mma_commit(smem_u32(tfull + buf));
+                if (ok) mma_commit(smem_u32(tfull));
             }
             mma_commit(smem_u32(drain));   // every issued MMA completes before TMEM is freed
             mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
     } else if (warp < 8) {
         // ------------------------------------------------ dequant: warps 0-3 gate rows, 4-7 up rows
+        // Thread (m, r) writes row r of matrix m's A stage in tensor memory: lane r, 32
+        // columns of 16-bit pairs in the codes' k order (x16 is stored in the same order).
         const int m = tid >> 7, r = tid & 127;
+        const uint32_t a_lane = tmem + ((uint32_t)(r & ~31) << 16) + kTmemA1 + (uint32_t)m * 32;
         int q = 0;
         bool ok = true;
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
@@ -387,33 +411,51 @@ __global__ void __launch_bounds__(kThreads1, 1)
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
                 if (s % kScaleChunk == 0) stage_scales<2>(myscale, srcs, row_ok, soff, G, s, r);
-                // the A stage of step q is free once the MMAs of step q - S are done
-                if (q >= S && !mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort)) {
-                    set_abort(s_abort, P.status);
-                    ok = false;
-                    break;
-                }
+                // the A stage of step q is free once the MMAs of step q - S are done; the fence
+                // orders this thread's tcgen05.st after those MMAs' reads
+                bool w_ok = q < S || mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort);
+                tc_fence_after();
                 const int cs = q % CS;
-                if (!mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort)) {
+                w_ok = w_ok && mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort);
+                uint32_t av[32];
+                if (w_ok) {
+                    const int gi = s % kScaleChunk;
+                    const __half2 sc = bf16_to_h2(myscale[(0 * kScaleChunk + gi) * 128 + r]);
+                    const __half2 bc = bf16_to_h2(myscale[(1 * kScaleChunk + gi) * 128 + r]);
+                    const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
+                    const uint4 w0 = cp[0], w1 = cp[1];
+                    const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 d = dequant8(cw[c], sc, bc);
+                        av[4 * c] = d.x;
+                        av[4 * c + 1] = d.y;
+                        av[4 * c + 2] = d.z;
+                        av[4 * c + 3] = d.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) av[c] = 0u;
+                }
+                // tcgen05.st / wait::st are warp-collective: the lanes left the polling loops
+                // above at different iterations, so reconverge first
+                __syncwarp();
+                tmem_st32(a_lane + (uint32_t)st * 64, av);
+                tmem_st_wait();
+                tc_fence_before();
+                // One arrive for the eight warps, after a barrier over all of them: with an
+                // arrive per thread, the MMAs were seen to read a stage before the stores of
+                // the last warps to arrive had landed.  The barrier also makes a failed wait
+                // a uniform stop.
+                if (bar_any(1, kDequantThreads, !w_ok)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
                 }
-                const int gi = s % kScaleChunk;
-                const __half2 sc = bf16_to_h2(myscale[(0 * kScaleChunk + gi) * 128 + r]);
-                const __half2 bc = bf16_to_h2(myscale[(1 * kScaleChunk + gi) * 128 + r]);
-                const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
-                const uint4 w0 = cp[0], w1 = cp[1];
-                const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                uint8_t *aa = (m == 0 ? sA_g : sA_u) + st * 16384;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(aa + swz128(r, c)) = dequant8(cw[c], sc, bc);
-                // Release the code slot only after its words have been consumed: the
-                // arrive does not wait for shared loads still in flight, and the TMA
-                // refill of the slot would race them.
-                mbar_arrive(smem_u32(cempty + cs));
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(afull + st));
+                if (tid == 0) {
+                    mbar_arrive(smem_u32(cempty + cs));    // every thread's code words are consumed
+                    mbar_arrive(smem_u32(afull + st));
+                }
             }
             if (bar_any(1, kDequantThreads, !ok || *s_abort)) break;   // the eight warps stop together
         }
@@ -425,8 +467,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
             const int N = (ti.ntok + 15) & ~15;
-            const int buf = i & 1;
-            bool got = mbar_wait(smem_u32(tfull + buf), (i >> 1) & 1, limit, s_abort);
+            bool got = mbar_wait(smem_u32(tfull), i & 1, limit, s_abort);
             got = __all_sync(0xffffffffu, got);              // tcgen05.ld needs the whole warp
             if (!got) {
                 set_abort(s_abort, P.status);
@@ -435,12 +476,16 @@ __global__ void __launch_bounds__(kThreads1, 1)
             tc_fence_after();
             const int erow = ti.mb * 128 + quad * 32 + lane;
             const int hcol = kperm_pos(erow);
-            const uint32_t d0 = tmem + lane_base + (uint32_t)buf * 256;
+            const uint32_t d0 = tmem + lane_base;
             for (int n0 = 0; n0 < N; n0 += 16) {
                 uint32_t gv[16], uv[16];
                 tmem_ld16(d0 + n0, gv);
                 tmem_ld16(d0 + 128 + n0, uv);
                 tmem_ld_wait();
+                if (n0 + 16 >= N) {                       // every column read: the MMAs may overwrite them
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(tempty));
+                }
                 if (erow < I) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -453,8 +498,6 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(smem_u32(tempty + buf));
         }
     }
     tc_fence_before();
@@ -529,10 +572,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_map(&map_dc);
             prefetch_map(&map_sdc);
+            // whole tiles (codes, scales, biases) requested from L2 in bulk one tile ahead
+            auto prefetch_tile = [&](int tp) {
+                if (tp >= ntiles) return;
+                const TileInfo t2 = tile_info(P.work, P.offsets, tp, MB, P.E, Tk);
+                const int rows = min(128, H - t2.mb * 128);
+                const size_t wrow = (size_t)(t2.shared_e ? 0 : t2.expert * H) + t2.mb * 128;
+                prefetch_rows((t2.shared_e ? P.sdc : P.dc) + wrow * (I / 2), (uint32_t)rows * (I / 2));
+                const uint32_t sb = (uint32_t)rows * GI * 2;
+                prefetch_rows((t2.shared_e ? P.sds : P.ds) + wrow * GI, sb);
+                prefetch_rows((t2.shared_e ? P.sdb : P.db) + wrow * GI, sb);
+            };
+            prefetch_tile(blockIdx.x);
             int q = 0;
             bool ok = true;
             for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
                 const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
+                prefetch_tile(tau + gridDim.x);
                 const CUtensorMap *md = ti.shared_e ? &map_sdc : &map_dc;
                 const int wrow = (ti.shared_e ? 0 : ti.expert * H) + ti.mb * 128;
                 for (int s = 0; s < nk; ++s, ++q) {
@@ -746,7 +802,7 @@ __global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict_
 
 size_t g1_smem()
 {
-    return 1024 + kStagesA1 * 32768 + kStagesB1 * 16384 + kCodeStages1 * 8192 + 4 * kScaleChunk * 128 * 2 +
+    return 1024 + kStagesB1 * 16384 + kCodeStages1 * 8192 + 4 * kScaleChunk * 128 * 2 +
            8 * (2 * kCodeStages1 + 2 * kStagesA1 + 2 * kStagesB1 + 5) + 256 * 4 + 16;
 }
 size_t g2_smem()
@@ -807,6 +863,10 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p1.perm = a.perm;
     p1.hs = a.hs;
     p1.x16 = a.x16;
+    p1.gc = a.gate.codes;
+    p1.uc = a.up.codes;
+    p1.sgc = a.has_shared ? a.s_gate.codes : a.gate.codes;
+    p1.suc = a.has_shared ? a.s_up.codes : a.up.codes;
     p1.gs = a.gate.scales;
     p1.gb = a.gate.biases;
     p1.us = a.up.scales;
@@ -837,6 +897,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p2.p = a.p;
     p2.w_s = a.w_s;
     p2.acc = a.acc;
+    p2.dc = a.down.codes;
+    p2.sdc = a.has_shared ? a.s_down.codes : a.down.codes;
     p2.ds = a.down.scales;
     p2.db = a.down.biases;
     p2.sds = a.s_down.scales;
