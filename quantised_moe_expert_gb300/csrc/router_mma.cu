@@ -21,7 +21,8 @@
 namespace qmoe {
 namespace {
 
-constexpr int kRWarps = 8;                 // 8 warps x 16 experts per block
+constexpr int kRWarps = 8;                 // 2 expert tiles (16 experts each) x 4 quarters of the input dimension
+constexpr int kRExp = 32;                  // experts per block
 constexpr int kRTok = 32;                  // tokens per block (4 n8 tiles)
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -49,14 +50,17 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
     return r;
 }
 
-// grid (ceil(E/128), ceil(T/32)), 256 threads.  Warp w: experts e0 + 16 w .. +15, all 32 tokens.
+// grid (ceil(E/32), ceil(T/32)), 256 threads.  Warp w: experts e0 + 16 (w & 1) .. +15 over the groups of
+// quarter w >> 1 of the input dimension, all 32 tokens; the four quarters' partial sums are added in a
+// fixed order (quarter 0 first) through shared memory.  A token's logits never depend on the other tokens.
 __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaArgs a)
 {
+    __shared__ float s_part[4][kRExp][kRTok + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int H = a.H, E = a.E, T = a.T, G = H / kGroup;
-    const int ebase = blockIdx.x * (kRWarps * 16) + warp * 16;
+    const int et = warp & 1, kq = warp >> 1;
+    const int ebase = blockIdx.x * kRExp + et * 16;
     const int tbase = blockIdx.y * kRTok;
-    if (ebase >= E) return;
     const int r0 = min(ebase + g, E - 1), r1 = min(ebase + g + 8, E - 1);   // clamped rows are not stored
     int tok[4];
 #pragma unroll
@@ -68,7 +72,8 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaArgs a)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
 
-    for (int grp = 0; grp < G; ++grp) {
+    const int gbeg = (kq * G) / 4, gend = ((kq + 1) * G) / 4;
+    for (int grp = gbeg; grp < gend; ++grp) {
         // 16 codes (bytes 16t..16t+15 of the group) of rows g and g+8
         const uint4 c0 = __ldg(reinterpret_cast<const uint4 *>(a.codes + (size_t)r0 * H + grp * 64 + 16 * t));
         const uint4 c1 = __ldg(reinterpret_cast<const uint4 *>(a.codes + (size_t)r1 * H + grp * 64 + 16 * t));
@@ -121,19 +126,26 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaArgs a)
             acc[j][3] = fmaf(s1, fmaf(16.f, dh[3], dl[3]), fmaf(k1, dx[3], acc[j][3]));
         }
     }
-    const int e0 = ebase + g, e1 = e0 + 8;
-    const float bias0 = (a.router_bias && e0 < E) ? __ldg(a.router_bias + e0) : 0.f;
-    const float bias1 = (a.router_bias && e1 < E) ? __ldg(a.router_bias + e1) : 0.f;
+    // partial sums of this quarter: [quarter][expert in block][token in block]
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int tA = tbase + j * 8 + 2 * t, tB = tA + 1;
-        if (tA < T) {
-            if (e0 < E) a.logits[(size_t)tA * E + e0] = a.router_bias ? acc[j][0] + bias0 : acc[j][0];
-            if (e1 < E) a.logits[(size_t)tA * E + e1] = a.router_bias ? acc[j][2] + bias1 : acc[j][2];
-        }
-        if (tB < T) {
-            if (e0 < E) a.logits[(size_t)tB * E + e0] = a.router_bias ? acc[j][1] + bias0 : acc[j][1];
-            if (e1 < E) a.logits[(size_t)tB * E + e1] = a.router_bias ? acc[j][3] + bias1 : acc[j][3];
+        const int c = j * 8 + 2 * t;
+        s_part[kq][et * 16 + g][c] = acc[j][0];
+        s_part[kq][et * 16 + g][c + 1] = acc[j][1];
+        s_part[kq][et * 16 + g + 8][c] = acc[j][2];
+        s_part[kq][et * 16 + g + 8][c + 1] = acc[j][3];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kRExp * kRTok; i += blockDim.x) {
+        const int el = i / kRTok, tl = i - el * kRTok;
+        const int e = blockIdx.x * kRExp + el, tt = tbase + tl;
+        if (e < E && tt < T) {
+            float l = s_part[0][el][tl];
+            l += s_part[1][el][tl];
+            l += s_part[2][el][tl];
+            l += s_part[3][el][tl];
+            if (a.router_bias) l = l + __ldg(a.router_bias + e);   // one fp32 rounding
+            a.logits[(size_t)tt * E + e] = l;
         }
     }
 }
@@ -142,7 +154,7 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaArgs a)
 
 cudaError_t launch_router_mma(const RouterMmaArgs &a, cudaStream_t st)
 {
-    dim3 grid((a.E + kRWarps * 16 - 1) / (kRWarps * 16), (a.T + kRTok - 1) / kRTok);
+    dim3 grid((a.E + kRExp - 1) / kRExp, (a.T + kRTok - 1) / kRTok);
     router_mma_kernel<<<grid, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
