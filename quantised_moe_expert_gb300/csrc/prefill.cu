@@ -104,14 +104,19 @@ __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<ui
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
 // 8 nibbles (inputs 0..7 of a chunk) -> 8 fp16 w = s*q + b in the order (0,4,1,5,2,6,3,7).
-__device__ __forceinline__ uint4 dequant8(uint32_t u, __half2 s2, __half2 b2)
+// The low nibble of each byte, ORed into the mantissa of 1024.0, gives 1024 + q; the high
+// nibble masked in place gives 1024 + 16 q, and s16 = s / 16 (a power-of-two division,
+// exact) makes (16 q) * s16 = q * s: one shift per word instead of three.  Every weight is
+// the exact s * q + b rounded once to fp16.
+__device__ __forceinline__ uint4 dequant8(uint32_t u, __half2 s2, __half2 s16, __half2 b2)
 {
     const __half2 k1024 = __float2half2_rn(1024.f);
+    const uint32_t v = u >> 8;
     uint4 o;
     o.x = h2u(__hfma2(__hsub2(u2h((u & 0x000F000Fu) | 0x64006400u), k1024), s2, b2));
-    o.y = h2u(__hfma2(__hsub2(u2h(((u >> 4) & 0x000F000Fu) | 0x64006400u), k1024), s2, b2));
-    o.z = h2u(__hfma2(__hsub2(u2h(((u >> 8) & 0x000F000Fu) | 0x64006400u), k1024), s2, b2));
-    o.w = h2u(__hfma2(__hsub2(u2h(((u >> 12) & 0x000F000Fu) | 0x64006400u), k1024), s2, b2));
+    o.y = h2u(__hfma2(__hsub2(u2h((u & 0x00F000F0u) | 0x64006400u), k1024), s16, b2));
+    o.z = h2u(__hfma2(__hsub2(u2h((v & 0x000F000Fu) | 0x64006400u), k1024), s2, b2));
+    o.w = h2u(__hfma2(__hsub2(u2h((v & 0x00F000F0u) | 0x64006400u), k1024), s16, b2));
     return o;
 }
 
@@ -231,10 +236,10 @@ __global__ void __launch_bounds__(kThreads1, 1)
     if (tid == 0) {
         for (int s = 0; s < CS; ++s) {
             mbar_init(smem_u32(cfull + s), 1);
-            mbar_init(smem_u32(cempty + s), 1);
+            mbar_init(smem_u32(cempty + s), kDequantThreads / 32);
         }
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(afull + s), 1);
+            mbar_init(smem_u32(afull + s), kDequantThreads / 32);
             mbar_init(smem_u32(aempty + s), 1);
         }
         for (int s = 0; s < SB; ++s) {
@@ -421,13 +426,14 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 if (w_ok) {
                     const int gi = s % kScaleChunk;
                     const __half2 sc = bf16_to_h2(myscale[(0 * kScaleChunk + gi) * 128 + r]);
+                    const __half2 sc16 = __hmul2(sc, __float2half2_rn(0.0625f));
                     const __half2 bc = bf16_to_h2(myscale[(1 * kScaleChunk + gi) * 128 + r]);
                     const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
                     const uint4 w0 = cp[0], w1 = cp[1];
                     const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint4 d = dequant8(cw[c], sc, bc);
+                        const uint4 d = dequant8(cw[c], sc, sc16, bc);
                         av[4 * c] = d.x;
                         av[4 * c + 1] = d.y;
                         av[4 * c + 2] = d.z;
@@ -443,17 +449,17 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 tmem_st32(a_lane + (uint32_t)st * 64, av);
                 tmem_st_wait();
                 tc_fence_before();
-                // One arrive for the eight warps, after a barrier over all of them: with an
-                // arrive per thread, the MMAs were seen to read a stage before the stores of
-                // the last warps to arrive had landed.  The barrier also makes a failed wait
-                // a uniform stop.
-                if (bar_any(1, kDequantThreads, !w_ok)) {
+                // One arrive per warp, after the warp has synchronised: with an arrive per
+                // thread, the MMAs were seen to read a stage before the stores of the last
+                // warps to arrive had landed.  A failed wait stops the whole warp.
+                if (__any_sync(0xffffffffu, !w_ok)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
                 }
-                if (tid == 0) {
-                    mbar_arrive(smem_u32(cempty + cs));    // every thread's code words are consumed
+                if (lane == 0) {
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(cempty + cs));    // the warp's code words are consumed
                     mbar_arrive(smem_u32(afull + st));
                 }
             }
@@ -697,13 +703,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int gi = s % kScaleChunk;
                 const __half2 sd = bf16_to_h2(myscale[(0 * kScaleChunk + gi) * 128 + r]);
+                const __half2 sd16 = __hmul2(sd, __float2half2_rn(0.0625f));
                 const __half2 bd = bf16_to_h2(myscale[(1 * kScaleChunk + gi) * 128 + r]);
                 const uint4 w = *reinterpret_cast<const uint4 *>(sC + cs * 4096 + r * 32 + half * 16);
                 const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
                 uint8_t *aa = sA + st * 16384;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(aa + swz128(r, half * 4 + c)) = dequant8(cw[c], sd, bd);
+                    *reinterpret_cast<uint4 *>(aa + swz128(r, half * 4 + c)) = dequant8(cw[c], sd, sd16, bd);
                 mbar_arrive(smem_u32(cempty + cs));
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(afull + st));
