@@ -51,15 +51,16 @@ using namespace tc;
 // Stage counts of the three rings of each GEMM: dequantised weights (A), token
 // operand (B) and int4 code tiles.  B runs deepest: its loads come from L2 /
 // HBM with a latency of several K-steps of MMA.
-constexpr int kStagesA1 = 4, kStagesB1 = 6, kCodeStages1 = 6;   // gate/up: A in TMEM (64 columns), 16 KB, 8 KB per stage
+constexpr int kStagesA1 = 4, kStagesB1 = 8, kCodeStages1 = 6;   // gate/up: A in TMEM (64 columns), 16 KB, 8 KB per stage
 constexpr int kStagesA2 = 3, kStagesB2 = 4, kCodeStages2 = 6;   // down:    16 KB, 32 KB, 4 KB per stage
-constexpr int kLoaderLag = kStagesB1 - 2;                       // token-row groups in flight beyond the newest
-// Warp roles (both GEMMs): 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue; the
-// gate/up GEMM adds warp 14, the token-row loader.
+// Warp roles (both GEMMs): 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue.  The gate/up
+// GEMM runs eight epilogue warps (10-17) and adds two token-row loader warps (18, 19)
+// that take the K-steps in turn, each with kLoaderDepth of its steps in flight.
 constexpr int kDequantThreads = 256;
-constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10, kWarpLoader = 14, kLoaderWarps = 4;
-constexpr int kThreads = 448;       // down GEMM
-constexpr int kThreads1 = 576;      // gate/up GEMM
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10;
+constexpr int kEpiWarps1 = 8, kWarpLoader1 = kWarpEpi + kEpiWarps1, kLoaderWarps1 = 2, kLoaderDepth = 2;
+constexpr int kThreads = 448;                                   // down GEMM
+constexpr int kThreads1 = 32 * (kWarpLoader1 + kLoaderWarps1);  // gate/up GEMM (640)
 constexpr int kScaleChunk = 16;     // groups of scales staged in shared memory at a time
 constexpr long long kDrainLimit = 1ll << 22;
 constexpr uint32_t kTmemA1 = 256;   // gate/up GEMM: accumulators in TMEM columns [0, 256), A stages from 256
@@ -76,6 +77,7 @@ struct G1Params {
     const uint16_t *sgs, *sgb, *sus, *sub; // shared expert [I, H/64]
     int *status;
     int T, H, I, E, k;
+    int async_scales;                  // 1: scale rows are 16-byte aligned (H % 512 == 0), fetched with cp.async
     long long wait_limit;
 };
 
@@ -220,8 +222,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sB = smem;                           // SB x 16 KB (128 token rows x 128 B)
     uint8_t *sC = sB + SB * 16384;                // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
-    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [4][kScaleChunk][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 4 * kScaleChunk * 128);
+    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [dequant thread][2][2][kScaleChunk]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kDequantThreads * 4 * kScaleChunk);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
@@ -243,11 +245,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
             mbar_init(smem_u32(aempty + s), 1);
         }
         for (int s = 0; s < SB; ++s) {
-            mbar_init(smem_u32(bfull + s), 32 * kLoaderWarps);
+            mbar_init(smem_u32(bfull + s), 32);           // the lanes of the step's loader warp
             mbar_init(smem_u32(bempty + s), 1);
         }
         mbar_init(smem_u32(tfull), 1);
-        mbar_init(smem_u32(tempty), 128);
+        mbar_init(smem_u32(tempty), 32 * kEpiWarps1);
         mbar_init(smem_u32(drain), 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -258,54 +260,65 @@ __global__ void __launch_bounds__(kThreads1, 1)
     const uint32_t tmem = *s_tmem;
     const long long limit = P.wait_limit;
 
-    if (warp >= kWarpLoader) {
+    if (warp >= kWarpLoader1) {
         // ------------------------------------------------ token rows of x (cp.async gather)
-        // Four loader warps, one token row of the tile per lane.  They run ahead of the
-        // dequant warps, bounded only by free B stages: step q's rows go into stage q % SB
-        // once the MMAs of step q - SB are done; a lane's arrive for step q is made when its
-        // copies have landed, kLoaderLag steps later.
-        const int n = (warp - kWarpLoader) * 32 + lane;      // row of the B tile
-        int q = 0, done = 0;                                  // steps [done, q) issued, not yet arrived
+        // The loader warps take the K-steps in turn (warp w: steps q = w mod kLoaderWarps1),
+        // each keeping kLoaderDepth of its own steps in flight; lane l gathers rows l, l + 32,
+        // l + 64 and l + 96 of the tile.  Step q's rows go into stage q % SB once the MMAs of
+        // step q - SB are done, and each lane arrives on the stage's full barrier as soon as
+        // its own copies of that step have landed.
+        const int lw = warp - kWarpLoader1;
+        int q = 0, q_last = -1, pending = 0;                  // pending: issued, not yet arrived
         bool ok = true;
         for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
-            const uint16_t *src = nullptr;                    // rows past ntok are never read
-            if (n < ti.ntok) {
-                int row = -1;
-                if (ti.shared_e) {
-                    row = ti.tok0 + n;
-                } else {
-                    const int pos = ti.pbase + n;
-                    const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
-                    if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
-                    else row = f / P.k;
+            const uint16_t *src[4];                           // rows past ntok are never read
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = lane + 32 * j;
+                src[j] = nullptr;
+                if (n < ti.ntok) {
+                    int row = -1;
+                    if (ti.shared_e) {
+                        row = ti.tok0 + n;
+                    } else {
+                        const int pos = ti.pbase + n;
+                        const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                        if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
+                        else row = f / P.k;
+                    }
+                    if (row >= 0) src[j] = P.x16 + (size_t)row * H;
                 }
-                if (row >= 0) src = P.x16 + (size_t)row * H;
             }
             for (int s = 0; s < nk; ++s, ++q) {
+                if (q % kLoaderWarps1 != lw) continue;
                 const int st = q % SB;
                 if (q >= SB && !mbar_wait(smem_u32(bempty + st), (q / SB - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
                 }
-                if (src) {
-                    uint8_t *dst = sB + st * 16384;
+                uint8_t *dst = sB + st * 16384;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) cp_async16(smem_u32(dst + swz128(n, c)), src + s * 64 + c * 8);
-                }
+                for (int j = 0; j < 4; ++j)
+                    if (src[j]) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            cp_async16(smem_u32(dst + swz128(lane + 32 * j, c)), src[j] + s * 64 + c * 8);
+                    }
                 cp_async_commit();
-                if (q - done >= kLoaderLag) {
-                    cp_async_wait_group<kLoaderLag>();        // step `done`'s rows have landed
+                q_last = q;
+                if (++pending == kLoaderDepth) {              // the oldest of this warp's steps has landed
+                    cp_async_wait_group<kLoaderDepth - 1>();
                     fence_proxy_async_smem();
-                    mbar_arrive(smem_u32(bfull + done % SB));
-                    ++done;
+                    mbar_arrive(smem_u32(bfull + (q - (kLoaderDepth - 1) * kLoaderWarps1) % SB));
+                    --pending;
                 }
             }
         }
         cp_async_wait_all();
         fence_proxy_async_smem();
-        for (; done < q; ++done) mbar_arrive(smem_u32(bfull + done % SB));
+        for (int d = pending - 1; d >= 0; --d) mbar_arrive(smem_u32(bfull + (q_last - d * kLoaderWarps1) % SB));
     } else if (warp == kWarpTma) {
         // ------------------------------------------------ code tiles (TMA)
         if (lane == 0) {
@@ -400,53 +413,118 @@ __global__ void __launch_bounds__(kThreads1, 1)
         // ------------------------------------------------ dequant: warps 0-3 gate rows, 4-7 up rows
         // Thread (m, r) writes row r of matrix m's A stage in tensor memory: lane r, 32
         // columns of 16-bit pairs in the codes' k order (x16 is stored in the same order).
+        // The row's scales and biases pass through a private double buffer of kScaleChunk
+        // groups: when a chunk starts, the next one (of this tile or of the next tile) is
+        // requested with cp.async, so the strided scale rows never stall the K loop.  The
+        // warps run independently; each stops at the first failed wait.
         const int m = tid >> 7, r = tid & 127;
         const uint32_t a_lane = tmem + ((uint32_t)(r & ~31) << 16) + kTmemA1 + (uint32_t)m * 32;
-        int q = 0;
+        uint16_t *mysc = sScale + (size_t)tid * (4 * kScaleChunk);   // [buffer][scale | bias][kScaleChunk]
+        const int nchunk = (G + kScaleChunk - 1) / kScaleChunk;
+        auto scale_src = [&](const TileInfo &t, size_t &off) {
+            off = ((size_t)(t.shared_e ? 0 : t.expert) * I + (size_t)(t.mb * 128 + r)) * G;
+        };
+        auto fetch_chunk = [&](const TileInfo &t, int c, int buf) {     // one commit group per call
+            if (t.mb * 128 + r < I) {
+                size_t off;
+                scale_src(t, off);
+                off += (size_t)c * kScaleChunk;
+                const uint16_t *ps = m == 0 ? (t.shared_e ? P.sgs : P.gs) : (t.shared_e ? P.sus : P.us);
+                const uint16_t *pb = m == 0 ? (t.shared_e ? P.sgb : P.gb) : (t.shared_e ? P.sub : P.ub);
+                uint16_t *d = mysc + buf * 2 * kScaleChunk;
+#pragma unroll
+                for (int piece = 0; piece < kScaleChunk / 8; ++piece)   // 8 groups = 16 bytes
+                    if (c * kScaleChunk + piece * 8 < G) {
+                        cp_async16(smem_u32(d + piece * 8), ps + off + piece * 8);
+                        cp_async16(smem_u32(d + kScaleChunk + piece * 8), pb + off + piece * 8);
+                    }
+            }
+            cp_async_commit();
+        };
+        auto load_chunk = [&](const TileInfo &t, int c, int buf) {      // the same with plain loads
+            const bool row_ok = t.mb * 128 + r < I;
+            size_t off;
+            scale_src(t, off);
+            off += (size_t)c * kScaleChunk;
+            const uint16_t *ps = m == 0 ? (t.shared_e ? P.sgs : P.gs) : (t.shared_e ? P.sus : P.us);
+            const uint16_t *pb = m == 0 ? (t.shared_e ? P.sgb : P.gb) : (t.shared_e ? P.sub : P.ub);
+            uint16_t v[2][kScaleChunk];
+#pragma unroll
+            for (int g = 0; g < kScaleChunk; ++g) {
+                const bool in = row_ok && c * kScaleChunk + g < G;
+                v[0][g] = in ? ps[off + g] : (uint16_t)0;
+                v[1][g] = in ? pb[off + g] : (uint16_t)0;
+            }
+            uint16_t *d = mysc + buf * 2 * kScaleChunk;
+#pragma unroll
+            for (int g = 0; g < kScaleChunk; ++g) {
+                d[g] = v[0][g];
+                d[kScaleChunk + g] = v[1][g];
+            }
+        };
+        int q = 0, j = 0;                                  // j: scale chunks started by this thread
         bool ok = true;
-        for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
+        if (P.async_scales) fetch_chunk(tile_info(P.work, P.offsets, blockIdx.x, MB, P.E, Tk), 0, 0);
+        const uint16_t *cur = mysc;
+        uint4 sreg = make_uint4(0, 0, 0, 0), breg = sreg;  // 8 groups' scales and biases (bf16 pairs)
+        for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
-            const int row = ti.mb * 128 + r;
-            const bool row_ok = row < I;
-            const int ee = ti.shared_e ? 0 : ti.expert;
-            const size_t soff = (size_t)ee * I * G + (size_t)row * G;
-            const uint16_t *srcs[2] = {m == 0 ? (ti.shared_e ? P.sgs : P.gs) : (ti.shared_e ? P.sus : P.us),
-                                       m == 0 ? (ti.shared_e ? P.sgb : P.gb) : (ti.shared_e ? P.sub : P.ub)};
-            uint16_t *myscale = sScale + m * 2 * kScaleChunk * 128;
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
-                if (s % kScaleChunk == 0) stage_scales<2>(myscale, srcs, row_ok, soff, G, s, r);
+                if (s % kScaleChunk == 0) {
+                    const int c = s / kScaleChunk;
+                    if (P.async_scales) {
+                        if (c + 1 < nchunk) fetch_chunk(ti, c + 1, (j + 1) & 1);
+                        else if (tau + (int)gridDim.x < ntiles)
+                            fetch_chunk(tile_info(P.work, P.offsets, tau + gridDim.x, MB, P.E, Tk), 0, (j + 1) & 1);
+                        else cp_async_commit();
+                        cp_async_wait_group<1>();                 // chunk j has landed
+                    } else {
+                        load_chunk(ti, c, j & 1);
+                    }
+                    cur = mysc + (j & 1) * 2 * kScaleChunk;
+                    ++j;
+                }
+                if ((s & 7) == 0) {
+                    sreg = *reinterpret_cast<const uint4 *>(cur + (s % kScaleChunk));
+                    breg = *reinterpret_cast<const uint4 *>(cur + kScaleChunk + (s % kScaleChunk));
+                }
                 // the A stage of step q is free once the MMAs of step q - S are done; the fence
                 // orders this thread's tcgen05.st after those MMAs' reads
                 bool w_ok = q < S || mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort);
                 tc_fence_after();
                 const int cs = q % CS;
                 w_ok = w_ok && mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort);
-                uint32_t av[32];
-                if (w_ok) {
-                    const int gi = s % kScaleChunk;
-                    const __half2 sc = bf16_to_h2(myscale[(0 * kScaleChunk + gi) * 128 + r]);
-                    const __half2 sc16 = __hmul2(sc, __float2half2_rn(0.0625f));
-                    const __half2 bc = bf16_to_h2(myscale[(1 * kScaleChunk + gi) * 128 + r]);
-                    const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
-                    const uint4 w0 = cp[0], w1 = cp[1];
-                    const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 d = dequant8(cw[c], sc, sc16, bc);
-                        av[4 * c] = d.x;
-                        av[4 * c + 1] = d.y;
-                        av[4 * c + 2] = d.z;
-                        av[4 * c + 3] = d.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) av[c] = 0u;
-                }
+                const int gi = s & 7;
+                const uint32_t sw = gi < 4 ? (gi < 2 ? sreg.x : sreg.y) : (gi < 6 ? sreg.z : sreg.w);
+                const uint32_t bw = gi < 4 ? (gi < 2 ? breg.x : breg.y) : (gi < 6 ? breg.z : breg.w);
+                const __half2 sc = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
+                const __half2 sc16 = __hmul2(sc, __float2half2_rn(0.0625f));
+                const __half2 bc = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
+                const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
                 // tcgen05.st / wait::st are warp-collective: the lanes left the polling loops
                 // above at different iterations, so reconverge first
                 __syncwarp();
-                tmem_st32(a_lane + (uint32_t)st * 64, av);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t av[16];
+                    if (w_ok) {
+                        const uint4 w = cp[hh];
+                        const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 d = dequant8(cw[c], sc, sc16, bc);
+                            av[4 * c] = d.x;
+                            av[4 * c + 1] = d.y;
+                            av[4 * c + 2] = d.z;
+                            av[4 * c + 3] = d.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) av[c] = 0u;
+                    }
+                    tmem_st16(a_lane + (uint32_t)st * 64 + (uint32_t)hh * 16, av);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 // One arrive per warp, after the warp has synchronised: with an arrive per
@@ -463,11 +541,14 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     mbar_arrive(smem_u32(afull + st));
                 }
             }
-            if (bar_any(1, kDequantThreads, !ok || *s_abort)) break;   // the eight warps stop together
+            if (*s_abort) break;
         }
+        cp_async_wait_all();                               // no copy into shared memory outlives the CTA
     } else {
         // ------------------------------------------------ epilogue: h = silu(g) * u
-        const int quad = warp & 3;                        // TMEM lanes 32 quad .. 32 quad + 31
+        // Eight warps: warp w reads TMEM lanes 32 (w & 3) .. + 31 (the lanes its position in a
+        // warpgroup allows) and the 16-column chunks of parity `half` of the accumulators.
+        const int quad = warp & 3, half = (warp - kWarpEpi) >> 2;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         int i = 0;
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
@@ -483,12 +564,16 @@ __global__ void __launch_bounds__(kThreads1, 1)
             const int erow = ti.mb * 128 + quad * 32 + lane;
             const int hcol = kperm_pos(erow);
             const uint32_t d0 = tmem + lane_base;
-            for (int n0 = 0; n0 < N; n0 += 16) {
+            if (16 * half >= N) {                             // no chunk of this parity: nothing to read
+                tc_fence_before();
+                mbar_arrive(smem_u32(tempty));
+            }
+            for (int n0 = 16 * half; n0 < N; n0 += 32) {
                 uint32_t gv[16], uv[16];
                 tmem_ld16(d0 + n0, gv);
                 tmem_ld16(d0 + 128 + n0, uv);
                 tmem_ld_wait();
-                if (n0 + 16 >= N) {                       // every column read: the MMAs may overwrite them
+                if (n0 + 32 >= N) {                       // this warp's last chunk: the MMAs may overwrite
                     tc_fence_before();
                     mbar_arrive(smem_u32(tempty));
                 }
@@ -498,7 +583,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
                         const int n = n0 + j;
                         if (n < ti.ntok) {
                             const float g = __uint_as_float(gv[j]), u = __uint_as_float(uv[j]);
-                            const float hv = g / (1.f + __expf(-g)) * u;
+                            const float hv = __fdividef(g * u, 1.f + __expf(-g));
                             P.hs[(size_t)(ti.pbase + n) * I + hcol] = __half_as_ushort(__float2half_rn(hv));
                         }
                     }
@@ -809,7 +894,7 @@ __global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict_
 
 size_t g1_smem()
 {
-    return 1024 + kStagesB1 * 16384 + kCodeStages1 * 8192 + 4 * kScaleChunk * 128 * 2 +
+    return 1024 + kStagesB1 * 16384 + kCodeStages1 * 8192 + kDequantThreads * 4 * kScaleChunk * 2 +
            8 * (2 * kCodeStages1 + 2 * kStagesA1 + 2 * kStagesB1 + 5) + 256 * 4 + 16;
 }
 size_t g2_smem()
@@ -888,6 +973,12 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p1.I = I;
     p1.E = E;
     p1.k = k;
+    {
+        const uint16_t *sc[8] = {p1.gs, p1.gb, p1.us, p1.ub, p1.sgs, p1.sgb, p1.sus, p1.sub};
+        bool al = (H / kGroup) % 8 == 0;
+        for (const uint16_t *ptr : sc) al = al && (ptr == nullptr || reinterpret_cast<uintptr_t>(ptr) % 16 == 0);
+        p1.async_scales = al ? 1 : 0;
+    }
     p1.wait_limit = a.wait_limit;
     const size_t s1 = g1_smem();
     auto k1 = gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1>;
