@@ -53,14 +53,19 @@ using namespace tc;
 // HBM with a latency of several K-steps of MMA.
 constexpr int kStagesA1 = 4, kStagesB1 = 8, kCodeStages1 = 6;   // gate/up: A in TMEM (64 columns), 16 KB, 8 KB per stage
 constexpr int kStagesA2 = 3, kStagesB2 = 4, kCodeStages2 = 6;   // down:    16 KB, 32 KB, 4 KB per stage
-// Warp roles (both GEMMs): 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue.  The gate/up
-// GEMM runs eight epilogue warps (10-17) and adds two token-row loader warps (18, 19)
-// that take the K-steps in turn, each with kLoaderDepth of its steps in flight.
+// Warp roles of the down GEMM: 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue.
 constexpr int kDequantThreads = 256;
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10;
-constexpr int kEpiWarps1 = 8, kWarpLoader1 = kWarpEpi + kEpiWarps1, kLoaderWarps1 = 2, kLoaderDepth = 2;
 constexpr int kThreads = 448;                                   // down GEMM
-constexpr int kThreads1 = 32 * (kWarpLoader1 + kLoaderWarps1);  // gate/up GEMM (640)
+// Gate/up GEMM: warps 0-15 dequantise (0-7 the even K-steps, 8-15 the odd ones, so two
+// steps of each row are in flight), 16 TMA, 17 MMA, 18-21 epilogue, and two token-row
+// loader warps (22, 23) that take the K-steps in turn, each with kLoaderDepth of its
+// steps in flight.
+constexpr int kDequantWarps1 = 16, kStepWarps1 = 8;
+constexpr int kWarpTma1 = 16, kWarpMma1 = 17, kWarpEpi1 = 18, kEpiWarps1 = 4;
+constexpr int kWarpLoader1 = kWarpEpi1 + kEpiWarps1, kLoaderWarps1 = 2, kLoaderDepth = 2;
+constexpr int kThreads1 = 32 * (kWarpLoader1 + kLoaderWarps1);  // 768
+constexpr int kScaleChunk1 = 8;                                 // gate/up: groups per scale chunk
 constexpr int kScaleChunk = 16;     // groups of scales staged in shared memory at a time
 constexpr long long kDrainLimit = 1ll << 22;
 constexpr uint32_t kTmemA1 = 256;   // gate/up GEMM: accumulators in TMEM columns [0, 256), A stages from 256
@@ -222,8 +227,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sB = smem;                           // SB x 16 KB (128 token rows x 128 B)
     uint8_t *sC = sB + SB * 16384;                // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
-    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [dequant thread][2][2][kScaleChunk]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kDequantThreads * 4 * kScaleChunk);
+    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [dequant thread][2][2][kScaleChunk1]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kDequantWarps1 * 32 * 4 * kScaleChunk1);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
@@ -231,17 +236,17 @@ __global__ void __launch_bounds__(kThreads1, 1)
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp == kWarpMma) {
+    if (warp == kWarpMma1) {
         tmem_alloc(smem_u32(s_tmem), 512);
         tmem_relinquish();
     }
     if (tid == 0) {
         for (int s = 0; s < CS; ++s) {
             mbar_init(smem_u32(cfull + s), 1);
-            mbar_init(smem_u32(cempty + s), kDequantThreads / 32);
+            mbar_init(smem_u32(cempty + s), kStepWarps1);
         }
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(afull + s), kDequantThreads / 32);
+            mbar_init(smem_u32(afull + s), kStepWarps1);
             mbar_init(smem_u32(aempty + s), 1);
         }
         for (int s = 0; s < SB; ++s) {
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
         cp_async_wait_all();
         fence_proxy_async_smem();
         for (int d = pending - 1; d >= 0; --d) mbar_arrive(smem_u32(bfull + (q_last - d * kLoaderWarps1) % SB));
-    } else if (warp == kWarpTma) {
+    } else if (warp == kWarpTma1) {
         // ------------------------------------------------ code tiles (TMA)
         if (lane == 0) {
             prefetch_map(&map_gc);
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 for (int d = (q > CS ? q - CS : 0); d < q; ++d)
                     mbar_wait(smem_u32(cfull + d % CS), (d / CS) & 1, kDrainLimit, nullptr);
         }
-    } else if (warp == kWarpMma) {
+    } else if (warp == kWarpMma1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             int q = 0, i = 0;
@@ -409,136 +414,126 @@ __global__ void __launch_bounds__(kThreads1, 1)
             mma_commit(smem_u32(drain));   // every issued MMA completes before TMEM is freed
             mbar_wait(smem_u32(drain), 0, kDrainLimit, nullptr);
         }
-    } else if (warp < 8) {
-        // ------------------------------------------------ dequant: warps 0-3 gate rows, 4-7 up rows
-        // Thread (m, r) writes row r of matrix m's A stage in tensor memory: lane r, 32
-        // columns of 16-bit pairs in the codes' k order (x16 is stored in the same order).
-        // The row's scales and biases pass through a private double buffer of kScaleChunk
-        // groups: when a chunk starts, the next one (of this tile or of the next tile) is
-        // requested with cp.async, so the strided scale rows never stall the K loop.  The
-        // warps run independently; each stops at the first failed wait.
-        const int m = tid >> 7, r = tid & 127;
+    } else if (warp < kDequantWarps1) {
+        // ------------------------------------------------ dequant
+        // Warp w: matrix m = (w >> 2) & 1 (gate, up), rows 32 (w & 3) .. + 31 (the TMEM lanes
+        // its position in a warpgroup allows), K-steps q of parity w >> 3.  Thread (m, r)
+        // writes row r of matrix m's A stage in tensor memory: lane r, 32 columns of 16-bit
+        // pairs in the codes' k order (x16 is stored in the same order).  The row's scales
+        // and biases pass through a private double buffer of kScaleChunk1 groups: when a
+        // chunk starts, the next one (of this tile or of the next tile) is requested with
+        // cp.async, so the strided scale rows never stall the K loop.  The warps run
+        // independently; each stops at the first failed wait.
+        const int m = (warp >> 2) & 1, r = lane + 32 * (warp & 3), par = warp >> 3;
         const uint32_t a_lane = tmem + ((uint32_t)(r & ~31) << 16) + kTmemA1 + (uint32_t)m * 32;
-        uint16_t *mysc = sScale + (size_t)tid * (4 * kScaleChunk);   // [buffer][scale | bias][kScaleChunk]
-        const int nchunk = (G + kScaleChunk - 1) / kScaleChunk;
-        auto scale_src = [&](const TileInfo &t, size_t &off) {
-            off = ((size_t)(t.shared_e ? 0 : t.expert) * I + (size_t)(t.mb * 128 + r)) * G;
+        uint16_t *mysc = sScale + (size_t)tid * (4 * kScaleChunk1);   // [buffer][scale | bias][kScaleChunk1]
+        const int nchunk = (G + kScaleChunk1 - 1) / kScaleChunk1;
+        auto row_src = [&](const TileInfo &t, int c, const uint16_t *&ps, const uint16_t *&pb) -> size_t {
+            ps = m == 0 ? (t.shared_e ? P.sgs : P.gs) : (t.shared_e ? P.sus : P.us);
+            pb = m == 0 ? (t.shared_e ? P.sgb : P.gb) : (t.shared_e ? P.sub : P.ub);
+            return ((size_t)(t.shared_e ? 0 : t.expert) * I + (size_t)(t.mb * 128 + r)) * G + (size_t)c * kScaleChunk1;
         };
         auto fetch_chunk = [&](const TileInfo &t, int c, int buf) {     // one commit group per call
             if (t.mb * 128 + r < I) {
-                size_t off;
-                scale_src(t, off);
-                off += (size_t)c * kScaleChunk;
-                const uint16_t *ps = m == 0 ? (t.shared_e ? P.sgs : P.gs) : (t.shared_e ? P.sus : P.us);
-                const uint16_t *pb = m == 0 ? (t.shared_e ? P.sgb : P.gb) : (t.shared_e ? P.sub : P.ub);
-                uint16_t *d = mysc + buf * 2 * kScaleChunk;
-#pragma unroll
-                for (int piece = 0; piece < kScaleChunk / 8; ++piece)   // 8 groups = 16 bytes
-                    if (c * kScaleChunk + piece * 8 < G) {
-                        cp_async16(smem_u32(d + piece * 8), ps + off + piece * 8);
-                        cp_async16(smem_u32(d + kScaleChunk + piece * 8), pb + off + piece * 8);
-                    }
+                const uint16_t *ps, *pb;
+                const size_t off = row_src(t, c, ps, pb);
+                uint16_t *d = mysc + buf * 2 * kScaleChunk1;
+                cp_async16(smem_u32(d), ps + off);                     // 8 groups = 16 bytes
+                cp_async16(smem_u32(d + kScaleChunk1), pb + off);
             }
             cp_async_commit();
         };
         auto load_chunk = [&](const TileInfo &t, int c, int buf) {      // the same with plain loads
             const bool row_ok = t.mb * 128 + r < I;
-            size_t off;
-            scale_src(t, off);
-            off += (size_t)c * kScaleChunk;
-            const uint16_t *ps = m == 0 ? (t.shared_e ? P.sgs : P.gs) : (t.shared_e ? P.sus : P.us);
-            const uint16_t *pb = m == 0 ? (t.shared_e ? P.sgb : P.gb) : (t.shared_e ? P.sub : P.ub);
-            uint16_t v[2][kScaleChunk];
+            const uint16_t *ps, *pb;
+            const size_t off = row_src(t, c, ps, pb);
+            uint16_t v[2][kScaleChunk1];
 #pragma unroll
-            for (int g = 0; g < kScaleChunk; ++g) {
-                const bool in = row_ok && c * kScaleChunk + g < G;
+            for (int g = 0; g < kScaleChunk1; ++g) {
+                const bool in = row_ok && c * kScaleChunk1 + g < G;
                 v[0][g] = in ? ps[off + g] : (uint16_t)0;
                 v[1][g] = in ? pb[off + g] : (uint16_t)0;
             }
-            uint16_t *d = mysc + buf * 2 * kScaleChunk;
+            uint16_t *d = mysc + buf * 2 * kScaleChunk1;
 #pragma unroll
-            for (int g = 0; g < kScaleChunk; ++g) {
+            for (int g = 0; g < kScaleChunk1; ++g) {
                 d[g] = v[0][g];
-                d[kScaleChunk + g] = v[1][g];
+                d[kScaleChunk1 + g] = v[1][g];
             }
         };
-        int q = 0, j = 0;                                  // j: scale chunks started by this thread
+        int q0 = 0, j = 0;                                 // q0: first K-step of the tile; j: chunks started
         bool ok = true;
         if (P.async_scales) fetch_chunk(tile_info(P.work, P.offsets, blockIdx.x, MB, P.E, Tk), 0, 0);
-        const uint16_t *cur = mysc;
-        uint4 sreg = make_uint4(0, 0, 0, 0), breg = sreg;  // 8 groups' scales and biases (bf16 pairs)
-        for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x) {
+        for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x, q0 += nk) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
-            for (int s = 0; s < nk && ok; ++s, ++q) {
-                const int st = q % S;
-                if (s % kScaleChunk == 0) {
-                    const int c = s / kScaleChunk;
-                    if (P.async_scales) {
-                        if (c + 1 < nchunk) fetch_chunk(ti, c + 1, (j + 1) & 1);
-                        else if (tau + (int)gridDim.x < ntiles)
-                            fetch_chunk(tile_info(P.work, P.offsets, tau + gridDim.x, MB, P.E, Tk), 0, (j + 1) & 1);
-                        else cp_async_commit();
-                        cp_async_wait_group<1>();                 // chunk j has landed
-                    } else {
-                        load_chunk(ti, c, j & 1);
-                    }
-                    cur = mysc + (j & 1) * 2 * kScaleChunk;
-                    ++j;
+            for (int c = 0; c < nchunk && ok; ++c) {
+                if (P.async_scales) {
+                    if (c + 1 < nchunk) fetch_chunk(ti, c + 1, (j + 1) & 1);
+                    else if (tau + (int)gridDim.x < ntiles)
+                        fetch_chunk(tile_info(P.work, P.offsets, tau + gridDim.x, MB, P.E, Tk), 0, (j + 1) & 1);
+                    else cp_async_commit();
+                    cp_async_wait_group<1>();                     // chunk j has landed
+                } else {
+                    load_chunk(ti, c, j & 1);
                 }
-                if ((s & 7) == 0) {
-                    sreg = *reinterpret_cast<const uint4 *>(cur + (s % kScaleChunk));
-                    breg = *reinterpret_cast<const uint4 *>(cur + kScaleChunk + (s % kScaleChunk));
-                }
-                // the A stage of step q is free once the MMAs of step q - S are done; the fence
-                // orders this thread's tcgen05.st after those MMAs' reads
-                bool w_ok = q < S || mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort);
-                tc_fence_after();
-                const int cs = q % CS;
-                w_ok = w_ok && mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort);
-                const int gi = s & 7;
-                const uint32_t sw = gi < 4 ? (gi < 2 ? sreg.x : sreg.y) : (gi < 6 ? sreg.z : sreg.w);
-                const uint32_t bw = gi < 4 ? (gi < 2 ? breg.x : breg.y) : (gi < 6 ? breg.z : breg.w);
-                const __half2 sc = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
-                const __half2 sc16 = __hmul2(sc, __float2half2_rn(0.0625f));
-                const __half2 bc = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
-                const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
-                // tcgen05.st / wait::st are warp-collective: the lanes left the polling loops
-                // above at different iterations, so reconverge first
-                __syncwarp();
+                const uint16_t *cur = mysc + (j & 1) * 2 * kScaleChunk1;
+                ++j;
+                const uint4 sreg = *reinterpret_cast<const uint4 *>(cur);   // 8 groups (bf16 pairs)
+                const uint4 breg = *reinterpret_cast<const uint4 *>(cur + kScaleChunk1);
+                const int s_end = min(nk, (c + 1) * kScaleChunk1);
+                for (int s = c * kScaleChunk1 + ((q0 + c * kScaleChunk1 + par) & 1); s < s_end; s += 2) {
+                    const int q = q0 + s, st = q % S;
+                    // the A stage of step q is free once the MMAs of step q - S are done; the
+                    // fence orders this thread's tcgen05.st after those MMAs' reads
+                    bool w_ok = q < S || mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort);
+                    tc_fence_after();
+                    const int cs = q % CS;
+                    w_ok = w_ok && mbar_wait(smem_u32(cfull + cs), (q / CS) & 1, limit, s_abort);
+                    const int gi = s & 7;
+                    const uint32_t sw = gi < 4 ? (gi < 2 ? sreg.x : sreg.y) : (gi < 6 ? sreg.z : sreg.w);
+                    const uint32_t bw = gi < 4 ? (gi < 2 ? breg.x : breg.y) : (gi < 6 ? breg.z : breg.w);
+                    const __half2 sc = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
+                    const __half2 sc16 = __hmul2(sc, __float2half2_rn(0.0625f));
+                    const __half2 bc = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
+                    const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
+                    // tcgen05.st / wait::st are warp-collective: the lanes left the polling loops
+                    // above at different iterations, so reconverge first
+                    __syncwarp();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t av[16];
-                    if (w_ok) {
-                        const uint4 w = cp[hh];
-                        const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t av[16];
+                        if (w_ok) {
+                            const uint4 w = cp[hh];
+                            const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 d = dequant8(cw[c], sc, sc16, bc);
-                            av[4 * c] = d.x;
-                            av[4 * c + 1] = d.y;
-                            av[4 * c + 2] = d.z;
-                            av[4 * c + 3] = d.w;
+                            for (int cc = 0; cc < 4; ++cc) {
+                                const uint4 d = dequant8(cw[cc], sc, sc16, bc);
+                                av[4 * cc] = d.x;
+                                av[4 * cc + 1] = d.y;
+                                av[4 * cc + 2] = d.z;
+                                av[4 * cc + 3] = d.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int cc = 0; cc < 16; ++cc) av[cc] = 0u;
                         }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) av[c] = 0u;
+                        tmem_st16(a_lane + (uint32_t)st * 64 + (uint32_t)hh * 16, av);
                     }
-                    tmem_st16(a_lane + (uint32_t)st * 64 + (uint32_t)hh * 16, av);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                // One arrive per warp, after the warp has synchronised: with an arrive per
-                // thread, the MMAs were seen to read a stage before the stores of the last
-                // warps to arrive had landed.  A failed wait stops the whole warp.
-                if (__any_sync(0xffffffffu, !w_ok)) {
-                    set_abort(s_abort, P.status);
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
+                    tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(smem_u32(cempty + cs));    // the warp's code words are consumed
-                    mbar_arrive(smem_u32(afull + st));
+                    // One arrive per warp, after the warp has synchronised: with an arrive per
+                    // thread, the MMAs were seen to read a stage before the stores of the last
+                    // warps to arrive had landed.  A failed wait stops the whole warp.
+                    if (__any_sync(0xffffffffu, !w_ok)) {
+                        set_abort(s_abort, P.status);
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(cempty + cs));    // the warp's code words are consumed
+                        mbar_arrive(smem_u32(afull + st));
+                    }
                 }
             }
             if (*s_abort) break;
@@ -546,9 +541,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
         cp_async_wait_all();                               // no copy into shared memory outlives the CTA
     } else {
         // ------------------------------------------------ epilogue: h = silu(g) * u
-        // Eight warps: warp w reads TMEM lanes 32 (w & 3) .. + 31 (the lanes its position in a
-        // warpgroup allows) and the 16-column chunks of parity `half` of the accumulators.
-        const int quad = warp & 3, half = (warp - kWarpEpi) >> 2;
+        // kEpiWarps1 warps: warp w reads TMEM lanes 32 (w & 3) .. + 31 (the lanes its position
+        // in a warpgroup allows) and every (kEpiWarps1 / 4)-th 16-column chunk of the
+        // accumulators, starting at chunk `half`.
+        constexpr int kHalves = kEpiWarps1 / 4;
+        const int quad = warp & 3, half = (warp - kWarpEpi1) >> 2;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         int i = 0;
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
@@ -568,12 +565,12 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 tc_fence_before();
                 mbar_arrive(smem_u32(tempty));
             }
-            for (int n0 = 16 * half; n0 < N; n0 += 32) {
+            for (int n0 = 16 * half; n0 < N; n0 += 16 * kHalves) {
                 uint32_t gv[16], uv[16];
                 tmem_ld16(d0 + n0, gv);
                 tmem_ld16(d0 + 128 + n0, uv);
                 tmem_ld_wait();
-                if (n0 + 32 >= N) {                       // this warp's last chunk: the MMAs may overwrite
+                if (n0 + 16 * kHalves >= N) {             // this warp's last chunk: the MMAs may overwrite
                     tc_fence_before();
                     mbar_arrive(smem_u32(tempty));
                 }
@@ -593,7 +590,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kWarpMma1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -894,7 +891,7 @@ __global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict_
 
 size_t g1_smem()
 {
-    return 1024 + kStagesB1 * 16384 + kCodeStages1 * 8192 + kDequantThreads * 4 * kScaleChunk * 2 +
+    return 1024 + kStagesB1 * 16384 + kCodeStages1 * 8192 + kDequantWarps1 * 32 * 4 * kScaleChunk1 * 2 +
            8 * (2 * kCodeStages1 + 2 * kStagesA1 + 2 * kStagesB1 + 5) + 256 * 4 + 16;
 }
 size_t g2_smem()
