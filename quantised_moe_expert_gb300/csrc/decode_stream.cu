@@ -228,12 +228,14 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, H = a.H, E = a.E, k = a.k, G = H / kGroup, cpr = H / 8;
+    #pragma unroll 1
     for (int i = tid; i < T * cpr; i += kSThreads) {
         const int tt = i / cpr, col = i - tt * cpr;
         cp_async16(smem_u32(s_x + tt * xs + col), reinterpret_cast<const uint4 *>(a.x + (size_t)tt * H) + col);
     }
     cp_async_commit();
     if (a.ids_in) {
+        #pragma unroll 1
         for (int i = tid; i < T * k; i += kSThreads) {
             const int tt = i / k, j = i - tt * k;
             int e = a.ids_in[i];
@@ -244,12 +246,14 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
             S.ids[tt][j] = e;
             S.p[tt][j] = bf16_bits_to_float(a.p_in[i]);
         }
+        #pragma unroll 1
         for (int tt = tid; tt < T; tt += kSThreads)
             S.ws[tt] = bf16_bits_to_float((a.has_shared && a.ws_in) ? a.ws_in[tt] : (uint16_t)0);
     } else if (warp < kConsumerWarps) {
         // one warp per token: lane l holds logits e = l + 32 r; k rounds of a warp max over
         // (key, 0xFFFF - id) give the ids in rank order (equal logits: lower id first)
         constexpr int RW = kMaxExperts / 32;
+        #pragma unroll 1
         for (int tt = warp; tt < T; tt += kConsumerWarps) {
             float val[RW];
             uint32_t key[RW];
@@ -260,6 +264,7 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
                 key[r] = e < E ? logit_key(val[r]) : 0u;
             }
             unsigned taken = 0;
+            #pragma unroll 1
             for (int j = 0; j < k; ++j) {
                 unsigned long long best = 0;
 #pragma unroll
@@ -288,14 +293,17 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
     }
     cp_async_wait_all();
     __syncthreads();
+    #pragma unroll 1
     for (int i = tid; i < T * cpr; i += kSThreads) {
         const int tt = i / cpr, col = i - tt * cpr;
         s_x[tt * xs + col] = kperm8(s_x[tt * xs + col]);   // each chunk read and written by one thread
     }
     if (blockIdx.x == 0 && !a.ids_in && a.ids_out)
+        #pragma unroll 1
         for (int i = tid; i < T * k; i += kSThreads) a.ids_out[i] = S.ids[i / k][i % k];
     __syncthreads();
     // per-token sums of x over each group (fixed order; the bias term of the gate/up GEMV)
+    #pragma unroll 1
     for (int i = tid; i < T * G; i += kSThreads) {
         const int tt = i / G, grp = i - tt * G;
         const uint4 *xr = s_x + tt * xs + grp * 8;
@@ -311,12 +319,14 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
         }
         s_sumx[i] = s;
     }
+    #pragma unroll 1
     for (int i = tid; i < T * k; i += kSThreads) S.lpos[S.ids[i / k][i % k]] = 0;   // mark the used experts
     __syncthreads();
     // distinct experts in increasing id (lpos[e] = list position), then the shared expert
     if (warp == 0) {
         const int per = (E + 31) / 32, b0 = lane * per, b1 = min(E, b0 + per);
         int local = 0;
+        #pragma unroll 1
         for (int e = b0; e < b1; ++e) local += S.lpos[e] == 0;
         int incl = local;
 #pragma unroll
@@ -325,6 +335,7 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
             if (lane >= o) incl += v;
         }
         int pos = incl - local;
+        #pragma unroll 1
         for (int e = b0; e < b1; ++e)
             if (S.lpos[e] == 0) {
                 S.list[pos] = e;
@@ -340,11 +351,13 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
     }
     __syncthreads();
     const int D = S.nlist;
+    #pragma unroll 1
     for (int i = tid; i < T * k; i += kSThreads) atomicAdd(&S.ncols[S.lpos[S.ids[i / k][i % k]]], 1);
     __syncthreads();
     if (warp == 0) {
         const int per = (D + 31) / 32, b0 = lane * per, b1 = min(D, b0 + per);
         int local = 0;
+        #pragma unroll 1
         for (int d = b0; d < b1; ++d) local += S.ncols[d];
         int incl = local;
 #pragma unroll
@@ -353,6 +366,7 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
             if (lane >= o) incl += v;
         }
         int run = incl - local;
+        #pragma unroll 1
         for (int d = b0; d < b1; ++d) {
             S.colptr[d] = run;
             run += S.ncols[d];
@@ -363,11 +377,13 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
     __syncthreads();
     // columns of each expert: its slots (in no particular order: every column is computed on
     // its own), the shared expert's in token order
+    #pragma unroll 1
     for (int i = tid; i < T * k; i += kSThreads) {
         const int d = S.lpos[S.ids[i / k][i % k]];
         S.colf[S.colptr[d] + atomicAdd(&S.cfill[d], 1)] = i;
     }
     if (a.has_shared)
+        #pragma unroll 1
         for (int tt = tid; tt < T; tt += kSThreads) S.colf[S.colptr[D - 1] + tt] = T * k + tt;
     __syncthreads();
 }
@@ -387,6 +403,7 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
         prefetch_map(&maps.sd);
     }
     int issued = 0;
+    #pragma unroll 1
     for (int w = blockIdx.x, i = 0; w < U; w += gridDim.x, ++i) {
         const int slot = i % R;
         if (i >= R && !mbar_wait_sleepy(smem_u32(&S.empty[slot]), ((i / R) - 1) & 1, a.wait_limit, &S.abort)) {
@@ -397,6 +414,7 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
         uint8_t *base = ring + (size_t)slot * geo.slot;
         const uint32_t fb = smem_u32(&S.full[slot]);
         // this unit into the slot, and the unit one ring length ahead into L2
+        #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
             const int wu = pass == 0 ? w : w + R * (int)gridDim.x;
             if (wu >= U) break;
@@ -409,6 +427,7 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
                 if (pass == 0) {
                     const CUtensorMap *mg = shr ? &maps.sg : &maps.g, *mu = shr ? &maps.su : &maps.u;
                     mbar_arrive_expect_tx(fb, geo.bytes1);
+                    #pragma unroll 1
                     for (int j = 0; j < geo.nb1; ++j) {
                         tma_load_2d(smem_u32(base + j * kBox1), mg, j * 128, row0, fb);
                         tma_load_2d(smem_u32(base + geo.up_off + j * kBox1), mu, j * 128, row0, fb);
@@ -437,6 +456,7 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
                 if (pass == 0) {
                     const CUtensorMap *md = shr ? &maps.sd : &maps.d;
                     mbar_arrive_expect_tx(fb, (uint32_t)geo.nb2 * kBox2 + 2 * sb2);
+                    #pragma unroll 1
                     for (int j = 0; j < geo.nb2; ++j) tma_load_2d(smem_u32(base + j * kBox2), md, j * 128, row0, fb);
                     bulk_load(smem_u32(base + geo.sc2_off), qd.scales + so, sb2, fb);
                     bulk_load(smem_u32(base + geo.sc2_off + kRows2 * GI * 2), qd.biases + so, sb2, fb);
@@ -450,6 +470,7 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
         issued = i + 1;
     }
     // every issued copy lands before the CTA may exit
+    #pragma unroll 1
     for (int q = issued > R ? issued - R : 0; q < issued; ++q)
         mbar_wait(smem_u32(&S.full[q % R]), (q / R) & 1, kDrainLimit, nullptr);
 }
@@ -469,6 +490,7 @@ __device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U
         double ex = 0.0;
         if (lane < k) ex = exp((double)S.lg[tt][lane] - (double)S.lg[tt][0]);
         double den = 0.0;
+        #pragma unroll 1
         for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order j = 0..k-1
         if (lane < k) {
             const uint16_t pb = double_to_bf16_bits(ex / den);
@@ -498,8 +520,11 @@ __device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U
     bool picks = a.ids_in != nullptr;       // given routing: S.p and S.ws were filled in phase 0
     // the published pick weights into shared memory (once every token's are out), for the combines
     auto take_picks = [&]() {
-#pragma unroll 8
-        for (int q = 0; q < T * k; ++q) S.p[q / k][q % k] = bf16_bits_to_float(__ldcg(a.p_glob + q));
+#pragma unroll 1
+        for (int tt = 0; tt < T; ++tt)
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) S.p[tt][j] = bf16_bits_to_float(__ldcg(a.p_glob + tt * k + j));
+        #pragma unroll 1
         for (int q = 0; q < T; ++q) S.ws[q] = bf16_bits_to_float(__ldcg(a.ws_glob + q));
     };
     long long polls = 0;
@@ -516,6 +541,7 @@ __device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U
         }
         polls = 0;
         __threadfence();
+        #pragma unroll 1
         for (; done < avail; ++done) {
             const int w = (int)blockIdx.x + done * (int)gridDim.x;
             if (w < U1) {
@@ -548,6 +574,7 @@ __device__ __noinline__ void combine_block(SSmem &S, const FusedDecodeArgs &a, i
 {
     const int tid = threadIdx.x, T = a.T, H = a.H, k = a.k;
     const int nrow = min(kRows2, H - rb * kRows2);
+    #pragma unroll 1
     for (int q = tid; q < nrow * T; q += kConsumers) {
         const int tt = q / nrow, row = rb * kRows2 + (q - tt * nrow);
         float ys[kMaxTopK + 1];                     // every load in flight before the first add
@@ -598,6 +625,7 @@ __global__ void __launch_bounds__(kSThreads, MINB)
         S.ncomb = 0;
         fence_mbar_init();
     }
+    #pragma unroll 1
     for (int e = tid; e < kMaxList; e += kSThreads) {
         S.lpos[e] = -1;
         S.ncols[e] = 0;
@@ -759,6 +787,7 @@ __global__ void __launch_bounds__(kSThreads, MINB)
                 break;
             }
             // the expert's h columns into shared memory (L2 reads, after the acquire above)
+            #pragma unroll 1
             for (int idx = tid, cpr = I / 8; idx < ncol * cpr; idx += kConsumers) {
                 const int c = idx / cpr, ch = idx - c * cpr;
                 *reinterpret_cast<uint4 *>(s_h + c * geo.h_stride + ch * 8) =
@@ -839,6 +868,7 @@ __global__ void __launch_bounds__(kSThreads, MINB)
     }
     // the remaining combines of this CTA, each as soon as the signal thread queues it, until it has
     // counted every unit (bounded)
+    #pragma unroll 1
     for (long long polls = 0;; ++polls) {
         if (tid == 0) {
             const int done = ld_acquire_cta(&S.sig_done);
