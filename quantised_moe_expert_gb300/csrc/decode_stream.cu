@@ -93,7 +93,8 @@ struct SSmem {
     float lg[kDecodeMaxTok][kMaxTopK];     // fp32 logit of each pick
     float p[kDecodeMaxTok][kMaxTopK];
     float ws[kDecodeMaxTok];
-    int lpos[kMaxList];                    // list position of each used expert, -1 if unused
+    int cnt[kMaxList];                     // picks of each expert
+    int lpos[kMaxList];                    // list position of each used expert
     int cfill[kMaxList];
     int list[kMaxList];
     int ncols[kMaxList];
@@ -221,21 +222,61 @@ __device__ __forceinline__ int col_token(int f, int T, int k) { return f < 0 ? -
 
 // ------------------------------------------------------------------ phase 0 (all threads)
 //
-// x rows into shared memory in the codes' k order, their per-group sums, the routing
-// (top-k of the fp32 logits, or the caller's ids), the list of distinct experts and
-// their columns.
+// x rows into shared memory in the codes' k order and their per-group sums (the caller's
+// input only: this part overlaps the router kernel), then the routing (top-k of the fp32
+// logits, or the caller's ids), the list of distinct experts and their columns.  The code
+// is kept short: at T = 1 every SM fetches it cold, and that fetch is on the critical path.
+__device__ __forceinline__ float key_logit(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4 *s_x, float *s_sumx, int xs)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, H = a.H, E = a.E, k = a.k, G = H / kGroup, cpr = H / 8;
-    #pragma unroll 1
+#pragma unroll 1
     for (int i = tid; i < T * cpr; i += kSThreads) {
         const int tt = i / cpr, col = i - tt * cpr;
         cp_async16(smem_u32(s_x + tt * xs + col), reinterpret_cast<const uint4 *>(a.x + (size_t)tt * H) + col);
     }
     cp_async_commit();
+#pragma unroll 1
+    for (int e = tid; e < kMaxList; e += kSThreads) {
+        S.cnt[e] = 0;
+        S.cfill[e] = 0;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+#pragma unroll 1
+    for (int i = tid; i < T * cpr; i += kSThreads) {
+        const int tt = i / cpr, col = i - tt * cpr;
+        s_x[tt * xs + col] = kperm8(s_x[tt * xs + col]);   // each chunk read and written by one thread
+    }
+    __syncthreads();
+    // per-token sums of x over each group (fixed order; the bias term of the gate/up GEMV)
+#pragma unroll 1
+    for (int i = tid; i < T * G; i += kSThreads) {
+        const int tt = i / G, grp = i - tt * G;
+        const uint4 *xr = s_x + tt * xs + grp * 8;
+        float sum = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = xr[c];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                sum += __uint_as_float(w4[q] << 16);
+                sum += __uint_as_float(w4[q] & 0xFFFF0000u);
+            }
+        }
+        s_sumx[i] = sum;
+    }
+
+    // everything below reads what the preceding kernels wrote (logits, gamma, zeroed counters)
+    pdl_wait();
     if (a.ids_in) {
-        #pragma unroll 1
+#pragma unroll 1
         for (int i = tid; i < T * k; i += kSThreads) {
             const int tt = i / k, j = i - tt * k;
             int e = a.ids_in[i];
@@ -245,146 +286,109 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
             }
             S.ids[tt][j] = e;
             S.p[tt][j] = bf16_bits_to_float(a.p_in[i]);
+            atomicAdd(&S.cnt[e], 1);
         }
-        #pragma unroll 1
+#pragma unroll 1
         for (int tt = tid; tt < T; tt += kSThreads)
             S.ws[tt] = bf16_bits_to_float((a.has_shared && a.ws_in) ? a.ws_in[tt] : (uint16_t)0);
-    } else if (warp < kConsumerWarps) {
-        // one warp per token: lane l holds logits e = l + 32 r; k rounds of a warp max over
-        // (key, 0xFFFF - id) give the ids in rank order (equal logits: lower id first)
+    } else {
+        // one warp per token: lane l holds the keys of logits e = l + 32 r; each of the k rounds
+        // takes the largest key (warp max), then the lowest id holding it (warp min), so the ids
+        // come in rank order with equal logits going to the lower id
         constexpr int RW = kMaxExperts / 32;
-        #pragma unroll 1
-        for (int tt = warp; tt < T; tt += kConsumerWarps) {
-            float val[RW];
+#pragma unroll 1
+        for (int tt = warp; tt < T; tt += kSThreads / 32) {
             uint32_t key[RW];
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
                 const int e = lane + 32 * r;
-                val[r] = e < E ? __ldg(a.logits + (size_t)tt * E + e) : 0.f;
-                key[r] = e < E ? logit_key(val[r]) : 0u;
+                key[r] = e < E ? logit_key(__ldg(a.logits + (size_t)tt * E + e)) : 0u;   // 0: below every logit
             }
-            unsigned taken = 0;
-            #pragma unroll 1
+#pragma unroll 1
             for (int j = 0; j < k; ++j) {
-                unsigned long long best = 0;
+                uint32_t bk = key[0];
+                int br = 0;
 #pragma unroll
-                for (int r = 0; r < RW; ++r) {
-                    const int e = lane + 32 * r;
-                    const unsigned long long c = ((unsigned long long)key[r] << 32) | (unsigned)(0xFFFF - e);
-                    if (e < E && !(taken & (1u << r)) && c > best) best = c;
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-                    best = other > best ? other : best;
-                }
-                const int id = 0xFFFF - (int)(best & 0xFFFFu);
-                if ((id & 31) == lane) {
-                    taken |= 1u << (id >> 5);
-                    float v = 0.f;
+                for (int r = 1; r < RW; ++r)
+                    if (key[r] > bk) {
+                        bk = key[r];
+                        br = r;
+                    }
+                const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+                const uint32_t mine = (uint32_t)(lane + 32 * br);
+                const uint32_t id = __reduce_min_sync(0xffffffffu, bk == mk ? mine : 0xffffffffu);
+                if (id == mine) {
 #pragma unroll
                     for (int r = 0; r < RW; ++r)
-                        if ((id >> 5) == r) v = val[r];
-                    S.ids[tt][j] = id;
-                    S.lg[tt][j] = v;
+                        if (r == br) key[r] = 0u;
+                    S.ids[tt][j] = (int)id;
+                    S.lg[tt][j] = key_logit(mk);
+                    atomicAdd(&S.cnt[id], 1);
                 }
             }
         }
     }
-    cp_async_wait_all();
     __syncthreads();
-    #pragma unroll 1
-    for (int i = tid; i < T * cpr; i += kSThreads) {
-        const int tt = i / cpr, col = i - tt * cpr;
-        s_x[tt * xs + col] = kperm8(s_x[tt * xs + col]);   // each chunk read and written by one thread
-    }
     if (blockIdx.x == 0 && !a.ids_in && a.ids_out)
-        #pragma unroll 1
+#pragma unroll 1
         for (int i = tid; i < T * k; i += kSThreads) a.ids_out[i] = S.ids[i / k][i % k];
-    __syncthreads();
-    // per-token sums of x over each group (fixed order; the bias term of the gate/up GEMV)
-    #pragma unroll 1
-    for (int i = tid; i < T * G; i += kSThreads) {
-        const int tt = i / G, grp = i - tt * G;
-        const uint4 *xr = s_x + tt * xs + grp * 8;
-        float s = 0.f;
-        for (int c = 0; c < 8; ++c) {
-            const uint4 v = xr[c];
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                s += __uint_as_float(w4[q] << 16);
-                s += __uint_as_float(w4[q] & 0xFFFF0000u);
-            }
-        }
-        s_sumx[i] = s;
-    }
-    #pragma unroll 1
-    for (int i = tid; i < T * k; i += kSThreads) S.lpos[S.ids[i / k][i % k]] = 0;   // mark the used experts
-    __syncthreads();
-    // distinct experts in increasing id (lpos[e] = list position), then the shared expert
+    // the distinct experts in increasing id (list position lpos), their column counts and
+    // offsets, then the shared expert's T columns
     if (warp == 0) {
         const int per = (E + 31) / 32, b0 = lane * per, b1 = min(E, b0 + per);
-        int local = 0;
-        #pragma unroll 1
-        for (int e = b0; e < b1; ++e) local += S.lpos[e] == 0;
-        int incl = local;
+        int nloc = 0, cloc = 0;
+#pragma unroll 1
+        for (int e = b0; e < b1; ++e) {
+            const int c = S.cnt[e];
+            nloc += c > 0;
+            cloc += c;
+        }
+        int ni = nloc, ci = cloc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
+            const int vn = __shfl_up_sync(0xffffffffu, ni, o), vc = __shfl_up_sync(0xffffffffu, ci, o);
+            if (lane >= o) {
+                ni += vn;
+                ci += vc;
+            }
         }
-        int pos = incl - local;
-        #pragma unroll 1
-        for (int e = b0; e < b1; ++e)
-            if (S.lpos[e] == 0) {
+        int pos = ni - nloc, col = ci - cloc;
+#pragma unroll 1
+        for (int e = b0; e < b1; ++e) {
+            const int c = S.cnt[e];
+            if (c > 0) {
+                if (c > T) record_status(a.status, MOE_ERR_DEVICE);   // an id repeated within a token
                 S.list[pos] = e;
-                S.lpos[e] = pos++;
+                S.lpos[e] = pos;
+                S.ncols[pos] = c;
+                S.colptr[pos] = col;
+                ++pos;
+                col += c;
             }
+        }
         if (lane == 31) {
-            S.nlist = incl + (a.has_shared ? 1 : 0);
+            int D = ni;
             if (a.has_shared) {
-                S.list[incl] = E;
-                S.ncols[incl] = T;
+                S.list[D] = E;
+                S.ncols[D] = T;
+                S.colptr[D] = ci;
+                ++D;
             }
+            S.colptr[D] = ci + (a.has_shared ? T : 0);
+            S.nlist = D;
         }
-    }
-    __syncthreads();
-    const int D = S.nlist;
-    #pragma unroll 1
-    for (int i = tid; i < T * k; i += kSThreads) atomicAdd(&S.ncols[S.lpos[S.ids[i / k][i % k]]], 1);
-    __syncthreads();
-    if (warp == 0) {
-        const int per = (D + 31) / 32, b0 = lane * per, b1 = min(D, b0 + per);
-        int local = 0;
-        #pragma unroll 1
-        for (int d = b0; d < b1; ++d) local += S.ncols[d];
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - local;
-        #pragma unroll 1
-        for (int d = b0; d < b1; ++d) {
-            S.colptr[d] = run;
-            run += S.ncols[d];
-            if (S.ncols[d] > T) record_status(a.status, MOE_ERR_DEVICE);   // an id repeated within a token
-        }
-        if (lane == 31) S.colptr[D] = incl;
     }
     __syncthreads();
     // columns of each expert: its slots (in no particular order: every column is computed on
     // its own), the shared expert's in token order
-    #pragma unroll 1
+#pragma unroll 1
     for (int i = tid; i < T * k; i += kSThreads) {
         const int d = S.lpos[S.ids[i / k][i % k]];
         S.colf[S.colptr[d] + atomicAdd(&S.cfill[d], 1)] = i;
     }
     if (a.has_shared)
-        #pragma unroll 1
-        for (int tt = tid; tt < T; tt += kSThreads) S.colf[S.colptr[D - 1] + tt] = T * k + tt;
+#pragma unroll 1
+        for (int tt = tid; tt < T; tt += kSThreads) S.colf[S.colptr[S.nlist - 1] + tt] = T * k + tt;
     __syncthreads();
 }
 
@@ -624,12 +628,6 @@ __global__ void __launch_bounds__(kSThreads, MINB)
         S.sig_done = 0;
         S.ncomb = 0;
         fence_mbar_init();
-    }
-    #pragma unroll 1
-    for (int e = tid; e < kMaxList; e += kSThreads) {
-        S.lpos[e] = -1;
-        S.ncols[e] = 0;
-        S.cfill[e] = 0;
     }
     phase0(S, a, s_x, s_sumx, xs);
 
@@ -1005,11 +1003,15 @@ cudaError_t launch_decode_stream(const FusedDecodeArgs &a, cudaStream_t st)
     cfg.blockDim = dim3(kSThreads);
     cfg.dynamicSmemBytes = geo.dyn;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    // cooperative (the CTAs wait on one another), and allowed to start while the router
+    // kernel before it still runs: phase 0 waits for it after staging x
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, maps, a, geo);
 }
 

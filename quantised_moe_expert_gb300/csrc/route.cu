@@ -6,6 +6,7 @@
 // normalised over the picks and rounded to bf16, shared slot weight
 // bf16(sigmoid(bf16(gate))).  The router is MLX affine 8-bit in groups of 64.
 #include "kernels.cuh"
+#include "tc_ptx.cuh"
 
 namespace qmoe {
 
@@ -21,6 +22,7 @@ namespace qmoe {
 // token's logits are the same bits at every batch size.
 __global__ void __launch_bounds__(256) route_gemv_kernel(RouteArgs a)
 {
+    tc::pdl_trigger();   // the fused decode kernel may start its prologue (it waits before reading our outputs)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y * 8;
     const int H = a.H, E = a.E, G = a.H / kGroup;
