@@ -47,11 +47,12 @@ struct PermuteArgs {
     const int32_t *ids;
     const int32_t *hist;
     int32_t *counts, *offsets, *perm, *inv_perm;
-    int32_t *nwork;               // [3]: decode items, gemm1 tiles, gemm2 tiles
+    int32_t *nwork;               // [5]: decode items, gemm1 items, gemm2 items, gemm1 / gemm2 items of the big kernels
     WorkItem *work_dec, *work_g1, *work_g2;
     int *status;
     int T, E, k, nblk, has_shared;
     int build_work;               // block 0 also writes the expert kernels' work lists
+    int small_tiles;              // GEMM lists split for the small-tile kernels
     int max_items[3];             // capacity of each work list
 };
 
@@ -70,6 +71,7 @@ struct WorklistArgs {
     int *zero;                    // non-null: zero[0, nzero) (counters of the fused decode kernel)
     int nzero;
     int T, E, has_shared;
+    int small_tiles;              // GEMM lists split for the small-tile kernels
     int max_items[3];
 };
 
@@ -110,6 +112,7 @@ struct ReduceArgs {
 struct PrefillArgs {
     const uint16_t *x;            // bf16 [T, H]
     uint16_t *x16;                // fp16 [T, H] scratch (K-permuted)
+    float *xsum;                  // f32 [T, H / 64] scratch: group sums of x16
     uint16_t *hs;                 // fp16 [T*k + T, I] scratch, expert-sorted rows
     QMatDev gate, up, down, s_gate, s_up, s_down;
     const int32_t *nwork, *offsets, *perm;
@@ -123,6 +126,13 @@ struct PrefillArgs {
 };
 
 cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st);
+
+// Small-tile grouped GEMMs (items of at most kSmallN tokens, exact int4 codes on mma.sync):
+// whether a layer shape takes them, and their launches (items [nwork[3], nwork[1]) of the
+// gate/up list, [nwork[4], nwork[2]) of the down list).
+bool prefill_small_fits(int H, int I);
+cudaError_t launch_small_gateup(const PrefillArgs &a, cudaStream_t st);
+cudaError_t launch_small_down(const PrefillArgs &a, cudaStream_t st);
 
 struct FusedDecodeArgs {
     const uint16_t *x;            // bf16 [T, H]

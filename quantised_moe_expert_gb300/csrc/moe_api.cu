@@ -134,6 +134,7 @@ PermuteArgs permute_args(const moe_config &c, const int32_t *ids, int T, int32_t
     pa.nblk = L.nblk;
     pa.has_shared = c.has_shared;
     pa.build_work = 1;
+    pa.small_tiles = prefill_small_fits(c.hidden, c.inter) ? 1 : 0;
     pa.max_items[0] = L.max_wd;
     pa.max_items[1] = L.max_w1;
     pa.max_items[2] = L.max_w2;
@@ -202,6 +203,7 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     PrefillArgs a{};
     a.x = ea.x;
     a.x16 = ws_at<uint16_t>(ws, L.x16);
+    a.xsum = ws_at<float>(ws, L.xsum);
     a.hs = ws_at<uint16_t>(ws, L.h);
     a.gate = ea.gate;
     a.up = ea.up;
@@ -384,6 +386,7 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     wa.T = T;
     wa.E = cfg->n_experts;
     wa.has_shared = cfg->has_shared;
+    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter) ? 1 : 0;
     wa.max_items[0] = L.max_wd;
     wa.max_items[1] = L.max_w1;
     wa.max_items[2] = L.max_w2;

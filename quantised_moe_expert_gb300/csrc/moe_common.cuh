@@ -22,6 +22,8 @@ constexpr int kDecodeMaxTok = 16;   // decode GEMV handles up to 16 tokens per e
 constexpr int kTileM = 128;
 constexpr int kTileN1 = 128;        // tokens per tile, gate/up GEMM (two accumulators)
 constexpr int kTileN2 = 256;        // tokens per tile, down GEMM
+constexpr int kSmallN = 32;         // tokens per item of the small-tile GEMMs (experts of at most kSmallN tokens)
+constexpr int kBigTok = kSmallN + 1;   // experts with at least this many tokens go to the tensor-memory GEMMs
 
 // One unit of work of a grouped kernel: an expert (E = shared) and a token range
 // [tok0, tok0 + ntok) of its permuted slot list.
@@ -45,12 +47,13 @@ struct WsLayout {
     size_t offsets;    // i32 [E + 1]
     size_t perm;       // i32 [T*k]
     size_t inv_perm;   // i32 [T*k]
-    size_t nwork;      // i32 [4]: decode active experts, gemm1 tiles, gemm2 tiles
+    size_t nwork;      // i32 [8]: decode items, gemm1 items, gemm2 items, big gemm1 / gemm2 items
     size_t counters;   // i32 [(E + 1 + H/128 + 1) * 32]: fused decode counters, 128 B apart
     size_t work_dec;   // WorkItem [E + 1]
     size_t work_g1;    // WorkItem [max tiles gemm1]
     size_t work_g2;    // WorkItem [max tiles gemm2]
     size_t x16;        // fp16 [T, H] (prefill B operand)
+    size_t xsum;       // f32 [T, H / 64] group sums of x16 (small-tile gate/up GEMM)
     size_t h;          // fp16 [T*k + T, I] (decode: slot order; prefill: expert-sorted, K-permuted)
     size_t yslot;      // f32 [T*k + T, H] (decode)
     size_t acc;        // f32 [T, H] (prefill accumulation)
@@ -80,8 +83,8 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
     L.nblk = (int)((Tz + kTokBlock - 1) / kTokBlock);
-    L.max_w1 = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kTileN1);
-    L.max_w2 = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kTileN2);
+    L.max_w1 = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kSmallN);   // bounds both item sizes
+    L.max_w2 = L.max_w1;
     L.status = take(256);
     L.logits = take(4 * Tz * E);
     L.ids = take(4 * Tz * k);
@@ -93,13 +96,14 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.offsets = take(4 * (E + 1));
     L.perm = take(4 * Tz * k);
     L.inv_perm = take(4 * Tz * k);
-    L.nwork = take(16);
+    L.nwork = take(32);
     L.counters = take(4 * 32 * (E + 1 + (H + 127) / 128 + 1));
     L.max_wd = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kDecodeMaxTok);
     L.work_dec = take(sizeof(WorkItem) * (size_t)L.max_wd);
     L.work_g1 = take(sizeof(WorkItem) * (size_t)L.max_w1);
     L.work_g2 = take(sizeof(WorkItem) * (size_t)L.max_w2);
     L.x16 = take(2 * Tz * H);
+    L.xsum = take(4 * Tz * (H / 64));
     L.h = take(2 * Tz * (k + 1) * I);
     L.yslot = take(4 * Tz * (k + 1) * H);
     L.acc = take(4 * Tz * H);

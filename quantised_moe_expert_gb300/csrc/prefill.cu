@@ -221,8 +221,14 @@ __global__ void __launch_bounds__(kThreads1, 1)
                        const G1Params P)
 {
     const int H = P.H, I = P.I, G = H / kGroup, nk = G, MB = (I + 127) / 128, Tk = P.T * P.k;
-    const int ntiles = __ldg(P.nwork + 1) * MB;
-    if ((int)blockIdx.x >= ntiles) return;
+    const int ntiles = __ldg(P.nwork + 3) * MB;          // the big items lead the list
+    // This grid may start while the small-tile gate/up GEMM still runs (programmatic
+    // dependent launch): it reads nothing that grid writes, and every CTA waits for that
+    // grid before it exits, so the kernels after both see all of h.
+    if ((int)blockIdx.x >= ntiles) {
+        pdl_wait();
+        return;
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sB = smem;                           // SB x 16 KB (128 token rows x 128 B)
@@ -594,6 +600,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    pdl_wait();
 }
 
 // --------------------------------------------------------------- down GEMM
@@ -607,8 +614,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap map_h, const G2Params P)
 {
     const int H = P.H, I = P.I, GI = I / kGroup, nk = GI, MB = (H + 127) / 128, Tk = P.T * P.k;
-    const int ntiles = __ldg(P.nwork + 2) * MB;
-    if ((int)blockIdx.x >= ntiles) return;
+    const int ntiles = __ldg(P.nwork + 4) * MB;          // the big items lead the list
+    // may start while the small-tile down GEMM still runs; waits for it before exiting
+    if ((int)blockIdx.x >= ntiles) {
+        pdl_wait();
+        return;
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;                           // S x 16 KB
@@ -864,26 +875,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    pdl_wait();
 }
 
-// x (bf16 [T, H]) -> x16 (fp16 [T, H], K-permuted within chunks of 8)
-__global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x16, size_t nchunks)
+// x (bf16) -> x16 (fp16, the codes' k order within each chunk of 8) and, per token and
+// group of 64, the sum of the fp16 values in a fixed order (the small-tile GEMM's bias
+// term).  One thread per (token, group).
+__global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x16, float *__restrict__ xsum,
+                                 size_t ngroups)
 {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += (size_t)gridDim.x * blockDim.x) {
-        const uint4 v = x[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float f[8];
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < ngroups; i += (size_t)gridDim.x * blockDim.x) {
+        float sum = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = x[i * 8 + c];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            float f[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = __uint_as_float(w[j] << 16);
-            f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = __uint_as_float(w[j] << 16);
+                f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+            const __half2 h0 = __floats2half2_rn(f[0], f[4]), h1 = __floats2half2_rn(f[1], f[5]);
+            const __half2 h2 = __floats2half2_rn(f[2], f[6]), h3 = __floats2half2_rn(f[3], f[7]);
+            uint4 o;
+            o.x = h2u(h0);
+            o.y = h2u(h1);
+            o.z = h2u(h2);
+            o.w = h2u(h3);
+            x16[i * 8 + c] = o;
+            const __half2 hs[4] = {h0, h1, h2, h3};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sum += __low2float(hs[j]);
+                sum += __high2float(hs[j]);
+            }
         }
-        uint4 o;
-        o.x = h2u(__floats2half2_rn(f[0], f[4]));
-        o.y = h2u(__floats2half2_rn(f[1], f[5]));
-        o.z = h2u(__floats2half2_rn(f[2], f[6]));
-        o.w = h2u(__floats2half2_rn(f[3], f[7]));
-        x16[i] = o;
+        xsum[i] = sum;
     }
 }
 
@@ -898,6 +926,24 @@ size_t g2_smem()
 {
     return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + kCodeStages2 * 4096 + 4 * kScaleChunk * 128 * 2 +
            8 * (2 * kCodeStages2 + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 1024 * 4 + 16;
+}
+
+// Launch allowed (pdl) to begin while the previous kernel of the stream still runs.
+template <typename... Args>
+cudaError_t launch_pdl(bool pdl, void (*kern)(Args...), int grid, int threads, size_t smem, cudaStream_t st,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 int sm_count()
@@ -916,10 +962,10 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     const int H = a.H, I = a.I, E = a.E, T = a.T, k = a.k;
     // x -> fp16, K-permuted
     {
-        const size_t n = (size_t)T * H / 8;
+        const size_t n = (size_t)T * (H / kGroup);
         const unsigned grid = (unsigned)std::min<size_t>((n + 255) / 256, 152 * 8);
         convert_x_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4 *>(a.x), reinterpret_cast<uint4 *>(a.x16),
-                                               n);
+                                               a.xsum, n);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -981,8 +1027,12 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     auto k1 = gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1>;
     cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     const int tiles1 = a.max_w1 * ((I + 127) / 128);
-    k1<<<std::min(sm_count(), tiles1), kThreads1, s1, st>>>(mgc, muc, msgc, msuc, p1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const bool small = prefill_small_fits(H, I);   // items of small experts: mma.sync tiles (nwork[3] on)
+    if (small && (e = launch_small_gateup(a, st)) != cudaSuccess) return e;
+    // behind the small-tile kernel (if any) as its programmatic dependent
+    if ((e = launch_pdl(small, k1, std::min(sm_count(), tiles1), kThreads1, s1, st, mgc, muc, msgc, msuc, p1)) !=
+        cudaSuccess)
+        return e;
 
     G2Params p2{};
     p2.nwork = a.nwork;
@@ -1009,8 +1059,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     auto k2 = gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2>;
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
     const int tiles2 = a.max_w2 * ((H + 127) / 128);
-    k2<<<std::min(sm_count(), tiles2), kThreads, s2, st>>>(mdc, msdc, mh, p2);
-    return cudaGetLastError();
+    if (small && (e = launch_small_down(a, st)) != cudaSuccess) return e;
+    return launch_pdl(small, k2, std::min(sm_count(), tiles2), kThreads, s2, st, mdc, msdc, mh, p2);
 }
 
 }  // namespace qmoe

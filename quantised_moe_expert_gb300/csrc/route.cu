@@ -230,40 +230,55 @@ __device__ int warp_exclusive_scan(int *a, int n)
 }
 
 // Work lists of the expert kernels from the per-expert slot counts: expert e
-// (in increasing id, the shared expert last as id E) contributes
-// ceil(count_e / n) items of at most n tokens, for n = 16 (decode GEMV),
-// kTileN1 (gate/up GEMM) and kTileN2 (down GEMM).  Called by a whole block.
-__device__ void build_work_lists(const int *s_cnt, int E, int T, int has_shared, int32_t *nwork,
+// (in increasing id, the shared expert last as id E) contributes items of at most
+// n tokens.  Decode GEMV list: n = 16.  GEMM lists (gate/up, down): an expert with at
+// least kBigTok tokens gets items of kTileN1 / kTileN2 tokens for the tensor-memory
+// GEMMs, placed first (nwork[3] / nwork[4] of them); the others get items of kSmallN
+// tokens for the small-tile kernels, placed after.  Without small tiles (small == 0)
+// every expert takes the first form.  Called by a whole block.
+__device__ void build_work_lists(const int *s_cnt, int E, int T, int has_shared, int small, int32_t *nwork,
                                  WorkItem *work_dec, WorkItem *work_g1, WorkItem *work_g2, const int *max_items,
                                  int *status)
 {
-    __shared__ int s_items[3][kMaxExperts + 2];
+    // rows: 0 decode, 1 gate/up big, 2 down big, 3 gate/up small, 4 down small
+    __shared__ int s_items[5][kMaxExperts + 2];
     const int tid = threadIdx.x;
-    const int tile_n[3] = {kDecodeMaxTok, kTileN1, kTileN2};
-    for (int w = 0; w < 3; ++w)
+    const int tile_n[5] = {kDecodeMaxTok, kTileN1, kTileN2, kSmallN, kSmallN};
+    const int big_min = small ? kBigTok : 0;
+    for (int w = 0; w < 5; ++w)
         for (int e = tid; e <= E; e += blockDim.x) {
             const int c = e < E ? s_cnt[e] : (has_shared ? T : 0);
-            s_items[w][e] = (c + tile_n[w] - 1) / tile_n[w];
+            const bool take = w == 0 || (w < 3 ? c >= big_min : c < big_min);
+            s_items[w][e] = take ? (c + tile_n[w] - 1) / tile_n[w] : 0;
         }
     __syncthreads();
-    if (tid < 3 * 32) {
+    if (tid < 5 * 32) {
         const int w = tid >> 5;
-        int run = warp_exclusive_scan(s_items[w], E + 1);
-        if ((tid & 31) == 0) {
-            if (run > max_items[w]) {        // counts inconsistent with T*k: build nothing
-                record_status(status, MOE_ERR_DEVICE);
-                run = -1;
-            }
-            s_items[w][E + 1] = run;
-            nwork[w] = run < 0 ? 0 : run;
-        }
+        const int run = warp_exclusive_scan(s_items[w], E + 1);
+        if ((tid & 31) == 0) s_items[w][E + 1] = run;
     }
     __syncthreads();
-    WorkItem *lists[3] = {work_dec, work_g1, work_g2};
-    for (int w = 0; w < 3; ++w)
-        for (int e = tid; e <= E && s_items[w][E + 1] >= 0; e += blockDim.x) {
+    if (tid == 0) {
+        const int n1 = s_items[1][E + 1] + s_items[3][E + 1], n2 = s_items[2][E + 1] + s_items[4][E + 1];
+        const bool bad = s_items[0][E + 1] > max_items[0] || n1 > max_items[1] || n2 > max_items[2];
+        if (bad) record_status(status, MOE_ERR_DEVICE);   // counts inconsistent with T*k: build nothing
+        nwork[0] = bad ? 0 : s_items[0][E + 1];
+        nwork[1] = bad ? 0 : n1;
+        nwork[2] = bad ? 0 : n2;
+        nwork[3] = bad ? 0 : s_items[1][E + 1];
+        nwork[4] = bad ? 0 : s_items[2][E + 1];
+        s_items[0][E + 1] = bad ? -1 : s_items[0][E + 1];
+    }
+    __syncthreads();
+    if (s_items[0][E + 1] < 0) return;
+    WorkItem *lists[5] = {work_dec, work_g1, work_g2, work_g1, work_g2};
+    for (int w = 0; w < 5; ++w) {
+        const int base = w >= 3 ? s_items[w - 2][E + 1] : 0;   // small items after the big ones
+        for (int e = tid; e <= E; e += blockDim.x) {
             const int c = e < E ? s_cnt[e] : (has_shared ? T : 0);
-            int pos = s_items[w][e];
+            int pos = base + s_items[w][e];
+            const bool take = w == 0 || (w < 3 ? c >= big_min : c < big_min);
+            if (!take) continue;
             for (int t0 = 0; t0 < c; t0 += tile_n[w]) {
                 WorkItem it;
                 it.expert = e;
@@ -273,10 +288,9 @@ __device__ void build_work_lists(const int *s_cnt, int E, int T, int has_shared,
                 lists[w][pos++] = it;
             }
         }
+    }
 }
 
-// Work lists alone, from caller-supplied counts (standalone expert FFN call).
-// Also clears the status word: it is the first kernel of that call.
 __global__ void __launch_bounds__(256) worklist_kernel(WorklistArgs a)
 {
     __shared__ int s_cnt[kMaxExperts];
@@ -291,7 +305,7 @@ __global__ void __launch_bounds__(256) worklist_kernel(WorklistArgs a)
         s_cnt[e] = c;
     }
     __syncthreads();
-    build_work_lists(s_cnt, a.E, a.T, a.has_shared, a.nwork, a.work_dec, a.work_g1, a.work_g2, a.max_items,
+    build_work_lists(s_cnt, a.E, a.T, a.has_shared, a.small_tiles, a.nwork, a.work_dec, a.work_g1, a.work_g2, a.max_items,
                      a.status);
 }
 
@@ -354,7 +368,8 @@ __global__ void __launch_bounds__(1024) permute_kernel(PermuteArgs a)
         for (int e = tid; e < E; e += blockDim.x) a.counts[e] = s_cnt[e];
         for (int e = tid; e <= E; e += blockDim.x) a.offsets[e] = s_off[e];
         if (a.build_work)
-            build_work_lists(s_cnt, E, a.T, a.has_shared, a.nwork, a.work_dec, a.work_g1, a.work_g2, a.max_items,
+            build_work_lists(s_cnt, E, a.T, a.has_shared, a.small_tiles, a.nwork, a.work_dec, a.work_g1, a.work_g2,
+                             a.max_items,
                              a.status);
     }
 
