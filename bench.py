@@ -457,16 +457,16 @@ def run_reference(args, wl, rank, world, steps, warmup):
 
 
 def traffic_for(kernel_key, workload):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source has not changed since."""
+    """DRAM bytes per launch from a committed ncu summary, if no source of the stage has changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         ent = d[kernel_key][workload]
-        src = os.path.join(ROOT, ent["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if h != ent["source_sha"]:
-            return None
+        for src, sha in zip(ent["sources"], ent["source_shas"]):
+            h = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+            if h != sha:
+                return None
         return float(ent["bytes_per_launch"])
     except Exception:
         return None
@@ -498,6 +498,13 @@ def main():
                 "traffic": traffic_for("decode_expert_ffn", wl.name),
                 "kernel": "expert-FFN stage (decode gate/up + down GEMV + slot combine)",
                 "algorithmic_bytes_per_launch": st["expert_bytes"], "peak_source": peak_src}
+    elif st["flops"] / max(st["expert_bytes"], 1.0) < tc * 1e12 / (hbm * 1e9):
+        # below the ridge point (e.g. T = 512: ~16 tokens per expert) the weights bound the stage
+        ach = st["expert_bytes"] / (st["ms"] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": traffic_for("prefill_expert_ffn", wl.name),
+                "kernel": "expert-FFN stage (grouped GEMMs)", "algorithmic_bytes_per_launch": st["expert_bytes"],
+                "tensor_frac": st["flops"] / (st["ms"] / 1e3) / 1e12 / tc, "peak_source": peak_src}
     else:
         ach = st["flops"] / (st["ms"] / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": tc, "unit": "TFLOP/s", "frac": ach / tc,
