@@ -37,16 +37,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int kSCodeStages = 8;     // gate/up: 8 KB per stage (gate 4 KB | up 4 KB); down: 4 KB codes + 4 KB h
-constexpr int kSXStages = 8;        // gate/up x stages: kSmallN rows x 128 B
+constexpr int kSCodeStages = 8;     // down: 4 KB h + 2 x 4 KB codes per stage (one K-step)
 constexpr int kSCompute = 16;       // compute warps of both kernels
-constexpr int kSWarpTma = 16, kSWarpAux = 17, kSLoaders = 2;
-constexpr int kSThreads1 = 32 * (kSWarpAux + kSLoaders);   // gate/up: + two loader warps (608)
+constexpr int kSWarpTma = 16, kSWarpAux = 17;
+constexpr int kSThreads1 = 32 * (kSCompute + 1);           // gate/up: + the producer warp (544)
 constexpr int kSThreads2 = 32 * (kSWarpAux + 1);           // down: + the column helper warp (576)
-constexpr int kSLoaderDepth = 2;    // steps in flight per loader warp
+// Gate/up stages cover four K-steps: the code boxes are then 128 bytes wide (whole lines of
+// each row, stored with the 128-byte swizzle), and each token row's 4 x 64 inputs one bulk copy.
+constexpr int kG1Steps = 4, kG1Stages = 2;
+constexpr int kG1XRow = 4 * 128 + 16;                       // x row stride: 8 rows on distinct banks
+constexpr int kG1Stage = (2 * 16384 + kSmallN * kG1XRow + 1023) / 1024 * 1024;   // gate | up codes | x rows
 constexpr long long kSDrainLimit = 1ll << 22;
 static_assert(kSmallN == 32, "one loader lane per token row, four n8 tiles");
-static_assert((kSLoaderDepth - 1) * kSLoaders < kSXStages, "a loader's lag must stay inside the x ring");
+static_assert(kG1Stage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled code boxes");
 
 // Named barrier over the compute warps that also ORs a predicate (a uniform stop decision).
 __device__ __forceinline__ bool compute_any(bool pred)
@@ -149,42 +152,45 @@ __device__ __forceinline__ STile stile(const SmallParams &P, int nbig, int tau, 
     return t;
 }
 
+// The producer's lanes wait together (one poll, the answer broadcast).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long limit, volatile int *abort)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, limit, abort);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // ------------------------------------------------------------------ gate/up
 __global__ void __launch_bounds__(kSThreads1, 1)
     small_gateup_kernel(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_u,
                         const __grid_constant__ CUtensorMap map_sg, const __grid_constant__ CUtensorMap map_su,
                         const SmallParams P)
 {
-    const int H = P.H, I = P.I, G = H / kGroup, nk = G, MB = (I + 127) / 128, Tk = P.T * P.k;
     pdl_trigger();   // the tensor-memory gate/up GEMM may take every SM this grid frees
+    const int H = P.H, I = P.I, G = H / kGroup, nk = G, MB = (I + 127) / 128, Tk = P.T * P.k;
+    const int nst = nk / kG1Steps;                  // stages per tile (H % 256 == 0)
     const int nbig = __ldg(P.nwork + 3);
     const int ntiles = (__ldg(P.nwork + 1) - nbig) * MB;
     if ((int)blockIdx.x >= ntiles) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sC = smem;                                        // kSCodeStages x 8 KB
-    uint8_t *sB = sC + kSCodeStages * 8192;                    // kSXStages x 4 KB (swizzled rows of 128 B)
-    float *sU = reinterpret_cast<float *>(sB + kSXStages * 4096);          // [2][8 warps][32 lanes][16]: up sums
+    uint8_t *sR = smem;                                                    // kG1Stages x kG1Stage
+    float *sU = reinterpret_cast<float *>(sR + kG1Stages * kG1Stage);      // [2][8 warps][32 lanes][16]: up sums
     uint16_t *sS = reinterpret_cast<uint16_t *>(sU + 2 * 8 * 32 * 16);     // [2][4][128][G]
     const int XS = G + 4;                  // group-sum row stride: distinct banks for the columns a warp reads
     float *sX = reinterpret_cast<float *>(sS + 2 * 4 * 128 * G);           // [2][kSmallN][XS]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sX + 2 * kSmallN * XS);
-    uint64_t *cfull = bars, *cempty = cfull + kSCodeStages, *bfull = cempty + kSCodeStages, *bempty = bfull + kSXStages;
-    uint64_t *tfull = bempty + kSXStages, *tempty = tfull + 2;
+    uint64_t *sfull = bars, *sempty = sfull + kG1Stages, *tfull = sempty + kG1Stages, *tempty = tfull + 2;
     volatile int *s_abort = reinterpret_cast<volatile int *>(tempty + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < kSCodeStages; ++s) {
-            mbar_init(smem_u32(cfull + s), 1);
-            mbar_init(smem_u32(cempty + s), kSCompute);
-        }
-        for (int s = 0; s < kSXStages; ++s) {
-            mbar_init(smem_u32(bfull + s), 32);               // the lanes of the step's loader warp
-            mbar_init(smem_u32(bempty + s), kSCompute);
+        for (int s = 0; s < kG1Stages; ++s) {
+            mbar_init(smem_u32(sfull + s), 1);
+            mbar_init(smem_u32(sempty + s), kSCompute);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(tfull + b), 2);     // TMA thread (scales) + loader lane 0 (group sums)
+            mbar_init(smem_u32(tfull + b), 1);
             mbar_init(smem_u32(tempty + b), kSCompute);
         }
         *s_abort = 0;
@@ -193,76 +199,19 @@ __global__ void __launch_bounds__(kSThreads1, 1)
     __syncthreads();
     const long long limit = P.wait_limit;
 
-    if (warp == kSWarpTma) {
-        // ------------------------------------------------ code boxes and scale rows (one thread)
-        if (lane != 0) return;
-        prefetch_map(&map_g);
-        prefetch_map(&map_u);
-        prefetch_map(&map_sg);
-        prefetch_map(&map_su);
+    if (warp == kSCompute) {
+        // ------------------------------------------------ producer: lane 0 the code boxes (TMA) and scale
+        // rows, lane n token row n (its group sums per tile, its 256 inputs per stage; bulk copies)
+        if (lane == 0) {
+            prefetch_map(&map_g);
+            prefetch_map(&map_u);
+            prefetch_map(&map_sg);
+            prefetch_map(&map_su);
+        }
+        // no L2 prefetch of the next tile: the code boxes are whole 128-byte lines, and lines
+        // requested a tile ahead were partly evicted before use (~40% more DRAM reads)
         auto rows_of = [&](const STile &t) { return min(128, I - t.mb * 128); };
-        auto prefetch_tile = [&](int tp) {
-            if (tp >= ntiles) return;
-            const STile t = stile(P, nbig, tp, MB, Tk);
-            const size_t wrow = (size_t)(t.shared_e ? 0 : t.expert * I) + t.mb * 128;
-            const uint32_t cb = (uint32_t)rows_of(t) * (H / 2);
-            prefetch_l2_bulk((t.shared_e ? P.sc0 : P.c0) + wrow * (H / 2), cb);
-            prefetch_l2_bulk((t.shared_e ? P.sc1 : P.c1) + wrow * (H / 2), cb);
-        };
-        prefetch_tile(blockIdx.x);
-        int q = 0, i = 0;
-        bool ok = true;
-        for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x, ++i) {
-            const STile t = stile(P, nbig, tau, MB, Tk);
-            prefetch_tile(tau + gridDim.x);
-            const int buf = i & 1;
-            if (i >= 2 && !mbar_wait(smem_u32(tempty + buf), ((i >> 1) - 1) & 1, limit, s_abort)) {
-                set_abort(s_abort, P.status);
-                break;
-            }
-            const size_t wrow = (size_t)(t.shared_e ? 0 : t.expert * I) + t.mb * 128;
-            const uint32_t sbytes = (uint32_t)rows_of(t) * G * 2;
-            const uint32_t tb = smem_u32(tfull + buf);
-            mbar_arrive_expect_tx(tb, 4 * sbytes);
-            const uint16_t *src[4] = {t.shared_e ? P.ss0 : P.s0, t.shared_e ? P.sb0 : P.b0,
-                                      t.shared_e ? P.ss1 : P.s1, t.shared_e ? P.sb1 : P.b1};
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-                bulk_load(smem_u32(sS + (buf * 4 + a) * 128 * G), src[a] + wrow * G, sbytes, tb);
-            const CUtensorMap *mg = t.shared_e ? &map_sg : &map_g;
-            const CUtensorMap *mu = t.shared_e ? &map_su : &map_u;
-#pragma unroll 1
-            for (int s = 0; s < nk; ++s, ++q) {
-                const int cs = q % kSCodeStages;
-                if (q >= kSCodeStages &&
-                    !mbar_wait(smem_u32(cempty + cs), (q / kSCodeStages - 1) & 1, limit, s_abort)) {
-                    set_abort(s_abort, P.status);
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = smem_u32(cfull + cs);
-                mbar_arrive_expect_tx(fb, 8192);
-                tma_load_2d(smem_u32(sC + cs * 8192), mg, s * 32, (int)wrow, fb);
-                tma_load_2d(smem_u32(sC + cs * 8192 + 4096), mu, s * 32, (int)wrow, fb);
-            }
-        }
-        // every issued copy lands before the CTA exits
-        for (int d = (q > kSCodeStages ? q - kSCodeStages : 0); d < q; ++d)
-            mbar_wait(smem_u32(cfull + d % kSCodeStages), (d / kSCodeStages) & 1, kSDrainLimit, nullptr);
-        for (int b = 0; b < 2 && b < i; ++b) {
-            const int last = i - 1 - ((i - 1 - b) & 1);   // the last tile that used buffer (i - 1 - b) & 1
-            mbar_wait(smem_u32(tfull + (last & 1)), (last >> 1) & 1, kSDrainLimit, nullptr);
-        }
-        return;
-    }
-
-    if (warp >= kSWarpAux) {
-        // ------------------------------------------------ token rows of x16 (and their group sums)
-        // Loader warp lw takes the K-steps q = lw mod kSLoaders, keeping kSLoaderDepth of its own
-        // steps in flight; lane l gathers token row l.  Warp kSWarpAux also brings the tile's
-        // group sums of x, into the tile buffer the scales go to.
-        const int lw = warp - kSWarpAux;
-        int q = 0, q_last = -1, pending = 0, i = 0;
+        int q = 0, i = 0;                           // q: stages issued
         bool ok = true;
         for (int tau = blockIdx.x; tau < ntiles && ok; tau += gridDim.x, ++i) {
             const STile t = stile(P, nbig, tau, MB, Tk);
@@ -277,55 +226,66 @@ __global__ void __launch_bounds__(kSThreads1, 1)
                     else row = f / P.k;
                 }
             }
-            if (lw == 0) {
-                // group sums of the tile's tokens into buffer buf, once the tile two back is done
-                const int buf = i & 1;
-                bool got = i < 2 || mbar_wait(smem_u32(tempty + buf), ((i >> 1) - 1) & 1, limit, s_abort);
-                got = __all_sync(0xffffffffu, got);
-                if (!got) {
-                    set_abort(s_abort, P.status);
-                    break;
-                }
-                const uint32_t tb = smem_u32(tfull + buf);
-                const int nrows = __popc(__ballot_sync(0xffffffffu, row >= 0));
-                if (lane == 0) mbar_arrive_expect_tx(tb, (uint32_t)nrows * G * 4);
-                __syncwarp();
-                if (row >= 0)
-                    bulk_load(smem_u32(sX + (buf * kSmallN + lane) * XS), P.xsum + (size_t)row * G, G * 4, tb);
+            const int nrows = __popc(__ballot_sync(0xffffffffu, row >= 0));
+            const int buf = i & 1;
+            if (i >= 2 && !warp_wait(smem_u32(tempty + buf), ((i >> 1) - 1) & 1, limit, s_abort)) {
+                set_abort(s_abort, P.status);
+                break;
             }
+            const size_t wrow = (size_t)(t.shared_e ? 0 : t.expert * I) + t.mb * 128;
+            const uint32_t sbytes = (uint32_t)rows_of(t) * G * 2;
+            const uint32_t tb = smem_u32(tfull + buf);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(tb, 4 * sbytes + (uint32_t)nrows * G * 4);
+                const uint16_t *src[4] = {t.shared_e ? P.ss0 : P.s0, t.shared_e ? P.sb0 : P.b0,
+                                          t.shared_e ? P.ss1 : P.s1, t.shared_e ? P.sb1 : P.b1};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+                    bulk_load(smem_u32(sS + (buf * 4 + a) * 128 * G), src[a] + wrow * G, sbytes, tb);
+            }
+            __syncwarp();
+            if (row >= 0) bulk_load(smem_u32(sX + (buf * kSmallN + lane) * XS), P.xsum + (size_t)row * G, G * 4, tb);
             const uint16_t *src = row >= 0 ? P.x16 + (size_t)row * H : nullptr;
+            const CUtensorMap *mg = t.shared_e ? &map_sg : &map_g;
+            const CUtensorMap *mu = t.shared_e ? &map_su : &map_u;
 #pragma unroll 1
-            for (int s = 0; s < nk; ++s, ++q) {
-                if (q % kSLoaders != lw) continue;
-                const int st = q % kSXStages;
-                if (q >= kSXStages &&
-                    !mbar_wait(smem_u32(bempty + st), (q / kSXStages - 1) & 1, limit, s_abort)) {
+            for (int k4 = 0; k4 < nst; ++k4, ++q) {
+                const int st = q % kG1Stages;
+                if (q >= kG1Stages &&
+                    !warp_wait(smem_u32(sempty + st), (q / kG1Stages - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
                     break;
                 }
-                if (src) {
-                    uint8_t *dst = sB + st * 4096;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) cp_async16(smem_u32(dst + swz128(lane, c)), src + s * 64 + c * 8);
+                uint8_t *stg = sR + st * kG1Stage;
+                const uint32_t fb = smem_u32(sfull + st);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, 2 * 16384 + (uint32_t)nrows * 512);
+                    tma_load_2d(smem_u32(stg), mg, k4 * 128, (int)wrow, fb);
+                    tma_load_2d(smem_u32(stg + 16384), mu, k4 * 128, (int)wrow, fb);
                 }
-                cp_async_commit();
-                q_last = q;
-                if (++pending == kSLoaderDepth) {          // the oldest of this warp's steps has landed
-                    cp_async_wait_group<kSLoaderDepth - 1>();
-                    mbar_arrive(smem_u32(bfull + (q - (kSLoaderDepth - 1) * kSLoaders) % kSXStages));
-                    --pending;
-                }
+                __syncwarp();
+                if (src) bulk_load(smem_u32(stg + 32768 + lane * kG1XRow), src + k4 * 256, 512, fb);
             }
         }
-        cp_async_wait_all();
-        for (int d = pending - 1; d >= 0; --d) mbar_arrive(smem_u32(bfull + (q_last - d * kSLoaders) % kSXStages));
+        // every issued copy lands before the CTA exits
+        if (lane == 0) {
+            for (int d = (q > kG1Stages ? q - kG1Stages : 0); d < q; ++d)
+                mbar_wait(smem_u32(sfull + d % kG1Stages), (d / kG1Stages) & 1, kSDrainLimit, nullptr);
+            for (int b = 0; b < 2 && b < i; ++b) {
+                const int last = i - 1 - ((i - 1 - b) & 1);   // the last tile that used buffer (i - 1 - b) & 1
+                mbar_wait(smem_u32(tfull + (last & 1)), (last >> 1) & 1, kSDrainLimit, nullptr);
+            }
+        }
         return;
     }
 
     // ---------------------------------------------------- compute warps: matrix w / 8, rows 16 (w % 8) ..
     const int g = lane >> 2, t4 = lane & 3, m = warp >> 3, rw = warp & 7;
     const int r0 = rw * 16 + g;                     // rows r0 and r0 + 8 of the tile
+    // byte offsets, inside a stage's 128-byte-swizzled box, of row r0 and row r0 + 8 (row r of a
+    // box sits at (r / 8) * 1024 + (r % 8) * 128 with its 16-byte chunk c at c ^ (r % 8); r0 % 8 = g)
+    const uint32_t crow0 = m * 16384 + (uint32_t)(2 * rw) * 1024 + g * 128, crow1 = crow0 + 1024;
     int q = 0, i = 0;
     for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
         const STile t = stile(P, nbig, tau, MB, Tk);
@@ -333,76 +293,59 @@ __global__ void __launch_bounds__(kSThreads1, 1)
         bool w_ok = mbar_wait(smem_u32(tfull + buf), (i >> 1) & 1, limit, s_abort);
         const uint16_t *ssc = sS + (buf * 4 + 2 * m) * 128 * G;   // this matrix's scales, then biases
         const float *sxs = sX + buf * kSmallN * XS;
-        uint2 ws0 = make_uint2(0, 0), ws1 = ws0, wb0 = ws0, wb1 = ws0;
         float acc[4][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-        // one K-step (tile step s, ring stage st, ring parity par, e = s % 8); with the step loop
-        // unrolled by 8 the stage, parity and scale slot are constants
-        auto step = [&](int s, int st, uint32_t par, int e) -> bool {
-            if (!mbar_wait(smem_u32(cfull + st), par, limit, s_abort) ||
-                !mbar_wait(smem_u32(bfull + st), par, limit, s_abort))
-                return false;
-            const uint8_t *cb = sC + st * 8192 + m * 4096 + r0 * 32 + t4 * 8;
-            const uint2 c0 = *reinterpret_cast<const uint2 *>(cb);
-            const uint2 c1 = *reinterpret_cast<const uint2 *>(cb + 256);
-            if ((e & 3) == 0) {
-                ws0 = scale_window(ssc, r0, G, s);
-                ws1 = scale_window(ssc, r0 + 8, G, s);
-                wb0 = scale_window(ssc + 128 * G, r0, G, s);
-                wb1 = scale_window(ssc + 128 * G, r0 + 8, G, s);
-            }
-            const float s0 = scale_pick(ws0, e & 3), s1 = scale_pick(ws1, e & 3);
-            const float k0 = fmaf(-1024.f, s0, scale_pick(wb0, e & 3));
-            const float k1 = fmaf(-1024.f, s1, scale_pick(wb1, e & 3));
-            uint32_t aa[2][8];
-            nib8(c0.x, aa[0]);
-            nib8(c0.y, aa[0] + 4);
-            nib8(c1.x, aa[1]);
-            nib8(c1.y, aa[1] + 4);
-            const uint8_t *bst = sB + st * 4096;
+#pragma unroll 1
+        for (int k4 = 0; k4 < nst && w_ok; ++k4, ++q) {
+            const int st = q % kG1Stages;
+            w_ok = mbar_wait(smem_u32(sfull + st), (q / kG1Stages) & 1, limit, s_abort);
+            if (!w_ok) break;
+            const uint8_t *stg = sR + st * kG1Stage;
+            const uint2 ws0 = scale_window(ssc, r0, G, k4 * 4), ws1 = scale_window(ssc, r0 + 8, G, k4 * 4);
+            const uint2 wb0 = scale_window(ssc + 128 * G, r0, G, k4 * 4);
+            const uint2 wb1 = scale_window(ssc + 128 * G, r0 + 8, G, k4 * 4);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (j * 8 >= ncol) break;
-                const int n = j * 8 + g;                // token column; rows past ncol hold stale data
-                const uint4 lo = *reinterpret_cast<const uint4 *>(bst + swz128(n, 2 * t4));
-                const uint4 hi = *reinterpret_cast<const uint4 *>(bst + swz128(n, 2 * t4 + 1));
-                const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int e = 0; e < kG1Steps; ++e) {
+                const int s = k4 * 4 + e;
+                // this lane's 8 code bytes of step e: 16-byte chunk 2 e + t4 / 2, half t4 % 2
+                const uint32_t co = (((2 * e + (t4 >> 1)) ^ g) << 4) | ((t4 & 1) << 3);
+                const uint2 c0 = *reinterpret_cast<const uint2 *>(stg + crow0 + co);
+                const uint2 c1 = *reinterpret_cast<const uint2 *>(stg + crow1 + co);
+                const float s0 = scale_pick(ws0, e), s1 = scale_pick(ws1, e);
+                const float k0 = fmaf(-1024.f, s0, scale_pick(wb0, e));
+                const float k1 = fmaf(-1024.f, s1, scale_pick(wb1, e));
+                uint32_t aa[2][8];
+                nib8(c0.x, aa[0]);
+                nib8(c0.y, aa[0] + 4);
+                nib8(c1.x, aa[1]);
+                nib8(c1.y, aa[1] + 4);
+                const uint8_t *xb = stg + 32768 + g * kG1XRow + e * 128 + t4 * 32;
 #pragma unroll
-                for (int mm = 0; mm < 4; ++mm)
-                    mma16816_f16(d, aa[0][2 * mm], aa[1][2 * mm], aa[0][2 * mm + 1], aa[1][2 * mm + 1], bp[2 * mm],
-                                 bp[2 * mm + 1]);
-                const int cA = j * 8 + 2 * t4;
-                const float sxA = sxs[cA * XS + s], sxB = sxs[(cA + 1) * XS + s];
-                acc[j][0] = fmaf(s0, d[0], fmaf(k0, sxA, acc[j][0]));
-                acc[j][1] = fmaf(s0, d[1], fmaf(k0, sxB, acc[j][1]));
-                acc[j][2] = fmaf(s1, d[2], fmaf(k1, sxA, acc[j][2]));
-                acc[j][3] = fmaf(s1, d[3], fmaf(k1, sxB, acc[j][3]));
+                for (int j = 0; j < 4; ++j) {
+                    if (j * 8 >= ncol) break;
+                    // token column j * 8 + g; rows past ncol hold stale data, only their own columns see it
+                    const uint4 lo = *reinterpret_cast<const uint4 *>(xb + j * 8 * kG1XRow);
+                    const uint4 hi = *reinterpret_cast<const uint4 *>(xb + j * 8 * kG1XRow + 16);
+                    const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int mm = 0; mm < 4; ++mm)
+                        mma16816_f16(d, aa[0][2 * mm], aa[1][2 * mm], aa[0][2 * mm + 1], aa[1][2 * mm + 1], bp[2 * mm],
+                                     bp[2 * mm + 1]);
+                    const int cA = j * 8 + 2 * t4;
+                    const float sxA = sxs[cA * XS + s], sxB = sxs[(cA + 1) * XS + s];
+                    acc[j][0] = fmaf(s0, d[0], fmaf(k0, sxA, acc[j][0]));
+                    acc[j][1] = fmaf(s0, d[1], fmaf(k0, sxB, acc[j][1]));
+                    acc[j][2] = fmaf(s1, d[2], fmaf(k1, sxA, acc[j][2]));
+                    acc[j][3] = fmaf(s1, d[3], fmaf(k1, sxB, acc[j][3]));
+                }
             }
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(cempty + st));
-                mbar_arrive(smem_u32(bempty + st));
-            }
-            return true;
-        };
-        static_assert(kSCodeStages == 8 && kSXStages == 8, "one ring index for codes and x, 8 steps per scale window");
-        if ((nk & 7) == 0) {                        // every tile starts at a multiple of 8 steps
-#pragma unroll 1
-            for (int s8 = 0; s8 < nk && w_ok; s8 += 8) {
-                const uint32_t par = ((q + s8) >> 3) & 1;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (w_ok) w_ok = step(s8 + e, e, par, e);
-            }
-        } else {
-#pragma unroll 1
-            for (int s = 0; s < nk && w_ok; ++s) w_ok = step(s, (q + s) & 7, ((q + s) >> 3) & 1, s & 7);
+            if (lane == 0) mbar_arrive(smem_u32(sempty + st));
         }
-        q += nk;
         if (!w_ok) set_abort(s_abort, P.status);
         __syncwarp();
         if (lane == 0 && w_ok) mbar_arrive(smem_u32(tempty + buf));   // scales and group sums no longer read
@@ -673,8 +616,8 @@ int sm_count_small()
 size_t small_g1_smem(int H)
 {
     const int G = H / kGroup;
-    return 1024 + kSCodeStages * 8192 + kSXStages * 4096 + 2 * 8 * 32 * 16 * 4 + 2 * 4 * 128 * G * 2 +
-           2 * kSmallN * (G + 4) * 4 + 8 * (2 * kSCodeStages + 2 * kSXStages + 4) + 16;
+    return 1024 + kG1Stages * kG1Stage + 2 * 8 * 32 * 16 * 4 + 2 * 4 * 128 * G * 2 + 2 * kSmallN * (G + 4) * 4 +
+           8 * (2 * kG1Stages + 4) + 16;
 }
 size_t small_g2_smem(int I)
 {
@@ -737,12 +680,12 @@ cudaError_t launch_small_gateup(const PrefillArgs &a, cudaStream_t st)
     const int H = a.H, I = a.I, E = a.E;
     CUtensorMap mg, mu, msg, msu;
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
-    bool ok = make_map_2d(&mg, a.gate.codes, u8, 1, H / 2, (uint64_t)E * I, 32, 128, none) &&
-              make_map_2d(&mu, a.up.codes, u8, 1, H / 2, (uint64_t)E * I, 32, 128, none);
+    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    bool ok = make_map_2d(&mg, a.gate.codes, u8, 1, H / 2, (uint64_t)E * I, 128, 128, sw128) &&
+              make_map_2d(&mu, a.up.codes, u8, 1, H / 2, (uint64_t)E * I, 128, 128, sw128);
     if (a.has_shared)
-        ok = ok && make_map_2d(&msg, a.s_gate.codes, u8, 1, H / 2, I, 32, 128, none) &&
-             make_map_2d(&msu, a.s_up.codes, u8, 1, H / 2, I, 32, 128, none);
+        ok = ok && make_map_2d(&msg, a.s_gate.codes, u8, 1, H / 2, I, 128, 128, sw128) &&
+             make_map_2d(&msu, a.s_up.codes, u8, 1, H / 2, I, 128, 128, sw128);
     else {
         msg = mg;
         msu = mu;
