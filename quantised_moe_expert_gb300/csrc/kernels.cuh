@@ -113,6 +113,7 @@ struct PrefillArgs {
     const uint16_t *x;            // bf16 [T, H]
     uint16_t *x16;                // fp16 [T, H] scratch (K-permuted)
     float *xsum;                  // f32 [T, H / 64] scratch: group sums of x16
+    float *hsum;                  // f32 [T*k + T, I / 64] scratch: group sums of h (small-tile items)
     uint16_t *hs;                 // fp16 [T*k + T, I] scratch, expert-sorted rows
     QMatDev gate, up, down, s_gate, s_up, s_down;
     const int32_t *nwork, *offsets, *perm;

@@ -204,6 +204,7 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     a.x = ea.x;
     a.x16 = ws_at<uint16_t>(ws, L.x16);
     a.xsum = ws_at<float>(ws, L.xsum);
+    a.hsum = ws_at<float>(ws, L.hsum);
     a.hs = ws_at<uint16_t>(ws, L.h);
     a.gate = ea.gate;
     a.up = ea.up;

@@ -54,6 +54,7 @@ struct WsLayout {
     size_t work_g2;    // WorkItem [max tiles gemm2]
     size_t x16;        // fp16 [T, H] (prefill B operand)
     size_t xsum;       // f32 [T, H / 64] group sums of x16 (small-tile gate/up GEMM)
+    size_t hsum;       // f32 [T*k + T, I / 64] group sums of h (small-tile GEMMs)
     size_t h;          // fp16 [T*k + T, I] (decode: slot order; prefill: expert-sorted, K-permuted)
     size_t yslot;      // f32 [T*k + T, H] (decode)
     size_t acc;        // f32 [T, H] (prefill accumulation)
@@ -104,6 +105,7 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.work_g2 = take(sizeof(WorkItem) * (size_t)L.max_w2);
     L.x16 = take(2 * Tz * H);
     L.xsum = take(4 * Tz * (H / 64));
+    L.hsum = take(4 * Tz * (k + 1) * (I / 64));
     L.h = take(2 * Tz * (k + 1) * I);
     L.yslot = take(4 * Tz * (k + 1) * H);
     L.acc = take(4 * Tz * H);

@@ -23,9 +23,9 @@
 //   hand their sums to the gate warps through shared memory, which store h = silu(g) * u
 //   as fp16 in the codes' k order.
 // Down kernel (tiles of 256 rows of H): the same with the down codes, the item's h rows
-//   (TMA, the same swizzle) and, instead of precomputed sums, an all-ones MMA for sum_j
-//   h_j; warp w < 16 owns rows 16 w .. + 15; the epilogue adds p * y into the fp32 layer
-//   accumulator.
+//   (TMA, the same swizzle) and the group sums of h that the gate/up kernel's epilogue
+//   stored; warp w < 16 owns rows 16 w .. + 15; the epilogue adds p * y into the fp32
+//   layer accumulator.
 #include <algorithm>
 
 #include "kernels.cuh"
@@ -71,6 +71,7 @@ struct SmallParams {
     uint16_t *hs;                      // fp16 [T*k + T, I] (k order), expert-sorted rows
     const uint16_t *x16;               // fp16 [T, H] (k order)
     const float *xsum;                 // f32 [T, H / 64]
+    float *hsum;                       // f32 [T*k + T, I / 64]: group sums of the stored (fp16) h
     const uint16_t *p, *w_s;           // bf16 pick weights [T, k], shared weights [T]
     float *acc;                        // f32 [T, H]
     const uint8_t *c0, *c1, *sc0, *sc1;            // codes (routed, shared) for L2 prefetch: gate, up / down
@@ -179,7 +180,8 @@ __global__ void __launch_bounds__(kSThreads1, 1)
     uint16_t *sS = reinterpret_cast<uint16_t *>(sU + 2 * 8 * 32 * 16);     // [2][4][128][G]
     const int XS = G + 4;                  // group-sum row stride: distinct banks for the columns a warp reads
     float *sX = reinterpret_cast<float *>(sS + 2 * 4 * 128 * G);           // [2][kSmallN][XS]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sX + 2 * kSmallN * XS);
+    float *sH = sX + 2 * kSmallN * XS;                                     // [2][8 gate warps][32]: h sums
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sH + 2 * 8 * 32);
     uint64_t *sfull = bars, *sempty = sfull + kG1Stages, *tfull = sempty + kG1Stages, *tempty = tfull + 2;
     volatile int *s_abort = reinterpret_cast<volatile int *>(tempty + 2);
 
@@ -361,19 +363,39 @@ __global__ void __launch_bounds__(kSThreads1, 1)
             break;
         }
         if (m == 0) {
-            // h = silu(g) * u for the tile's rows and tokens, fp16, at the row's k-order column
+            // h = silu(g) * u for the tile's rows and tokens, fp16, at the row's k-order column; and
+            // per token the sum of the stored h over each group of 64 rows (the down GEMM's bias term):
+            // this warp's 16 rows by shuffles, the group's four warps through shared memory in order
+            float *hp = sH + (buf * 8 + rw) * 32;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                float part[2] = {0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int col = j * 8 + 2 * t4 + (e & 1);
                     const int erow = t.mb * 128 + r0 + 8 * (e >> 1);
                     if (col < ncol && erow < I) {
                         const float gv = acc[j][e], uv = xu[j * 4 + e];
-                        const float hv = __fdividef(gv * uv, 1.f + __expf(-gv));
-                        P.hs[(size_t)(t.pbase + col) * I + kperm_pos(erow)] = __half_as_ushort(__float2half_rn(hv));
+                        const __half hq = __float2half_rn(__fdividef(gv * uv, 1.f + __expf(-gv)));
+                        P.hs[(size_t)(t.pbase + col) * I + kperm_pos(erow)] = __half_as_ushort(hq);
+                        part[e & 1] += __half2float(hq);
                     }
                 }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) part[c] += __shfl_xor_sync(0xffffffffu, part[c], o);
+                }
+                if (g == 0) {
+                    hp[j * 8 + 2 * t4] = part[0];
+                    hp[j * 8 + 2 * t4 + 1] = part[1];
+                }
+            }
+            asm volatile("bar.sync 2, %0;" ::"n"(8 * 32) : "memory");   // the eight gate warps
+            const int grp = 2 * t.mb + (rw >> 2), GI = I / kGroup;
+            if ((rw & 3) == 0 && lane < ncol && grp < GI) {
+                const float *q4 = sH + (buf * 8 + rw) * 32 + lane;
+                P.hsum[(size_t)(t.pbase + lane) * GI + grp] = ((q4[0] + q4[32]) + q4[64]) + q4[96];
             }
         }
     }
@@ -395,7 +417,9 @@ __global__ void __launch_bounds__(kSThreads2, 1)
     uint16_t *sS = reinterpret_cast<uint16_t *>(sC + kSCodeStages * 12288);  // [2][2][256][GI]
     int *s_tok = reinterpret_cast<int *>(sS + 2 * 2 * 256 * GI);             // [2][kSmallN]
     float *s_w = reinterpret_cast<float *>(s_tok + 2 * kSmallN);             // [2][kSmallN]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(s_w + 2 * kSmallN);
+    const int XH = GI + 4;                 // h-sum row stride: distinct banks for the columns a warp reads
+    float *s_hs = s_w + 2 * kSmallN;                                         // [2][kSmallN][XH]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_hs + 2 * kSmallN * XH);
     uint64_t *cfull = bars, *cempty = cfull + kSCodeStages, *tfull = cempty + kSCodeStages, *tempty = tfull + 2;
     volatile int *s_abort = reinterpret_cast<volatile int *>(tempty + 2);
 
@@ -502,6 +526,10 @@ __global__ void __launch_bounds__(kSThreads2, 1)
             }
             s_tok[buf * kSmallN + lane] = tok;
             s_w[buf * kSmallN + lane] = wgt;
+            float *hsr = s_hs + (buf * kSmallN + lane) * XH;
+            const float *hsg = P.hsum + (size_t)(t.pbase + lane) * GI;
+#pragma unroll 1
+            for (int gi = 0; gi < GI; ++gi) hsr[gi] = lane < t.ntok ? __ldg(hsg + gi) : 0.f;
             mbar_arrive(smem_u32(tfull + buf));
         }
         return;
@@ -510,13 +538,13 @@ __global__ void __launch_bounds__(kSThreads2, 1)
     // ---------------------------------------------------- compute warps: rows 16 w .. 16 w + 15 of 256
     const int g = lane >> 2, t4 = lane & 3;
     const int r0 = warp * 16 + g;
-    constexpr uint32_t ones = 0x3C003C00u;
     int q = 0, i = 0;
     for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
         const STile t = stile(P, nbig, tau, MB, Tk);
         const int buf = i & 1, ncol = t.ntok;
         bool w_ok = mbar_wait(smem_u32(tfull + buf), (i >> 1) & 1, limit, s_abort);
         const uint16_t *ssc = sS + buf * 2 * 256 * GI;
+        const float *shs = s_hs + buf * kSmallN * XH;
         uint2 ws0 = make_uint2(0, 0), ws1 = ws0, wb0 = ws0, wb1 = ws0;
         float acc[4][4];
 #pragma unroll
@@ -550,17 +578,17 @@ __global__ void __launch_bounds__(kSThreads2, 1)
                 const uint4 lo = *reinterpret_cast<const uint4 *>(stg + swz128(n, 2 * t4));
                 const uint4 hi = *reinterpret_cast<const uint4 *>(stg + swz128(n, 2 * t4 + 1));
                 const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                float dd[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
+                float dd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int mm = 0; mm < 4; ++mm) {
+                for (int mm = 0; mm < 4; ++mm)
                     mma16816_f16(dd, ad[0][2 * mm], ad[1][2 * mm], ad[0][2 * mm + 1], ad[1][2 * mm + 1], bp[2 * mm],
                                  bp[2 * mm + 1]);
-                    mma16816_f16(dx, ones, ones, ones, ones, bp[2 * mm], bp[2 * mm + 1]);
-                }
-                acc[j][0] = fmaf(s0, dd[0], fmaf(k0, dx[0], acc[j][0]));
-                acc[j][1] = fmaf(s0, dd[1], fmaf(k0, dx[1], acc[j][1]));
-                acc[j][2] = fmaf(s1, dd[2], fmaf(k1, dx[2], acc[j][2]));
-                acc[j][3] = fmaf(s1, dd[3], fmaf(k1, dx[3], acc[j][3]));
+                const int cA = j * 8 + 2 * t4;           // h sums of the two columns over this group
+                const float hA = shs[cA * XH + s], hB = shs[(cA + 1) * XH + s];
+                acc[j][0] = fmaf(s0, dd[0], fmaf(k0, hA, acc[j][0]));
+                acc[j][1] = fmaf(s0, dd[1], fmaf(k0, hB, acc[j][1]));
+                acc[j][2] = fmaf(s1, dd[2], fmaf(k1, hA, acc[j][2]));
+                acc[j][3] = fmaf(s1, dd[3], fmaf(k1, hB, acc[j][3]));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(cempty + st));
@@ -617,12 +645,13 @@ size_t small_g1_smem(int H)
 {
     const int G = H / kGroup;
     return 1024 + kG1Stages * kG1Stage + 2 * 8 * 32 * 16 * 4 + 2 * 4 * 128 * G * 2 + 2 * kSmallN * (G + 4) * 4 +
-           8 * (2 * kG1Stages + 4) + 16;
+           2 * 8 * 32 * 4 + 8 * (2 * kG1Stages + 4) + 16;
 }
 size_t small_g2_smem(int I)
 {
     const int GI = I / kGroup;
-    return 1024 + kSCodeStages * 12288 + 2 * 2 * 256 * GI * 2 + 2 * kSmallN * 8 + 8 * (2 * kSCodeStages + 4) + 16;
+    return 1024 + kSCodeStages * 12288 + 2 * 2 * 256 * GI * 2 + 2 * kSmallN * 8 + 2 * kSmallN * (GI + 4) * 4 +
+           8 * (2 * kSCodeStages + 4) + 16;
 }
 
 SmallParams small_params(const PrefillArgs &a, bool down)
@@ -635,6 +664,7 @@ SmallParams small_params(const PrefillArgs &a, bool down)
     p.hs = a.hs;
     p.x16 = a.x16;
     p.xsum = a.xsum;
+    p.hsum = a.hsum;
     p.p = a.p;
     p.w_s = a.w_s;
     p.acc = a.acc;

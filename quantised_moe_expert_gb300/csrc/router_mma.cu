@@ -21,7 +21,6 @@
 namespace qmoe {
 namespace {
 
-constexpr int kRWarps = 8;                 // 2 expert tiles (16 experts each) x 4 quarters of the input dimension
 constexpr int kRExp = 32;                  // experts per block
 constexpr int kRTok = 32;                  // tokens per block (4 n8 tiles)
 
