@@ -66,7 +66,6 @@ constexpr int kWarpTma1 = 16, kWarpMma1 = 17, kWarpEpi1 = 18, kEpiWarps1 = 4;
 constexpr int kWarpLoader1 = kWarpEpi1 + kEpiWarps1, kLoaderWarps1 = 2, kLoaderDepth = 2;
 constexpr int kThreads1 = 32 * (kWarpLoader1 + kLoaderWarps1);  // 768
 constexpr int kScaleChunk1 = 8;                                 // gate/up: groups per scale chunk
-constexpr int kScaleChunk = 16;     // groups of scales staged in shared memory at a time
 constexpr long long kDrainLimit = 1ll << 22;
 constexpr uint32_t kTmemA1 = 256;   // gate/up GEMM: accumulators in TMEM columns [0, 256), A stages from 256
 
@@ -99,6 +98,7 @@ struct G2Params {
     const uint16_t *sds, *sdb;         // shared [H, I/64]
     int *status;
     int T, H, I, E, k;
+    int async_scales;                  // 1: scale rows are 16-byte aligned (I % 512 == 0), fetched with cp.async
     long long wait_limit;
 };
 
@@ -143,25 +143,6 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *status)
 {
     *abort = 1;
     record_status(status, MOE_ERR_TIMEOUT);
-}
-
-// Stage one chunk of a row's scales and biases (groups [g0, g0 + kScaleChunk)) into the
-// thread-private columns of the shared staging arrays.  Every load is issued
-// before the first store, so the chunk costs one memory round trip.
-template <int NSRC>
-__device__ __forceinline__ void stage_scales(uint16_t *dst, const uint16_t *const *src, int row_ok, size_t row_off,
-                                             int G, int g0, int r)
-{
-    uint16_t v[NSRC][kScaleChunk];
-#pragma unroll
-    for (int a = 0; a < NSRC; ++a)
-#pragma unroll
-        for (int g = 0; g < kScaleChunk; ++g)
-            v[a][g] = (row_ok && g0 + g < G) ? src[a][row_off + g0 + g] : (uint16_t)0;
-#pragma unroll
-    for (int a = 0; a < NSRC; ++a)
-#pragma unroll
-        for (int g = 0; g < kScaleChunk; ++g) dst[(a * kScaleChunk + g) * 128 + r] = v[a][g];
 }
 
 // Named barrier `id` over `count` threads that also ORs a predicate: every
@@ -625,8 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sA = smem;                           // S x 16 KB
     uint8_t *sB = sA + S * 16384;                 // SB x 32 KB (256 rows x 128 B)
     uint8_t *sC = sB + SB * 32768;                // CS x 4 KB
-    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 4096);   // [2 halves][2][kScaleChunk][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + 4 * kScaleChunk * 128);
+    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 4096);   // [dequant thread][2][2][kScaleChunk1]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kDequantThreads * 4 * kScaleChunk1);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
@@ -769,20 +750,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 8) {
         // ------------------------------------------------ dequant: thread = half a row (4 chunks)
+        // The row's scales and biases pass through a private double buffer of kScaleChunk1
+        // groups, the next chunk (of this tile or of the next) requested with cp.async when
+        // the current one starts: a tile has only I / 64 K-steps, so a synchronous load at
+        // every tile start would stall the ring for a memory round trip each time.
         const int r = tid & 127, half = tid >> 7;
-        int q = 0;
+        uint16_t *mysc = sScale + (size_t)tid * (4 * kScaleChunk1);   // [buffer][scale | bias][kScaleChunk1]
+        const int nchunk = (GI + kScaleChunk1 - 1) / kScaleChunk1;
+        auto src_of = [&](const TileInfo &t, const uint16_t *&ps, const uint16_t *&pb) -> size_t {
+            ps = t.shared_e ? P.sds : P.ds;
+            pb = t.shared_e ? P.sdb : P.db;
+            return ((size_t)(t.shared_e ? 0 : t.expert) * H + (size_t)(t.mb * 128 + r)) * GI;
+        };
+        auto fetch_chunk = [&](const TileInfo &t, int c, int buf) {     // one commit group per call
+            if (t.mb * 128 + r < H) {
+                const uint16_t *ps, *pb;
+                const size_t off = src_of(t, ps, pb) + (size_t)c * kScaleChunk1;
+                uint16_t *d = mysc + buf * 2 * kScaleChunk1;
+                cp_async16(smem_u32(d), ps + off);
+                cp_async16(smem_u32(d + kScaleChunk1), pb + off);
+            }
+            cp_async_commit();
+        };
+        auto load_chunk = [&](const TileInfo &t, int c, int buf) {      // the same with plain loads
+            const bool row_ok = t.mb * 128 + r < H;
+            const uint16_t *ps, *pb;
+            const size_t off = src_of(t, ps, pb) + (size_t)c * kScaleChunk1;
+            uint16_t *d = mysc + buf * 2 * kScaleChunk1;
+#pragma unroll
+            for (int g = 0; g < kScaleChunk1; ++g) {
+                const bool in = row_ok && c * kScaleChunk1 + g < GI;
+                d[g] = in ? ps[off + g] : (uint16_t)0;
+                d[kScaleChunk1 + g] = in ? pb[off + g] : (uint16_t)0;
+            }
+        };
+        int q = 0, j = 0;                                  // j: scale chunks started by this thread
         bool ok = true;
+        if (P.async_scales) fetch_chunk(tile_info(P.work, P.offsets, blockIdx.x, MB, P.E, Tk), 0, 0);
+        uint4 sreg = make_uint4(0, 0, 0, 0), breg = sreg;  // 8 groups' scales and biases (bf16 pairs)
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
-            const int row = ti.mb * 128 + r;
-            const bool row_ok = row < H;
-            const int ee = ti.shared_e ? 0 : ti.expert;
-            const size_t soff = (size_t)ee * H * GI + (size_t)row * GI;
-            const uint16_t *srcs[2] = {ti.shared_e ? P.sds : P.ds, ti.shared_e ? P.sdb : P.db};
-            uint16_t *myscale = sScale + half * 2 * kScaleChunk * 128;   // each half keeps its own copy
             for (int s = 0; s < nk && ok; ++s, ++q) {
                 const int st = q % S;
-                if (s % kScaleChunk == 0) stage_scales<2>(myscale, srcs, row_ok, soff, GI, s, r);
+                if (s % kScaleChunk1 == 0) {
+                    const int c = s / kScaleChunk1;
+                    if (P.async_scales) {
+                        if (c + 1 < nchunk) fetch_chunk(ti, c + 1, (j + 1) & 1);
+                        else if (tau + (int)gridDim.x < ntiles)
+                            fetch_chunk(tile_info(P.work, P.offsets, tau + gridDim.x, MB, P.E, Tk), 0, (j + 1) & 1);
+                        else cp_async_commit();
+                        cp_async_wait_group<1>();                 // chunk j has landed
+                    } else {
+                        load_chunk(ti, c, j & 1);
+                    }
+                    const uint16_t *cur = mysc + (j & 1) * 2 * kScaleChunk1;
+                    ++j;
+                    sreg = *reinterpret_cast<const uint4 *>(cur);
+                    breg = *reinterpret_cast<const uint4 *>(cur + kScaleChunk1);
+                }
                 if (q >= S && !mbar_wait(smem_u32(aempty + st), (q / S - 1) & 1, limit, s_abort)) {
                     set_abort(s_abort, P.status);
                     ok = false;
@@ -794,10 +819,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int gi = s % kScaleChunk;
-                const __half2 sd = bf16_to_h2(myscale[(0 * kScaleChunk + gi) * 128 + r]);
+                const int gi = s & 7;
+                const uint32_t sw = gi < 4 ? (gi < 2 ? sreg.x : sreg.y) : (gi < 6 ? sreg.z : sreg.w);
+                const uint32_t bw = gi < 4 ? (gi < 2 ? breg.x : breg.y) : (gi < 6 ? breg.z : breg.w);
+                const __half2 sd = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
                 const __half2 sd16 = __hmul2(sd, __float2half2_rn(0.0625f));
-                const __half2 bd = bf16_to_h2(myscale[(1 * kScaleChunk + gi) * 128 + r]);
+                const __half2 bd = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
                 const uint4 w = *reinterpret_cast<const uint4 *>(sC + cs * 4096 + r * 32 + half * 16);
                 const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
                 uint8_t *aa = sA + st * 16384;
@@ -810,6 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (bar_any(1, kDequantThreads, !ok || *s_abort)) break;   // the eight warps stop together
         }
+        cp_async_wait_all();                               // no copy into shared memory outlives the CTA
     } else {
         // ------------------------------------------------ epilogue: acc[t, row] += w * y
         const int quad = warp & 3;
@@ -924,7 +952,7 @@ size_t g1_smem()
 }
 size_t g2_smem()
 {
-    return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + kCodeStages2 * 4096 + 4 * kScaleChunk * 128 * 2 +
+    return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + kCodeStages2 * 4096 + kDequantThreads * 4 * kScaleChunk1 * 2 +
            8 * (2 * kCodeStages2 + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 1024 * 4 + 16;
 }
 
@@ -1054,6 +1082,12 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p2.I = I;
     p2.E = E;
     p2.k = k;
+    {
+        const uint16_t *sc[4] = {p2.ds, p2.db, p2.sds, p2.sdb};
+        bool al = (I / kGroup) % 8 == 0;
+        for (const uint16_t *ptr : sc) al = al && (ptr == nullptr || reinterpret_cast<uintptr_t>(ptr) % 16 == 0);
+        p2.async_scales = al ? 1 : 0;
+    }
     p2.wait_limit = a.wait_limit;
     const size_t s2 = g2_smem();
     auto k2 = gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2>;
