@@ -52,7 +52,8 @@ using namespace tc;
 // operand (B) and int4 code tiles.  B runs deepest: its loads come from L2 /
 // HBM with a latency of several K-steps of MMA.
 constexpr int kStagesA1 = 4, kStagesB1 = 8, kCodeStages1 = 6;   // gate/up: A in TMEM (64 columns), 16 KB, 8 KB per stage
-constexpr int kStagesA2 = 3, kStagesB2 = 4, kCodeStages2 = 6;   // down:    16 KB, 32 KB, 4 KB per stage
+constexpr int kStagesA2 = 3, kStagesB2 = 3, kCodeStages2 = 6;   // down:    16 KB, 32 KB, 4 KB per stage
+constexpr int kRedCols = 16;        // down epilogue: columns per bulk-reduce chunk (two chunk buffers)
 // Warp roles of the down GEMM: 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue.
 constexpr int kDequantThreads = 256;
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10;
@@ -143,6 +144,12 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *status)
 {
     *abort = 1;
     record_status(status, MOE_ERR_TIMEOUT);
+}
+
+// Named barrier `id` over `count` threads.
+__device__ __forceinline__ void named_bar(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Named barrier `id` over `count` threads that also ORs a predicate: every
@@ -607,7 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sB = sA + S * 16384;                 // SB x 32 KB (256 rows x 128 B)
     uint8_t *sC = sB + SB * 32768;                // CS x 4 KB
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 4096);   // [dequant thread][2][2][kScaleChunk1]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kDequantThreads * 4 * kScaleChunk1);
+    float *sRed = reinterpret_cast<float *>(sScale + kDequantThreads * 4 * kScaleChunk1);   // [2][kRedCols][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sRed + 2 * kRedCols * 128);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
@@ -842,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue: acc[t, row] += w * y
         const int quad = warp & 3;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        int i = 0;
+        int i = 0, redc = 0;
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
             const int N = (ti.ntok + 15) & ~15;
@@ -877,25 +885,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!got) set_abort(s_abort, P.status);
             if (bar_any(2, 128, !got)) break;                // the four warps stop together
             tc_fence_after();
-            const int erow = ti.mb * 128 + quad * 32 + lane;
+            // w * y of 16 columns at a time into a shared-memory chunk [column][row], then one bulk
+            // reduce-add per column into the token's row of acc (the tile's rows are contiguous
+            // there): the bulk copy engine does the adds, not one atomic per element
+            const int rloc = quad * 32 + lane, nrow = min(128, H - ti.mb * 128), e = tid - kWarpEpi * 32;
             const uint32_t d0 = tmem + lane_base + (uint32_t)buf * 256;
-            for (int n0 = 0; n0 < N; n0 += 16) {
+            for (int n0 = 0; n0 < N; n0 += kRedCols, ++redc) {
                 uint32_t v[16];
                 tmem_ld16(d0 + n0, v);
                 tmem_ld_wait();
-                if (erow < H) {
+                if (n0 + kRedCols >= N) {                 // every column read: the MMAs may overwrite them
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(tempty + buf));
+                }
+                float *red = sRed + (redc & 1) * kRedCols * 128;
+                if (e < kRedCols) bulk_wait_read<1>();    // this buffer's reduces (two chunks ago) have read it
+                named_bar(2, 128);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = n0 + j;
-                        const int t = n < ti.ntok ? tok[n] : -1;
-                        if (t >= 0) atomicAdd(P.acc + (size_t)t * H + erow, wv[n] * __uint_as_float(v[j]));
-                    }
+                for (int j = 0; j < 16; ++j) red[j * 128 + rloc] = wv[n0 + j] * __uint_as_float(v[j]);
+                fence_proxy_async_smem();
+                named_bar(2, 128);
+                if (e < kRedCols) {
+                    const int n = n0 + e;
+                    const int t = n < ti.ntok ? tok[n] : -1;
+                    if (t >= 0) bulk_reduce_add_f32(P.acc + (size_t)t * H + ti.mb * 128, smem_u32(red + e * 128),
+                                                    (uint32_t)nrow * 4);
+                    bulk_commit();
                 }
             }
-            tc_fence_before();
-            mbar_arrive(smem_u32(tempty + buf));
             if (bar_any(2, 128, *s_abort)) break;           // tok/wv of this buffer are reused two tiles later
         }
+        bulk_wait<0>();                                   // every reduce-add has completed
     }
     tc_fence_before();
     __syncthreads();
@@ -953,6 +973,7 @@ size_t g1_smem()
 size_t g2_smem()
 {
     return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + kCodeStages2 * 4096 + kDequantThreads * 4 * kScaleChunk1 * 2 +
+           2 * kRedCols * 128 * 4 +
            8 * (2 * kCodeStages2 + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 1024 * 4 + 16;
 }
 
