@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(kSThreads, MINB)
 {
     __shared__ SSmem S;
     extern __shared__ uint8_t dyn_raw[];
-    uint8_t *dyn = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *dyn = align_smem_1024(dyn_raw);
     uint8_t *ring = dyn;
     uint4 *s_x = reinterpret_cast<uint4 *>(dyn + geo.x_off);          // [T][x_stride] bf16 rows, k order
     float *s_sumx = reinterpret_cast<float *>(dyn + geo.sumx_off);    // [T][G]

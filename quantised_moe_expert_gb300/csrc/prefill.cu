@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
         return;
     }
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *sB = smem;                           // SB x 16 KB (128 token rows x 128 B)
     uint8_t *sC = sB + SB * 16384;                // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [dequant thread][2][2][kScaleChunk1]
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *sA = smem;                           // S x 16 KB
     uint8_t *sB = sA + S * 16384;                 // SB x 32 KB (256 rows x 128 B)
     uint8_t *sC = sB + SB * 32768;                // CS x 4 KB

@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kSThreads1, 1)
     const int ntiles = (__ldg(P.nwork + 1) - nbig) * MB;
     if ((int)blockIdx.x >= ntiles) return;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *sR = smem;                                                    // kG1Stages x kG1Stage
     float *sU = reinterpret_cast<float *>(sR + kG1Stages * kG1Stage);      // [2][8 warps][32 lanes][16]: up sums
     uint16_t *sS = reinterpret_cast<uint16_t *>(sU + 2 * 8 * 32 * 16);     // [2][4][128][G]
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kSThreads2, 1)
     const int ntiles = (__ldg(P.nwork + 2) - nbig) * MB;
     if ((int)blockIdx.x >= ntiles) return;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *sC = smem;                                        // kSCodeStages x (h 4 KB | codes 2 x 4 KB)
     uint16_t *sS = reinterpret_cast<uint16_t *>(sC + kSCodeStages * 12288);  // [2][2][256][GI]
     int *s_tok = reinterpret_cast<int *>(sS + 2 * 2 * 256 * GI);             // [2][kSmallN]

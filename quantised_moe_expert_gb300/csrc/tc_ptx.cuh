@@ -14,6 +14,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory array advanced to the next 1024-byte boundary by pointer
+// arithmetic on the array itself (no round trip through an integer), so the compiler
+// still knows that every pointer derived from it addresses shared memory and emits
+// shared-memory loads and stores for them instead of generic ones.
+__device__ __forceinline__ uint8_t *align_smem_1024(uint8_t *raw)
+{
+    return raw + ((0u - smem_u32(raw)) & 1023u);
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
@@ -108,7 +117,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  : "memory");
 }
 
-// Asks L2 to fetch a contiguous range (16-byte aligned address and size); no completion signal.
 // dst[i] += src[i] in global memory for `bytes` / 4 fp32 values, performed by the bulk copy
 // engine from shared memory (both addresses 16-byte aligned, size a multiple of 16); tracked
 // by the issuing thread's bulk groups.
@@ -126,6 +134,7 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 template <int N>
 __device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
 
+// Asks L2 to fetch a contiguous range (16-byte aligned address and size); no completion signal.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
