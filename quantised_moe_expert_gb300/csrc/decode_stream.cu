@@ -11,8 +11,8 @@
 //   - a producer thread streams each unit's int4 codes with 2D TMA (128-byte
 //     swizzled boxes, so the MMA fragment reads below hit no bank twice) and
 //     its scales and biases with bulk copies into a ring of shared-memory
-//     slots, as far ahead as the ring allows, and asks L2 for the unit one ring
-//     length further; down units are loaded before their inputs exist;
+//     slots, as far ahead as the ring allows; down units are loaded before
+//     their inputs exist;
 //   - eight consumer warps compute each unit from shared memory, write its
 //     result to global memory, release the slot and publish the unit in
 //     shared memory;
@@ -58,7 +58,6 @@ namespace {
 using namespace tc;
 
 constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kWarpProd = 8, kWarpSig = 9;
 constexpr int kSThreads = 320;
 constexpr int kCounterStride = 32;       // counters 128 bytes apart: pollers and writers do not share a line
@@ -83,7 +82,7 @@ struct StreamGeom {
     uint32_t up_off, sc1_off, sb1, bytes1;
     int nb2;               // 128-byte boxes per down code row (I / 256)
     uint32_t sc2_off;
-    uint32_t x_off, sumx_off, h_off, red_off, dyn;
+    uint32_t x_off, sumx_off, h_off, hs_off, red_off, dyn;
     int x_stride;          // uint4 per staged x row
     int h_stride;          // fp16 per staged h column
 };
@@ -100,12 +99,13 @@ struct SSmem {
     int ncols[kMaxList];
     int colptr[kMaxList + 1];
     int colf[kDecodeMaxTok * (kMaxTopK + 1)];   // slot index f of each column, expert after expert
+    int ctok[kDecodeMaxTok * (kMaxTopK + 1)];   // token of each column
     int nlist;
-    int ready;
+    int ready[2];                          // per consumer group
     int abort;
-    int sig;                               // units finished by the consumers (the signal thread reads it)
+    int sig[2];                            // units finished by each consumer group (the signal thread reads them)
     int sig_done;                          // the signal thread has counted every unit
-    int ncomb, ncomb_snap;                 // combines queued for the consumers, and their snapshot
+    int ncomb, ncomb_snap[2];              // combines queued for the consumers, and each group's snapshot
     int combq[kMaxRowBlocks];
     uint64_t full[kMaxSlots], empty[kMaxSlots];
 };
@@ -165,6 +165,15 @@ __device__ __forceinline__ uint32_t swz_chunk(int grp, int g, int t4)
     return (uint32_t)((((((grp & 3) << 1) | (t4 >> 1)) ^ g) << 4) | ((t4 & 1) << 3));
 }
 
+// Element q (0..3) of four bf16 values packed in a uint2, as a float.
+__device__ __forceinline__ float bf16x4_at(uint2 v, int q)
+{
+    const uint32_t w = q < 2 ? v.x : v.y;
+    return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+__device__ __forceinline__ float f4_at(float4 v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
+__device__ __forceinline__ uint2 lds_u2(const uint16_t *p) { return *reinterpret_cast<const uint2 *>(p); }
+
 __device__ __forceinline__ uint32_t logit_key(float f)
 {
     uint32_t u = __float_as_uint(f);
@@ -204,19 +213,39 @@ __device__ __forceinline__ void st_release_cta(int *p, int v)
     asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Named barriers of the consumer warps: 1 + g for consumer group g (CT threads), 3 for all
+// consumer warps when there are two groups.
+// (The ids are immediates, g being warp-uniform, so that a CTA reserves only the barriers it uses.)
+template <int CT>
+__device__ __forceinline__ void group_bar(int g)
+{
+    if (g == 0)
+        asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");
+    else
+        asm volatile("bar.sync 2, %0;" ::"n"(CT) : "memory");
+}
 
-// Named barrier 1 over the consumer warps that also ORs a predicate (uniform stop decisions).
-__device__ __forceinline__ bool consumer_any(bool pred)
+// The group barrier that also ORs a predicate over the group (uniform stop decisions).
+template <int CT>
+__device__ __forceinline__ bool group_any(int g, bool pred)
 {
     uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred)
-        : "memory");
+    if (g == 0)
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"((uint32_t)pred), "n"(CT)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"((uint32_t)pred), "n"(CT)
+            : "memory");
     return r != 0;
 }
+
+__device__ __forceinline__ void all_consumers_bar() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
 __device__ __forceinline__ int col_token(int f, int T, int k) { return f < 0 ? -1 : (f >= T * k ? f - T * k : f / k); }
 
@@ -390,91 +419,84 @@ __device__ __forceinline__ void phase0(SSmem &S, const FusedDecodeArgs &a, uint4
 #pragma unroll 1
         for (int tt = tid; tt < T; tt += kSThreads) S.colf[S.colptr[S.nlist - 1] + tt] = T * k + tt;
     __syncthreads();
+#pragma unroll 1
+    for (int i = tid; i < S.colptr[S.nlist]; i += kSThreads) S.ctok[i] = col_token(S.colf[i], T, k);
+    __syncthreads();
 }
 
 // ------------------------------------------------------------------ producer (one thread)
 __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const FusedDecodeArgs &a,
                                       const StreamGeom &geo, uint8_t *ring, int U1, int U)
 {
+    // Every argument the loop needs, read once into registers: the arguments are reached through
+    // references here, and each copy instruction below is a compiler memory barrier, so fields
+    // read inside the loop would be fetched again after every copy.
     const int H = a.H, I = a.I, E = a.E, G = H / kGroup, GI = I / kGroup, R = geo.R;
     const int RBI = I / kRows1, RBH = (H + kRows2 - 1) / kRows2;
-    prefetch_map(&maps.g);
-    prefetch_map(&maps.u);
-    prefetch_map(&maps.d);
+    const int nb1 = geo.nb1, nb2 = geo.nb2;
+    const uint32_t slot_bytes = geo.slot, up_off = geo.up_off, sc1_off = geo.sc1_off, sb1 = geo.sb1;
+    const uint32_t bytes1 = geo.bytes1, sc2_off = geo.sc2_off;
+    const long long wait_limit = a.wait_limit;
+    const uint16_t *gsc = a.gate.scales, *gbi = a.gate.biases, *usc = a.up.scales, *ubi = a.up.biases;
+    const uint16_t *dsc = a.down.scales, *dbi = a.down.biases;
+    const uint16_t *sgsc = a.s_gate.scales, *sgbi = a.s_gate.biases, *susc = a.s_up.scales, *subi = a.s_up.biases;
+    const uint16_t *sdsc = a.s_down.scales, *sdbi = a.s_down.biases;
+    const CUtensorMap *mg_r = &maps.g, *mu_r = &maps.u, *md_r = &maps.d;
+    const CUtensorMap *mg_s = &maps.sg, *mu_s = &maps.su, *md_s = &maps.sd;
+    prefetch_map(mg_r);
+    prefetch_map(mu_r);
+    prefetch_map(md_r);
     if (a.has_shared) {
-        prefetch_map(&maps.sg);
-        prefetch_map(&maps.su);
-        prefetch_map(&maps.sd);
+        prefetch_map(mg_s);
+        prefetch_map(mu_s);
+        prefetch_map(md_s);
     }
     int issued = 0;
-    #pragma unroll 1
+#pragma unroll 1
     for (int w = blockIdx.x, i = 0; w < U; w += gridDim.x, ++i) {
         const int slot = i % R;
-        if (i >= R && !mbar_wait_sleepy(smem_u32(&S.empty[slot]), ((i / R) - 1) & 1, a.wait_limit, &S.abort)) {
+        if (i >= R && !mbar_wait_sleepy(smem_u32(&S.empty[slot]), ((i / R) - 1) & 1, wait_limit, &S.abort)) {
             S.abort = 1;
             record_status(a.status, MOE_ERR_TIMEOUT);
             break;
         }
-        uint8_t *base = ring + (size_t)slot * geo.slot;
+        uint8_t *base = ring + (size_t)slot * slot_bytes;
         const uint32_t fb = smem_u32(&S.full[slot]);
-        // this unit into the slot, and the unit one ring length ahead into L2
-        #pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-            const int wu = pass == 0 ? w : w + R * (int)gridDim.x;
-            if (wu >= U) break;
-            if (wu < U1) {
-                const int d = wu / RBI, rb = wu - d * RBI, e = S.list[d];
-                const bool shr = e == E;
-                const int row0 = (shr ? 0 : e * I) + rb * kRows1;
-                const QMatDev &qg = shr ? a.s_gate : a.gate, &qu = shr ? a.s_up : a.up;
-                const size_t so = (size_t)row0 * G;
-                if (pass == 0) {
-                    const CUtensorMap *mg = shr ? &maps.sg : &maps.g, *mu = shr ? &maps.su : &maps.u;
-                    mbar_arrive_expect_tx(fb, geo.bytes1);
-                    #pragma unroll 1
-                    for (int j = 0; j < geo.nb1; ++j) {
-                        tma_load_2d(smem_u32(base + j * kBox1), mg, j * 128, row0, fb);
-                        tma_load_2d(smem_u32(base + geo.up_off + j * kBox1), mu, j * 128, row0, fb);
-                    }
-                    bulk_load(smem_u32(base + geo.sc1_off), qg.scales + so, geo.sb1, fb);
-                    bulk_load(smem_u32(base + geo.sc1_off + geo.sb1), qg.biases + so, geo.sb1, fb);
-                    bulk_load(smem_u32(base + geo.sc1_off + 2 * geo.sb1), qu.scales + so, geo.sb1, fb);
-                    bulk_load(smem_u32(base + geo.sc1_off + 3 * geo.sb1), qu.biases + so, geo.sb1, fb);
-                } else {
-                    const uint32_t cb = (uint32_t)kRows1 * (H / 2);
-                    prefetch_l2_bulk(qg.codes + (size_t)row0 * (H / 2), cb);
-                    prefetch_l2_bulk(qu.codes + (size_t)row0 * (H / 2), cb);
-                    prefetch_l2_bulk(qg.scales + so, geo.sb1);
-                    prefetch_l2_bulk(qg.biases + so, geo.sb1);
-                    prefetch_l2_bulk(qu.scales + so, geo.sb1);
-                    prefetch_l2_bulk(qu.biases + so, geo.sb1);
-                }
-            } else {
-                const int v = wu - U1, d = v / RBH, rb = v - d * RBH, e = S.list[d];
-                const bool shr = e == E;
-                const int row0 = (shr ? 0 : e * H) + rb * kRows2;
-                const int nrows = min(kRows2, H - rb * kRows2);
-                const uint32_t sb2 = (uint32_t)nrows * GI * 2;
-                const QMatDev &qd = shr ? a.s_down : a.down;
-                const size_t so = (size_t)row0 * GI;
-                if (pass == 0) {
-                    const CUtensorMap *md = shr ? &maps.sd : &maps.d;
-                    mbar_arrive_expect_tx(fb, (uint32_t)geo.nb2 * kBox2 + 2 * sb2);
-                    #pragma unroll 1
-                    for (int j = 0; j < geo.nb2; ++j) tma_load_2d(smem_u32(base + j * kBox2), md, j * 128, row0, fb);
-                    bulk_load(smem_u32(base + geo.sc2_off), qd.scales + so, sb2, fb);
-                    bulk_load(smem_u32(base + geo.sc2_off + kRows2 * GI * 2), qd.biases + so, sb2, fb);
-                } else {
-                    prefetch_l2_bulk(qd.codes + (size_t)row0 * (I / 2), (uint32_t)nrows * (I / 2));
-                    prefetch_l2_bulk(qd.scales + so, sb2);
-                    prefetch_l2_bulk(qd.biases + so, sb2);
-                }
+        // this unit into the slot
+        if (w < U1) {
+            const int d = w / RBI, rb = w - d * RBI, e = S.list[d];
+            const bool shr = e == E;
+            const int row0 = (shr ? 0 : e * I) + rb * kRows1;
+            const size_t so = (size_t)row0 * G;
+            const CUtensorMap *mg = shr ? mg_s : mg_r, *mu = shr ? mu_s : mu_r;
+            mbar_arrive_expect_tx(fb, bytes1);
+#pragma unroll 1
+            for (int j = 0; j < nb1; ++j) {
+                tma_load_2d(smem_u32(base + j * kBox1), mg, j * 128, row0, fb);
+                tma_load_2d(smem_u32(base + up_off + j * kBox1), mu, j * 128, row0, fb);
             }
+            bulk_load(smem_u32(base + sc1_off), (shr ? sgsc : gsc) + so, sb1, fb);
+            bulk_load(smem_u32(base + sc1_off + sb1), (shr ? sgbi : gbi) + so, sb1, fb);
+            bulk_load(smem_u32(base + sc1_off + 2 * sb1), (shr ? susc : usc) + so, sb1, fb);
+            bulk_load(smem_u32(base + sc1_off + 3 * sb1), (shr ? subi : ubi) + so, sb1, fb);
+        } else {
+            const int v = w - U1, d = v / RBH, rb = v - d * RBH, e = S.list[d];
+            const bool shr = e == E;
+            const int row0 = (shr ? 0 : e * H) + rb * kRows2;
+            const int nrows = min(kRows2, H - rb * kRows2);
+            const uint32_t sb2 = (uint32_t)nrows * GI * 2;
+            const size_t so = (size_t)row0 * GI;
+            const CUtensorMap *md = shr ? md_s : md_r;
+            mbar_arrive_expect_tx(fb, (uint32_t)nb2 * kBox2 + 2 * sb2);
+#pragma unroll 1
+            for (int j = 0; j < nb2; ++j) tma_load_2d(smem_u32(base + j * kBox2), md, j * 128, row0, fb);
+            bulk_load(smem_u32(base + sc2_off), (shr ? sdsc : dsc) + so, sb2, fb);
+            bulk_load(smem_u32(base + sc2_off + kRows2 * GI * 2), (shr ? sdbi : dbi) + so, sb2, fb);
         }
         issued = i + 1;
     }
     // every issued copy lands before the CTA may exit
-    #pragma unroll 1
+#pragma unroll 1
     for (int q = issued > R ? issued - R : 0; q < issued; ++q)
         mbar_wait(smem_u32(&S.full[q % R]), (q / R) & 1, kDrainLimit, nullptr);
 }
@@ -485,6 +507,7 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
 // exp(l - l_top) / sum over the picks and w_s = sigmoid(bf16(gamma)) in fp64, one rounding
 // to bf16, published for the combining CTAs.  Then (lane 0) the completion signals of
 // this CTA's units.
+template <int CG>
 __device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U1, int U, int D)
 {
     const int lane = threadIdx.x & 31, T = a.T, k = a.k, H = a.H, I = a.I;
@@ -517,10 +540,14 @@ __device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U
         }
     }
     if (lane != 0) return;
-    // The consumers publish every finished unit in S.sig (release at CTA scope).  One fence
-    // makes a batch of units' global stores visible GPU-wide, then each unit is counted.
+    int *const cnt_expert = a.cnt_expert, *const cnt_rows = a.cnt_rows;   // read once (see the producer)
+    const int *const cnt_pick = a.cnt_pick;
+    const long long wait_limit = a.wait_limit;
+    // Consumer group g takes this CTA's units g, g + CG, g + 2 CG, ... and publishes how many it
+    // has finished in S.sig[g] (release at CTA scope).  One fence makes a batch of units' global
+    // stores visible GPU-wide, then each unit is counted.
     const int nmine = (int)blockIdx.x < U ? (U - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    int done = 0, nq = 0;
+    int done = 0, nq = 0, gdone0 = 0, gdone1 = 0;
     bool picks = a.ids_in != nullptr;       // given routing: S.p and S.ws were filled in phase 0
     // the published pick weights into shared memory (once every token's are out), for the combines
     auto take_picks = [&]() {
@@ -533,10 +560,11 @@ __device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U
     };
     long long polls = 0;
     while (done < nmine) {
-        const int avail = ld_acquire_cta(&S.sig);
-        if (avail <= done) {
-            if (S.abort || ++polls > a.wait_limit) break;
-            if (!picks && ld_acquire(a.cnt_pick) >= T) {   // idle: fetch the pick weights ahead of any combine
+        const int avail0 = ld_acquire_cta(&S.sig[0]), avail1 = CG > 1 ? ld_acquire_cta(&S.sig[1]) : 0;
+        const int fresh = (avail0 - gdone0) + (avail1 - gdone1);
+        if (fresh <= 0) {
+            if (S.abort || ++polls > wait_limit) break;
+            if (!picks && ld_acquire(cnt_pick) >= T) {   // idle: fetch the pick weights ahead of any combine
                 take_picks();
                 picks = true;
             }
@@ -546,17 +574,20 @@ __device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U
         polls = 0;
         __threadfence();
         #pragma unroll 1
-        for (; done < avail; ++done) {
-            const int w = (int)blockIdx.x + done * (int)gridDim.x;
+        for (int q = 0; q < fresh; ++q, ++done) {
+            // the next finished unit: group 0's first, then group 1's
+            const bool g0 = gdone0 < avail0;
+            const int ui = g0 ? CG * gdone0++ : 1 + CG * gdone1++;
+            const int w = (int)blockIdx.x + ui * (int)gridDim.x;
             if (w < U1) {
-                atomicAdd(a.cnt_expert + (w / RBI) * kCounterStride, 1);
+                atomicAdd(cnt_expert + (w / RBI) * kCounterStride, 1);
                 continue;
             }
             const int rb = (w - U1) % RBH;
-            if (atomicAdd(a.cnt_rows + rb * kCounterStride, 1) != D - 1) continue;
+            if (atomicAdd(cnt_rows + rb * kCounterStride, 1) != D - 1) continue;
             __threadfence();                  // every unit's slot outputs, before the combine reads them
             if (!picks) {
-                picks = poll_at_least(a.cnt_pick, T, a.wait_limit);
+                picks = poll_at_least(cnt_pick, T, wait_limit);
                 if (picks) take_picks();
                 else record_status(a.status, MOE_ERR_TIMEOUT);
             }
@@ -574,57 +605,69 @@ __device__ __noinline__ void signaller(SSmem &S, const FusedDecodeArgs &a, int U
 //
 // Row block rb of y (or acc): sum over the token's slots in slot order, one rounding.  The
 // pick weights are in shared memory: the signal thread filled them before queueing the block.
-__device__ __noinline__ void combine_block(SSmem &S, const FusedDecodeArgs &a, int rb)
+template <int CT>
+__device__ __noinline__ void combine_block(SSmem &S, const FusedDecodeArgs &a, int rb, int gid)
 {
-    const int tid = threadIdx.x, T = a.T, H = a.H, k = a.k;
+    const int gt = threadIdx.x - gid * CT, T = a.T, H = a.H, k = a.k;
+    const bool has_shared = a.has_shared != 0;
+    const float *const yslot = a.yslot;       // arguments read once (see the producer)
+    uint16_t *const y = a.y;
+    float *const acc = a.acc;
     const int nrow = min(kRows2, H - rb * kRows2);
-    #pragma unroll 1
-    for (int q = tid; q < nrow * T; q += kConsumers) {
+#pragma unroll 1
+    for (int q = gt; q < nrow * T; q += CT) {
         const int tt = q / nrow, row = rb * kRows2 + (q - tt * nrow);
         float ys[kMaxTopK + 1];                     // every load in flight before the first add
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) ys[j] = j < k ? __ldcg(a.yslot + ((size_t)tt * k + j) * H + row) : 0.f;
-        ys[kMaxTopK] = a.has_shared ? __ldcg(a.yslot + ((size_t)T * k + tt) * H + row) : 0.f;
+        for (int j = 0; j < kMaxTopK; ++j) ys[j] = j < k ? __ldcg(yslot + ((size_t)tt * k + j) * H + row) : 0.f;
+        ys[kMaxTopK] = has_shared ? __ldcg(yslot + ((size_t)T * k + tt) * H + row) : 0.f;
         float s = 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)
             if (j < k) s = fmaf(S.p[tt][j], ys[j], s);
-        if (a.has_shared) s = fmaf(S.ws[tt], ys[kMaxTopK], s);
-        if (a.y)
-            a.y[(size_t)tt * H + row] = float_to_bf16_bits(s);
+        if (has_shared) s = fmaf(S.ws[tt], ys[kMaxTopK], s);
+        if (y)
+            y[(size_t)tt * H + row] = float_to_bf16_bits(s);
         else
-            a.acc[(size_t)tt * H + row] += s;
+            acc[(size_t)tt * H + row] += s;
     }
-    consumer_bar();
+    group_bar<CT>(gid);
 }
 
 // ------------------------------------------------------------------ kernel
-template <int NT, int MINB>
+//
+// CG consumer groups of 8 / CG warps: group g computes this CTA's units g, g + CG, ...
+// With two groups one group's per-unit latencies (waits, barriers, the epilogue, the h
+// exchange) overlap the other group's arithmetic.  The staged h columns of the down units
+// share their shared memory with x: a group stages h only once both groups are past their
+// last gate/up unit.
+template <int NT, int MINB, int CG>
 __global__ void __launch_bounds__(kSThreads, MINB)
     decode_stream_kernel(const __grid_constant__ StreamMaps maps, const __grid_constant__ FusedDecodeArgs a,
                          const __grid_constant__ StreamGeom geo)
 {
+    constexpr int CW = kConsumerWarps / CG, CT = CW * 32;   // warps and threads per consumer group
+    constexpr int RT = kRows2 / (16 * CW);                  // 16-row tiles per warp in a down unit
     __shared__ SSmem S;
     extern __shared__ uint8_t dyn_raw[];
     uint8_t *dyn = align_smem_1024(dyn_raw);
     uint8_t *ring = dyn;
     uint4 *s_x = reinterpret_cast<uint4 *>(dyn + geo.x_off);          // [T][x_stride] bf16 rows, k order
     float *s_sumx = reinterpret_cast<float *>(dyn + geo.sumx_off);    // [T][G]
-    uint16_t *s_h = reinterpret_cast<uint16_t *>(dyn + geo.h_off);    // [NT * 8][h_stride] fp16 columns, k order
-    float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);      // [8][2][16][NT * 8]
+    float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);      // [CG][8][2][16][NT * 8] split-K partials
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    const int T = a.T, H = a.H, I = a.I, k = a.k;
+    const int T = a.T, H = a.H, I = a.I;
     const int G = H / kGroup, GI = I / kGroup, xs = geo.x_stride, R = geo.R;
     const long long limit = a.wait_limit;
 
     if (tid == 0) {
         for (int s = 0; s < R; ++s) {
             mbar_init(smem_u32(&S.full[s]), 1);
-            mbar_init(smem_u32(&S.empty[s]), kConsumers);
+            mbar_init(smem_u32(&S.empty[s]), CT);   // one group consumes each unit
         }
         S.abort = 0;
-        S.sig = 0;
+        S.sig[0] = S.sig[1] = 0;
         S.sig_done = 0;
         S.ncomb = 0;
         fence_mbar_init();
@@ -640,250 +683,342 @@ __global__ void __launch_bounds__(kSThreads, MINB)
         return;
     }
     if (warp == kWarpSig) {
-        signaller(S, a, U1, U, D);
+        signaller<CG>(S, a, U1, U, D);
         return;
     }
 
     // ---------------------------------------------------------------- consumers (warps 0-7)
     constexpr int NC = NT * 8;
-    const int gbeg = (warp * G) / kConsumerWarps, gend = ((warp + 1) * G) / kConsumerWarps;
-    int ncomb_done = 0;
+    const int gid = warp / CW, gw = warp - gid * CW, gt = tid - gid * CT;
+    uint16_t *s_h = reinterpret_cast<uint16_t *>(dyn + geo.h_off) + (size_t)gid * NC * geo.h_stride;   // [NC][h_stride]
+    float *s_hs = reinterpret_cast<float *>(dyn + geo.hs_off) + gid * NC * GI;                        // [NC][I / 64]
+    int ncomb_done = gid;               // this group runs the queued combines gid, gid + CG, ...
+    bool past_gateup = false;           // both groups are past their gate/up units (h may replace x)
+    auto run_combines = [&](int snap) {
+        for (; ncomb_done < snap; ncomb_done += CG) combine_block<CT>(S, a, S.combq[ncomb_done], gid);
+    };
 
-    for (int w = blockIdx.x, i = 0; w < U; w += gridDim.x, ++i) {
+    for (int w = blockIdx.x + gid * (int)gridDim.x, i = gid; w < U; w += CG * (int)gridDim.x, i += CG) {
         const int slot = i % R;
         const bool got = mbar_wait(smem_u32(&S.full[slot]), (i / R) & 1, limit, &S.abort);
         if (!got) {
             S.abort = 1;
             record_status(a.status, MOE_ERR_TIMEOUT);
         }
-        if (tid == 0) S.ncomb_snap = ld_acquire_cta(&S.ncomb);
-        if (consumer_any(!got)) break;
-        for (const int snap = S.ncomb_snap; ncomb_done < snap; ++ncomb_done) combine_block(S, a, S.combq[ncomb_done]);
+        if (gt == 0) S.ncomb_snap[gid] = ld_acquire_cta(&S.ncomb);
+        if (group_any<CT>(gid, !got)) break;
+        run_combines(S.ncomb_snap[gid]);
         const uint8_t *base = ring + (size_t)slot * geo.slot;
         const uint32_t eb = smem_u32(&S.empty[slot]);
 
         if (w < U1) {
-            // ------------------------------------------------ gate/up unit: 16 rows, split-K over the warps
+            // ------------------------------------------------ gate/up unit: 16 rows, split-K over the group's warps
             const int d = w / RBI, rb = w - d * RBI;
             const int ncol = min(S.ncols[d], T);
-            const int *colf = S.colf + S.colptr[d];
+            const int *colf = S.colf + S.colptr[d], *ctok = S.ctok + S.colptr[d];
             int xrow[NT], tA[NT], tB[NT];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int c = j * 8 + g, cA = j * 8 + 2 * t4;
-                xrow[j] = col_token(c < ncol ? colf[c] : -1, T, k);
-                tA[j] = col_token(cA < ncol ? colf[cA] : -1, T, k);
-                tB[j] = col_token(cA + 1 < ncol ? colf[cA + 1] : -1, T, k);
+                xrow[j] = c < ncol ? ctok[c] : -1;
+                tA[j] = cA < ncol ? ctok[cA] : -1;
+                tB[j] = cA + 1 < ncol ? ctok[cA + 1] : -1;
             }
             const uint16_t *gs = reinterpret_cast<const uint16_t *>(base + geo.sc1_off) + g * G;
             const uint16_t *gbi = gs + kRows1 * G, *us = gbi + kRows1 * G, *ubi = us + kRows1 * G;
             const uint8_t *cb = base + g * 128;          // row g of box 0; row g + 8 is 1024 bytes further
-            float acc_g[NT][4], acc_u[NT][4];
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc_g[j][q] = acc_u[j][q] = 0.f;
+            // Split-K in a fixed partition whatever the number of groups: partial v (0..7) is the sum over
+            // the 128-byte code boxes v, v + 8, ... (four groups of both matrices per box), and the
+            // partials are added in the order v = 0..7.  Warp gw of the group computes the partials
+            // gw, gw + CW, ...; a token's h is thus the same in every batch.
+            float *red = s_red + (size_t)gid * kConsumerWarps * 2 * 16 * NC;   // [8][2][16][NC]
+            float last[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-            for (int grp = gbeg; grp < gend; ++grp) {
-                const uint32_t o = (uint32_t)(grp >> 2) * kBox1 + swz_chunk(grp, g, t4);
-                const uint2 cg0 = *reinterpret_cast<const uint2 *>(cb + o);
-                const uint2 cg1 = *reinterpret_cast<const uint2 *>(cb + o + 1024);
-                const uint2 cu0 = *reinterpret_cast<const uint2 *>(cb + geo.up_off + o);
-                const uint2 cu1 = *reinterpret_cast<const uint2 *>(cb + geo.up_off + o + 1024);
-                const float s_g0 = bf16_bits_to_float(gs[grp]), s_g1 = bf16_bits_to_float(gs[8 * G + grp]);
-                const float s_u0 = bf16_bits_to_float(us[grp]), s_u1 = bf16_bits_to_float(us[8 * G + grp]);
-                const float c_g0 = fmaf(-128.f, s_g0, bf16_bits_to_float(gbi[grp]));
-                const float c_g1 = fmaf(-128.f, s_g1, bf16_bits_to_float(gbi[8 * G + grp]));
-                const float c_u0 = fmaf(-128.f, s_u0, bf16_bits_to_float(ubi[grp]));
-                const float c_u1 = fmaf(-128.f, s_u1, bf16_bits_to_float(ubi[8 * G + grp]));
-                uint32_t ag[2][8], au[2][8];
-                nib8<false>(cg0.x, ag[0]);
-                nib8<false>(cg0.y, ag[0] + 4);
-                nib8<false>(cg1.x, ag[1]);
-                nib8<false>(cg1.y, ag[1] + 4);
-                nib8<false>(cu0.x, au[0]);
-                nib8<false>(cu0.y, au[0] + 4);
-                nib8<false>(cu1.x, au[1]);
-                nib8<false>(cu1.y, au[1] + 4);
+            for (int v = gw; v < kConsumerWarps; v += CW) {
+                float acc_g[NT][4], acc_u[NT][4];
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc_g[j][q] = acc_u[j][q] = 0.f;
+                // one box per step, unrolled so that every shared-memory load of a box is in flight before
+                // its first MMA
+#pragma unroll 1
+                for (int bx = v; bx < geo.nb1; bx += kConsumerWarps) {
+                    const uint2 vsg0 = lds_u2(gs + 4 * bx), vsg1 = lds_u2(gs + 8 * G + 4 * bx);
+                    const uint2 vbg0 = lds_u2(gbi + 4 * bx), vbg1 = lds_u2(gbi + 8 * G + 4 * bx);
+                    const uint2 vsu0 = lds_u2(us + 4 * bx), vsu1 = lds_u2(us + 8 * G + 4 * bx);
+                    const uint2 vbu0 = lds_u2(ubi + 4 * bx), vbu1 = lds_u2(ubi + 8 * G + 4 * bx);
+                    float4 sxA[NT], sxB[NT];                  // sums of x over the box's four groups
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                        sxA[j] = tA[j] >= 0 ? *reinterpret_cast<const float4 *>(s_sumx + tA[j] * G + 4 * bx) : z;
+                        sxB[j] = tB[j] >= 0 ? *reinterpret_cast<const float4 *>(s_sumx + tB[j] * G + 4 * bx) : z;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int grp = 4 * bx + q;
+                        const uint32_t o = (uint32_t)bx * kBox1 + swz_chunk(q, g, t4);
+                        const uint2 cg0 = *reinterpret_cast<const uint2 *>(cb + o);
+                        const uint2 cg1 = *reinterpret_cast<const uint2 *>(cb + o + 1024);
+                        const uint2 cu0 = *reinterpret_cast<const uint2 *>(cb + geo.up_off + o);
+                        const uint2 cu1 = *reinterpret_cast<const uint2 *>(cb + geo.up_off + o + 1024);
+                        const float s_g0 = bf16x4_at(vsg0, q), s_g1 = bf16x4_at(vsg1, q);
+                        const float s_u0 = bf16x4_at(vsu0, q), s_u1 = bf16x4_at(vsu1, q);
+                        const float c_g0 = fmaf(-128.f, s_g0, bf16x4_at(vbg0, q));
+                        const float c_g1 = fmaf(-128.f, s_g1, bf16x4_at(vbg1, q));
+                        const float c_u0 = fmaf(-128.f, s_u0, bf16x4_at(vbu0, q));
+                        const float c_u1 = fmaf(-128.f, s_u1, bf16x4_at(vbu1, q));
+                        uint32_t ag[2][8], au[2][8];
+                        nib8<false>(cg0.x, ag[0]);
+                        nib8<false>(cg0.y, ag[0] + 4);
+                        nib8<false>(cg1.x, ag[1]);
+                        nib8<false>(cg1.y, ag[1] + 4);
+                        nib8<false>(cu0.x, au[0]);
+                        nib8<false>(cu0.y, au[0] + 4);
+                        nib8<false>(cu1.x, au[1]);
+                        nib8<false>(cu1.y, au[1] + 4);
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) {
+                            if (j * 8 >= ncol) break;
+                            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                            if (xrow[j] >= 0) {
+                                const uint4 *xr = s_x + xrow[j] * xs + grp * 8 + 2 * t4;
+                                lo = xr[0];
+                                hi = xr[1];
+                            }
+                            const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                            float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                mma16816<false>(dg, ag[0][2 * m], ag[1][2 * m], ag[0][2 * m + 1], ag[1][2 * m + 1], bp[2 * m],
+                                                bp[2 * m + 1]);
+                                mma16816<false>(du, au[0][2 * m], au[1][2 * m], au[0][2 * m + 1], au[1][2 * m + 1], bp[2 * m],
+                                                bp[2 * m + 1]);
+                            }
+                            const float sA = f4_at(sxA[j], q), sB = f4_at(sxB[j], q);
+                            acc_g[j][0] = fmaf(s_g0, dg[0], fmaf(c_g0, sA, acc_g[j][0]));
+                            acc_g[j][1] = fmaf(s_g0, dg[1], fmaf(c_g0, sB, acc_g[j][1]));
+                            acc_g[j][2] = fmaf(s_g1, dg[2], fmaf(c_g1, sA, acc_g[j][2]));
+                            acc_g[j][3] = fmaf(s_g1, dg[3], fmaf(c_g1, sB, acc_g[j][3]));
+                            acc_u[j][0] = fmaf(s_u0, du[0], fmaf(c_u0, sA, acc_u[j][0]));
+                            acc_u[j][1] = fmaf(s_u0, du[1], fmaf(c_u0, sB, acc_u[j][1]));
+                            acc_u[j][2] = fmaf(s_u1, du[2], fmaf(c_u1, sA, acc_u[j][2]));
+                            acc_u[j][3] = fmaf(s_u1, du[3], fmaf(c_u1, sB, acc_u[j][3]));
+                        }
+                    }
+                }
+                float *rg = red + (v * 2 + 0) * 16 * NC, *ru = rg + 16 * NC;
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    if (j * 8 >= ncol) break;
-                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                    if (xrow[j] >= 0) {
-                        const uint4 *xr = s_x + xrow[j] * xs + grp * 8 + 2 * t4;
-                        lo = xr[0];
-                        hi = xr[1];
-                    }
-                    const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                    float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        mma16816<false>(dg, ag[0][2 * m], ag[1][2 * m], ag[0][2 * m + 1], ag[1][2 * m + 1], bp[2 * m],
-                                        bp[2 * m + 1]);
-                        mma16816<false>(du, au[0][2 * m], au[1][2 * m], au[0][2 * m + 1], au[1][2 * m + 1], bp[2 * m],
-                                        bp[2 * m + 1]);
-                    }
-                    const float sxA = tA[j] >= 0 ? s_sumx[tA[j] * G + grp] : 0.f;
-                    const float sxB = tB[j] >= 0 ? s_sumx[tB[j] * G + grp] : 0.f;
-                    acc_g[j][0] = fmaf(s_g0, dg[0], fmaf(c_g0, sxA, acc_g[j][0]));
-                    acc_g[j][1] = fmaf(s_g0, dg[1], fmaf(c_g0, sxB, acc_g[j][1]));
-                    acc_g[j][2] = fmaf(s_g1, dg[2], fmaf(c_g1, sxA, acc_g[j][2]));
-                    acc_g[j][3] = fmaf(s_g1, dg[3], fmaf(c_g1, sxB, acc_g[j][3]));
-                    acc_u[j][0] = fmaf(s_u0, du[0], fmaf(c_u0, sxA, acc_u[j][0]));
-                    acc_u[j][1] = fmaf(s_u0, du[1], fmaf(c_u0, sxB, acc_u[j][1]));
-                    acc_u[j][2] = fmaf(s_u1, du[2], fmaf(c_u1, sxA, acc_u[j][2]));
-                    acc_u[j][3] = fmaf(s_u1, du[3], fmaf(c_u1, sxB, acc_u[j][3]));
+                    const int c0 = j * 8 + 2 * t4;
+                    rg[g * NC + c0] = acc_g[j][0];
+                    rg[g * NC + c0 + 1] = acc_g[j][1];
+                    rg[(g + 8) * NC + c0] = acc_g[j][2];
+                    rg[(g + 8) * NC + c0 + 1] = acc_g[j][3];
+                    ru[g * NC + c0] = acc_u[j][0];
+                    ru[g * NC + c0 + 1] = acc_u[j][1];
+                    ru[(g + 8) * NC + c0] = acc_u[j][2];
+                    ru[(g + 8) * NC + c0 + 1] = acc_u[j][3];
                 }
+                last[0] = acc_g[0][0];
+                last[1] = acc_g[0][2];
+                last[2] = acc_u[0][0];
+                last[3] = acc_u[0][2];
             }
-            mbar_arrive_after(eb, acc_g[0][0], acc_g[0][2], acc_u[0][0], acc_u[0][2]);
-            float *rg = s_red + (warp * 2 + 0) * 16 * NC, *ru = rg + 16 * NC;
+            mbar_arrive_after(eb, last[0], last[1], last[2], last[3]);
+            group_bar<CT>(gid);
+            // the partial sums in a fixed order, h = silu(g) u stored as fp16 in the
+            // codes' k order (so the down unit's fragments are plain loads)
+#pragma unroll 1
+            for (int q = gt; q < 16 * ncol; q += CT) {
+                const int row = q & 15, c = q >> 4;
+                float gsum = 0.f, usum = 0.f;
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const int c0 = j * 8 + 2 * t4;
-                rg[g * NC + c0] = acc_g[j][0];
-                rg[g * NC + c0 + 1] = acc_g[j][1];
-                rg[(g + 8) * NC + c0] = acc_g[j][2];
-                rg[(g + 8) * NC + c0 + 1] = acc_g[j][3];
-                ru[g * NC + c0] = acc_u[j][0];
-                ru[g * NC + c0 + 1] = acc_u[j][1];
-                ru[(g + 8) * NC + c0] = acc_u[j][2];
-                ru[(g + 8) * NC + c0 + 1] = acc_u[j][3];
-            }
-            consumer_bar();
-            {
-                const int row = tid & 15, c = tid >> 4;   // 256 threads = 16 rows x 16 columns
-                if (c < ncol) {
-                    float gsum = 0.f, usum = 0.f;
-#pragma unroll
-                    for (int ww = 0; ww < kConsumerWarps; ++ww) {
-                        gsum += s_red[((ww * 2 + 0) * 16 + row) * NC + c];
-                        usum += s_red[((ww * 2 + 1) * 16 + row) * NC + c];
-                    }
-                    const float hv = gsum / (1.f + __expf(-gsum)) * usum;
-                    // h in the codes' k order: the down unit's fragments are plain loads
-                    a.h[(size_t)colf[c] * I + kperm_pos(rb * kRows1 + row)] = __half_as_ushort(__float2half_rn(hv));
+                for (int v = 0; v < kConsumerWarps; ++v) {
+                    gsum += red[((v * 2 + 0) * 16 + row) * NC + c];
+                    usum += red[((v * 2 + 1) * 16 + row) * NC + c];
                 }
+                const float hv = gsum / (1.f + __expf(-gsum)) * usum;
+                a.h[(size_t)colf[c] * I + kperm_pos(rb * kRows1 + row)] = __half_as_ushort(__float2half_rn(hv));
             }
-            consumer_bar();
-            if (tid == 0) st_release_cta(&S.sig, i + 1);
+            group_bar<CT>(gid);
+            if (gt == 0) st_release_cta(&S.sig[gid], (i - gid) / CG + 1);
         } else {
-            // ------------------------------------------------ down unit: 128 rows, warp w rows 16 w .. 16 w + 15
+            // ------------------------------------------------ down unit: 128 rows, RT 16-row tiles per warp
+            if (CG > 1 && !past_gateup) {
+                all_consumers_bar();          // x is dead from here on: h takes its place
+                past_gateup = true;
+            }
             const int v = w - U1, d = v / RBH, rb = v - d * RBH;
             const int ncol = min(S.ncols[d], T);
             const int *colf = S.colf + S.colptr[d];
-            if (tid == 0) {
+            if (gt == 0) {
                 const bool ok = poll_at_least(a.cnt_expert + d * kCounterStride, RBI, limit);
                 if (!ok) {
                     S.abort = 1;
                     record_status(a.status, MOE_ERR_TIMEOUT);
                 }
-                S.ready = ok;
+                S.ready[gid] = ok;
             }
-            consumer_bar();
-            if (!S.ready) {
+            group_bar<CT>(gid);
+            if (!S.ready[gid]) {
                 mbar_arrive(eb);
                 break;
             }
-            // the expert's h columns into shared memory (L2 reads, after the acquire above)
-            #pragma unroll 1
-            for (int idx = tid, cpr = I / 8; idx < ncol * cpr; idx += kConsumers) {
-                const int c = idx / cpr, ch = idx - c * cpr;
-                *reinterpret_cast<uint4 *>(s_h + c * geo.h_stride + ch * 8) =
-                    __ldcg(reinterpret_cast<const uint4 *>(a.h + (size_t)colf[c] * I) + ch);
-            }
-            consumer_bar();
-            const int r0 = warp * 16 + g;                        // rows r0 and r0 + 8 of the unit
-            const bool wactive = rb * kRows2 + warp * 16 < H;   // H is a multiple of 64: warps are all in or out
-            const uint16_t *dsc = reinterpret_cast<const uint16_t *>(base + geo.sc2_off) + r0 * GI;
-            const uint16_t *dbi = dsc + kRows2 * GI;
-            const uint8_t *cb = base + r0 * 128;
-            float acc[NT][4];
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
-            if (wactive) {
+            // the expert's h columns into shared memory (L2 reads, after the acquire above), and each
+            // column's sums over the groups of those fp16 values: 8 values per thread, then a shuffle
+            // tree over the group's 8 threads (one fixed order)
+            {
+                const int cpr = I / 8, n = ncol * cpr;
 #pragma unroll 1
-                for (int grp = 0; grp < GI; ++grp) {
-                    const uint32_t o = (uint32_t)(grp >> 2) * kBox2 + swz_chunk(grp, g, t4);
-                    const uint2 c0 = *reinterpret_cast<const uint2 *>(cb + o);
-                    const uint2 c1 = *reinterpret_cast<const uint2 *>(cb + o + 1024);
-                    const float s0 = bf16_bits_to_float(dsc[grp]), s1 = bf16_bits_to_float(dsc[8 * GI + grp]);
-                    const float k0 = fmaf(-1024.f, s0, bf16_bits_to_float(dbi[grp]));
-                    const float k1 = fmaf(-1024.f, s1, bf16_bits_to_float(dbi[8 * GI + grp]));
-                    uint32_t ad[2][8];
-                    nib8<true>(c0.x, ad[0]);
-                    nib8<true>(c0.y, ad[0] + 4);
-                    nib8<true>(c1.x, ad[1]);
-                    nib8<true>(c1.y, ad[1] + 4);
+                for (int b0 = 0; b0 < n; b0 += CT) {
+                    const int idx = b0 + gt, c = idx / cpr, ch = idx - c * cpr;
+                    uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+                    if (idx < n) {
+                        hv = __ldcg(reinterpret_cast<const uint4 *>(a.h + (size_t)colf[c] * I) + ch);
+                        *reinterpret_cast<uint4 *>(s_h + c * geo.h_stride + ch * 8) = hv;
+                    }
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&hv.x));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&hv.y));
+                    const float2 f2 = __half22float2(*reinterpret_cast<const __half2 *>(&hv.z));
+                    const float2 f3 = __half22float2(*reinterpret_cast<const __half2 *>(&hv.w));
+                    float sum = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                    if (idx < n && (ch & 7) == 0) s_hs[c * GI + (ch >> 3)] = sum;
+                }
+            }
+            group_bar<CT>(gid);
+            float acc[RT][NT][4];
+#pragma unroll
+            for (int t = 0; t < RT; ++t)
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[t][j][q] = 0.f;
+            const int wrow = gw * 16 * RT;                          // first row of this warp in the unit
+            const int ntile = min(RT, max(0, (H - rb * kRows2 - wrow) / 16));   // H is a multiple of 64
+            const uint16_t *dsc = reinterpret_cast<const uint16_t *>(base + geo.sc2_off) + (wrow + g) * GI;
+            const uint16_t *dbi = dsc + kRows2 * GI;
+            const uint8_t *cb = base + (wrow + g) * 128;
+            if (ntile > 0) {
+                // one 128-byte code box (four groups) per step, unrolled; the h fragments serve every tile
+#pragma unroll 1
+                for (int bx = 0; bx < geo.nb2; ++bx) {
+                    uint2 vs0[RT], vs1[RT], vb0[RT], vb1[RT];
+#pragma unroll
+                    for (int t = 0; t < RT; ++t) {
+                        vs0[t] = lds_u2(dsc + (16 * t) * GI + 4 * bx);
+                        vs1[t] = lds_u2(dsc + (16 * t + 8) * GI + 4 * bx);
+                        vb0[t] = lds_u2(dbi + (16 * t) * GI + 4 * bx);
+                        vb1[t] = lds_u2(dbi + (16 * t + 8) * GI + 4 * bx);
+                    }
+                    float4 hA[NT], hB[NT];                    // sums of h over the box's four groups
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
-                        if (j * 8 >= ncol) break;
-                        const int c = j * 8 + g;
-                        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                        if (c < ncol) {
-                            const uint4 *hr = reinterpret_cast<const uint4 *>(s_h + c * geo.h_stride + grp * 64 + 16 * t4);
-                            lo = hr[0];
-                            hi = hr[1];
-                        }
-                        const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                        constexpr uint32_t ones = 0x3C003C00u;
-                        float dd[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
+                        const int cA = j * 8 + 2 * t4;
+                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                        hA[j] = cA < ncol ? *reinterpret_cast<const float4 *>(s_hs + cA * GI + 4 * bx) : z;
+                        hB[j] = cA + 1 < ncol ? *reinterpret_cast<const float4 *>(s_hs + (cA + 1) * GI + 4 * bx) : z;
+                    }
 #pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            mma16816<true>(dd, ad[0][2 * m], ad[1][2 * m], ad[0][2 * m + 1], ad[1][2 * m + 1], bp[2 * m],
-                                           bp[2 * m + 1]);
-                            mma16816<true>(dx, ones, ones, ones, ones, bp[2 * m], bp[2 * m + 1]);
+                    for (int q = 0; q < 4; ++q) {
+                        const int grp = 4 * bx + q;
+                        const uint32_t o = (uint32_t)bx * kBox2 + swz_chunk(q, g, t4);
+                        uint32_t ad[RT][2][8];
+#pragma unroll
+                        for (int t = 0; t < RT; ++t) {
+                            const uint2 c0 = *reinterpret_cast<const uint2 *>(cb + t * 2048 + o);
+                            const uint2 c1 = *reinterpret_cast<const uint2 *>(cb + t * 2048 + o + 1024);
+                            nib8<true>(c0.x, ad[t][0]);
+                            nib8<true>(c0.y, ad[t][0] + 4);
+                            nib8<true>(c1.x, ad[t][1]);
+                            nib8<true>(c1.y, ad[t][1] + 4);
                         }
-                        acc[j][0] = fmaf(s0, dd[0], fmaf(k0, dx[0], acc[j][0]));
-                        acc[j][1] = fmaf(s0, dd[1], fmaf(k0, dx[1], acc[j][1]));
-                        acc[j][2] = fmaf(s1, dd[2], fmaf(k1, dx[2], acc[j][2]));
-                        acc[j][3] = fmaf(s1, dd[3], fmaf(k1, dx[3], acc[j][3]));
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) {
+                            if (j * 8 >= ncol) break;
+                            const int c = j * 8 + g;
+                            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                            if (c < ncol) {
+                                const uint4 *hr =
+                                    reinterpret_cast<const uint4 *>(s_h + c * geo.h_stride + grp * 64 + 16 * t4);
+                                lo = hr[0];
+                                hi = hr[1];
+                            }
+                            const float xA = f4_at(hA[j], q), xB = f4_at(hB[j], q);
+#pragma unroll
+                            for (int t = 0; t < RT; ++t) {
+                                if (t >= ntile) break;
+                                const float s0 = bf16x4_at(vs0[t], q), s1 = bf16x4_at(vs1[t], q);
+                                const float k0 = fmaf(-1024.f, s0, bf16x4_at(vb0[t], q));
+                                const float k1 = fmaf(-1024.f, s1, bf16x4_at(vb1[t], q));
+                                float dd[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma16816<true>(dd, ad[t][0][0], ad[t][1][0], ad[t][0][1], ad[t][1][1], lo.x, lo.y);
+                                mma16816<true>(dd, ad[t][0][2], ad[t][1][2], ad[t][0][3], ad[t][1][3], lo.z, lo.w);
+                                mma16816<true>(dd, ad[t][0][4], ad[t][1][4], ad[t][0][5], ad[t][1][5], hi.x, hi.y);
+                                mma16816<true>(dd, ad[t][0][6], ad[t][1][6], ad[t][0][7], ad[t][1][7], hi.z, hi.w);
+                                acc[t][j][0] = fmaf(s0, dd[0], fmaf(k0, xA, acc[t][j][0]));
+                                acc[t][j][1] = fmaf(s0, dd[1], fmaf(k0, xB, acc[t][j][1]));
+                                acc[t][j][2] = fmaf(s1, dd[2], fmaf(k1, xA, acc[t][j][2]));
+                                acc[t][j][3] = fmaf(s1, dd[3], fmaf(k1, xB, acc[t][j][3]));
+                            }
+                        }
                     }
                 }
             }
-            mbar_arrive_after(eb, acc[0][0], acc[0][2], acc[0][1], acc[0][3]);
-            if (wactive) {
-                const int w0 = rb * kRows2 + r0, w1 = w0 + 8;
+            mbar_arrive_after(eb, acc[0][0][0], acc[0][0][2], acc[0][0][1], acc[0][0][3]);
+#pragma unroll
+            for (int t = 0; t < RT; ++t) {
+                if (t >= ntile) break;
+                const int w0 = rb * kRows2 + wrow + 16 * t + g, w1 = w0 + 8;
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
                     const int cA = j * 8 + 2 * t4, cB = cA + 1;
                     if (cA < ncol) {
                         const int f = colf[cA];
-                        a.yslot[(size_t)f * H + w0] = acc[j][0];
-                        a.yslot[(size_t)f * H + w1] = acc[j][2];
+                        a.yslot[(size_t)f * H + w0] = acc[t][j][0];
+                        a.yslot[(size_t)f * H + w1] = acc[t][j][2];
                     }
                     if (cB < ncol) {
                         const int f = colf[cB];
-                        a.yslot[(size_t)f * H + w0] = acc[j][1];
-                        a.yslot[(size_t)f * H + w1] = acc[j][3];
+                        a.yslot[(size_t)f * H + w0] = acc[t][j][1];
+                        a.yslot[(size_t)f * H + w1] = acc[t][j][3];
                     }
                 }
             }
-            consumer_bar();
-            if (tid == 0) st_release_cta(&S.sig, i + 1);
+            group_bar<CT>(gid);
+            if (gt == 0) st_release_cta(&S.sig[gid], (i - gid) / CG + 1);
         }
     }
-    // the remaining combines of this CTA, each as soon as the signal thread queues it, until it has
-    // counted every unit (bounded)
-    #pragma unroll 1
+    if (CG > 1 && !past_gateup) all_consumers_bar();   // every consumer thread takes that barrier once
+    // the remaining combines of this group, each as soon as the signal thread queues it, until it
+    // has counted every unit (bounded)
+#pragma unroll 1
     for (long long polls = 0;; ++polls) {
-        if (tid == 0) {
+        if (gt == 0) {
             const int done = ld_acquire_cta(&S.sig_done);
-            S.ncomb_snap = ld_acquire_cta(&S.ncomb);
-            S.ready = done || polls > limit;
+            S.ncomb_snap[gid] = ld_acquire_cta(&S.ncomb);
+            S.ready[gid] = done || polls > limit;
             if (!done && polls > limit) record_status(a.status, MOE_ERR_TIMEOUT);
         }
-        consumer_bar();
-        const bool last = S.ready;
-        for (const int snap = S.ncomb_snap; ncomb_done < snap; ++ncomb_done) combine_block(S, a, S.combq[ncomb_done]);
+        group_bar<CT>(gid);
+        const bool last = S.ready[gid];
+        run_combines(S.ncomb_snap[gid]);
         if (last) break;
-        if (tid == 0) __nanosleep(64);
-        consumer_bar();
+        if (gt == 0) __nanosleep(64);
+        group_bar<CT>(gid);
     }
 }
 
 // ------------------------------------------------------------------ host side
+
+// Consumer groups: two (alternating units) once a batch has more than two tokens, where a CTA
+// has many units; one for one or two tokens, where each CTA has one or two units and all eight
+// warps on a unit finish it soonest.
+int consumer_groups(int T) { return T > 2 ? 2 : 1; }
 
 // The ring layout needs 128-byte code boxes: H and I multiples of 256.
 bool stream_geometry(int T, int H, int I, size_t smem_budget, StreamGeom *out)
@@ -903,9 +1038,15 @@ bool stream_geometry(int T, int H, int I, size_t smem_budget, StreamGeom *out)
     g.slot = (uint32_t)align_up(size1 > size2 ? size1 : size2, 1024);
     g.x_stride = H / 8 + 1;
     g.h_stride = I + 8;
+    // x (read by the gate/up units) and each consumer group's staged h columns and their group
+    // sums (read by the down units, which every CTA takes after all of its gate/up units) share
+    // one region
+    const size_t CG = consumer_groups(T);
     const size_t xb = (size_t)T * g.x_stride * 16, sumb = (size_t)T * G * 4;
-    const size_t hb = (size_t)NT * 8 * g.h_stride * 2, redb = (size_t)kConsumerWarps * 2 * 16 * NT * 8 * 4;
-    const size_t fixed = align_up(xb, 16) + align_up(sumb, 16) + align_up(hb, 16) + redb + 1024;
+    const size_t hb = CG * NT * 8 * g.h_stride * 2, hsb = CG * NT * 8 * GI * 4;
+    const size_t region = std::max(align_up(xb, 16), align_up(hb, 16) + align_up(hsb, 16));
+    const size_t redb = CG * kConsumerWarps * 2 * 16 * NT * 8 * 4;
+    const size_t fixed = region + align_up(sumb, 16) + redb + 1024;
     const size_t budget = smem_budget - sizeof(SSmem) - 256;
     if (budget <= fixed) return false;
     size_t R = (budget - fixed) / g.slot;
@@ -913,12 +1054,11 @@ bool stream_geometry(int T, int H, int I, size_t smem_budget, StreamGeom *out)
     if (R < 2) return false;
     g.R = (int)R;
     size_t o = R * g.slot;
-    g.x_off = (uint32_t)o;
-    o += align_up(xb, 16);
+    g.x_off = g.h_off = (uint32_t)o;
+    g.hs_off = (uint32_t)(o + align_up(hb, 16));
+    o += region;
     g.sumx_off = (uint32_t)o;
     o += align_up(sumb, 16);
-    g.h_off = (uint32_t)o;
-    o += align_up(hb, 16);
     g.red_off = (uint32_t)o;
     o += redb;
     g.dyn = (uint32_t)(o + 1024);      // slack for aligning the base to 1024 bytes
@@ -991,7 +1131,10 @@ cudaError_t launch_decode_stream(const FusedDecodeArgs &a, cudaStream_t st)
         maps.sd = maps.d;
     }
     if (!ok) return cudaErrorInvalidValue;
-    auto kern = a.T > 8 ? decode_stream_kernel<2, 1> : (want == 2 ? decode_stream_kernel<1, 2> : decode_stream_kernel<1, 1>);
+    auto kern = a.T > 8                      ? decode_stream_kernel<2, 1, 2>
+                : consumer_groups(a.T) == 2  ? decode_stream_kernel<1, 1, 2>
+                : want == 2                  ? decode_stream_kernel<1, 2, 1>
+                                             : decode_stream_kernel<1, 1, 1>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.dyn)) != cudaSuccess)
         return e;
     int per_sm = 0;
