@@ -72,6 +72,9 @@ constexpr long long kDrainLimit = 1ll << 22;
 
 struct StreamMaps {
     CUtensorMap g, u, d, sg, su, sd;     // int4 codes of gate, up, down (routed stacks, then the shared expert)
+    // 1: 3D maps (128-byte chunk, row, chunk index), so that one copy brings every 128-byte box of a
+    // unit's rows; 0: 2D maps, one copy per box
+    int whole;
 };
 
 // Shared-memory geometry (bytes), fixed per (T, H, I) on the host.
@@ -443,6 +446,7 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
     const uint16_t *sdsc = a.s_down.scales, *sdbi = a.s_down.biases;
     const CUtensorMap *mg_r = &maps.g, *mu_r = &maps.u, *md_r = &maps.d;
     const CUtensorMap *mg_s = &maps.sg, *mu_s = &maps.su, *md_s = &maps.sd;
+    const bool whole = maps.whole != 0;
     prefetch_map(mg_r);
     prefetch_map(mu_r);
     prefetch_map(md_r);
@@ -470,10 +474,15 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
             const size_t so = (size_t)row0 * G;
             const CUtensorMap *mg = shr ? mg_s : mg_r, *mu = shr ? mu_s : mu_r;
             mbar_arrive_expect_tx(fb, bytes1);
+            if (whole) {
+                tma_load_3d(smem_u32(base), mg, 0, row0, 0, fb);
+                tma_load_3d(smem_u32(base + up_off), mu, 0, row0, 0, fb);
+            } else {
 #pragma unroll 1
-            for (int j = 0; j < nb1; ++j) {
-                tma_load_2d(smem_u32(base + j * kBox1), mg, j * 128, row0, fb);
-                tma_load_2d(smem_u32(base + up_off + j * kBox1), mu, j * 128, row0, fb);
+                for (int j = 0; j < nb1; ++j) {
+                    tma_load_2d(smem_u32(base + j * kBox1), mg, j * 128, row0, fb);
+                    tma_load_2d(smem_u32(base + up_off + j * kBox1), mu, j * 128, row0, fb);
+                }
             }
             bulk_load(smem_u32(base + sc1_off), (shr ? sgsc : gsc) + so, sb1, fb);
             bulk_load(smem_u32(base + sc1_off + sb1), (shr ? sgbi : gbi) + so, sb1, fb);
@@ -488,8 +497,12 @@ __device__ __noinline__ void producer(SSmem &S, const StreamMaps &maps, const Fu
             const size_t so = (size_t)row0 * GI;
             const CUtensorMap *md = shr ? md_s : md_r;
             mbar_arrive_expect_tx(fb, (uint32_t)nb2 * kBox2 + 2 * sb2);
+            if (whole) {
+                tma_load_3d(smem_u32(base), md, 0, row0, 0, fb);
+            } else {
 #pragma unroll 1
-            for (int j = 0; j < nb2; ++j) tma_load_2d(smem_u32(base + j * kBox2), md, j * 128, row0, fb);
+                for (int j = 0; j < nb2; ++j) tma_load_2d(smem_u32(base + j * kBox2), md, j * 128, row0, fb);
+            }
             bulk_load(smem_u32(base + sc2_off), (shr ? sdsc : dsc) + so, sb2, fb);
             bulk_load(smem_u32(base + sc2_off + kRows2 * GI * 2), (shr ? sdbi : dbi) + so, sb2, fb);
         }
@@ -613,23 +626,51 @@ __device__ __noinline__ void combine_block(SSmem &S, const FusedDecodeArgs &a, i
     const float *const yslot = a.yslot;       // arguments read once (see the producer)
     uint16_t *const y = a.y;
     float *const acc = a.acc;
-    const int nrow = min(kRows2, H - rb * kRows2);
+    const int nrow = min(kRows2, H - rb * kRows2), n4 = nrow / 4;   // H is a multiple of 64
+    // four consecutive rows per thread: 16-byte loads, every load in flight before the first add
 #pragma unroll 1
-    for (int q = gt; q < nrow * T; q += CT) {
-        const int tt = q / nrow, row = rb * kRows2 + (q - tt * nrow);
-        float ys[kMaxTopK + 1];                     // every load in flight before the first add
+    for (int q = gt; q < n4 * T; q += CT) {
+        const int tt = q / n4, row = rb * kRows2 + 4 * (q - tt * n4);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 ysh = has_shared ? __ldcg(reinterpret_cast<const float4 *>(yslot + ((size_t)T * k + tt) * H + row)) : z;
+        float4 sum = z;
+        // the picks in order j = 0, 1, ..., eight slots' loads in flight at a time
+#pragma unroll 1
+        for (int jb = 0; jb < k; jb += 8) {
+            float4 ys[8];
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) ys[j] = j < k ? __ldcg(yslot + ((size_t)tt * k + j) * H + row) : 0.f;
-        ys[kMaxTopK] = has_shared ? __ldcg(yslot + ((size_t)T * k + tt) * H + row) : 0.f;
-        float s = 0.f;
+            for (int j = 0; j < 8; ++j)
+                ys[j] = jb + j < k ? __ldcg(reinterpret_cast<const float4 *>(yslot + ((size_t)tt * k + jb + j) * H + row)) : z;
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (j < k) s = fmaf(S.p[tt][j], ys[j], s);
-        if (has_shared) s = fmaf(S.ws[tt], ys[kMaxTopK], s);
-        if (y)
-            y[(size_t)tt * H + row] = float_to_bf16_bits(s);
-        else
-            acc[(size_t)tt * H + row] += s;
+            for (int j = 0; j < 8; ++j)
+                if (jb + j < k) {
+                    const float pj = S.p[tt][jb + j];
+                    sum.x = fmaf(pj, ys[j].x, sum.x);
+                    sum.y = fmaf(pj, ys[j].y, sum.y);
+                    sum.z = fmaf(pj, ys[j].z, sum.z);
+                    sum.w = fmaf(pj, ys[j].w, sum.w);
+                }
+        }
+        if (has_shared) {
+            const float wsv = S.ws[tt];
+            sum.x = fmaf(wsv, ysh.x, sum.x);
+            sum.y = fmaf(wsv, ysh.y, sum.y);
+            sum.z = fmaf(wsv, ysh.z, sum.z);
+            sum.w = fmaf(wsv, ysh.w, sum.w);
+        }
+        if (y) {
+            const uint32_t lo = (uint32_t)float_to_bf16_bits(sum.x) | ((uint32_t)float_to_bf16_bits(sum.y) << 16);
+            const uint32_t hi = (uint32_t)float_to_bf16_bits(sum.z) | ((uint32_t)float_to_bf16_bits(sum.w) << 16);
+            *reinterpret_cast<uint2 *>(y + (size_t)tt * H + row) = make_uint2(lo, hi);
+        } else {
+            float4 *ap = reinterpret_cast<float4 *>(acc + (size_t)tt * H + row);
+            float4 av = *ap;
+            av.x += sum.x;
+            av.y += sum.y;
+            av.z += sum.z;
+            av.w += sum.w;
+            *ap = av;
+        }
     }
     group_bar<CT>(gid);
 }
@@ -1091,6 +1132,17 @@ bool plan_launch(int T, int H, int I, int dev, StreamGeom *geo, int *per_sm)
     return stream_geometry(T, H, I, (size_t)optin_smem(dev), geo);
 }
 
+// One copy per unit: the codes seen as (128-byte chunk, row, chunk index) with the chunk index
+// outermost, so that the box lands in shared memory as the 2D boxes of the chunks one after the
+// other (the 128-byte swizzle still keyed on the row).
+bool code_map_whole(CUtensorMap *m, const uint8_t *codes, int row_bytes, uint64_t rows, int box_rows)
+{
+    const uint64_t dims[3] = {128u, rows, (uint64_t)row_bytes / 128u};
+    const uint64_t strides[2] = {(uint64_t)row_bytes, 128u};
+    const uint32_t box[3] = {128u, (uint32_t)box_rows, (uint32_t)row_bytes / 128u};
+    return make_map_3d(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool code_map(CUtensorMap *m, const uint8_t *codes, int row_bytes, uint64_t rows, int box_rows)
 {
     return make_map_2d(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)row_bytes, rows, 128u, (uint32_t)box_rows,
@@ -1118,17 +1170,21 @@ cudaError_t launch_decode_stream(const FusedDecodeArgs &a, cudaStream_t st)
     if (!plan_launch(a.T, a.H, a.I, dev, &geo, &want)) return cudaErrorInvalidValue;
     StreamMaps maps;
     const uint64_t E = (uint64_t)a.E;
-    bool ok = code_map(&maps.g, a.gate.codes, a.H / 2, E * a.I, kRows1) &&
-              code_map(&maps.u, a.up.codes, a.H / 2, E * a.I, kRows1) &&
-              code_map(&maps.d, a.down.codes, a.I / 2, E * a.H, kRows2);
-    if (ok && a.has_shared)
-        ok = code_map(&maps.sg, a.s_gate.codes, a.H / 2, a.I, kRows1) &&
-             code_map(&maps.su, a.s_up.codes, a.H / 2, a.I, kRows1) &&
-             code_map(&maps.sd, a.s_down.codes, a.I / 2, a.H, kRows2);
-    else if (ok) {
-        maps.sg = maps.g;
-        maps.su = maps.u;
-        maps.sd = maps.d;
+    // whole-unit 3D maps where the driver takes them, else one 2D map box per 128-byte chunk
+    bool ok = false;
+    for (int whole = 1; whole >= 0 && !ok; --whole) {
+        auto mk = whole ? code_map_whole : code_map;
+        maps.whole = whole;
+        ok = mk(&maps.g, a.gate.codes, a.H / 2, E * a.I, kRows1) && mk(&maps.u, a.up.codes, a.H / 2, E * a.I, kRows1) &&
+             mk(&maps.d, a.down.codes, a.I / 2, E * a.H, kRows2);
+        if (ok && a.has_shared)
+            ok = mk(&maps.sg, a.s_gate.codes, a.H / 2, a.I, kRows1) && mk(&maps.su, a.s_up.codes, a.H / 2, a.I, kRows1) &&
+                 mk(&maps.sd, a.s_down.codes, a.I / 2, a.H, kRows2);
+        else if (ok) {
+            maps.sg = maps.g;
+            maps.su = maps.u;
+            maps.sd = maps.d;
+        }
     }
     if (!ok) return cudaErrorInvalidValue;
     auto kern = a.T > 8                      ? decode_stream_kernel<2, 1, 2>

@@ -38,4 +38,18 @@ inline bool make_map_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3D map with explicit byte strides for dimensions 1 and 2 (inner dimension contiguous).
+inline bool make_map_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, const uint64_t dims[3],
+                        const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle swz)
+{
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    cuuint64_t st[2] = {strides[0], strides[1]};
+    cuuint32_t b[3] = {box[0], box[1], box[2]};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace qmoe
