@@ -8,14 +8,15 @@
 //   - the work is a list of units: gate/up units (expert, 16 rows of I, both
 //     matrices, all of H) followed by down units (expert, 128 rows of H, all
 //     of I); CTA c takes units c, c + grid, c + 2 grid, ...;
-//   - a producer thread streams each unit's int4 codes with 2D TMA (128-byte
-//     swizzled boxes, so the MMA fragment reads below hit no bank twice) and
-//     its scales and biases with bulk copies into a ring of shared-memory
-//     slots, as far ahead as the ring allows; down units are loaded before
-//     their inputs exist;
-//   - eight consumer warps compute each unit from shared memory, write its
-//     result to global memory, release the slot and publish the unit in
-//     shared memory;
+//   - a producer thread streams each unit's int4 codes with TMA (one 3D copy per
+//     matrix: the 128-byte chunks of the unit's rows, 128-byte swizzled, so the
+//     MMA fragment reads below hit no bank twice) and its scales and biases
+//     with bulk copies into a ring of shared-memory slots, as far ahead as the
+//     ring allows; down units are loaded before their inputs exist;
+//   - the eight consumer warps, as one group (T <= 2) or as two groups of four
+//     taking alternate units (T > 2), compute each unit from shared memory,
+//     write its result to global memory, release the slot and publish the unit
+//     in shared memory;
 //   - a signal thread makes the published units visible GPU-wide (one fence
 //     per batch) and counts them: gate/up units per expert, down units per
 //     128-row block; the last down unit of a row block queues that block's
@@ -26,26 +27,28 @@
 // Phase 0 (every CTA): stage x (in the codes' k order) and its per-group sums
 // in shared memory, redo the top-k from the fp32 logits (same comparisons as
 // the top-k kernel), list the distinct experts (increasing id, shared expert
-// last) and their columns.
-// Gate/up unit: split-K over the eight warps, fixed-order reduction, h =
-// silu(g) * u stored as fp16 in the codes' k order.  Down unit: one thread
-// waits (bounded, with backoff) for the expert's gate/up units, the expert's
-// h columns are staged in shared memory, the raw expert output is written per
-// slot.  Combine: y = bf16(sum_j p_j y_slot[t k + j] + w_s y_slot[T k + t]) in
-// slot order, one rounding.
+// last), their columns and the columns' tokens.
+// Gate/up unit: split-K in a fixed partition (eight partials over the 128-byte
+// code boxes, added in one order), h = silu(g) * u stored as fp16 in the codes'
+// k order.  Down unit: one thread waits (bounded, with backoff) for the
+// expert's gate/up units, the expert's h columns are staged in shared memory
+// (in the place of x, which no unit needs any more) with their group sums, the
+// raw expert output is written per slot.  Combine: y = bf16(sum_j p_j
+// y_slot[t k + j] + w_s y_slot[T k + t]) in slot order, one rounding.
 //
 // Arithmetic (the GEMV of the decode path): over one group of 64 inputs
 //     sum_j w_j x_j = s (sum_j (OFF + q_j) x_j) + (b - OFF s) sum_j x_j,
 // OFF + q exact in the MMA operand type (bf16 128 + q for x, fp16 1024 + q for
 // h), products on mma.sync m16n8k16 with fp32 accumulation, per-group scale and
-// bias in fp32.  Every output element is one MMA column: a token's result does
-// not depend on the other tokens of the batch.
+// bias in fp32.  Every output element is one MMA column and every sum has one
+// order: a token's result does not depend on the other tokens of the batch.
 //
 // Code size matters here as much as arithmetic: at T = 1 every SM runs each
 // code path two or three times, so instruction fetch is part of the critical
-// path.  The hot loops are therefore not unrolled across groups, and the rarely
-// run parts (routing, lists, producer, signals, combine) are separate
-// functions.  Counters are zeroed by the kernel that precedes this launch.
+// path.  The hot loops are unrolled over one 128-byte box (four groups) only,
+// and the rarely run parts (routing, lists, producer, signals, combine) are
+// separate functions.  Counters are zeroed by the kernel that precedes this
+// launch.
 #include <algorithm>
 
 #include "kernels.cuh"
