@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--profile", action="store_true",
                     help="warm-up and timed steps only (for a profiler's launch list): no clocks, stage, e2e, "
                          "CPU baseline or sweep")
+    ap.add_argument("--timeline", action="store_true",
+                    help="decode workloads: print the per-phase timeline of single launches (fused decode kernel "
+                         "stamps) as one JSON line and exit")
     return ap.parse_args()
 
 
@@ -212,11 +215,13 @@ class Workload:
             self.bias = torch.from_numpy(synth.zipf_bias(wl.shape, wl.zipf_s, wl.seed)).cuda()
         self.ws = [qm.workspace(base.cfg, T) for _ in range(copies)]
         self.y = [torch.empty((T, wl.shape.hidden), dtype=torch.int16, device="cuda") for _ in range(copies)]
-        self.ids = [torch.empty((T, wl.shape.top_k), dtype=torch.int32, device="cuda") for _ in range(copies)]
+        self.ids = [torch.full((T, wl.shape.top_k), -1, dtype=torch.int32, device="cuda") for _ in range(copies)]
         self.copies = copies
+        self.executed = set()        # copies whose step has run (their ids are real)
 
     def step(self, i, stream):
         c = i % self.copies
+        self.executed.add(c)
         L = self.layers[c]
         self.qm.moe_forward(L.cfg, L.w, self.x[c], self.wl.tokens, self.bias, None, self.y[c], self.ids[c],
                             None, None, self.qm.MOE_PATH_AUTO, self.ws[c], stream)
@@ -225,13 +230,16 @@ class Workload:
         return self.qm.MOE_PATH_DECODE if self.wl.tokens <= 16 else self.qm.MOE_PATH_PREFILL
 
     def kernels_per_step(self):
-        return 6
+        # decode: the one fused kernel; prefill: router GEMV (gamma), router MMA, top-k, permute,
+        # x conversion, accumulator zeroing, two small-tile and two tensor-memory GEMMs, combine
+        return 1 if self.wl.tokens <= 16 else 11
 
     def distinct_experts(self):
-        """Distinct routed experts of each copy's step (plus the shared expert)."""
+        """Distinct routed experts (plus the shared expert) of each copy whose step was executed."""
         out = []
-        for c in range(self.copies):
+        for c in sorted(self.executed):
             ids = self.ids[c].cpu().numpy()
+            assert ids.min() >= 0, "a copy marked executed has no routing"
             out.append(len(np.unique(ids)) + self.wl.shape.has_shared)
         return out
 
@@ -321,8 +329,11 @@ def run_ours(args, wl, rank, world, pg, steps, warmup, want_extras):
     res["kernels"] = steps * W.kernels_per_step()
     res["clocks"] = clocks.stop() if clocks else None
     if want_extras and not args.profile:
-        res["stage"] = stage_timing(W, stream, steps, expert_bytes, flops)
         res["e2e"] = e2e_timing(W, stream, steps, warmup)
+        if wl.tokens <= 16:
+            res["cold"] = cold_call_latency(W, stream)
+    if not args.profile:
+        res["stage"] = stage_timing(W, stream, steps, expert_bytes, flops)
     del g_warm, g_timed
     return res
 
@@ -372,6 +383,56 @@ def stage_timing(W, stream, steps, expert_bytes, flops):
     return dict(ms=ms, expert_bytes=expert_bytes, flops=flops, launches=n)
 
 
+def cold_call_latency(W, stream, reps=20):
+    """One moe_forward after an L2-flushing write (a buffer larger than L2), device time per call."""
+    import torch
+    qm = W.qm
+    wl = W.wl
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    times = []
+    for i in range(reps):
+        c = i % W.copies
+        L = W.layers[c]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.fill_(i & 0xFF)
+            e0.record(stream)
+            qm.moe_forward(L.cfg, L.w, W.x[c], wl.tokens, W.bias, None, W.y[c], None, None, None,
+                           qm.MOE_PATH_AUTO, W.ws[c], stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    del flush
+    return dict(ms_median=float(np.median(times)), ms_min=float(np.min(times)), calls=reps,
+                flush="512 MiB write before each call")
+
+
+def timeline(W, stream, reps=20):
+    """Per-phase times of single fused decode launches from the kernel's %globaltimer stamps (us from
+    the earliest CTA start): median over launches of the median and the last CTA of each stamp."""
+    import torch
+    qm = W.qm
+    wl = W.wl
+    names = ["start", "x_staged", "router_published", "router_counter", "topk_done", "list_done", "routing_done",
+             "first_gate_chunk", "first_down_chunk", "units_done", "units_counter", "combine_done"]
+    per = []
+    for i in range(reps):
+        c = i % W.copies
+        L = W.layers[c]
+        with torch.cuda.stream(stream):
+            qm.moe_forward(L.cfg, L.w, W.x[c], wl.tokens, W.bias, None, W.y[c], None, None, None,
+                           qm.MOE_PATH_AUTO, W.ws[c], stream)
+        st = qm.moe_decode_timeline(L.cfg, wl.tokens, W.ws[c], stream).astype(np.int64)
+        t0 = st[:, 0].min()
+        rel = (st - t0) / 1e3
+        per.append((np.median(rel, axis=0), rel.max(axis=0)))
+    med = np.median(np.stack([p[0] for p in per]), axis=0)
+    last = np.median(np.stack([p[1] for p in per]), axis=0)
+    return {"workload": wl.name, "launches": reps, "ctas": int(st.shape[0]),
+            "median_cta_us": dict(zip(names, [round(float(v), 3) for v in med])),
+            "last_cta_us": dict(zip(names, [round(float(v), 3) for v in last]))}
+
+
 def e2e_timing(W, stream, steps, warmup):
     """Same metric through the public API per step: pinned-host x -> device, forward, y -> pinned host."""
     import torch
@@ -407,6 +468,36 @@ def e2e_timing(W, stream, steps, warmup):
 
 
 # ----------------------------------------------------------------- oracle (CPU) legs
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def oracle_single_core(wl, seconds=5.0):
+    """The same oracle sample on one core: a fresh process with OMP_NUM_THREADS=1."""
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; from quantised_moe_expert_gb300 import synth; "
+            "r, n, dt = bench.oracle_sample(synth.WORKLOADS[%d], seconds=%r); print(json.dumps(r))"
+            % (ROOT, synth.WORKLOADS.index(wl), seconds))
+    env = dict(os.environ, OMP_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120, env=env)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as e:
+        return {"error": str(e)[:200]}
+
 
 def oracle_sample(wl, seconds=12.0, max_tokens=None):
     """FP64 oracle throughput on this host's cores over a bounded sample of the workload's tokens."""
@@ -456,6 +547,31 @@ def run_reference(args, wl, rank, world, steps, warmup):
     print(json.dumps(line), flush=True)
 
 
+def stage_roofline(wl, st, hbm, tc, peak_src):
+    """Roofline of the expert-FFN stage from its CUDA-event time: HBM below the ridge point, else tensor."""
+    decode = wl.tokens <= 16
+    if decode:
+        ach = st["expert_bytes"] / (st["ms"] / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": traffic_for("decode_expert_ffn", wl.name),
+                "kernel": "expert-FFN stage (fused decode kernel: units + combine)",
+                "kernel_us": st["ms"] * 1e3, "algorithmic_bytes_per_launch": st["expert_bytes"],
+                "peak_source": peak_src}
+    if st["flops"] / max(st["expert_bytes"], 1.0) < tc * 1e12 / (hbm * 1e9):
+        # below the ridge point (e.g. T = 512: ~16 tokens per expert) the weights bound the stage
+        ach = st["expert_bytes"] / (st["ms"] / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": traffic_for("prefill_expert_ffn", wl.name),
+                "kernel": "expert-FFN stage (grouped GEMMs)", "kernel_us": st["ms"] * 1e3,
+                "algorithmic_bytes_per_launch": st["expert_bytes"],
+                "tensor_frac": st["flops"] / (st["ms"] / 1e3) / 1e12 / tc, "peak_source": peak_src}
+    ach = st["flops"] / (st["ms"] / 1e3) / 1e12
+    return {"bound": "tensor", "achieved": ach, "peak": tc, "unit": "TFLOP/s", "frac": ach / tc,
+            "traffic": traffic_for("prefill_expert_ffn", wl.name),
+            "kernel": "expert-FFN stage (grouped GEMMs)", "kernel_us": st["ms"] * 1e3,
+            "algorithmic_flops_per_launch": st["flops"], "peak_source": peak_src}
+
+
 def traffic_for(kernel_key, workload):
     """DRAM bytes per launch from a committed ncu summary, if no source of the stage has changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -485,32 +601,23 @@ def main():
     import torch
     rank, world, local, pg = dist_setup(args.gpus)
     hbm, tc, tc_sus, peak_src = peaks()
+    if args.timeline:
+        import quantised_moe_expert_gb300 as qm
+        qm.load()
+        W = Workload(wl, args.copies or 4)
+        stream = torch.cuda.Stream()
+        for i in range(3):
+            W.step(i, stream)
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps(timeline(W, stream)), flush=True)
+        return
     r = run_ours(args, wl, rank, world, pg, steps, warmup, want_extras=True)
     if args.profile:
         if rank == 0:
             print(json.dumps({"profile_run": wl.name, "ms_per_step": r["ms_per_step"], "steps": steps}), flush=True)
         return
-    st = r["stage"]
-    decode = wl.tokens <= 16
-    if decode:
-        ach = st["expert_bytes"] / (st["ms"] / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "traffic": traffic_for("decode_expert_ffn", wl.name),
-                "kernel": "expert-FFN stage (decode gate/up + down GEMV + slot combine)",
-                "algorithmic_bytes_per_launch": st["expert_bytes"], "peak_source": peak_src}
-    elif st["flops"] / max(st["expert_bytes"], 1.0) < tc * 1e12 / (hbm * 1e9):
-        # below the ridge point (e.g. T = 512: ~16 tokens per expert) the weights bound the stage
-        ach = st["expert_bytes"] / (st["ms"] / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "traffic": traffic_for("prefill_expert_ffn", wl.name),
-                "kernel": "expert-FFN stage (grouped GEMMs)", "algorithmic_bytes_per_launch": st["expert_bytes"],
-                "tensor_frac": st["flops"] / (st["ms"] / 1e3) / 1e12 / tc, "peak_source": peak_src}
-    else:
-        ach = st["flops"] / (st["ms"] / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": tc, "unit": "TFLOP/s", "frac": ach / tc,
-                "traffic": traffic_for("prefill_expert_ffn", wl.name),
-                "kernel": "expert-FFN stage (grouped GEMMs)", "algorithmic_flops_per_launch": st["flops"],
-                "peak_source": peak_src}
+    roof = stage_roofline(wl, r["stage"], hbm, tc, peak_src)
     line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": steps,
             "warmup": warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int4-affine/bf16 in, fp32 accumulate", "data": "synthetic",
@@ -526,8 +633,15 @@ def main():
             "layer_tensor": {"flops_per_step": r["flops_step"],
                              "frac_of_peak": r["flops_step"] / (r["ms_per_step"] / 1e3) / 1e12 / tc},
             "e2e": r["e2e"], "gpu_launches": r["kernels"], "clocks": r["clocks"]}
+    if "cold" in r:
+        line["cold_single_call"] = r["cold"]
     if rank == 0 and not args.no_cpu_baseline:
         cb, _, _ = oracle_sample(wl)
+        one = oracle_single_core(wl)
+        cb["cpu_model"] = cpu_model()
+        cb["host_cores"] = os.cpu_count()
+        cb["single_core"] = {"value": one.get("value"), "unit": "tokens/s", "cores": 1,
+                             "sample": one.get("sample", one.get("error"))}
         line["cpu_baseline"] = cb
     if not args.no_sweep and rank == 0:
         sweep = {}
@@ -538,7 +652,9 @@ def main():
                 rr = run_ours(args, other, 0, 1, None, default_steps(other) // 2, 3, want_extras=False)
                 sweep[other.name] = {"value": rr["value"], "ms_per_step": rr["ms_per_step"],
                                      "hbm_frac": rr["bytes_step"] / (rr["ms_per_step"] / 1e3) / 1e9 / hbm,
-                                     "tc_frac": rr["flops_step"] / (rr["ms_per_step"] / 1e3) / 1e12 / tc}
+                                     "tc_frac": rr["flops_step"] / (rr["ms_per_step"] / 1e3) / 1e12 / tc,
+                                     "distinct_experts_mean": float(np.mean(rr["distinct"])),
+                                     "stage_roofline": stage_roofline(other, rr["stage"], hbm, tc, peak_src)}
             except Exception as e:  # a path not built yet reports why
                 sweep[other.name] = {"error": str(e)[:200]}
         line["sweep"] = sweep

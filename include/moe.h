@@ -32,12 +32,22 @@
  *     All work is enqueued asynchronously on it, in order.
  *   - `ws`/`ws_bytes` is caller-owned device scratch of at least
  *     moe_workspace_size() bytes for the call's T; it must not be shared by
- *     calls that may run concurrently.  Its contents between calls are
- *     meaningless, except that moe_get_device_status reads the status word
- *     that kernels running on it set.
+ *     calls that may run concurrently.  Its first 512 bytes (the header: the
+ *     status word and the grid-wide counters of the fused decode kernel) must
+ *     be zero before the workspace's first use: allocate it zero-filled, or
+ *     call moe_get_device_status on it once.  The kernels leave the counters
+ *     zero when they end; the rest of the workspace carries nothing between
+ *     calls.  A header that was not zero-filled is detected as far as the
+ *     kernels can (MOE_ERR_WORKSPACE in the status word).
  *   - Device-side failures (a bounded wait that ran out, an index out of
- *     range) never trap: the kernel writes a nonzero code into the workspace
- *     status word and returns; the host reads it with moe_get_device_status.
+ *     range, a header that was not zero-filled) never trap: the kernel writes
+ *     a nonzero code into the workspace status word and returns.  The word
+ *     keeps the first such code until moe_get_device_status reads it.
+ *   - Values: x and the weights are finite.  Each token's x is scaled by a
+ *     power of two before the 16-bit intermediate steps and the scale is
+ *     undone after them (exact), so rows far above the fp16 range or entirely
+ *     below its normal range keep their precision; only an output beyond the
+ *     bf16 range overflows.
  *
  * Storage formats (MLX layout, [out, in] with quantisation along `in`)
  *   codes   4-bit: uint8 [rows, in/2], element j of a row in byte j/2, low
@@ -68,7 +78,8 @@ enum moe_status {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative or oversized size */
     MOE_ERR_UNSUPPORTED = 2,  /* a format or shape the kernels do not implement */
-    MOE_ERR_WORKSPACE = 3,    /* ws_bytes below moe_workspace_size() */
+    MOE_ERR_WORKSPACE = 3,    /* ws_bytes below moe_workspace_size(); as a device status: a
+                                 workspace header that was not zero-filled */
     MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute query) */
     MOE_ERR_TIMEOUT = 5,      /* device status: a bounded wait inside a kernel ran out */
     MOE_ERR_DEVICE = 6        /* device status: a kernel found an index out of range */
@@ -80,10 +91,15 @@ enum moe_path {
     MOE_PATH_PREFILL = 2   /* tcgen05 grouped GEMM kernels (any T >= 1) */
 };
 
-/* Layer shape.  Supported: group == 64, bits == 4, router_bits == 8,
- * hidden and inter multiples of 64 (hidden <= 8192, inter <= 4096),
- * 1 <= top_k <= min(n_experts, 16), 1 <= n_experts <= 256, has_shared in {0,1}.
- * Anything else returns MOE_ERR_UNSUPPORTED. */
+/* Layer shape and per-call options.  Supported: group == 64, bits == 4,
+ * router_bits == 8, hidden and inter multiples of 64 (hidden <= 8192,
+ * inter <= 4096), 1 <= top_k <= min(n_experts, 16), 1 <= n_experts <= 256,
+ * has_shared in {0,1}.  Anything else returns MOE_ERR_UNSUPPORTED.
+ * wait_polls bounds every wait inside the kernels of the call: a wait polls
+ * at most that many times (the first poll does not block, later ones sleep
+ * briefly), then records MOE_ERR_TIMEOUT and the kernel returns early.
+ * 0 (or less) selects the default, 1 << 20 polls (about a second).  A limit
+ * of 1 makes any wait that is not already satisfied run out (fault tests). */
 typedef struct moe_config {
     int hidden;       /* H */
     int inter;        /* I, intermediate size of every expert, shared included */
@@ -93,6 +109,7 @@ typedef struct moe_config {
     int bits;         /* expert code width */
     int router_bits;  /* router code width */
     int has_shared;   /* 1: the layer has a shared expert slot */
+    int wait_polls;   /* bound on every in-kernel wait of the call; 0 = default */
 } moe_config;
 
 /* One affine-quantised matrix (or a stack of them), device pointers. */
@@ -190,10 +207,11 @@ MOE_API int moe_forward(const moe_config *cfg, const moe_weights *w, const uint1
  * runs inside another engine's enqueue callback (that engine owns all device
  * memory) or a process that must not allocate after start-up.
  * Same arguments and results as moe_forward with MOE_PATH_DECODE, but no
- * workspace: the scratch is a fixed 4 MiB array in the library's own device
- * memory, held on every GPU that loads the library until the process exits.
- * Layers whose decode scratch exceeds 4 MiB are refused with
- * MOE_ERR_WORKSPACE; T outside 0..16 with MOE_ERR_INVALID_ARG.
+ * workspace: the scratch is a fixed 24 MiB array in the library's own device
+ * memory, held on every GPU that loads the library until the process exits
+ * (zero at load; the kernels leave its counters zero).  Layers whose decode
+ * scratch exceeds 24 MiB are refused with MOE_ERR_WORKSPACE; T outside 0..16
+ * with MOE_ERR_INVALID_ARG.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array, which keeps the last call's
@@ -204,19 +222,40 @@ MOE_API int moe_forward_decode_static(const moe_config *cfg, const moe_weights *
                                       const float *router_bias, const float *logits_in, uint16_t *y,
                                       int32_t *ids_out, uint16_t *p_out, uint16_t *w_shared_out, void *stream);
 
-/* Synchronises `stream`, then reads and clears the device status word of `ws`.
- * *device_status receives MOE_OK or the first error code a kernel recorded. */
+/* Synchronises `stream`, then reads the device status word of `ws` and zeroes
+ * the workspace header (status word and counters).  *device_status receives
+ * MOE_OK or the first error code a kernel recorded since the last read. */
 MOE_API int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_status);
 
-/* Upper bound on the polls of every bounded wait inside the kernels (mbarrier
- * waits of the tensor-core pipeline, readiness counters of the fused decode
- * kernel).  The first poll does not block; later polls suspend for up to about
- * a microsecond.  A wait that reaches the bound records MOE_ERR_TIMEOUT and
- * the kernel returns early.  Default 1 << 20 polls (about a second); values
- * <= 0 restore the default.  Affects launches enqueued after the call; meant
- * for fault-handling tests (a limit of 1 makes any wait that is not already
- * satisfied run out). */
-MOE_API int moe_set_wait_limit(long long polls);
+/* The intermediate stages of the expert FFNs, for checking each projection on
+ * its own (the FP64 check of every projection class in the section "Gate" of
+ * the proposal page): for every slot f (routed: f = t k + j, shared:
+ * f = T k + t)
+ *   h_out     fp32 [T (k + 1), I]  h = silu(W_gate x) * (W_up x) exactly as the
+ *             down projection consumes it (after the kernels' own rounding), or NULL;
+ *   yslot_out fp32 [T (k + 1), H]  the slot's expert output W_down h before the
+ *             pick weight, or NULL.
+ * ids/counts/offsets/perm as for moe_expert_ffn (counts/offsets/perm are read
+ * on the prefill path only).  The same kernels as moe_expert_ffn compute the
+ * stages; nothing is added into an accumulator.  Rows of h_out / yslot_out of
+ * slots that do not exist (the shared rows without a shared expert) are not
+ * written.  Returns MOE_ERR_UNSUPPORTED for a path whose kernels cannot emit
+ * their stages. */
+MOE_API int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T,
+                              const int32_t *ids, const int32_t *counts, const int32_t *offsets,
+                              const int32_t *perm, float *h_out, float *yslot_out, int path,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* Timeline of the last fused decode launch on `ws` (T <= 16, decode path):
+ * synchronises `stream`, then copies per CTA twelve %globaltimer stamps (ns)
+ * to host_stamps [max_ctas, 12]: kernel start, x staged, router logits
+ * published, router counter reached, top-k done, expert list done, routing
+ * done, first gate chunk landed, first down chunk landed, expert units done,
+ * unit counter reached, combine done (a stamp that was not reached keeps an
+ * older value).
+ * *n_ctas receives the number of CTAs of the launch. */
+MOE_API int moe_decode_timeline(const moe_config *cfg, int T, void *ws, size_t ws_bytes, void *stream,
+                                unsigned long long *host_stamps, int max_ctas, int *n_ctas);
 
 #ifdef __cplusplus
 }

@@ -31,8 +31,8 @@ MOE_PATH_DECODE = 1
 MOE_PATH_PREFILL = 2
 
 EXPORTED = ("moe_status_string", "moe_check_config", "moe_workspace_size", "moe_route", "moe_permute",
-            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status", "moe_set_wait_limit",
-            "moe_forward_decode_static")
+            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status", "moe_expert_stages",
+            "moe_decode_timeline", "moe_forward_decode_static")
 
 
 class MoeError(RuntimeError):
@@ -43,7 +43,8 @@ class MoeError(RuntimeError):
 
 class moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
-                ("hidden", "inter", "n_experts", "top_k", "group", "bits", "router_bits", "has_shared")]
+                ("hidden", "inter", "n_experts", "top_k", "group", "bits", "router_bits", "has_shared",
+                 "wait_polls")]
 
 
 class moe_qmat(ctypes.Structure):
@@ -91,7 +92,9 @@ def load(build: bool = True):
         lib.moe_forward.argtypes = [P(moe_config), P(moe_weights), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP,
                                     _SZ, _VP]
         lib.moe_get_device_status.argtypes = [_VP, _SZ, _VP, P(ctypes.c_int)]
-        lib.moe_set_wait_limit.argtypes = [ctypes.c_longlong]
+        lib.moe_expert_stages.argtypes = [P(moe_config), P(moe_weights), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _I,
+                                          _VP, _SZ, _VP]
+        lib.moe_decode_timeline.argtypes = [P(moe_config), _I, _VP, _SZ, _VP, _VP, _I, P(ctypes.c_int)]
         lib.moe_forward_decode_static.argtypes = [P(moe_config), P(moe_weights), _VP, _I, _VP, _VP, _VP, _VP, _VP,
                                                   _VP, _VP]
         for name in EXPORTED:
@@ -124,10 +127,10 @@ def _check(fn: str, rc: int):
         raise MoeError(fn, rc)
 
 
-def config_of(shape) -> moe_config:
+def config_of(shape, wait_polls: int = 0) -> moe_config:
     """moe_config from any object with the layer-shape attributes (e.g. synth.LayerShape)."""
     return moe_config(shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.group, shape.bits,
-                      shape.router_bits, shape.has_shared)
+                      shape.router_bits, shape.has_shared, wait_polls)
 
 
 class DeviceLayer:
@@ -235,20 +238,34 @@ def moe_get_device_status(ws, stream=None) -> int:
     return st.value
 
 
-def moe_set_wait_limit(polls: int):
-    _check("moe_set_wait_limit", load().moe_set_wait_limit(int(polls)))
+def moe_expert_stages(cfg, w, x, T, ids, counts, offsets, perm, h_out, yslot_out, path, ws, stream=None):
+    rc = load().moe_expert_stages(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), T, _ptr(ids), _ptr(counts),
+                                  _ptr(offsets), _ptr(perm), _ptr(h_out), _ptr(yslot_out), path, _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream))
+    _check("moe_expert_stages", rc)
+
+
+def moe_decode_timeline(cfg, T, ws, stream=None, max_ctas: int = 256) -> np.ndarray:
+    """Per-CTA %globaltimer stamps (ns) of the last fused decode launch on ws: [n_ctas, 12] uint64."""
+    buf = np.zeros((max_ctas, 12), dtype=np.uint64)
+    n = ctypes.c_int(0)
+    rc = load().moe_decode_timeline(ctypes.byref(cfg), T, _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream), ctypes.c_void_p(buf.ctypes.data), max_ctas, ctypes.byref(n))
+    _check("moe_decode_timeline", rc)
+    return buf[:min(n.value, max_ctas)]
 
 
 # ---------------------------------------------------------------- conveniences
 
 def workspace(cfg: moe_config, T: int, device="cuda") -> torch.Tensor:
-    """A device workspace tensor of moe_workspace_size bytes (uint8, 256-byte aligned by the allocator)."""
-    return torch.empty(moe_workspace_size(cfg, T), dtype=torch.uint8, device=device)
+    """A zero-filled device workspace of moe_workspace_size bytes (uint8, 256-byte aligned by the allocator)."""
+    return torch.zeros(moe_workspace_size(cfg, T), dtype=torch.uint8, device=device)
 
 
 def forward(layer: DeviceLayer, x: torch.Tensor, ws: torch.Tensor, router_bias=None, logits_in=None,
-            path: int = MOE_PATH_AUTO, stream=None, with_routing: bool = False):
-    """y (int16 view of bf16 bits) = layer(x); optionally also (ids, p, w_s)."""
+            path: int = MOE_PATH_AUTO, stream=None, with_routing: bool = False, cfg: Optional[moe_config] = None):
+    """y (int16 view of bf16 bits) = layer(x); optionally also (ids, p, w_s).  cfg overrides layer.cfg
+    (e.g. to set wait_polls for one call)."""
     T = x.shape[0]
     dev = x.device
     y = torch.empty((T, layer.shape.hidden), dtype=torch.int16, device=dev)
@@ -257,5 +274,6 @@ def forward(layer: DeviceLayer, x: torch.Tensor, ws: torch.Tensor, router_bias=N
         ids = torch.empty((T, layer.shape.top_k), dtype=torch.int32, device=dev)
         p = torch.empty((T, layer.shape.top_k), dtype=torch.int16, device=dev)
         w_s = torch.empty((max(T, 1),), dtype=torch.int16, device=dev)
-    moe_forward(layer.cfg, layer.w, x, T, router_bias, logits_in, y, ids, p, w_s, path, ws, stream)
+    moe_forward(cfg if cfg is not None else layer.cfg, layer.w, x, T, router_bias, logits_in, y, ids, p, w_s, path,
+                ws, stream)
     return (y, ids, p, w_s) if with_routing else y

@@ -1,0 +1,1236 @@
+// Fused decode layer for T <= 16: router, top-k, expert FFNs and combine in one cooperative launch.
+//
+// At decode sizes the layer's cost is the bytes of the selected experts (page "POC for
+// qwen3.5 / qwen3.6 support optimized for AGX Orin", Phases 1-4: the batch-1 "gemv MoE
+// path"; "both stacks are now weight-BW bound"): at one token ~16 MB, two or three
+// microseconds of HBM time on this part.  What stands between that and the layer time is
+// the chain of dependent steps (router -> top-k -> expert weights -> combine), so the
+// launch is arranged to cross the grid only twice:
+//
+//   1. Router (every CTA, one CTA per SM).  The CTA's router rows (experts c, c + grid,
+//      ...) are loaded into registers before the wait for the preceding kernel; then x
+//      is staged in shared memory, pre-scaled per token by a power of two (x' = x 2^-e,
+//      max |x'| in [1, 2): exact, and it keeps h inside the fp16 range, see below), and
+//      the CTA's logits go to global memory.  One grid-wide counter; then every CTA reads
+//      all logits and runs the same top-k (warp max / min reductions, ties to the lower
+//      id) and builds the same expert list.
+//   2. Units.  A unit is (expert, 32-row slice s of the intermediate dimension): the
+//      slice's gate and up rows (all of H) and the slice's 32 columns of the down matrix
+//      (all H rows).  Because the affine rule holds for any subset of a group,
+//          sum_{j in S} (s q_j + b) h_j = s sum_{j in S} q_j h_j + b sum_{j in S} h_j,
+//      the CTA that computes h for its slice also applies the down projection to it at
+//      once: no h crosses the grid.  A producer warp streams each unit's three chunks
+//      (gate, up, down codes with the gate/up scales and biases) into a ring of shared-
+//      memory slots with TMA; eight consumer warps compute them on mma.sync with exact
+//      integer codes (bf16 128 + q against x' for gate/up, signed fp16 q - 8 against h'
+//      for down), and write per slice the raw down sums P = sum (q - 8) h' and sum h'.
+//   3. One grid-wide counter; then CTA c combines rows [c RB, c RB + RB) of y: per slot,
+//      y_e = 2^(2e) sum_g [ s_g (P_{2g} + P_{2g+1}) + (b_g + 8 s_g)(Hs_{2g} + Hs_{2g+1}) ],
+//      then y = bf16(sum_j p_j y_ej + w_s y_shared) in slot order, one rounding.  The down
+//      scales are read here, once per expert and row, in whole rows.
+//
+// The pick weights (fp64, one rounding to bf16) and the shared weight of token t are
+// computed by CTA grid - 1 - t, off the critical path, and published before step 3.
+//
+// Range.  With x' = x 2^-e per token, g' = g 2^-e and u' = u 2^-e; the kernel forms
+// h' = g' u' sigmoid(g' 2^e) = h 2^-2e, which is bounded by |g'||u'| whatever the size of
+// x, stores it as fp16 and undoes the 2^-2e (exact) in step 3.  Rows of x far above the
+// fp16 range, or entirely below its normal range, therefore lose nothing.
+//
+// Determinism.  Every sum has one order that depends only on the token's own data and on
+// the fixed slice partition, so a token's outputs are the same bits in any batch of 1..16.
+//
+// Synchronisation state lives in the workspace header (three counters); the last CTA to
+// leave resets them, so a workspace needs to be zero-filled only before its first use.
+// Every wait is bounded (a status code is recorded instead of hanging).
+#include <mutex>
+
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+#include "tma_host.cuh"
+
+namespace qmoe {
+namespace {
+
+using namespace tc;
+
+constexpr int kCW = 8;                         // consumer warps
+constexpr int kWarpProd = 8;                   // TMA producer warp
+constexpr int kWarpAux = 9;                    // per-token weights and routing outputs
+constexpr int kThreads = 320;
+constexpr int kSlice = 32;                     // rows of the intermediate dimension per unit
+constexpr int kMaxSlots = 6;
+constexpr int kMaxCols = kDecodeMaxTok * (kMaxTopK + 1);
+constexpr int kMaxList = kMaxExperts + 1;
+constexpr long long kDrainLimit = 1ll << 22;
+// Staged x: each group of 64 inputs padded to 72 elements and each token row by 8 more, so that
+// neither lanes reading different groups (router) nor lanes reading different tokens (MMA B
+// fragments) meet in one shared-memory bank.
+constexpr int kXG = 72;
+
+// Timeline stamps (trace columns), in the order a CTA reaches them.
+enum {
+    kStStart = 0, kStXStaged, kStRouterPub, kStRouterCnt, kStTopk, kStListed, kStRouted, kStFirstGate,
+    kStFirstDown, kStUnitsDone, kStUnitsCnt, kStCombined
+};
+
+struct FusedMaps {
+    CUtensorMap g, u, sg, su;   // int4 codes of gate and up (routed stacks, shared expert): 3D, 32-row boxes
+};
+
+struct FusedGeom {
+    int R;              // ring slots
+    uint32_t slot;      // bytes per slot (multiple of 1024)
+    uint32_t codes1;    // code bytes of a gate/up chunk: 32 rows x H / 2
+    uint32_t sc1;       // bytes of its scales (and of its biases): 32 x H / 64 x 2
+    uint32_t codes2;    // bytes of a down chunk: H rows x 16
+    uint32_t x_off, xs_off, red_off, h_off, hs_off, dyn;
+    int RB;             // rows of y combined per CTA (multiple of 4)
+};
+
+struct FSmem {
+    int ids[kDecodeMaxTok][kMaxTopK];
+    float lg[kDecodeMaxTok][kMaxTopK];      // fp32 logit of each pick
+    float p[kDecodeMaxTok][kMaxTopK];
+    float ws[kDecodeMaxTok];
+    int xe[kDecodeMaxTok];                  // x' = x 2^-xe
+    int xmax[kDecodeMaxTok];                // largest |x| bits of each token (bf16 magnitude)
+    int fill[kMaxList];                     // columns handed out per list entry
+    int cnt[kMaxList];                      // picks of each expert
+    int lpos[kMaxList];                     // list position of each picked expert
+    int list[kMaxList];
+    int ncols[kMaxList];
+    int colptr[kMaxList + 1];
+    int colof[kDecodeMaxTok][kMaxTopK + 1]; // column of (t, j); j == k: the shared slot
+    int ctok[kMaxCols];                     // token of each column
+    int colf[kMaxCols];                     // slot index f of each column (t k + j, or T k + t)
+    int nlist;
+    int abort;
+    uint64_t full[kMaxSlots], empty[kMaxSlots];
+};
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    if constexpr (F16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// 8 nibbles -> four 16-bit pairs of (OFF + q) in the MMA operand type: elements (0,4), (1,5), (2,6), (3,7).
+template <bool F16>
+__device__ __forceinline__ void nib8(uint32_t u, uint32_t *r)
+{
+    constexpr uint32_t base = F16 ? 0x64006400u : 0x43004300u;   // fp16 1024, bf16 128
+    r[0] = (u & 0x000F000Fu) | base;
+    r[1] = ((u >> 4) & 0x000F000Fu) | base;
+    r[2] = ((u >> 8) & 0x000F000Fu) | base;
+    r[3] = ((u >> 12) & 0x000F000Fu) | base;
+}
+
+// The same pairs as signed fp16 codes q - 8 (exact): (1024 + q) - 1032.
+__device__ __forceinline__ void nib8_signed_f16(uint32_t u, uint32_t *r)
+{
+    nib8<true>(u, r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) asm("sub.f16x2 %0, %0, %1;" : "+r"(r[i]) : "r"(0x64086408u));
+}
+
+// 8 consecutive 16-bit values -> the codes' k order (0,4,1,5,2,6,3,7).
+__device__ __forceinline__ uint4 kperm8(uint4 v)
+{
+    uint4 o;
+    o.x = prmt(v.x, v.z, 0x5410u);
+    o.y = prmt(v.x, v.z, 0x7632u);
+    o.z = prmt(v.y, v.w, 0x5410u);
+    o.w = prmt(v.y, v.w, 0x7632u);
+    return o;
+}
+
+// 2^n as a float, exactly, for -149 <= n <= 127 (powers of two below 2^-126 are subnormal).
+__device__ __forceinline__ float pow2f(int n)
+{
+    return n >= -126 ? __int_as_float((n + 127) << 23) : __int_as_float(1 << (n + 149));
+}
+
+// Position of element i in the k order of its chunk of 8.
+__device__ __forceinline__ int kperm_pos(int i) { return (i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1); }
+
+// Element i (natural order, 0..7) of a k-ordered chunk of 8 bf16 values, as a float.
+__device__ __forceinline__ float kchunk_at(const uint32_t (&w)[4], int i)
+{
+    return __uint_as_float(i < 4 ? (w[i & 3] << 16) : (w[i & 3] & 0xFFFF0000u));
+}
+
+// Byte offset, inside a row of a 128-byte code box, of the 8 code bytes lane (g, t4) reads for
+// group q (0..3) of the box: 16-byte chunk 2q + t4/2 stored at chunk index (chunk ^ g).
+__device__ __forceinline__ uint32_t swz_chunk(int q, int g, int t4)
+{
+    return (uint32_t)((((((q & 3) << 1) | (t4 >> 1)) ^ g) << 4) | ((t4 & 1) << 3));
+}
+
+__device__ __forceinline__ float bf16x4_at(uint2 v, int q)
+{
+    const uint32_t w = q < 2 ? v.x : v.y;
+    return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+__device__ __forceinline__ float f4_at(float4 v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
+__device__ __forceinline__ uint2 lds_u2(const uint16_t *p) { return *reinterpret_cast<const uint2 *>(p); }
+
+__device__ __forceinline__ uint32_t logit_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7FFFFFFFu) == 0) u = 0;        // -0 == +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded poll until *p >= target: one poll, then at most limit - 1 more, spaced by a short sleep.
+__device__ __noinline__ bool poll_geq(const int *p, int target, long long limit)
+{
+    if (ld_acquire_gpu(p) >= target) return true;
+    for (long long n = 1; n < limit; ++n) {
+        __nanosleep(32);
+        if (ld_acquire_gpu(p) >= target) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void stamp(const FusedDecodeArgs &a, int i)
+{
+    if (a.trace && threadIdx.x == 0) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        a.trace[(size_t)blockIdx.x * kTraceStamps + i] = t;
+    }
+}
+
+// Named barrier 1 over the 256 consumer threads, and the same barrier ORing a predicate.
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool consumer_any(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// A warp-uniform bounded wait on an mbarrier phase (every lane polls; the warp agrees on the outcome).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, long long limit, int *abort)
+{
+    const bool ok = mbar_wait(smem_u32(bar), parity, limit, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------------ routing (all threads)
+//
+// Top-k of every token from the fp32 logits (one warp per token: lane l holds the keys of
+// experts l + 32 r; each round takes the largest key, then the lowest id holding it), or the
+// caller's ids; then the distinct experts (increasing id, the shared expert last) and the
+// columns: the (t, j) slots of each expert in increasing t k + j, then the shared slots.
+__device__ __noinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, const float *logits)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = a.T, E = a.E, k = a.k;
+    if (a.ids_in) {
+#pragma unroll 1
+        for (int i = tid; i < T * k; i += kThreads) {
+            int e = a.ids_in[i];
+            if (e < 0 || e >= E) {
+                record_status(a.status, MOE_ERR_DEVICE);
+                e = 0;
+            }
+            S.ids[i / k][i % k] = e;
+            atomicAdd(&S.cnt[e], 1);
+        }
+    } else {
+        constexpr int RW = kMaxExperts / 32;
+#pragma unroll 1
+        for (int t = warp; t < T; t += kThreads / 32) {
+            uint32_t key[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int e = lane + 32 * r;
+                key[r] = e < E ? logit_key(__ldcg(logits + (size_t)t * E + e)) : 0u;   // 0: below every logit
+            }
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) {
+                uint32_t bk = key[0];
+                int br = 0;
+#pragma unroll
+                for (int r = 1; r < RW; ++r)
+                    if (key[r] > bk) {
+                        bk = key[r];
+                        br = r;
+                    }
+                const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+                const uint32_t mine = (uint32_t)(lane + 32 * br);
+                const uint32_t id = __reduce_min_sync(0xffffffffu, bk == mk ? mine : 0xffffffffu);
+                if (id == mine) {
+#pragma unroll
+                    for (int r = 0; r < RW; ++r)
+                        if (r == br) key[r] = 0u;
+                    S.ids[t][j] = (int)id;
+                    S.lg[t][j] = key_logit(mk);
+                    atomicAdd(&S.cnt[id], 1);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    stamp(a, kStTopk);
+    if (warp == 0) {
+        const int per = (E + 31) / 32, b0 = lane * per, b1 = min(E, b0 + per);
+        int nloc = 0, cloc = 0;
+#pragma unroll 1
+        for (int e = b0; e < b1; ++e) {
+            nloc += S.cnt[e] > 0;
+            cloc += S.cnt[e];
+        }
+        int ni = nloc, ci = cloc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vn = __shfl_up_sync(0xffffffffu, ni, o), vc = __shfl_up_sync(0xffffffffu, ci, o);
+            if (lane >= o) {
+                ni += vn;
+                ci += vc;
+            }
+        }
+        int pos = ni - nloc, col = ci - cloc;
+#pragma unroll 1
+        for (int e = b0; e < b1; ++e) {
+            const int c = S.cnt[e];
+            if (c > 0) {
+                if (c > T) record_status(a.status, MOE_ERR_DEVICE);   // an id repeated within a token
+                S.list[pos] = e;
+                S.lpos[e] = pos;
+                S.ncols[pos] = c;
+                S.colptr[pos] = col;
+                ++pos;
+                col += c;
+            }
+        }
+        if (lane == 31) {
+            int D = ni;
+            if (a.has_shared) {
+                S.list[D] = E;
+                S.ncols[D] = T;
+                S.colptr[D] = ci;
+                ++D;
+            }
+            S.colptr[D] = ci + (a.has_shared ? T : 0);
+            S.nlist = D;
+        }
+    }
+    __syncthreads();
+    stamp(a, kStListed);
+    // columns: the routed slots of each expert in increasing t (one warp, token after token; a
+    // token's k picks are distinct experts, so its lanes never share a list entry)
+    if (warp == 0) {
+#pragma unroll 1
+        for (int d = lane; d < S.nlist; d += 32) S.fill[d] = 0;
+        __syncwarp();
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            const int e = lane < k ? S.ids[t][lane] : -1 - lane;
+            if (__popc(__match_any_sync(0xffffffffu, e)) > 1) record_status(a.status, MOE_ERR_DEVICE);
+            if (lane < k) {
+                const int d = S.lpos[e];
+                const int col = S.colptr[d] + atomicAdd(&S.fill[d], 1);
+                S.colof[t][lane] = col;
+                S.colf[col] = t * k + lane;
+                S.ctok[col] = t;
+            }
+            __syncwarp();
+        }
+    }
+    if (a.has_shared)
+#pragma unroll 1
+        for (int t = tid; t < T; t += kThreads) {
+            const int col = S.colptr[S.nlist - 1] + t;
+            S.colof[t][k] = col;
+            S.colf[col] = T * k + t;
+            S.ctok[col] = t;
+        }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ per-token weights (aux warp)
+//
+// Token t = grid - 1 - blockIdx: gamma = x . v in fp32 (lane l sums the groups l, l + 32, ...
+// element by element, then a fixed shuffle tree), w_s = bf16(sigmoid(bf16(gamma))) and
+// p_j = bf16(exp(l_j - l_0) / sum_i exp(l_i - l_0)) in fp64, published for the combining CTAs.
+__device__ __noinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a, const uint16_t *s_x)
+{
+    const int lane = threadIdx.x & 31, T = a.T, k = a.k, G = a.H / kGroup;
+    const int t = (int)gridDim.x - 1 - (int)blockIdx.x;
+    if (a.ids_in || t < 0 || t >= T) return;
+    if (a.ids_out && lane < k) a.ids_out[t * k + lane] = S.ids[t][lane];
+    double ex = 0.0;
+    if (lane < k) ex = exp((double)S.lg[t][lane] - (double)S.lg[t][0]);
+    double den = 0.0;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order j = 0..k-1
+    if (lane < k) {
+        const uint16_t pb = double_to_bf16_bits(ex / den);
+        a.p_glob[t * k + lane] = pb;
+        if (a.p_out) a.p_out[t * k + lane] = pb;
+    }
+    float part = 0.f;
+    if (a.has_shared) {
+#pragma unroll 1
+        for (int grp = lane; grp < G; grp += 32) {
+            const uint4 *xr = reinterpret_cast<const uint4 *>(s_x + (size_t)t * (G * kXG + 8) + grp * kXG);
+            const uint4 *vp = reinterpret_cast<const uint4 *>(a.v + grp * kGroup);
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                const uint4 xv = xr[c], vv = __ldg(vp + c);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float vf = __uint_as_float((i & 1) ? (vw[i >> 1] & 0xFFFF0000u) : (vw[i >> 1] << 16));
+                    part = fmaf(kchunk_at(xw, i), vf, part);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    }
+    if (lane == 0) {
+        uint16_t wsb = 0;
+        if (a.has_shared) {
+            const float gamma = part * pow2f(S.xe[t]);
+            const float gb = bf16_bits_to_float(float_to_bf16_bits(gamma));
+            wsb = double_to_bf16_bits(1.0 / (1.0 + exp(-(double)gb)));
+        }
+        a.ws_glob[t] = wsb;
+        if (a.ws_out) a.ws_out[t] = wsb;
+    }
+}
+
+// ------------------------------------------------------------------ producer (one warp)
+//
+// Gate and up chunks: lane 0 waits for the slot, then one 3D TMA copy brings the 32 code rows (each
+// 128-byte box in the 128-byte swizzle) and two bulk copies their scales and biases; the other
+// lanes arrive.  Down chunk: the slice's 16-byte column of all H rows, which TMA moves one narrow
+// row at a time; here the 32 lanes take the rows in turn with 16-byte cp.async and each arrives
+// (without a count increment) once its own copies have landed.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __noinline__ void fused_producer(FSmem &S, const FusedMaps &maps, const FusedDecodeArgs &a,
+                                            const FusedGeom &geo, uint8_t *ring, int U)
+{
+    const int lane = threadIdx.x & 31;
+    // every argument read once into registers (each copy instruction is a compiler memory barrier)
+    const int H = a.H, I = a.I, E = a.E, G = H / kGroup, SL = I / kSlice, R = geo.R;
+    const uint32_t slot_bytes = geo.slot, codes1 = geo.codes1, sc1 = geo.sc1;
+    const size_t drow = (size_t)I / 2;
+    const long long limit = a.wait_limit;
+    const uint16_t *gsc = a.gate.scales, *gbi = a.gate.biases, *usc = a.up.scales, *ubi = a.up.biases;
+    const uint16_t *sgsc = a.s_gate.scales, *sgbi = a.s_gate.biases, *susc = a.s_up.scales, *subi = a.s_up.biases;
+    const uint8_t *dcodes = a.down.codes, *sdcodes = a.s_down.codes;
+    const CUtensorMap *mg = &maps.g, *mu = &maps.u, *msg = &maps.sg, *msu = &maps.su;
+    int issued = 0;
+    bool stop = false;
+#pragma unroll 1
+    for (int u = blockIdx.x, i = 0; u < U && !stop; u += gridDim.x, ++i) {
+        const int d = u / SL, s = u - d * SL, e = S.list[d];
+        const bool shr = e == E;
+#pragma unroll 1
+        for (int c = 0; c < 3; ++c) {
+            const int q = 3 * i + c, slot = q % R;
+            bool ok = true;
+            if (lane == 0 && q >= R &&
+                !mbar_wait_sleepy(smem_u32(&S.empty[slot]), ((q / R) - 1) & 1, limit, &S.abort)) {
+                S.abort = 1;
+                record_status(a.status, MOE_ERR_TIMEOUT);
+                ok = false;
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                stop = true;
+                break;
+            }
+            uint8_t *base = ring + (size_t)slot * slot_bytes;
+            const uint32_t fb = smem_u32(&S.full[slot]);
+            if (c < 2) {
+                if (lane == 0) {
+                    const int row0 = (shr ? 0 : e * I) + s * kSlice;
+                    const size_t so = (size_t)row0 * G;
+                    const uint16_t *sc = c == 0 ? (shr ? sgsc : gsc) : (shr ? susc : usc);
+                    const uint16_t *bi = c == 0 ? (shr ? sgbi : gbi) : (shr ? subi : ubi);
+                    mbar_arrive_expect_tx(fb, codes1 + 2 * sc1);
+                    tma_load_3d(smem_u32(base), c == 0 ? (shr ? msg : mg) : (shr ? msu : mu), 0, row0, 0, fb);
+                    bulk_load(smem_u32(base + codes1), sc + so, sc1, fb);
+                    bulk_load(smem_u32(base + codes1 + sc1), bi + so, sc1, fb);
+                } else {
+                    mbar_arrive(fb);
+                }
+            } else {
+                const uint8_t *src = (shr ? sdcodes : dcodes) + (size_t)(shr ? 0 : e) * H * drow + s * 16;
+                const uint32_t dst = smem_u32(base);
+#pragma unroll 4
+                for (int r = lane; r < H; r += 32) cp_async16(dst + r * 16, src + (size_t)r * drow);
+                cp_async_mbar_arrive_noinc(fb);
+            }
+            issued = q + 1;
+        }
+    }
+    // every issued copy lands before the CTA may leave: a slot is refilled only after the warps that
+    // read it saw its previous copy land, so the copies still in flight are among the last R issued
+    if (lane == 0)
+#pragma unroll 1
+        for (int q = issued > R ? issued - R : 0; q < issued; ++q)
+            mbar_wait(smem_u32(&S.full[q % R]), (q / R) & 1, kDrainLimit, nullptr);
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------ consumers (warps 0-7)
+//
+// Gate/up chunk: warp w takes matrix m = w / 4 (gate, up), 16-row tile mt = (w / 2) % 2 and the
+// groups of parity kh = w % 2, with every group's product s (sum (128 + q) x') + (b - 128 s) sum x'
+// added in increasing group order; the two parities are added in h = silu(g) u.  Down chunk:
+// warp w takes H / 128 tiles of 16 rows, K = 32 (the slice), raw sums P = sum (q - 8) h'.  The
+// down codes enter the MMA signed: with 1024 + q the sum would be ~1024 sum h' and cancel about
+// eight bits against the bias term, beyond what the tensor cores' fp32 accumulation keeps.
+template <int NT>
+__device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs &a, const FusedGeom &geo,
+                                                const uint8_t *ring, const uint16_t *s_x, const float *s_xs,
+                                                float *s_red, uint16_t *s_h, float *s_hs, int U)
+{
+    constexpr int NC = NT * 8;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+    const int T = a.T, H = a.H, I = a.I, G = H / kGroup, SL = I / kSlice, R = geo.R;
+    const int m = warp >> 2, mt = (warp >> 1) & 1, kh = warp & 1, nbx = G / 4, XS = G * kXG + 8;
+    const long long limit = a.wait_limit;
+    float *const part = a.part;
+    float *const hsum = a.hsum;
+    bool fail_d = false;
+#pragma unroll 1
+    for (int u = blockIdx.x, i = 0; u < U; u += gridDim.x, ++i) {
+        const int d = u / SL, s = u - d * SL;
+        const int ncol = min(S.ncols[d], T), colbase = S.colptr[d];
+        const int q1 = 3 * i + m, slot1 = q1 % R, slot_o = (3 * i + 1 - m) % R;
+        bool ok = !fail_d && warp_wait(&S.full[slot1], (q1 / R) & 1, limit, &S.abort);
+        if (i == 0) stamp(a, kStFirstGate);
+        if (ok) {
+            const uint8_t *chunk = ring + (size_t)slot1 * geo.slot;
+            const uint8_t *cb = chunk + (mt * 16 + g) * 128;              // row mt 16 + g of every 4 KB box
+            const uint16_t *scs = reinterpret_cast<const uint16_t *>(chunk + geo.codes1) + (mt * 16 + g) * G;
+            const uint16_t *bis = scs + kSlice * G;
+            int xrow[NT], tA[NT], tB[NT];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c = j * 8 + g, cA = j * 8 + 2 * t4;
+                xrow[j] = c < ncol ? S.ctok[colbase + c] : -1;
+                tA[j] = cA < ncol ? S.ctok[colbase + cA] : -1;
+                tB[j] = cA + 1 < ncol ? S.ctok[colbase + cA + 1] : -1;
+            }
+            float acc[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) acc[j][v] = 0.f;
+#pragma unroll 1
+            for (int bx = 0; bx < nbx; ++bx) {
+                const uint2 vs0 = lds_u2(scs + 4 * bx), vs1 = lds_u2(scs + 8 * G + 4 * bx);
+                const uint2 vb0 = lds_u2(bis + 4 * bx), vb1 = lds_u2(bis + 8 * G + 4 * bx);
+                float4 sxA[NT], sxB[NT];
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    sxA[j] = tA[j] >= 0 ? *reinterpret_cast<const float4 *>(s_xs + tA[j] * G + 4 * bx) : z;
+                    sxB[j] = tB[j] >= 0 ? *reinterpret_cast<const float4 *>(s_xs + tB[j] * G + 4 * bx) : z;
+                }
+#pragma unroll
+                for (int qq = 0; qq < 2; ++qq) {
+                    const int q = kh + 2 * qq, grp = 4 * bx + q;
+                    const uint32_t o = (uint32_t)bx * (kSlice * 128) + swz_chunk(q, g, t4);
+                    const uint2 c0 = *reinterpret_cast<const uint2 *>(cb + o);
+                    const uint2 c1 = *reinterpret_cast<const uint2 *>(cb + o + 1024);
+                    const float s0 = bf16x4_at(vs0, q), s1 = bf16x4_at(vs1, q);
+                    const float k0 = fmaf(-128.f, s0, bf16x4_at(vb0, q));
+                    const float k1 = fmaf(-128.f, s1, bf16x4_at(vb1, q));
+                    uint32_t a0[8], a1[8];
+                    nib8<false>(c0.x, a0);
+                    nib8<false>(c0.y, a0 + 4);
+                    nib8<false>(c1.x, a1);
+                    nib8<false>(c1.y, a1 + 4);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        if (j * 8 >= ncol) break;
+                        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                        if (xrow[j] >= 0) {
+                            const uint4 *xr = reinterpret_cast<const uint4 *>(s_x + (size_t)xrow[j] * XS + grp * kXG) +
+                                              2 * t4;
+                            lo = xr[0];
+                            hi = xr[1];
+                        }
+                        const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                        float dd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int mm = 0; mm < 4; ++mm)
+                            mma16816<false>(dd, a0[2 * mm], a1[2 * mm], a0[2 * mm + 1], a1[2 * mm + 1], bp[2 * mm],
+                                            bp[2 * mm + 1]);
+                        const float xA = f4_at(sxA[j], q), xB = f4_at(sxB[j], q);
+                        acc[j][0] = fmaf(s0, dd[0], fmaf(k0, xA, acc[j][0]));
+                        acc[j][1] = fmaf(s0, dd[1], fmaf(k0, xB, acc[j][1]));
+                        acc[j][2] = fmaf(s1, dd[2], fmaf(k1, xA, acc[j][2]));
+                        acc[j][3] = fmaf(s1, dd[3], fmaf(k1, xB, acc[j][3]));
+                    }
+                }
+            }
+            float *red = s_red + ((size_t)(m * 2 + kh) * kSlice + mt * 16) * NC;   // [32 rows][NC]
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c0 = j * 8 + 2 * t4;
+                red[g * NC + c0] = acc[j][0];
+                red[g * NC + c0 + 1] = acc[j][1];
+                red[(g + 8) * NC + c0] = acc[j][2];
+                red[(g + 8) * NC + c0 + 1] = acc[j][3];
+            }
+        }
+        // A warp releases the chunk it reads only once that chunk has landed (its wait succeeded):
+        // otherwise the producer could issue the next copy into a slot whose copy is still in
+        // flight.  The other matrix's chunk it never reads, so it releases that one at once; the
+        // slot's phase still needs the arrivals of the warps that read it.
+        __syncwarp();
+        if (lane == 0) {
+            if (ok) mbar_arrive(smem_u32(&S.empty[slot1]));
+            mbar_arrive(smem_u32(&S.empty[slot_o]));
+        }
+        if (!ok && lane == 0) {
+            S.abort = 1;
+            record_status(a.status, MOE_ERR_TIMEOUT);
+        }
+        if (consumer_any(!ok)) break;
+
+        // h' = g' u' sigmoid(g' 2^e) for the slice's 32 rows, as fp16 in the codes' k order, and its sum
+#pragma unroll 1
+        for (int c = warp; c < ncol; c += kCW) {
+            const int row = lane;
+            const float gs = s_red[((0 * 2 + 0) * kSlice + row) * NC + c] + s_red[((0 * 2 + 1) * kSlice + row) * NC + c];
+            const float us = s_red[((1 * 2 + 0) * kSlice + row) * NC + c] + s_red[((1 * 2 + 1) * kSlice + row) * NC + c];
+            const int t = S.ctok[colbase + c];
+            const float hv = gs / (1.f + __expf(-gs * pow2f(S.xe[t]))) * us;
+            const __half hb = __float2half_rn(hv);
+            s_h[c * kSlice + kperm_pos(row)] = __half_as_ushort(hb);
+            const float hf = __half2float(hb);
+            float sum = hf;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0) {
+                s_hs[c] = sum;
+                hsum[(size_t)(colbase + c) * SL + s] = sum;
+            }
+            if (a.h_out) {
+                const float up = pow2f(S.xe[t]);
+                a.h_out[(size_t)S.colf[colbase + c] * I + s * kSlice + row] = hf * up * up;
+            }
+        }
+        consumer_bar();
+
+        const int q2 = 3 * i + 2, slot2 = q2 % R;
+        const bool okd = warp_wait(&S.full[slot2], (q2 / R) & 1, limit, &S.abort);
+        if (i == 0) stamp(a, kStFirstDown);
+        if (okd) {
+            const uint8_t *dch = ring + (size_t)slot2 * geo.slot;
+            uint32_t hb[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c = j * 8 + g;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (c < ncol) v = *reinterpret_cast<const uint4 *>(s_h + c * kSlice + 8 * t4);
+                hb[j][0] = v.x;
+                hb[j][1] = v.y;
+                hb[j][2] = v.z;
+                hb[j][3] = v.w;
+            }
+            const int MT = H / (16 * kCW);
+            float *pbase = part + (size_t)colbase * SL * H + (size_t)s * H;
+#pragma unroll 2
+            for (int tt = 0; tt < MT; ++tt) {
+                const int r0 = (warp * MT + tt) * 16 + g;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(dch + r0 * 16 + 4 * t4);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(dch + (r0 + 8) * 16 + 4 * t4);
+                uint32_t a0[4], a1[4];
+                nib8_signed_f16(w0, a0);
+                nib8_signed_f16(w1, a1);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    if (j * 8 >= ncol) break;
+                    float dd[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma16816<true>(dd, a0[0], a1[0], a0[1], a1[1], hb[j][0], hb[j][1]);
+                    mma16816<true>(dd, a0[2], a1[2], a0[3], a1[3], hb[j][2], hb[j][3]);
+                    const int cA = j * 8 + 2 * t4;
+                    if (cA < ncol) {
+                        float *pc = pbase + (size_t)cA * SL * H;
+                        pc[r0] = dd[0];
+                        pc[r0 + 8] = dd[2];
+                    }
+                    if (cA + 1 < ncol) {
+                        float *pc = pbase + (size_t)(cA + 1) * SL * H;
+                        pc[r0] = dd[1];
+                        pc[r0 + 8] = dd[3];
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && okd) mbar_arrive(smem_u32(&S.empty[slot2]));
+        if (!okd && lane == 0) {
+            S.abort = 1;
+            record_status(a.status, MOE_ERR_TIMEOUT);
+        }
+        fail_d = !okd;
+    }
+}
+
+// ------------------------------------------------------------------ combine (all threads)
+//
+// Rows [blockIdx RB, blockIdx RB + RB) of every token.  Per (token, 4 rows, slot): the slot's
+// expert output y_e = 2^(2e) sum over groups, in order, of s (P_{2g} + P_{2g+1}) + (b + 8 s)
+// (Hs_{2g} + Hs_{2g+1}); then per (token, 4 rows): y = sum_j p_j y_ej + w_s y_s in slot order, one
+// rounding (or added to acc).  An item's loads are all issued before its first add.
+__device__ __noinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a, const FusedGeom &geo, float4 *s_t)
+{
+    const int tid = threadIdx.x;
+    const int T = a.T, H = a.H, I = a.I, k = a.k, GI = I / kGroup, SL = I / kSlice;
+    const int NS = k + (a.has_shared ? 1 : 0);
+    const int r0 = (int)blockIdx.x * geo.RB;
+    const int nrows = min(geo.RB, H - r0);
+    if (nrows <= 0) return;
+    const int nq = nrows / 4;
+#pragma unroll 1
+    for (int i = tid; i < T * k; i += kThreads)
+        S.p[i / k][i % k] = bf16_bits_to_float(a.ids_in ? a.p_in[i] : __ldcg(a.p_glob + i));
+#pragma unroll 1
+    for (int t = tid; t < T; t += kThreads) {
+        uint16_t wb = 0;
+        if (a.has_shared) wb = a.ids_in ? (a.ws_in ? a.ws_in[t] : (uint16_t)0) : __ldcg(a.ws_glob + t);
+        S.ws[t] = bf16_bits_to_float(wb);
+    }
+    const int nitem = T * nq * NS;
+#pragma unroll 1
+    for (int it = tid; it < nitem; it += kThreads) {
+        const int j = it % NS, rest = it / NS, q = rest % nq, t = rest / nq;
+        const bool shr = j == k;
+        const int e = shr ? 0 : S.ids[t][j];
+        const int col = S.colof[t][j];
+        const int r = r0 + 4 * q;
+        const QMatDev &dm = shr ? a.s_down : a.down;
+        const uint16_t *sp = dm.scales + ((size_t)e * H + r) * GI;
+        const uint16_t *bp = dm.biases + ((size_t)e * H + r) * GI;
+        const float *pp = a.part + (size_t)col * SL * H + r;
+        const float *hp = a.hsum + (size_t)col * SL;
+        float ye[4] = {0.f, 0.f, 0.f, 0.f};
+        if (GI == 8) {
+            // every load of the item first: 16 slices of 4 rows, 16 sums of h', the 4 rows' scales and biases
+            float4 pv[16];
+#pragma unroll
+            for (int v = 0; v < 16; ++v) pv[v] = __ldcg(reinterpret_cast<const float4 *>(pp + (size_t)v * H));
+            float4 hv[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) hv[v] = __ldcg(reinterpret_cast<const float4 *>(hp) + v);
+            uint4 sv[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                sv[i] = __ldg(reinterpret_cast<const uint4 *>(sp) + i);
+                bv[i] = __ldg(reinterpret_cast<const uint4 *>(bp) + i);
+            }
+            const float hsl[16] = {hv[0].x, hv[0].y, hv[0].z, hv[0].w, hv[1].x, hv[1].y, hv[1].z, hv[1].w,
+                                   hv[2].x, hv[2].y, hv[2].z, hv[2].w, hv[3].x, hv[3].y, hv[3].z, hv[3].w};
+#pragma unroll
+            for (int gg = 0; gg < 8; ++gg) {
+                const float hs = hsl[2 * gg] + hsl[2 * gg + 1];
+                const float4 p0 = pv[2 * gg], p1 = pv[2 * gg + 1];
+                const float ps[4] = {p0.x + p1.x, p0.y + p1.y, p0.z + p1.z, p0.w + p1.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t sw = gg < 2 ? sv[i].x : gg < 4 ? sv[i].y : gg < 6 ? sv[i].z : sv[i].w;
+                    const uint32_t bw = gg < 2 ? bv[i].x : gg < 4 ? bv[i].y : gg < 6 ? bv[i].z : bv[i].w;
+                    const float sc = __uint_as_float((gg & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
+                    const float bi = __uint_as_float((gg & 1) ? (bw & 0xFFFF0000u) : (bw << 16));
+                    ye[i] += fmaf(sc, ps[i], fmaf(8.f, sc, bi) * hs);
+                }
+            }
+        } else {
+#pragma unroll 4
+            for (int gg = 0; gg < GI; ++gg) {
+                const float4 p0 = __ldcg(reinterpret_cast<const float4 *>(pp + (size_t)(2 * gg) * H));
+                const float4 p1 = __ldcg(reinterpret_cast<const float4 *>(pp + (size_t)(2 * gg + 1) * H));
+                const float hs = __ldcg(hp + 2 * gg) + __ldcg(hp + 2 * gg + 1);
+                const float ps[4] = {p0.x + p1.x, p0.y + p1.y, p0.z + p1.z, p0.w + p1.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float sc = bf16_bits_to_float(__ldg(sp + (size_t)i * GI + gg));
+                    const float bi = bf16_bits_to_float(__ldg(bp + (size_t)i * GI + gg));
+                    ye[i] += fmaf(sc, ps[i], fmaf(8.f, sc, bi) * hs);
+                }
+            }
+        }
+        const float up = pow2f(S.xe[t]);
+        const float4 v = make_float4(ye[0] * up * up, ye[1] * up * up, ye[2] * up * up, ye[3] * up * up);
+        s_t[it] = v;
+        if (a.yslot_out) {
+            const int f = shr ? T * k + t : t * k + j;
+            *reinterpret_cast<float4 *>(a.yslot_out + (size_t)f * H + r) = v;
+        }
+    }
+    __syncthreads();
+    if (a.stages_only) return;
+#pragma unroll 1
+    for (int it = tid; it < T * nq; it += kThreads) {
+        const int q = it % nq, t = it / nq, r = r0 + 4 * q;
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int j = 0; j < NS; ++j) {
+            const float4 ye = s_t[(size_t)it * NS + j];
+            const float w = j == k ? S.ws[t] : S.p[t][j];
+            sum.x = fmaf(w, ye.x, sum.x);
+            sum.y = fmaf(w, ye.y, sum.y);
+            sum.z = fmaf(w, ye.z, sum.z);
+            sum.w = fmaf(w, ye.w, sum.w);
+        }
+        if (a.y) {
+            const uint32_t lo = (uint32_t)float_to_bf16_bits(sum.x) | ((uint32_t)float_to_bf16_bits(sum.y) << 16);
+            const uint32_t hi = (uint32_t)float_to_bf16_bits(sum.z) | ((uint32_t)float_to_bf16_bits(sum.w) << 16);
+            *reinterpret_cast<uint2 *>(a.y + (size_t)t * H + r) = make_uint2(lo, hi);
+        } else {
+            float4 *ap = reinterpret_cast<float4 *>(a.acc + (size_t)t * H + r);
+            float4 av = *ap;
+            av.x += sum.x;
+            av.y += sum.y;
+            av.z += sum.z;
+            av.w += sum.w;
+            *ap = av;
+        }
+    }
+}
+
+// Asks L2 for the down scale and bias rows this CTA combines, for every listed expert (they are
+// read after the unit counter, on the critical path).
+__device__ __noinline__ void prefetch_combine_scales(const FSmem &S, const FusedDecodeArgs &a, const FusedGeom &geo)
+{
+    const int lane = threadIdx.x & 31, H = a.H, E = a.E, GI = a.I / kGroup;
+    const int r0 = (int)blockIdx.x * geo.RB, nrows = min(geo.RB, H - r0);
+    const uint32_t bytes = (uint32_t)nrows * GI * 2;
+    if (nrows <= 0 || (bytes & 15u)) return;
+#pragma unroll 1
+    for (int d = lane; d < S.nlist; d += 32) {
+        const int e = S.list[d];
+        const bool shr = e == E;
+        const QMatDev &dm = shr ? a.s_down : a.down;
+        const size_t o = ((size_t)(shr ? 0 : e) * H + r0) * GI;
+        if (((reinterpret_cast<uintptr_t>(dm.scales + o) | reinterpret_cast<uintptr_t>(dm.biases + o)) & 15u) == 0) {
+            prefetch_l2_bulk(dm.scales + o, bytes);
+            prefetch_l2_bulk(dm.biases + o, bytes);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_fused_kernel(const __grid_constant__ FusedMaps maps, const __grid_constant__ FusedDecodeArgs a,
+                        const __grid_constant__ FusedGeom geo)
+{
+    __shared__ FSmem S;
+    extern __shared__ uint8_t dyn_raw[];
+    uint8_t *dyn = align_smem_1024(dyn_raw);
+    uint8_t *ring = dyn;
+    uint16_t *s_x = reinterpret_cast<uint16_t *>(dyn + geo.x_off);    // [T][G * 72 + 8] bf16 x', k order
+    float *s_xs = reinterpret_cast<float *>(dyn + geo.xs_off);         // [T][G] group sums of x'
+    float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);       // [2][2][32][NC]
+    uint16_t *s_h = reinterpret_cast<uint16_t *>(dyn + geo.h_off);     // [NC][32] fp16 h', k order
+    float *s_hs = reinterpret_cast<float *>(dyn + geo.hs_off);         // [NC]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = a.T, H = a.H, E = a.E, G = H / kGroup, SL = a.I / kSlice;
+    const int grid = gridDim.x, cta = blockIdx.x;
+    const long long limit = a.wait_limit;
+    int *const cnt_router = a.sync + kSyncRouter, *const cnt_units = a.sync + kSyncUnits;
+    int *const cnt_exit = a.sync + kSyncExit;
+    stamp(a, kStStart);
+
+    if (tid == 0) {
+        for (int s = 0; s < geo.R; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 32);   // every producer lane arrives once per chunk
+            mbar_init(smem_u32(&S.empty[s]), kCW);
+        }
+        S.abort = 0;
+        fence_mbar_init();
+    }
+#pragma unroll 1
+    for (int e = tid; e < kMaxList; e += kThreads) S.cnt[e] = 0;
+    if (tid < kDecodeMaxTok) S.xmax[tid] = 0;
+
+    // this CTA's router rows (weights only: read before the wait for the preceding kernel)
+    const bool router = a.ids_in == nullptr && a.logits_in == nullptr;
+    const int nre = router && cta < E ? (E - 1 - cta) / grid + 1 : 0;
+    int er = -1, rt0 = 0, rstep = 1;
+    uint4 rc[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                   make_uint4(0u, 0u, 0u, 0u)};
+    float rs = 0.f, rbias = 0.f;
+    if (nre > 0 && warp < kCW) {
+        const int stride = kCW / nre;
+        if (warp / nre < stride) {
+            er = cta + grid * (warp % nre);
+            rt0 = warp / nre;
+            rstep = stride;
+        }
+        if (er >= 0 && lane < G) {
+            const uint4 *cp = reinterpret_cast<const uint4 *>(a.r_codes + (size_t)er * H + lane * kGroup);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) rc[c] = __ldg(cp + c);
+            rs = bf16_bits_to_float(__ldg(a.r_scales + (size_t)er * G + lane));
+            rbias = bf16_bits_to_float(__ldg(a.r_biases + (size_t)er * G + lane));
+        }
+    }
+    if (warp == kWarpProd && lane == 0) {
+        prefetch_map(&maps.g);
+        prefetch_map(&maps.u);
+        if (a.has_shared) {
+            prefetch_map(&maps.sg);
+            prefetch_map(&maps.su);
+        }
+    }
+
+    __syncthreads();       // barrier inits and zeroed counts visible
+    // ---- x (written by the preceding kernel) into shared memory: the raw chunks are copied into the
+    // padded layout, each token's largest |x| is found, then a pass scales by 2^-e (exact), puts each
+    // chunk of 8 in the codes' k order and sums each group of 64 (its 8 chunks sit in 8 consecutive
+    // lanes: a fixed shuffle tree)
+    pdl_wait();
+    const int XS = G * kXG + 8;
+    const int cpr = H / 8;
+#pragma unroll 1
+    for (int i = tid; i < T * cpr; i += kThreads) {
+        const int t = i / cpr, c = i - t * cpr;
+        cp_async16(smem_u32(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8), reinterpret_cast<const uint4 *>(a.x) + i);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    // a warp's 32 chunks of one pass belong to one token (H / 8 is a multiple of 32): one atomic per warp
+#pragma unroll 1
+    for (int i = tid; i < T * cpr; i += kThreads) {
+        const int t = i / cpr, c = i - t * cpr;
+        const uint4 v = *reinterpret_cast<const uint4 *>(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8);
+        const uint32_t m0 = max(max(v.x & 0x7FFFu, v.x >> 16 & 0x7FFFu), max(v.y & 0x7FFFu, v.y >> 16 & 0x7FFFu));
+        const uint32_t m1 = max(max(v.z & 0x7FFFu, v.z >> 16 & 0x7FFFu), max(v.w & 0x7FFFu, v.w >> 16 & 0x7FFFu));
+        const uint32_t mw = __reduce_max_sync(__activemask(), max(m0, m1));
+        if ((i & 31) == 0) atomicMax(&S.xmax[t], (int)mw);
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int i = tid; i < T * cpr; i += kThreads) {
+        const int t = i / cpr, c = i - t * cpr;
+        const int ef = S.xmax[t] >> 7, xe = ef == 0 ? -126 : ef - 127;
+        const float sc = pow2f(-xe);
+        uint4 *px = reinterpret_cast<uint4 *>(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8);
+        const uint4 v = *px;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(w[q] << 16) * sc, hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
+            w[q] = (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
+            sum += __uint_as_float(w[q] << 16);
+            sum += __uint_as_float(w[q] & 0xFFFF0000u);
+        }
+        *px = kperm8(make_uint4(w[0], w[1], w[2], w[3]));
+        const unsigned gm = 0xFFu << (lane & 24);          // the 8 lanes holding this group's chunks
+        sum += __shfl_xor_sync(gm, sum, 1);
+        sum += __shfl_xor_sync(gm, sum, 2);
+        sum += __shfl_xor_sync(gm, sum, 4);
+        if ((c & 7) == 0) s_xs[t * G + (c >> 3)] = sum;
+        if (c == 0) S.xe[t] = xe;
+    }
+    __syncthreads();
+    stamp(a, kStXStaged);
+
+    // ---- router logits of this CTA's experts: per group s sum q x + b sum x in fp32, elements in
+    // order, then a fixed shuffle tree (the same operations as the router kernel, on x' = x 2^-e,
+    // which scales every intermediate exactly); then the grid-wide counter
+    if (er >= 0) {
+#pragma unroll 1
+        for (int t = rt0; t < T; t += rstep) {
+            float prt = 0.f;
+            if (lane < G) {
+                const uint4 *xr = reinterpret_cast<const uint4 *>(s_x + (size_t)t * XS + lane * kXG);
+                float dq = 0.f, sx = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 xv = xr[c];
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    const uint32_t clo = (c & 1) ? rc[c >> 1].z : rc[c >> 1].x;
+                    const uint32_t chi = (c & 1) ? rc[c >> 1].w : rc[c >> 1].y;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float qv = (float)(((i < 4 ? clo : chi) >> ((i & 3) * 8)) & 0xFFu);
+                        const float xv1 = kchunk_at(xw, i);
+                        dq = fmaf(qv, xv1, dq);
+                        sx += xv1;
+                    }
+                }
+                prt = fmaf(rs, dq, fmaf(rbias, sx, 0.f));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) prt += __shfl_xor_sync(0xffffffffu, prt, o);
+            if (lane == 0) {
+                float l = prt * pow2f(S.xe[t]);
+                if (a.router_bias) l = l + __ldg(a.router_bias + er);   // one fp32 rounding
+                a.logits[(size_t)t * E + er] = l;
+            }
+        }
+    }
+    __syncthreads();
+    if (router) {
+        if (tid == 0) {
+            __threadfence();
+            const int old = atomicAdd(cnt_router, 1);
+            stamp(a, kStRouterPub);
+            if (old < 0 || old >= grid) {
+                record_status(a.status, MOE_ERR_WORKSPACE);   // the workspace header was not zero-filled
+                S.abort = 1;
+            } else if (!poll_geq(cnt_router, grid, limit)) {
+                record_status(a.status, MOE_ERR_TIMEOUT);
+                S.abort = 1;
+            }
+        }
+        __syncthreads();
+    }
+    stamp(a, kStRouterCnt);
+
+    int U = 0;
+    if (!S.abort) {
+        route_and_list(S, a, a.logits_in ? a.logits_in : a.logits);
+        U = S.nlist * SL;
+    }
+    stamp(a, kStRouted);
+
+    if (!S.abort) {
+        if (warp == kWarpProd) {
+            fused_producer(S, maps, a, geo, ring, U);
+        } else if (warp == kWarpAux) {
+            prefetch_combine_scales(S, a, geo);
+            token_weights(S, a, s_x);
+        } else {
+            fused_consumers<NT>(S, a, geo, ring, s_x, s_xs, s_red, s_h, s_hs, U);
+        }
+    }
+    if ((int)blockIdx.x >= U) {          // no units: the first-chunk stamps take this time
+        stamp(a, kStFirstGate);
+        stamp(a, kStFirstDown);
+    }
+    __syncthreads();
+    stamp(a, kStUnitsDone);
+    if (tid == 0 && !S.abort) {
+        __threadfence();            // this CTA's partial sums and published weights, before the count
+        const int old = atomicAdd(cnt_units, 1);
+        if (old < 0 || old >= grid) {
+            record_status(a.status, MOE_ERR_WORKSPACE);
+            S.abort = 1;
+        } else if (!poll_geq(cnt_units, grid, limit)) {
+            record_status(a.status, MOE_ERR_TIMEOUT);
+            S.abort = 1;
+        }
+    }
+    __syncthreads();
+    stamp(a, kStUnitsCnt);
+    pdl_trigger();
+    if (!S.abort) fused_combine(S, a, geo, reinterpret_cast<float4 *>(ring));
+    __syncthreads();
+    stamp(a, kStCombined);
+    // the last CTA out resets the counters for the next call on this workspace
+    if (tid == 0) {
+        const int old = atomicAdd(cnt_exit, 1);
+        if (old == grid - 1) {
+            *cnt_router = 0;
+            *cnt_units = 0;
+            *cnt_exit = 0;
+        } else if (old < 0 || old >= grid) {
+            record_status(a.status, MOE_ERR_WORKSPACE);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+std::mutex g_attr_mutex;
+
+// Cached per-device attributes (device ids 0..kMaxDev-1).
+constexpr int kMaxDev = 64;
+struct DevInfo {
+    int sms = 0, optin = 0;
+};
+DevInfo g_dev[kMaxDev];
+uint32_t g_smem_set[kMaxDev][2];     // largest dynamic shared-memory size set so far per kernel
+
+bool dev_info(int dev, DevInfo *out)
+{
+    if (dev < 0 || dev >= kMaxDev) return false;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    DevInfo &d = g_dev[dev];
+    if (d.sms == 0) {
+        int sms = 0, optin = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return false;
+        d.sms = sms;
+        d.optin = optin;
+    }
+    *out = d;
+    return true;
+}
+
+bool fused_geometry(int T, int H, int I, int k, int has_shared, int grid, int optin, FusedGeom *out)
+{
+    if (T < 1 || T > kDecodeMaxTok || H % 256 || H > 2048 || I % 64 || I > 4096 || grid < 1) return false;
+    FusedGeom g{};
+    const int G = H / kGroup, NT = T > 8 ? 2 : 1, NC = 8 * NT;
+    g.codes1 = (uint32_t)kSlice * H / 2;
+    g.sc1 = (uint32_t)kSlice * G * 2;
+    g.codes2 = (uint32_t)H * 16;
+    g.slot = (uint32_t)align_up(std::max(g.codes1 + 2 * g.sc1, g.codes2), 1024);
+    const size_t xb = align_up((size_t)T * (G * kXG + 8) * 2, 16), xsb = align_up((size_t)T * G * 4, 16);
+    const size_t redb = (size_t)2 * 2 * kSlice * NC * 4, hb = (size_t)NC * kSlice * 2, hsb = align_up((size_t)NC * 4, 16);
+    const size_t fixed = xb + xsb + redb + hb + hsb;
+    const long long budget = (long long)optin - (long long)sizeof(FSmem) - 1024 - 64;
+    if (budget <= (long long)fixed) return false;
+    long long R = (budget - (long long)fixed) / g.slot;
+    if (R > kMaxSlots) R = kMaxSlots;
+    if (R < 3) return false;
+    g.R = (int)R;
+    g.RB = 4 * ((H + 4 * grid - 1) / (4 * grid));
+    const int NS = k + (has_shared ? 1 : 0);
+    if ((size_t)T * (g.RB / 4) * NS * 16 > (size_t)g.R * g.slot) return false;   // combine terms in the ring
+    size_t o = (size_t)g.R * g.slot;
+    g.x_off = (uint32_t)o;
+    o += xb;
+    g.xs_off = (uint32_t)o;
+    o += xsb;
+    g.red_off = (uint32_t)o;
+    o += redb;
+    g.h_off = (uint32_t)o;
+    o += hb;
+    g.hs_off = (uint32_t)o;
+    o += hsb;
+    g.dyn = (uint32_t)(o + 1024);    // slack for aligning the base to 1024 bytes
+    *out = g;
+    return true;
+}
+
+bool code_map_rows(CUtensorMap *m, const uint8_t *codes, int row_bytes, uint64_t rows, int box_rows)
+{
+    // (128-byte chunk, row, chunk index), chunk index outermost: one copy brings every 128-byte box
+    // of a unit's rows, each box landing as [box_rows][128] with the 128-byte swizzle
+    const uint64_t dims[3] = {128u, rows, (uint64_t)row_bytes / 128u};
+    const uint64_t strides[2] = {(uint64_t)row_bytes, 128u};
+    const uint32_t box[3] = {128u, (uint32_t)box_rows, (uint32_t)row_bytes / 128u};
+    return make_map_3d(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared)
+{
+    int dev = 0;
+    DevInfo di;
+    if (cudaGetDevice(&dev) != cudaSuccess || !dev_info(dev, &di)) return false;
+    if (E > kCW * di.sms || di.sms > kTraceMaxCtas) return false;   // at most eight router experts per CTA
+    FusedGeom g;
+    return fused_geometry(T, H, I, k, has_shared, di.sms, di.optin, &g);
+}
+
+size_t decode_fused_trace_ctas()
+{
+    int dev = 0;
+    DevInfo di;
+    if (cudaGetDevice(&dev) != cudaSuccess || !dev_info(dev, &di)) return 0;
+    return (size_t)di.sms;
+}
+
+cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t st)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    DevInfo di;
+    if (!dev_info(dev, &di)) return cudaErrorInvalidDevice;
+    FusedGeom geo;
+    if (!fused_geometry(a.T, a.H, a.I, a.k, a.has_shared, di.sms, di.optin, &geo)) return cudaErrorInvalidValue;
+    FusedMaps maps;
+    const uint64_t E = (uint64_t)a.E;
+    bool ok = code_map_rows(&maps.g, a.gate.codes, a.H / 2, E * a.I, kSlice) &&
+              code_map_rows(&maps.u, a.up.codes, a.H / 2, E * a.I, kSlice);
+    if (ok && a.has_shared)
+        ok = code_map_rows(&maps.sg, a.s_gate.codes, a.H / 2, a.I, kSlice) &&
+             code_map_rows(&maps.su, a.s_up.codes, a.H / 2, a.I, kSlice);
+    else if (ok) {
+        maps.sg = maps.g;
+        maps.su = maps.u;
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    const int which = a.T > 8 ? 1 : 0;
+    auto kern = which ? decode_fused_kernel<2> : decode_fused_kernel<1>;
+    {
+        // raised (never lowered) to the largest size a launch of this kernel on the device asks for
+        std::lock_guard<std::mutex> lock(g_attr_mutex);
+        if (g_smem_set[dev][which] < geo.dyn) {
+            if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.dyn)) !=
+                cudaSuccess)
+                return e;
+            g_smem_set[dev][which] = geo.dyn;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(di.sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = geo.dyn;
+    cfg.stream = st;
+    // cooperative (the CTAs wait on one another), and allowed to start while the kernel
+    // before it still runs: only weights are read before the wait for it
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, maps, a, geo);
+}
+
+}  // namespace qmoe

@@ -137,33 +137,42 @@ cudaError_t launch_small_down(const PrefillArgs &a, cudaStream_t st);
 
 struct FusedDecodeArgs {
     const uint16_t *x;            // bf16 [T, H]
+    const uint8_t *r_codes;       // router u8 [E, H]
+    const uint16_t *r_scales;     // bf16 [E, H/64]
+    const uint16_t *r_biases;
+    const uint16_t *v;            // bf16 [H] shared gate vector (null without a shared expert)
+    const float *router_bias;     // f32 [E] or null
+    const float *logits_in;       // f32 [T, E] caller logits (no router GEMV), or null
     QMatDev gate, up, down, s_gate, s_up, s_down;
-    const float *logits;          // f32 [T, E] (routing source unless ids_in is given)
-    const float *gamma;           // f32 [T]
     const int32_t *ids_in;        // [T, k] given routing (then p_in / ws_in too), or null
     const uint16_t *p_in;         // bf16 [T, k]
     const uint16_t *ws_in;        // bf16 [T] or null
     int32_t *ids_out;             // [T, k] or null
     uint16_t *p_out;              // bf16 [T, k] or null
     uint16_t *ws_out;             // bf16 [T] or null
-    uint16_t *h;                  // fp16 [T*k + T, I], slot order
-    float *yslot;                 // f32 [T*k + T, H]
+    float *logits;                // f32 [T, E] published logits (workspace)
+    uint16_t *p_glob;             // bf16 [T, k] published pick weights (workspace)
+    uint16_t *ws_glob;            // bf16 [T] published shared weights (workspace)
+    float *part;                  // f32 [T (k + 1), I / 32, H] raw down sums per column and slice (workspace)
+    float *hsum;                  // f32 [T (k + 1), I / 32] sums of h' per column and slice (workspace)
     uint16_t *y;                  // bf16 [T, H] = bf16(sum), or null
     float *acc;                   // f32 [T, H] += sum (when y is null)
-    int *cnt_expert;              // [(E + 1) * 32] gate/up units done per expert-list entry, stride 32 (zeroed before launch)
-    int *cnt_rows;                // [(H / 128) * 32] down units done per 128-row block, stride 32 (zeroed before launch)
-    int *cnt_pick;                // tokens whose pick weights are published (zeroed before launch)
-    uint16_t *p_glob;             // bf16 [T, k] published pick weights
-    uint16_t *ws_glob;            // bf16 [T] published shared weights
+    float *h_out;                 // f32 [T (k + 1), I] h per slot as the down projection consumes it, or null
+    float *yslot_out;             // f32 [T (k + 1), H] expert output per slot before weighting, or null
+    int stages_only;              // 1: write h_out / yslot_out only (no y, no acc)
+    int *sync;                    // workspace header: status word, then the three counters
     int *status;
+    unsigned long long *trace;    // [grid, kTraceStamps] %globaltimer stamps per CTA, or null
     int T, H, I, E, k, has_shared;
     long long wait_limit;
 };
 
-// Streaming decode kernel (T <= 16): whether the layer shape fits its shared-memory
-// ring on the current device, and the cooperative launch (one CTA per SM).
-bool decode_stream_fits(int T, int H, int I);
-cudaError_t launch_decode_stream(const FusedDecodeArgs &a, cudaStream_t st);
+// Fused decode kernel (T <= 16): router, top-k, expert FFNs and combine in one cooperative
+// launch of one CTA per SM.  decode_fused_fits: whether the layer shape fits its shared-memory
+// plan on the current device; decode_fused_trace_ctas: CTAs of that launch (rows of the trace).
+bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared);
+size_t decode_fused_trace_ctas();
+cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t st);
 cudaError_t launch_route_gemv(const RouteArgs &a, cudaStream_t st);
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t st);
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t st);

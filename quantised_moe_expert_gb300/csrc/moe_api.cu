@@ -1,14 +1,15 @@
 // C ABI of the MoE layer library: argument checks, workspace carving, launches.
 // The operations and their contract are stated in include/moe.h.
-#include <atomic>
-
 #include "kernels.cuh"
 
 using namespace qmoe;
 
 namespace {
 
-std::atomic<long long> g_wait_limit{1ll << 20};
+constexpr long long kDefaultWaitPolls = 1ll << 20;
+
+// Polls of every bounded wait inside the kernels of one call (moe_config.wait_polls).
+long long wait_limit_of(const moe_config &c) { return c.wait_polls > 0 ? (long long)c.wait_polls : kDefaultWaitPolls; }
 
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned16_or_null(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -48,8 +49,7 @@ int resolve_path(int path, int T)
     return path;
 }
 
-// Router GEMV (or pass-through of supplied logits) and top-k into the given buffers.
-// Router GEMV (and gamma) only; zeroes the fused decode counters.
+// Arguments of the router GEMV kernel (logits and gamma).
 RouteArgs route_args(const moe_config &c, const moe_weights &w, const uint16_t *x, int T, const float *router_bias,
                      const float *logits_in, float *logits, const WsLayout &L, void *ws)
 {
@@ -62,7 +62,7 @@ RouteArgs route_args(const moe_config &c, const moe_weights &w, const uint16_t *
     ra.router_bias = router_bias;
     ra.logits = logits;
     ra.gamma = ws_at<float>(ws, L.gamma);
-    ra.status_reset = ws_at<int>(ws, L.status);
+    ra.status_reset = nullptr;        // the status word keeps the first error until it is read
     ra.T = T;
     ra.H = c.hidden;
     ra.E = c.n_experts;
@@ -76,7 +76,7 @@ int enqueue_route(const moe_config &c, const moe_weights &w, const uint16_t *x, 
 {
     RouteArgs ra = route_args(c, w, x, T, router_bias, logits_in, logits, L, ws);
     const bool mma_router = !logits_in && T > kDecodeMaxTok;
-    if (mma_router) ra.n_expert_tiles = 0;                  // gamma (and zeroing) only
+    if (mma_router) ra.n_expert_tiles = 0;                  // gamma (and the histogram zeroing) only
     ra.zero = ws_at<int>(ws, L.hist);                       // the top-k counts into a zeroed histogram
     ra.nzero = L.nblk * c.n_experts;
     int rc = cuda_rc(launch_route_gemv(ra, st));
@@ -230,16 +230,20 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     a.has_shared = c.has_shared;
     a.max_w1 = L.max_w1;
     a.max_w2 = L.max_w2;
-    a.wait_limit = g_wait_limit.load();
+    a.wait_limit = wait_limit_of(c);
     return cuda_rc(launch_prefill_experts(a, st));
 }
 
-// Arguments of the fused decode kernel common to both of its callers.
+// Arguments of the fused decode kernel common to all of its callers.
 FusedDecodeArgs fused_args(const moe_config &c, const moe_weights &w, const uint16_t *x, int T, const WsLayout &L,
                            void *ws)
 {
     FusedDecodeArgs fa{};
     fa.x = x;
+    fa.r_codes = w.router.codes;
+    fa.r_scales = w.router.scales;
+    fa.r_biases = w.router.biases;
+    fa.v = c.has_shared ? w.shared_gate_vec : nullptr;
     fa.gate = dev(w.gate);
     fa.up = dev(w.up);
     fa.down = dev(w.down);
@@ -248,22 +252,28 @@ FusedDecodeArgs fused_args(const moe_config &c, const moe_weights &w, const uint
         fa.s_up = dev(w.s_up);
         fa.s_down = dev(w.s_down);
     }
-    fa.h = ws_at<uint16_t>(ws, L.h);
-    fa.yslot = ws_at<float>(ws, L.yslot);
-    fa.cnt_expert = ws_at<int>(ws, L.counters);
-    fa.cnt_rows = fa.cnt_expert + 32 * (c.n_experts + 1);
-    fa.cnt_pick = fa.cnt_rows + 32 * ((c.hidden + 127) / 128);
+    fa.logits = ws_at<float>(ws, L.logits);
     fa.p_glob = ws_at<uint16_t>(ws, L.p);
     fa.ws_glob = ws_at<uint16_t>(ws, L.w_s);
+    fa.part = ws_at<float>(ws, L.dpart);
+    fa.hsum = ws_at<float>(ws, L.dhsum);
+    fa.sync = ws_at<int>(ws, L.status);
     fa.status = ws_at<int>(ws, L.status);
+    fa.trace = ws_at<unsigned long long>(ws, L.trace);
     fa.T = T;
     fa.H = c.hidden;
     fa.I = c.inter;
     fa.E = c.n_experts;
     fa.k = c.top_k;
     fa.has_shared = c.has_shared;
-    fa.wait_limit = g_wait_limit.load();
+    fa.wait_limit = wait_limit_of(c);
     return fa;
+}
+
+bool fused_fits(const moe_config &c, int T)
+{
+    return T >= 1 && T <= kDecodeMaxTok &&
+           decode_fused_fits(T, c.hidden, c.inter, c.n_experts, c.top_k, c.has_shared);
 }
 
 bool weights_ok(const moe_config &c, const moe_weights *w, bool need_router, bool need_experts)
@@ -392,20 +402,15 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     wa.max_items[1] = L.max_w1;
     wa.max_items[2] = L.max_w2;
     const int rp = resolve_path(path, T);
-    const bool fused = rp == MOE_PATH_DECODE && T <= kDecodeMaxTok && decode_stream_fits(T, cfg->hidden, cfg->inter);
-    if (fused) {
-        wa.zero = ws_at<int>(ws, L.counters);
-        wa.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128 + 1);
-    }
-    if ((rc = cuda_rc(launch_worklist(wa, st)))) return rc;
-    if (fused) {
+    if (rp == MOE_PATH_DECODE && fused_fits(*cfg, T)) {
         FusedDecodeArgs fa = fused_args(*cfg, *w, x, T, L, ws);
         fa.ids_in = ids;
         fa.p_in = p;
-        fa.ws_in = w_shared;
+        fa.ws_in = cfg->has_shared ? w_shared : nullptr;
         fa.acc = acc;
-        return cuda_rc(launch_decode_stream(fa, st));
+        return cuda_rc(launch_decode_fused(fa, st));
     }
+    if ((rc = cuda_rc(launch_worklist(wa, st)))) return rc;
     ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_shared, offsets, perm, acc, L, ws);
     if (rp == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, nullptr, st);
     return enqueue_prefill_experts(*cfg, ea, L, ws, 0, st);
@@ -437,21 +442,16 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
     if (T == 0) return MOE_OK;
     const int rp = resolve_path(path, T);
     auto st = static_cast<cudaStream_t>(stream);
-    if (rp == MOE_PATH_DECODE && T <= kDecodeMaxTok && decode_stream_fits(T, cfg->hidden, cfg->inter)) {
-        // router GEMV (zeroing the counters), then one cooperative launch for the rest of the layer
-        float *lg = logits_in ? const_cast<float *>(logits_in) : ws_at<float>(ws, L.logits);
-        RouteArgs ra = route_args(*cfg, *w, x, T, router_bias, logits_in, lg, L, ws);
-        ra.zero = ws_at<int>(ws, L.counters);
-        ra.nzero = 32 * (cfg->n_experts + 1 + (cfg->hidden + 127) / 128 + 1);
-        if ((rc = cuda_rc(launch_route_gemv(ra, st)))) return rc;
+    if (rp == MOE_PATH_DECODE && fused_fits(*cfg, T)) {
+        // the whole layer in one cooperative launch
         FusedDecodeArgs fa = fused_args(*cfg, *w, x, T, L, ws);
-        fa.logits = lg;
-        fa.gamma = ra.gamma;
+        fa.router_bias = logits_in ? nullptr : router_bias;
+        fa.logits_in = logits_in;
         fa.ids_out = ids_out;
         fa.p_out = p_out;
         fa.ws_out = w_shared_out;
         fa.y = y;
-        return cuda_rc(launch_decode_stream(fa, st));
+        return cuda_rc(launch_decode_fused(fa, st));
     }
     int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.ids);
     uint16_t *p = p_out ? p_out : ws_at<uint16_t>(ws, L.p);
@@ -472,21 +472,65 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
 
 int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_status)
 {
-    if (!aligned16(ws) || ws_bytes < 256 || !device_status) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws) || ws_bytes < kHeaderBytes || !device_status) return MOE_ERR_INVALID_ARG;
     auto st = static_cast<cudaStream_t>(stream);
     int v = 0;
     int rc = cuda_rc(cudaStreamSynchronize(st));
     if (!rc) rc = cuda_rc(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost));
-    if (!rc) rc = cuda_rc(cudaMemset(ws, 0, sizeof(int)));
+    if (!rc) rc = cuda_rc(cudaMemset(ws, 0, kHeaderBytes));   // status word and counters
     if (rc) return rc;
     *device_status = v;
     return MOE_OK;
 }
 
-int moe_set_wait_limit(long long polls)
+int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T, const int32_t *ids,
+                      const int32_t *counts, const int32_t *offsets, const int32_t *perm, float *h_out,
+                      float *yslot_out, int path, void *ws, size_t ws_bytes, void *stream)
 {
-    g_wait_limit.store(polls > 0 ? polls : (1ll << 20));
-    return MOE_OK;
+    int rc = check_common(cfg, T);
+    if (rc) return rc;
+    if (!weights_ok(*cfg, w, false, true) || !aligned16(x) || !aligned16(ids) || !aligned16_or_null(h_out) ||
+        !aligned16_or_null(yslot_out))
+        return MOE_ERR_INVALID_ARG;
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_PREFILL) return MOE_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
+    if (T == 0 || (!h_out && !yslot_out)) return MOE_OK;
+    auto st = static_cast<cudaStream_t>(stream);
+    const int rp = resolve_path(path, T);
+    if (rp == MOE_PATH_DECODE && fused_fits(*cfg, T)) {
+        FusedDecodeArgs fa = fused_args(*cfg, *w, x, T, L, ws);
+        fa.ids_in = ids;
+        fa.p_in = ws_at<uint16_t>(ws, L.p);     // weights are not applied: any values serve
+        fa.ws_in = nullptr;
+        fa.h_out = h_out;
+        fa.yslot_out = yslot_out;
+        fa.stages_only = 1;
+        return cuda_rc(launch_decode_fused(fa, st));
+    }
+    (void)counts;
+    (void)offsets;
+    (void)perm;
+    return MOE_ERR_UNSUPPORTED;
+}
+
+int moe_decode_timeline(const moe_config *cfg, int T, void *ws, size_t ws_bytes, void *stream,
+                        unsigned long long *host_stamps, int max_ctas, int *n_ctas)
+{
+    int rc = check_common(cfg, T);
+    if (rc) return rc;
+    if (!host_stamps || !n_ctas || max_ctas < 0) return MOE_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
+    const int n = (int)decode_fused_trace_ctas();
+    if (n <= 0 || n > kTraceMaxCtas) return MOE_ERR_CUDA;
+    *n_ctas = n;
+    const int m = n < max_ctas ? n : max_ctas;
+    rc = cuda_rc(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    if (!rc && m > 0)
+        rc = cuda_rc(cudaMemcpy(host_stamps, ws_at<unsigned long long>(ws, L.trace),
+                                sizeof(unsigned long long) * kTraceStamps * (size_t)m, cudaMemcpyDeviceToHost));
+    return rc;
 }
 
 }  // extern "C"

@@ -25,6 +25,17 @@ constexpr int kTileN2 = 256;        // tokens per tile, down GEMM
 constexpr int kSmallN = 32;         // tokens per item of the small-tile GEMMs (experts of at most kSmallN tokens)
 constexpr int kBigTok = kSmallN + 1;   // experts with at least this many tokens go to the tensor-memory GEMMs
 
+// Workspace header (int offsets from the start of the workspace): the device status word, then
+// the fused decode kernel's grid-wide counters, 128 bytes apart.  The counters must be zero
+// before a workspace's first use; the fused decode kernel leaves them zero when it ends.
+constexpr int kSyncRouter = 32;     // CTAs whose router logits are published
+constexpr int kSyncUnits = 64;      // CTAs whose expert units are done
+constexpr int kSyncExit = 96;       // CTAs that have left
+constexpr size_t kHeaderBytes = 512;
+constexpr int kTraceStamps = 12;    // %globaltimer stamps per CTA of the fused decode kernel
+constexpr int kTraceMaxCtas = 256;
+constexpr int kDecodeSlice = 32;    // rows of the intermediate dimension per fused decode unit
+
 // One unit of work of a grouped kernel: an expert (E = shared) and a token range
 // [tok0, tok0 + ntok) of its permuted slot list.
 struct WorkItem {
@@ -36,7 +47,7 @@ struct WorkItem {
 
 // Offsets (bytes) of every scratch array inside the caller's workspace.
 struct WsLayout {
-    size_t status;     // int32 status word + counters (256 B)
+    size_t status;     // header: int32 status word + fused decode counters (kHeaderBytes)
     size_t logits;     // f32 [T, E]
     size_t ids;        // i32 [T, k]
     size_t p;          // u16 [T, k]
@@ -48,7 +59,7 @@ struct WsLayout {
     size_t perm;       // i32 [T*k]
     size_t inv_perm;   // i32 [T*k]
     size_t nwork;      // i32 [8]: decode items, gemm1 items, gemm2 items, big gemm1 / gemm2 items
-    size_t counters;   // i32 [(E + 1 + H/128 + 1) * 32]: fused decode counters, 128 B apart
+    size_t trace;      // u64 [kTraceMaxCtas, kTraceStamps] fused decode timeline
     size_t work_dec;   // WorkItem [E + 1]
     size_t work_g1;    // WorkItem [max tiles gemm1]
     size_t work_g2;    // WorkItem [max tiles gemm2]
@@ -56,7 +67,9 @@ struct WsLayout {
     size_t xsum;       // f32 [T, H / 64] group sums of x16 (small-tile gate/up GEMM)
     size_t hsum;       // f32 [T*k + T, I / 64] group sums of h (small-tile GEMMs)
     size_t h;          // fp16 [T*k + T, I] (decode: slot order; prefill: expert-sorted, K-permuted)
-    size_t yslot;      // f32 [T*k + T, H] (decode)
+    size_t yslot;      // f32 [T*k + T, H] (decode kernels of shapes the fused kernel does not take)
+    size_t dpart;      // f32 [T*k + T, I / 32, H] fused decode: raw down sums per column and slice
+    size_t dhsum;      // f32 [T*k + T, I / 32] fused decode: sums of h per column and slice
     size_t acc;        // f32 [T, H] (prefill accumulation)
     size_t total;
     int nblk;
@@ -86,7 +99,7 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.nblk = (int)((Tz + kTokBlock - 1) / kTokBlock);
     L.max_w1 = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kSmallN);   // bounds both item sizes
     L.max_w2 = L.max_w1;
-    L.status = take(256);
+    L.status = take(kHeaderBytes);
     L.logits = take(4 * Tz * E);
     L.ids = take(4 * Tz * k);
     L.p = take(2 * Tz * k);
@@ -98,7 +111,7 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.perm = take(4 * Tz * k);
     L.inv_perm = take(4 * Tz * k);
     L.nwork = take(32);
-    L.counters = take(4 * 32 * (E + 1 + (H + 127) / 128 + 1));
+    L.trace = take(8 * (size_t)kTraceMaxCtas * kTraceStamps);
     L.max_wd = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kDecodeMaxTok);
     L.work_dec = take(sizeof(WorkItem) * (size_t)L.max_wd);
     L.work_g1 = take(sizeof(WorkItem) * (size_t)L.max_w1);
@@ -109,6 +122,9 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.h = take(2 * Tz * (k + 1) * I);
     L.yslot = take(4 * Tz * (k + 1) * H);
     L.acc = take(4 * Tz * H);
+    const size_t Td = Tz <= (size_t)kDecodeMaxTok ? Tz : 0;   // the fused decode kernel takes T <= 16
+    L.dpart = take(4 * Td * (k + 1) * (I / kDecodeSlice) * H);
+    L.dhsum = take(4 * Td * (k + 1) * (I / kDecodeSlice));
     L.total = o;
     return L;
 }

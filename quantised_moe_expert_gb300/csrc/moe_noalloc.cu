@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr size_t kStaticScratchBytes = 4u << 20;   // 4 MiB
+constexpr size_t kStaticScratchBytes = 24u << 20;   // 24 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_moe_static_scratch[kStaticScratchBytes];

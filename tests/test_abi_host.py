@@ -49,7 +49,8 @@ def test_status_strings(lib):
 
 
 def cfg_from(**kw):
-    d = dict(hidden=2048, inter=512, n_experts=256, top_k=8, group=64, bits=4, router_bits=8, has_shared=1)
+    d = dict(hidden=2048, inter=512, n_experts=256, top_k=8, group=64, bits=4, router_bits=8, has_shared=1,
+             wait_polls=0)
     d.update(kw)
     return qm.moe_config(**d)
 
@@ -144,8 +145,32 @@ def test_other_entry_points_reject_bad_arguments(lib):
     st = ctypes.c_int()
     assert lib.moe_get_device_status(None, big, None, ctypes.byref(st)) == qm.MOE_ERR_INVALID_ARG
     assert lib.moe_get_device_status(FAKE, 8, None, ctypes.byref(st)) == qm.MOE_ERR_INVALID_ARG
-    assert lib.moe_set_wait_limit(1000) == qm.MOE_OK
-    assert lib.moe_set_wait_limit(0) == qm.MOE_OK
+    assert lib.moe_get_device_status(FAKE, 256, None, ctypes.byref(st)) == qm.MOE_ERR_INVALID_ARG   # header is 512 B
+    # stage outputs: misaligned h_out, bad path, too small a workspace; T == 0 or no outputs enqueue nothing
+    assert lib.moe_expert_stages(ctypes.byref(cfg), ctypes.byref(w), FAKE, 4, FAKE, FAKE, FAKE, FAKE, MISALIGNED,
+                                 None, 0, FAKE, big, None) == qm.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_stages(ctypes.byref(cfg), ctypes.byref(w), FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 9,
+                                 FAKE, big, None) == qm.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_stages(ctypes.byref(cfg), ctypes.byref(w), FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0,
+                                 FAKE, 16, None) == qm.MOE_ERR_WORKSPACE
+    assert lib.moe_expert_stages(ctypes.byref(cfg), ctypes.byref(w), FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0,
+                                 FAKE, big, None) == qm.MOE_OK
+    assert lib.moe_expert_stages(ctypes.byref(cfg), ctypes.byref(w), FAKE, 4, FAKE, FAKE, FAKE, FAKE, None, None, 0,
+                                 FAKE, big, None) == qm.MOE_OK
+    n = ctypes.c_int()
+    assert lib.moe_decode_timeline(ctypes.byref(cfg), 1, FAKE, big, None, None, 4, ctypes.byref(n)) == \
+        qm.MOE_ERR_INVALID_ARG
+    assert lib.moe_decode_timeline(ctypes.byref(cfg), 1, FAKE, 16, None, FAKE, 4, ctypes.byref(n)) == \
+        qm.MOE_ERR_WORKSPACE
+
+
+def test_wait_limit_is_a_field_of_the_call_config(lib):
+    """The bound on in-kernel waits travels with each call (no process-wide setting)."""
+    names = [f[0] for f in qm.moe_config._fields_]
+    assert names[-1] == "wait_polls"
+    assert lib.moe_check_config(ctypes.byref(cfg_from(wait_polls=1))) == qm.MOE_OK
+    assert lib.moe_check_config(ctypes.byref(cfg_from(wait_polls=-5))) == qm.MOE_OK
+    assert "moe_set_wait_limit" not in open(HEADER).read()
 
 
 def test_python_binding_has_every_entry_point():

@@ -1,10 +1,10 @@
 """Device-side failure handling without a GPU fault.
 
-Every wait inside the kernels is bounded.  Setting the bound to one poll makes
-the tensor-core pipeline's waits run out before any copy can land: the kernels
-must record MOE_ERR_TIMEOUT in the workspace status word, drain what they
-issued, free their TMEM and return, leaving the context usable.  Nothing here
-traps, faults or hangs the GPU.
+Every wait inside the kernels is bounded by the call's moe_config.wait_polls.
+A bound of one poll makes the waits run out before any copy can land or any
+other CTA can arrive: the kernels must record MOE_ERR_TIMEOUT in the workspace
+status word, drain what they issued, free their TMEM and return, leaving the
+context usable.  Nothing here traps, faults or hangs the GPU.
 """
 import numpy as np
 import pytest
@@ -24,18 +24,12 @@ def _cuda():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
     qm.load()
-    yield
-    qm.moe_set_wait_limit(0)
 
 
 def test_prefill_wait_limit_runs_out_then_recovers():
     wl, w, layer = H.device_layer(0)
     x = synth.make_x(wl.shape, 40, wl.seed, stream=9)
-    qm.moe_set_wait_limit(1)
-    try:
-        got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
-    finally:
-        qm.moe_set_wait_limit(0)
+    got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL, cfg=qm.config_of(wl.shape, wait_polls=1))
     assert got["status"] == qm.MOE_ERR_TIMEOUT
     again = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
     assert again["status"] == 0
@@ -44,20 +38,48 @@ def test_prefill_wait_limit_runs_out_then_recovers():
     H.check_y(again["y"], ref["y"])
 
 
-def test_decode_wait_limit_is_bounded_then_recovers():
+@pytest.mark.parametrize("T", [1, 16])
+def test_decode_wait_limit_runs_out_then_recovers(T):
+    """One poll: the first CTAs at the router counter cannot find every other CTA there yet."""
     wl, w, layer = H.device_layer(2)
-    x = synth.make_x(wl.shape, 16, wl.seed, stream=9)
-    qm.moe_set_wait_limit(1)
-    try:
-        got = H.run_forward(layer, x, path=qm.MOE_PATH_DECODE)
-    finally:
-        qm.moe_set_wait_limit(0)
-    assert got["status"] in (0, qm.MOE_ERR_TIMEOUT)
+    x = synth.make_x(wl.shape, T, wl.seed, stream=9)
+    got = H.run_forward(layer, x, path=qm.MOE_PATH_DECODE, cfg=qm.config_of(wl.shape, wait_polls=1))
+    assert got["status"] == qm.MOE_ERR_TIMEOUT
     again = H.run_forward(layer, x, path=qm.MOE_PATH_DECODE)
     assert again["status"] == 0
     ref = oracle.forward(wl.shape, w, x)
     same = np.all(again["ids"] == ref["ids"], axis=1)
     H.check_y(again["y"], ref["y"], rows=np.nonzero(same)[0])
+
+
+def test_decode_workspace_reused_after_timeout():
+    """A call that timed out leaves the workspace's counters zero: the next call on it is correct."""
+    wl, w, layer = H.device_layer(1)
+    x = H.to_dev_u16(synth.make_x(wl.shape, 1, wl.seed, stream=10))
+    ws = qm.workspace(layer.cfg, 1)
+    qm.forward(layer, x, ws, path=qm.MOE_PATH_DECODE, cfg=qm.config_of(wl.shape, wait_polls=1))
+    torch.cuda.synchronize()
+    hdr = ws[:512].view(torch.int32).cpu().numpy()
+    assert hdr[0] == qm.MOE_ERR_TIMEOUT and not hdr[1:].any()      # status set, counters back to zero
+    y1 = qm.forward(layer, x, ws, path=qm.MOE_PATH_DECODE)
+    torch.cuda.synchronize()
+    assert qm.moe_get_device_status(ws) == qm.MOE_ERR_TIMEOUT     # the earlier call's status, kept until read
+    y2 = qm.forward(layer, x, ws, path=qm.MOE_PATH_DECODE)
+    torch.cuda.synchronize()
+    assert qm.moe_get_device_status(ws) == 0
+    assert torch.equal(y1, y2)
+
+
+def test_decode_dirty_header_is_reported():
+    """A workspace whose header was not zero-filled is reported, not silently used."""
+    wl, w, layer = H.device_layer(0)
+    x = H.to_dev_u16(synth.make_x(wl.shape, 2, wl.seed, stream=12))
+    ws = qm.workspace(layer.cfg, 2)
+    ws[:512].view(torch.int32)[1:].fill_(0x33333333)
+    qm.forward(layer, x, ws, path=qm.MOE_PATH_DECODE, cfg=qm.config_of(wl.shape, wait_polls=64))
+    assert qm.moe_get_device_status(ws) in (qm.MOE_ERR_WORKSPACE, qm.MOE_ERR_TIMEOUT)
+    y = qm.forward(layer, x, ws, path=qm.MOE_PATH_DECODE)            # the status read reset the header
+    assert qm.moe_get_device_status(ws) == 0
 
 
 def test_bad_expert_ids_are_reported_not_trapped():

@@ -1,8 +1,9 @@
 """GPU parity of the prefill (tcgen05 grouped GEMM) path against the FP64 oracle.
 
-Small cases are compared element by element on every row; the T = 512 and
-T = 4096 layers on sampled rows (the oracle's rows are independent), and
-routing (ids, permutation) on every row.
+Every case is compared element by element on every row, the T = 512 and
+T = 4096 layers included.  Rows whose ids differ from the oracle's (only
+allowed where the oracle's k-th and (k+1)-th logits are within 1e-5) are
+compared with the oracle run on the GPU's own fp32 logits for those rows.
 """
 import numpy as np
 import pytest
@@ -32,9 +33,26 @@ def _compare_rows(wl, w, x, got, rows, bias=None, logits_in=None):
     clear = gap >= (0 if logits_in is not None else H.AMBIGUOUS_GAP)
     assert np.array_equal(g["ids"][clear], ref["ids"][clear])
     same = np.nonzero(np.all(g["ids"] == ref["ids"], axis=1))[0]
-    assert len(same) >= len(rows) - 2
     assert H.ulp_diff_bf16(g["p"][same], ref["p"][same]).max(initial=0) <= 1
-    return H.check_y(g["y"], ref["y"], rows=same)
+    return H.check_y(g["y"], ref["y"], rows=same), ref
+
+
+def _compare_all_rows(wl, w, layer, x, got, bias=None, logits_in=None):
+    """Every row: ids, p, w_s and y against the oracle; near-tie rows under the GPU's own logits."""
+    T = x.shape[0]
+    stats, ref = _compare_rows(wl, w, x, got, np.arange(T), bias=bias, logits_in=logits_in)
+    if wl.shape.has_shared:
+        assert H.ulp_diff_bf16(got["w_s"], ref["w_s"]).max(initial=0) <= 1
+    diff = np.nonzero(np.any(got["ids"] != ref["ids"], axis=1))[0]
+    if len(diff):
+        assert logits_in is None
+        r = H.run_route(layer, x, router_bias=bias)
+        assert np.array_equal(r["ids"], got["ids"])
+        ref2 = oracle.forward(wl.shape, w, x, logits_in=r["logits"], rows=diff)
+        assert np.array_equal(ref2["ids"], got["ids"][diff])
+        assert np.array_equal(ref2["p"], got["p"][diff])
+        H.check_y(got["y"][diff], ref2["y"])
+    return stats, len(diff)
 
 
 def test_prefill_tiny_all_rows():
@@ -42,7 +60,7 @@ def test_prefill_tiny_all_rows():
     x = synth.make_x(wl.shape, wl.tokens, wl.seed)
     got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
     assert got["status"] == 0
-    stats = _compare_rows(wl, w, x, got, np.arange(wl.tokens))
+    stats, _ = _compare_rows(wl, w, x, got, np.arange(wl.tokens))
     assert stats["max_abs"] <= 2e-2, stats
 
 
@@ -56,7 +74,7 @@ def test_prefill_ragged_token_counts_small_layer(T):
     _compare_rows(wl, w, x, got, np.arange(T))
 
 
-def test_prefill_t512_sampled_rows():
+def test_prefill_t512_every_row():
     wl, w, layer = H.device_layer(3)
     x = synth.make_x(wl.shape, wl.tokens, wl.seed)
     got = H.run_forward(layer, x, path=qm.MOE_PATH_AUTO)
@@ -64,30 +82,23 @@ def test_prefill_t512_sampled_rows():
     r = H.run_route(layer, x)
     ref_logits = oracle.router_logits(wl.shape, w, x)
     assert np.abs(r["logits"].astype(np.float64) - ref_logits).max() <= H.LOGIT_TOL
-    rows = np.random.default_rng(0).choice(wl.tokens, 24, replace=False)
-    rows = np.concatenate([rows, [0, wl.tokens - 1]])
-    _compare_rows(wl, w, x, got, rows)
+    _, ndiff = _compare_all_rows(wl, w, layer, x, got)
+    assert ndiff <= 2
 
 
-def test_prefill_t4096_zipf_sampled_rows_and_full_routing():
+def test_prefill_t4096_zipf_every_row():
     wl, w, layer = H.device_layer(4)
     x = synth.make_x(wl.shape, wl.tokens, wl.seed)
     bias = synth.zipf_bias(wl.shape, wl.zipf_s, wl.seed)
     got = H.run_forward(layer, x, path=qm.MOE_PATH_AUTO, router_bias=bias)
     assert got["status"] == 0
-    rows = np.random.default_rng(1).choice(wl.tokens, 24, replace=False)
-    _compare_rows(wl, w, x, got, np.concatenate([rows, [wl.tokens - 1]]), bias=bias)
-    # every row's routing against the oracle's router and top-k
     ref_logits = oracle.router_logits(wl.shape, w, x, bias)
-    ref_ids = oracle.topk(ref_logits, wl.shape.top_k)
     r = H.run_route(layer, x, router_bias=bias)
     err = np.abs(r["logits"].astype(np.float64) - ref_logits)
     assert err.max() <= H.LOGIT_TOL, (err.max(), np.unravel_index(err.argmax(), err.shape))
-    assert np.array_equal(r["ids"], got["ids"])
-    clear = H.oracle_gap(ref_logits, wl.shape.top_k) >= H.AMBIGUOUS_GAP
-    bad = np.nonzero(np.any(got["ids"] != ref_ids, axis=1) & clear)[0]
-    assert len(bad) == 0, (len(bad), bad[:8], err.max())
-    counts = np.bincount(ref_ids.ravel(), minlength=wl.shape.n_experts)
+    _, ndiff = _compare_all_rows(wl, w, layer, x, got, bias=bias)
+    assert ndiff <= 2
+    counts = np.bincount(got["ids"].ravel(), minlength=wl.shape.n_experts)
     assert counts.max() > 8 * wl.tokens * wl.shape.top_k / wl.shape.n_experts   # the skew is real
 
 
@@ -118,10 +129,11 @@ def test_prefill_t4096_forced_ties_bit_exact_routing():
     rc, ro, rp, ri = oracle.permute(ref_ids, 256)
     assert np.array_equal(perm.cpu().numpy(), rp) and np.array_equal(inv.cpu().numpy(), ri)
     assert np.array_equal(counts.cpu().numpy(), rc) and np.array_equal(offsets.cpu().numpy(), ro)
-    # the whole layer on the forced-tie logits, sampled rows (tie rows included)
+    # the whole layer on the forced-tie logits, every row: routing bit-exact, y within tolerance
     got = H.run_forward(layer, x, logits_in=lg)
-    rows = np.concatenate([np.arange(0, T, 20)[:12], np.random.default_rng(2).choice(T, 12, replace=False)])
-    _compare_rows(wl, w, x, got, rows, logits_in=lg)
+    assert got["status"] == 0
+    assert np.array_equal(got["ids"], ref_ids) and np.array_equal(got["p"], ref_p)
+    _compare_all_rows(wl, w, layer, x, got, logits_in=lg)
 
 
 def test_decode_and_prefill_paths_agree():

@@ -323,3 +323,47 @@ def test_permutation_matches_stable_argsort(orc):
         assert offsets[0] == 0 and np.array_equal(np.diff(offsets), counts) and offsets[-1] == T * k
         assert np.array_equal(perm, np.argsort(flat, kind="stable"))
         assert np.array_equal(inv[perm], np.arange(T * k))
+
+
+# ----------------------------------------------------------------- expert down projection
+
+def test_expert_down_equals_float64_matmul_and_one_hot_columns(orc):
+    """oracle_expert_down against a torch float64 matmul of the dequantised down matrix, a one-hot
+    h (which must pick out column j of that matrix: pins the [H, I] orientation and the column
+    index), and linearity in h."""
+    shape = synth.TINY_SHAPE
+    w = synth.make_weights(shape, 5)
+    rng = np.random.default_rng(17)
+    for e in (0, 7, -1):
+        m = w.s_down if e < 0 else w.down
+        i = 0 if e < 0 else e
+        Wd = orc.dequant_matrix(m.codes[i], m.scales[i], m.biases[i], 4, shape.inter)
+        assert Wd.shape == (shape.hidden, shape.inter)
+        h = rng.normal(0, 2, shape.inter)
+        got = orc.expert_down(shape, w, e, h)
+        ref = (torch.from_numpy(Wd) @ torch.from_numpy(h)).numpy()
+        assert np.max(np.abs(got - ref)) <= 1e-12 * (1 + np.abs(ref).max())
+        for j in (0, 1, 33, shape.inter - 1):
+            onehot = np.zeros(shape.inter)
+            onehot[j] = 1.0
+            assert np.array_equal(orc.expert_down(shape, w, e, onehot), Wd[:, j])
+        h2 = rng.normal(0, 1, shape.inter)
+        lin = orc.expert_down(shape, w, e, 3.0 * h + h2)
+        assert np.max(np.abs(lin - (3.0 * got + orc.expert_down(shape, w, e, h2)))) <= 1e-11
+
+
+def test_expert_ffn_h_equals_float64_swiglu_of_dequantised_rows(orc):
+    """The h that oracle_expert_ffn returns is silu(Wg x) * (Wu x) of the dequantised matrices."""
+    shape = synth.TINY_SHAPE
+    w = synth.make_weights(shape, 6)
+    x = synth.bf16_bits_to_f32(synth.make_x(shape, 1, 6)).astype(np.float64)[0]
+    for e in (3, -1):
+        mg, mu = (w.s_gate, w.s_up) if e < 0 else (w.gate, w.up)
+        i = 0 if e < 0 else e
+        Wg = torch.from_numpy(orc.dequant_matrix(mg.codes[i], mg.scales[i], mg.biases[i], 4, shape.hidden))
+        Wu = torch.from_numpy(orc.dequant_matrix(mu.codes[i], mu.scales[i], mu.biases[i], 4, shape.hidden))
+        xt = torch.from_numpy(x)
+        ref = (torch.nn.functional.silu(Wg @ xt) * (Wu @ xt)).numpy()
+        h, y = orc.expert_ffn(shape, w, e, x)
+        assert np.max(np.abs(h - ref)) <= 1e-12 * (1 + np.abs(ref).max())
+        assert np.max(np.abs(y - orc.expert_down(shape, w, e, h))) <= 1e-12 * (1 + np.abs(y).max())

@@ -44,6 +44,29 @@ def test_static_scratch_decode_matches_workspace_decode(wl_index, T):
         H.check_y(H.u16(y), H.u16(y_ref))
 
 
+def test_static_scratch_refuses_layers_beyond_its_size():
+    """A layer whose decode scratch exceeds the fixed array is refused before anything is enqueued."""
+    wl, w, layer = H.device_layer(1)
+    big = qm.moe_config(8192, 4096, 256, 16, 64, 4, 8, 1, 0)
+    assert qm.moe_workspace_size(big, 16) > 24 << 20
+    x = torch.zeros((16, 8192), dtype=torch.int16, device="cuda")
+    y = torch.full((16, 8192), 7, dtype=torch.int16, device="cuda")
+    with pytest.raises(qm.MoeError) as e:
+        qm.moe_forward_decode_static(big, layer.w, x, 16, None, None, y, None, None, None)
+    assert e.value.status == qm.MOE_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(y == 7)
+
+
+def test_static_scratch_zero_tokens_is_a_no_op():
+    wl, w, layer = H.device_layer(1)
+    x = torch.zeros((1, wl.shape.hidden), dtype=torch.int16, device="cuda")
+    y = torch.full((1, wl.shape.hidden), 7, dtype=torch.int16, device="cuda")
+    qm.moe_forward_decode_static(layer.cfg, layer.w, x, 0, None, None, y, None, None, None)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7)
+
+
 def test_static_scratch_refuses_prefill_sizes():
     wl, w, layer = H.device_layer(1)
     x = torch.zeros((17, wl.shape.hidden), dtype=torch.int16, device="cuda")
