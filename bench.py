@@ -407,30 +407,41 @@ def cold_call_latency(W, stream, reps=20):
                 flush="512 MiB write before each call")
 
 
-def timeline(W, stream, reps=20):
-    """Per-phase times of single fused decode launches from the kernel's %globaltimer stamps (us from
-    the earliest CTA start): median over launches of the median and the last CTA of each stamp."""
+TIMELINE = ["start", "router_published", "x_staged", "logits_seen", "topk_done", "list_done", "routing_done",
+            "first_gate_chunk", "first_down_chunk", "first_down_done", "units_done", "units_counter",
+            "combine_loads_done", "combine_done"]
+
+
+def timeline(W, stream, graph_steps=200):
+    """Per-phase times of the fused decode kernel in steady state: a graph of back-to-back steps is
+    replayed, then each weight copy's workspace holds the stamps of its last launch (us from the
+    launch's earliest CTA start; median CTA and last CTA), and consecutive launches give the gap
+    from one launch's last CTA to the next launch's first."""
     import torch
     qm = W.qm
     wl = W.wl
-    names = ["start", "x_staged", "router_published", "router_counter", "topk_done", "list_done", "routing_done",
-             "first_gate_chunk", "first_down_chunk", "units_done", "units_counter", "combine_done"]
-    per = []
-    for i in range(reps):
-        c = i % W.copies
+    g = capture(lambda i: W.step(i, stream), graph_steps, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    traces = []
+    for c in range(W.copies):
         L = W.layers[c]
-        with torch.cuda.stream(stream):
-            qm.moe_forward(L.cfg, L.w, W.x[c], wl.tokens, W.bias, None, W.y[c], None, None, None,
-                           qm.MOE_PATH_AUTO, W.ws[c], stream)
-        st = qm.moe_decode_timeline(L.cfg, wl.tokens, W.ws[c], stream).astype(np.int64)
-        t0 = st[:, 0].min()
-        rel = (st - t0) / 1e3
-        per.append((np.median(rel, axis=0), rel.max(axis=0)))
-    med = np.median(np.stack([p[0] for p in per]), axis=0)
-    last = np.median(np.stack([p[1] for p in per]), axis=0)
-    return {"workload": wl.name, "launches": reps, "ctas": int(st.shape[0]),
-            "median_cta_us": dict(zip(names, [round(float(v), 3) for v in med])),
-            "last_cta_us": dict(zip(names, [round(float(v), 3) for v in last]))}
+        traces.append(qm.moe_decode_timeline(L.cfg, wl.tokens, W.ws[c], stream).astype(np.int64))
+    med, last = [], []
+    for st in traces:
+        rel = (st - st[:, 0].min()) / 1e3
+        med.append(np.median(rel, axis=0))
+        last.append(rel.max(axis=0))
+    # launches of the last replay in order: copies (graph_steps - copies .. graph_steps - 1) % copies
+    order = [(graph_steps - W.copies + j) % W.copies for j in range(W.copies)]
+    gaps = [(traces[b][:, 0].min() - traces[a][:, -1].max()) / 1e3 for a, b in zip(order[:-1], order[1:])]
+    del g
+    return {"workload": wl.name, "launches_read": W.copies, "ctas": int(traces[0].shape[0]),
+            "median_cta_us": dict(zip(TIMELINE, [round(float(v), 3) for v in np.median(np.stack(med), axis=0)])),
+            "last_cta_us": dict(zip(TIMELINE, [round(float(v), 3) for v in np.median(np.stack(last), axis=0)])),
+            "gap_between_launches_us": round(float(np.median(gaps)), 3) if gaps else None}
 
 
 def e2e_timing(W, stream, steps, warmup):
@@ -604,11 +615,8 @@ def main():
     if args.timeline:
         import quantised_moe_expert_gb300 as qm
         qm.load()
-        W = Workload(wl, args.copies or 4)
+        W = Workload(wl, args.copies or 8)
         stream = torch.cuda.Stream()
-        for i in range(3):
-            W.step(i, stream)
-        torch.cuda.synchronize()
         if rank == 0:
             print(json.dumps(timeline(W, stream)), flush=True)
         return

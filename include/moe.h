@@ -95,11 +95,15 @@ enum moe_path {
  * router_bits == 8, hidden and inter multiples of 64 (hidden <= 8192,
  * inter <= 4096), 1 <= top_k <= min(n_experts, 16), 1 <= n_experts <= 256,
  * has_shared in {0,1}.  Anything else returns MOE_ERR_UNSUPPORTED.
- * wait_polls bounds every wait inside the kernels of the call: a wait polls
- * at most that many times (the first poll does not block, later ones sleep
- * briefly), then records MOE_ERR_TIMEOUT and the kernel returns early.
- * 0 (or less) selects the default, 1 << 20 polls (about a second).  A limit
- * of 1 makes any wait that is not already satisfied run out (fault tests). */
+ * wait_polls bounds the in-kernel waits of the call: a wait polls at most
+ * that many times (the first poll does not block, later ones sleep briefly),
+ * then records MOE_ERR_TIMEOUT and the kernel returns early.  0 (or less)
+ * selects the default, 1 << 20 polls (about a second).  A limit of 1 makes
+ * any such wait that is not already satisfied run out (fault tests).  In the
+ * fused decode kernel (T <= 16) it bounds the waits on other CTAs (published
+ * router logits, the grid-wide unit counter); a CTA's waits on its own
+ * shared-memory copies keep a fixed bound of the same order, so that a small
+ * limit never leaves the copy ring in mid-flight. */
 typedef struct moe_config {
     int hidden;       /* H */
     int inter;        /* I, intermediate size of every expert, shared included */
@@ -109,7 +113,7 @@ typedef struct moe_config {
     int bits;         /* expert code width */
     int router_bits;  /* router code width */
     int has_shared;   /* 1: the layer has a shared expert slot */
-    int wait_polls;   /* bound on every in-kernel wait of the call; 0 = default */
+    int wait_polls;   /* bound on the in-kernel waits of the call; 0 = default */
 } moe_config;
 
 /* One affine-quantised matrix (or a stack of them), device pointers. */
@@ -120,7 +124,12 @@ typedef struct moe_qmat {
 } moe_qmat;
 
 /* All weights of one layer, device pointers.  s_* and shared_gate_vec may be
- * NULL when has_shared == 0. */
+ * NULL when has_shared == 0.
+ * down_packed / s_down_packed (optional, NULL for none): the down codes
+ * rearranged by moe_pack_down, which the decode kernel streams one contiguous
+ * block per (expert, 32 columns of the intermediate dimension) instead of
+ * gathering 16-byte pieces of every row.  They are read only by the decode
+ * path and give the same results as the MLX layout. */
 typedef struct moe_weights {
     moe_qmat router;   /* [E, H], router_bits */
     moe_qmat gate;     /* [E, I, H] */
@@ -130,6 +139,8 @@ typedef struct moe_weights {
     moe_qmat s_up;     /* [I, H] */
     moe_qmat s_down;   /* [H, I] */
     const uint16_t *shared_gate_vec;  /* bf16 [H] */
+    const uint8_t *down_packed;       /* [E, I/32, H, 16] bytes, or NULL */
+    const uint8_t *s_down_packed;     /* [I/32, H, 16] bytes, or NULL */
 } moe_weights;
 
 /* Human-readable name of a status code; never NULL, static storage. */
@@ -222,6 +233,16 @@ MOE_API int moe_forward_decode_static(const moe_config *cfg, const moe_weights *
                                       const float *router_bias, const float *logits_in, uint16_t *y,
                                       int32_t *ids_out, uint16_t *p_out, uint16_t *w_shared_out, void *stream);
 
+/* Writes the decode layout of the 4-bit down codes: for expert e and column
+ * slice c (32 columns of the intermediate dimension, 16 bytes of every row),
+ *   down_packed[((e * (I/32) + c) * H + r) * 16 + b] = down.codes[(e * H + r) * I/2 + c * 16 + b]
+ * and the same for the shared expert into s_down_packed (skipped when NULL or
+ * has_shared == 0).  Each output holds as many bytes as its source; both are
+ * caller-owned device memory.  Enqueued on `stream`; run it once after the
+ * weights are loaded. */
+MOE_API int moe_pack_down(const moe_config *cfg, const moe_weights *w, uint8_t *down_packed,
+                          uint8_t *s_down_packed, void *stream);
+
 /* Synchronises `stream`, then reads the device status word of `ws` and zeroes
  * the workspace header (status word and counters).  *device_status receives
  * MOE_OK or the first error code a kernel recorded since the last read. */
@@ -247,12 +268,12 @@ MOE_API int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const
                               void *ws, size_t ws_bytes, void *stream);
 
 /* Timeline of the last fused decode launch on `ws` (T <= 16, decode path):
- * synchronises `stream`, then copies per CTA twelve %globaltimer stamps (ns)
- * to host_stamps [max_ctas, 12]: kernel start, x staged, router logits
- * published, router counter reached, top-k done, expert list done, routing
- * done, first gate chunk landed, first down chunk landed, expert units done,
- * unit counter reached, combine done (a stamp that was not reached keeps an
- * older value).
+ * synchronises `stream`, then copies per CTA fourteen %globaltimer stamps
+ * (ns) to host_stamps [max_ctas, 14]: kernel start, router logits published,
+ * x staged for the expert units, every logit seen, top-k done, expert list
+ * done, routing done, first gate chunk landed, first down chunk landed, first
+ * down chunk computed, expert units done, unit counter reached, combine loads
+ * done, combine done (a stamp that was not reached keeps an older value).
  * *n_ctas receives the number of CTAs of the launch. */
 MOE_API int moe_decode_timeline(const moe_config *cfg, int T, void *ws, size_t ws_bytes, void *stream,
                                 unsigned long long *host_stamps, int max_ctas, int *n_ctas);

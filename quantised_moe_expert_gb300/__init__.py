@@ -31,7 +31,8 @@ MOE_PATH_DECODE = 1
 MOE_PATH_PREFILL = 2
 
 EXPORTED = ("moe_status_string", "moe_check_config", "moe_workspace_size", "moe_route", "moe_permute",
-            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status", "moe_expert_stages",
+            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status", "moe_pack_down",
+            "moe_expert_stages",
             "moe_decode_timeline", "moe_forward_decode_static")
 
 
@@ -53,7 +54,8 @@ class moe_qmat(ctypes.Structure):
 
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, moe_qmat) for n in ("router", "gate", "up", "down", "s_gate", "s_up", "s_down")] + \
-               [("shared_gate_vec", ctypes.c_void_p)]
+               [("shared_gate_vec", ctypes.c_void_p), ("down_packed", ctypes.c_void_p),
+                ("s_down_packed", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -92,6 +94,7 @@ def load(build: bool = True):
         lib.moe_forward.argtypes = [P(moe_config), P(moe_weights), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP,
                                     _SZ, _VP]
         lib.moe_get_device_status.argtypes = [_VP, _SZ, _VP, P(ctypes.c_int)]
+        lib.moe_pack_down.argtypes = [P(moe_config), P(moe_weights), _VP, _VP, _VP]
         lib.moe_expert_stages.argtypes = [P(moe_config), P(moe_weights), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _I,
                                           _VP, _SZ, _VP]
         lib.moe_decode_timeline.argtypes = [P(moe_config), _I, _VP, _SZ, _VP, _VP, _I, P(ctypes.c_int)]
@@ -134,9 +137,12 @@ def config_of(shape, wait_polls: int = 0) -> moe_config:
 
 
 class DeviceLayer:
-    """One layer's weights resident on a CUDA device, plus the C weight struct."""
+    """One layer's weights resident on a CUDA device, plus the C weight struct.
 
-    def __init__(self, host, device="cuda"):
+    pack=True also makes the decode layout of the down codes (moe_pack_down) and hands it to the
+    library in moe_weights.down_packed / s_down_packed."""
+
+    def __init__(self, host, device="cuda", pack: bool = True):
         self.shape = host.shape
         self.cfg = config_of(host.shape)
         self.tensors = {}
@@ -157,7 +163,26 @@ class DeviceLayer:
 
         self.w = moe_weights(q("router", host.router), q("gate", host.gate), q("up", host.up),
                              q("down", host.down), q("s_gate", host.s_gate), q("s_up", host.s_up),
-                             q("s_down", host.s_down), up("v", host.shared_gate_vec).data_ptr())
+                             q("s_down", host.s_down), up("v", host.shared_gate_vec).data_ptr(), None, None)
+        if pack:
+            self.pack()
+
+    def pack(self):
+        """The decode layout of the down codes, made on the device by moe_pack_down."""
+        d, sd = self.tensors["down.codes"], self.tensors["s_down.codes"]
+        dp = torch.empty_like(d)
+        sdp = torch.empty_like(sd) if self.shape.has_shared else None
+        moe_pack_down(self.cfg, self.w, dp, sdp)
+        self.tensors["down.packed"] = dp
+        self.w.down_packed = dp.data_ptr()
+        if sdp is not None:
+            self.tensors["s_down.packed"] = sdp
+            self.w.s_down_packed = sdp.data_ptr()
+
+    def unpacked(self) -> "DeviceLayer":
+        """The same layer without the packed down codes (the decode kernel gathers from the MLX layout)."""
+        t = {k: v for k, v in self.tensors.items() if not k.endswith(".packed")}
+        return DeviceLayer.from_tensors(self.shape, t)
 
     @staticmethod
     def from_tensors(shape, tensors):
@@ -170,8 +195,9 @@ class DeviceLayer:
         def q(name):
             return moe_qmat(tensors[name + ".codes"].data_ptr(), tensors[name + ".scales"].data_ptr(),
                             tensors[name + ".biases"].data_ptr())
+        opt = lambda name: tensors[name].data_ptr() if name in tensors else None
         obj.w = moe_weights(q("router"), q("gate"), q("up"), q("down"), q("s_gate"), q("s_up"), q("s_down"),
-                            tensors["v"].data_ptr())
+                            tensors["v"].data_ptr(), opt("down.packed"), opt("s_down.packed"))
         return obj
 
 
@@ -238,6 +264,12 @@ def moe_get_device_status(ws, stream=None) -> int:
     return st.value
 
 
+def moe_pack_down(cfg, w, down_packed, s_down_packed=None, stream=None):
+    rc = load().moe_pack_down(ctypes.byref(cfg), ctypes.byref(w), _ptr(down_packed), _ptr(s_down_packed),
+                              _stream(stream))
+    _check("moe_pack_down", rc)
+
+
 def moe_expert_stages(cfg, w, x, T, ids, counts, offsets, perm, h_out, yslot_out, path, ws, stream=None):
     rc = load().moe_expert_stages(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), T, _ptr(ids), _ptr(counts),
                                   _ptr(offsets), _ptr(perm), _ptr(h_out), _ptr(yslot_out), path, _ptr(ws),
@@ -246,8 +278,8 @@ def moe_expert_stages(cfg, w, x, T, ids, counts, offsets, perm, h_out, yslot_out
 
 
 def moe_decode_timeline(cfg, T, ws, stream=None, max_ctas: int = 256) -> np.ndarray:
-    """Per-CTA %globaltimer stamps (ns) of the last fused decode launch on ws: [n_ctas, 12] uint64."""
-    buf = np.zeros((max_ctas, 12), dtype=np.uint64)
+    """Per-CTA %globaltimer stamps (ns) of the last fused decode launch on ws: [n_ctas, 14] uint64."""
+    buf = np.zeros((max_ctas, 14), dtype=np.uint64)
     n = ctypes.c_int(0)
     rc = load().moe_decode_timeline(ctypes.byref(cfg), T, _ptr(ws), ws.numel() * ws.element_size(),
                                     _stream(stream), ctypes.c_void_p(buf.ctypes.data), max_ctas, ctypes.byref(n))

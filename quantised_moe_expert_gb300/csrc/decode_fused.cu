@@ -8,12 +8,12 @@
 // launch is arranged to cross the grid only twice:
 //
 //   1. Router (every CTA, one CTA per SM).  The CTA's router rows (experts c, c + grid,
-//      ...) are loaded into registers before the wait for the preceding kernel; then x
-//      is staged in shared memory, pre-scaled per token by a power of two (x' = x 2^-e,
-//      max |x'| in [1, 2): exact, and it keeps h inside the fp16 range, see below), and
-//      the CTA's logits go to global memory.  One grid-wide counter; then every CTA reads
-//      all logits and runs the same top-k (warp max / min reductions, ties to the lower
-//      id) and builds the same expert list.
+//      ...) are loaded into registers before the wait for the preceding kernel; then x is
+//      staged in shared memory, the CTA's logits go to global memory tagged with the
+//      launch's epoch, and x is pre-scaled per token by a power of two (x' = x 2^-e, max |x'|
+//      in [1, 2): exact, and it keeps h inside the fp16 range, see below).  Every CTA then
+//      polls the tagged logits until all carry the epoch, runs the same top-k (warp max /
+//      min reductions, ties to the lower id) and builds the same expert list: no counter.
 //   2. Units.  A unit is (expert, 32-row slice s of the intermediate dimension): the
 //      slice's gate and up rows (all of H) and the slice's 32 columns of the down matrix
 //      (all H rows).  Because the affine rule holds for any subset of a group,
@@ -40,9 +40,11 @@
 // Determinism.  Every sum has one order that depends only on the token's own data and on
 // the fixed slice partition, so a token's outputs are the same bits in any batch of 1..16.
 //
-// Synchronisation state lives in the workspace header (three counters); the last CTA to
-// leave resets them, so a workspace needs to be zero-filled only before its first use.
-// Every wait is bounded (a status code is recorded instead of hanging).
+// Synchronisation state lives in the workspace header (two counters and an epoch); the last CTA
+// to leave resets the counters and advances the epoch, so a workspace needs to be zero-filled
+// only before its first use.
+// Every wait is bounded (a status code is recorded instead of hanging): the waits on other CTAs by
+// the caller's limit, a CTA's waits on its own copies by a fixed one (kRingLimit).
 #include <mutex>
 
 #include "kernels.cuh"
@@ -62,7 +64,12 @@ constexpr int kSlice = 32;                     // rows of the intermediate dimen
 constexpr int kMaxSlots = 6;
 constexpr int kMaxCols = kDecodeMaxTok * (kMaxTopK + 1);
 constexpr int kMaxList = kMaxExperts + 1;
+// Waits on this CTA's own copies (the ring's full and empty phases, the drain) are bounded by a
+// fixed number of polls, about a second: they end early only if the copy engine fails.  The
+// caller's limit (moe_config.wait_polls) bounds the waits on other CTAs: the published logits and
+// the unit counter.  So a small caller limit never abandons the ring with copies in flight.
 constexpr long long kDrainLimit = 1ll << 22;
+constexpr long long kRingLimit = 1ll << 20;
 // Staged x: each group of 64 inputs padded to 72 elements and each token row by 8 more, so that
 // neither lanes reading different groups (router) nor lanes reading different tokens (MMA B
 // fragments) meet in one shared-memory bank.
@@ -70,8 +77,8 @@ constexpr int kXG = 72;
 
 // Timeline stamps (trace columns), in the order a CTA reaches them.
 enum {
-    kStStart = 0, kStXStaged, kStRouterPub, kStRouterCnt, kStTopk, kStListed, kStRouted, kStFirstGate,
-    kStFirstDown, kStUnitsDone, kStUnitsCnt, kStCombined
+    kStStart = 0, kStRouterPub, kStXStaged, kStLogitsSeen, kStTopk, kStListed, kStRouted, kStFirstGate,
+    kStFirstDown, kStFirstDownDone, kStUnitsDone, kStUnitsCnt, kStCombineLoads, kStCombined
 };
 
 struct FusedMaps {
@@ -94,9 +101,8 @@ struct FSmem {
     float p[kDecodeMaxTok][kMaxTopK];
     float ws[kDecodeMaxTok];
     int xe[kDecodeMaxTok];                  // x' = x 2^-xe
-    int xmax[kDecodeMaxTok];                // largest |x| bits of each token (bf16 magnitude)
-    int fill[kMaxList];                     // columns handed out per list entry
-    int cnt[kMaxList];                      // picks of each expert
+    uint32_t pickmap[kMaxExperts / 32];     // experts picked by any token (bit e)
+    uint32_t tokmask[kMaxExperts];          // tokens that picked expert e (bit t)
     int lpos[kMaxList];                     // list position of each picked expert
     int list[kMaxList];
     int ncols[kMaxList];
@@ -106,6 +112,7 @@ struct FSmem {
     int colf[kMaxCols];                     // slot index f of each column (t k + j, or T k + t)
     int nlist;
     int abort;
+    uint32_t epoch;                         // this launch's tag on the published logits
     uint64_t full[kMaxSlots], empty[kMaxSlots];
 };
 
@@ -171,10 +178,12 @@ __device__ __forceinline__ float pow2f(int n)
 // Position of element i in the k order of its chunk of 8.
 __device__ __forceinline__ int kperm_pos(int i) { return (i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1); }
 
-// Element i (natural order, 0..7) of a k-ordered chunk of 8 bf16 values, as a float.
+// Element i (natural order, 0..7) of a k-ordered chunk of 8 bf16 values (four words), as a float.
 __device__ __forceinline__ float kchunk_at(const uint32_t (&w)[4], int i)
 {
-    return __uint_as_float(i < 4 ? (w[i & 3] << 16) : (w[i & 3] & 0xFFFF0000u));
+    const int pos = kperm_pos(i);
+    const uint32_t word = w[pos >> 1];
+    return __uint_as_float((pos & 1) ? (word & 0xFFFF0000u) : (word << 16));
 }
 
 // Byte offset, inside a row of a 128-byte code box, of the 8 code bytes lane (g, t4) reads for
@@ -184,13 +193,6 @@ __device__ __forceinline__ uint32_t swz_chunk(int q, int g, int t4)
     return (uint32_t)((((((q & 3) << 1) | (t4 >> 1)) ^ g) << 4) | ((t4 & 1) << 3));
 }
 
-__device__ __forceinline__ float bf16x4_at(uint2 v, int q)
-{
-    const uint32_t w = q < 2 ? v.x : v.y;
-    return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
-}
-__device__ __forceinline__ float f4_at(float4 v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
-__device__ __forceinline__ uint2 lds_u2(const uint16_t *p) { return *reinterpret_cast<const uint2 *>(p); }
 
 __device__ __forceinline__ uint32_t logit_key(float f)
 {
@@ -210,6 +212,17 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p)
     return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Bounded poll until *p >= target: one poll, then at most limit - 1 more, spaced by a short sleep.
 __device__ __noinline__ bool poll_geq(const int *p, int target, long long limit)
 {
@@ -221,6 +234,7 @@ __device__ __noinline__ bool poll_geq(const int *p, int target, long long limit)
     return false;
 }
 
+// Called by whole warps; thread 0 writes the stamp and the warp is brought back together.
 __device__ __forceinline__ void stamp(const FusedDecodeArgs &a, int i)
 {
     if (a.trace && threadIdx.x == 0) {
@@ -228,15 +242,23 @@ __device__ __forceinline__ void stamp(const FusedDecodeArgs &a, int i)
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
         a.trace[(size_t)blockIdx.x * kTraceStamps + i] = t;
     }
+    __syncwarp();
 }
 
-// Named barrier 1 over the 256 consumer threads, and the same barrier ORing a predicate.
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Named barrier 1 over the 256 consumer threads, and the same barrier ORing a predicate.  The
+// non-aligned forms: a warp may reach them with its lanes apart (after a branch taken by lane 0
+// only), and each warp is brought back together first as well.
+__device__ __forceinline__ void consumer_bar()
+{
+    __syncwarp();
+    asm volatile("barrier.sync 1, 256;" ::: "memory");
+}
 __device__ __forceinline__ bool consumer_any(bool pred)
 {
+    __syncwarp();
     uint32_t r;
     asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)pred)
         : "memory");
@@ -254,9 +276,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, long l
 //
 // Top-k of every token from the fp32 logits (one warp per token: lane l holds the keys of
 // experts l + 32 r; each round takes the largest key, then the lowest id holding it), or the
-// caller's ids; then the distinct experts (increasing id, the shared expert last) and the
-// columns: the (t, j) slots of each expert in increasing t k + j, then the shared slots.
-__device__ __noinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, const float *logits)
+// caller's ids.  Then, in parallel over the picks, a bitmap of the picked experts and per expert
+// the set of tokens that picked it; from those the distinct experts in increasing id (the shared
+// expert last), each expert's column count, and the column of pick (t, j): the expert's first
+// column plus the number of earlier tokens that picked the same expert.
+// logits: the caller's fp32 logits, or null for the logits this launch publishes (tagged with its epoch).
+__device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, const float *logits)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, E = a.E, k = a.k;
@@ -269,17 +294,54 @@ __device__ __noinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, 
                 e = 0;
             }
             S.ids[i / k][i % k] = e;
-            atomicAdd(&S.cnt[e], 1);
         }
     } else {
         constexpr int RW = kMaxExperts / 32;
 #pragma unroll 1
         for (int t = warp; t < T; t += kThreads / 32) {
             uint32_t key[RW];
+            if (logits) {
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                const int e = lane + 32 * r;
-                key[r] = e < E ? logit_key(__ldcg(logits + (size_t)t * E + e)) : 0u;   // 0: below every logit
+                for (int r = 0; r < RW; ++r) {
+                    const int e = lane + 32 * r;
+                    key[r] = e < E ? logit_key(__ldcg(logits + (size_t)t * E + e)) : 0u;   // 0: below every logit
+                }
+            } else {
+                // logits published by the CTAs of this launch, each tagged with the launch's epoch: poll
+                // the row until every entry carries it (bounded)
+                const unsigned long long *row = a.logits64 + (size_t)t * E;
+                uint32_t pend = 0;
+#pragma unroll
+                for (int r = 0; r < RW; ++r) {
+                    const int e = lane + 32 * r;
+                    key[r] = 0u;
+                    if (e < E) {
+                        const unsigned long long v = ld_relaxed_u64(row + e);
+                        if ((uint32_t)(v >> 32) == S.epoch) key[r] = logit_key(__uint_as_float((uint32_t)v));
+                        else pend |= 1u << r;
+                    }
+                }
+                long long polls = 1;
+                while (__any_sync(0xffffffffu, pend != 0)) {
+                    if (polls++ >= a.wait_limit) {
+                        if (lane == 0) {
+                            S.abort = 1;
+                            record_status(a.status, MOE_ERR_TIMEOUT);
+                        }
+                        break;
+                    }
+                    __nanosleep(32);
+#pragma unroll
+                    for (int r = 0; r < RW; ++r)
+                        if (pend & (1u << r)) {
+                            const unsigned long long v = ld_relaxed_u64(row + lane + 32 * r);
+                            if ((uint32_t)(v >> 32) == S.epoch) {
+                                key[r] = logit_key(__uint_as_float((uint32_t)v));
+                                pend &= ~(1u << r);
+                            }
+                        }
+                }
+                if (t == 0) stamp(a, kStLogitsSeen);
             }
 #pragma unroll 1
             for (int j = 0; j < k; ++j) {
@@ -300,77 +362,65 @@ __device__ __noinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, 
                         if (r == br) key[r] = 0u;
                     S.ids[t][j] = (int)id;
                     S.lg[t][j] = key_logit(mk);
-                    atomicAdd(&S.cnt[id], 1);
                 }
             }
         }
     }
+    if (a.ids_in || logits) stamp(a, kStLogitsSeen);
     __syncthreads();
     stamp(a, kStTopk);
-    if (warp == 0) {
-        const int per = (E + 31) / 32, b0 = lane * per, b1 = min(E, b0 + per);
-        int nloc = 0, cloc = 0;
 #pragma unroll 1
-        for (int e = b0; e < b1; ++e) {
-            nloc += S.cnt[e] > 0;
-            cloc += S.cnt[e];
-        }
-        int ni = nloc, ci = cloc;
+    for (int i = tid; i < T * k; i += kThreads) {
+        const int t = i / k, e = S.ids[t][i - t * k];
+        atomicOr(&S.pickmap[e >> 5], 1u << (e & 31));
+        if (atomicOr(&S.tokmask[e], 1u << t) & (1u << t)) record_status(a.status, MOE_ERR_DEVICE);   // repeated id
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // lane l scans the experts [32 l, 32 l + 32): list positions and first columns by two scans
+        const uint32_t bits = lane < (E + 31) / 32 ? S.pickmap[lane] : 0u;
+        int ncol = 0;
+        for (uint32_t b = bits; b; b &= b - 1) ncol += __popc(S.tokmask[32 * lane + __ffs(b) - 1]);
+        int np = __popc(bits), nc = ncol;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int vn = __shfl_up_sync(0xffffffffu, ni, o), vc = __shfl_up_sync(0xffffffffu, ci, o);
+            const int vp = __shfl_up_sync(0xffffffffu, np, o), vc = __shfl_up_sync(0xffffffffu, nc, o);
             if (lane >= o) {
-                ni += vn;
-                ci += vc;
+                np += vp;
+                nc += vc;
             }
         }
-        int pos = ni - nloc, col = ci - cloc;
-#pragma unroll 1
-        for (int e = b0; e < b1; ++e) {
-            const int c = S.cnt[e];
-            if (c > 0) {
-                if (c > T) record_status(a.status, MOE_ERR_DEVICE);   // an id repeated within a token
-                S.list[pos] = e;
-                S.lpos[e] = pos;
-                S.ncols[pos] = c;
-                S.colptr[pos] = col;
-                ++pos;
-                col += c;
-            }
+        int pos = np - __popc(bits), col = nc - ncol;
+        for (uint32_t b = bits; b; b &= b - 1) {
+            const int e = 32 * lane + __ffs(b) - 1, c = __popc(S.tokmask[e]);
+            S.list[pos] = e;
+            S.lpos[e] = pos;
+            S.ncols[pos] = c;
+            S.colptr[pos] = col;
+            ++pos;
+            col += c;
         }
         if (lane == 31) {
-            int D = ni;
+            int D = np;
             if (a.has_shared) {
                 S.list[D] = E;
                 S.ncols[D] = T;
-                S.colptr[D] = ci;
+                S.colptr[D] = nc;
                 ++D;
             }
-            S.colptr[D] = ci + (a.has_shared ? T : 0);
+            S.colptr[D] = nc + (a.has_shared ? T : 0);
             S.nlist = D;
         }
     }
     __syncthreads();
     stamp(a, kStListed);
-    // columns: the routed slots of each expert in increasing t (one warp, token after token; a
-    // token's k picks are distinct experts, so its lanes never share a list entry)
-    if (warp == 0) {
 #pragma unroll 1
-        for (int d = lane; d < S.nlist; d += 32) S.fill[d] = 0;
-        __syncwarp();
-#pragma unroll 1
-        for (int t = 0; t < T; ++t) {
-            const int e = lane < k ? S.ids[t][lane] : -1 - lane;
-            if (__popc(__match_any_sync(0xffffffffu, e)) > 1) record_status(a.status, MOE_ERR_DEVICE);
-            if (lane < k) {
-                const int d = S.lpos[e];
-                const int col = S.colptr[d] + atomicAdd(&S.fill[d], 1);
-                S.colof[t][lane] = col;
-                S.colf[col] = t * k + lane;
-                S.ctok[col] = t;
-            }
-            __syncwarp();
-        }
+    for (int i = tid; i < T * k; i += kThreads) {
+        const int t = i / k, j = i - t * k, e = S.ids[t][j];
+        const int col = S.colptr[S.lpos[e]] + __popc(S.tokmask[e] & ((1u << t) - 1u));
+        S.colof[t][j] = col;
+        S.colf[col] = i;
+        S.ctok[col] = t;
     }
     if (a.has_shared)
 #pragma unroll 1
@@ -386,9 +436,11 @@ __device__ __noinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, 
 // ------------------------------------------------------------------ per-token weights (aux warp)
 //
 // Token t = grid - 1 - blockIdx: gamma = x . v in fp32 (lane l sums the groups l, l + 32, ...
-// element by element, then a fixed shuffle tree), w_s = bf16(sigmoid(bf16(gamma))) and
-// p_j = bf16(exp(l_j - l_0) / sum_i exp(l_i - l_0)) in fp64, published for the combining CTAs.
-__device__ __noinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a, const uint16_t *s_x)
+// element by element in natural order, then a fixed shuffle tree: the router kernel's operations;
+// on x' = x 2^-e every product and partial sum is the unscaled one times 2^-e, exactly), w_s =
+// bf16(sigmoid(bf16(gamma))) and p_j = bf16(exp(l_j - l_0) / sum_i exp(l_i - l_0)) in fp64,
+// published for the combining CTAs.
+__device__ __forceinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a, const uint16_t *s_x)
 {
     const int lane = threadIdx.x & 31, T = a.T, k = a.k, G = a.H / kGroup;
     const int t = (int)gridDim.x - 1 - (int)blockIdx.x;
@@ -440,15 +492,16 @@ __device__ __noinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a, c
 //
 // Gate and up chunks: lane 0 waits for the slot, then one 3D TMA copy brings the 32 code rows (each
 // 128-byte box in the 128-byte swizzle) and two bulk copies their scales and biases; the other
-// lanes arrive.  Down chunk: the slice's 16-byte column of all H rows, which TMA moves one narrow
-// row at a time; here the 32 lanes take the rows in turn with 16-byte cp.async and each arrives
-// (without a count increment) once its own copies have landed.
+// lanes arrive.  Down chunk: the slice's 16-byte column of all H rows.  From the packed layout it
+// is one contiguous block (one bulk copy); from the MLX layout it is 16 bytes of every 256-byte
+// row, which the 32 lanes take in turn with 16-byte cp.async, each arriving (without a count
+// increment) once its own copies have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __noinline__ void fused_producer(FSmem &S, const FusedMaps &maps, const FusedDecodeArgs &a,
+__device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, const FusedDecodeArgs &a,
                                             const FusedGeom &geo, uint8_t *ring, int U)
 {
     const int lane = threadIdx.x & 31;
@@ -456,10 +509,11 @@ __device__ __noinline__ void fused_producer(FSmem &S, const FusedMaps &maps, con
     const int H = a.H, I = a.I, E = a.E, G = H / kGroup, SL = I / kSlice, R = geo.R;
     const uint32_t slot_bytes = geo.slot, codes1 = geo.codes1, sc1 = geo.sc1;
     const size_t drow = (size_t)I / 2;
-    const long long limit = a.wait_limit;
+    const long long limit = kRingLimit;
     const uint16_t *gsc = a.gate.scales, *gbi = a.gate.biases, *usc = a.up.scales, *ubi = a.up.biases;
     const uint16_t *sgsc = a.s_gate.scales, *sgbi = a.s_gate.biases, *susc = a.s_up.scales, *subi = a.s_up.biases;
     const uint8_t *dcodes = a.down.codes, *sdcodes = a.s_down.codes;
+    const uint8_t *packed = a.down_packed, *spacked = a.s_down_packed;
     const CUtensorMap *mg = &maps.g, *mu = &maps.u, *msg = &maps.sg, *msu = &maps.su;
     int issued = 0;
     bool stop = false;
@@ -467,6 +521,13 @@ __device__ __noinline__ void fused_producer(FSmem &S, const FusedMaps &maps, con
     for (int u = blockIdx.x, i = 0; u < U && !stop; u += gridDim.x, ++i) {
         const int d = u / SL, s = u - d * SL, e = S.list[d];
         const bool shr = e == E;
+        if (e < 0 || e > E || d >= S.nlist) {           // a list entry out of range: report, issue nothing
+            if (lane == 0) {
+                S.abort = 1;
+                record_status(a.status, MOE_ERR_DEVICE);
+            }
+            break;
+        }
 #pragma unroll 1
         for (int c = 0; c < 3; ++c) {
             const int q = 3 * i + c, slot = q % R;
@@ -484,9 +545,11 @@ __device__ __noinline__ void fused_producer(FSmem &S, const FusedMaps &maps, con
             }
             uint8_t *base = ring + (size_t)slot * slot_bytes;
             const uint32_t fb = smem_u32(&S.full[slot]);
+            const int row0 = (shr ? 0 : e * I) + s * kSlice;
             if (c < 2) {
+                // gate or up chunk: one 3D copy of the 32 code rows (each 128-byte box in the 128-byte
+                // swizzle) and two bulk copies of their scales and biases
                 if (lane == 0) {
-                    const int row0 = (shr ? 0 : e * I) + s * kSlice;
                     const size_t so = (size_t)row0 * G;
                     const uint16_t *sc = c == 0 ? (shr ? sgsc : gsc) : (shr ? susc : usc);
                     const uint16_t *bi = c == 0 ? (shr ? sgbi : gbi) : (shr ? subi : ubi);
@@ -494,6 +557,15 @@ __device__ __noinline__ void fused_producer(FSmem &S, const FusedMaps &maps, con
                     tma_load_3d(smem_u32(base), c == 0 ? (shr ? msg : mg) : (shr ? msu : mu), 0, row0, 0, fb);
                     bulk_load(smem_u32(base + codes1), sc + so, sc1, fb);
                     bulk_load(smem_u32(base + codes1 + sc1), bi + so, sc1, fb);
+                } else {
+                    mbar_arrive(fb);
+                }
+            } else if (packed != nullptr && (!shr || spacked != nullptr)) {
+                // the slice's down codes are one contiguous block of the packed layout: one bulk copy
+                if (lane == 0) {
+                    const uint8_t *src = shr ? spacked + (size_t)s * H * 16 : packed + ((size_t)e * SL + s) * H * 16;
+                    mbar_arrive_expect_tx(fb, (uint32_t)H * 16);
+                    bulk_load(smem_u32(base), src, (uint32_t)H * 16, fb);
                 } else {
                     mbar_arrive(fb);
                 }
@@ -516,11 +588,63 @@ __device__ __noinline__ void fused_producer(FSmem &S, const FusedMaps &maps, con
     __syncwarp();
 }
 
+// x' for the MMAs from the raw staged rows, one warp per token (every warp of the CTA): lane l takes
+// the row's 16-byte chunks l, l + 32, ..., the warp finds the row's largest |x|, scales by 2^-e
+// (exact), puts each chunk of 8 in the codes' k order and sums each group of 64 (its 8 chunks sit
+// in 8 consecutive lanes: a fixed shuffle tree).
+__device__ __forceinline__ void convert_x(FSmem &S, const FusedDecodeArgs &a, const uint16_t *s_xr, uint16_t *s_x,
+                                          float *s_xs)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, T = a.T, H = a.H, G = H / kGroup, XS = G * kXG + 8;
+    {
+        constexpr int kMaxChunks = 2048 / 8 / 32;          // chunks per lane at the largest H
+        const int cpl = H / 256;                            // chunks per lane
+#pragma unroll 1
+        for (int t = warp; t < T; t += kThreads / 32) {
+            uint4 v[kMaxChunks];
+            uint32_t mx = 0;
+#pragma unroll
+            for (int i = 0; i < kMaxChunks; ++i)
+                if (i < cpl) {
+                    const int c = lane + 32 * i;
+                    v[i] = *reinterpret_cast<const uint4 *>(s_xr + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8);
+                    const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7FFFu, w4[q] >> 16 & 0x7FFFu));
+                }
+            mx = __reduce_max_sync(0xffffffffu, mx);
+            const int ef = (int)(mx >> 7), xe = ef == 0 ? -126 : ef - 127;
+            const float sc = pow2f(-xe);
+#pragma unroll
+            for (int i = 0; i < kMaxChunks; ++i)
+                if (i < cpl) {
+                    const int c = lane + 32 * i;                // chunk of the row; its group is c / 8
+                    uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                    float sum = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float lo = __uint_as_float(w[q] << 16) * sc, hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
+                        w[q] = (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
+                        sum += __uint_as_float(w[q] << 16);
+                        sum += __uint_as_float(w[q] & 0xFFFF0000u);
+                    }
+                    *reinterpret_cast<uint4 *>(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8) =
+                        kperm8(make_uint4(w[0], w[1], w[2], w[3]));
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                    if ((c & 7) == 0) s_xs[t * G + (c >> 3)] = sum;
+                }
+            if (lane == 0) S.xe[t] = xe;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ consumers (warps 0-7)
 //
-// Gate/up chunk: warp w takes matrix m = w / 4 (gate, up), 16-row tile mt = (w / 2) % 2 and the
-// groups of parity kh = w % 2, with every group's product s (sum (128 + q) x') + (b - 128 s) sum x'
-// added in increasing group order; the two parities are added in h = silu(g) u.  Down chunk:
+// Gate and up chunks: warp w takes the 16-row tile mt = w % 2 and quarter kq = w / 2 of the groups of
+// both matrices, with every group's product s (sum (128 + q) x') + (b - 128 s) sum x' added in
+// increasing group order; the four quarters are added in order in h = silu(g) u.  Down chunk:
 // warp w takes H / 128 tiles of 16 rows, K = 32 (the slice), raw sums P = sum (q - 8) h'.  The
 // down codes enter the MMA signed: with 1024 + q the sum would be ~1024 sum h' and cancel about
 // eight bits against the bias term, beyond what the tensor cores' fp32 accumulation keeps.
@@ -532,8 +656,8 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
     constexpr int NC = NT * 8;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     const int T = a.T, H = a.H, I = a.I, G = H / kGroup, SL = I / kSlice, R = geo.R;
-    const int m = warp >> 2, mt = (warp >> 1) & 1, kh = warp & 1, nbx = G / 4, XS = G * kXG + 8;
-    const long long limit = a.wait_limit;
+    const int mt = warp & 1, kq = warp >> 1, gq = G / 4, XS = G * kXG + 8;
+    const long long limit = kRingLimit;
     float *const part = a.part;
     float *const hsum = a.hsum;
     bool fail_d = false;
@@ -541,47 +665,41 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
     for (int u = blockIdx.x, i = 0; u < U; u += gridDim.x, ++i) {
         const int d = u / SL, s = u - d * SL;
         const int ncol = min(S.ncols[d], T), colbase = S.colptr[d];
-        const int q1 = 3 * i + m, slot1 = q1 % R, slot_o = (3 * i + 1 - m) % R;
-        bool ok = !fail_d && warp_wait(&S.full[slot1], (q1 / R) & 1, limit, &S.abort);
-        if (i == 0) stamp(a, kStFirstGate);
-        if (ok) {
-            const uint8_t *chunk = ring + (size_t)slot1 * geo.slot;
-            const uint8_t *cb = chunk + (mt * 16 + g) * 128;              // row mt 16 + g of every 4 KB box
-            const uint16_t *scs = reinterpret_cast<const uint16_t *>(chunk + geo.codes1) + (mt * 16 + g) * G;
-            const uint16_t *bis = scs + kSlice * G;
-            int xrow[NT], tA[NT], tB[NT];
+        int xrow[NT], tA[NT], tB[NT];
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const int c = j * 8 + g, cA = j * 8 + 2 * t4;
-                xrow[j] = c < ncol ? S.ctok[colbase + c] : -1;
-                tA[j] = cA < ncol ? S.ctok[colbase + cA] : -1;
-                tB[j] = cA + 1 < ncol ? S.ctok[colbase + cA + 1] : -1;
-            }
-            float acc[NT][4];
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int v = 0; v < 4; ++v) acc[j][v] = 0.f;
+        for (int j = 0; j < NT; ++j) {
+            const int c = j * 8 + g, cA = j * 8 + 2 * t4;
+            xrow[j] = c < ncol ? S.ctok[colbase + c] : -1;
+            tA[j] = cA < ncol ? S.ctok[colbase + cA] : -1;
+            tB[j] = cA + 1 < ncol ? S.ctok[colbase + cA + 1] : -1;
+        }
+        // the gate chunk, then the up chunk, each computed by all eight warps: warp w takes the 16-row
+        // tile mt = w % 2 and the groups of quarter kq = w / 2 of the input dimension
+        bool ok = !fail_d;
 #pragma unroll 1
-            for (int bx = 0; bx < nbx; ++bx) {
-                const uint2 vs0 = lds_u2(scs + 4 * bx), vs1 = lds_u2(scs + 8 * G + 4 * bx);
-                const uint2 vb0 = lds_u2(bis + 4 * bx), vb1 = lds_u2(bis + 8 * G + 4 * bx);
-                float4 sxA[NT], sxB[NT];
+        for (int m = 0; m < 2; ++m) {
+            const int q1 = 3 * i + m, slot1 = q1 % R;
+            ok = ok && warp_wait(&S.full[slot1], (q1 / R) & 1, limit, &S.abort);
+            if (i == 0 && m == 0) stamp(a, kStFirstGate);
+            if (ok) {
+                const uint8_t *chunk = ring + (size_t)slot1 * geo.slot;
+                const uint8_t *cb = chunk + (mt * 16 + g) * 128;              // row mt 16 + g of every 4 KB box
+                const uint16_t *scs = reinterpret_cast<const uint16_t *>(chunk + geo.codes1) + (mt * 16 + g) * G;
+                const uint16_t *bis = scs + kSlice * G;
+                float acc[NT][4];
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                    sxA[j] = tA[j] >= 0 ? *reinterpret_cast<const float4 *>(s_xs + tA[j] * G + 4 * bx) : z;
-                    sxB[j] = tB[j] >= 0 ? *reinterpret_cast<const float4 *>(s_xs + tB[j] * G + 4 * bx) : z;
-                }
+                for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    const int q = kh + 2 * qq, grp = 4 * bx + q;
-                    const uint32_t o = (uint32_t)bx * (kSlice * 128) + swz_chunk(q, g, t4);
+                    for (int v = 0; v < 4; ++v) acc[j][v] = 0.f;
+#pragma unroll 2
+                for (int gi = 0; gi < gq; ++gi) {
+                    const int grp = kq * gq + gi, q = grp & 3;
+                    const uint32_t o = (uint32_t)(grp >> 2) * (kSlice * 128) + swz_chunk(q, g, t4);
                     const uint2 c0 = *reinterpret_cast<const uint2 *>(cb + o);
                     const uint2 c1 = *reinterpret_cast<const uint2 *>(cb + o + 1024);
-                    const float s0 = bf16x4_at(vs0, q), s1 = bf16x4_at(vs1, q);
-                    const float k0 = fmaf(-128.f, s0, bf16x4_at(vb0, q));
-                    const float k1 = fmaf(-128.f, s1, bf16x4_at(vb1, q));
+                    const float s0 = bf16_bits_to_float(scs[grp]), s1 = bf16_bits_to_float(scs[8 * G + grp]);
+                    const float k0 = fmaf(-128.f, s0, bf16_bits_to_float(bis[grp]));
+                    const float k1 = fmaf(-128.f, s1, bf16_bits_to_float(bis[8 * G + grp]));
                     uint32_t a0[8], a1[8];
                     nib8<false>(c0.x, a0);
                     nib8<false>(c0.y, a0 + 4);
@@ -603,32 +721,28 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                         for (int mm = 0; mm < 4; ++mm)
                             mma16816<false>(dd, a0[2 * mm], a1[2 * mm], a0[2 * mm + 1], a1[2 * mm + 1], bp[2 * mm],
                                             bp[2 * mm + 1]);
-                        const float xA = f4_at(sxA[j], q), xB = f4_at(sxB[j], q);
+                        const float xA = tA[j] >= 0 ? s_xs[tA[j] * G + grp] : 0.f;
+                        const float xB = tB[j] >= 0 ? s_xs[tB[j] * G + grp] : 0.f;
                         acc[j][0] = fmaf(s0, dd[0], fmaf(k0, xA, acc[j][0]));
                         acc[j][1] = fmaf(s0, dd[1], fmaf(k0, xB, acc[j][1]));
                         acc[j][2] = fmaf(s1, dd[2], fmaf(k1, xA, acc[j][2]));
                         acc[j][3] = fmaf(s1, dd[3], fmaf(k1, xB, acc[j][3]));
                     }
                 }
-            }
-            float *red = s_red + ((size_t)(m * 2 + kh) * kSlice + mt * 16) * NC;   // [32 rows][NC]
+                float *red = s_red + ((size_t)(m * 4 + kq) * kSlice + mt * 16) * NC;   // [32 rows][NC]
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const int c0 = j * 8 + 2 * t4;
-                red[g * NC + c0] = acc[j][0];
-                red[g * NC + c0 + 1] = acc[j][1];
-                red[(g + 8) * NC + c0] = acc[j][2];
-                red[(g + 8) * NC + c0 + 1] = acc[j][3];
+                for (int j = 0; j < NT; ++j) {
+                    const int c0 = j * 8 + 2 * t4;
+                    red[g * NC + c0] = acc[j][0];
+                    red[g * NC + c0 + 1] = acc[j][1];
+                    red[(g + 8) * NC + c0] = acc[j][2];
+                    red[(g + 8) * NC + c0 + 1] = acc[j][3];
+                }
             }
-        }
-        // A warp releases the chunk it reads only once that chunk has landed (its wait succeeded):
-        // otherwise the producer could issue the next copy into a slot whose copy is still in
-        // flight.  The other matrix's chunk it never reads, so it releases that one at once; the
-        // slot's phase still needs the arrivals of the warps that read it.
-        __syncwarp();
-        if (lane == 0) {
-            if (ok) mbar_arrive(smem_u32(&S.empty[slot1]));
-            mbar_arrive(smem_u32(&S.empty[slot_o]));
+            // a warp releases a chunk only once it has landed (its wait succeeded): otherwise the
+            // producer could issue the next copy into a slot whose copy is still in flight
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(smem_u32(&S.empty[slot1]));
         }
         if (!ok && lane == 0) {
             S.abort = 1;
@@ -640,8 +754,12 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
 #pragma unroll 1
         for (int c = warp; c < ncol; c += kCW) {
             const int row = lane;
-            const float gs = s_red[((0 * 2 + 0) * kSlice + row) * NC + c] + s_red[((0 * 2 + 1) * kSlice + row) * NC + c];
-            const float us = s_red[((1 * 2 + 0) * kSlice + row) * NC + c] + s_red[((1 * 2 + 1) * kSlice + row) * NC + c];
+            float gs = s_red[((0 * 4 + 0) * kSlice + row) * NC + c], us = s_red[((4 + 0) * kSlice + row) * NC + c];
+#pragma unroll
+            for (int v = 1; v < 4; ++v) {
+                gs += s_red[((0 * 4 + v) * kSlice + row) * NC + c];
+                us += s_red[((4 + v) * kSlice + row) * NC + c];
+            }
             const int t = S.ctok[colbase + c];
             const float hv = gs / (1.f + __expf(-gs * pow2f(S.xe[t]))) * us;
             const __half hb = __float2half_rn(hv);
@@ -679,7 +797,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             }
             const int MT = H / (16 * kCW);
             float *pbase = part + (size_t)colbase * SL * H + (size_t)s * H;
-#pragma unroll 2
+#pragma unroll 1
             for (int tt = 0; tt < MT; ++tt) {
                 const int r0 = (warp * MT + tt) * 16 + g;
                 const uint32_t w0 = *reinterpret_cast<const uint32_t *>(dch + r0 * 16 + 4 * t4);
@@ -708,6 +826,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             }
         }
         __syncwarp();
+        if (i == 0) stamp(a, kStFirstDownDone);
         if (lane == 0 && okd) mbar_arrive(smem_u32(&S.empty[slot2]));
         if (!okd && lane == 0) {
             S.abort = 1;
@@ -723,14 +842,17 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
 // expert output y_e = 2^(2e) sum over groups, in order, of s (P_{2g} + P_{2g+1}) + (b + 8 s)
 // (Hs_{2g} + Hs_{2g+1}); then per (token, 4 rows): y = sum_j p_j y_ej + w_s y_s in slot order, one
 // rounding (or added to acc).  An item's loads are all issued before its first add.
-__device__ __noinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a, const FusedGeom &geo, float4 *s_t)
+__device__ __forceinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a, const FusedGeom &geo, float4 *s_t)
 {
     const int tid = threadIdx.x;
     const int T = a.T, H = a.H, I = a.I, k = a.k, GI = I / kGroup, SL = I / kSlice;
     const int NS = k + (a.has_shared ? 1 : 0);
     const int r0 = (int)blockIdx.x * geo.RB;
     const int nrows = min(geo.RB, H - r0);
-    if (nrows <= 0) return;
+    if (nrows <= 0) {
+        stamp(a, kStCombineLoads);
+        return;
+    }
     const int nq = nrows / 4;
 #pragma unroll 1
     for (int i = tid; i < T * k; i += kThreads)
@@ -749,6 +871,11 @@ __device__ __noinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a, c
         const int e = shr ? 0 : S.ids[t][j];
         const int col = S.colof[t][j];
         const int r = r0 + 4 * q;
+        if (e < 0 || e >= a.E || col < 0 || col >= S.colptr[S.nlist]) {   // out of range: report, skip
+            record_status(a.status, MOE_ERR_DEVICE);
+            s_t[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+        }
         const QMatDev &dm = shr ? a.s_down : a.down;
         const uint16_t *sp = dm.scales + ((size_t)e * H + r) * GI;
         const uint16_t *bp = dm.biases + ((size_t)e * H + r) * GI;
@@ -809,6 +936,7 @@ __device__ __noinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a, c
         }
     }
     __syncthreads();
+    stamp(a, kStCombineLoads);
     if (a.stages_only) return;
 #pragma unroll 1
     for (int it = tid; it < T * nq; it += kThreads) {
@@ -840,22 +968,28 @@ __device__ __noinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a, c
 }
 
 // Asks L2 for the down scale and bias rows this CTA combines, for every listed expert (they are
-// read after the unit counter, on the critical path).
-__device__ __noinline__ void prefetch_combine_scales(const FSmem &S, const FusedDecodeArgs &a, const FusedGeom &geo)
+// read after the unit counter, on the critical path).  Per-thread line prefetches, not bulk ones:
+// a CTA that stops early (a wait ran out) leaves soon after this, and a bulk prefetch has no
+// completion the CTA could wait for, so none may still sit in the copy engine when it exits.
+__device__ __forceinline__ void prefetch_combine_scales(const FSmem &S, const FusedDecodeArgs &a, const FusedGeom &geo)
 {
     const int lane = threadIdx.x & 31, H = a.H, E = a.E, GI = a.I / kGroup;
     const int r0 = (int)blockIdx.x * geo.RB, nrows = min(geo.RB, H - r0);
-    const uint32_t bytes = (uint32_t)nrows * GI * 2;
-    if (nrows <= 0 || (bytes & 15u)) return;
+    if (nrows <= 0) return;
+    const int bytes = nrows * GI * 2, nlines = (bytes + 127) / 128;
 #pragma unroll 1
     for (int d = lane; d < S.nlist; d += 32) {
         const int e = S.list[d];
         const bool shr = e == E;
         const QMatDev &dm = shr ? a.s_down : a.down;
         const size_t o = ((size_t)(shr ? 0 : e) * H + r0) * GI;
-        if (((reinterpret_cast<uintptr_t>(dm.scales + o) | reinterpret_cast<uintptr_t>(dm.biases + o)) & 15u) == 0) {
-            prefetch_l2_bulk(dm.scales + o, bytes);
-            prefetch_l2_bulk(dm.biases + o, bytes);
+        const uint8_t *sp = reinterpret_cast<const uint8_t *>(dm.scales + o);
+        const uint8_t *bp = reinterpret_cast<const uint8_t *>(dm.biases + o);
+#pragma unroll 1
+        for (int l = 0; l < nlines; ++l) {
+            const int off = min(l * 128, bytes - 1);
+            prefetch_l2_line(sp + off);
+            prefetch_l2_line(bp + off);
         }
     }
 }
@@ -872,7 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *ring = dyn;
     uint16_t *s_x = reinterpret_cast<uint16_t *>(dyn + geo.x_off);    // [T][G * 72 + 8] bf16 x', k order
     float *s_xs = reinterpret_cast<float *>(dyn + geo.xs_off);         // [T][G] group sums of x'
-    float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);       // [2][2][32][NC]
+    float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);       // [2][4][32][NC]
     uint16_t *s_h = reinterpret_cast<uint16_t *>(dyn + geo.h_off);     // [NC][32] fp16 h', k order
     float *s_hs = reinterpret_cast<float *>(dyn + geo.hs_off);         // [NC]
 
@@ -880,8 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int T = a.T, H = a.H, E = a.E, G = H / kGroup, SL = a.I / kSlice;
     const int grid = gridDim.x, cta = blockIdx.x;
     const long long limit = a.wait_limit;
-    int *const cnt_router = a.sync + kSyncRouter, *const cnt_units = a.sync + kSyncUnits;
-    int *const cnt_exit = a.sync + kSyncExit;
+    int *const cnt_units = a.sync + kSyncUnits, *const cnt_exit = a.sync + kSyncExit;
     stamp(a, kStStart);
 
     if (tid == 0) {
@@ -893,8 +1026,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
 #pragma unroll 1
-    for (int e = tid; e < kMaxList; e += kThreads) S.cnt[e] = 0;
-    if (tid < kDecodeMaxTok) S.xmax[tid] = 0;
+    for (int e = tid; e < kMaxExperts; e += kThreads) S.tokmask[e] = 0u;
+    if (tid < kMaxExperts / 32) S.pickmap[tid] = 0u;
 
     // this CTA's router rows (weights only: read before the wait for the preceding kernel)
     const bool router = a.ids_in == nullptr && a.logits_in == nullptr;
@@ -927,69 +1060,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    __syncthreads();       // barrier inits and zeroed counts visible
-    // ---- x (written by the preceding kernel) into shared memory: the raw chunks are copied into the
-    // padded layout, each token's largest |x| is found, then a pass scales by 2^-e (exact), puts each
-    // chunk of 8 in the codes' k order and sums each group of 64 (its 8 chunks sit in 8 consecutive
-    // lanes: a fixed shuffle tree)
+    // ---- everything below reads what the preceding kernel wrote (x, the workspace header).  Raw x
+    // goes into the ring area (idle until the units start) with its groups of 64 padded to 72
+    // elements, so that lanes reading different groups meet in no shared-memory bank.
     pdl_wait();
     const int XS = G * kXG + 8;
-    const int cpr = H / 8;
+    uint16_t *s_xr = reinterpret_cast<uint16_t *>(ring);        // [T][XS] bf16 x, natural order
+    {
+        const int cpr = H / 8;
 #pragma unroll 1
-    for (int i = tid; i < T * cpr; i += kThreads) {
-        const int t = i / cpr, c = i - t * cpr;
-        cp_async16(smem_u32(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8), reinterpret_cast<const uint4 *>(a.x) + i);
+        for (int i = tid; i < T * cpr; i += kThreads) {
+            const int t = i / cpr, c = i - t * cpr;
+            cp_async16(smem_u32(s_xr + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8),
+                       reinterpret_cast<const uint4 *>(a.x) + i);
+        }
+        cp_async_commit();
     }
-    cp_async_commit();
+    uint32_t epoch = 0;
+    if (lane == 0) epoch = (uint32_t)ld_acquire_gpu(a.sync + kSyncEpoch) + 1u;   // in flight with x
+    if (tid == 0) S.epoch = epoch;
     cp_async_wait_all();
     __syncthreads();
-    // a warp's 32 chunks of one pass belong to one token (H / 8 is a multiple of 32): one atomic per warp
-#pragma unroll 1
-    for (int i = tid; i < T * cpr; i += kThreads) {
-        const int t = i / cpr, c = i - t * cpr;
-        const uint4 v = *reinterpret_cast<const uint4 *>(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8);
-        const uint32_t m0 = max(max(v.x & 0x7FFFu, v.x >> 16 & 0x7FFFu), max(v.y & 0x7FFFu, v.y >> 16 & 0x7FFFu));
-        const uint32_t m1 = max(max(v.z & 0x7FFFu, v.z >> 16 & 0x7FFFu), max(v.w & 0x7FFFu, v.w >> 16 & 0x7FFFu));
-        const uint32_t mw = __reduce_max_sync(__activemask(), max(m0, m1));
-        if ((i & 31) == 0) atomicMax(&S.xmax[t], (int)mw);
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int i = tid; i < T * cpr; i += kThreads) {
-        const int t = i / cpr, c = i - t * cpr;
-        const int ef = S.xmax[t] >> 7, xe = ef == 0 ? -126 : ef - 127;
-        const float sc = pow2f(-xe);
-        uint4 *px = reinterpret_cast<uint4 *>(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8);
-        const uint4 v = *px;
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float sum = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float lo = __uint_as_float(w[q] << 16) * sc, hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
-            w[q] = (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
-            sum += __uint_as_float(w[q] << 16);
-            sum += __uint_as_float(w[q] & 0xFFFF0000u);
-        }
-        *px = kperm8(make_uint4(w[0], w[1], w[2], w[3]));
-        const unsigned gm = 0xFFu << (lane & 24);          // the 8 lanes holding this group's chunks
-        sum += __shfl_xor_sync(gm, sum, 1);
-        sum += __shfl_xor_sync(gm, sum, 2);
-        sum += __shfl_xor_sync(gm, sum, 4);
-        if ((c & 7) == 0) s_xs[t * G + (c >> 3)] = sum;
-        if (c == 0) S.xe[t] = xe;
-    }
-    __syncthreads();
-    stamp(a, kStXStaged);
 
     // ---- router logits of this CTA's experts: per group s sum q x + b sum x in fp32, elements in
-    // order, then a fixed shuffle tree (the same operations as the router kernel, on x' = x 2^-e,
-    // which scales every intermediate exactly); then the grid-wide counter
+    // order, then a fixed shuffle tree (the operations of the router kernel, on the same unscaled x),
+    // published as (logit, epoch) pairs that the other CTAs poll
     if (er >= 0) {
 #pragma unroll 1
         for (int t = rt0; t < T; t += rstep) {
             float prt = 0.f;
             if (lane < G) {
-                const uint4 *xr = reinterpret_cast<const uint4 *>(s_x + (size_t)t * XS + lane * kXG);
+                const uint4 *xr = reinterpret_cast<const uint4 *>(s_xr + (size_t)t * XS + lane * kXG);
                 float dq = 0.f, sx = 0.f;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -998,11 +1099,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t clo = (c & 1) ? rc[c >> 1].z : rc[c >> 1].x;
                     const uint32_t chi = (c & 1) ? rc[c >> 1].w : rc[c >> 1].y;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float qv = (float)(((i < 4 ? clo : chi) >> ((i & 3) * 8)) & 0xFFu);
-                        const float xv1 = kchunk_at(xw, i);
-                        dq = fmaf(qv, xv1, dq);
-                        sx += xv1;
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t cw = q < 2 ? clo : chi;
+                        const float q0 = (float)((cw >> ((2 * q & 3) * 8)) & 0xFFu);
+                        const float q1 = (float)((cw >> (((2 * q & 3) + 1) * 8)) & 0xFFu);
+                        const float x0 = __uint_as_float(xw[q] << 16), x1 = __uint_as_float(xw[q] & 0xFFFF0000u);
+                        dq = fmaf(q0, x0, dq);
+                        dq = fmaf(q1, x1, dq);
+                        sx += x0;
+                        sx += x1;
                     }
                 }
                 prt = fmaf(rs, dq, fmaf(rbias, sx, 0.f));
@@ -1010,38 +1115,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) prt += __shfl_xor_sync(0xffffffffu, prt, o);
             if (lane == 0) {
-                float l = prt * pow2f(S.xe[t]);
+                float l = prt;
                 if (a.router_bias) l = l + __ldg(a.router_bias + er);   // one fp32 rounding
-                a.logits[(size_t)t * E + er] = l;
+                st_relaxed_u64(a.logits64 + (size_t)t * E + er, ((unsigned long long)epoch << 32) | __float_as_uint(l));
             }
         }
     }
+    stamp(a, kStRouterPub);
+
+    // ---- x' for the expert units (from the raw rows in the ring area), then the ring area is handed
+    // to the copy engine: the generic-proxy reads of it are ordered before the first copy into it
+    convert_x(S, a, s_xr, s_x, s_xs);
+    fence_proxy_async_smem();
     __syncthreads();
-    if (router) {
-        if (tid == 0) {
-            __threadfence();
-            const int old = atomicAdd(cnt_router, 1);
-            stamp(a, kStRouterPub);
-            if (old < 0 || old >= grid) {
-                record_status(a.status, MOE_ERR_WORKSPACE);   // the workspace header was not zero-filled
-                S.abort = 1;
-            } else if (!poll_geq(cnt_router, grid, limit)) {
-                record_status(a.status, MOE_ERR_TIMEOUT);
-                S.abort = 1;
-            }
-        }
-        __syncthreads();
-    }
-    stamp(a, kStRouterCnt);
+    stamp(a, kStXStaged);
+
 
     int U = 0;
     if (!S.abort) {
-        route_and_list(S, a, a.logits_in ? a.logits_in : a.logits);
+        route_and_list(S, a, a.logits_in);
         U = S.nlist * SL;
     }
     stamp(a, kStRouted);
+    // every warp takes its role or none: the flag is read before any role may set it
+    const bool go = !S.abort;
+    __syncthreads();
 
-    if (!S.abort) {
+    if (go) {
         if (warp == kWarpProd) {
             fused_producer(S, maps, a, geo, ring, U);
         } else if (warp == kWarpAux) {
@@ -1051,9 +1151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             fused_consumers<NT>(S, a, geo, ring, s_x, s_xs, s_red, s_h, s_hs, U);
         }
     }
-    if ((int)blockIdx.x >= U) {          // no units: the first-chunk stamps take this time
+    if ((int)blockIdx.x >= U) {          // no units: the first-unit stamps take this time
         stamp(a, kStFirstGate);
         stamp(a, kStFirstDown);
+        stamp(a, kStFirstDownDone);
     }
     __syncthreads();
     stamp(a, kStUnitsDone);
@@ -1078,9 +1179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         const int old = atomicAdd(cnt_exit, 1);
         if (old == grid - 1) {
-            *cnt_router = 0;
             *cnt_units = 0;
             *cnt_exit = 0;
+            a.sync[kSyncEpoch] = (int)S.epoch;   // the next launch tags its logits with epoch + 1
         } else if (old < 0 || old >= grid) {
             record_status(a.status, MOE_ERR_WORKSPACE);
         }
@@ -1126,7 +1227,7 @@ bool fused_geometry(int T, int H, int I, int k, int has_shared, int grid, int op
     g.codes2 = (uint32_t)H * 16;
     g.slot = (uint32_t)align_up(std::max(g.codes1 + 2 * g.sc1, g.codes2), 1024);
     const size_t xb = align_up((size_t)T * (G * kXG + 8) * 2, 16), xsb = align_up((size_t)T * G * 4, 16);
-    const size_t redb = (size_t)2 * 2 * kSlice * NC * 4, hb = (size_t)NC * kSlice * 2, hsb = align_up((size_t)NC * 4, 16);
+    const size_t redb = (size_t)2 * 4 * kSlice * NC * 4, hb = (size_t)NC * kSlice * 2, hsb = align_up((size_t)NC * 4, 16);
     const size_t fixed = xb + xsb + redb + hb + hsb;
     const long long budget = (long long)optin - (long long)sizeof(FSmem) - 1024 - 64;
     if (budget <= (long long)fixed) return false;
@@ -1137,6 +1238,7 @@ bool fused_geometry(int T, int H, int I, int k, int has_shared, int grid, int op
     g.RB = 4 * ((H + 4 * grid - 1) / (4 * grid));
     const int NS = k + (has_shared ? 1 : 0);
     if ((size_t)T * (g.RB / 4) * NS * 16 > (size_t)g.R * g.slot) return false;   // combine terms in the ring
+    if ((size_t)T * (G * kXG + 8) * 2 > (size_t)g.R * g.slot) return false;       // raw x in the ring
     size_t o = (size_t)g.R * g.slot;
     g.x_off = (uint32_t)o;
     o += xb;
@@ -1231,6 +1333,30 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t st)
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, maps, a, geo);
+}
+
+__global__ void __launch_bounds__(256) pack_down_kernel(const uint8_t *src, uint8_t *dst, int n, int H, int I)
+{
+    // one 16-byte piece per thread: (matrix m, row r, slice c) -> dst[((m * SL + c) * H + r) * 16]
+    const int SL = I / kSlice;
+    const size_t total = (size_t)n * H * SL;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i % SL);
+        const size_t mr = i / SL;
+        const int r = (int)(mr % H);
+        const size_t m = mr / H;
+        const uint4 v = *reinterpret_cast<const uint4 *>(src + mr * (size_t)(I / 2) + (size_t)c * 16);
+        *reinterpret_cast<uint4 *>(dst + ((m * SL + c) * H + r) * 16) = v;
+    }
+}
+
+cudaError_t launch_pack_down(const uint8_t *src, uint8_t *dst, int n, int H, int I, cudaStream_t st)
+{
+    const size_t total = (size_t)n * H * (I / kSlice);
+    const int blocks = (int)std::min<size_t>((total + 255) / 256, 4096);
+    if (blocks == 0) return cudaSuccess;
+    pack_down_kernel<<<blocks, 256, 0, st>>>(src, dst, n, H, I);
+    return cudaGetLastError();
 }
 
 }  // namespace qmoe

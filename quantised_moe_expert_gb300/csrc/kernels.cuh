@@ -144,13 +144,15 @@ struct FusedDecodeArgs {
     const float *router_bias;     // f32 [E] or null
     const float *logits_in;       // f32 [T, E] caller logits (no router GEMV), or null
     QMatDev gate, up, down, s_gate, s_up, s_down;
+    const uint8_t *down_packed;   // down codes in the slice layout [E, I/32, H, 16], or null (gathered)
+    const uint8_t *s_down_packed; // shared expert, [I/32, H, 16], or null
     const int32_t *ids_in;        // [T, k] given routing (then p_in / ws_in too), or null
     const uint16_t *p_in;         // bf16 [T, k]
     const uint16_t *ws_in;        // bf16 [T] or null
     int32_t *ids_out;             // [T, k] or null
     uint16_t *p_out;              // bf16 [T, k] or null
     uint16_t *ws_out;             // bf16 [T] or null
-    float *logits;                // f32 [T, E] published logits (workspace)
+    unsigned long long *logits64; // [T, E] published logits: fp32 bits | epoch << 32 (workspace)
     uint16_t *p_glob;             // bf16 [T, k] published pick weights (workspace)
     uint16_t *ws_glob;            // bf16 [T] published shared weights (workspace)
     float *part;                  // f32 [T (k + 1), I / 32, H] raw down sums per column and slice (workspace)
@@ -173,6 +175,8 @@ struct FusedDecodeArgs {
 bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared);
 size_t decode_fused_trace_ctas();
 cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t st);
+// Down codes [n, H, I/2] -> slice layout [n, I/32, H, 16].
+cudaError_t launch_pack_down(const uint8_t *src, uint8_t *dst, int n, int H, int I, cudaStream_t st);
 cudaError_t launch_route_gemv(const RouteArgs &a, cudaStream_t st);
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t st);
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t st);

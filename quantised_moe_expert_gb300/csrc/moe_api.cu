@@ -252,7 +252,9 @@ FusedDecodeArgs fused_args(const moe_config &c, const moe_weights &w, const uint
         fa.s_up = dev(w.s_up);
         fa.s_down = dev(w.s_down);
     }
-    fa.logits = ws_at<float>(ws, L.logits);
+    fa.down_packed = w.down_packed;
+    fa.s_down_packed = c.has_shared ? w.s_down_packed : nullptr;
+    fa.logits64 = ws_at<unsigned long long>(ws, L.logits);
     fa.p_glob = ws_at<uint16_t>(ws, L.p);
     fa.ws_glob = ws_at<uint16_t>(ws, L.w_s);
     fa.part = ws_at<float>(ws, L.dpart);
@@ -279,6 +281,7 @@ bool fused_fits(const moe_config &c, int T)
 bool weights_ok(const moe_config &c, const moe_weights *w, bool need_router, bool need_experts)
 {
     if (!w) return false;
+    if (!aligned16_or_null(w->down_packed) || !aligned16_or_null(w->s_down_packed)) return false;
     if (need_router && !qmat_ok(w->router)) return false;
     if (need_experts) {
         if (!qmat_ok(w->gate) || !qmat_ok(w->up) || !qmat_ok(w->down)) return false;
@@ -474,13 +477,35 @@ int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_s
 {
     if (!aligned16(ws) || ws_bytes < kHeaderBytes || !device_status) return MOE_ERR_INVALID_ARG;
     auto st = static_cast<cudaStream_t>(stream);
-    int v = 0;
+    int hdr[kHeaderBytes / sizeof(int)];
     int rc = cuda_rc(cudaStreamSynchronize(st));
-    if (!rc) rc = cuda_rc(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost));
-    if (!rc) rc = cuda_rc(cudaMemset(ws, 0, kHeaderBytes));   // status word and counters
+    if (!rc) rc = cuda_rc(cudaMemcpy(hdr, ws, kHeaderBytes, cudaMemcpyDeviceToHost));
+    if (rc) return rc;
+    const int v = hdr[0];
+    // status word and counters to zero; the epoch moves on, so that logits a kernel published
+    // under the old one can never pass for the next launch's
+    const int epoch = hdr[kSyncEpoch] + 1;
+    for (int &h : hdr) h = 0;
+    hdr[kSyncEpoch] = epoch;
+    rc = cuda_rc(cudaMemcpy(ws, hdr, kHeaderBytes, cudaMemcpyHostToDevice));
     if (rc) return rc;
     *device_status = v;
     return MOE_OK;
+}
+
+int moe_pack_down(const moe_config *cfg, const moe_weights *w, uint8_t *down_packed, uint8_t *s_down_packed,
+                  void *stream)
+{
+    int rc = check_common(cfg, 0);
+    if (rc) return rc;
+    if (!w || !aligned16(w->down.codes) || !aligned16(down_packed) || !aligned16_or_null(s_down_packed))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->inter % kDecodeSlice) return MOE_ERR_UNSUPPORTED;
+    auto st = static_cast<cudaStream_t>(stream);
+    rc = cuda_rc(launch_pack_down(w->down.codes, down_packed, cfg->n_experts, cfg->hidden, cfg->inter, st));
+    if (rc || !cfg->has_shared || !s_down_packed) return rc;
+    if (!aligned16(w->s_down.codes)) return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_pack_down(w->s_down.codes, s_down_packed, 1, cfg->hidden, cfg->inter, st));
 }
 
 int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T, const int32_t *ids,

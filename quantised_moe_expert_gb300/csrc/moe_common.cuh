@@ -26,13 +26,14 @@ constexpr int kSmallN = 32;         // tokens per item of the small-tile GEMMs (
 constexpr int kBigTok = kSmallN + 1;   // experts with at least this many tokens go to the tensor-memory GEMMs
 
 // Workspace header (int offsets from the start of the workspace): the device status word, then
-// the fused decode kernel's grid-wide counters, 128 bytes apart.  The counters must be zero
-// before a workspace's first use; the fused decode kernel leaves them zero when it ends.
-constexpr int kSyncRouter = 32;     // CTAs whose router logits are published
+// the fused decode kernel's grid-wide counters, 128 bytes apart, and the epoch of its last
+// launch.  The counters must be zero before a workspace's first use; the fused decode kernel
+// leaves them zero when it ends and advances the epoch (the tag of the logits it publishes).
 constexpr int kSyncUnits = 64;      // CTAs whose expert units are done
 constexpr int kSyncExit = 96;       // CTAs that have left
+constexpr int kSyncEpoch = 120;     // launches so far (wraps)
 constexpr size_t kHeaderBytes = 512;
-constexpr int kTraceStamps = 12;    // %globaltimer stamps per CTA of the fused decode kernel
+constexpr int kTraceStamps = 14;    // %globaltimer stamps per CTA of the fused decode kernel
 constexpr int kTraceMaxCtas = 256;
 constexpr int kDecodeSlice = 32;    // rows of the intermediate dimension per fused decode unit
 
@@ -48,7 +49,7 @@ struct WorkItem {
 // Offsets (bytes) of every scratch array inside the caller's workspace.
 struct WsLayout {
     size_t status;     // header: int32 status word + fused decode counters (kHeaderBytes)
-    size_t logits;     // f32 [T, E]
+    size_t logits;     // f32 [T, E] (prefill) or u64 [T, E] (fused decode)
     size_t ids;        // i32 [T, k]
     size_t p;          // u16 [T, k]
     size_t w_s;        // u16 [T]
@@ -100,7 +101,7 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.max_w1 = max_tiles((int)Tz, (int)k, (int)E, c.has_shared, kSmallN);   // bounds both item sizes
     L.max_w2 = L.max_w1;
     L.status = take(kHeaderBytes);
-    L.logits = take(4 * Tz * E);
+    L.logits = take(8 * Tz * E);     // fp32 logits, or the fused decode kernel's (logit, epoch) pairs
     L.ids = take(4 * Tz * k);
     L.p = take(2 * Tz * k);
     L.w_s = take(2 * Tz);

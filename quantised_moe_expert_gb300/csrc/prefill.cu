@@ -146,19 +146,22 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *status)
     record_status(status, MOE_ERR_TIMEOUT);
 }
 
-// Named barrier `id` over `count` threads.
+// Named barrier `id` over `count` threads.  The non-aligned form: a warp may reach it with its
+// lanes apart (after a branch taken by one lane), and each warp is brought back together first.
 __device__ __forceinline__ void named_bar(int id, int count)
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+    __syncwarp();
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Named barrier `id` over `count` threads that also ORs a predicate: every
 // participant gets the same answer, so a group of warps stops together.
 __device__ __forceinline__ bool bar_any(int id, int count, bool pred)
 {
+    __syncwarp();
     uint32_t r;
     asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)pred), "r"(id), "r"(count)
         : "memory");

@@ -51,12 +51,14 @@ constexpr long long kSDrainLimit = 1ll << 22;
 static_assert(kSmallN == 32, "one loader lane per token row, four n8 tiles");
 static_assert(kG1Stage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled code boxes");
 
-// Named barrier over the compute warps that also ORs a predicate (a uniform stop decision).
+// Named barrier over the compute warps that also ORs a predicate (a uniform stop decision).  The
+// non-aligned form, each warp brought back together first: lanes may arrive apart.
 __device__ __forceinline__ bool compute_any(bool pred)
 {
+    __syncwarp();
     uint32_t r;
     asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)pred), "n"(kSCompute * 32)
         : "memory");
@@ -391,7 +393,8 @@ __global__ void __launch_bounds__(kSThreads1, 1)
                     hp[j * 8 + 2 * t4 + 1] = part[1];
                 }
             }
-            asm volatile("bar.sync 2, %0;" ::"n"(8 * 32) : "memory");   // the eight gate warps
+            __syncwarp();
+            asm volatile("barrier.sync 2, %0;" ::"n"(8 * 32) : "memory");   // the eight gate warps
             const int grp = 2 * t.mb + (rw >> 2), GI = I / kGroup;
             if ((rw & 3) == 0 && lane < ncol && grp < GI) {
                 const float *q4 = sH + (buf * 8 + rw) * 32 + lane;

@@ -143,10 +143,19 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 template <int N>
 __device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Asks L2 to fetch a contiguous range (16-byte aligned address and size); no completion signal.
+// Asks L2 to fetch a contiguous range (16-byte aligned address and size) through the bulk copy
+// engine; no completion signal, so a CTA can exit with it still queued.  Only for a thread that
+// later issues bulk loads of its own which the CTA waits for before it exits.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Asks L2 for the 128-byte line holding `p`: a plain per-thread instruction, nothing left queued
+// in the bulk copy engine.
+__device__ __forceinline__ void prefetch_l2_line(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Arrive on `bar` only once the four values are available: they are computed

@@ -157,6 +157,12 @@ def test_other_entry_points_reject_bad_arguments(lib):
                                  FAKE, big, None) == qm.MOE_OK
     assert lib.moe_expert_stages(ctypes.byref(cfg), ctypes.byref(w), FAKE, 4, FAKE, FAKE, FAKE, FAKE, None, None, 0,
                                  FAKE, big, None) == qm.MOE_OK
+    assert lib.moe_pack_down(ctypes.byref(cfg), ctypes.byref(w), MISALIGNED, None, None) == qm.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_down(ctypes.byref(cfg), ctypes.byref(fake_weights("down")), FAKE, None, None) == \
+        qm.MOE_ERR_INVALID_ARG
+    bad = fake_weights()
+    bad.down_packed = MISALIGNED
+    assert forward(lib, cfg, bad) == qm.MOE_ERR_INVALID_ARG
     n = ctypes.c_int()
     assert lib.moe_decode_timeline(ctypes.byref(cfg), 1, FAKE, big, None, None, 4, ctypes.byref(n)) == \
         qm.MOE_ERR_INVALID_ARG

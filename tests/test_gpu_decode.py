@@ -327,3 +327,30 @@ def test_decode_timeline_is_ordered():
     d = np.diff(st.astype(np.int64), axis=1)
     assert np.all(d >= 0), d.min()
     assert qm.moe_get_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("wl_index,T", [(0, 4), (2, 16)])
+def test_packed_and_gathered_down_codes_give_the_same_bytes(wl_index, T):
+    """The decode kernel's two ways of reading the down codes (the packed copy, one block per
+    slice, or 16-byte pieces of the MLX rows) feed the same arithmetic: identical outputs."""
+    wl, w, layer = H.device_layer(wl_index)
+    x = synth.make_x(wl.shape, T, wl.seed, stream=40)
+    a = H.run_forward(layer, x, path=qm.MOE_PATH_DECODE)
+    b = H.run_forward(layer.unpacked(), x, path=qm.MOE_PATH_DECODE)
+    assert a["status"] == 0 and b["status"] == 0
+    for key in ("y", "ids", "p", "w_s"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_pack_down_layout():
+    """moe_pack_down writes byte b of row r, column slice c of expert e at ((e * I/32 + c) * H + r) * 16 + b."""
+    wl, w, layer = H.device_layer(0)
+    sh = wl.shape
+    got = layer.tensors["down.packed"].cpu().numpy().view(np.uint8)
+    src = w.down.codes
+    E, Hd, half = src.shape
+    ref = src.reshape(E, Hd, half // 16, 16).transpose(0, 2, 1, 3).reshape(-1)
+    assert np.array_equal(got.reshape(-1), ref)
+    sgot = layer.tensors["s_down.packed"].cpu().numpy().view(np.uint8)
+    sref = w.s_down.codes.reshape(1, Hd, half // 16, 16).transpose(0, 2, 1, 3).reshape(-1)
+    assert np.array_equal(sgot.reshape(-1), sref)
