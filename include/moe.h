@@ -258,10 +258,11 @@ MOE_API int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *
  *             pick weight, or NULL.
  * ids/counts/offsets/perm as for moe_expert_ffn (counts/offsets/perm are read
  * on the prefill path only).  The same kernels as moe_expert_ffn compute the
- * stages; nothing is added into an accumulator.  Rows of h_out / yslot_out of
- * slots that do not exist (the shared rows without a shared expert) are not
- * written.  Returns MOE_ERR_UNSUPPORTED for a path whose kernels cannot emit
- * their stages. */
+ * stages; nothing is added into an accumulator.  On the prefill path
+ * yslot_out must be zero-filled by the caller (the down GEMM adds each tile's
+ * rows into it).  Rows of h_out / yslot_out of slots that do not exist (the
+ * shared rows without a shared expert) are not written.  Returns
+ * MOE_ERR_UNSUPPORTED for a path whose kernels cannot emit their stages. */
 MOE_API int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T,
                               const int32_t *ids, const int32_t *counts, const int32_t *offsets,
                               const int32_t *perm, float *h_out, float *yslot_out, int path,

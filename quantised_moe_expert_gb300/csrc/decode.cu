@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
 {
     extern __shared__ uint4 s_x[];                 // [NT*8][H/8 + 1] (one uint4 of padding per row)
     __shared__ float s_red[8][2][16][NT * 8];      // [warp][gate/up][row][col]
-    __shared__ int s_tok[kDecodeMaxTok], s_slot[kDecodeMaxTok];
+    __shared__ int s_tok[kDecodeMaxTok], s_slot[kDecodeMaxTok], s_e[kDecodeMaxTok];
     if ((int)blockIdx.y >= __ldg(a.nwork + 0)) return;
     const WorkItem it = a.work[blockIdx.y];
     const int H = a.H, I = a.I, G = H / kGroup, rowu4 = H / 8 + 1;
@@ -171,6 +171,23 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
                                         : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
+    // e of each column's token (2^e <= max |x| < 2^(e + 1)): h is stored as fp16 h 2^-2e, which stays
+    // inside the fp16 range whatever the size of x; the down kernel undoes the scale (exact)
+    for (int c = warp; c < NT * 8 && c < kDecodeMaxTok; c += 8) {
+        uint32_t mx = 0;
+        for (int col = lane; col < H / 8; col += 32) {
+            const uint4 v = s_x[c * rowu4 + col];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7FFFu, (w4[q] >> 16) & 0x7FFFu));
+        }
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) {
+            const int e = row_scale_exponent(mx);
+            s_e[c] = e;
+            if (blockIdx.x == 0 && s_tok[c] >= 0) a.xe[s_tok[c]] = e;   // for the down kernel
+        }
+    }
 
     const ExpertView vg = is_shared ? expert_view(a.s_gate, 0, I, H) : expert_view(a.gate, it.expert, I, H);
     const ExpertView vu = is_shared ? expert_view(a.s_up, 0, I, H) : expert_view(a.up, it.expert, I, H);
@@ -259,8 +276,8 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
             gs += s_red[w][0][row][c];
             us += s_red[w][1][row][c];
         }
-        const float hv = gs / (1.f + __expf(-gs)) * us;
-        a.h[(size_t)f * I + blockIdx.x * 16 + row] = __half_as_ushort(__float2half_rn(hv));
+        const float hv = gs / (1.f + __expf(-gs)) * us, dn = pow2f(-s_e[c]);
+        a.h[(size_t)f * I + blockIdx.x * 16 + row] = __half_as_ushort(__float2half_rn(hv * dn * dn));
     }
 }
 
@@ -337,17 +354,20 @@ __global__ void __launch_bounds__(128) decode_down_kernel(ExpertArgs a)
             }
         }
     }
+    // h was stored as h 2^-2e: the slot's output is scaled back by 2^2e (exact)
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const int cA = j * 8 + 2 * t, cB = cA + 1;
         const int fA = cA < kDecodeMaxTok ? s_slot[cA] : -1, fB = cB < kDecodeMaxTok ? s_slot[cB] : -1;
         if (fA >= 0) {
-            a.yslot[(size_t)fA * H + r0] = acc[j][0];
-            a.yslot[(size_t)fA * H + r1] = acc[j][2];
+            const float up = pow2f(__ldg(a.xe + s_tok[cA]));
+            a.yslot[(size_t)fA * H + r0] = acc[j][0] * up * up;
+            a.yslot[(size_t)fA * H + r1] = acc[j][2] * up * up;
         }
         if (fB >= 0) {
-            a.yslot[(size_t)fB * H + r0] = acc[j][1];
-            a.yslot[(size_t)fB * H + r1] = acc[j][3];
+            const float up = pow2f(__ldg(a.xe + s_tok[cB]));
+            a.yslot[(size_t)fB * H + r0] = acc[j][1] * up * up;
+            a.yslot[(size_t)fB * H + r1] = acc[j][3] * up * up;
         }
     }
 }

@@ -169,12 +169,6 @@ __device__ __forceinline__ uint4 kperm8(uint4 v)
     return o;
 }
 
-// 2^n as a float, exactly, for -149 <= n <= 127 (powers of two below 2^-126 are subnormal).
-__device__ __forceinline__ float pow2f(int n)
-{
-    return n >= -126 ? __int_as_float((n + 127) << 23) : __int_as_float(1 << (n + 149));
-}
-
 // Position of element i in the k order of its chunk of 8.
 __device__ __forceinline__ int kperm_pos(int i) { return (i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1); }
 
@@ -613,7 +607,7 @@ __device__ __forceinline__ void convert_x(FSmem &S, const FusedDecodeArgs &a, co
                     for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7FFFu, w4[q] >> 16 & 0x7FFFu));
                 }
             mx = __reduce_max_sync(0xffffffffu, mx);
-            const int ef = (int)(mx >> 7), xe = ef == 0 ? -126 : ef - 127;
+            const int xe = row_scale_exponent(mx);
             const float sc = pow2f(-xe);
 #pragma unroll
             for (int i = 0; i < kMaxChunks; ++i)

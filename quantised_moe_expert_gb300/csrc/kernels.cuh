@@ -90,8 +90,9 @@ struct ExpertArgs {
     const int32_t *perm;          // [T*k]
     const int32_t *nwork;         // [3]
     const WorkItem *work;         // decode items or GEMM tiles
-    uint16_t *h;                  // bf16 [T*k + T, I], slot-major (f = t*k + j; shared f = T*k + t)
+    uint16_t *h;                  // fp16 [T*k + T, I], slot-major (f = t*k + j; shared f = T*k + t): h 2^-2e
     float *yslot;                 // f32 [T*k + T, H] (decode)
+    int *xe;                      // i32 [T]: e of each token, 2^e <= max |x| < 2^(e + 1) (workspace)
     const uint16_t *p;            // bf16 [T, k]
     const uint16_t *w_s;          // bf16 [T]
     float *acc;                   // f32 [T, H]
@@ -111,8 +112,9 @@ struct ReduceArgs {
 
 struct PrefillArgs {
     const uint16_t *x;            // bf16 [T, H]
-    uint16_t *x16;                // fp16 [T, H] scratch (K-permuted)
+    uint16_t *x16;                // fp16 [T, H] scratch (K-permuted): x' = x 2^-e per token
     float *xsum;                  // f32 [T, H / 64] scratch: group sums of x16
+    int *xe;                      // i32 [T] scratch: the token's e (max |x'| in [1, 2))
     float *hsum;                  // f32 [T*k + T, I / 64] scratch: group sums of h (small-tile items)
     uint16_t *hs;                 // fp16 [T*k + T, I] scratch, expert-sorted rows
     QMatDev gate, up, down, s_gate, s_up, s_down;
@@ -121,6 +123,8 @@ struct PrefillArgs {
     const uint16_t *p, *w_s;
     float *acc;                   // f32 [T, H]
     int acc_zero;                 // 1: zero acc first
+    float *h_out;                 // f32 [T (k + 1), I] h per slot (stage output), or null
+    float *yslot_out;             // f32 [T (k + 1), H] expert output per slot, unweighted, instead of acc; or null
     int *status;
     int T, H, I, E, k, has_shared, max_w1, max_w2;
     long long wait_limit;

@@ -160,6 +160,7 @@ ExpertArgs expert_args(const moe_config &c, const moe_weights &w, const uint16_t
     ea.nwork = ws_at<int32_t>(ws, L.nwork);
     ea.h = ws_at<uint16_t>(ws, L.h);
     ea.yslot = ws_at<float>(ws, L.yslot);
+    ea.xe = ws_at<int>(ws, L.xe);
     ea.p = p;
     ea.w_s = w_s;
     ea.acc = acc;
@@ -198,12 +199,15 @@ int enqueue_decode_experts(const moe_config &c, ExpertArgs ea, const WsLayout &L
 
 // Prefill expert GEMMs; acc is zeroed first when acc_zero (the fused forward).
 int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsLayout &L, void *ws, int acc_zero,
-                            cudaStream_t st)
+                            cudaStream_t st, float *h_out = nullptr, float *yslot_out = nullptr)
 {
     PrefillArgs a{};
     a.x = ea.x;
     a.x16 = ws_at<uint16_t>(ws, L.x16);
     a.xsum = ws_at<float>(ws, L.xsum);
+    a.xe = ws_at<int>(ws, L.xe);
+    a.h_out = h_out;
+    a.yslot_out = yslot_out;
     a.hsum = ws_at<float>(ws, L.hsum);
     a.hs = ws_at<uint16_t>(ws, L.h);
     a.gate = ea.gate;
@@ -533,10 +537,29 @@ int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_
         fa.stages_only = 1;
         return cuda_rc(launch_decode_fused(fa, st));
     }
-    (void)counts;
-    (void)offsets;
-    (void)perm;
-    return MOE_ERR_UNSUPPORTED;
+    if (rp == MOE_PATH_DECODE) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(counts) || !aligned16(offsets) || !aligned16(perm)) return MOE_ERR_INVALID_ARG;
+    // prefill: the grouped GEMMs of moe_expert_ffn, h per slot from the gate/up epilogue and the
+    // unweighted expert output per slot from the down epilogue (no accumulator)
+    WorklistArgs wa{};
+    wa.counts = counts;
+    wa.nwork = ws_at<int32_t>(ws, L.nwork);
+    wa.work_dec = ws_at<WorkItem>(ws, L.work_dec);
+    wa.work_g1 = ws_at<WorkItem>(ws, L.work_g1);
+    wa.work_g2 = ws_at<WorkItem>(ws, L.work_g2);
+    wa.status = ws_at<int>(ws, L.status);
+    wa.T = T;
+    wa.E = cfg->n_experts;
+    wa.has_shared = cfg->has_shared;
+    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter) ? 1 : 0;
+    wa.max_items[0] = L.max_wd;
+    wa.max_items[1] = L.max_w1;
+    wa.max_items[2] = L.max_w2;
+    if ((rc = cuda_rc(launch_worklist(wa, st)))) return rc;
+    // the weights are not applied: any values serve (the workspace's own p and w_s rows)
+    ExpertArgs ea = expert_args(*cfg, *w, x, T, ws_at<uint16_t>(ws, L.p), ws_at<uint16_t>(ws, L.w_s), offsets, perm,
+                                ws_at<float>(ws, L.acc), L, ws);
+    return enqueue_prefill_experts(*cfg, ea, L, ws, 1, st, h_out, yslot_out);
 }
 
 int moe_decode_timeline(const moe_config *cfg, int T, void *ws, size_t ws_bytes, void *stream,

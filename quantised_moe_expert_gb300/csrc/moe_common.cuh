@@ -66,6 +66,7 @@ struct WsLayout {
     size_t work_g2;    // WorkItem [max tiles gemm2]
     size_t x16;        // fp16 [T, H] (prefill B operand)
     size_t xsum;       // f32 [T, H / 64] group sums of x16 (small-tile gate/up GEMM)
+    size_t xe;         // i32 [T] prefill pre-scale exponents: x16 holds x' = x 2^-xe
     size_t hsum;       // f32 [T*k + T, I / 64] group sums of h (small-tile GEMMs)
     size_t h;          // fp16 [T*k + T, I] (decode: slot order; prefill: expert-sorted, K-permuted)
     size_t yslot;      // f32 [T*k + T, H] (decode kernels of shapes the fused kernel does not take)
@@ -119,6 +120,7 @@ inline WsLayout ws_layout(const moe_config &c, int T)
     L.work_g2 = take(sizeof(WorkItem) * (size_t)L.max_w2);
     L.x16 = take(2 * Tz * H);
     L.xsum = take(4 * Tz * (H / 64));
+    L.xe = take(4 * Tz);
     L.hsum = take(4 * Tz * (k + 1) * (I / 64));
     L.h = take(2 * Tz * (k + 1) * I);
     L.yslot = take(4 * Tz * (k + 1) * H);
@@ -158,6 +160,21 @@ __device__ __forceinline__ uint16_t double_to_bf16_bits(double d)
     u &= ~((1ull << 45) - 1ull);
     float f = (float)__longlong_as_double((long long)u);
     return (uint16_t)(__float_as_uint(f) >> 16);
+}
+
+// 2^n as a float, exactly, for -149 <= n <= 127 (powers of two below 2^-126 are subnormal).
+__device__ __forceinline__ float pow2f(int n)
+{
+    return n >= -126 ? __int_as_float((n + 127) << 23) : __int_as_float(1 << (n + 149));
+}
+
+// Exponent e of a token's pre-scale from the largest |x| of its row as bf16 magnitude bits (sign
+// cleared): 2^e <= max |x| < 2^(e + 1), so x' = x 2^-e has max |x'| in [1, 2) (e = -126 for a row of
+// zeros and subnormals).
+__device__ __forceinline__ int row_scale_exponent(uint32_t max_bits)
+{
+    const int ef = (int)(max_bits >> 7);
+    return ef == 0 ? -126 : ef - 127;
 }
 
 }  // namespace qmoe

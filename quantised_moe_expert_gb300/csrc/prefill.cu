@@ -75,8 +75,10 @@ struct G1Params {
     const WorkItem *work;
     const int32_t *offsets;
     const int32_t *perm;
-    uint16_t *hs;                      // fp16 [T*k + T, I] (K-permuted), expert-sorted rows
-    const uint16_t *x16;               // fp16 [T, H] (K-permuted)
+    uint16_t *hs;                      // fp16 [T*k + T, I] (K-permuted), expert-sorted rows: h' = h 2^-2e
+    const uint16_t *x16;               // fp16 [T, H] (K-permuted): x' = x 2^-e
+    const int *xe;                     // i32 [T]: e of each token
+    float *h_out;                      // f32 [T*k + T, I] h per slot (stage output), or null
     const uint8_t *gc, *uc, *sgc, *suc;    // int4 codes (routed [E, I, H/2], shared [I, H/2]), for L2 prefetch
     const uint16_t *gs, *gb, *us, *ub;     // routed gate/up scales, biases [E, I, H/64]
     const uint16_t *sgs, *sgb, *sus, *sub; // shared expert [I, H/64]
@@ -94,6 +96,8 @@ struct G2Params {
     const uint16_t *p;                 // bf16 [T, k]
     const uint16_t *w_s;               // bf16 [T]
     float *acc;                        // f32 [T, H]
+    const int *xe;                     // i32 [T]: e of each token (the h tile holds h 2^-2e)
+    float *yslot_out;                  // f32 [T*k + T, H]: unweighted expert output per slot instead of acc, or null
     const uint8_t *dc, *sdc;           // int4 codes (routed [E, H, I/2], shared [H, I/2]), for L2 prefetch
     const uint16_t *ds, *db;           // routed down scales, biases [E, H, I/64]
     const uint16_t *sds, *sdb;         // shared [H, I/64]
@@ -225,7 +229,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
     uint8_t *sB = smem;                           // SB x 16 KB (128 token rows x 128 B)
     uint8_t *sC = sB + SB * 16384;                // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [dequant thread][2][2][kScaleChunk1]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kDequantWarps1 * 32 * 4 * kScaleChunk1);
+    int *s_col = reinterpret_cast<int *>(sScale + kDequantWarps1 * 32 * 4 * kScaleChunk1);   // [2][e 128 | slot 128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_col + 2 * 256);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
@@ -537,23 +542,45 @@ __global__ void __launch_bounds__(kThreads1, 1)
         }
         cp_async_wait_all();                               // no copy into shared memory outlives the CTA
     } else {
-        // ------------------------------------------------ epilogue: h = silu(g) * u
-        // kEpiWarps1 warps: warp w reads TMEM lanes 32 (w & 3) .. + 31 (the lanes its position
-        // in a warpgroup allows) and every (kEpiWarps1 / 4)-th 16-column chunk of the
-        // accumulators, starting at chunk `half`.
+        // ------------------------------------------------ epilogue: h' = g' u' sigmoid(g' 2^e)
+        // The accumulators hold g' = g 2^-e and u' = u 2^-e of token n (x' = x 2^-e); the stored fp16
+        // h' = h 2^-2e stays inside the fp16 range whatever the size of x.  kEpiWarps1 warps: warp w
+        // reads TMEM lanes 32 (w & 3) .. + 31 (the lanes its position in a warpgroup allows) and every
+        // (kEpiWarps1 / 4)-th 16-column chunk of the accumulators, starting at chunk `half`.
         constexpr int kHalves = kEpiWarps1 / 4;
-        const int quad = warp & 3, half = (warp - kWarpEpi1) >> 2;
+        const int quad = warp & 3, half = (warp - kWarpEpi1) >> 2, et = tid - kWarpEpi1 * 32;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         int i = 0;
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
             const int N = (ti.ntok + 15) & ~15;
+            // e and slot of each column (token n of the tile; 128 epilogue threads, 128 columns at
+            // most), two tile buffers: the barrier of tile i + 1 orders every read of tile i before
+            // tile i + 2 refills the buffer
+            int *ce = s_col + (i & 1) * 256, *cf = ce + 128;
+            for (int n = et; n < 128; n += 32 * kEpiWarps1) {
+                int e = 0, f = -1;
+                if (n < ti.ntok) {
+                    int t = -1;
+                    if (ti.shared_e) {
+                        t = ti.tok0 + n;
+                        f = Tk + t;
+                    } else {
+                        const int pos = ti.pbase + n;
+                        f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                        if (f >= 0 && f < Tk) t = f / P.k;
+                        else f = -1;
+                    }
+                    if (t >= 0) e = __ldg(P.xe + t);
+                }
+                ce[n] = e;
+                cf[n] = f;
+            }
+            if (bar_any(3, 32 * kEpiWarps1, *s_abort)) break;
             bool got = mbar_wait(smem_u32(tfull), i & 1, limit, s_abort);
             got = __all_sync(0xffffffffu, got);              // tcgen05.ld needs the whole warp
-            if (!got) {
-                set_abort(s_abort, P.status);
-                break;
-            }
+            if (!got) set_abort(s_abort, P.status);
+            if (bar_any(3, 32 * kEpiWarps1, !got)) break;    // the epilogue warps stop together
             tc_fence_after();
             const int erow = ti.mb * 128 + quad * 32 + lane;
             const int hcol = kperm_pos(erow);
@@ -577,8 +604,13 @@ __global__ void __launch_bounds__(kThreads1, 1)
                         const int n = n0 + j;
                         if (n < ti.ntok) {
                             const float g = __uint_as_float(gv[j]), u = __uint_as_float(uv[j]);
-                            const float hv = __fdividef(g * u, 1.f + __expf(-g));
-                            P.hs[(size_t)(ti.pbase + n) * I + hcol] = __half_as_ushort(__float2half_rn(hv));
+                            const int e = ce[n];
+                            const __half hq = __float2half_rn(__fdividef(g * u, 1.f + __expf(-g * pow2f(e))));
+                            P.hs[(size_t)(ti.pbase + n) * I + hcol] = __half_as_ushort(hq);
+                            if (P.h_out != nullptr && cf[n] >= 0) {
+                                const float up = pow2f(e);
+                                P.h_out[(size_t)cf[n] * I + erow] = __half2float(hq) * up * up;
+                            }
                         }
                     }
                 }
@@ -860,17 +892,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = i & 1;
             int *tok = s_tok + buf * 256;
             float *wv = s_w + buf * 256;
-            // token and weight of each column (epilogue threads 192..319 fill them)
+            // destination row and factor of each column (epilogue threads 320..447 fill them): the
+            // token's row of acc and p 2^2e (the h tile holds h 2^-2e; exact), or in stage mode the
+            // slot's row of yslot_out and 2^2e
             for (int n = tid - kWarpEpi * 32; n < 256; n += 128) {
-                int t = -1;
+                int dst = -1;
                 float wgt = 0.f;
                 if (n < ti.ntok) {
+                    int t = -1, f = -1;
                     if (ti.shared_e) {
                         t = ti.tok0 + n;
+                        f = Tk + t;
                         wgt = bf16_bits_to_float(P.w_s[t]);
                     } else {
                         const int pos = ti.pbase + n;
-                        const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                        f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
                         if (f < 0 || f >= Tk) {
                             record_status(P.status, MOE_ERR_DEVICE);
                         } else {
@@ -878,8 +914,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             wgt = bf16_bits_to_float(P.p[f]);
                         }
                     }
+                    if (t >= 0) {
+                        const float up = pow2f(__ldg(P.xe + t));
+                        if (P.yslot_out != nullptr) {
+                            dst = f;
+                            wgt = up * up;
+                        } else {
+                            dst = t;
+                            wgt = wgt * up * up;
+                        }
+                    }
                 }
-                tok[n] = t;
+                tok[n] = dst;
                 wv[n] = wgt;
             }
             if (bar_any(2, 128, *s_abort)) break;
@@ -911,7 +957,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (e < kRedCols) {
                     const int n = n0 + e;
                     const int t = n < ti.ntok ? tok[n] : -1;
-                    if (t >= 0) bulk_reduce_add_f32(P.acc + (size_t)t * H + ti.mb * 128, smem_u32(red + e * 128),
+                    float *dst_base = P.yslot_out != nullptr ? P.yslot_out : P.acc;
+                    if (t >= 0) bulk_reduce_add_f32(dst_base + (size_t)t * H + ti.mb * 128, smem_u32(red + e * 128),
                                                     (uint32_t)nrow * 4);
                     bulk_commit();
                 }
@@ -929,40 +976,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
 }
 
-// x (bf16) -> x16 (fp16, the codes' k order within each chunk of 8) and, per token and
-// group of 64, the sum of the fp16 values in a fixed order (the small-tile GEMM's bias
-// term).  One thread per (token, group).
+// x (bf16) -> x' = x 2^-e per token (e from the row's largest |x|: max |x'| in [1, 2); exact) as
+// fp16 in the codes' k order within each chunk of 8, e per token, and per token and group of 64
+// the sum of the stored fp16 values (each chunk in element order, then a fixed shuffle tree over
+// the group's eight chunks; the small-tile GEMM's bias term).  One warp per token: lane l takes the
+// row's chunks l, l + 32, ...; a group's chunks sit in eight consecutive lanes.
 __global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x16, float *__restrict__ xsum,
-                                 size_t ngroups)
+                                 int *__restrict__ xe, int T, int H)
 {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < ngroups; i += (size_t)gridDim.x * blockDim.x) {
-        float sum = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-            const uint4 v = x[i * 8 + c];
+    const int lane = threadIdx.x & 31, cpr = H / 8, G = H / kGroup;
+    const int wpb = blockDim.x >> 5, nw = gridDim.x * wpb;
+    for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += nw) {
+        const uint4 *xr = x + (size_t)t * cpr;
+        uint32_t mx = 0;
+        for (int c = lane; c < cpr; c += 32) {
+            const uint4 v = xr[c];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            float f[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                f[2 * j] = __uint_as_float(w[j] << 16);
-                f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-            }
-            const __half2 h0 = __floats2half2_rn(f[0], f[4]), h1 = __floats2half2_rn(f[1], f[5]);
-            const __half2 h2 = __floats2half2_rn(f[2], f[6]), h3 = __floats2half2_rn(f[3], f[7]);
-            uint4 o;
-            o.x = h2u(h0);
-            o.y = h2u(h1);
-            o.z = h2u(h2);
-            o.w = h2u(h3);
-            x16[i * 8 + c] = o;
-            const __half2 hs[4] = {h0, h1, h2, h3};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                sum += __low2float(hs[j]);
-                sum += __high2float(hs[j]);
-            }
+            for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
         }
-        xsum[i] = sum;
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        const int e = row_scale_exponent(mx);
+        const float sc = pow2f(-e);
+        for (int c0 = 0; c0 < cpr; c0 += 32) {          // every lane runs every round (the shuffles)
+            const int c = c0 + lane;
+            float sum = 0.f;
+            if (c < cpr) {
+                const uint4 v = xr[c];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    f[2 * j] = __uint_as_float(w[j] << 16) * sc;
+                    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u) * sc;
+                }
+                const __half2 h0 = __floats2half2_rn(f[0], f[4]), h1 = __floats2half2_rn(f[1], f[5]);
+                const __half2 h2 = __floats2half2_rn(f[2], f[6]), h3 = __floats2half2_rn(f[3], f[7]);
+                uint4 o;
+                o.x = h2u(h0);
+                o.y = h2u(h1);
+                o.z = h2u(h2);
+                o.w = h2u(h3);
+                x16[(size_t)t * cpr + c] = o;
+                const __half2 hs[4] = {h0, h1, h2, h3};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    sum += __low2float(hs[j]);
+                    sum += __high2float(hs[j]);
+                }
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            if (c < cpr && (c & 7) == 0) xsum[(size_t)t * G + (c >> 3)] = sum;
+        }
+        if (lane == 0) xe[t] = e;
     }
 }
 
@@ -970,7 +1038,7 @@ __global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict_
 
 size_t g1_smem()
 {
-    return 1024 + kStagesB1 * 16384 + kCodeStages1 * 8192 + kDequantWarps1 * 32 * 4 * kScaleChunk1 * 2 +
+    return 1024 + kStagesB1 * 16384 + kCodeStages1 * 8192 + kDequantWarps1 * 32 * 4 * kScaleChunk1 * 2 + 2 * 256 * 4 +
            8 * (2 * kCodeStages1 + 2 * kStagesA1 + 2 * kStagesB1 + 5) + 256 * 4 + 16;
 }
 size_t g2_smem()
@@ -1012,17 +1080,16 @@ int sm_count()
 cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
 {
     const int H = a.H, I = a.I, E = a.E, T = a.T, k = a.k;
-    // x -> fp16, K-permuted
+    // x -> x' = x 2^-e per token, fp16, K-permuted (one warp per token)
     {
-        const size_t n = (size_t)T * (H / kGroup);
-        const unsigned grid = (unsigned)std::min<size_t>((n + 255) / 256, 152 * 8);
+        const unsigned grid = (unsigned)std::min<int>((T + 7) / 8, 152 * 8);
         convert_x_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4 *>(a.x), reinterpret_cast<uint4 *>(a.x16),
-                                               a.xsum, n);
+                                               a.xsum, a.xe, T, H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaSuccess;
-    if (a.acc_zero && (e = launch_zero(a.acc, (size_t)T * H, st)) != cudaSuccess) return e;
+    if (a.acc_zero && !a.yslot_out && (e = launch_zero(a.acc, (size_t)T * H, st)) != cudaSuccess) return e;
 
     CUtensorMap mgc, muc, msgc, msuc, mdc, msdc, mh;
     const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE, sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -1050,6 +1117,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p1.perm = a.perm;
     p1.hs = a.hs;
     p1.x16 = a.x16;
+    p1.xe = a.xe;
+    p1.h_out = a.h_out;
     p1.gc = a.gate.codes;
     p1.uc = a.up.codes;
     p1.sgc = a.has_shared ? a.s_gate.codes : a.gate.codes;
@@ -1094,6 +1163,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p2.p = a.p;
     p2.w_s = a.w_s;
     p2.acc = a.acc;
+    p2.xe = a.xe;
+    p2.yslot_out = a.yslot_out;
     p2.dc = a.down.codes;
     p2.sdc = a.has_shared ? a.s_down.codes : a.down.codes;
     p2.ds = a.down.scales;

@@ -70,9 +70,12 @@ struct SmallParams {
     const WorkItem *work;
     const int32_t *offsets;
     const int32_t *perm;
-    uint16_t *hs;                      // fp16 [T*k + T, I] (k order), expert-sorted rows
-    const uint16_t *x16;               // fp16 [T, H] (k order)
+    uint16_t *hs;                      // fp16 [T*k + T, I] (k order), expert-sorted rows: h' = h 2^-2e
+    const uint16_t *x16;               // fp16 [T, H] (k order): x' = x 2^-e
     const float *xsum;                 // f32 [T, H / 64]
+    const int *xe;                     // i32 [T]: e of each token
+    float *h_out;                      // f32 [T*k + T, I] h per slot (stage output), or null
+    float *yslot_out;                  // f32 [T*k + T, H] unweighted expert output per slot instead of acc, or null
     float *hsum;                       // f32 [T*k + T, I / 64]: group sums of the stored (fp16) h
     const uint16_t *p, *w_s;           // bf16 pick weights [T, k], shared weights [T]
     float *acc;                        // f32 [T, H]
@@ -183,7 +186,8 @@ __global__ void __launch_bounds__(kSThreads1, 1)
     const int XS = G + 4;                  // group-sum row stride: distinct banks for the columns a warp reads
     float *sX = reinterpret_cast<float *>(sS + 2 * 4 * 128 * G);           // [2][kSmallN][XS]
     float *sH = sX + 2 * kSmallN * XS;                                     // [2][8 gate warps][32]: h sums
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sH + 2 * 8 * 32);
+    int *s_e = reinterpret_cast<int *>(sH + 2 * 8 * 32);                   // [3][kSmallN]: e of each column
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_e + 3 * kSmallN);
     uint64_t *sfull = bars, *sempty = sfull + kG1Stages, *tfull = sempty + kG1Stages, *tempty = tfull + 2;
     volatile int *s_abort = reinterpret_cast<volatile int *>(tempty + 2);
 
@@ -239,6 +243,11 @@ __global__ void __launch_bounds__(kSThreads1, 1)
             const size_t wrow = (size_t)(t.shared_e ? 0 : t.expert * I) + t.mb * 128;
             const uint32_t sbytes = (uint32_t)rows_of(t) * G * 2;
             const uint32_t tb = smem_u32(tfull + buf);
+            // e of column `lane` for the gate warps' epilogue, in tile slot i % 3: it is refilled (tile
+            // i + 3) only after every compute warp released tile i + 1, i.e. after tile i's epilogue;
+            // ordered before lane 0's arrival on the tile barrier by the warp barrier
+            s_e[(i % 3) * kSmallN + lane] = row >= 0 ? __ldg(P.xe + row) : 0;
+            __syncwarp();
             if (lane == 0) {
                 mbar_arrive_expect_tx(tb, 4 * sbytes + (uint32_t)nrows * G * 4);
                 const uint16_t *src[4] = {t.shared_e ? P.ss0 : P.s0, t.shared_e ? P.sb0 : P.b0,
@@ -365,10 +374,12 @@ __global__ void __launch_bounds__(kSThreads1, 1)
             break;
         }
         if (m == 0) {
-            // h = silu(g) * u for the tile's rows and tokens, fp16, at the row's k-order column; and
-            // per token the sum of the stored h over each group of 64 rows (the down GEMM's bias term):
-            // this warp's 16 rows by shuffles, the group's four warps through shared memory in order
+            // h' = g' u' sigmoid(g' 2^e) for the tile's rows and tokens (g' = g 2^-e, u' = u 2^-e: x is
+            // pre-scaled per token; h' = h 2^-2e), fp16, at the row's k-order column; and per token the
+            // sum of the stored h' over each group of 64 rows (the down GEMM's bias term): this warp's
+            // 16 rows by shuffles, the group's four warps through shared memory in order
             float *hp = sH + (buf * 8 + rw) * 32;
+            const int *ecol = s_e + (i % 3) * kSmallN;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 float part[2] = {0.f, 0.f};
@@ -377,10 +388,21 @@ __global__ void __launch_bounds__(kSThreads1, 1)
                     const int col = j * 8 + 2 * t4 + (e & 1);
                     const int erow = t.mb * 128 + r0 + 8 * (e >> 1);
                     if (col < ncol && erow < I) {
-                        const float gv = acc[j][e], uv = xu[j * 4 + e];
-                        const __half hq = __float2half_rn(__fdividef(gv * uv, 1.f + __expf(-gv)));
+                        const float gv = acc[j][e], uv = xu[j * 4 + e], up = pow2f(ecol[col]);
+                        const __half hq = __float2half_rn(__fdividef(gv * uv, 1.f + __expf(-gv * up)));
                         P.hs[(size_t)(t.pbase + col) * I + kperm_pos(erow)] = __half_as_ushort(hq);
                         part[e & 1] += __half2float(hq);
+                        if (P.h_out != nullptr) {           // stage output: h of the slot
+                            int f = -1;
+                            if (t.shared_e) {
+                                f = Tk + t.tok0 + col;
+                            } else {
+                                const int pos = t.pbase + col;
+                                f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                                if (f >= Tk) f = -1;
+                            }
+                            if (f >= 0) P.h_out[(size_t)f * I + erow] = __half2float(hq) * up * up;
+                        }
                     }
                 }
 #pragma unroll
@@ -504,20 +526,34 @@ __global__ void __launch_bounds__(kSThreads2, 1)
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
             const STile t = stile(P, nbig, tau, MB, Tk);
             const int buf = i & 1;
+            // destination row and factor of column `lane`: the token's row of acc and p 2^2e (the h
+            // tile holds h 2^-2e; exact), or in stage mode the slot's row of yslot_out and 2^2e
             int tok = -1;
             float wgt = 0.f;
             if (lane < t.ntok) {
+                int tt = -1, f = -1;
                 if (t.shared_e) {
-                    tok = t.tok0 + lane;
-                    wgt = bf16_bits_to_float(P.w_s[tok]);
+                    tt = t.tok0 + lane;
+                    f = Tk + tt;
+                    wgt = bf16_bits_to_float(P.w_s[tt]);
                 } else {
                     const int pos = t.pbase + lane;
-                    const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                    f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
                     if (f < 0 || f >= Tk) {
                         record_status(P.status, MOE_ERR_DEVICE);
                     } else {
-                        tok = f / P.k;
+                        tt = f / P.k;
                         wgt = bf16_bits_to_float(P.p[f]);
+                    }
+                }
+                if (tt >= 0) {
+                    const float up = pow2f(__ldg(P.xe + tt));
+                    if (P.yslot_out != nullptr) {
+                        tok = f;
+                        wgt = up * up;
+                    } else {
+                        tok = tt;
+                        wgt = wgt * up * up;
                     }
                 }
             }
@@ -615,7 +651,8 @@ __global__ void __launch_bounds__(kSThreads2, 1)
             set_abort(s_abort, P.status);
             break;
         }
-        // acc[t, row] += w * y for the tile's rows and tokens
+        // acc[t, row] += w * y for the tile's rows and tokens (or the slot's row of yslot_out)
+        float *const dst_base = P.yslot_out != nullptr ? P.yslot_out : P.acc;
         const int *tok = s_tok + buf * kSmallN;
         const float *wv = s_w + buf * kSmallN;
 #pragma unroll
@@ -626,7 +663,7 @@ __global__ void __launch_bounds__(kSThreads2, 1)
                 const int erow = t.mb * 256 + r0 + 8 * (e >> 1);
                 if (col < ncol) {
                     const int tt = tok[col];
-                    if (tt >= 0) atomicAdd(P.acc + (size_t)tt * H + erow, wv[col] * acc[j][e]);
+                    if (tt >= 0) atomicAdd(dst_base + (size_t)tt * H + erow, wv[col] * acc[j][e]);
                 }
             }
         }
@@ -648,7 +685,7 @@ size_t small_g1_smem(int H)
 {
     const int G = H / kGroup;
     return 1024 + kG1Stages * kG1Stage + 2 * 8 * 32 * 16 * 4 + 2 * 4 * 128 * G * 2 + 2 * kSmallN * (G + 4) * 4 +
-           2 * 8 * 32 * 4 + 8 * (2 * kG1Stages + 4) + 16;
+           2 * 8 * 32 * 4 + 3 * kSmallN * 4 + 8 * (2 * kG1Stages + 4) + 16;
 }
 size_t small_g2_smem(int I)
 {
@@ -667,6 +704,9 @@ SmallParams small_params(const PrefillArgs &a, bool down)
     p.hs = a.hs;
     p.x16 = a.x16;
     p.xsum = a.xsum;
+    p.xe = a.xe;
+    p.h_out = a.h_out;
+    p.yslot_out = a.yslot_out;
     p.hsum = a.hsum;
     p.p = a.p;
     p.w_s = a.w_s;

@@ -192,86 +192,11 @@ def test_fused_routing_equals_route_kernel():
     assert np.array_equal(r["w_s"], f["w_s"])
 
 
-def _stages(layer, x_bits, ids, path):
-    sh = layer.shape
-    T = x_bits.shape[0]
-    nslot = T * (sh.top_k + sh.has_shared)
-    x = H.to_dev_u16(x_bits)
-    ws = qm.workspace(layer.cfg, T)
-    d_ids = torch.from_numpy(np.ascontiguousarray(ids, np.int32)).cuda()
-    counts = torch.empty(sh.n_experts, dtype=torch.int32, device="cuda")
-    offsets = torch.empty(sh.n_experts + 1, dtype=torch.int32, device="cuda")
-    perm = torch.empty(T * sh.top_k, dtype=torch.int32, device="cuda")
-    inv = torch.empty(T * sh.top_k, dtype=torch.int32, device="cuda")
-    qm.moe_permute(layer.cfg, d_ids, T, counts, offsets, perm, inv, ws)
-    h = torch.full((nslot, sh.inter), float("nan"), dtype=torch.float32, device="cuda")
-    ys = torch.full((nslot, sh.hidden), float("nan"), dtype=torch.float32, device="cuda")
-    qm.moe_expert_stages(layer.cfg, layer.w, x, T, d_ids, counts, offsets, perm, h, ys, path, ws)
-    torch.cuda.synchronize()
-    assert qm.moe_get_device_status(ws) == 0
-    return h.cpu().numpy().astype(np.float64), ys.cpu().numpy().astype(np.float64)
-
-
-def check_stages_against_fp64(wl, w, layer, x_bits, path):
-    """Each projection class on its own against an FP64 restatement fed the same inputs.
-
-    gate/up pair: h from the GPU against the oracle's h for the same x (the GPU rounds h to
-    fp16: 11 significant bits).  down: the GPU's slot output against the oracle's down
-    projection of the GPU's own h (no rounding on either side but fp32 sums).
-    """
-    sh = wl.shape
-    T, k = x_bits.shape[0], sh.top_k
-    ids = oracle.topk(oracle.router_logits(sh, w, x_bits), k)
-    h_gpu, y_gpu = _stages(layer, x_bits, ids, path)
-    xs = H.bf16_to_f64(x_bits)
-    worst_h, worst_y = 0.0, 0.0
-    for t in range(T):
-        slots = [(t * k + j, int(ids[t, j])) for j in range(k)]
-        if sh.has_shared:
-            slots.append((T * k + t, -1))
-        for f, e in slots:
-            h_ref, _ = oracle.expert_ffn(sh, w, e, xs[t])
-            dh = np.abs(h_gpu[f] - h_ref) / np.maximum(1.0, np.abs(h_ref))
-            worst_h = max(worst_h, float(dh.max()))
-            y_ref = oracle.expert_down(sh, w, e, h_gpu[f])
-            dy = np.abs(y_gpu[f] - y_ref) / np.maximum(1.0, np.abs(y_ref))
-            worst_y = max(worst_y, float(dy.max()))
-    # h: fp16 rounding (2^-11 relative) plus fp32 sums of g and u; down: fp32 sums of exact products
-    print(f"stage errors T={T} path={path}: h {worst_h:.3e}, down {worst_y:.3e}")
-    assert worst_h <= H.STAGE_H_TOL, worst_h
-    assert worst_y <= H.STAGE_DOWN_TOL, worst_y
-    return worst_h, worst_y
-
-
 @pytest.mark.parametrize("wl_index,T", [(0, 4), (1, 1), (2, 16)])
 def test_decode_stages_against_fp64(wl_index, T):
     wl, w, layer = H.device_layer(wl_index)
     x = synth.make_x(wl.shape, T, wl.seed, stream=6)
-    check_stages_against_fp64(wl, w, layer, x, qm.MOE_PATH_DECODE)
-
-
-def range_rows(shape, seed):
-    """Rows of x whose magnitudes leave the fp16 range: max |x| of 1e3, 7e4 and 1e6, a row entirely
-    below 2^-14 (the smallest fp16 normal), and an ordinary row."""
-    base = synth.bf16_bits_to_f32(synth.make_x(shape, 5, seed, stream=21)).astype(np.float64)
-    scale = np.array([1e3, 7e4, 1e6, 2.0 ** -20, 1.0])
-    rows = base / np.abs(base).max(axis=1, keepdims=True) * scale[:, None]
-    rows[4] = base[4]
-    return synth.f32_to_bf16_bits(rows.astype(np.float32))
-
-
-def check_rows_scale_free(y_gpu, y_ref):
-    """The output rule of check_y made independent of each row's scale: per-row relative RMS, and every
-    element within 4e-3 of the row's RMS (the plain 2e-2 bound at the workloads' output RMS of ~5) or
-    one bf16 rounding flip from the oracle."""
-    for t in range(y_ref.shape[0]):
-        g, r = H.bf16_to_f64(y_gpu[t]), H.bf16_to_f64(y_ref[t])
-        assert np.all(np.isfinite(g)), t
-        rms = np.sqrt((r ** 2).mean())
-        rel = np.sqrt(((g - r) ** 2).sum() / (r ** 2).sum())
-        assert rel <= H.REL_RMS_TOL, (t, rel)
-        beyond = np.abs(g - r) > 4e-3 * rms
-        assert H.ulp_diff_bf16(y_gpu[t][beyond], y_ref[t][beyond]).max(initial=0) <= 1, (t, rms)
+    H.check_stages_against_fp64(wl, w, layer, x, qm.MOE_PATH_DECODE)
 
 
 @pytest.mark.parametrize("wl_index", [0, 1])
@@ -279,13 +204,13 @@ def test_decode_rows_beyond_fp16_range(wl_index):
     """x far above the fp16 range, or entirely below its normal range: per-token power-of-two
     scaling keeps every 16-bit intermediate in range (routing pinned with the oracle's logits)."""
     wl, w, layer = H.device_layer(wl_index)
-    x = range_rows(wl.shape, wl.seed)
+    x = H.range_rows(wl.shape, wl.seed)
     lg = oracle.router_logits(wl.shape, w, x)
     got = H.run_forward(layer, x, path=qm.MOE_PATH_DECODE, logits_in=lg)
     assert got["status"] == 0
     ref = oracle.forward(wl.shape, w, x, logits_in=lg)
     assert np.array_equal(got["ids"], ref["ids"])
-    check_rows_scale_free(got["y"], ref["y"])
+    H.check_rows_scale_free(got["y"], ref["y"])
 
 
 @pytest.mark.parametrize("nstreams", [2, 4])

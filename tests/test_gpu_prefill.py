@@ -174,3 +174,36 @@ def test_staged_prefill_expert_ffn_accumulates():
     torch.cuda.synchronize()
     ref = oracle.forward(sh, w, x_bits)
     H.check_y(H.u16(y), ref["y"])
+
+
+@pytest.mark.parametrize("forced", [False, True])
+def test_prefill_rows_beyond_fp16_range(forced):
+    """x far above the fp16 range, or entirely below its normal range, on the prefill path.  Five rows
+    alone take the small-tile kernels (a few tokens per expert); the same rows repeated 40 times with
+    every token routed to experts 0..7 make tiles of up to 128 tokens of the tensor-memory GEMMs, each
+    tile mixing rows of max |x| 1e6 and 2^-20.  Per-token power-of-two scaling keeps every 16-bit
+    intermediate in range; routing is pinned with supplied logits."""
+    wl, w, layer = H.device_layer(1)
+    x = H.range_rows(wl.shape, wl.seed)
+    if forced:
+        x = np.tile(x, (40, 1))
+        lg = np.zeros((x.shape[0], wl.shape.n_experts), dtype=np.float32)
+        lg[:, :8] = np.arange(8, 0, -1, dtype=np.float32)
+    else:
+        lg = oracle.router_logits(wl.shape, w, x).astype(np.float32)
+    got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL, logits_in=lg)
+    assert got["status"] == 0
+    ref = oracle.forward(wl.shape, w, x, logits_in=lg)
+    assert np.array_equal(got["ids"], ref["ids"])
+    H.check_rows_scale_free(got["y"], ref["y"])
+
+
+@pytest.mark.parametrize("wl_index,T", [(0, 40), (3, 512), (4, 4096)])
+def test_prefill_stages_against_fp64(wl_index, T):
+    """h and the down projection of every slot on the prefill path against FP64 (the T = 4096 layer with
+    its Zipf router bias: hot experts go through the tensor-memory GEMMs, cold ones through the
+    small-tile kernels)."""
+    wl, w, layer = H.device_layer(wl_index)
+    x = synth.make_x(wl.shape, T, wl.seed, stream=6)
+    bias = synth.zipf_bias(wl.shape, wl.zipf_s, wl.seed) if getattr(wl, "zipf_s", None) else None
+    H.check_stages_against_fp64(wl, w, layer, x, qm.MOE_PATH_PREFILL, bias=bias)
