@@ -407,7 +407,7 @@ def cold_call_latency(W, stream, reps=20):
                 flush="512 MiB write before each call")
 
 
-TIMELINE = ["start", "router_published", "x_staged", "logits_seen", "topk_done", "list_done", "routing_done",
+TIMELINE = ["start", "router_published", "logits_seen", "x_staged", "topk_done", "list_done", "routing_done",
             "first_gate_chunk", "first_down_chunk", "first_down_done", "units_done", "units_counter",
             "combine_loads_done", "combine_done"]
 

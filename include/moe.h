@@ -271,7 +271,7 @@ MOE_API int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const
 /* Timeline of the last fused decode launch on `ws` (T <= 16, decode path):
  * synchronises `stream`, then copies per CTA fourteen %globaltimer stamps
  * (ns) to host_stamps [max_ctas, 14]: kernel start, router logits published,
- * x staged for the expert units, every logit seen, top-k done, expert list
+ * every logit seen, x staged for the expert units, top-k done, expert list
  * done, routing done, first gate chunk landed, first down chunk landed, first
  * down chunk computed, expert units done, unit counter reached, combine loads
  * done, combine done (a stamp that was not reached keeps an older value).

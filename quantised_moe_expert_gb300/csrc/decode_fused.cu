@@ -77,7 +77,7 @@ constexpr int kXG = 72;
 
 // Timeline stamps (trace columns), in the order a CTA reaches them.
 enum {
-    kStStart = 0, kStRouterPub, kStXStaged, kStLogitsSeen, kStTopk, kStListed, kStRouted, kStFirstGate,
+    kStStart = 0, kStRouterPub, kStLogitsSeen, kStXStaged, kStTopk, kStListed, kStRouted, kStFirstGate,
     kStFirstDown, kStFirstDownDone, kStUnitsDone, kStUnitsCnt, kStCombineLoads, kStCombined
 };
 
@@ -266,19 +266,72 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, long l
     return __all_sync(0xffffffffu, ok);
 }
 
+// x' for the MMAs of token t from its raw staged row, by one warp: lane l takes the row's 16-byte
+// chunks l, l + 32, ..., the warp finds the row's largest |x|, scales by 2^-e (exact), puts each chunk
+// of 8 in the codes' k order and sums each group of 64 (its 8 chunks sit in 8 consecutive lanes: a
+// fixed shuffle tree).
+__device__ __forceinline__ void convert_row(FSmem &S, const FusedDecodeArgs &a, const uint16_t *s_xr, uint16_t *s_x,
+                                            float *s_xs, int t)
+{
+    const int lane = threadIdx.x & 31, H = a.H, G = H / kGroup, XS = G * kXG + 8;
+    constexpr int kMaxChunks = 2048 / 8 / 32;          // chunks per lane at the largest H
+    const int cpl = H / 256;                            // chunks per lane
+    uint4 v[kMaxChunks];
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxChunks; ++i)
+        if (i < cpl) {
+            const int c = lane + 32 * i;
+            v[i] = *reinterpret_cast<const uint4 *>(s_xr + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8);
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7FFFu, w4[q] >> 16 & 0x7FFFu));
+        }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    const int xe = row_scale_exponent(mx);
+    const float sc = pow2f(-xe);
+#pragma unroll
+    for (int i = 0; i < kMaxChunks; ++i)
+        if (i < cpl) {
+            const int c = lane + 32 * i;                // chunk of the row; its group is c / 8
+            uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float lo = __uint_as_float(w[q] << 16) * sc, hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
+                w[q] = (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
+                sum += __uint_as_float(w[q] << 16);
+                sum += __uint_as_float(w[q] & 0xFFFF0000u);
+            }
+            *reinterpret_cast<uint4 *>(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8) =
+                kperm8(make_uint4(w[0], w[1], w[2], w[3]));
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            if ((c & 7) == 0) s_xs[t * G + (c >> 3)] = sum;
+        }
+    if (lane == 0) S.xe[t] = xe;
+}
+
 // ------------------------------------------------------------------ routing (all threads)
 //
 // Top-k of every token from the fp32 logits (one warp per token: lane l holds the keys of
 // experts l + 32 r; each round takes the largest key, then the lowest id holding it), or the
-// caller's ids.  Then, in parallel over the picks, a bitmap of the picked experts and per expert
-// the set of tokens that picked it; from those the distinct experts in increasing id (the shared
+// caller's ids; each pick is registered at once in a bitmap of the picked experts and, per expert,
+// the set of tokens that picked it.  x' of every token is formed meanwhile by other warps (warp w
+// converts tokens 9 - w, 19 - w before it polls tokens w, w + 10: the conversion fills the time the
+// logits take to arrive).  Then warp 0 alone: the distinct experts in increasing id (the shared
 // expert last), each expert's column count, and the column of pick (t, j): the expert's first
 // column plus the number of earlier tokens that picked the same expert.
 // logits: the caller's fp32 logits, or null for the logits this launch publishes (tagged with its epoch).
-__device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, const float *logits)
+__device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, const float *logits,
+                                               const uint16_t *s_xr, uint16_t *s_x, float *s_xs)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, E = a.E, k = a.k;
+    constexpr int kW = kThreads / 32;
+#pragma unroll 1
+    for (int t = kW - 1 - warp; t < T; t += kW) convert_row(S, a, s_xr, s_x, s_xs, t);
     if (a.ids_in) {
 #pragma unroll 1
         for (int i = tid; i < T * k; i += kThreads) {
@@ -287,12 +340,15 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
                 record_status(a.status, MOE_ERR_DEVICE);
                 e = 0;
             }
-            S.ids[i / k][i % k] = e;
+            const int t = i / k;
+            S.ids[t][i - t * k] = e;
+            atomicOr(&S.pickmap[e >> 5], 1u << (e & 31));
+            if (atomicOr(&S.tokmask[e], 1u << t) & (1u << t)) record_status(a.status, MOE_ERR_DEVICE);   // repeated id
         }
     } else {
         constexpr int RW = kMaxExperts / 32;
 #pragma unroll 1
-        for (int t = warp; t < T; t += kThreads / 32) {
+        for (int t = warp; t < T; t += kW) {
             uint32_t key[RW];
             if (logits) {
 #pragma unroll
@@ -356,20 +412,16 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
                         if (r == br) key[r] = 0u;
                     S.ids[t][j] = (int)id;
                     S.lg[t][j] = key_logit(mk);
+                    atomicOr(&S.pickmap[id >> 5], 1u << (id & 31));
+                    if (atomicOr(&S.tokmask[id], 1u << t) & (1u << t)) record_status(a.status, MOE_ERR_DEVICE);
                 }
             }
         }
     }
     if (a.ids_in || logits) stamp(a, kStLogitsSeen);
-    __syncthreads();
+    __syncthreads();                 // ids, the pick bitmap and token sets, and x' of every token complete
+    stamp(a, kStXStaged);
     stamp(a, kStTopk);
-#pragma unroll 1
-    for (int i = tid; i < T * k; i += kThreads) {
-        const int t = i / k, e = S.ids[t][i - t * k];
-        atomicOr(&S.pickmap[e >> 5], 1u << (e & 31));
-        if (atomicOr(&S.tokmask[e], 1u << t) & (1u << t)) record_status(a.status, MOE_ERR_DEVICE);   // repeated id
-    }
-    __syncthreads();
     if (warp == 0) {
         // lane l scans the experts [32 l, 32 l + 32): list positions and first columns by two scans
         const uint32_t bits = lane < (E + 31) / 32 ? S.pickmap[lane] : 0u;
@@ -405,26 +457,26 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
             S.colptr[D] = nc + (a.has_shared ? T : 0);
             S.nlist = D;
         }
+        __syncwarp();                // the list, positions and first columns of every lane
+#pragma unroll 1
+        for (int i = lane; i < T * k; i += 32) {
+            const int t = i / k, j = i - t * k, e = S.ids[t][j];
+            const int col = S.colptr[S.lpos[e]] + __popc(S.tokmask[e] & ((1u << t) - 1u));
+            S.colof[t][j] = col;
+            S.colf[col] = i;
+            S.ctok[col] = t;
+        }
+        if (a.has_shared)
+#pragma unroll 1
+            for (int t = lane; t < T; t += 32) {
+                const int col = S.colptr[S.nlist - 1] + t;
+                S.colof[t][k] = col;
+                S.colf[col] = T * k + t;
+                S.ctok[col] = t;
+            }
     }
     __syncthreads();
     stamp(a, kStListed);
-#pragma unroll 1
-    for (int i = tid; i < T * k; i += kThreads) {
-        const int t = i / k, j = i - t * k, e = S.ids[t][j];
-        const int col = S.colptr[S.lpos[e]] + __popc(S.tokmask[e] & ((1u << t) - 1u));
-        S.colof[t][j] = col;
-        S.colf[col] = i;
-        S.ctok[col] = t;
-    }
-    if (a.has_shared)
-#pragma unroll 1
-        for (int t = tid; t < T; t += kThreads) {
-            const int col = S.colptr[S.nlist - 1] + t;
-            S.colof[t][k] = col;
-            S.colf[col] = T * k + t;
-            S.ctok[col] = t;
-        }
-    __syncthreads();
 }
 
 // ------------------------------------------------------------------ per-token weights (aux warp)
@@ -580,58 +632,6 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
         for (int q = issued > R ? issued - R : 0; q < issued; ++q)
             mbar_wait(smem_u32(&S.full[q % R]), (q / R) & 1, kDrainLimit, nullptr);
     __syncwarp();
-}
-
-// x' for the MMAs from the raw staged rows, one warp per token (every warp of the CTA): lane l takes
-// the row's 16-byte chunks l, l + 32, ..., the warp finds the row's largest |x|, scales by 2^-e
-// (exact), puts each chunk of 8 in the codes' k order and sums each group of 64 (its 8 chunks sit
-// in 8 consecutive lanes: a fixed shuffle tree).
-__device__ __forceinline__ void convert_x(FSmem &S, const FusedDecodeArgs &a, const uint16_t *s_xr, uint16_t *s_x,
-                                          float *s_xs)
-{
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, T = a.T, H = a.H, G = H / kGroup, XS = G * kXG + 8;
-    {
-        constexpr int kMaxChunks = 2048 / 8 / 32;          // chunks per lane at the largest H
-        const int cpl = H / 256;                            // chunks per lane
-#pragma unroll 1
-        for (int t = warp; t < T; t += kThreads / 32) {
-            uint4 v[kMaxChunks];
-            uint32_t mx = 0;
-#pragma unroll
-            for (int i = 0; i < kMaxChunks; ++i)
-                if (i < cpl) {
-                    const int c = lane + 32 * i;
-                    v[i] = *reinterpret_cast<const uint4 *>(s_xr + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8);
-                    const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7FFFu, w4[q] >> 16 & 0x7FFFu));
-                }
-            mx = __reduce_max_sync(0xffffffffu, mx);
-            const int xe = row_scale_exponent(mx);
-            const float sc = pow2f(-xe);
-#pragma unroll
-            for (int i = 0; i < kMaxChunks; ++i)
-                if (i < cpl) {
-                    const int c = lane + 32 * i;                // chunk of the row; its group is c / 8
-                    uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-                    float sum = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float lo = __uint_as_float(w[q] << 16) * sc, hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
-                        w[q] = (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
-                        sum += __uint_as_float(w[q] << 16);
-                        sum += __uint_as_float(w[q] & 0xFFFF0000u);
-                    }
-                    *reinterpret_cast<uint4 *>(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8) =
-                        kperm8(make_uint4(w[0], w[1], w[2], w[3]));
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                    if ((c & 7) == 0) s_xs[t * G + (c >> 3)] = sum;
-                }
-            if (lane == 0) S.xe[t] = xe;
-        }
-    }
 }
 
 // ------------------------------------------------------------------ consumers (warps 0-7)
@@ -858,16 +858,19 @@ __device__ __forceinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a
         S.ws[t] = bf16_bits_to_float(wb);
     }
     const int nitem = T * nq * NS;
+    // item it: the quad q varies fastest, so the threads of one (token, slot) read the 4 nq consecutive
+    // rows of each slice's partial sums (and of the scale and bias rows) as one contiguous block
 #pragma unroll 1
     for (int it = tid; it < nitem; it += kThreads) {
-        const int j = it % NS, rest = it / NS, q = rest % nq, t = rest / nq;
+        const int q = it % nq, rest = it / nq, j = rest % NS, t = rest / NS;
+        const int sidx = (t * nq + q) * NS + j;          // slot-order position of the item's terms
         const bool shr = j == k;
         const int e = shr ? 0 : S.ids[t][j];
         const int col = S.colof[t][j];
         const int r = r0 + 4 * q;
         if (e < 0 || e >= a.E || col < 0 || col >= S.colptr[S.nlist]) {   // out of range: report, skip
             record_status(a.status, MOE_ERR_DEVICE);
-            s_t[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+            s_t[sidx] = make_float4(0.f, 0.f, 0.f, 0.f);
             continue;
         }
         const QMatDev &dm = shr ? a.s_down : a.down;
@@ -923,7 +926,7 @@ __device__ __forceinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a
         }
         const float up = pow2f(S.xe[t]);
         const float4 v = make_float4(ye[0] * up * up, ye[1] * up * up, ye[2] * up * up, ye[3] * up * up);
-        s_t[it] = v;
+        s_t[sidx] = v;
         if (a.yslot_out) {
             const int f = shr ? T * k + t : t * k + j;
             *reinterpret_cast<float4 *>(a.yslot_out + (size_t)f * H + r) = v;
@@ -1117,22 +1120,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     stamp(a, kStRouterPub);
 
-    // ---- x' for the expert units (from the raw rows in the ring area), then the ring area is handed
-    // to the copy engine: the generic-proxy reads of it are ordered before the first copy into it
-    convert_x(S, a, s_xr, s_x, s_xs);
-    fence_proxy_async_smem();
-    __syncthreads();
-    stamp(a, kStXStaged);
-
-
+    // ---- routing, and x' for the expert units from the raw rows in the ring area (route_and_list)
     int U = 0;
     if (!S.abort) {
-        route_and_list(S, a, a.logits_in);
+        route_and_list(S, a, a.logits_in, s_xr, s_x, s_xs);
         U = S.nlist * SL;
     }
     stamp(a, kStRouted);
-    // every warp takes its role or none: the flag is read before any role may set it
+    // every warp takes its role or none: the flag is read before any role may set it; the ring area is
+    // handed to the copy engine after this barrier (its generic-proxy reads are ordered before it)
     const bool go = !S.abort;
+    fence_proxy_async_smem();
     __syncthreads();
 
     if (go) {
