@@ -667,76 +667,96 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             tA[j] = cA < ncol ? S.ctok[colbase + cA] : -1;
             tB[j] = cA + 1 < ncol ? S.ctok[colbase + cA + 1] : -1;
         }
-        // the gate chunk, then the up chunk, each computed by all eight warps: warp w takes the 16-row
-        // tile mt = w % 2 and the groups of quarter kq = w / 2 of the input dimension
-        bool ok = !fail_d;
+        // the gate and up chunks in one pass, by all eight warps: warp w takes the 16-row tile mt = w % 2
+        // and the groups of quarter kq = w / 2 of the input dimension of both matrices, so each x
+        // fragment and group sum serves both and the two MMA chains interleave
+        const int qg = 3 * i, qu = qg + 1, slotg = qg % R, slotu = qu % R;
+        bool ok = !fail_d && warp_wait(&S.full[slotg], (qg / R) & 1, limit, &S.abort);
+        if (i == 0) stamp(a, kStFirstGate);
+        ok = ok && warp_wait(&S.full[slotu], (qu / R) & 1, limit, &S.abort);
+        if (ok) {
+            const uint8_t *chg = ring + (size_t)slotg * geo.slot, *chu = ring + (size_t)slotu * geo.slot;
+            const uint8_t *cbg = chg + (mt * 16 + g) * 128, *cbu = chu + (mt * 16 + g) * 128;   // row mt 16 + g of every 4 KB box
+            const uint16_t *scg = reinterpret_cast<const uint16_t *>(chg + geo.codes1) + (mt * 16 + g) * G;
+            const uint16_t *scu = reinterpret_cast<const uint16_t *>(chu + geo.codes1) + (mt * 16 + g) * G;
+            const uint16_t *big = scg + kSlice * G, *biu = scu + kSlice * G;
+            float accg[NT][4], accu[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) accg[j][v] = accu[j][v] = 0.f;
 #pragma unroll 1
-        for (int m = 0; m < 2; ++m) {
-            const int q1 = 3 * i + m, slot1 = q1 % R;
-            ok = ok && warp_wait(&S.full[slot1], (q1 / R) & 1, limit, &S.abort);
-            if (i == 0 && m == 0) stamp(a, kStFirstGate);
-            if (ok) {
-                const uint8_t *chunk = ring + (size_t)slot1 * geo.slot;
-                const uint8_t *cb = chunk + (mt * 16 + g) * 128;              // row mt 16 + g of every 4 KB box
-                const uint16_t *scs = reinterpret_cast<const uint16_t *>(chunk + geo.codes1) + (mt * 16 + g) * G;
-                const uint16_t *bis = scs + kSlice * G;
-                float acc[NT][4];
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) acc[j][v] = 0.f;
-#pragma unroll 2
-                for (int gi = 0; gi < gq; ++gi) {
-                    const int grp = kq * gq + gi, q = grp & 3;
-                    const uint32_t o = (uint32_t)(grp >> 2) * (kSlice * 128) + swz_chunk(q, g, t4);
-                    const uint2 c0 = *reinterpret_cast<const uint2 *>(cb + o);
-                    const uint2 c1 = *reinterpret_cast<const uint2 *>(cb + o + 1024);
-                    const float s0 = bf16_bits_to_float(scs[grp]), s1 = bf16_bits_to_float(scs[8 * G + grp]);
-                    const float k0 = fmaf(-128.f, s0, bf16_bits_to_float(bis[grp]));
-                    const float k1 = fmaf(-128.f, s1, bf16_bits_to_float(bis[8 * G + grp]));
-                    uint32_t a0[8], a1[8];
-                    nib8<false>(c0.x, a0);
-                    nib8<false>(c0.y, a0 + 4);
-                    nib8<false>(c1.x, a1);
-                    nib8<false>(c1.y, a1 + 4);
-#pragma unroll
-                    for (int j = 0; j < NT; ++j) {
-                        if (j * 8 >= ncol) break;
-                        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                        if (xrow[j] >= 0) {
-                            const uint4 *xr = reinterpret_cast<const uint4 *>(s_x + (size_t)xrow[j] * XS + grp * kXG) +
-                                              2 * t4;
-                            lo = xr[0];
-                            hi = xr[1];
-                        }
-                        const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                        float dd[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int mm = 0; mm < 4; ++mm)
-                            mma16816<false>(dd, a0[2 * mm], a1[2 * mm], a0[2 * mm + 1], a1[2 * mm + 1], bp[2 * mm],
-                                            bp[2 * mm + 1]);
-                        const float xA = tA[j] >= 0 ? s_xs[tA[j] * G + grp] : 0.f;
-                        const float xB = tB[j] >= 0 ? s_xs[tB[j] * G + grp] : 0.f;
-                        acc[j][0] = fmaf(s0, dd[0], fmaf(k0, xA, acc[j][0]));
-                        acc[j][1] = fmaf(s0, dd[1], fmaf(k0, xB, acc[j][1]));
-                        acc[j][2] = fmaf(s1, dd[2], fmaf(k1, xA, acc[j][2]));
-                        acc[j][3] = fmaf(s1, dd[3], fmaf(k1, xB, acc[j][3]));
-                    }
-                }
-                float *red = s_red + ((size_t)(m * 4 + kq) * kSlice + mt * 16) * NC;   // [32 rows][NC]
+            for (int gi = 0; gi < gq; ++gi) {
+                const int grp = kq * gq + gi, q = grp & 3;
+                const uint32_t o = (uint32_t)(grp >> 2) * (kSlice * 128) + swz_chunk(q, g, t4);
+                const uint2 g0 = *reinterpret_cast<const uint2 *>(cbg + o), g1 = *reinterpret_cast<const uint2 *>(cbg + o + 1024);
+                const uint2 u0 = *reinterpret_cast<const uint2 *>(cbu + o), u1 = *reinterpret_cast<const uint2 *>(cbu + o + 1024);
+                const float sg0 = bf16_bits_to_float(scg[grp]), sg1 = bf16_bits_to_float(scg[8 * G + grp]);
+                const float su0 = bf16_bits_to_float(scu[grp]), su1 = bf16_bits_to_float(scu[8 * G + grp]);
+                const float kg0 = fmaf(-128.f, sg0, bf16_bits_to_float(big[grp]));
+                const float kg1 = fmaf(-128.f, sg1, bf16_bits_to_float(big[8 * G + grp]));
+                const float ku0 = fmaf(-128.f, su0, bf16_bits_to_float(biu[grp]));
+                const float ku1 = fmaf(-128.f, su1, bf16_bits_to_float(biu[8 * G + grp]));
+                uint32_t ag0[8], ag1[8], au0[8], au1[8];
+                nib8<false>(g0.x, ag0);
+                nib8<false>(g0.y, ag0 + 4);
+                nib8<false>(g1.x, ag1);
+                nib8<false>(g1.y, ag1 + 4);
+                nib8<false>(u0.x, au0);
+                nib8<false>(u0.y, au0 + 4);
+                nib8<false>(u1.x, au1);
+                nib8<false>(u1.y, au1 + 4);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    const int c0 = j * 8 + 2 * t4;
-                    red[g * NC + c0] = acc[j][0];
-                    red[g * NC + c0 + 1] = acc[j][1];
-                    red[(g + 8) * NC + c0] = acc[j][2];
-                    red[(g + 8) * NC + c0 + 1] = acc[j][3];
+                    if (j * 8 >= ncol) break;
+                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                    if (xrow[j] >= 0) {
+                        const uint4 *xr = reinterpret_cast<const uint4 *>(s_x + (size_t)xrow[j] * XS + grp * kXG) + 2 * t4;
+                        lo = xr[0];
+                        hi = xr[1];
+                    }
+                    const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int mm = 0; mm < 4; ++mm) {
+                        mma16816<false>(dg, ag0[2 * mm], ag1[2 * mm], ag0[2 * mm + 1], ag1[2 * mm + 1], bp[2 * mm],
+                                        bp[2 * mm + 1]);
+                        mma16816<false>(du, au0[2 * mm], au1[2 * mm], au0[2 * mm + 1], au1[2 * mm + 1], bp[2 * mm],
+                                        bp[2 * mm + 1]);
+                    }
+                    const float xA = tA[j] >= 0 ? s_xs[tA[j] * G + grp] : 0.f;
+                    const float xB = tB[j] >= 0 ? s_xs[tB[j] * G + grp] : 0.f;
+                    accg[j][0] = fmaf(sg0, dg[0], fmaf(kg0, xA, accg[j][0]));
+                    accg[j][1] = fmaf(sg0, dg[1], fmaf(kg0, xB, accg[j][1]));
+                    accg[j][2] = fmaf(sg1, dg[2], fmaf(kg1, xA, accg[j][2]));
+                    accg[j][3] = fmaf(sg1, dg[3], fmaf(kg1, xB, accg[j][3]));
+                    accu[j][0] = fmaf(su0, du[0], fmaf(ku0, xA, accu[j][0]));
+                    accu[j][1] = fmaf(su0, du[1], fmaf(ku0, xB, accu[j][1]));
+                    accu[j][2] = fmaf(su1, du[2], fmaf(ku1, xA, accu[j][2]));
+                    accu[j][3] = fmaf(su1, du[3], fmaf(ku1, xB, accu[j][3]));
                 }
             }
-            // a warp releases a chunk only once it has landed (its wait succeeded): otherwise the
-            // producer could issue the next copy into a slot whose copy is still in flight
-            __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(smem_u32(&S.empty[slot1]));
+            float *redg = s_red + ((size_t)(0 * 4 + kq) * kSlice + mt * 16) * NC;   // [32 rows][NC]
+            float *redu = s_red + ((size_t)(1 * 4 + kq) * kSlice + mt * 16) * NC;
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int c0 = j * 8 + 2 * t4;
+                redg[g * NC + c0] = accg[j][0];
+                redg[g * NC + c0 + 1] = accg[j][1];
+                redg[(g + 8) * NC + c0] = accg[j][2];
+                redg[(g + 8) * NC + c0 + 1] = accg[j][3];
+                redu[g * NC + c0] = accu[j][0];
+                redu[g * NC + c0 + 1] = accu[j][1];
+                redu[(g + 8) * NC + c0] = accu[j][2];
+                redu[(g + 8) * NC + c0 + 1] = accu[j][3];
+            }
+        }
+        // a warp releases the chunks only once both have landed (its waits succeeded): otherwise the
+        // producer could issue the next copy into a slot whose copy is still in flight
+        __syncwarp();
+        if (lane == 0 && ok) {
+            mbar_arrive(smem_u32(&S.empty[slotg]));
+            mbar_arrive(smem_u32(&S.empty[slotu]));
         }
         if (!ok && lane == 0) {
             S.abort = 1;
