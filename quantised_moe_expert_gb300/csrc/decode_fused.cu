@@ -393,6 +393,7 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
                 }
                 if (t == 0) stamp(a, kStLogitsSeen);
             }
+            int pick = 0;
 #pragma unroll 1
             for (int j = 0; j < k; ++j) {
                 uint32_t bk = key[0];
@@ -412,9 +413,14 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
                         if (r == br) key[r] = 0u;
                     S.ids[t][j] = (int)id;
                     S.lg[t][j] = key_logit(mk);
-                    atomicOr(&S.pickmap[id >> 5], 1u << (id & 31));
-                    if (atomicOr(&S.tokmask[id], 1u << t) & (1u << t)) record_status(a.status, MOE_ERR_DEVICE);
                 }
+                if (lane == j) pick = (int)id;
+            }
+            // every pick registered at once, lane j pick j: the bitmap of picked experts and each
+            // expert's set of tokens (a repeated id is reported)
+            if (lane < k) {
+                atomicOr(&S.pickmap[pick >> 5], 1u << (pick & 31));
+                if (atomicOr(&S.tokmask[pick], 1u << t) & (1u << t)) record_status(a.status, MOE_ERR_DEVICE);
             }
         }
     }
@@ -685,7 +691,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             for (int j = 0; j < NT; ++j)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) accg[j][v] = accu[j][v] = 0.f;
-#pragma unroll 1
+#pragma unroll 2
             for (int gi = 0; gi < gq; ++gi) {
                 const int grp = kq * gq + gi, q = grp & 3;
                 const uint32_t o = (uint32_t)(grp >> 2) * (kSlice * 128) + swz_chunk(q, g, t4);
@@ -811,7 +817,8 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             }
             const int MT = H / (16 * kCW);
             float *pbase = part + (size_t)colbase * SL * H + (size_t)s * H;
-#pragma unroll 1
+            // independent 16-row tiles: four per iteration give the warp four chains to overlap
+#pragma unroll 4
             for (int tt = 0; tt < MT; ++tt) {
                 const int r0 = (warp * MT + tt) * 16 + g;
                 const uint32_t w0 = *reinterpret_cast<const uint32_t *>(dch + r0 * 16 + 4 * t4);
