@@ -1,12 +1,14 @@
 """Throughput of the routed-expert MoE layer on GB300, in tokens/s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference] [--no-sweep]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C | --workload NAME]
+                    [--impl ours|reference] [--no-sweep]
 
 A step is one forward of the whole layer (router GEMV, top-k, permutation,
 expert FFNs, combine) over one batch of T tokens, through the C ABI.  The
 default workload is the T = 1 decode layer (hidden 2048, 256 experts, top-8 +
 shared, intermediate 512, int4 g64 experts, 8-bit router); --config picks
-another of the named workloads in quantised_moe_expert_gb300.synth.WORKLOADS.
+another of the named workloads in quantised_moe_expert_gb300.synth.WORKLOADS,
+--workload any workload by name (the 8-bit expert layers of WORKLOADS_B8 too).
 
 Timing: W warm-up steps, then exactly K steps replayed from one CUDA graph,
 bracketed by a barrier and a device synchronize, timed with CUDA events on
@@ -51,6 +53,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--workload", default=None,
+                    help="a workload by name (any of synth.WORKLOADS or synth.WORKLOADS_B8); overrides --config")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -230,9 +234,13 @@ class Workload:
         return self.qm.MOE_PATH_DECODE if self.wl.tokens <= 16 else self.qm.MOE_PATH_PREFILL
 
     def kernels_per_step(self):
-        # decode: the one fused kernel; prefill: router GEMV (gamma), router MMA, top-k, permute,
-        # x conversion, accumulator zeroing, two small-tile and two tensor-memory GEMMs, combine
-        return 1 if self.wl.tokens <= 16 else 11
+        # decode: the one fused kernel (8-bit experts: router GEMV, top-k, permute, gate/up, down,
+        # reduce); prefill: router GEMV (gamma), router MMA, top-k, permute, x conversion, accumulator
+        # zeroing, two small-tile (4-bit experts only) and two tensor-memory GEMMs, combine
+        b8 = self.wl.shape.bits == 8
+        if self.wl.tokens <= 16:
+            return 6 if b8 else 1
+        return 9 if b8 else 11
 
     def distinct_experts(self):
         """Distinct routed experts (plus the shared expert) of each copy whose step was executed."""
@@ -499,9 +507,9 @@ def cpu_model():
 
 def oracle_single_core(wl, seconds=5.0):
     """The same oracle sample on one core: a fresh process with OMP_NUM_THREADS=1."""
-    code = ("import sys, json; sys.path.insert(0, %r); import bench; from quantised_moe_expert_gb300 import synth; "
-            "r, n, dt = bench.oracle_sample(synth.WORKLOADS[%d], seconds=%r); print(json.dumps(r))"
-            % (ROOT, synth.WORKLOADS.index(wl), seconds))
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
+            "r, n, dt = bench.oracle_sample(bench.workload_named(%r), seconds=%r); print(json.dumps(r))"
+            % (ROOT, wl.name, seconds))
     env = dict(os.environ, OMP_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
     try:
         out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120, env=env)
@@ -565,7 +573,8 @@ def stage_roofline(wl, st, hbm, tc, peak_src):
         ach = st["expert_bytes"] / (st["ms"] / 1e3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                 "traffic": traffic_for("decode_expert_ffn", wl.name),
-                "kernel": "expert-FFN stage (fused decode kernel: units + combine)",
+                "kernel": ("expert-FFN stage (decode gate/up, down and reduce kernels)" if wl.shape.bits == 8
+                           else "expert-FFN stage (fused decode kernel: units + combine)"),
                 "kernel_us": st["ms"] * 1e3, "algorithmic_bytes_per_launch": st["expert_bytes"],
                 "peak_source": peak_src}
     if st["flops"] / max(st["expert_bytes"], 1.0) < tc * 1e12 / (hbm * 1e9):
@@ -599,9 +608,16 @@ def traffic_for(kernel_key, workload):
         return None
 
 
+def workload_named(name):
+    for wl in synth.WORKLOADS + synth.WORKLOADS_B8:
+        if wl.name == name:
+            return wl
+    raise SystemExit(f"unknown workload {name!r}")
+
+
 def main():
     args = parse()
-    wl = synth.WORKLOADS[args.config]
+    wl = workload_named(args.workload) if args.workload else synth.WORKLOADS[args.config]
     steps = args.steps or default_steps(wl)
     warmup = max(3, args.warmup if args.warmup is not None else 20)
     if args.impl == "reference":
@@ -628,10 +644,11 @@ def main():
     roof = stage_roofline(wl, r["stage"], hbm, tc, peak_src)
     line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": steps,
             "warmup": warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int4-affine/bf16 in, fp32 accumulate", "data": "synthetic",
+            "vs_baseline": None, "dtype": f"int{wl.shape.bits}-affine/bf16 in, fp32 accumulate", "data": "synthetic",
             "config": {"workload": wl.name, "tokens": wl.tokens, "hidden": wl.shape.hidden,
                        "inter": wl.shape.inter, "experts": wl.shape.n_experts, "top_k": wl.shape.top_k,
-                       "shared": wl.shape.has_shared, "parallelism": f"replicas x{world}",
+                       "shared": wl.shape.has_shared, "expert_bits": wl.shape.bits,
+                       "parallelism": f"replicas x{world}",
                        "l2": f"{r['copies']} rotating weight copies and inputs: no step finds its weights in L2"},
             "roofline": roof,
             "layer_hbm": {"bytes_per_step": r["bytes_step"], "achieved_gbs": r["bytes_step"] / (r["ms_per_step"] / 1e3) / 1e9,
@@ -653,9 +670,8 @@ def main():
         line["cpu_baseline"] = cb
     if not args.no_sweep and rank == 0:
         sweep = {}
-        for ci, other in enumerate(synth.WORKLOADS):
-            if ci in (0, args.config):
-                continue
+        others = [o for o in synth.WORKLOADS + synth.WORKLOADS_B8 if o.name != wl.name and o.tokens > 4]
+        for other in others:
             try:
                 rr = run_ours(args, other, 0, 1, None, default_steps(other) // 2, 3, want_extras=False)
                 sweep[other.name] = {"value": rr["value"], "ms_per_step": rr["ms_per_step"],

@@ -17,7 +17,11 @@
  *   6. y = bf16( sum_j p_j y_{e_j} + w_s y_shared ), rounded once.
  * Weights are MLX affine quantised (same slice): experts 4-bit, router 8-bit,
  * groups of 64 consecutive inputs of one output row sharing a bf16 scale s
- * and bias b, w = s * q + b.
+ * and bias b, w = s * q + b.  The page's slice "8-bit experts" (the same
+ * rule with expert codes q in [0, 255]) is supported too: moe_config.bits = 8.
+ * Code layout: a row of n inputs holds n * bits / 8 bytes; at 4 bits input j
+ * is the low nibble of byte j / 2 for even j and the high nibble for odd j,
+ * at 8 bits input j is byte j.
  *
  * Conventions shared by every entry point
  *   - Every function returns an int status (enum moe_status).  Argument,
@@ -91,7 +95,7 @@ enum moe_path {
     MOE_PATH_PREFILL = 2   /* tcgen05 grouped GEMM kernels (any T >= 1) */
 };
 
-/* Layer shape and per-call options.  Supported: group == 64, bits == 4,
+/* Layer shape and per-call options.  Supported: group == 64, bits == 4 or 8,
  * router_bits == 8, hidden and inter multiples of 64 (hidden <= 8192,
  * inter <= 4096), 1 <= top_k <= min(n_experts, 16), 1 <= n_experts <= 256,
  * has_shared in {0,1}.  Anything else returns MOE_ERR_UNSUPPORTED.
@@ -103,7 +107,11 @@ enum moe_path {
  * fused decode kernel (T <= 16) it bounds the waits on other CTAs (published
  * router logits, the grid-wide unit counter); a CTA's waits on its own
  * shared-memory copies keep a fixed bound of the same order, so that a small
- * limit never leaves the copy ring in mid-flight. */
+ * limit never leaves the copy ring in mid-flight.
+ * With bits == 8 the decode path runs the weight-streaming gate/up, down and
+ * reduce kernels after the routing kernels (the fused decode kernel and the
+ * packed down layout are for 4-bit codes), and the prefill path runs every
+ * expert on the tensor-memory GEMMs. */
 typedef struct moe_config {
     int hidden;       /* H */
     int inter;        /* I, intermediate size of every expert, shared included */
@@ -233,7 +241,8 @@ MOE_API int moe_forward_decode_static(const moe_config *cfg, const moe_weights *
                                       const float *router_bias, const float *logits_in, uint16_t *y,
                                       int32_t *ids_out, uint16_t *p_out, uint16_t *w_shared_out, void *stream);
 
-/* Writes the decode layout of the 4-bit down codes: for expert e and column
+/* Writes the decode layout of the 4-bit down codes (bits == 4 only, else
+ * MOE_ERR_UNSUPPORTED): for expert e and column
  * slice c (32 columns of the intermediate dimension, 16 bytes of every row),
  *   down_packed[((e * (I/32) + c) * H + r) * 16 + b] = down.codes[(e * H + r) * I/2 + c * 16 + b]
  * and the same for the shared expert into s_down_packed (skipped when NULL or
@@ -262,7 +271,9 @@ MOE_API int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *
  * yslot_out must be zero-filled by the caller (the down GEMM adds each tile's
  * rows into it).  Rows of h_out / yslot_out of slots that do not exist (the
  * shared rows without a shared expert) are not written.  Returns
- * MOE_ERR_UNSUPPORTED for a path whose kernels cannot emit their stages. */
+ * MOE_ERR_UNSUPPORTED for a path whose kernels cannot emit their stages (the
+ * decode path of a layer that does not take the fused decode kernel: bits == 8,
+ * or a shape outside its shared-memory plan). */
 MOE_API int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T,
                               const int32_t *ids, const int32_t *counts, const int32_t *offsets,
                               const int32_t *perm, float *h_out, float *yslot_out, int path,

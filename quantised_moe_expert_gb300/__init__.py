@@ -140,7 +140,8 @@ class DeviceLayer:
     """One layer's weights resident on a CUDA device, plus the C weight struct.
 
     pack=True also makes the decode layout of the down codes (moe_pack_down) and hands it to the
-    library in moe_weights.down_packed / s_down_packed."""
+    library in moe_weights.down_packed / s_down_packed (4-bit experts only: the layout and the fused
+    decode kernel that reads it are for 4-bit codes)."""
 
     def __init__(self, host, device="cuda", pack: bool = True):
         self.shape = host.shape
@@ -164,7 +165,7 @@ class DeviceLayer:
         self.w = moe_weights(q("router", host.router), q("gate", host.gate), q("up", host.up),
                              q("down", host.down), q("s_gate", host.s_gate), q("s_up", host.s_up),
                              q("s_down", host.s_down), up("v", host.shared_gate_vec).data_ptr(), None, None)
-        if pack:
+        if pack and host.shape.bits == 4:
             self.pack()
 
     def pack(self):

@@ -18,14 +18,25 @@
 // rounding before fp32 accumulation is the fp16 storage of h (11 significant
 // bits: bf16's 8 would put the layer output outside the parity tolerance).
 //
-// Fragment layout.  Thread (g = lane/4, t = lane%4) loads 8 bytes (16 codes) of
-// rows g and g+8 of a group: bytes 8t..8t+7.  A u32 of 8 nibbles splits into
-// four bf16x2 registers holding elements (0,4) (1,5) (2,6) (3,7); MMA m of the
-// group's four takes registers 2m, 2m+1.  The MMA's k order is therefore a
-// permutation of the group's inputs; the B fragment (x or h) is permuted the
-// same way with byte permutes, so each product still pairs w_j with x_j.
-// Every output element is one column of the MMA and never mixes tokens, so a
-// token's result does not depend on the batch it is in.
+// Fragment layout.  Thread (g = lane/4, t = lane%4) loads the 16 codes of
+// inputs 16t..16t+15 of rows g and g+8 of a group (8 bytes of 4-bit codes, 16
+// bytes of 8-bit codes).  Eight codes split into four bf16x2 registers holding
+// elements (0,4) (1,5) (2,6) (3,7); MMA m of the group's four takes registers
+// 2m, 2m+1.  The MMA's k order is therefore a permutation of the group's inputs;
+// the B fragment (x or h) is permuted the same way with byte permutes, so each
+// product still pairs w_j with x_j.  Every output element is one column of the
+// MMA and never mixes tokens, so a token's result does not depend on the batch
+// it is in.
+//
+// 8-bit codes (the "8-bit experts" slice of the page on Qwen3.6-35B-A3B on the
+// native Metal engine: the same affine rule with q in [0, 255]).  1024 + q is
+// still exact in fp16, so the down projection only swaps the code expansion.
+// In bf16 only 128 + n with n < 128 is exact, so the gate/up projection splits
+// q = 16 qh + ql into nibbles and runs two code chains:
+//     sum_j q_j x_j = 16 sum_j (128 + qh_j) x_j + sum_j (128 + ql_j) x_j - 2176 sum_j x_j,
+// with the 2176 folded into the bias term as for the 4-bit codes.
+#include <type_traits>
+
 #include "kernels.cuh"
 
 namespace qmoe {
@@ -70,6 +81,40 @@ __device__ __forceinline__ void nib8(uint32_t u, uint32_t *r)
     r[3] = ((u >> 12) & 0x000F000Fu) | base;
 }
 
+// Byte pairs (0,4), (1,5), (2,6), (3,7) of 8 byte codes (u0: codes 0-3, u1: codes 4-7), each pair in
+// bytes 0 and 2 of a word (bytes 1 and 3 are copies, masked off by the callers).
+__device__ __forceinline__ void byte_pairs(uint32_t u0, uint32_t u1, uint32_t *t)
+{
+    t[0] = prmt(u0, u1, 0x4400u);
+    t[1] = prmt(u0, u1, 0x5511u);
+    t[2] = prmt(u0, u1, 0x6622u);
+    t[3] = prmt(u0, u1, 0x7733u);
+}
+
+// 16 byte codes -> eight fp16x2 of 1024 + q (exact), elements (0,4) (1,5) (2,6) (3,7) (8,12) ... (11,15).
+__device__ __forceinline__ void byte16_f16(uint4 c, uint32_t *r)
+{
+    uint32_t t[8];
+    byte_pairs(c.x, c.y, t);
+    byte_pairs(c.z, c.w, t + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = (t[i] & 0x00FF00FFu) | 0x64006400u;
+}
+
+// 16 byte codes -> eight bf16x2 of 128 + ql (lo) and eight of 128 + qh (hi), q = 16 qh + ql, in the
+// element order of byte16_f16.
+__device__ __forceinline__ void byte16_nibbles(uint4 c, uint32_t *lo, uint32_t *hi)
+{
+    uint32_t t[8];
+    byte_pairs(c.x, c.y, t);
+    byte_pairs(c.z, c.w, t + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        lo[i] = (t[i] & 0x000F000Fu) | 0x43004300u;
+        hi[i] = ((t[i] >> 4) & 0x000F000Fu) | 0x43004300u;
+    }
+}
+
 // 16 consecutive bf16 (two uint4) -> eight bf16x2 in the codes' element order.
 __device__ __forceinline__ void permute_b(const uint4 &lo, const uint4 &hi, uint32_t *b)
 {
@@ -86,21 +131,53 @@ __device__ __forceinline__ void permute_b(const uint4 &lo, const uint4 &hi, uint
 // One group (64 inputs) of a 16-row block against one n8 tile of B:
 // codes u64 of rows g / g+8, B registers bp[8]; accumulates the code chain
 // sum (OFF + q) b and, with do_ones, the ones chain sum b over the group.
+// The same with the code registers ra (row g) and rb (row g+8) already expanded.
 template <bool F16>
-__device__ __forceinline__ void group_mma(uint2 c_lo, uint2 c_hi, const uint32_t *bp, float (&dq)[4],
-                                          float (&dx)[4], bool do_ones)
+__device__ __forceinline__ void group_mma_regs(const uint32_t *ra, const uint32_t *rb, const uint32_t *bp,
+                                               float (&dq)[4], float (&dx)[4], bool do_ones)
 {
     constexpr uint32_t ones = F16 ? 0x3C003C00u : 0x3F803F80u;   // {1, 1}
-    uint32_t ra[8], rb[8];
-    nib8<F16>(c_lo.x, ra);
-    nib8<F16>(c_lo.y, ra + 4);
-    nib8<F16>(c_hi.x, rb);
-    nib8<F16>(c_hi.y, rb + 4);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         mma16816<F16>(dq, ra[2 * m], rb[2 * m], ra[2 * m + 1], rb[2 * m + 1], bp[2 * m], bp[2 * m + 1]);
         if (do_ones) mma16816<F16>(dx, ones, ones, ones, ones, bp[2 * m], bp[2 * m + 1]);
     }
+}
+
+template <bool F16>
+__device__ __forceinline__ void group_mma(uint2 c_lo, uint2 c_hi, const uint32_t *bp, float (&dq)[4],
+                                          float (&dx)[4], bool do_ones)
+{
+    uint32_t ra[8], rb[8];
+    nib8<F16>(c_lo.x, ra);
+    nib8<F16>(c_lo.y, ra + 4);
+    nib8<F16>(c_hi.x, rb);
+    nib8<F16>(c_hi.y, rb + 4);
+    group_mma_regs<F16>(ra, rb, bp, dq, dx, do_ones);
+}
+
+// Down projection, 8-bit codes: chain of 1024 + q (fp16) and, with do_ones, the ones chain.
+__device__ __forceinline__ void group_mma(uint4 c_lo, uint4 c_hi, const uint32_t *bp, float (&dq)[4],
+                                          float (&dx)[4], bool do_ones)
+{
+    uint32_t ra[8], rb[8];
+    byte16_f16(c_lo, ra);
+    byte16_f16(c_hi, rb);
+    group_mma_regs<true>(ra, rb, bp, dq, dx, do_ones);
+}
+
+// Gate/up projection, 8-bit codes (bf16): dq = 16 sum (128 + qh) b + sum (128 + ql) b = sum (2176 + q) b.
+__device__ __forceinline__ void group_mma_bf16_b8(uint4 c_lo, uint4 c_hi, const uint32_t *bp, float (&dq)[4],
+                                                  float (&dx)[4], bool do_ones)
+{
+    uint32_t la[8], ha[8], lb[8], hb[8];
+    byte16_nibbles(c_lo, la, ha);
+    byte16_nibbles(c_hi, lb, hb);
+    float dh[4] = {0.f, 0.f, 0.f, 0.f};
+    group_mma_regs<false>(la, lb, bp, dq, dx, do_ones);
+    group_mma_regs<false>(ha, hb, bp, dh, dx, false);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dq[i] = fmaf(16.f, dh[i], dq[i]);
 }
 
 struct ExpertView {
@@ -109,11 +186,11 @@ struct ExpertView {
     const uint16_t *biases;
 };
 
-__device__ __forceinline__ ExpertView expert_view(const QMatDev &m, int e, int rows, int cols)
+__device__ __forceinline__ ExpertView expert_view(const QMatDev &m, int e, int rows, int cols, int bits)
 {
     ExpertView v;
     const size_t eo = (size_t)e * rows;
-    v.codes = m.codes + eo * (cols / 2);
+    v.codes = m.codes + eo * ((size_t)cols * bits / 8);
     v.scales = m.scales + eo * (cols / kGroup);
     v.biases = m.biases + eo * (cols / kGroup);
     return v;
@@ -150,7 +227,8 @@ __device__ __forceinline__ void item_columns(const ExpertArgs &a, const WorkItem
 // [16 rb, 16 rb + 16) of gate and up for the item's <= 16 tokens; warp w takes
 // an eighth of the hidden groups and the eighths are added in warp order (the
 // same split and order as the fused decode kernel, so both give the same bits).
-template <int NT>
+// BITS: expert code width (4 or 8).
+template <int NT, int BITS>
 __global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
 {
     extern __shared__ uint4 s_x[];                 // [NT*8][H/8 + 1] (one uint4 of padding per row)
@@ -189,8 +267,11 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
         }
     }
 
-    const ExpertView vg = is_shared ? expert_view(a.s_gate, 0, I, H) : expert_view(a.gate, it.expert, I, H);
-    const ExpertView vu = is_shared ? expert_view(a.s_up, 0, I, H) : expert_view(a.up, it.expert, I, H);
+    using Code = typename std::conditional<BITS == 8, uint4, uint2>::type;   // 16 codes
+    constexpr int kRowBytes = BITS == 8 ? 1 : 2;                              // inputs per byte
+    const ExpertView vg = is_shared ? expert_view(a.s_gate, 0, I, H, BITS) : expert_view(a.gate, it.expert, I, H, BITS);
+    const ExpertView vu = is_shared ? expert_view(a.s_up, 0, I, H, BITS) : expert_view(a.up, it.expert, I, H, BITS);
+    const size_t rstride = (size_t)H / kRowBytes;
     const int r0 = blockIdx.x * 16 + g, r1 = r0 + 8;
     const int gbeg = (warp * G) / 8, gend = ((warp + 1) * G) / 8;
 
@@ -202,17 +283,17 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
 
     constexpr int GB = 4;   // groups whose loads are issued together
     for (int gb = gbeg; gb < gend; gb += GB) {
-        uint2 cg0[GB], cg1[GB], cu0[GB], cu1[GB];
+        Code cg0[GB], cg1[GB], cu0[GB], cu1[GB];
         uint16_t sg[GB][2], bg[GB][2], su[GB][2], bu[GB][2];
 #pragma unroll
         for (int i = 0; i < GB; ++i) {
             const int grp = gb + i;
             if (grp < gend) {
-                const size_t co = (size_t)grp * 32 + 8 * t;
-                cg0[i] = __ldg(reinterpret_cast<const uint2 *>(vg.codes + (size_t)r0 * (H / 2) + co));
-                cg1[i] = __ldg(reinterpret_cast<const uint2 *>(vg.codes + (size_t)r1 * (H / 2) + co));
-                cu0[i] = __ldg(reinterpret_cast<const uint2 *>(vu.codes + (size_t)r0 * (H / 2) + co));
-                cu1[i] = __ldg(reinterpret_cast<const uint2 *>(vu.codes + (size_t)r1 * (H / 2) + co));
+                const size_t co = ((size_t)grp * 64 + 16 * t) / kRowBytes;
+                cg0[i] = __ldg(reinterpret_cast<const Code *>(vg.codes + (size_t)r0 * rstride + co));
+                cg1[i] = __ldg(reinterpret_cast<const Code *>(vg.codes + (size_t)r1 * rstride + co));
+                cu0[i] = __ldg(reinterpret_cast<const Code *>(vu.codes + (size_t)r0 * rstride + co));
+                cu1[i] = __ldg(reinterpret_cast<const Code *>(vu.codes + (size_t)r1 * rstride + co));
                 sg[i][0] = __ldg(vg.scales + (size_t)r0 * G + grp);
                 sg[i][1] = __ldg(vg.scales + (size_t)r1 * G + grp);
                 bg[i][0] = __ldg(vg.biases + (size_t)r0 * G + grp);
@@ -229,18 +310,24 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
             if (grp >= gend) break;
             const float s_g0 = bf16_bits_to_float(sg[i][0]), s_g1 = bf16_bits_to_float(sg[i][1]);
             const float s_u0 = bf16_bits_to_float(su[i][0]), s_u1 = bf16_bits_to_float(su[i][1]);
-            const float c_g0 = fmaf(-128.f, s_g0, bf16_bits_to_float(bg[i][0]));   // b - 128 s, exact
-            const float c_g1 = fmaf(-128.f, s_g1, bf16_bits_to_float(bg[i][1]));
-            const float c_u0 = fmaf(-128.f, s_u0, bf16_bits_to_float(bu[i][0]));
-            const float c_u1 = fmaf(-128.f, s_u1, bf16_bits_to_float(bu[i][1]));
+            constexpr float off = BITS == 8 ? -2176.f : -128.f;                  // b - 128 s (b - 2176 s)
+            const float c_g0 = fmaf(off, s_g0, bf16_bits_to_float(bg[i][0]));
+            const float c_g1 = fmaf(off, s_g1, bf16_bits_to_float(bg[i][1]));
+            const float c_u0 = fmaf(off, s_u0, bf16_bits_to_float(bu[i][0]));
+            const float c_u1 = fmaf(off, s_u1, bf16_bits_to_float(bu[i][1]));
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const uint4 *xr = s_x + (j * 8 + g) * rowu4 + grp * 8 + 2 * t;
                 uint32_t bp[8];
                 permute_b(xr[0], xr[1], bp);
                 float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
-                group_mma<false>(cg0[i], cg1[i], bp, dg, dx, true);
-                group_mma<false>(cu0[i], cu1[i], bp, du, dx, false);
+                if constexpr (BITS == 8) {
+                    group_mma_bf16_b8(cg0[i], cg1[i], bp, dg, dx, true);
+                    group_mma_bf16_b8(cu0[i], cu1[i], bp, du, dx, false);
+                } else {
+                    group_mma<false>(cg0[i], cg1[i], bp, dg, dx, true);
+                    group_mma<false>(cu0[i], cu1[i], bp, du, dx, false);
+                }
                 // rows: d[0], d[1] -> row g; d[2], d[3] -> row g+8
                 acc_g[j][0] = fmaf(s_g0, dg[0], fmaf(c_g0, dx[0], acc_g[j][0]));
                 acc_g[j][1] = fmaf(s_g0, dg[1], fmaf(c_g0, dx[1], acc_g[j][1]));
@@ -286,7 +373,7 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(ExpertArgs a)
 // grid (H/64, max items); 128 threads, warp w owns rows [64 bx + 16 w, +16) of
 // the down matrix over all of the intermediate dimension; writes the raw
 // expert output y_e for each of the item's slots.
-template <int NT>
+template <int NT, int BITS>
 __global__ void __launch_bounds__(128) decode_down_kernel(ExpertArgs a)
 {
     extern __shared__ uint4 s_h[];                 // [NT*8][I/8 + 1]
@@ -307,7 +394,10 @@ __global__ void __launch_bounds__(128) decode_down_kernel(ExpertArgs a)
     }
     __syncthreads();
 
-    const ExpertView vd = is_shared ? expert_view(a.s_down, 0, H, I) : expert_view(a.down, it.expert, H, I);
+    using Code = typename std::conditional<BITS == 8, uint4, uint2>::type;   // 16 codes
+    constexpr int kRowBytes = BITS == 8 ? 1 : 2;                              // inputs per byte
+    const ExpertView vd = is_shared ? expert_view(a.s_down, 0, H, I, BITS) : expert_view(a.down, it.expert, H, I, BITS);
+    const size_t rstride = (size_t)I / kRowBytes;
     const int rbase = blockIdx.x * 64 + warp * 16;
     const int r0 = rbase + g, r1 = r0 + 8;
     float acc[NT][4];
@@ -318,15 +408,15 @@ __global__ void __launch_bounds__(128) decode_down_kernel(ExpertArgs a)
 
     constexpr int GB = 8;
     for (int gb = 0; gb < GI; gb += GB) {
-        uint2 c0[GB], c1[GB];
+        Code c0[GB], c1[GB];
         uint16_t sv[GB][2], bv[GB][2];
 #pragma unroll
         for (int i = 0; i < GB; ++i) {
             const int grp = gb + i;
             if (grp < GI) {
-                const size_t co = (size_t)grp * 32 + 8 * t;
-                c0[i] = __ldg(reinterpret_cast<const uint2 *>(vd.codes + (size_t)r0 * (I / 2) + co));
-                c1[i] = __ldg(reinterpret_cast<const uint2 *>(vd.codes + (size_t)r1 * (I / 2) + co));
+                const size_t co = ((size_t)grp * 64 + 16 * t) / kRowBytes;
+                c0[i] = __ldg(reinterpret_cast<const Code *>(vd.codes + (size_t)r0 * rstride + co));
+                c1[i] = __ldg(reinterpret_cast<const Code *>(vd.codes + (size_t)r1 * rstride + co));
                 sv[i][0] = __ldg(vd.scales + (size_t)r0 * GI + grp);
                 sv[i][1] = __ldg(vd.scales + (size_t)r1 * GI + grp);
                 bv[i][0] = __ldg(vd.biases + (size_t)r0 * GI + grp);
@@ -346,7 +436,8 @@ __global__ void __launch_bounds__(128) decode_down_kernel(ExpertArgs a)
                 uint32_t bp[8];
                 permute_b(hr[0], hr[1], bp);
                 float d[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
-                group_mma<true>(c0[i], c1[i], bp, d, dx, true);
+                if constexpr (BITS == 8) group_mma(c0[i], c1[i], bp, d, dx, true);
+                else group_mma<true>(c0[i], c1[i], bp, d, dx, true);
                 acc[j][0] = fmaf(s0, d[0], fmaf(k0, dx[0], acc[j][0]));
                 acc[j][1] = fmaf(s0, d[1], fmaf(k0, dx[1], acc[j][1]));
                 acc[j][2] = fmaf(s1, d[2], fmaf(k1, dx[2], acc[j][2]));
@@ -394,34 +485,40 @@ __global__ void decode_reduce_kernel(ReduceArgs a)
 
 }  // namespace
 
+namespace {
+
+template <int NT, int BITS>
+cudaError_t launch_gateup_as(const ExpertArgs &a, size_t smem, cudaStream_t st)
+{
+    cudaFuncSetAttribute(decode_gateup_kernel<NT, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    decode_gateup_kernel<NT, BITS><<<dim3(a.I / 16, a.max_items), 256, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int NT, int BITS>
+cudaError_t launch_down_as(const ExpertArgs &a, size_t smem, cudaStream_t st)
+{
+    cudaFuncSetAttribute(decode_down_kernel<NT, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    decode_down_kernel<NT, BITS><<<dim3(a.H / 64, a.max_items), 128, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_decode_gateup(const ExpertArgs &a, cudaStream_t st)
 {
     const int ncol = a.T >= 9 ? 16 : 8;
     const size_t smem = (size_t)ncol * (a.H / 8 + 1) * 16;
-    dim3 grid(a.I / 16, a.max_items);
-    if (ncol == 16) {
-        cudaFuncSetAttribute(decode_gateup_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        decode_gateup_kernel<2><<<grid, 256, smem, st>>>(a);
-    } else {
-        cudaFuncSetAttribute(decode_gateup_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        decode_gateup_kernel<1><<<grid, 256, smem, st>>>(a);
-    }
-    return cudaGetLastError();
+    if (a.bits == 8) return ncol == 16 ? launch_gateup_as<2, 8>(a, smem, st) : launch_gateup_as<1, 8>(a, smem, st);
+    return ncol == 16 ? launch_gateup_as<2, 4>(a, smem, st) : launch_gateup_as<1, 4>(a, smem, st);
 }
 
 cudaError_t launch_decode_down(const ExpertArgs &a, cudaStream_t st)
 {
     const int ncol = a.T >= 9 ? 16 : 8;
     const size_t smem = (size_t)ncol * (a.I / 8 + 1) * 16;
-    dim3 grid(a.H / 64, a.max_items);
-    if (ncol == 16) {
-        cudaFuncSetAttribute(decode_down_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        decode_down_kernel<2><<<grid, 128, smem, st>>>(a);
-    } else {
-        cudaFuncSetAttribute(decode_down_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        decode_down_kernel<1><<<grid, 128, smem, st>>>(a);
-    }
-    return cudaGetLastError();
+    if (a.bits == 8) return ncol == 16 ? launch_down_as<2, 8>(a, smem, st) : launch_down_as<1, 8>(a, smem, st);
+    return ncol == 16 ? launch_down_as<2, 4>(a, smem, st) : launch_down_as<1, 4>(a, smem, st);
 }
 
 cudaError_t launch_decode_reduce(const ReduceArgs &a, cudaStream_t st)

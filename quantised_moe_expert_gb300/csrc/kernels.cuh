@@ -98,6 +98,7 @@ struct ExpertArgs {
     float *acc;                   // f32 [T, H]
     int *status;
     int T, H, I, E, k, has_shared;
+    int bits;                     // expert code width: 4 or 8
     int max_items;
 };
 
@@ -127,15 +128,16 @@ struct PrefillArgs {
     float *yslot_out;             // f32 [T (k + 1), H] expert output per slot, unweighted, instead of acc; or null
     int *status;
     int T, H, I, E, k, has_shared, max_w1, max_w2;
+    int bits;                     // expert code width: 4 or 8
     long long wait_limit;
 };
 
 cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st);
 
 // Small-tile grouped GEMMs (items of at most kSmallN tokens, exact int4 codes on mma.sync):
-// whether a layer shape takes them, and their launches (items [nwork[3], nwork[1]) of the
-// gate/up list, [nwork[4], nwork[2]) of the down list).
-bool prefill_small_fits(int H, int I);
+// whether a layer shape takes them (4-bit experts only), and their launches (items
+// [nwork[3], nwork[1]) of the gate/up list, [nwork[4], nwork[2]) of the down list).
+bool prefill_small_fits(int H, int I, int bits);
 cudaError_t launch_small_gateup(const PrefillArgs &a, cudaStream_t st);
 cudaError_t launch_small_down(const PrefillArgs &a, cudaStream_t st);
 

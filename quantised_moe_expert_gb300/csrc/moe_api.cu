@@ -134,7 +134,7 @@ PermuteArgs permute_args(const moe_config &c, const int32_t *ids, int T, int32_t
     pa.nblk = L.nblk;
     pa.has_shared = c.has_shared;
     pa.build_work = 1;
-    pa.small_tiles = prefill_small_fits(c.hidden, c.inter) ? 1 : 0;
+    pa.small_tiles = prefill_small_fits(c.hidden, c.inter, c.bits) ? 1 : 0;
     pa.max_items[0] = L.max_wd;
     pa.max_items[1] = L.max_w1;
     pa.max_items[2] = L.max_w2;
@@ -171,6 +171,7 @@ ExpertArgs expert_args(const moe_config &c, const moe_weights &w, const uint16_t
     ea.E = c.n_experts;
     ea.k = c.top_k;
     ea.has_shared = c.has_shared;
+    ea.bits = c.bits;
     return ea;
 }
 
@@ -234,6 +235,7 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     a.has_shared = c.has_shared;
     a.max_w1 = L.max_w1;
     a.max_w2 = L.max_w2;
+    a.bits = c.bits;
     a.wait_limit = wait_limit_of(c);
     return cuda_rc(launch_prefill_experts(a, st));
 }
@@ -278,7 +280,7 @@ FusedDecodeArgs fused_args(const moe_config &c, const moe_weights &w, const uint
 
 bool fused_fits(const moe_config &c, int T)
 {
-    return T >= 1 && T <= kDecodeMaxTok &&
+    return c.bits == 4 && T >= 1 && T <= kDecodeMaxTok &&
            decode_fused_fits(T, c.hidden, c.inter, c.n_experts, c.top_k, c.has_shared);
 }
 
@@ -316,7 +318,7 @@ int moe_check_config(const moe_config *c)
 {
     if (!c) return MOE_ERR_INVALID_ARG;
     if (c->hidden <= 0 || c->inter <= 0 || c->n_experts <= 0 || c->top_k <= 0) return MOE_ERR_INVALID_ARG;
-    if (c->group != kGroup || c->bits != 4 || c->router_bits != 8) return MOE_ERR_UNSUPPORTED;
+    if (c->group != kGroup || (c->bits != 4 && c->bits != 8) || c->router_bits != 8) return MOE_ERR_UNSUPPORTED;
     if (c->hidden % 64 || c->inter % 64 || c->hidden > 8192 || c->inter > 4096) return MOE_ERR_UNSUPPORTED;
     if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->top_k > c->n_experts) return MOE_ERR_UNSUPPORTED;
     if (c->has_shared != 0 && c->has_shared != 1) return MOE_ERR_UNSUPPORTED;
@@ -404,7 +406,7 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     wa.T = T;
     wa.E = cfg->n_experts;
     wa.has_shared = cfg->has_shared;
-    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter) ? 1 : 0;
+    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter, cfg->bits) ? 1 : 0;
     wa.max_items[0] = L.max_wd;
     wa.max_items[1] = L.max_w1;
     wa.max_items[2] = L.max_w2;
@@ -504,7 +506,7 @@ int moe_pack_down(const moe_config *cfg, const moe_weights *w, uint8_t *down_pac
     if (rc) return rc;
     if (!w || !aligned16(w->down.codes) || !aligned16(down_packed) || !aligned16_or_null(s_down_packed))
         return MOE_ERR_INVALID_ARG;
-    if (cfg->inter % kDecodeSlice) return MOE_ERR_UNSUPPORTED;
+    if (cfg->inter % kDecodeSlice || cfg->bits != 4) return MOE_ERR_UNSUPPORTED;
     auto st = static_cast<cudaStream_t>(stream);
     rc = cuda_rc(launch_pack_down(w->down.codes, down_packed, cfg->n_experts, cfg->hidden, cfg->inter, st));
     if (rc || !cfg->has_shared || !s_down_packed) return rc;
@@ -551,7 +553,7 @@ int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_
     wa.T = T;
     wa.E = cfg->n_experts;
     wa.has_shared = cfg->has_shared;
-    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter) ? 1 : 0;
+    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter, cfg->bits) ? 1 : 0;
     wa.max_items[0] = L.max_wd;
     wa.max_items[1] = L.max_w1;
     wa.max_items[2] = L.max_w2;

@@ -49,10 +49,18 @@ namespace {
 using namespace tc;
 
 // Stage counts of the three rings of each GEMM: dequantised weights (A), token
-// operand (B) and int4 code tiles.  B runs deepest: its loads come from L2 /
-// HBM with a latency of several K-steps of MMA.
+// operand (B) and code tiles.  B runs deepest: its loads come from L2 / HBM with
+// a latency of several K-steps of MMA.  A code stage holds one K-step (64 inputs)
+// of 128 rows: 32 bytes a row for 4-bit codes, 64 for 8-bit codes, so the 8-bit
+// rings have half the stages in the same bytes.
 constexpr int kStagesA1 = 4, kStagesB1 = 8, kCodeStages1 = 6;   // gate/up: A in TMEM (64 columns), 16 KB, 8 KB per stage
 constexpr int kStagesA2 = 3, kStagesB2 = 3, kCodeStages2 = 6;   // down:    16 KB, 32 KB, 4 KB per stage
+constexpr int kCodeStages1B8 = 3, kCodeStages2B8 = 3;           // 8-bit codes: 16 KB / 8 KB per stage
+
+// Bytes of one row's codes per K-step, and of one code stage of each GEMM (gate | up; down).
+constexpr int code_row_bytes(int bits) { return 8 * bits; }
+constexpr int code_stage1(int bits) { return 2 * 128 * code_row_bytes(bits); }
+constexpr int code_stage2(int bits) { return 128 * code_row_bytes(bits); }
 constexpr int kRedCols = 16;        // down epilogue: columns per bulk-reduce chunk (two chunk buffers)
 // Warp roles of the down GEMM: 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue.
 constexpr int kDequantThreads = 256;
@@ -137,6 +145,37 @@ __device__ __forceinline__ __half2 bf16_to_h2(uint16_t b)
     return __float2half2_rn(bf16_bits_to_float(b));
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// 8 byte codes (u0: inputs 0-3, u1: inputs 4-7 of a chunk) -> 8 fp16 w = s*q + b in the same order
+// (0,4,1,5,2,6,3,7).  Each byte pair is moved into the mantissas of two 1024.0: 1024 + q is exact for
+// q < 1024, the subtraction of 1024 is exact, and w is the exact s * q + b rounded once to fp16.
+__device__ __forceinline__ uint4 dequant8_b8(uint32_t u0, uint32_t u1, __half2 s2, __half2 b2)
+{
+    const __half2 k1024 = __float2half2_rn(1024.f);
+    auto one = [&](uint32_t sel) {
+        return h2u(__hfma2(__hsub2(u2h((prmt(u0, u1, sel) & 0x00FF00FFu) | 0x64006400u), k1024), s2, b2));
+    };
+    uint4 o;
+    o.x = one(0x4400u);
+    o.y = one(0x5511u);
+    o.z = one(0x6622u);
+    o.w = one(0x7733u);
+    return o;
+}
+
+// 8-bit code tiles arrive with the 64-byte swizzle (rows of 64 bytes): 16-byte chunk c of row r sits
+// at chunk c ^ ((r >> 1) & 3), so the 8 rows that one quarter-warp reads cover all 32 banks.
+__device__ __forceinline__ uint32_t swz64(int row, int chunk)
+{
+    return (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
 // Position of input i in the K-permuted storage of its 8-input chunk.
 __device__ __forceinline__ int kperm_pos(int i)
 {
@@ -209,13 +248,16 @@ __device__ __forceinline__ void prefetch_rows(const void *p, uint32_t bytes)
 // epilogue; warps 14-17 gather the token rows of x with cp.async, SB - 2 steps ahead.
 // Tensor memory: gate and up accumulators in columns [0, 256) (one buffer, so a tile's
 // first MMAs wait for the previous epilogue's reads), A stages from column 256.
-template <int S, int SB, int CS>
+// BITS: expert code width (4 or 8).
+template <int S, int SB, int CS, int BITS>
 __global__ void __launch_bounds__(kThreads1, 1)
     gemm_gateup_kernel(const __grid_constant__ CUtensorMap map_gc, const __grid_constant__ CUtensorMap map_uc,
                        const __grid_constant__ CUtensorMap map_sgc, const __grid_constant__ CUtensorMap map_suc,
                        const G1Params P)
 {
     const int H = P.H, I = P.I, G = H / kGroup, nk = G, MB = (I + 127) / 128, Tk = P.T * P.k;
+    constexpr int CB = code_row_bytes(BITS), CST = code_stage1(BITS);
+    const size_t crow = (size_t)H * BITS / 8;            // bytes of one weight row's codes
     const int ntiles = __ldg(P.nwork + 3) * MB;          // the big items lead the list
     // This grid may start while the small-tile gate/up GEMM still runs (programmatic
     // dependent launch): it reads nothing that grid writes, and every CTA waits for that
@@ -227,8 +269,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *sB = smem;                           // SB x 16 KB (128 token rows x 128 B)
-    uint8_t *sC = sB + SB * 16384;                // CS x 8 KB (gate codes 4 KB | up codes 4 KB)
-    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 8192);   // [dequant thread][2][2][kScaleChunk1]
+    uint8_t *sC = sB + SB * 16384;                // CS x CST (gate codes | up codes)
+    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * CST);    // [dequant thread][2][2][kScaleChunk1]
     int *s_col = reinterpret_cast<int *>(sScale + kDequantWarps1 * 32 * 4 * kScaleChunk1);   // [2][e 128 | slot 128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(s_col + 2 * 256);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
@@ -333,16 +375,16 @@ __global__ void __launch_bounds__(kThreads1, 1)
             prefetch_map(&map_uc);
             prefetch_map(&map_sgc);
             prefetch_map(&map_suc);
-            // The code boxes are 32 bytes of 128 rows 1 KB apart: fetched from DRAM piece by
-            // piece they would cost a DRAM burst each.  A tile's rows are contiguous, so the
-            // whole tile (codes, scales, biases) is requested from L2 in bulk one tile ahead.
+            // The code boxes are 32 (64) bytes of 128 rows 1 KB (2 KB) apart: fetched from DRAM
+            // piece by piece they would cost a DRAM burst each.  A tile's rows are contiguous, so
+            // the whole tile (codes, scales, biases) is requested from L2 in bulk one tile ahead.
             auto prefetch_tile = [&](int tp) {
                 if (tp >= ntiles) return;
                 const TileInfo t2 = tile_info(P.work, P.offsets, tp, MB, P.E, Tk);
                 const int rows = min(128, I - t2.mb * 128);
                 const size_t wrow = (size_t)(t2.shared_e ? 0 : t2.expert * I) + t2.mb * 128;
-                prefetch_rows((t2.shared_e ? P.sgc : P.gc) + wrow * (H / 2), (uint32_t)rows * (H / 2));
-                prefetch_rows((t2.shared_e ? P.suc : P.uc) + wrow * (H / 2), (uint32_t)rows * (H / 2));
+                prefetch_rows((t2.shared_e ? P.sgc : P.gc) + wrow * crow, (uint32_t)(rows * crow));
+                prefetch_rows((t2.shared_e ? P.suc : P.uc) + wrow * crow, (uint32_t)(rows * crow));
                 const uint32_t sb = (uint32_t)rows * G * 2;
                 prefetch_rows((t2.shared_e ? P.sgs : P.gs) + wrow * G, sb);
                 prefetch_rows((t2.shared_e ? P.sgb : P.gb) + wrow * G, sb);
@@ -366,9 +408,9 @@ __global__ void __launch_bounds__(kThreads1, 1)
                         break;
                     }
                     const uint32_t fb = smem_u32(cfull + cs);
-                    mbar_arrive_expect_tx(fb, 8192);
-                    tma_load_2d(smem_u32(sC + cs * 8192), mg, s * 32, wrow, fb);
-                    tma_load_2d(smem_u32(sC + cs * 8192 + 4096), mu, s * 32, wrow, fb);
+                    mbar_arrive_expect_tx(fb, CST);
+                    tma_load_2d(smem_u32(sC + cs * CST), mg, s * CB, wrow, fb);
+                    tma_load_2d(smem_u32(sC + cs * CST + CST / 2), mu, s * CB, wrow, fb);
                 }
             }
             if (!ok || *s_abort)   // every issued copy lands before the CTA exits
@@ -497,19 +539,29 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     const __half2 sc = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
                     const __half2 sc16 = __hmul2(sc, __float2half2_rn(0.0625f));
                     const __half2 bc = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
-                    const uint4 *cp = reinterpret_cast<const uint4 *>(sC + cs * 8192 + m * 4096 + r * 32);
+                    const uint8_t *cbase = sC + cs * CST + m * (CST / 2);
                     // tcgen05.st / wait::st are warp-collective: the lanes left the polling loops
                     // above at different iterations, so reconverge first
                     __syncwarp();
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < 2; ++hh) {           // inputs 32 hh .. 32 hh + 31
                         uint32_t av[16];
                         if (w_ok) {
-                            const uint4 w = cp[hh];
-                            const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
+                            uint32_t cw[BITS];                 // the 32 inputs' codes
+                            if constexpr (BITS == 8) {
+                                const uint4 w0 = *reinterpret_cast<const uint4 *>(cbase + swz64(r, 2 * hh));
+                                const uint4 w1 = *reinterpret_cast<const uint4 *>(cbase + swz64(r, 2 * hh + 1));
+                                cw[0] = w0.x, cw[1] = w0.y, cw[2] = w0.z, cw[3] = w0.w;
+                                cw[4] = w1.x, cw[5] = w1.y, cw[6] = w1.z, cw[7] = w1.w;
+                            } else {
+                                const uint4 w = *reinterpret_cast<const uint4 *>(cbase + r * CB + hh * 16);
+                                cw[0] = w.x, cw[1] = w.y, cw[2] = w.z, cw[3] = w.w;
+                            }
 #pragma unroll
                             for (int cc = 0; cc < 4; ++cc) {
-                                const uint4 d = dequant8(cw[cc], sc, sc16, bc);
+                                uint4 d;
+                                if constexpr (BITS == 8) d = dequant8_b8(cw[2 * cc], cw[2 * cc + 1], sc, bc);
+                                else d = dequant8(cw[cc], sc, sc16, bc);
                                 av[4 * cc] = d.x;
                                 av[4 * cc + 1] = d.y;
                                 av[4 * cc + 2] = d.z;
@@ -631,12 +683,14 @@ __global__ void __launch_bounds__(kThreads1, 1)
 // Same structure; the token operand is the h tile of the expert's rows, loaded
 // with TMA by a second thread of warp 4 as soon as each stage is free, and the
 // epilogue adds p * y into the fp32 layer accumulator.
-template <int S, int SB, int CS>
+template <int S, int SB, int CS, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_down_kernel(const __grid_constant__ CUtensorMap map_dc, const __grid_constant__ CUtensorMap map_sdc,
                      const __grid_constant__ CUtensorMap map_h, const G2Params P)
 {
     const int H = P.H, I = P.I, GI = I / kGroup, nk = GI, MB = (H + 127) / 128, Tk = P.T * P.k;
+    constexpr int CB = code_row_bytes(BITS), CST = code_stage2(BITS);
+    const size_t crow = (size_t)I * BITS / 8;            // bytes of one weight row's codes
     const int ntiles = __ldg(P.nwork + 4) * MB;          // the big items lead the list
     // may start while the small-tile down GEMM still runs; waits for it before exiting
     if ((int)blockIdx.x >= ntiles) {
@@ -647,8 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *sA = smem;                           // S x 16 KB
     uint8_t *sB = sA + S * 16384;                 // SB x 32 KB (256 rows x 128 B)
-    uint8_t *sC = sB + SB * 32768;                // CS x 4 KB
-    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * 4096);   // [dequant thread][2][2][kScaleChunk1]
+    uint8_t *sC = sB + SB * 32768;                // CS x CST
+    uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * CST);    // [dequant thread][2][2][kScaleChunk1]
     float *sRed = reinterpret_cast<float *>(sScale + kDequantThreads * 4 * kScaleChunk1);   // [2][kRedCols][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sRed + 2 * kRedCols * 128);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
@@ -701,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const TileInfo t2 = tile_info(P.work, P.offsets, tp, MB, P.E, Tk);
                 const int rows = min(128, H - t2.mb * 128);
                 const size_t wrow = (size_t)(t2.shared_e ? 0 : t2.expert * H) + t2.mb * 128;
-                prefetch_rows((t2.shared_e ? P.sdc : P.dc) + wrow * (I / 2), (uint32_t)rows * (I / 2));
+                prefetch_rows((t2.shared_e ? P.sdc : P.dc) + wrow * crow, (uint32_t)(rows * crow));
                 const uint32_t sb = (uint32_t)rows * GI * 2;
                 prefetch_rows((t2.shared_e ? P.sds : P.ds) + wrow * GI, sb);
                 prefetch_rows((t2.shared_e ? P.sdb : P.db) + wrow * GI, sb);
@@ -722,8 +776,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t fb = smem_u32(cfull + cs);
-                    mbar_arrive_expect_tx(fb, 4096);
-                    tma_load_2d(smem_u32(sC + cs * 4096), md, s * 32, wrow, fb);
+                    mbar_arrive_expect_tx(fb, CST);
+                    tma_load_2d(smem_u32(sC + cs * CST), md, s * CB, wrow, fb);
                 }
             }
             if (!ok || *s_abort)
@@ -868,12 +922,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __half2 sd = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
                 const __half2 sd16 = __hmul2(sd, __float2half2_rn(0.0625f));
                 const __half2 bd = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
-                const uint4 w = *reinterpret_cast<const uint4 *>(sC + cs * 4096 + r * 32 + half * 16);
-                const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
                 uint8_t *aa = sA + st * 16384;
+                if constexpr (BITS == 8) {                 // inputs 32 half .. + 31: code chunks 2 half, 2 half + 1
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(sC + cs * CST + swz64(r, 2 * half));
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(sC + cs * CST + swz64(r, 2 * half + 1));
+                    const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(aa + swz128(r, half * 4 + c)) = dequant8(cw[c], sd, sd16, bd);
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(aa + swz128(r, half * 4 + c)) = dequant8_b8(cw[2 * c], cw[2 * c + 1], sd, bd);
+                } else {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(sC + cs * CST + r * CB + half * 16);
+                    const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(aa + swz128(r, half * 4 + c)) = dequant8(cw[c], sd, sd16, bd);
+                }
                 mbar_arrive(smem_u32(cempty + cs));
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(afull + st));
@@ -1036,16 +1099,16 @@ __global__ void convert_x_kernel(const uint4 *__restrict__ x, uint4 *__restrict_
 
 // ------------------------------------------------------------------ host side
 
-size_t g1_smem()
+size_t g1_smem(int cs, int bits)
 {
-    return 1024 + kStagesB1 * 16384 + kCodeStages1 * 8192 + kDequantWarps1 * 32 * 4 * kScaleChunk1 * 2 + 2 * 256 * 4 +
-           8 * (2 * kCodeStages1 + 2 * kStagesA1 + 2 * kStagesB1 + 5) + 256 * 4 + 16;
+    return 1024 + kStagesB1 * 16384 + (size_t)cs * code_stage1(bits) + kDequantWarps1 * 32 * 4 * kScaleChunk1 * 2 +
+           2 * 256 * 4 + 8 * (2 * cs + 2 * kStagesA1 + 2 * kStagesB1 + 5) + 256 * 4 + 16;
 }
-size_t g2_smem()
+size_t g2_smem(int cs, int bits)
 {
-    return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + kCodeStages2 * 4096 + kDequantThreads * 4 * kScaleChunk1 * 2 +
-           2 * kRedCols * 128 * 4 +
-           8 * (2 * kCodeStages2 + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 1024 * 4 + 16;
+    return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + (size_t)cs * code_stage2(bits) +
+           kDequantThreads * 4 * kScaleChunk1 * 2 + 2 * kRedCols * 128 * 4 +
+           8 * (2 * cs + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 1024 * 4 + 16;
 }
 
 // Launch allowed (pdl) to begin while the previous kernel of the stream still runs.
@@ -1091,18 +1154,24 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     cudaError_t e = cudaSuccess;
     if (a.acc_zero && !a.yslot_out && (e = launch_zero(a.acc, (size_t)T * H, st)) != cudaSuccess) return e;
 
+    if (a.bits != 4 && a.bits != 8) return cudaErrorInvalidValue;
+    const bool b8 = a.bits == 8;
     CUtensorMap mgc, muc, msgc, msuc, mdc, msdc, mh;
-    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE, sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    // code boxes: 32 bytes (4-bit, unswizzled) or 64 bytes with the 64-byte swizzle (8-bit) of 128 rows
+    const CUtensorMapSwizzle csw = b8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const uint32_t cbox = (uint32_t)code_row_bytes(a.bits);
+    const uint64_t hrow = (uint64_t)H * a.bits / 8, irow = (uint64_t)I * a.bits / 8;   // code bytes per row
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int ns = a.has_shared ? 1 : 0;
-    bool ok = make_map_2d(&mgc, a.gate.codes, u8, 1, H / 2, (uint64_t)E * I, 32, 128, none) &&
-              make_map_2d(&muc, a.up.codes, u8, 1, H / 2, (uint64_t)E * I, 32, 128, none) &&
-              make_map_2d(&mdc, a.down.codes, u8, 1, I / 2, (uint64_t)E * H, 32, 128, none) &&
+    bool ok = make_map_2d(&mgc, a.gate.codes, u8, 1, hrow, (uint64_t)E * I, cbox, 128, csw) &&
+              make_map_2d(&muc, a.up.codes, u8, 1, hrow, (uint64_t)E * I, cbox, 128, csw) &&
+              make_map_2d(&mdc, a.down.codes, u8, 1, irow, (uint64_t)E * H, cbox, 128, csw) &&
               make_map_2d(&mh, a.hs, f16, 2, I, (uint64_t)T * k + (uint64_t)T, 64, 32, sw128);
     if (ns)
-        ok = ok && make_map_2d(&msgc, a.s_gate.codes, u8, 1, H / 2, I, 32, 128, none) &&
-             make_map_2d(&msuc, a.s_up.codes, u8, 1, H / 2, I, 32, 128, none) &&
-             make_map_2d(&msdc, a.s_down.codes, u8, 1, I / 2, H, 32, 128, none);
+        ok = ok && make_map_2d(&msgc, a.s_gate.codes, u8, 1, hrow, I, cbox, 128, csw) &&
+             make_map_2d(&msuc, a.s_up.codes, u8, 1, hrow, I, cbox, 128, csw) &&
+             make_map_2d(&msdc, a.s_down.codes, u8, 1, irow, H, cbox, 128, csw);
     else {
         msgc = mgc;
         msuc = muc;
@@ -1144,11 +1213,12 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
         p1.async_scales = al ? 1 : 0;
     }
     p1.wait_limit = a.wait_limit;
-    const size_t s1 = g1_smem();
-    auto k1 = gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1>;
+    const size_t s1 = b8 ? g1_smem(kCodeStages1B8, 8) : g1_smem(kCodeStages1, 4);
+    auto k1 = b8 ? gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1B8, 8>
+                 : gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1, 4>;
     cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     const int tiles1 = a.max_w1 * ((I + 127) / 128);
-    const bool small = prefill_small_fits(H, I);   // items of small experts: mma.sync tiles (nwork[3] on)
+    const bool small = prefill_small_fits(H, I, a.bits);   // items of small experts: mma.sync tiles (nwork[3] on)
     if (small && (e = launch_small_gateup(a, st)) != cudaSuccess) return e;
     // behind the small-tile kernel (if any) as its programmatic dependent
     if ((e = launch_pdl(small, k1, std::min(sm_count(), tiles1), kThreads1, s1, st, mgc, muc, msgc, msuc, p1)) !=
@@ -1184,8 +1254,9 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
         p2.async_scales = al ? 1 : 0;
     }
     p2.wait_limit = a.wait_limit;
-    const size_t s2 = g2_smem();
-    auto k2 = gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2>;
+    const size_t s2 = b8 ? g2_smem(kCodeStages2B8, 8) : g2_smem(kCodeStages2, 4);
+    auto k2 = b8 ? gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2B8, 8>
+                 : gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2, 4>;
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
     const int tiles2 = a.max_w2 * ((H + 127) / 128);
     if (small && (e = launch_small_down(a, st)) != cudaSuccess) return e;

@@ -746,7 +746,10 @@ SmallParams small_params(const PrefillArgs &a, bool down)
 
 // H: code rows of 128-byte... every per-tile block of scales fits the double buffer
 // (H <= 2048), group-sum rows are 16-byte multiples (H % 256 == 0), whole groups in I.
-bool prefill_small_fits(int H, int I) { return H % 256 == 0 && H <= 2048 && I % 64 == 0 && I <= 4096; }
+bool prefill_small_fits(int H, int I, int bits)
+{
+    return bits == 4 && H % 256 == 0 && H <= 2048 && I % 64 == 0 && I <= 4096;
+}
 
 cudaError_t launch_small_gateup(const PrefillArgs &a, cudaStream_t st)
 {

@@ -11,15 +11,18 @@ Layer shapes follow the qwen3_5_moe routed-expert layer described on the page
 "r9700-vllm-blogs part 13" (hidden size 2048, moe_intermediate 512).  The
 storage format is the MLX affine rule quoted in the same proposal (experts at
 4 bits in groups of 64, router at 8 bits): a group of 64 consecutive inputs of
-one output row shares one bf16 scale and one bf16 bias.
+one output row shares one bf16 scale and one bf16 bias.  The same page's slice
+"8-bit experts" names the variant with 8-bit expert codes (same rule, q in
+0..255); the WORKLOADS_B8 list draws it.
 
 Storage layout (all little-endian, rows dense):
   x        bf16 bits, uint16 [T, H]
   router   codes uint8 [E, H], scales/biases bf16 bits uint16 [E, H/64]
   v        shared-expert gate vector, bf16 bits uint16 [H]
   gate, up codes uint8 [E, I, H/2] (4-bit: element j of a row is byte j//2,
-           low nibble for even j), scales/biases uint16 [E, I, H/64]
-  down     codes uint8 [E, H, I/2], scales/biases uint16 [E, H, I/64]
+           low nibble for even j; 8-bit: [E, I, H], element j is byte j),
+           scales/biases uint16 [E, I, H/64]
+  down     codes uint8 [E, H, I/2] (8-bit: [E, H, I]), scales/biases uint16 [E, H, I/64]
   s_gate, s_up, s_down: the shared expert, same layouts with a leading dim of 1
 """
 from __future__ import annotations
@@ -56,6 +59,7 @@ class Workload:
 
 
 QWEN_SHAPE = LayerShape(hidden=2048, inter=512, n_experts=256, top_k=8)
+QWEN_SHAPE_B8 = dataclasses.replace(QWEN_SHAPE, bits=8)
 TINY_SHAPE = LayerShape(hidden=256, inter=64, n_experts=16, top_k=2)
 
 WORKLOADS = [
@@ -65,6 +69,13 @@ WORKLOADS = [
     Workload("prefill_T512_H2048_E256_k8", QWEN_SHAPE, 512, seed=3),
     Workload("prefill_T4096_zipf1.1_H2048_E256_k8", QWEN_SHAPE, 4096, seed=4,
              zipf_s=1.1, tie_every=20),
+]
+
+# The same layer with 8-bit expert codes (router unchanged).
+WORKLOADS_B8 = [
+    Workload("decode_T1_H2048_E256_k8_b8", QWEN_SHAPE_B8, 1, seed=11),
+    Workload("decode_T16_H2048_E256_k8_b8", QWEN_SHAPE_B8, 16, seed=12),
+    Workload("prefill_T512_H2048_E256_k8_b8", QWEN_SHAPE_B8, 512, seed=13),
 ]
 
 
@@ -116,6 +127,18 @@ def _expert_qmat(rng: np.random.Generator, n: int, rows: int, cols: int) -> QMat
     return QMat(codes, s, b)
 
 
+def _expert_qmat8(rng: np.random.Generator, n: int, rows: int, cols: int) -> QMat:
+    """8-bit codes uniform in 0..255, scale ~ U(0.005, 0.02) / 16 rounded to bf16, bias = -128*scale.
+
+    The same weight spread as the 4-bit draw (|w| up to about 0.16), over 256 levels.
+    """
+    codes = rng.integers(0, 256, size=(n, rows, cols), dtype=np.uint8)
+    s = f32_to_bf16_bits(rng.uniform(0.005 / 16, 0.02 / 16, size=(n, rows, cols // GROUP)).astype(np.float32))
+    # -128 * s is exact in bf16 (power-of-two scaling of a bf16 value).
+    b = f32_to_bf16_bits(-128.0 * bf16_bits_to_f32(s))
+    return QMat(codes, s, b)
+
+
 def _quantise_8bit(w: np.ndarray) -> QMat:
     """Generator-side 8-bit affine quantiser for the router (group 64 along the input dim).
 
@@ -139,18 +162,19 @@ def _quantise_8bit(w: np.ndarray) -> QMat:
 
 def make_weights(shape: LayerShape, seed: int) -> LayerWeights:
     """Draw one layer's weights.  Draw order: router, v, gate, up, down, shared gate/up/down."""
-    assert shape.bits == 4 and shape.router_bits == 8 and shape.group == GROUP
+    assert shape.bits in (4, 8) and shape.router_bits == 8 and shape.group == GROUP
     H, I, E = shape.hidden, shape.inter, shape.n_experts
     rng = np.random.default_rng([seed, 1])
     router = _quantise_8bit(rng.normal(0.0, 0.02, size=(E, H)).astype(np.float32))
     v = f32_to_bf16_bits(rng.normal(0.0, 0.02, size=(H,)).astype(np.float32))
-    gate = _expert_qmat(rng, E, I, H)
-    up = _expert_qmat(rng, E, I, H)
-    down = _expert_qmat(rng, E, H, I)
+    qmat = _expert_qmat8 if shape.bits == 8 else _expert_qmat
+    gate = qmat(rng, E, I, H)
+    up = qmat(rng, E, I, H)
+    down = qmat(rng, E, H, I)
     ns = 1 if shape.has_shared else 0
-    s_gate = _expert_qmat(rng, ns, I, H)
-    s_up = _expert_qmat(rng, ns, I, H)
-    s_down = _expert_qmat(rng, ns, H, I)
+    s_gate = qmat(rng, ns, I, H)
+    s_up = qmat(rng, ns, I, H)
+    s_down = qmat(rng, ns, H, I)
     return LayerWeights(shape, router, gate, up, down, s_gate, s_up, s_down, v)
 
 
@@ -214,6 +238,6 @@ def nominal_tokens_per_expert(wl: Workload) -> float:
 
 
 if __name__ == "__main__":
-    for wl in WORKLOADS:
+    for wl in WORKLOADS + WORKLOADS_B8:
         print(wl.name, active_expert_bytes(wl.shape), router_bytes(wl.shape),
               expert_flops_per_token(wl.shape), math.ceil(nominal_tokens_per_expert(wl)))

@@ -30,17 +30,27 @@ STAGE_DOWN_TOL = 1e-4
 # small-tile kernels, exact codes, 4.7e-4 and 9.7e-5 at T = 40).
 PREFILL_STAGE_H_TOL = 4e-3
 PREFILL_STAGE_DOWN_TOL = 4e-3
+# With 8-bit codes that rounding is real for every weight: s (q - 128) needs up to 16 significant bits
+# (the synthetic 4-bit weights s (q - 8) need at most 11 and are exact in fp16), so each weight carries
+# up to 2^-11 relative error and a row's sum up to 2^-11 sum_j |w_j x_j|, some 1e-2 of max(1, |g|) at
+# the worst of 2.4 million elements (measured on GB300 at T = 512: h 1.7e-2, down 1.0e-2).  The
+# relative RMS over all slots stays near 2^-11 / sqrt(3) of the typical term and is checked tightly.
+PREFILL_B8_STAGE_TOL = 4e-2
+PREFILL_B8_STAGE_REL_RMS = 2e-3
+STAGE_REL_RMS = 1e-3
 
 _layers = {}
 
 
-def device_layer(wl_index: int):
-    """(workload, host weights, device layer) for a named workload, cached per session."""
-    if wl_index not in _layers:
-        wl = synth.WORKLOADS[wl_index]
+def device_layer(wl):
+    """(workload, host weights, device layer) for a named workload (a synth.Workload, or an index
+    into synth.WORKLOADS), cached per session."""
+    if isinstance(wl, int):
+        wl = synth.WORKLOADS[wl]
+    if wl.name not in _layers:
         w = synth.make_weights(wl.shape, wl.seed)
-        _layers[wl_index] = (wl, w, qm.DeviceLayer(w))
-    return _layers[wl_index]
+        _layers[wl.name] = (wl, w, qm.DeviceLayer(w))
+    return _layers[wl.name]
 
 
 def to_dev_u16(a):
@@ -189,14 +199,59 @@ def check_stages_against_fp64(wl, w, layer, x_bits, path, bias=None):
         dh = float((np.abs(h_gpu[f] - h_ref) / np.maximum(1.0, np.abs(h_ref))).max())
         y_ref = oracle.expert_down(sh, w, e, h_gpu[f])
         dy = float((np.abs(y_gpu[f] - y_ref) / np.maximum(1.0, np.abs(y_ref))).max())
-        return dh, dy
+        # squared error and squared reference sums, for the relative RMS over all slots
+        return (dh, dy, float(((h_gpu[f] - h_ref) ** 2).sum()), float((h_ref ** 2).sum()),
+                float(((y_gpu[f] - y_ref) ** 2).sum()), float((y_ref ** 2).sum()))
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
         errs = np.array(list(ex.map(one, slots, chunksize=64)))
-    worst_h, worst_y = float(np.nanmax(errs[:, 0])), float(np.nanmax(errs[:, 1]))
     assert not np.isnan(errs).any(), "a stage output holds NaN (not written)"
+    worst_h, worst_y = float(errs[:, 0].max()), float(errs[:, 1].max())
+    rms_h = float(np.sqrt(errs[:, 2].sum() / errs[:, 3].sum()))
+    rms_y = float(np.sqrt(errs[:, 4].sum() / errs[:, 5].sum()))
     prefill = path == qm.MOE_PATH_PREFILL
-    print(f"stage errors T={T} path={path}: h {worst_h:.3e}, down {worst_y:.3e} over {len(slots)} slots")
-    assert worst_h <= (PREFILL_STAGE_H_TOL if prefill else STAGE_H_TOL), worst_h
-    assert worst_y <= (PREFILL_STAGE_DOWN_TOL if prefill else STAGE_DOWN_TOL), worst_y
+    print(f"stage errors T={T} bits={sh.bits} path={path}: h {worst_h:.3e} (rel RMS {rms_h:.3e}), "
+          f"down {worst_y:.3e} (rel RMS {rms_y:.3e}) over {len(slots)} slots")
+    if prefill and sh.bits == 8:
+        tol_h = tol_y = PREFILL_B8_STAGE_TOL
+        tol_rms = PREFILL_B8_STAGE_REL_RMS
+    elif prefill:
+        tol_h, tol_y, tol_rms = PREFILL_STAGE_H_TOL, PREFILL_STAGE_DOWN_TOL, STAGE_REL_RMS
+    else:
+        tol_h, tol_y, tol_rms = STAGE_H_TOL, STAGE_DOWN_TOL, STAGE_REL_RMS
+    assert worst_h <= tol_h, worst_h
+    assert worst_y <= tol_y, worst_y
+    assert rms_h <= tol_rms and rms_y <= tol_rms, (rms_h, rms_y)
     return worst_h, worst_y
+
+
+def compare_rows(wl, w, x, got, rows, bias=None, logits_in=None):
+    """ids (outside near-ties), p and y of the given rows against the oracle; returns (y stats, oracle)."""
+    import oracle
+    ref = oracle.forward(wl.shape, w, x, bias=bias, logits_in=logits_in, rows=rows)
+    g = {key: got[key][rows] for key in ("y", "ids", "p", "w_s")}
+    gap = oracle_gap(ref["logits"], wl.shape.top_k)
+    clear = gap >= (0 if logits_in is not None else AMBIGUOUS_GAP)
+    assert np.array_equal(g["ids"][clear], ref["ids"][clear])
+    same = np.nonzero(np.all(g["ids"] == ref["ids"], axis=1))[0]
+    assert ulp_diff_bf16(g["p"][same], ref["p"][same]).max(initial=0) <= 1
+    return check_y(g["y"], ref["y"], rows=same), ref
+
+
+def compare_all_rows(wl, w, layer, x, got, bias=None, logits_in=None):
+    """Every row: ids, p, w_s and y against the oracle; near-tie rows under the GPU's own logits."""
+    import oracle
+    T = x.shape[0]
+    stats, ref = compare_rows(wl, w, x, got, np.arange(T), bias=bias, logits_in=logits_in)
+    if wl.shape.has_shared:
+        assert ulp_diff_bf16(got["w_s"], ref["w_s"]).max(initial=0) <= 1
+    diff = np.nonzero(np.any(got["ids"] != ref["ids"], axis=1))[0]
+    if len(diff):
+        assert logits_in is None
+        r = run_route(layer, x, router_bias=bias)
+        assert np.array_equal(r["ids"], got["ids"])
+        ref2 = oracle.forward(wl.shape, w, x, logits_in=r["logits"], rows=diff)
+        assert np.array_equal(ref2["ids"], got["ids"][diff])
+        assert np.array_equal(ref2["p"], got["p"][diff])
+        check_y(got["y"][diff], ref2["y"])
+    return stats, len(diff)

@@ -59,7 +59,9 @@ def cfg_from(**kw):
     ({}, qm.MOE_OK),
     (dict(hidden=256, inter=64, n_experts=16, top_k=2), qm.MOE_OK),
     (dict(has_shared=0), qm.MOE_OK),
-    (dict(bits=8), qm.MOE_ERR_UNSUPPORTED),
+    (dict(bits=8), qm.MOE_OK),
+    (dict(bits=2), qm.MOE_ERR_UNSUPPORTED),
+    (dict(bits=6), qm.MOE_ERR_UNSUPPORTED),
     (dict(group=32), qm.MOE_ERR_UNSUPPORTED),
     (dict(router_bits=4), qm.MOE_ERR_UNSUPPORTED),
     (dict(hidden=100), qm.MOE_ERR_UNSUPPORTED),
@@ -115,7 +117,7 @@ def test_forward_rejects_bad_arguments(lib):
         assert forward(lib, cfg, fake_weights(m)) == qm.MOE_ERR_INVALID_ARG, m
     # the router is not needed when logits are supplied
     assert forward(lib, cfg, fake_weights("router"), T=0, logits_in=FAKE) == qm.MOE_OK
-    assert forward(lib, cfg_from(bits=8), w) == qm.MOE_ERR_UNSUPPORTED
+    assert forward(lib, cfg_from(bits=3), w) == qm.MOE_ERR_UNSUPPORTED
 
 
 def test_forward_workspace_too_small(lib):
@@ -160,6 +162,9 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.moe_pack_down(ctypes.byref(cfg), ctypes.byref(w), MISALIGNED, None, None) == qm.MOE_ERR_INVALID_ARG
     assert lib.moe_pack_down(ctypes.byref(cfg), ctypes.byref(fake_weights("down")), FAKE, None, None) == \
         qm.MOE_ERR_INVALID_ARG
+    # the decode layout of the down codes is for 4-bit codes (the fused decode kernel reads it)
+    assert lib.moe_pack_down(ctypes.byref(cfg_from(bits=8)), ctypes.byref(w), FAKE, None, None) == \
+        qm.MOE_ERR_UNSUPPORTED
     bad = fake_weights()
     bad.down_packed = MISALIGNED
     assert forward(lib, cfg, bad) == qm.MOE_ERR_INVALID_ARG

@@ -26,41 +26,12 @@ def _cuda():
     oracle.build()
 
 
-def _compare_rows(wl, w, x, got, rows, bias=None, logits_in=None):
-    ref = oracle.forward(wl.shape, w, x, bias=bias, logits_in=logits_in, rows=rows)
-    g = {key: got[key][rows] for key in ("y", "ids", "p", "w_s")}
-    gap = H.oracle_gap(ref["logits"], wl.shape.top_k)
-    clear = gap >= (0 if logits_in is not None else H.AMBIGUOUS_GAP)
-    assert np.array_equal(g["ids"][clear], ref["ids"][clear])
-    same = np.nonzero(np.all(g["ids"] == ref["ids"], axis=1))[0]
-    assert H.ulp_diff_bf16(g["p"][same], ref["p"][same]).max(initial=0) <= 1
-    return H.check_y(g["y"], ref["y"], rows=same), ref
-
-
-def _compare_all_rows(wl, w, layer, x, got, bias=None, logits_in=None):
-    """Every row: ids, p, w_s and y against the oracle; near-tie rows under the GPU's own logits."""
-    T = x.shape[0]
-    stats, ref = _compare_rows(wl, w, x, got, np.arange(T), bias=bias, logits_in=logits_in)
-    if wl.shape.has_shared:
-        assert H.ulp_diff_bf16(got["w_s"], ref["w_s"]).max(initial=0) <= 1
-    diff = np.nonzero(np.any(got["ids"] != ref["ids"], axis=1))[0]
-    if len(diff):
-        assert logits_in is None
-        r = H.run_route(layer, x, router_bias=bias)
-        assert np.array_equal(r["ids"], got["ids"])
-        ref2 = oracle.forward(wl.shape, w, x, logits_in=r["logits"], rows=diff)
-        assert np.array_equal(ref2["ids"], got["ids"][diff])
-        assert np.array_equal(ref2["p"], got["p"][diff])
-        H.check_y(got["y"][diff], ref2["y"])
-    return stats, len(diff)
-
-
 def test_prefill_tiny_all_rows():
     wl, w, layer = H.device_layer(0)
     x = synth.make_x(wl.shape, wl.tokens, wl.seed)
     got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
     assert got["status"] == 0
-    stats, _ = _compare_rows(wl, w, x, got, np.arange(wl.tokens))
+    stats, _ = H.compare_rows(wl, w, x, got, np.arange(wl.tokens))
     assert stats["max_abs"] <= 2e-2, stats
 
 
@@ -71,7 +42,7 @@ def test_prefill_ragged_token_counts_small_layer(T):
     x = synth.make_x(wl.shape, T, wl.seed, stream=T)
     got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
     assert got["status"] == 0
-    _compare_rows(wl, w, x, got, np.arange(T))
+    H.compare_rows(wl, w, x, got, np.arange(T))
 
 
 def test_prefill_t512_every_row():
@@ -82,7 +53,7 @@ def test_prefill_t512_every_row():
     r = H.run_route(layer, x)
     ref_logits = oracle.router_logits(wl.shape, w, x)
     assert np.abs(r["logits"].astype(np.float64) - ref_logits).max() <= H.LOGIT_TOL
-    _, ndiff = _compare_all_rows(wl, w, layer, x, got)
+    _, ndiff = H.compare_all_rows(wl, w, layer, x, got)
     assert ndiff <= 2
 
 
@@ -96,7 +67,7 @@ def test_prefill_t4096_zipf_every_row():
     r = H.run_route(layer, x, router_bias=bias)
     err = np.abs(r["logits"].astype(np.float64) - ref_logits)
     assert err.max() <= H.LOGIT_TOL, (err.max(), np.unravel_index(err.argmax(), err.shape))
-    _, ndiff = _compare_all_rows(wl, w, layer, x, got, bias=bias)
+    _, ndiff = H.compare_all_rows(wl, w, layer, x, got, bias=bias)
     assert ndiff <= 2
     counts = np.bincount(got["ids"].ravel(), minlength=wl.shape.n_experts)
     assert counts.max() > 8 * wl.tokens * wl.shape.top_k / wl.shape.n_experts   # the skew is real
@@ -133,7 +104,7 @@ def test_prefill_t4096_forced_ties_bit_exact_routing():
     got = H.run_forward(layer, x, logits_in=lg)
     assert got["status"] == 0
     assert np.array_equal(got["ids"], ref_ids) and np.array_equal(got["p"], ref_p)
-    _compare_all_rows(wl, w, layer, x, got, logits_in=lg)
+    H.compare_all_rows(wl, w, layer, x, got, logits_in=lg)
 
 
 def test_decode_and_prefill_paths_agree():

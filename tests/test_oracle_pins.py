@@ -287,6 +287,32 @@ def test_expert_relabelling_invariance(orc):
     assert np.array_equal(out["p"], base["p"])
 
 
+def test_eight_bit_layer_equals_four_bit_layer_with_the_same_weights(orc):
+    """Every 4-bit code written as one byte (q in 0..15), same scales and biases: the same weights, so
+    the 8-bit layer's output, routing and every stage equal the 4-bit layer's bit for bit.  Several
+    experts and both matrix orientations: an 8-bit row or expert stride taken as the 4-bit one fails."""
+    import copy
+    shape4 = synth.LayerShape(hidden=192, inter=128, n_experts=6, top_k=3)
+    shape8 = synth.LayerShape(hidden=192, inter=128, n_experts=6, top_k=3, bits=8)
+    w4 = synth.make_weights(shape4, 31)
+    w8 = copy.deepcopy(w4)
+    for name in ("gate", "up", "down", "s_gate", "s_up", "s_down"):
+        c4 = getattr(w4, name).codes
+        c8 = np.empty(c4.shape[:-1] + (2 * c4.shape[-1],), np.uint8)
+        c8[..., 0::2] = c4 & 0x0F            # element 2i: low nibble of byte i
+        c8[..., 1::2] = c4 >> 4
+        getattr(w8, name).codes = c8
+    x = synth.make_x(shape4, 7, 31)
+    a, b = orc.forward(shape4, w4, x), orc.forward(shape8, w8, x)
+    for key in ("y", "y_exact", "ids", "p", "w_s", "logits"):
+        assert np.array_equal(a[key], b[key]), key
+    xf = synth.bf16_bits_to_f32(x[2]).astype(np.float64)
+    for e in (-1, 0, 5):
+        h4, y4 = orc.expert_ffn(shape4, w4, e, xf)
+        h8, y8 = orc.expert_ffn(shape8, w8, e, xf)
+        assert np.array_equal(h4, h8) and np.array_equal(y4, y8), e
+
+
 def test_rows_are_independent(orc):
     shape = synth.TINY_SHAPE
     w = synth.make_weights(shape, 0)
