@@ -569,6 +569,9 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
     const CUtensorMap *mg = &maps.g, *mu = &maps.u, *msg = &maps.sg, *msu = &maps.su;
     int issued = 0;
     bool stop = false;
+    // every weight byte is read once per launch: evict-first in L2, so the per-slice partial sums that
+    // the combine reads back stay there
+    const uint64_t pol = l2_evict_first_policy();
 #pragma unroll 1
     for (int u = blockIdx.x, i = 0; u < U && !stop; u += gridDim.x, ++i) {
         const int d = u / SL, s = u - d * SL, e = S.list[d];
@@ -606,9 +609,9 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
                     const uint16_t *sc = c == 0 ? (shr ? sgsc : gsc) : (shr ? susc : usc);
                     const uint16_t *bi = c == 0 ? (shr ? sgbi : gbi) : (shr ? subi : ubi);
                     mbar_arrive_expect_tx(fb, codes1 + 2 * sc1);
-                    tma_load_3d(smem_u32(base), c == 0 ? (shr ? msg : mg) : (shr ? msu : mu), 0, row0, 0, fb);
-                    bulk_load(smem_u32(base + codes1), sc + so, sc1, fb);
-                    bulk_load(smem_u32(base + codes1 + sc1), bi + so, sc1, fb);
+                    tma_load_3d_hint(smem_u32(base), c == 0 ? (shr ? msg : mg) : (shr ? msu : mu), 0, row0, 0, fb, pol);
+                    bulk_load_hint(smem_u32(base + codes1), sc + so, sc1, fb, pol);
+                    bulk_load_hint(smem_u32(base + codes1 + sc1), bi + so, sc1, fb, pol);
                 } else {
                     mbar_arrive(fb);
                 }
@@ -617,7 +620,7 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
                 if (lane == 0) {
                     const uint8_t *src = shr ? spacked + (size_t)s * H * 16 : packed + ((size_t)e * SL + s) * H * 16;
                     mbar_arrive_expect_tx(fb, (uint32_t)H * 16);
-                    bulk_load(smem_u32(base), src, (uint32_t)H * 16, fb);
+                    bulk_load_hint(smem_u32(base), src, (uint32_t)H * 16, fb, pol);
                 } else {
                     mbar_arrive(fb);
                 }
