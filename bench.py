@@ -235,12 +235,12 @@ class Workload:
 
     def kernels_per_step(self):
         # decode: the one fused kernel (8-bit experts: router GEMV, top-k, permute, gate/up, down,
-        # reduce); prefill: router GEMV (gamma), router MMA, top-k, permute, x conversion, accumulator
-        # zeroing, two small-tile (4-bit experts only) and two tensor-memory GEMMs, combine
+        # slot sum); prefill: router GEMV (gamma), router MMA, top-k, permute, x conversion, two
+        # small-tile (4-bit experts only) and two tensor-memory GEMMs, slot sum
         b8 = self.wl.shape.bits == 8
         if self.wl.tokens <= 16:
             return 6 if b8 else 1
-        return 9 if b8 else 11
+        return 8 if b8 else 10
 
     def distinct_experts(self):
         """Distinct routed experts (plus the shared expert) of each copy whose step was executed."""

@@ -196,11 +196,13 @@ MOE_API int moe_permute(const moe_config *cfg, const int32_t *ids, int T, int32_
  * acc is fp32 [T, H], caller-initialised (zero for a plain layer).
  * ids/p/w_shared as produced by moe_route; counts/offsets/perm as produced by
  * moe_permute from the same ids.  w_shared may be NULL when has_shared == 0.
- * path selects the kernels (enum moe_path).  On the decode path every acc
- * element receives one fixed-order sum (bit-reproducible for a given input,
- * independent of the other tokens in the batch); the prefill path adds slot
- * contributions with fp32 atomics, so the order of additions (and the last
- * bits of acc) may vary between runs. */
+ * path selects the kernels (enum moe_path).  On both paths each slot's expert
+ * output is computed once and every acc element receives one fixed-order sum
+ * of them, so the result is bit-reproducible for a given batch.  On the decode
+ * path it is also independent of the other tokens in the batch; on the
+ * prefill path an expert's token count selects the kernels that compute it
+ * (exact-code small tiles up to 32 tokens, fp16-dequantised tensor-memory
+ * GEMMs above), so a token's last bits can depend on its batch. */
 MOE_API int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int T,
                    const int32_t *ids, const uint16_t *p, const uint16_t *w_shared,
                    const int32_t *counts, const int32_t *offsets, const int32_t *perm,
@@ -267,9 +269,8 @@ MOE_API int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *
  *             pick weight, or NULL.
  * ids/counts/offsets/perm as for moe_expert_ffn (counts/offsets/perm are read
  * on the prefill path only).  The same kernels as moe_expert_ffn compute the
- * stages; nothing is added into an accumulator.  On the prefill path
- * yslot_out must be zero-filled by the caller (the down GEMM adds each tile's
- * rows into it).  Rows of h_out / yslot_out of slots that do not exist (the
+ * stages; nothing is added into an accumulator.  Rows of h_out / yslot_out
+ * of slots that do not exist (the
  * shared rows without a shared expert) are not written.  Returns
  * MOE_ERR_UNSUPPORTED for a path whose kernels cannot emit their stages (the
  * decode path of a layer that does not take the fused decode kernel: bits == 8,

@@ -1,4 +1,4 @@
-// The single rounding of the combine: y = bf16_rne(acc), and the zeroing of acc.
+// The single rounding of moe_combine: y = bf16_rne(acc).
 #include "kernels.cuh"
 
 namespace qmoe {
@@ -15,12 +15,6 @@ __global__ void combine_kernel(const float4 *__restrict__ acc, uint2 *__restrict
     }
 }
 
-__global__ void zero_kernel(float4 *__restrict__ p, size_t n4)
-{
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
-        p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
 unsigned grid_for(size_t n)
 {
     const size_t want = (n + 255) / 256;
@@ -34,12 +28,6 @@ cudaError_t launch_combine(const float *acc, uint16_t *y, size_t n, cudaStream_t
 {
     combine_kernel<<<grid_for(n / 4), 256, 0, st>>>(reinterpret_cast<const float4 *>(acc),
                                                        reinterpret_cast<uint2 *>(y), n / 4);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_zero(float *p, size_t n, cudaStream_t st)
-{
-    zero_kernel<<<grid_for(n / 4), 256, 0, st>>>(reinterpret_cast<float4 *>(p), n / 4);
     return cudaGetLastError();
 }
 

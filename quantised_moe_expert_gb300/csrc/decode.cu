@@ -463,24 +463,75 @@ __global__ void __launch_bounds__(128) decode_down_kernel(ExpertArgs a)
     }
 }
 
-// ------------------------------------------------------------ fixed-order combine
+// ------------------------------------------------------------ fixed-order slot sum
 //
 // sum[t, n] = sum_{j < k} p[t,j] * y_slot[t*k + j, n] + w_s[t] * y_slot[T*k + t, n],
-// added in slot order; y = bf16(sum) or acc += sum.
-__global__ void decode_reduce_kernel(ReduceArgs a)
+// added in slot order; y = bf16(sum) or acc += sum.  One thread per 4 consecutive n of a token.
+// Routed slot f sits in row pos[f] of the slot buffer (row f without pos).
+__global__ void slot_sum_kernel(ReduceArgs a)
 {
+    const int H4 = a.H / 4, k = a.k, Tk = a.T * a.k;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (size_t)a.T * a.H) return;
-    const int t = (int)(idx / a.H), n = (int)(idx - (size_t)t * a.H);
-    float s = 0.f;
-    for (int j = 0; j < a.k; ++j)
-        s = fmaf(bf16_bits_to_float(a.p[(size_t)t * a.k + j]), a.yslot[((size_t)t * a.k + j) * a.H + n], s);
-    if (a.has_shared)
-        s = fmaf(bf16_bits_to_float(a.w_s[t]), a.yslot[((size_t)a.T * a.k + t) * a.H + n], s);
-    if (a.y)
-        a.y[idx] = float_to_bf16_bits(s);
-    else
-        a.acc[idx] += s;
+    if (idx >= (size_t)a.T * H4) return;
+    const int t = (int)(idx / H4), n4 = (int)(idx - (size_t)t * H4);
+    const float4 *ys = reinterpret_cast<const float4 *>(a.yslot);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float w, float4 v) {
+        s.x = fmaf(w, v.x, s.x);
+        s.y = fmaf(w, v.y, s.y);
+        s.z = fmaf(w, v.z, s.z);
+        s.w = fmaf(w, v.w, s.w);
+    };
+#pragma unroll 4
+    for (int j = 0; j < k; ++j) {
+        const int f = t * k + j;
+        const int r = a.pos ? __ldg(a.pos + f) : f;
+        if (r < 0 || r >= Tk) {                        // an inconsistent permutation: report, skip the slot
+            record_status(a.status, MOE_ERR_DEVICE);
+            continue;
+        }
+        add(bf16_bits_to_float(a.p[f]), __ldcs(ys + (size_t)r * H4 + n4));
+    }
+    if (a.has_shared) add(bf16_bits_to_float(a.w_s[t]), __ldcs(ys + ((size_t)Tk + t) * H4 + n4));
+    if (a.y) {
+        uint2 o;
+        o.x = (uint32_t)float_to_bf16_bits(s.x) | ((uint32_t)float_to_bf16_bits(s.y) << 16);
+        o.y = (uint32_t)float_to_bf16_bits(s.z) | ((uint32_t)float_to_bf16_bits(s.w) << 16);
+        reinterpret_cast<uint2 *>(a.y)[idx] = o;
+    } else {
+        float4 *acc = reinterpret_cast<float4 *>(a.acc) + idx;
+        float4 v = *acc;
+        v.x += s.x;
+        v.y += s.y;
+        v.z += s.z;
+        v.w += s.w;
+        *acc = v;
+    }
+}
+
+__global__ void invert_perm_kernel(const int32_t *__restrict__ perm, int32_t *__restrict__ inv, int n, int *status)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int f = perm[i];
+    if (f < 0 || f >= n) record_status(status, MOE_ERR_DEVICE);
+    else inv[f] = i;
+}
+
+// One thread per 4 consecutive columns of one output slot.
+__global__ void slot_gather_kernel(const float4 *__restrict__ ys, const int32_t *__restrict__ pos, float4 *__restrict__ out,
+                                   int T, int H4, int k, int has_shared, int *status)
+{
+    const int Tk = T * k, nslot = Tk + (has_shared ? T : 0);
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)nslot * H4) return;
+    const int f = (int)(idx / H4), n4 = (int)(idx - (size_t)f * H4);
+    const int r = f < Tk ? __ldg(pos + f) : f;
+    if (r < 0 || r >= nslot) {
+        record_status(status, MOE_ERR_DEVICE);
+        return;
+    }
+    out[idx] = ys[(size_t)r * H4 + n4];
 }
 
 }  // namespace
@@ -521,10 +572,28 @@ cudaError_t launch_decode_down(const ExpertArgs &a, cudaStream_t st)
     return ncol == 16 ? launch_down_as<2, 4>(a, smem, st) : launch_down_as<1, 4>(a, smem, st);
 }
 
-cudaError_t launch_decode_reduce(const ReduceArgs &a, cudaStream_t st)
+cudaError_t launch_slot_sum(const ReduceArgs &a, cudaStream_t st)
 {
-    const size_t n = (size_t)a.T * a.H;
-    decode_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+    const size_t n = (size_t)a.T * (a.H / 4);
+    slot_sum_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_invert_perm(const int32_t *perm, int32_t *inv, int n, int *status, cudaStream_t st)
+{
+    if (n <= 0) return cudaSuccess;
+    invert_perm_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(perm, inv, n, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_slot_gather(const float *yslot, const int32_t *pos, float *out, int T, int H, int k, int has_shared,
+                               int *status, cudaStream_t st)
+{
+    const size_t n = (size_t)(T * k + (has_shared ? T : 0)) * (H / 4);
+    if (n == 0) return cudaSuccess;
+    slot_gather_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(yslot), pos,
+                                                                     reinterpret_cast<float4 *>(out), T, H / 4, k,
+                                                                     has_shared, status);
     return cudaGetLastError();
 }
 

@@ -103,7 +103,9 @@ struct ExpertArgs {
 };
 
 struct ReduceArgs {
-    const float *yslot;
+    const float *yslot;           // f32 [T (k + 1), H] slot outputs
+    const int32_t *pos;           // [T k] row of yslot holding routed slot f (null: row f); shared slot T k + t: row T k + t
+    int *status;
     const uint16_t *p;
     const uint16_t *w_s;
     float *acc;                   // acc += sum (when y == null)
@@ -121,11 +123,9 @@ struct PrefillArgs {
     QMatDev gate, up, down, s_gate, s_up, s_down;
     const int32_t *nwork, *offsets, *perm;
     const WorkItem *work_g1, *work_g2;
-    const uint16_t *p, *w_s;
-    float *acc;                   // f32 [T, H]
-    int acc_zero;                 // 1: zero acc first
     float *h_out;                 // f32 [T (k + 1), I] h per slot (stage output), or null
-    float *yslot_out;             // f32 [T (k + 1), H] expert output per slot, unweighted, instead of acc; or null
+    float *yslot;                 // f32 [T (k + 1), H] each slot's expert output before its pick weight, rows in
+                                  // expert-sorted position order (every element of the slots present written once)
     int *status;
     int T, H, I, E, k, has_shared, max_w1, max_w2;
     int bits;                     // expert code width: 4 or 8
@@ -190,8 +190,13 @@ cudaError_t launch_hist(const HistArgs &a, cudaStream_t st);
 cudaError_t launch_worklist(const WorklistArgs &a, cudaStream_t st);
 cudaError_t launch_decode_gateup(const ExpertArgs &a, cudaStream_t st);
 cudaError_t launch_decode_down(const ExpertArgs &a, cudaStream_t st);
-cudaError_t launch_decode_reduce(const ReduceArgs &a, cudaStream_t st);
+// y (or acc) from the slot outputs: the fixed-order weighted sum over each token's slots.
+cudaError_t launch_slot_sum(const ReduceArgs &a, cudaStream_t st);
+// inv[perm[i]] = i for i < n (an entry out of range is reported in status and skipped).
+cudaError_t launch_invert_perm(const int32_t *perm, int32_t *inv, int n, int *status, cudaStream_t st);
+// out[f, :] = yslot[pos[f], :] for routed slots f < T k, out[f, :] = yslot[f, :] for shared slots.
+cudaError_t launch_slot_gather(const float *yslot, const int32_t *pos, float *out, int T, int H, int k, int has_shared,
+                               int *status, cudaStream_t st);
 cudaError_t launch_combine(const float *acc, uint16_t *y, size_t n, cudaStream_t st);
-cudaError_t launch_zero(float *p, size_t n, cudaStream_t st);
 
 }  // namespace qmoe

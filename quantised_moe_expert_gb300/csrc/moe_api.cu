@@ -175,6 +175,26 @@ ExpertArgs expert_args(const moe_config &c, const moe_weights &w, const uint16_t
     return ea;
 }
 
+// The fixed-order sum of every token's slot outputs (ea.yslot; routed slot f in row pos[f], or row f
+// when pos is null): into y (rounded once) or added to ea.acc.
+int enqueue_slot_sum(const moe_config &c, const ExpertArgs &ea, uint16_t *y, cudaStream_t st,
+                     const int32_t *pos = nullptr)
+{
+    ReduceArgs r{};
+    r.yslot = ea.yslot;
+    r.pos = pos;
+    r.status = ea.status;
+    r.p = ea.p;
+    r.w_s = ea.w_s;
+    r.acc = ea.acc;
+    r.y = y;
+    r.T = ea.T;
+    r.H = c.hidden;
+    r.k = c.top_k;
+    r.has_shared = c.has_shared;
+    return cuda_rc(launch_slot_sum(r, st));
+}
+
 // Decode expert kernels; the sum lands in y (rounded) or is added to acc.
 int enqueue_decode_experts(const moe_config &c, ExpertArgs ea, const WsLayout &L, void *ws, uint16_t *y,
                            cudaStream_t st)
@@ -185,22 +205,17 @@ int enqueue_decode_experts(const moe_config &c, ExpertArgs ea, const WsLayout &L
     if (rc) return rc;
     rc = cuda_rc(launch_decode_down(ea, st));
     if (rc) return rc;
-    ReduceArgs r{};
-    r.yslot = ea.yslot;
-    r.p = ea.p;
-    r.w_s = ea.w_s;
-    r.acc = ea.acc;
-    r.y = y;
-    r.T = ea.T;
-    r.H = c.hidden;
-    r.k = c.top_k;
-    r.has_shared = c.has_shared;
-    return cuda_rc(launch_decode_reduce(r, st));
+    return enqueue_slot_sum(c, ea, y, st);
 }
 
-// Prefill expert GEMMs; acc is zeroed first when acc_zero (the fused forward).
-int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsLayout &L, void *ws, int acc_zero,
-                            cudaStream_t st, float *h_out = nullptr, float *yslot_out = nullptr)
+// Prefill expert GEMMs.  Each slot's expert output goes to the workspace's slot buffer (rows in
+// expert-sorted position order); pos (the inverse of perm: routed slot f -> position) then locates
+// the slots of every token, which are summed in a fixed order into y (rounded once) or added to acc;
+// or, for the stage outputs (stages), gathered in slot order into yslot_out (when non-null) with h
+// to h_out, and nothing is summed.
+int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsLayout &L, void *ws, uint16_t *y,
+                            const int32_t *pos, cudaStream_t st, bool stages = false, float *h_out = nullptr,
+                            float *yslot_out = nullptr)
 {
     PrefillArgs a{};
     a.x = ea.x;
@@ -208,7 +223,7 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     a.xsum = ws_at<float>(ws, L.xsum);
     a.xe = ws_at<int>(ws, L.xe);
     a.h_out = h_out;
-    a.yslot_out = yslot_out;
+    a.yslot = ea.yslot;
     a.hsum = ws_at<float>(ws, L.hsum);
     a.hs = ws_at<uint16_t>(ws, L.h);
     a.gate = ea.gate;
@@ -222,10 +237,6 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     a.perm = ea.perm;
     a.work_g1 = ws_at<WorkItem>(ws, L.work_g1);
     a.work_g2 = ws_at<WorkItem>(ws, L.work_g2);
-    a.p = ea.p;
-    a.w_s = ea.w_s;
-    a.acc = ea.acc;
-    a.acc_zero = acc_zero;
     a.status = ea.status;
     a.T = ea.T;
     a.H = c.hidden;
@@ -237,7 +248,13 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     a.max_w2 = L.max_w2;
     a.bits = c.bits;
     a.wait_limit = wait_limit_of(c);
-    return cuda_rc(launch_prefill_experts(a, st));
+    const int rc = cuda_rc(launch_prefill_experts(a, st));
+    if (rc) return rc;
+    if (stages)
+        return yslot_out ? cuda_rc(launch_slot_gather(ea.yslot, pos, yslot_out, ea.T, c.hidden, c.top_k, c.has_shared,
+                                                      ea.status, st))
+                         : MOE_OK;
+    return enqueue_slot_sum(c, ea, y, st, pos);
 }
 
 // Arguments of the fused decode kernel common to all of its callers.
@@ -422,7 +439,9 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     if ((rc = cuda_rc(launch_worklist(wa, st)))) return rc;
     ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_shared, offsets, perm, acc, L, ws);
     if (rp == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, nullptr, st);
-    return enqueue_prefill_experts(*cfg, ea, L, ws, 0, st);
+    int32_t *pos = ws_at<int32_t>(ws, L.inv_perm);     // routed slot -> expert-sorted position
+    if ((rc = cuda_rc(launch_invert_perm(perm, pos, T * cfg->top_k, ea.status, st)))) return rc;
+    return enqueue_prefill_experts(*cfg, ea, L, ws, nullptr, pos, st);
 }
 
 int moe_combine(const moe_config *cfg, int T, const float *acc, uint16_t *y, void *stream)
@@ -475,8 +494,7 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
         return rc;
     ExpertArgs ea = expert_args(*cfg, *w, x, T, p, w_s, offsets, perm, ws_at<float>(ws, L.acc), L, ws);
     if (rp == MOE_PATH_DECODE) return enqueue_decode_experts(*cfg, ea, L, ws, y, st);
-    if ((rc = enqueue_prefill_experts(*cfg, ea, L, ws, 1, st))) return rc;
-    return cuda_rc(launch_combine(ea.acc, y, (size_t)T * cfg->hidden, st));
+    return enqueue_prefill_experts(*cfg, ea, L, ws, y, inv_perm, st);
 }
 
 int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *device_status)
@@ -561,7 +579,9 @@ int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_
     // the weights are not applied: any values serve (the workspace's own p and w_s rows)
     ExpertArgs ea = expert_args(*cfg, *w, x, T, ws_at<uint16_t>(ws, L.p), ws_at<uint16_t>(ws, L.w_s), offsets, perm,
                                 ws_at<float>(ws, L.acc), L, ws);
-    return enqueue_prefill_experts(*cfg, ea, L, ws, 1, st, h_out, yslot_out);
+    int32_t *pos = ws_at<int32_t>(ws, L.inv_perm);     // routed slot -> expert-sorted position
+    if ((rc = cuda_rc(launch_invert_perm(perm, pos, T * cfg->top_k, ea.status, st)))) return rc;
+    return enqueue_prefill_experts(*cfg, ea, L, ws, nullptr, pos, st, true, h_out, yslot_out);
 }
 
 int moe_decode_timeline(const moe_config *cfg, int T, void *ws, size_t ws_bytes, void *stream,

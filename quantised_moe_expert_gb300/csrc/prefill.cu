@@ -20,10 +20,11 @@
 //     and store them in the swizzled K-major layout the MMA reads;
 //   - one thread issues tcgen05.mma (fp16 in, fp32 accumulate in TMEM) and
 //     releases each stage with tcgen05.commit.
-// Four epilogue warps read the previous tile's accumulators with tcgen05.ld
-// from the other half of TMEM while the next tile accumulates: the gate/up
-// GEMM writes h = silu(g) * u as fp16 in expert-sorted row order, the down
-// GEMM adds p * y into the fp32 layer accumulator with atomics.
+// Epilogue warps read the accumulators with tcgen05.ld: the gate/up GEMM writes
+// h = silu(g) * u as fp16 in expert-sorted row order; the down GEMM, from the
+// other half of TMEM while the next tile accumulates, writes each slot's expert
+// output y_e (fp32) once with bulk stores, and the slots of every token are
+// summed afterwards in a fixed order (the pick weights applied there).
 //
 // Operand type.  MMA operands are fp16: dequantised weights and the
 // intermediate h keep 11 significant bits (bf16 would keep 8, which puts the
@@ -61,19 +62,20 @@ constexpr int kCodeStages1B8 = 3, kCodeStages2B8 = 3;           // 8-bit codes: 
 constexpr int code_row_bytes(int bits) { return 8 * bits; }
 constexpr int code_stage1(int bits) { return 2 * 128 * code_row_bytes(bits); }
 constexpr int code_stage2(int bits) { return 128 * code_row_bytes(bits); }
-constexpr int kRedCols = 16;        // down epilogue: columns per bulk-reduce chunk (two chunk buffers)
+constexpr int kRedCols = 16, kRedBufs = 2;   // down epilogue: columns per bulk-reduce chunk, chunk buffers
 // Warp roles of the down GEMM: 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue.
 constexpr int kDequantThreads = 256;
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10;
 constexpr int kThreads = 448;                                   // down GEMM
 // Gate/up GEMM: warps 0-15 dequantise (0-7 the even K-steps, 8-15 the odd ones, so two
-// steps of each row are in flight), 16 TMA, 17 MMA, 18-21 epilogue, and two token-row
-// loader warps (22, 23) that take the K-steps in turn, each with kLoaderDepth of its
+// steps of each row are in flight), 16 TMA, 17 MMA, 18-25 epilogue (two per TMEM lane quarter:
+// the epilogue holds the single accumulator pair, so the MMAs of the next tile wait for it),
+// and two token-row loader warps (26, 27) that take the K-steps in turn, each with kLoaderDepth of its
 // steps in flight.
 constexpr int kDequantWarps1 = 16, kStepWarps1 = 8;
-constexpr int kWarpTma1 = 16, kWarpMma1 = 17, kWarpEpi1 = 18, kEpiWarps1 = 4;
+constexpr int kWarpTma1 = 16, kWarpMma1 = 17, kWarpEpi1 = 18, kEpiWarps1 = 8;
 constexpr int kWarpLoader1 = kWarpEpi1 + kEpiWarps1, kLoaderWarps1 = 2, kLoaderDepth = 2;
-constexpr int kThreads1 = 32 * (kWarpLoader1 + kLoaderWarps1);  // 768
+constexpr int kThreads1 = 32 * (kWarpLoader1 + kLoaderWarps1);  // 896
 constexpr int kScaleChunk1 = 8;                                 // gate/up: groups per scale chunk
 constexpr long long kDrainLimit = 1ll << 22;
 constexpr uint32_t kTmemA1 = 256;   // gate/up GEMM: accumulators in TMEM columns [0, 256), A stages from 256
@@ -101,11 +103,9 @@ struct G2Params {
     const WorkItem *work;
     const int32_t *offsets;
     const int32_t *perm;
-    const uint16_t *p;                 // bf16 [T, k]
-    const uint16_t *w_s;               // bf16 [T]
-    float *acc;                        // f32 [T, H]
     const int *xe;                     // i32 [T]: e of each token (the h tile holds h 2^-2e)
-    float *yslot_out;                  // f32 [T*k + T, H]: unweighted expert output per slot instead of acc, or null
+    float *yslot;                      // f32 [T*k + T, H]: each slot's expert output before its pick weight, rows
+                                       // in expert-sorted position order (the rows of the h tiles)
     const uint8_t *dc, *sdc;           // int4 codes (routed [E, H, I/2], shared [H, I/2]), for L2 prefetch
     const uint16_t *ds, *db;           // routed down scales, biases [E, H, I/64]
     const uint16_t *sds, *sdb;         // shared [H, I/64]
@@ -241,11 +241,11 @@ __device__ __forceinline__ void prefetch_rows(const void *p, uint32_t bytes)
 // --------------------------------------------------------------- gate/up GEMM
 //
 // Persistent: one CTA per SM loops over tiles tau = blockIdx.x + i * gridDim.x.
-// Roles: warps 0-7 dequantise the code tiles (0-3 gate rows, 4-7 up rows) into A
-// stages in tensor memory; warp 8 (one thread) streams code tiles with TMA through a
-// ring of CS stages and asks L2 for the next tile in bulk; warp 9 (one thread)
-// issues the MMAs (A from tensor memory, B from shared memory); warps 10-13 run the
-// epilogue; warps 14-17 gather the token rows of x with cp.async, SB - 2 steps ahead.
+// Roles (constants above): the dequantising warps turn code tiles into A stages in tensor
+// memory; one thread streams code tiles with TMA through a ring of CS stages and asks L2
+// for the next tile in bulk; one thread issues the MMAs (A from tensor memory, B from
+// shared memory); the epilogue warps turn the accumulators into h; the loader warps
+// gather the token rows of x with cp.async into a ring of SB stages.
 // Tensor memory: gate and up accumulators in columns [0, 256) (one buffer, so a tile's
 // first MMAs wait for the previous epilogue's reads), A stages from column 256.
 // BITS: expert code width (4 or 8).
@@ -686,7 +686,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
 template <int S, int SB, int CS, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_down_kernel(const __grid_constant__ CUtensorMap map_dc, const __grid_constant__ CUtensorMap map_sdc,
-                     const __grid_constant__ CUtensorMap map_h, const G2Params P)
+                     const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_y,
+                     const G2Params P)
 {
     const int H = P.H, I = P.I, GI = I / kGroup, nk = GI, MB = (H + 127) / 128, Tk = P.T * P.k;
     constexpr int CB = code_row_bytes(BITS), CST = code_stage2(BITS);
@@ -703,13 +704,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sB = sA + S * 16384;                 // SB x 32 KB (256 rows x 128 B)
     uint8_t *sC = sB + SB * 32768;                // CS x CST
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * CST);    // [dequant thread][2][2][kScaleChunk1]
-    float *sRed = reinterpret_cast<float *>(sScale + kDequantThreads * 4 * kScaleChunk1);   // [2][kRedCols][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sRed + 2 * kRedCols * 128);
+    float *sRed = reinterpret_cast<float *>(sScale + kDequantThreads * 4 * kScaleChunk1);   // [kRedBufs][kRedCols][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sRed + kRedBufs * kRedCols * 128);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
-    int *s_tok = reinterpret_cast<int *>(drain + 1);           // [2][256]
-    float *s_w = reinterpret_cast<float *>(s_tok + 512);       // [2][256]
+    float *s_w = reinterpret_cast<float *>(drain + 1);          // [2][256]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_w + 512);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
@@ -953,42 +953,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
             const int N = (ti.ntok + 15) & ~15;
             const int buf = i & 1;
-            int *tok = s_tok + buf * 256;
             float *wv = s_w + buf * 256;
-            // destination row and factor of each column (epilogue threads 320..447 fill them): the
-            // token's row of acc and p 2^2e (the h tile holds h 2^-2e; exact), or in stage mode the
-            // slot's row of yslot_out and 2^2e
+            // factor 2^2e of each column (epilogue threads 320..447 fill them): the h tile holds h 2^-2e,
+            // the factor undoes it (exact)
             for (int n = tid - kWarpEpi * 32; n < 256; n += 128) {
-                int dst = -1;
                 float wgt = 0.f;
                 if (n < ti.ntok) {
-                    int t = -1, f = -1;
+                    int t = -1;
                     if (ti.shared_e) {
                         t = ti.tok0 + n;
-                        f = Tk + t;
-                        wgt = bf16_bits_to_float(P.w_s[t]);
                     } else {
                         const int pos = ti.pbase + n;
-                        f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
-                        if (f < 0 || f >= Tk) {
-                            record_status(P.status, MOE_ERR_DEVICE);
-                        } else {
-                            t = f / P.k;
-                            wgt = bf16_bits_to_float(P.p[f]);
-                        }
+                        const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                        if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
+                        else t = f / P.k;
                     }
                     if (t >= 0) {
                         const float up = pow2f(__ldg(P.xe + t));
-                        if (P.yslot_out != nullptr) {
-                            dst = f;
-                            wgt = up * up;
-                        } else {
-                            dst = t;
-                            wgt = wgt * up * up;
-                        }
+                        wgt = up * up;
                     }
                 }
-                tok[n] = dst;
                 wv[n] = wgt;
             }
             if (bar_any(2, 128, *s_abort)) break;
@@ -997,9 +981,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!got) set_abort(s_abort, P.status);
             if (bar_any(2, 128, !got)) break;                // the four warps stop together
             tc_fence_after();
-            // w * y of 16 columns at a time into a shared-memory chunk [column][row], then one bulk
-            // reduce-add per column into the token's row of acc (the tile's rows are contiguous
-            // there): the bulk copy engine does the adds, not one atomic per element
+            // 2^2e y of 16 columns at a time into a shared-memory chunk [column][row], then one tiled
+            // store of the chunk: its columns are 16 consecutive rows of yslot (expert-sorted positions)
+            // and the tile's 128 rows of H are contiguous there (a ragged last chunk: one bulk store per
+            // column).  Every (slot, row) is written once; the slots are summed afterwards in a fixed
+            // order.
             const int rloc = quad * 32 + lane, nrow = min(128, H - ti.mb * 128), e = tid - kWarpEpi * 32;
             const uint32_t d0 = tmem + lane_base + (uint32_t)buf * 256;
             for (int n0 = 0; n0 < N; n0 += kRedCols, ++redc) {
@@ -1010,25 +996,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     mbar_arrive(smem_u32(tempty + buf));
                 }
-                float *red = sRed + (redc & 1) * kRedCols * 128;
-                if (e < kRedCols) bulk_wait_read<1>();    // this buffer's reduces (two chunks ago) have read it
+                float *red = sRed + (redc % kRedBufs) * kRedCols * 128;
+                if (e < kRedCols) bulk_wait_read<kRedBufs - 1>();   // this buffer's stores (kRedBufs chunks ago) have read it
                 named_bar(2, 128);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) red[j * 128 + rloc] = wv[n0 + j] * __uint_as_float(v[j]);
                 fence_proxy_async_smem();
                 named_bar(2, 128);
                 if (e < kRedCols) {
-                    const int n = n0 + e;
-                    const int t = n < ti.ntok ? tok[n] : -1;
-                    float *dst_base = P.yslot_out != nullptr ? P.yslot_out : P.acc;
-                    if (t >= 0) bulk_reduce_add_f32(dst_base + (size_t)t * H + ti.mb * 128, smem_u32(red + e * 128),
-                                                    (uint32_t)nrow * 4);
+                    if (n0 + kRedCols <= ti.ntok) {
+                        if (e == 0) tma_store_2d(&map_y, ti.mb * 128, ti.pbase + n0, smem_u32(red));
+                    } else if (n0 + e < ti.ntok) {
+                        bulk_store(P.yslot + (size_t)(ti.pbase + n0 + e) * H + ti.mb * 128, smem_u32(red + e * 128),
+                                   (uint32_t)nrow * 4);
+                    }
                     bulk_commit();
                 }
             }
-            if (bar_any(2, 128, *s_abort)) break;           // tok/wv of this buffer are reused two tiles later
+            if (bar_any(2, 128, *s_abort)) break;           // wv of this buffer is reused two tiles later
         }
-        bulk_wait<0>();                                   // every reduce-add has completed
+        bulk_wait<0>();                                   // every bulk store has completed
     }
     tc_fence_before();
     __syncthreads();
@@ -1107,8 +1094,8 @@ size_t g1_smem(int cs, int bits)
 size_t g2_smem(int cs, int bits)
 {
     return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + (size_t)cs * code_stage2(bits) +
-           kDequantThreads * 4 * kScaleChunk1 * 2 + 2 * kRedCols * 128 * 4 +
-           8 * (2 * cs + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 1024 * 4 + 16;
+           kDequantThreads * 4 * kScaleChunk1 * 2 + kRedBufs * kRedCols * 128 * 4 +
+           8 * (2 * cs + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 512 * 4 + 16;
 }
 
 // Launch allowed (pdl) to begin while the previous kernel of the stream still runs.
@@ -1152,11 +1139,10 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
         if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaSuccess;
-    if (a.acc_zero && !a.yslot_out && (e = launch_zero(a.acc, (size_t)T * H, st)) != cudaSuccess) return e;
 
     if (a.bits != 4 && a.bits != 8) return cudaErrorInvalidValue;
     const bool b8 = a.bits == 8;
-    CUtensorMap mgc, muc, msgc, msuc, mdc, msdc, mh;
+    CUtensorMap mgc, muc, msgc, msuc, mdc, msdc, mh, my;
     const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
     // code boxes: 32 bytes (4-bit, unswizzled) or 64 bytes with the 64-byte swizzle (8-bit) of 128 rows
     const CUtensorMapSwizzle csw = b8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -1167,7 +1153,9 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     bool ok = make_map_2d(&mgc, a.gate.codes, u8, 1, hrow, (uint64_t)E * I, cbox, 128, csw) &&
               make_map_2d(&muc, a.up.codes, u8, 1, hrow, (uint64_t)E * I, cbox, 128, csw) &&
               make_map_2d(&mdc, a.down.codes, u8, 1, irow, (uint64_t)E * H, cbox, 128, csw) &&
-              make_map_2d(&mh, a.hs, f16, 2, I, (uint64_t)T * k + (uint64_t)T, 64, 32, sw128);
+              make_map_2d(&mh, a.hs, f16, 2, I, (uint64_t)T * k + (uint64_t)T, 64, 32, sw128) &&
+              make_map_2d(&my, a.yslot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, (uint64_t)T * k + (uint64_t)T, 128,
+                          kRedCols, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (ns)
         ok = ok && make_map_2d(&msgc, a.s_gate.codes, u8, 1, hrow, I, cbox, 128, csw) &&
              make_map_2d(&msuc, a.s_up.codes, u8, 1, hrow, I, cbox, 128, csw) &&
@@ -1230,11 +1218,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p2.work = a.work_g2;
     p2.offsets = a.offsets;
     p2.perm = a.perm;
-    p2.p = a.p;
-    p2.w_s = a.w_s;
-    p2.acc = a.acc;
     p2.xe = a.xe;
-    p2.yslot_out = a.yslot_out;
+    p2.yslot = a.yslot;
     p2.dc = a.down.codes;
     p2.sdc = a.has_shared ? a.s_down.codes : a.down.codes;
     p2.ds = a.down.scales;
@@ -1260,7 +1245,7 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
     const int tiles2 = a.max_w2 * ((H + 127) / 128);
     if (small && (e = launch_small_down(a, st)) != cudaSuccess) return e;
-    return launch_pdl(small, k2, std::min(sm_count(), tiles2), kThreads, s2, st, mdc, msdc, mh, p2);
+    return launch_pdl(small, k2, std::min(sm_count(), tiles2), kThreads, s2, st, mdc, msdc, mh, my, p2);
 }
 
 }  // namespace qmoe

@@ -24,8 +24,8 @@
 //   as fp16 in the codes' k order.
 // Down kernel (tiles of 256 rows of H): the same with the down codes, the item's h rows
 //   (TMA, the same swizzle) and the group sums of h that the gate/up kernel's epilogue
-//   stored; warp w < 16 owns rows 16 w .. + 15; the epilogue adds p * y into the fp32
-//   layer accumulator.
+//   stored; warp w < 16 owns rows 16 w .. + 15; the epilogue writes each slot's expert
+//   output y_e (fp32) once into the slot buffer.
 #include <algorithm>
 
 #include "kernels.cuh"
@@ -75,10 +75,9 @@ struct SmallParams {
     const float *xsum;                 // f32 [T, H / 64]
     const int *xe;                     // i32 [T]: e of each token
     float *h_out;                      // f32 [T*k + T, I] h per slot (stage output), or null
-    float *yslot_out;                  // f32 [T*k + T, H] unweighted expert output per slot instead of acc, or null
+    float *yslot;                      // f32 [T*k + T, H] each slot's expert output before its pick weight, rows in
+                                       // expert-sorted position order (the rows of the h tiles)
     float *hsum;                       // f32 [T*k + T, I / 64]: group sums of the stored (fp16) h
-    const uint16_t *p, *w_s;           // bf16 pick weights [T, k], shared weights [T]
-    float *acc;                        // f32 [T, H]
     const uint8_t *c0, *c1, *sc0, *sc1;            // codes (routed, shared) for L2 prefetch: gate, up / down
     const uint16_t *s0, *b0, *s1, *b1;             // routed scales, biases: gate, up / down
     const uint16_t *ss0, *sb0, *ss1, *sb1;         // shared expert
@@ -526,35 +525,24 @@ __global__ void __launch_bounds__(kSThreads2, 1)
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
             const STile t = stile(P, nbig, tau, MB, Tk);
             const int buf = i & 1;
-            // destination row and factor of column `lane`: the token's row of acc and p 2^2e (the h
-            // tile holds h 2^-2e; exact), or in stage mode the slot's row of yslot_out and 2^2e
+            // row of yslot (the column's expert-sorted position) and factor 2^2e of column `lane` (the h
+            // tile holds h 2^-2e; exact)
             int tok = -1;
             float wgt = 0.f;
             if (lane < t.ntok) {
-                int tt = -1, f = -1;
+                int tt = -1;
                 if (t.shared_e) {
                     tt = t.tok0 + lane;
-                    f = Tk + tt;
-                    wgt = bf16_bits_to_float(P.w_s[tt]);
                 } else {
                     const int pos = t.pbase + lane;
-                    f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
-                    if (f < 0 || f >= Tk) {
-                        record_status(P.status, MOE_ERR_DEVICE);
-                    } else {
-                        tt = f / P.k;
-                        wgt = bf16_bits_to_float(P.p[f]);
-                    }
+                    const int f = (pos >= 0 && pos < Tk) ? __ldg(P.perm + pos) : -1;
+                    if (f < 0 || f >= Tk) record_status(P.status, MOE_ERR_DEVICE);
+                    else tt = f / P.k;
                 }
                 if (tt >= 0) {
                     const float up = pow2f(__ldg(P.xe + tt));
-                    if (P.yslot_out != nullptr) {
-                        tok = f;
-                        wgt = up * up;
-                    } else {
-                        tok = tt;
-                        wgt = wgt * up * up;
-                    }
+                    tok = t.pbase + lane;
+                    wgt = up * up;
                 }
             }
             bool got = i < 2 || mbar_wait(smem_u32(tempty + buf), ((i >> 1) - 1) & 1, limit, s_abort);
@@ -651,8 +639,7 @@ __global__ void __launch_bounds__(kSThreads2, 1)
             set_abort(s_abort, P.status);
             break;
         }
-        // acc[t, row] += w * y for the tile's rows and tokens (or the slot's row of yslot_out)
-        float *const dst_base = P.yslot_out != nullptr ? P.yslot_out : P.acc;
+        // y of the tile's rows and tokens into their rows of yslot (each element written once)
         const int *tok = s_tok + buf * kSmallN;
         const float *wv = s_w + buf * kSmallN;
 #pragma unroll
@@ -663,7 +650,7 @@ __global__ void __launch_bounds__(kSThreads2, 1)
                 const int erow = t.mb * 256 + r0 + 8 * (e >> 1);
                 if (col < ncol) {
                     const int tt = tok[col];
-                    if (tt >= 0) atomicAdd(dst_base + (size_t)tt * H + erow, wv[col] * acc[j][e]);
+                    if (tt >= 0) P.yslot[(size_t)tt * H + erow] = wv[col] * acc[j][e];
                 }
             }
         }
@@ -706,11 +693,8 @@ SmallParams small_params(const PrefillArgs &a, bool down)
     p.xsum = a.xsum;
     p.xe = a.xe;
     p.h_out = a.h_out;
-    p.yslot_out = a.yslot_out;
+    p.yslot = a.yslot;
     p.hsum = a.hsum;
-    p.p = a.p;
-    p.w_s = a.w_s;
-    p.acc = a.acc;
     if (down) {
         p.c0 = a.down.codes;
         p.sc0 = a.has_shared ? a.s_down.codes : a.down.codes;

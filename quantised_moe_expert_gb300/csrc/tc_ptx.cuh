@@ -165,6 +165,23 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float *dst, uint32_t src, ui
                  "r"(bytes)
                  : "memory");
 }
+// dst[0, bytes) = src[0, bytes): shared -> global by the bulk copy engine (both addresses 16-byte
+// aligned, size a multiple of 16); tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+// Tiled shared -> global store of one box at (x, y) of a 2D tensor map (x * element size a multiple of
+// 16 bytes, y >= 0); elements outside the tensor are not written.  Tracked by the issuing thread's
+// bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until all but the newest N of this thread's bulk groups have read their source.
 template <int N>

@@ -167,10 +167,8 @@ def stages(layer, x_bits, ids, path):
     inv = torch.empty(T * sh.top_k, dtype=torch.int32, device="cuda")
     qm.moe_permute(layer.cfg, d_ids, T, counts, offsets, perm, inv, ws)
     h = torch.full((nslot, sh.inter), float("nan"), dtype=torch.float32, device="cuda")
-    # the prefill GEMMs add each tile's rows into the slot outputs: zero-filled there (a row never
-    # written then shows as a mismatch); the decode kernels write every element (NaN marks a miss)
-    fill = 0.0 if path == qm.MOE_PATH_PREFILL else float("nan")
-    ys = torch.full((nslot, sh.hidden), fill, dtype=torch.float32, device="cuda")
+    # both paths write every element of the slot outputs once: NaN marks an element never written
+    ys = torch.full((nslot, sh.hidden), float("nan"), dtype=torch.float32, device="cuda")
     qm.moe_expert_stages(layer.cfg, layer.w, x, T, d_ids, counts, offsets, perm, h, ys, path, ws)
     torch.cuda.synchronize()
     assert qm.moe_get_device_status(ws) == 0
