@@ -651,6 +651,13 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
 // warp w takes H / 128 tiles of 16 rows, K = 32 (the slice), raw sums P = sum (q - 8) h'.  The
 // down codes enter the MMA signed: with 1024 + q the sum would be ~1024 sum h' and cancel about
 // eight bits against the bias term, beyond what the tensor cores' fp32 accumulation keeps.
+// Element e (0..7, a compile-time index after unrolling) of eight bf16 packed in a uint4, as fp32.
+__device__ __forceinline__ float bf16_of8(uint4 v, int e)
+{
+    const uint32_t w = e < 2 ? v.x : e < 4 ? v.y : e < 6 ? v.z : v.w;
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
 template <int NT>
 __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs &a, const FusedGeom &geo,
                                                 const uint8_t *ring, const uint16_t *s_x, const float *s_xs,
@@ -694,18 +701,13 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             for (int j = 0; j < NT; ++j)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) accg[j][v] = accu[j][v] = 0.f;
-#pragma unroll 2
-            for (int gi = 0; gi < gq; ++gi) {
-                const int grp = kq * gq + gi, q = grp & 3;
+            // one group: codes of rows g, g + 8 of both matrices, the group's scales s and offsets b - 128 s
+            auto group_step = [&](int grp, float sg0, float sg1, float kg0, float kg1, float su0, float su1, float ku0,
+                                  float ku1) {
+                const int q = grp & 3;
                 const uint32_t o = (uint32_t)(grp >> 2) * (kSlice * 128) + swz_chunk(q, g, t4);
                 const uint2 g0 = *reinterpret_cast<const uint2 *>(cbg + o), g1 = *reinterpret_cast<const uint2 *>(cbg + o + 1024);
                 const uint2 u0 = *reinterpret_cast<const uint2 *>(cbu + o), u1 = *reinterpret_cast<const uint2 *>(cbu + o + 1024);
-                const float sg0 = bf16_bits_to_float(scg[grp]), sg1 = bf16_bits_to_float(scg[8 * G + grp]);
-                const float su0 = bf16_bits_to_float(scu[grp]), su1 = bf16_bits_to_float(scu[8 * G + grp]);
-                const float kg0 = fmaf(-128.f, sg0, bf16_bits_to_float(big[grp]));
-                const float kg1 = fmaf(-128.f, sg1, bf16_bits_to_float(big[8 * G + grp]));
-                const float ku0 = fmaf(-128.f, su0, bf16_bits_to_float(biu[grp]));
-                const float ku1 = fmaf(-128.f, su1, bf16_bits_to_float(biu[8 * G + grp]));
                 uint32_t ag0[8], ag1[8], au0[8], au1[8];
                 nib8<false>(g0.x, ag0);
                 nib8<false>(g0.y, ag0 + 4);
@@ -744,20 +746,55 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                     accu[j][2] = fmaf(su1, du[2], fmaf(ku1, xA, accu[j][2]));
                     accu[j][3] = fmaf(su1, du[3], fmaf(ku1, xB, accu[j][3]));
                 }
+            };
+            if ((gq & 7) == 0) {
+                // scales and biases of eight groups per 16-byte load: rows g and g + 8 sit 64 bytes apart
+                // per 32 groups, so each 2-byte load would meet three other rows in its bank
+#pragma unroll 1
+                for (int gb = 0; gb < gq; gb += 8) {
+                    const int g0 = kq * gq + gb;
+                    const uint4 vsg0 = *reinterpret_cast<const uint4 *>(scg + g0);
+                    const uint4 vsg1 = *reinterpret_cast<const uint4 *>(scg + 8 * G + g0);
+                    const uint4 vbg0 = *reinterpret_cast<const uint4 *>(big + g0);
+                    const uint4 vbg1 = *reinterpret_cast<const uint4 *>(big + 8 * G + g0);
+                    const uint4 vsu0 = *reinterpret_cast<const uint4 *>(scu + g0);
+                    const uint4 vsu1 = *reinterpret_cast<const uint4 *>(scu + 8 * G + g0);
+                    const uint4 vbu0 = *reinterpret_cast<const uint4 *>(biu + g0);
+                    const uint4 vbu1 = *reinterpret_cast<const uint4 *>(biu + 8 * G + g0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float sg0 = bf16_of8(vsg0, e), sg1 = bf16_of8(vsg1, e);
+                        const float su0 = bf16_of8(vsu0, e), su1 = bf16_of8(vsu1, e);
+                        group_step(g0 + e, sg0, sg1, fmaf(-128.f, sg0, bf16_of8(vbg0, e)), fmaf(-128.f, sg1, bf16_of8(vbg1, e)),
+                                   su0, su1, fmaf(-128.f, su0, bf16_of8(vbu0, e)), fmaf(-128.f, su1, bf16_of8(vbu1, e)));
+                    }
+                }
+            } else {
+#pragma unroll 2
+                for (int gi = 0; gi < gq; ++gi) {
+                    const int grp = kq * gq + gi;
+                    const float sg0 = bf16_bits_to_float(scg[grp]), sg1 = bf16_bits_to_float(scg[8 * G + grp]);
+                    const float su0 = bf16_bits_to_float(scu[grp]), su1 = bf16_bits_to_float(scu[8 * G + grp]);
+                    group_step(grp, sg0, sg1, fmaf(-128.f, sg0, bf16_bits_to_float(big[grp])),
+                               fmaf(-128.f, sg1, bf16_bits_to_float(big[8 * G + grp])), su0, su1,
+                               fmaf(-128.f, su0, bf16_bits_to_float(biu[grp])),
+                               fmaf(-128.f, su1, bf16_bits_to_float(biu[8 * G + grp])));
+                }
             }
-            float *redg = s_red + ((size_t)(0 * 4 + kq) * kSlice + mt * 16) * NC;   // [32 rows][NC]
-            float *redu = s_red + ((size_t)(1 * 4 + kq) * kSlice + mt * 16) * NC;
+            // column-major [NC][32 rows]: the h step below reads one column's 32 rows, one per lane
+            float *redg = s_red + (size_t)(0 * 4 + kq) * NC * kSlice + mt * 16;
+            float *redu = s_red + (size_t)(1 * 4 + kq) * NC * kSlice + mt * 16;
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int c0 = j * 8 + 2 * t4;
-                redg[g * NC + c0] = accg[j][0];
-                redg[g * NC + c0 + 1] = accg[j][1];
-                redg[(g + 8) * NC + c0] = accg[j][2];
-                redg[(g + 8) * NC + c0 + 1] = accg[j][3];
-                redu[g * NC + c0] = accu[j][0];
-                redu[g * NC + c0 + 1] = accu[j][1];
-                redu[(g + 8) * NC + c0] = accu[j][2];
-                redu[(g + 8) * NC + c0 + 1] = accu[j][3];
+                redg[c0 * kSlice + g] = accg[j][0];
+                redg[(c0 + 1) * kSlice + g] = accg[j][1];
+                redg[c0 * kSlice + g + 8] = accg[j][2];
+                redg[(c0 + 1) * kSlice + g + 8] = accg[j][3];
+                redu[c0 * kSlice + g] = accu[j][0];
+                redu[(c0 + 1) * kSlice + g] = accu[j][1];
+                redu[c0 * kSlice + g + 8] = accu[j][2];
+                redu[(c0 + 1) * kSlice + g + 8] = accu[j][3];
             }
         }
         // a warp releases the chunks only once both have landed (its waits succeeded): otherwise the
@@ -777,11 +814,11 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
 #pragma unroll 1
         for (int c = warp; c < ncol; c += kCW) {
             const int row = lane;
-            float gs = s_red[((0 * 4 + 0) * kSlice + row) * NC + c], us = s_red[((4 + 0) * kSlice + row) * NC + c];
+            float gs = s_red[((0 * 4 + 0) * NC + c) * kSlice + row], us = s_red[((4 + 0) * NC + c) * kSlice + row];
 #pragma unroll
             for (int v = 1; v < 4; ++v) {
-                gs += s_red[((0 * 4 + v) * kSlice + row) * NC + c];
-                us += s_red[((4 + v) * kSlice + row) * NC + c];
+                gs += s_red[((0 * 4 + v) * NC + c) * kSlice + row];
+                us += s_red[((4 + v) * NC + c) * kSlice + row];
             }
             const int t = S.ctok[colbase + c];
             const float hv = gs / (1.f + __expf(-gs * pow2f(S.xe[t]))) * us;
@@ -1033,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *ring = dyn;
     uint16_t *s_x = reinterpret_cast<uint16_t *>(dyn + geo.x_off);    // [T][G * 72 + 8] bf16 x', k order
     float *s_xs = reinterpret_cast<float *>(dyn + geo.xs_off);         // [T][G] group sums of x'
-    float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);       // [2][4][32][NC]
+    float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);       // [2][4][NC][32]
     uint16_t *s_h = reinterpret_cast<uint16_t *>(dyn + geo.h_off);     // [NC][32] fp16 h', k order
     float *s_hs = reinterpret_cast<float *>(dyn + geo.hs_off);         // [NC]
 

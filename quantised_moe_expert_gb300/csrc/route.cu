@@ -132,6 +132,21 @@ __device__ __forceinline__ uint32_t logit_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// bf16 rounding of a positive fp32 value v known to a few fp32 ulps: the rounded bits when v lies more
+// than kBf16Margin fp32 ulps from a bf16 rounding midpoint (so the exact value rounds the same way),
+// else kBf16Unclear (not a bf16 of a finite positive value below 2).  Values below 2^-100 (where an
+// underflowing exp loses its relative accuracy) are always unclear.
+constexpr int kBf16Margin = 64;
+constexpr uint16_t kBf16Unclear = 0xFFFFu;
+__device__ __forceinline__ uint16_t bf16_if_clear(float v)
+{
+    if (!(v >= 0x1p-100f)) return kBf16Unclear;
+    const uint32_t u = __float_as_uint(v);
+    const int low = (int)(u & 0xFFFFu) - 0x8000;       // distance from the midpoint in fp32 ulps
+    if (low > -kBf16Margin && low < kBf16Margin) return kBf16Unclear;
+    return float_to_bf16_bits(v);
+}
+
 __global__ void __launch_bounds__(256) topk_kernel(TopkArgs a)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,21 +199,40 @@ __global__ void __launch_bounds__(256) topk_kernel(TopkArgs a)
             if (j == 0) top_l = v;
             if (lane == j) { my_id = id; my_l = v; }
         }
-        // pick weights in fp64: p_j = exp(l_j - l_top) / sum_i exp(l_i - l_top)
-        double ex = 0.0;
-        if (lane < k) ex = exp((double)my_l - (double)top_l);
-        double den = 0.0;
-        for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order j = 0..k-1
+        // pick weights p_j = exp(l_j - l_top) / sum_i exp(l_i - l_top), rounded once to bf16.  In fp32
+        // first (the difference split exactly into hi + lo by Knuth's two-sum, exp(hi) (1 + lo), the sum in
+        // order j = 0..k-1): within about a dozen fp32 ulps of the exact value, so where every p lies more
+        // than kBf16Margin ulps from a bf16 rounding midpoint it rounds as the exact value does; otherwise
+        // the warp takes fp64.
+        float exf = 0.f;
+        if (lane < k) {
+            const float hi = my_l - top_l, bb = hi - my_l;
+            const float lo = (my_l - (hi - bb)) + (-top_l - bb);      // my_l - top_l = hi + lo exactly
+            exf = expf(hi) * (1.f + lo);
+        }
+        float denf = 0.f;
+        for (int j = 0; j < k; ++j) denf += __shfl_sync(0xffffffffu, exf, j);
+        const float pf = exf / denf;
+        uint16_t pb = bf16_if_clear(pf);
+        if (__any_sync(0xffffffffu, lane < k && pb == kBf16Unclear)) {
+            double ex = 0.0;
+            if (lane < k) ex = exp((double)my_l - (double)top_l);
+            double den = 0.0;
+            for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order j = 0..k-1
+            pb = double_to_bf16_bits(ex / den);
+        }
         if (lane < k) {
             a.ids[(size_t)t * k + lane] = my_id;
-            a.p[(size_t)t * k + lane] = double_to_bf16_bits(ex / den);
+            a.p[(size_t)t * k + lane] = pb;
             atomicAdd(a.hist + (size_t)(t / kTokBlock) * E + my_id, 1);
         }
         if (lane == 0 && a.w_s) {
             uint16_t ws = 0;
             if (a.has_shared) {
+                // bf16(sigmoid(bf16(gamma))): fp32 first, fp64 near a rounding midpoint
                 const float gb = bf16_bits_to_float(float_to_bf16_bits(a.gamma[t]));
-                ws = double_to_bf16_bits(1.0 / (1.0 + exp(-(double)gb)));
+                ws = bf16_if_clear(1.f / (1.f + expf(-gb)));
+                if (ws == kBf16Unclear) ws = double_to_bf16_bits(1.0 / (1.0 + exp(-(double)gb)));
             }
             a.w_s[t] = ws;
         }

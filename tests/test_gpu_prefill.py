@@ -35,9 +35,10 @@ def test_prefill_tiny_all_rows():
     assert stats["max_abs"] <= 2e-2, stats
 
 
-@pytest.mark.parametrize("T", [1, 3, 17, 40, 129])
+@pytest.mark.parametrize("T", [1, 3, 17, 40, 129, 2000])
 def test_prefill_ragged_token_counts_small_layer(T):
-    """Token counts that leave ragged N tiles, several tiles per expert and tiny experts."""
+    """Token counts that leave ragged N tiles, several tiles per expert and tiny experts (T = 2000:
+    every routed expert above 32 tokens, on the tensor-memory GEMMs)."""
     wl, w, layer = H.device_layer(0)
     x = synth.make_x(wl.shape, T, wl.seed, stream=T)
     got = H.run_forward(layer, x, path=qm.MOE_PATH_PREFILL)
