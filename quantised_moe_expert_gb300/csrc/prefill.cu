@@ -62,11 +62,12 @@ constexpr int kCodeStages1B8 = 3, kCodeStages2B8 = 3;           // 8-bit codes: 
 constexpr int code_row_bytes(int bits) { return 8 * bits; }
 constexpr int code_stage1(int bits) { return 2 * 128 * code_row_bytes(bits); }
 constexpr int code_stage2(int bits) { return 128 * code_row_bytes(bits); }
-constexpr int kRedCols = 16, kRedBufs = 2;   // down epilogue: columns per bulk-reduce chunk, chunk buffers
-// Warp roles of the down GEMM: 0-7 dequantise, 8 TMA, 9 MMA, 10-13 epilogue.
+constexpr int kRedCols = 16, kRedBufs = 2;   // down epilogue: columns per store chunk, chunk buffers per team
+// Warp roles of the down GEMM: 0-7 dequantise, 8 TMA, 9 MMA, 10-17 epilogue (two teams of four warps,
+// one warp per TMEM lane quarter, taking the 16-column chunks of a tile in turn).
 constexpr int kDequantThreads = 256;
-constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10;
-constexpr int kThreads = 448;                                   // down GEMM
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10, kEpiTeams2 = 2;
+constexpr int kThreads = 32 * (kWarpEpi + 4 * kEpiTeams2);     // down GEMM: 576
 // Gate/up GEMM: warps 0-15 dequantise (0-7 the even K-steps, 8-15 the odd ones, so two
 // steps of each row are in flight), 16 TMA, 17 MMA, 18-25 epilogue (two per TMEM lane quarter:
 // the epilogue holds the single accumulator pair, so the MMAs of the next tile wait for it),
@@ -704,8 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sB = sA + S * 16384;                 // SB x 32 KB (256 rows x 128 B)
     uint8_t *sC = sB + SB * 32768;                // CS x CST
     uint16_t *sScale = reinterpret_cast<uint16_t *>(sC + CS * CST);    // [dequant thread][2][2][kScaleChunk1]
-    float *sRed = reinterpret_cast<float *>(sScale + kDequantThreads * 4 * kScaleChunk1);   // [kRedBufs][kRedCols][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sRed + kRedBufs * kRedCols * 128);
+    float *sRed = reinterpret_cast<float *>(sScale + kDequantThreads * 4 * kScaleChunk1);   // [team][kRedBufs][kRedCols][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sRed + kEpiTeams2 * kRedBufs * kRedCols * 128);
     uint64_t *cfull = bars, *cempty = cfull + CS, *afull = cempty + CS, *aempty = afull + S;
     uint64_t *bfull = aempty + S, *bempty = bfull + SB;
     uint64_t *tfull = bempty + SB, *tempty = tfull + 2, *drain = tempty + 2;
@@ -733,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(tfull + b), 1);
-            mbar_init(smem_u32(tempty + b), 128);
+            mbar_init(smem_u32(tempty + b), 128 * kEpiTeams2);
         }
         mbar_init(smem_u32(drain), 1);
         *s_abort = 0;
@@ -945,18 +946,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cp_async_wait_all();                               // no copy into shared memory outlives the CTA
     } else {
-        // ------------------------------------------------ epilogue: acc[t, row] += w * y
-        const int quad = warp & 3;
+        // ------------------------------------------------ epilogue: the slot outputs 2^2e y
+        // Team tm (warps 10 + 4 tm ..) takes chunks tm, tm + kEpiTeams2, ... of each tile with its own
+        // chunk buffers and named barrier (id 2 + tm); barrier 5 spans both teams.
+        constexpr int kEpiThreads = 128 * kEpiTeams2;
+        const int quad = warp & 3, tm = (warp - kWarpEpi) >> 2, et = tid - kWarpEpi * 32, e = et & 127;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        float *const sRedT = sRed + tm * kRedBufs * kRedCols * 128;
         int i = 0, redc = 0;
         for (int tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++i) {
             const TileInfo ti = tile_info(P.work, P.offsets, tau, MB, P.E, Tk);
             const int N = (ti.ntok + 15) & ~15;
             const int buf = i & 1;
             float *wv = s_w + buf * 256;
-            // factor 2^2e of each column (epilogue threads 320..447 fill them): the h tile holds h 2^-2e,
-            // the factor undoes it (exact)
-            for (int n = tid - kWarpEpi * 32; n < 256; n += 128) {
+            // factor 2^2e of each column (one per epilogue thread): the h tile holds h 2^-2e, the factor
+            // undoes it (exact)
+            for (int n = et; n < 256; n += kEpiThreads) {
                 float wgt = 0.f;
                 if (n < ti.ntok) {
                     int t = -1;
@@ -975,34 +980,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 wv[n] = wgt;
             }
-            if (bar_any(2, 128, *s_abort)) break;
+            if (bar_any(5, kEpiThreads, *s_abort)) break;
             bool got = mbar_wait(smem_u32(tfull + buf), (i >> 1) & 1, limit, s_abort);
             got = __all_sync(0xffffffffu, got);              // tcgen05.ld needs the whole warp
             if (!got) set_abort(s_abort, P.status);
-            if (bar_any(2, 128, !got)) break;                // the four warps stop together
+            if (bar_any(5, kEpiThreads, !got)) break;        // the epilogue warps stop together
             tc_fence_after();
             // 2^2e y of 16 columns at a time into a shared-memory chunk [column][row], then one tiled
             // store of the chunk: its columns are 16 consecutive rows of yslot (expert-sorted positions)
             // and the tile's 128 rows of H are contiguous there (a ragged last chunk: one bulk store per
             // column).  Every (slot, row) is written once; the slots are summed afterwards in a fixed
             // order.
-            const int rloc = quad * 32 + lane, nrow = min(128, H - ti.mb * 128), e = tid - kWarpEpi * 32;
+            const int rloc = quad * 32 + lane, nrow = min(128, H - ti.mb * 128);
             const uint32_t d0 = tmem + lane_base + (uint32_t)buf * 256;
-            for (int n0 = 0; n0 < N; n0 += kRedCols, ++redc) {
+            if (tm * kRedCols >= N) {                     // no chunk for this team: nothing to read
+                tc_fence_before();
+                mbar_arrive(smem_u32(tempty + buf));
+            }
+            for (int n0 = tm * kRedCols; n0 < N; n0 += kEpiTeams2 * kRedCols, ++redc) {
                 uint32_t v[16];
                 tmem_ld16(d0 + n0, v);
                 tmem_ld_wait();
-                if (n0 + kRedCols >= N) {                 // every column read: the MMAs may overwrite them
+                if (n0 + kEpiTeams2 * kRedCols >= N) {    // this team's last chunk read: the MMAs may overwrite
                     tc_fence_before();
                     mbar_arrive(smem_u32(tempty + buf));
                 }
-                float *red = sRed + (redc % kRedBufs) * kRedCols * 128;
+                float *red = sRedT + (redc % kRedBufs) * kRedCols * 128;
                 if (e < kRedCols) bulk_wait_read<kRedBufs - 1>();   // this buffer's stores (kRedBufs chunks ago) have read it
-                named_bar(2, 128);
+                named_bar(2 + tm, 128);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) red[j * 128 + rloc] = wv[n0 + j] * __uint_as_float(v[j]);
                 fence_proxy_async_smem();
-                named_bar(2, 128);
+                named_bar(2 + tm, 128);
                 if (e < kRedCols) {
                     if (n0 + kRedCols <= ti.ntok) {
                         if (e == 0) tma_store_2d(&map_y, ti.mb * 128, ti.pbase + n0, smem_u32(red));
@@ -1013,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_commit();
                 }
             }
-            if (bar_any(2, 128, *s_abort)) break;           // wv of this buffer is reused two tiles later
+            if (bar_any(5, kEpiThreads, *s_abort)) break;   // wv of this buffer is reused two tiles later
         }
         bulk_wait<0>();                                   // every bulk store has completed
     }
@@ -1094,7 +1103,7 @@ size_t g1_smem(int cs, int bits)
 size_t g2_smem(int cs, int bits)
 {
     return 1024 + kStagesA2 * 16384 + kStagesB2 * 32768 + (size_t)cs * code_stage2(bits) +
-           kDequantThreads * 4 * kScaleChunk1 * 2 + kRedBufs * kRedCols * 128 * 4 +
+           kDequantThreads * 4 * kScaleChunk1 * 2 + kEpiTeams2 * kRedBufs * kRedCols * 128 * 4 +
            8 * (2 * cs + 2 * kStagesA2 + 2 * kStagesB2 + 5) + 512 * 4 + 16;
 }
 
