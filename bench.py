@@ -670,7 +670,7 @@ def main():
         line["cpu_baseline"] = cb
     if not args.no_sweep and rank == 0:
         sweep = {}
-        others = [o for o in synth.WORKLOADS + synth.WORKLOADS_B8 if o.name != wl.name and o.tokens > 4]
+        others = [o for o in synth.WORKLOADS[1:] + synth.WORKLOADS_B8 if o.name != wl.name]   # not the tiny layer
         for other in others:
             try:
                 rr = run_ours(args, other, 0, 1, None, default_steps(other) // 2, 3, want_extras=False)
