@@ -1,6 +1,8 @@
 // Shared device/host definitions of the MoE layer kernels (sm_103a).
 #pragma once
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -89,6 +91,25 @@ inline int max_tiles(int T, int k, int E, int has_shared, int tile_n)
     const long long active = (long long)T * k < E ? (long long)T * k : E;
     long long t = (long long)T * k / tile_n + active + (has_shared ? (T + tile_n - 1) / tile_n : 0) + 1;
     return (int)t;
+}
+
+// Number of SMs of the current device, cached per device (atomics: calls may come from any host thread;
+// devices beyond the cache are queried every time).
+inline int device_sm_count()
+{
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cache[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const bool cached = dev >= 0 && dev < kMaxDev;
+    if (cached) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+    if (cached) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 inline WsLayout ws_layout(const moe_config &c, int T)

@@ -1125,14 +1125,6 @@ cudaError_t launch_pdl(bool pdl, void (*kern)(Args...), int grid, int threads, s
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-int sm_count()
-{
-    static int n[16] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!n[dev & 15]) cudaDeviceGetAttribute(&n[dev & 15], cudaDevAttrMultiProcessorCount, dev);
-    return n[dev & 15] > 0 ? n[dev & 15] : 1;
-}
 
 }  // namespace
 
@@ -1218,7 +1210,7 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     const bool small = prefill_small_fits(H, I, a.bits);   // items of small experts: mma.sync tiles (nwork[3] on)
     if (small && (e = launch_small_gateup(a, st)) != cudaSuccess) return e;
     // behind the small-tile kernel (if any) as its programmatic dependent
-    if ((e = launch_pdl(small, k1, std::min(sm_count(), tiles1), kThreads1, s1, st, mgc, muc, msgc, msuc, p1)) !=
+    if ((e = launch_pdl(small, k1, std::min(device_sm_count(), tiles1), kThreads1, s1, st, mgc, muc, msgc, msuc, p1)) !=
         cudaSuccess)
         return e;
 
@@ -1254,7 +1246,7 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
     const int tiles2 = a.max_w2 * ((H + 127) / 128);
     if (small && (e = launch_small_down(a, st)) != cudaSuccess) return e;
-    return launch_pdl(small, k2, std::min(sm_count(), tiles2), kThreads, s2, st, mdc, msdc, mh, my, p2);
+    return launch_pdl(small, k2, std::min(device_sm_count(), tiles2), kThreads, s2, st, mdc, msdc, mh, my, p2);
 }
 
 }  // namespace qmoe

@@ -659,14 +659,6 @@ __global__ void __launch_bounds__(kSThreads2, 1)
     }
 }
 
-int sm_count_small()
-{
-    static int n[16] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!n[dev & 15]) cudaDeviceGetAttribute(&n[dev & 15], cudaDevAttrMultiProcessorCount, dev);
-    return n[dev & 15] > 0 ? n[dev & 15] : 1;
-}
 
 size_t small_g1_smem(int H)
 {
@@ -756,7 +748,7 @@ cudaError_t launch_small_gateup(const PrefillArgs &a, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(small_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int tiles = a.max_w1 * ((I + 127) / 128);
-    small_gateup_kernel<<<std::max(1, std::min(sm_count_small(), tiles)), kSThreads1, smem, st>>>(mg, mu, msg, msu, p);
+    small_gateup_kernel<<<std::max(1, std::min(device_sm_count(), tiles)), kSThreads1, smem, st>>>(mg, mu, msg, msu, p);
     return cudaGetLastError();
 }
 
@@ -778,7 +770,7 @@ cudaError_t launch_small_down(const PrefillArgs &a, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(small_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int tiles = a.max_w2 * (H / 256);
-    small_down_kernel<<<std::max(1, std::min(sm_count_small(), tiles)), kSThreads2, smem, st>>>(md, msd, mh, p);
+    small_down_kernel<<<std::max(1, std::min(device_sm_count(), tiles)), kSThreads2, smem, st>>>(md, msd, mh, p);
     return cudaGetLastError();
 }
 

@@ -233,7 +233,9 @@ def compare_rows(wl, w, x, got, rows, bias=None, logits_in=None):
     assert np.array_equal(g["ids"][clear], ref["ids"][clear])
     same = np.nonzero(np.all(g["ids"] == ref["ids"], axis=1))[0]
     assert ulp_diff_bf16(g["p"][same], ref["p"][same]).max(initial=0) <= 1
-    return check_y(g["y"], ref["y"], rows=same), ref
+    stats = check_y(g["y"], ref["y"], rows=same)
+    print(f"y vs oracle {wl.name} T={x.shape[0]} rows={len(same)}: {stats}")
+    return stats, ref
 
 
 def compare_all_rows(wl, w, layer, x, got, bias=None, logits_in=None):

@@ -61,6 +61,7 @@ def test_decode_forward_matches_oracle(wl_index):
     ref = oracle.forward(wl.shape, w, x)
     same = _check_routing_against_oracle(layer, wl, x, got, ref)
     stats = H.check_y(got["y"], ref["y"], rows=np.nonzero(same)[0])
+    print(f"y vs oracle {wl.name} T={wl.tokens}: {stats}")
     if wl_index == 0:
         # the small layer's outputs are O(1): the plain 2e-2 max-abs bound applies too
         assert stats["max_abs"] <= 2e-2, stats
