@@ -110,6 +110,7 @@ struct FSmem {
     int colof[kDecodeMaxTok][kMaxTopK + 1]; // column of (t, j); j == k: the shared slot
     int ctok[kMaxCols];                     // token of each column
     int colf[kMaxCols];                     // slot index f of each column (t k + j, or T k + t)
+    int scanp[kThreads / 32], scanc[kThreads / 32];   // per-warp sums of the list scans
     int nlist;
     int abort;
     uint32_t epoch;                         // this launch's tag on the published logits
@@ -316,13 +317,13 @@ __device__ __forceinline__ void convert_row(FSmem &S, const FusedDecodeArgs &a, 
 // ------------------------------------------------------------------ routing (all threads)
 //
 // Top-k of every token from the fp32 logits (one warp per token: lane l holds the keys of
-// experts l + 32 r; each round takes the largest key, then the lowest id holding it), or the
-// caller's ids; each pick is registered at once in a bitmap of the picked experts and, per expert,
-// the set of tokens that picked it.  x' of every token is formed meanwhile by other warps (warp w
-// converts tokens 9 - w, 19 - w before it polls tokens w, w + 10: the conversion fills the time the
-// logits take to arrive).  Then warp 0 alone: the distinct experts in increasing id (the shared
-// expert last), each expert's column count, and the column of pick (t, j): the expert's first
-// column plus the number of earlier tokens that picked the same expert.
+// experts l + 32 r, sorted once; each round takes the largest key, then the lowest id holding it),
+// or the caller's ids; each pick is registered at once in a bitmap of the picked experts and, per
+// expert, the set of tokens that picked it.  x' of every token is formed meanwhile by other warps
+// (warp w converts tokens 9 - w, 19 - w before it polls tokens w, w + 10: the conversion fills the
+// time the logits take to arrive).  Then the whole CTA: the distinct experts in increasing id (the
+// shared expert last) and each expert's column count by block-wide scans, and the column of pick
+// (t, j): the expert's first column plus the number of earlier tokens that picked the same expert.
 // logits: the caller's fp32 logits, or null for the logits this launch publishes (tagged with its epoch).
 __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, const float *logits,
                                                const uint16_t *s_xr, uint16_t *s_x, float *s_xs)
@@ -393,28 +394,54 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
                 }
                 if (t == 0) stamp(a, kStLogitsSeen);
             }
+            // the lane's RW (key, id) pairs sorted once, largest first (the key, then the lower id:
+            // hi = 0xFFFF - e orders equal keys), by an 8-input sorting network; then each round takes
+            // the warp's largest head (the key by one reduction, the id among equal keys by another)
+            // and its lane pops it
+            static_assert(RW == 8, "the sorting network below is for eight keys per lane");
+            uint32_t hk[RW], hi[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                hk[r] = key[r];
+                hi[r] = 0xFFFFu - (uint32_t)(lane + 32 * r);
+            }
+            auto cx = [&](int a0, int b0) {           // (hk, hi)[a0] >= (hk, hi)[b0] afterwards
+                const bool sw = hk[b0] > hk[a0] || (hk[b0] == hk[a0] && hi[b0] > hi[a0]);
+                const uint32_t ka = hk[a0], ia = hi[a0];
+                hk[a0] = sw ? hk[b0] : ka;
+                hi[a0] = sw ? hi[b0] : ia;
+                hk[b0] = sw ? ka : hk[b0];
+                hi[b0] = sw ? ia : hi[b0];
+            };
+            cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+            cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+            cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+            cx(2, 4); cx(3, 5);
+            cx(1, 4); cx(3, 6);
+            cx(1, 2); cx(3, 4); cx(5, 6);
             int pick = 0;
+            float plg = 0.f;
 #pragma unroll 1
             for (int j = 0; j < k; ++j) {
-                uint32_t bk = key[0];
-                int br = 0;
+                const uint32_t mk = __reduce_max_sync(0xffffffffu, hk[0]);
+                const uint32_t mi = __reduce_max_sync(0xffffffffu, hk[0] == mk ? hi[0] : 0u);
+                if (hk[0] == mk && hi[0] == mi) {   // this lane's head is the pick: pop it
 #pragma unroll
-                for (int r = 1; r < RW; ++r)
-                    if (key[r] > bk) {
-                        bk = key[r];
-                        br = r;
+                    for (int r = 0; r < RW - 1; ++r) {
+                        hk[r] = hk[r + 1];
+                        hi[r] = hi[r + 1];
                     }
-                const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-                const uint32_t mine = (uint32_t)(lane + 32 * br);
-                const uint32_t id = __reduce_min_sync(0xffffffffu, bk == mk ? mine : 0xffffffffu);
-                if (id == mine) {
-#pragma unroll
-                    for (int r = 0; r < RW; ++r)
-                        if (r == br) key[r] = 0u;
-                    S.ids[t][j] = (int)id;
-                    S.lg[t][j] = key_logit(mk);
+                    hk[RW - 1] = 0u;
+                    hi[RW - 1] = 0u;
                 }
-                if (lane == j) pick = (int)id;
+                if (lane == j) {
+                    pick = 0xFFFF - (int)mi;
+                    plg = key_logit(mk);
+                }
+            }
+            if (lane < k) {
+                S.ids[t][lane] = pick;
+                S.lg[t][lane] = plg;
             }
             // every pick registered at once, lane j pick j: the bitmap of picked experts and each
             // expert's set of tokens (a repeated id is reported)
@@ -428,31 +455,43 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
     __syncthreads();                 // ids, the pick bitmap and token sets, and x' of every token complete
     stamp(a, kStXStaged);
     stamp(a, kStTopk);
-    if (warp == 0) {
-        // lane l scans the experts [32 l, 32 l + 32): list positions and first columns by two scans
-        const uint32_t bits = lane < (E + 31) / 32 ? S.pickmap[lane] : 0u;
-        int ncol = 0;
-        for (uint32_t b = bits; b; b &= b - 1) ncol += __popc(S.tokmask[32 * lane + __ffs(b) - 1]);
-        int np = __popc(bits), nc = ncol;
+    // the list of picked experts in increasing id (the shared expert last), each one's column count and
+    // first column: thread e < E, two block-wide exclusive scans (picked flags, column counts)
+    {
+        const int picked = tid < E ? (int)((S.pickmap[tid >> 5] >> (tid & 31)) & 1u) : 0;
+        const int c = picked ? __popc(S.tokmask[tid]) : 0;
+        int sp = picked, sc = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int vp = __shfl_up_sync(0xffffffffu, np, o), vc = __shfl_up_sync(0xffffffffu, nc, o);
+            const int vp = __shfl_up_sync(0xffffffffu, sp, o), vc = __shfl_up_sync(0xffffffffu, sc, o);
             if (lane >= o) {
-                np += vp;
-                nc += vc;
+                sp += vp;
+                sc += vc;
             }
         }
-        int pos = np - __popc(bits), col = nc - ncol;
-        for (uint32_t b = bits; b; b &= b - 1) {
-            const int e = 32 * lane + __ffs(b) - 1, c = __popc(S.tokmask[e]);
-            S.list[pos] = e;
-            S.lpos[e] = pos;
-            S.ncols[pos] = c;
-            S.colptr[pos] = col;
-            ++pos;
-            col += c;
-        }
         if (lane == 31) {
+            S.scanp[warp] = sp;
+            S.scanc[warp] = sc;
+        }
+        __syncthreads();
+        int bp = 0, bc = 0, np = 0, nc = 0;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {
+            if (w < warp) {
+                bp += S.scanp[w];
+                bc += S.scanc[w];
+            }
+            np += S.scanp[w];
+            nc += S.scanc[w];
+        }
+        if (picked) {
+            const int pos = bp + sp - 1;
+            S.list[pos] = tid;
+            S.lpos[tid] = pos;
+            S.ncols[pos] = c;
+            S.colptr[pos] = bc + sc - c;
+        }
+        if (tid == 0) {
             int D = np;
             if (a.has_shared) {
                 S.list[D] = E;
@@ -463,24 +502,25 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
             S.colptr[D] = nc + (a.has_shared ? T : 0);
             S.nlist = D;
         }
-        __syncwarp();                // the list, positions and first columns of every lane
+    }
+    __syncthreads();
+    // the column of every pick (t, j): the expert's first column plus the earlier tokens that picked it
 #pragma unroll 1
-        for (int i = lane; i < T * k; i += 32) {
-            const int t = i / k, j = i - t * k, e = S.ids[t][j];
-            const int col = S.colptr[S.lpos[e]] + __popc(S.tokmask[e] & ((1u << t) - 1u));
-            S.colof[t][j] = col;
-            S.colf[col] = i;
+    for (int i = tid; i < T * k; i += kThreads) {
+        const int t = i / k, j = i - t * k, e = S.ids[t][j];
+        const int col = S.colptr[S.lpos[e]] + __popc(S.tokmask[e] & ((1u << t) - 1u));
+        S.colof[t][j] = col;
+        S.colf[col] = i;
+        S.ctok[col] = t;
+    }
+    if (a.has_shared)
+#pragma unroll 1
+        for (int t = tid; t < T; t += kThreads) {
+            const int col = S.colptr[S.nlist - 1] + t;
+            S.colof[t][k] = col;
+            S.colf[col] = T * k + t;
             S.ctok[col] = t;
         }
-        if (a.has_shared)
-#pragma unroll 1
-            for (int t = lane; t < T; t += 32) {
-                const int col = S.colptr[S.nlist - 1] + t;
-                S.colof[t][k] = col;
-                S.colf[col] = T * k + t;
-                S.ctok[col] = t;
-            }
-    }
     __syncthreads();
     stamp(a, kStListed);
 }
