@@ -21,9 +21,9 @@
 //      the CTA that computes h for its slice also applies the down projection to it at
 //      once: no h crosses the grid.  A producer warp streams each unit's three chunks
 //      (gate, up, down codes with the gate/up scales and biases) into a ring of shared-
-//      memory slots with TMA; eight consumer warps compute them on mma.sync with exact
-//      integer codes (bf16 128 + q against x' for gate/up, signed fp16 q - 8 against h'
-//      for down), and write per slice the raw down sums P = sum (q - 8) h' and sum h'.
+//      memory slots with TMA; eight consumer warps compute them on mma.sync with the exact
+//      signed codes q - 8 in fp16 (against fp16 x' for gate/up, fp16 h' for down), and write
+//      per slice the raw down sums P = sum (q - 8) h' and sum h'.
 //   3. One grid-wide counter; then CTA c combines rows [c RB, c RB + RB) of y: per slot,
 //      y_e = 2^(2e) sum_g [ s_g (P_{2g} + P_{2g+1}) + (b_g + 8 s_g)(Hs_{2g} + Hs_{2g+1}) ],
 //      then y = bf16(sum_j p_j y_ej + w_s y_shared) in slot order, one rounding.  The down
@@ -81,11 +81,17 @@ enum {
     kStFirstDown, kStFirstDownDone, kStUnitsDone, kStUnitsCnt, kStCombineLoads, kStCombined
 };
 
+// Constants of the code conversion (nib8_signed), passed with the launch.
+struct DequantK {
+    uint32_t lo, hi, one024, sub, mul, add;   // 0x000F000F, 0x00F000F0, 1024, 1032, 1/16, -72 (f16x2)
+};
+
 struct FusedMaps {
     CUtensorMap g, u, sg, su;   // int4 codes of gate and up (routed stacks, shared expert): 3D, 32-row boxes
 };
 
 struct FusedGeom {
+    DequantK dq;        // code conversion constants (nib8_signed)
     int R;              // ring slots
     uint32_t slot;      // bytes per slot (multiple of 1024)
     uint32_t codes1;    // code bytes of a gate/up chunk: 32 rows x H / 2
@@ -140,23 +146,25 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
     return r;
 }
 
-// 8 nibbles -> four 16-bit pairs of (OFF + q) in the MMA operand type: elements (0,4), (1,5), (2,6), (3,7).
-template <bool F16>
-__device__ __forceinline__ void nib8(uint32_t u, uint32_t *r)
+// 8 nibbles of a code word -> four fp16 pairs of the signed codes q - 8 (exact): elements (0,4), (1,5),
+// (2,6), (3,7).  A nibble at bits 0-3 or 4-7 of a 16-bit half lies inside the fp16 mantissa once the
+// half is ORed with 1024 (0x6400): 1024 + q, or 1024 + 16 q, which one exact f16x2 add or fma maps to
+// q - 8.  So a word costs four masks and a single shift (for the nibbles at bits 8-15); the integer
+// pipe, not the tensor pipe, bounds these loops.  The six constants (DequantK) come in as launch
+// parameters: as literals the compiler rebuilds them in registers inside the loops, which costs the
+// integer pipe about a third more.
+__device__ __forceinline__ void nib8_signed(uint32_t u, uint32_t *r, const DequantK &k)
 {
-    constexpr uint32_t base = F16 ? 0x64006400u : 0x43004300u;   // fp16 1024, bf16 128
-    r[0] = (u & 0x000F000Fu) | base;
-    r[1] = ((u >> 4) & 0x000F000Fu) | base;
-    r[2] = ((u >> 8) & 0x000F000Fu) | base;
-    r[3] = ((u >> 12) & 0x000F000Fu) | base;
-}
-
-// The same pairs as signed fp16 codes q - 8 (exact): (1024 + q) - 1032.
-__device__ __forceinline__ void nib8_signed_f16(uint32_t u, uint32_t *r)
-{
-    nib8<true>(u, r);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) asm("sub.f16x2 %0, %0, %1;" : "+r"(r[i]) : "r"(0x64086408u));
+    const uint32_t v = u >> 8;
+    r[0] = (u & k.lo) | k.one024;
+    r[1] = (u & k.hi) | k.one024;
+    r[2] = (v & k.lo) | k.one024;
+    r[3] = (v & k.hi) | k.one024;
+    // (1024 + q) - 1032 and (1024 + 16 q) / 16 - 72
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r[0]) : "r"(k.sub));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(r[1]) : "r"(k.mul), "r"(k.add));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r[2]) : "r"(k.sub));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(r[3]) : "r"(k.mul), "r"(k.add));
 }
 
 // 8 consecutive 16-bit values -> the codes' k order (0,4,1,5,2,6,3,7).
@@ -172,14 +180,6 @@ __device__ __forceinline__ uint4 kperm8(uint4 v)
 
 // Position of element i in the k order of its chunk of 8.
 __device__ __forceinline__ int kperm_pos(int i) { return (i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1); }
-
-// Element i (natural order, 0..7) of a k-ordered chunk of 8 bf16 values (four words), as a float.
-__device__ __forceinline__ float kchunk_at(const uint32_t (&w)[4], int i)
-{
-    const int pos = kperm_pos(i);
-    const uint32_t word = w[pos >> 1];
-    return __uint_as_float((pos & 1) ? (word & 0xFFFF0000u) : (word << 16));
-}
 
 // Byte offset, inside a row of a 128-byte code box, of the 8 code bytes lane (g, t4) reads for
 // group q (0..3) of the box: 16-byte chunk 2q + t4/2 stored at chunk index (chunk ^ g).
@@ -268,9 +268,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, long l
 }
 
 // x' for the MMAs of token t from its raw staged row, by one warp: lane l takes the row's 16-byte
-// chunks l, l + 32, ..., the warp finds the row's largest |x|, scales by 2^-e (exact), puts each chunk
-// of 8 in the codes' k order and sums each group of 64 (its 8 chunks sit in 8 consecutive lanes: a
-// fixed shuffle tree).
+// chunks l, l + 32, ..., the warp finds the row's largest |x|, scales by 2^-e (exact), rounds to fp16
+// (max |x'| in [1, 2): exact for every element of at least 2^-17, and off by at most 2^-25 below),
+// puts each chunk of 8 in the codes' k order and sums each group of 64 of the fp16 values (its 8
+// chunks sit in 8 consecutive lanes: a fixed shuffle tree).
 __device__ __forceinline__ void convert_row(FSmem &S, const FusedDecodeArgs &a, const uint16_t *s_xr, uint16_t *s_x,
                                             float *s_xs, int t)
 {
@@ -300,9 +301,11 @@ __device__ __forceinline__ void convert_row(FSmem &S, const FusedDecodeArgs &a, 
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float lo = __uint_as_float(w[q] << 16) * sc, hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
-                w[q] = (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
-                sum += __uint_as_float(w[q] << 16);
-                sum += __uint_as_float(w[q] & 0xFFFF0000u);
+                const __half2 hv = __floats2half2_rn(lo, hi);
+                w[q] = *reinterpret_cast<const uint32_t *>(&hv);
+                const float2 hf = __half22float2(hv);
+                sum += hf.x;
+                sum += hf.y;
             }
             *reinterpret_cast<uint4 *>(s_x + (size_t)t * XS + (c >> 3) * kXG + (c & 7) * 8) =
                 kperm8(make_uint4(w[0], w[1], w[2], w[3]));
@@ -528,11 +531,11 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
 // ------------------------------------------------------------------ per-token weights (aux warp)
 //
 // Token t = grid - 1 - blockIdx: gamma = x . v in fp32 (lane l sums the groups l, l + 32, ...
-// element by element in natural order, then a fixed shuffle tree: the router kernel's operations;
-// on x' = x 2^-e every product and partial sum is the unscaled one times 2^-e, exactly), w_s =
+// element by element in natural order, then a fixed shuffle tree: the router kernel's operations on
+// the raw row, read from global memory since the staged one is gone by now), w_s =
 // bf16(sigmoid(bf16(gamma))) and p_j = bf16(exp(l_j - l_0) / sum_i exp(l_i - l_0)) in fp64,
 // published for the combining CTAs.
-__device__ __forceinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a, const uint16_t *s_x)
+__device__ __forceinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a)
 {
     const int lane = threadIdx.x & 31, T = a.T, k = a.k, G = a.H / kGroup;
     const int t = (int)gridDim.x - 1 - (int)blockIdx.x;
@@ -552,7 +555,7 @@ __device__ __forceinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a
     if (a.has_shared) {
 #pragma unroll 1
         for (int grp = lane; grp < G; grp += 32) {
-            const uint4 *xr = reinterpret_cast<const uint4 *>(s_x + (size_t)t * (G * kXG + 8) + grp * kXG);
+            const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + grp * kGroup);
             const uint4 *vp = reinterpret_cast<const uint4 *>(a.v + grp * kGroup);
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
@@ -560,8 +563,9 @@ __device__ __forceinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a
                 const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
+                    const float xf = __uint_as_float((i & 1) ? (xw[i >> 1] & 0xFFFF0000u) : (xw[i >> 1] << 16));
                     const float vf = __uint_as_float((i & 1) ? (vw[i >> 1] & 0xFFFF0000u) : (vw[i >> 1] << 16));
-                    part = fmaf(kchunk_at(xw, i), vf, part);
+                    part = fmaf(xf, vf, part);
                 }
             }
         }
@@ -571,8 +575,7 @@ __device__ __forceinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a
     if (lane == 0) {
         uint16_t wsb = 0;
         if (a.has_shared) {
-            const float gamma = part * pow2f(S.xe[t]);
-            const float gb = bf16_bits_to_float(float_to_bf16_bits(gamma));
+            const float gb = bf16_bits_to_float(float_to_bf16_bits(part));
             wsb = double_to_bf16_bits(1.0 / (1.0 + exp(-(double)gb)));
         }
         a.ws_glob[t] = wsb;
@@ -686,10 +689,10 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
 // ------------------------------------------------------------------ consumers (warps 0-7)
 //
 // Gate and up chunks: warp w takes the 16-row tile mt = w % 2 and quarter kq = w / 2 of the groups of
-// both matrices, with every group's product s (sum (128 + q) x') + (b - 128 s) sum x' added in
+// both matrices, with every group's product s (sum (q - 8) x') + (b + 8 s) sum x' added in
 // increasing group order; the four quarters are added in order in h = silu(g) u.  Down chunk:
 // warp w takes H / 128 tiles of 16 rows, K = 32 (the slice), raw sums P = sum (q - 8) h'.  The
-// down codes enter the MMA signed: with 1024 + q the sum would be ~1024 sum h' and cancel about
+// codes enter the MMAs signed: with 1024 + q a sum would carry ~1024 sum x' (or h') and cancel about
 // eight bits against the bias term, beyond what the tensor cores' fp32 accumulation keeps.
 // Element e (0..7, a compile-time index after unrolling) of eight bf16 packed in a uint4, as fp32.
 __device__ __forceinline__ float bf16_of8(uint4 v, int e)
@@ -708,6 +711,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
     const int T = a.T, H = a.H, I = a.I, G = H / kGroup, SL = I / kSlice, R = geo.R;
     const int mt = warp & 1, kq = warp >> 1, gq = G / 4, XS = G * kXG + 8;
     const long long limit = kRingLimit;
+    const DequantK dq = geo.dq;
     float *const part = a.part;
     float *const hsum = a.hsum;
     bool fail_d = false;
@@ -715,13 +719,18 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
     for (int u = blockIdx.x, i = 0; u < U; u += gridDim.x, ++i) {
         const int d = u / SL, s = u - d * SL;
         const int ncol = min(S.ncols[d], T), colbase = S.colptr[d];
-        int xrow[NT], tA[NT], tB[NT];
+        // the x' row and the group-sum rows of the lane's B column (c) and D columns (cA, cA + 1); a lane
+        // whose column is past the expert's reads the first column's token instead (those MMA columns and
+        // sums are never read), so every lane runs the same loads
+        const int tok0 = S.ctok[colbase];
+        const uint16_t *xq[NT];
+        const float *xa[NT], *xb[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int c = j * 8 + g, cA = j * 8 + 2 * t4;
-            xrow[j] = c < ncol ? S.ctok[colbase + c] : -1;
-            tA[j] = cA < ncol ? S.ctok[colbase + cA] : -1;
-            tB[j] = cA + 1 < ncol ? S.ctok[colbase + cA + 1] : -1;
+            xq[j] = s_x + (size_t)(c < ncol ? S.ctok[colbase + c] : tok0) * XS + 16 * t4;
+            xa[j] = s_xs + (cA < ncol ? S.ctok[colbase + cA] : tok0) * G;
+            xb[j] = s_xs + (cA + 1 < ncol ? S.ctok[colbase + cA + 1] : tok0) * G;
         }
         // the gate and up chunks in one pass, by all eight warps: warp w takes the 16-row tile mt = w % 2
         // and the groups of quarter kq = w / 2 of the input dimension of both matrices, so each x
@@ -741,42 +750,35 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             for (int j = 0; j < NT; ++j)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) accg[j][v] = accu[j][v] = 0.f;
-            // one group: codes of rows g, g + 8 of both matrices, the group's scales s and offsets b - 128 s
-            auto group_step = [&](int grp, float sg0, float sg1, float kg0, float kg1, float su0, float su1, float ku0,
-                                  float ku1) {
-                const int q = grp & 3;
-                const uint32_t o = (uint32_t)(grp >> 2) * (kSlice * 128) + swz_chunk(q, g, t4);
-                const uint2 g0 = *reinterpret_cast<const uint2 *>(cbg + o), g1 = *reinterpret_cast<const uint2 *>(cbg + o + 1024);
-                const uint2 u0 = *reinterpret_cast<const uint2 *>(cbu + o), u1 = *reinterpret_cast<const uint2 *>(cbu + o + 1024);
+            // one group: the code words of rows g, g + 8 of both matrices, the x' fragment at element xo of
+            // the lane's row, the group sums at index so, the group's scales s and offsets b + 8 s
+            // (sum (s q + b) x' = s sum (q - 8) x' + (b + 8 s) sum x')
+            auto group_step = [&](uint2 cg0, uint2 cg1, uint2 cu0, uint2 cu1, int xo, int so, float sg0, float sg1,
+                                  float kg0, float kg1, float su0, float su1, float ku0, float ku1) {
                 uint32_t ag0[8], ag1[8], au0[8], au1[8];
-                nib8<false>(g0.x, ag0);
-                nib8<false>(g0.y, ag0 + 4);
-                nib8<false>(g1.x, ag1);
-                nib8<false>(g1.y, ag1 + 4);
-                nib8<false>(u0.x, au0);
-                nib8<false>(u0.y, au0 + 4);
-                nib8<false>(u1.x, au1);
-                nib8<false>(u1.y, au1 + 4);
+                nib8_signed(cg0.x, ag0, dq);
+                nib8_signed(cg0.y, ag0 + 4, dq);
+                nib8_signed(cg1.x, ag1, dq);
+                nib8_signed(cg1.y, ag1 + 4, dq);
+                nib8_signed(cu0.x, au0, dq);
+                nib8_signed(cu0.y, au0 + 4, dq);
+                nib8_signed(cu1.x, au1, dq);
+                nib8_signed(cu1.y, au1 + 4, dq);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    if (j * 8 >= ncol) break;
-                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                    if (xrow[j] >= 0) {
-                        const uint4 *xr = reinterpret_cast<const uint4 *>(s_x + (size_t)xrow[j] * XS + grp * kXG) + 2 * t4;
-                        lo = xr[0];
-                        hi = xr[1];
-                    }
+                    if (j > 0 && j * 8 >= ncol) break;        // every expert has a first column
+                    const uint4 *xr = reinterpret_cast<const uint4 *>(xq[j] + xo);
+                    const uint4 lo = xr[0], hi = xr[1];
                     const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                     float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int mm = 0; mm < 4; ++mm) {
-                        mma16816<false>(dg, ag0[2 * mm], ag1[2 * mm], ag0[2 * mm + 1], ag1[2 * mm + 1], bp[2 * mm],
-                                        bp[2 * mm + 1]);
-                        mma16816<false>(du, au0[2 * mm], au1[2 * mm], au0[2 * mm + 1], au1[2 * mm + 1], bp[2 * mm],
-                                        bp[2 * mm + 1]);
+                        mma16816<true>(dg, ag0[2 * mm], ag1[2 * mm], ag0[2 * mm + 1], ag1[2 * mm + 1], bp[2 * mm],
+                                       bp[2 * mm + 1]);
+                        mma16816<true>(du, au0[2 * mm], au1[2 * mm], au0[2 * mm + 1], au1[2 * mm + 1], bp[2 * mm],
+                                       bp[2 * mm + 1]);
                     }
-                    const float xA = tA[j] >= 0 ? s_xs[tA[j] * G + grp] : 0.f;
-                    const float xB = tB[j] >= 0 ? s_xs[tB[j] * G + grp] : 0.f;
+                    const float xA = xa[j][so], xB = xb[j][so];
                     accg[j][0] = fmaf(sg0, dg[0], fmaf(kg0, xA, accg[j][0]));
                     accg[j][1] = fmaf(sg0, dg[1], fmaf(kg0, xB, accg[j][1]));
                     accg[j][2] = fmaf(sg1, dg[2], fmaf(kg1, xA, accg[j][2]));
@@ -788,11 +790,17 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                 }
             };
             if ((gq & 7) == 0) {
-                // scales and biases of eight groups per 16-byte load: rows g and g + 8 sit 64 bytes apart
-                // per 32 groups, so each 2-byte load would meet three other rows in its bank
+                // blocks of eight groups (g0 a multiple of 8): the lane's four code offsets inside a box row
+                // (group position q = 0..3) are fixed, so every load of the block is a base plus a constant.
+                // Scales and biases of the eight groups per 16-byte load: rows g and g + 8 sit 64 bytes
+                // apart per 32 groups, so each 2-byte load would meet three other rows in its bank.
+                uint32_t swz[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) swz[q] = swz_chunk(q, g, t4);
 #pragma unroll 1
                 for (int gb = 0; gb < gq; gb += 8) {
                     const int g0 = kq * gq + gb;
+                    const uint8_t *bg = cbg + (g0 >> 2) * (kSlice * 128), *bu = cbu + (g0 >> 2) * (kSlice * 128);
                     const uint4 vsg0 = *reinterpret_cast<const uint4 *>(scg + g0);
                     const uint4 vsg1 = *reinterpret_cast<const uint4 *>(scg + 8 * G + g0);
                     const uint4 vbg0 = *reinterpret_cast<const uint4 *>(big + g0);
@@ -803,22 +811,29 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                     const uint4 vbu1 = *reinterpret_cast<const uint4 *>(biu + 8 * G + g0);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
+                        const uint32_t o = (uint32_t)(e >> 2) * (kSlice * 128) + swz[e & 3];
+                        const uint2 cg0 = *reinterpret_cast<const uint2 *>(bg + o), cg1 = *reinterpret_cast<const uint2 *>(bg + o + 1024);
+                        const uint2 cu0 = *reinterpret_cast<const uint2 *>(bu + o), cu1 = *reinterpret_cast<const uint2 *>(bu + o + 1024);
                         const float sg0 = bf16_of8(vsg0, e), sg1 = bf16_of8(vsg1, e);
                         const float su0 = bf16_of8(vsu0, e), su1 = bf16_of8(vsu1, e);
-                        group_step(g0 + e, sg0, sg1, fmaf(-128.f, sg0, bf16_of8(vbg0, e)), fmaf(-128.f, sg1, bf16_of8(vbg1, e)),
-                                   su0, su1, fmaf(-128.f, su0, bf16_of8(vbu0, e)), fmaf(-128.f, su1, bf16_of8(vbu1, e)));
+                        group_step(cg0, cg1, cu0, cu1, (g0 + e) * kXG, g0 + e, sg0, sg1, fmaf(8.f, sg0, bf16_of8(vbg0, e)),
+                                   fmaf(8.f, sg1, bf16_of8(vbg1, e)), su0, su1, fmaf(8.f, su0, bf16_of8(vbu0, e)),
+                                   fmaf(8.f, su1, bf16_of8(vbu1, e)));
                     }
                 }
             } else {
 #pragma unroll 2
                 for (int gi = 0; gi < gq; ++gi) {
                     const int grp = kq * gq + gi;
+                    const uint32_t o = (uint32_t)(grp >> 2) * (kSlice * 128) + swz_chunk(grp & 3, g, t4);
+                    const uint2 cg0 = *reinterpret_cast<const uint2 *>(cbg + o), cg1 = *reinterpret_cast<const uint2 *>(cbg + o + 1024);
+                    const uint2 cu0 = *reinterpret_cast<const uint2 *>(cbu + o), cu1 = *reinterpret_cast<const uint2 *>(cbu + o + 1024);
                     const float sg0 = bf16_bits_to_float(scg[grp]), sg1 = bf16_bits_to_float(scg[8 * G + grp]);
                     const float su0 = bf16_bits_to_float(scu[grp]), su1 = bf16_bits_to_float(scu[8 * G + grp]);
-                    group_step(grp, sg0, sg1, fmaf(-128.f, sg0, bf16_bits_to_float(big[grp])),
-                               fmaf(-128.f, sg1, bf16_bits_to_float(big[8 * G + grp])), su0, su1,
-                               fmaf(-128.f, su0, bf16_bits_to_float(biu[grp])),
-                               fmaf(-128.f, su1, bf16_bits_to_float(biu[8 * G + grp])));
+                    group_step(cg0, cg1, cu0, cu1, grp * kXG, grp, sg0, sg1, fmaf(8.f, sg0, bf16_bits_to_float(big[grp])),
+                               fmaf(8.f, sg1, bf16_bits_to_float(big[8 * G + grp])), su0, su1,
+                               fmaf(8.f, su0, bf16_bits_to_float(biu[grp])),
+                               fmaf(8.f, su1, bf16_bits_to_float(biu[8 * G + grp])));
                 }
             }
             // column-major [NC][32 rows]: the h step below reads one column's 32 rows, one per lane
@@ -904,8 +919,8 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                 const uint32_t w0 = *reinterpret_cast<const uint32_t *>(dch + r0 * 16 + 4 * t4);
                 const uint32_t w1 = *reinterpret_cast<const uint32_t *>(dch + (r0 + 8) * 16 + 4 * t4);
                 uint32_t a0[4], a1[4];
-                nib8_signed_f16(w0, a0);
-                nib8_signed_f16(w1, a1);
+                nib8_signed(w0, a0, dq);
+                nib8_signed(w1, a1, dq);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
                     if (j * 8 >= ncol) break;
@@ -1245,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fused_producer(S, maps, a, geo, ring, U);
         } else if (warp == kWarpAux) {
             prefetch_combine_scales(S, a, geo);
-            token_weights(S, a, s_x);
+            token_weights(S, a);
         } else {
             fused_consumers<NT>(S, a, geo, ring, s_x, s_xs, s_red, s_h, s_hs, U);
         }
@@ -1320,6 +1335,7 @@ bool fused_geometry(int T, int H, int I, int k, int has_shared, int grid, int op
 {
     if (T < 1 || T > kDecodeMaxTok || H % 256 || H > 2048 || I % 64 || I > 4096 || grid < 1) return false;
     FusedGeom g{};
+    g.dq = DequantK{0x000F000Fu, 0x00F000F0u, 0x64006400u, 0x64086408u, 0x2C002C00u, 0xD480D480u};
     const int G = H / kGroup, NT = T > 8 ? 2 : 1, NC = 8 * NT;
     g.codes1 = (uint32_t)kSlice * H / 2;
     g.sc1 = (uint32_t)kSlice * G * 2;
