@@ -81,11 +81,6 @@ enum {
     kStFirstDown, kStFirstDownDone, kStUnitsDone, kStUnitsCnt, kStCombineLoads, kStCombined
 };
 
-// Constants of the code conversion (nib8_signed), passed with the launch.
-struct DequantK {
-    uint32_t lo, hi, one024, sub, mul, add;   // 0x000F000F, 0x00F000F0, 1024, 1032, 1/16, -72 (f16x2)
-};
-
 struct FusedMaps {
     CUtensorMap g, u, sg, su;   // int4 codes of gate and up (routed stacks, shared expert): 3D, 32-row boxes
 };
@@ -144,27 +139,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
-}
-
-// 8 nibbles of a code word -> four fp16 pairs of the signed codes q - 8 (exact): elements (0,4), (1,5),
-// (2,6), (3,7).  A nibble at bits 0-3 or 4-7 of a 16-bit half lies inside the fp16 mantissa once the
-// half is ORed with 1024 (0x6400): 1024 + q, or 1024 + 16 q, which one exact f16x2 add or fma maps to
-// q - 8.  So a word costs four masks and a single shift (for the nibbles at bits 8-15); the integer
-// pipe, not the tensor pipe, bounds these loops.  The six constants (DequantK) come in as launch
-// parameters: as literals the compiler rebuilds them in registers inside the loops, which costs the
-// integer pipe about a third more.
-__device__ __forceinline__ void nib8_signed(uint32_t u, uint32_t *r, const DequantK &k)
-{
-    const uint32_t v = u >> 8;
-    r[0] = (u & k.lo) | k.one024;
-    r[1] = (u & k.hi) | k.one024;
-    r[2] = (v & k.lo) | k.one024;
-    r[3] = (v & k.hi) | k.one024;
-    // (1024 + q) - 1032 and (1024 + 16 q) / 16 - 72
-    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r[0]) : "r"(k.sub));
-    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(r[1]) : "r"(k.mul), "r"(k.add));
-    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r[2]) : "r"(k.sub));
-    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(r[3]) : "r"(k.mul), "r"(k.add));
 }
 
 // 8 consecutive 16-bit values -> the codes' k order (0,4,1,5,2,6,3,7).
@@ -1335,7 +1309,7 @@ bool fused_geometry(int T, int H, int I, int k, int has_shared, int grid, int op
 {
     if (T < 1 || T > kDecodeMaxTok || H % 256 || H > 2048 || I % 64 || I > 4096 || grid < 1) return false;
     FusedGeom g{};
-    g.dq = DequantK{0x000F000Fu, 0x00F000F0u, 0x64006400u, 0x64086408u, 0x2C002C00u, 0xD480D480u};
+    g.dq = kDequantK;
     const int G = H / kGroup, NT = T > 8 ? 2 : 1, NC = 8 * NT;
     g.codes1 = (uint32_t)kSlice * H / 2;
     g.sc1 = (uint32_t)kSlice * G * 2;

@@ -39,6 +39,32 @@ constexpr int kTraceStamps = 14;    // %globaltimer stamps per CTA of the fused 
 constexpr int kTraceMaxCtas = 256;
 constexpr int kDecodeSlice = 32;    // rows of the intermediate dimension per fused decode unit
 
+// 4-bit codes for mma.sync: the 8 nibbles of a code word -> four fp16 pairs of the signed codes q - 8
+// (exact), elements (0,4), (1,5), (2,6), (3,7) of the word.  A nibble at bits 0-3 or 4-7 of a 16-bit
+// half lies inside the fp16 mantissa once the half is ORed with 1024 (0x6400): 1024 + q, or
+// 1024 + 16 q, which one exact f16x2 add or fma maps to q - 8.  So a word costs four masks and a
+// single shift (for the nibbles at bits 8-15); in the weight-streaming GEMMs the integer pipe, not the
+// tensor pipe, is the bound.  The six constants (DequantK) reach the kernels as launch parameters: as
+// literals the compiler rebuilds them in registers inside the loops, which costs the integer pipe
+// about a third more.
+struct DequantK {
+    uint32_t lo, hi, one024, sub, mul, add;   // 0x000F000F, 0x00F000F0, 1024, 1032, 1/16, -72 (f16x2)
+};
+constexpr DequantK kDequantK{0x000F000Fu, 0x00F000F0u, 0x64006400u, 0x64086408u, 0x2C002C00u, 0xD480D480u};
+__device__ __forceinline__ void nib8_signed(uint32_t u, uint32_t *r, const DequantK &k)
+{
+    const uint32_t v = u >> 8;
+    r[0] = (u & k.lo) | k.one024;
+    r[1] = (u & k.hi) | k.one024;
+    r[2] = (v & k.lo) | k.one024;
+    r[3] = (v & k.hi) | k.one024;
+    // (1024 + q) - 1032 and (1024 + 16 q) / 16 - 72
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r[0]) : "r"(k.sub));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(r[1]) : "r"(k.mul), "r"(k.add));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r[2]) : "r"(k.sub));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(r[3]) : "r"(k.mul), "r"(k.add));
+}
+
 // One unit of work of a grouped kernel: an expert (E = shared) and a token range
 // [tok0, tok0 + ntok) of its permuted slot list.
 struct WorkItem {

@@ -9,9 +9,9 @@
 // tcgen05 MMA with M = 128, K = 16 costs ~46 cycles for any N <= 64 on this GPU, and the
 // dequantisation of every weight to fp16 comes on top; so these tiles use the decode
 // GEMV's arithmetic on mma.sync instead, with the codes used exactly:
-//     sum_j w_j x_j = s * sum_j (1024 + q_j) x_j + (b - 1024 s) * sum_j x_j
-// over each group of 64 inputs, 1024 + q exact in fp16, fp32 accumulation, scale and
-// bias per group in fp32.  The tensor-memory kernels keep the experts with many tokens.
+//     sum_j w_j x_j = s * sum_j (q_j - 8) x_j + (b + 8 s) * sum_j x_j
+// over each group of 64 inputs, q - 8 exact in fp16 (nib8_signed), fp32 accumulation, scale
+// and bias per group in fp32.  The tensor-memory kernels keep the experts with many tokens.
 //
 // Gate/up kernel (one CTA per SM, persistent over tiles = item x 128-row block of I):
 //   warp 16 (one thread) streams each K-step's gate and up code boxes (128 rows x 32
@@ -84,6 +84,7 @@ struct SmallParams {
     int *status;
     int T, H, I, E, k;
     long long wait_limit;
+    DequantK dq;                       // code conversion constants (kDequantK)
 };
 
 __device__ __forceinline__ uint32_t swz128(int row, int chunk)
@@ -97,16 +98,6 @@ __device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 8 nibbles -> four fp16 pairs of 1024 + q, elements (0,4), (1,5), (2,6), (3,7): the codes'
-// k order, which x16 and h share.
-__device__ __forceinline__ void nib8(uint32_t u, uint32_t *r)
-{
-    r[0] = (u & 0x000F000Fu) | 0x64006400u;
-    r[1] = ((u >> 4) & 0x000F000Fu) | 0x64006400u;
-    r[2] = ((u >> 8) & 0x000F000Fu) | 0x64006400u;
-    r[3] = ((u >> 12) & 0x000F000Fu) | 0x64006400u;
 }
 
 __device__ __forceinline__ int kperm_pos(int i) { return (i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1); }
@@ -205,6 +196,7 @@ __global__ void __launch_bounds__(kSThreads1, 1)
     }
     __syncthreads();
     const long long limit = P.wait_limit;
+    const DequantK dq = P.dq;
 
     if (warp == kSCompute) {
         // ------------------------------------------------ producer: lane 0 the code boxes (TMA) and scale
@@ -327,13 +319,13 @@ __global__ void __launch_bounds__(kSThreads1, 1)
                 const uint2 c0 = *reinterpret_cast<const uint2 *>(stg + crow0 + co);
                 const uint2 c1 = *reinterpret_cast<const uint2 *>(stg + crow1 + co);
                 const float s0 = scale_pick(ws0, e), s1 = scale_pick(ws1, e);
-                const float k0 = fmaf(-1024.f, s0, scale_pick(wb0, e));
-                const float k1 = fmaf(-1024.f, s1, scale_pick(wb1, e));
+                const float k0 = fmaf(8.f, s0, scale_pick(wb0, e));
+                const float k1 = fmaf(8.f, s1, scale_pick(wb1, e));
                 uint32_t aa[2][8];
-                nib8(c0.x, aa[0]);
-                nib8(c0.y, aa[0] + 4);
-                nib8(c1.x, aa[1]);
-                nib8(c1.y, aa[1] + 4);
+                nib8_signed(c0.x, aa[0], dq);
+                nib8_signed(c0.y, aa[0] + 4, dq);
+                nib8_signed(c1.x, aa[1], dq);
+                nib8_signed(c1.y, aa[1] + 4, dq);
                 const uint8_t *xb = stg + 32768 + g * kG1XRow + e * 128 + t4 * 32;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -462,6 +454,7 @@ __global__ void __launch_bounds__(kSThreads2, 1)
     }
     __syncthreads();
     const long long limit = P.wait_limit;
+    const DequantK dq = P.dq;
 
     if (warp == kSWarpTma) {
         // ------------------------------------------------ h boxes, code boxes, scale rows (one thread)
@@ -591,13 +584,13 @@ __global__ void __launch_bounds__(kSThreads2, 1)
                 wb1 = scale_window(ssc + 256 * GI, r0 + 8, GI, s);
             }
             const float s0 = scale_pick(ws0, e & 3), s1 = scale_pick(ws1, e & 3);
-            const float k0 = fmaf(-1024.f, s0, scale_pick(wb0, e & 3));
-            const float k1 = fmaf(-1024.f, s1, scale_pick(wb1, e & 3));
+            const float k0 = fmaf(8.f, s0, scale_pick(wb0, e & 3));
+            const float k1 = fmaf(8.f, s1, scale_pick(wb1, e & 3));
             uint32_t ad[2][8];
-            nib8(c0.x, ad[0]);
-            nib8(c0.y, ad[0] + 4);
-            nib8(c1.x, ad[1]);
-            nib8(c1.y, ad[1] + 4);
+            nib8_signed(c0.x, ad[0], dq);
+            nib8_signed(c0.y, ad[0] + 4, dq);
+            nib8_signed(c1.x, ad[1], dq);
+            nib8_signed(c1.y, ad[1] + 4, dq);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (j * 8 >= ncol) break;
@@ -676,6 +669,7 @@ size_t small_g2_smem(int I)
 SmallParams small_params(const PrefillArgs &a, bool down)
 {
     SmallParams p{};
+    p.dq = kDequantK;
     p.nwork = a.nwork;
     p.work = down ? a.work_g2 : a.work_g1;
     p.offsets = a.offsets;
