@@ -886,9 +886,10 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             }
             const int MT = H / (16 * kCW);
             float *pbase = part + (size_t)colbase * SL * H + (size_t)s * H;
-            // independent 16-row tiles: four per iteration give the warp four chains to overlap
-#pragma unroll 4
-            for (int tt = 0; tt < MT; ++tt) {
+            // one 16-row tile: independent of the others, and straight-line code (no branch: every
+            // expert has a first column), so the scheduler overlaps the tiles' loads, conversions and
+            // MMA chains
+            auto tile = [&](int tt) {
                 const int r0 = (warp * MT + tt) * 16 + g;
                 const uint32_t w0 = *reinterpret_cast<const uint32_t *>(dch + r0 * 16 + 4 * t4);
                 const uint32_t w1 = *reinterpret_cast<const uint32_t *>(dch + (r0 + 8) * 16 + 4 * t4);
@@ -897,7 +898,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                 nib8_signed(w1, a1, dq);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    if (j * 8 >= ncol) break;
+                    if (j > 0 && j * 8 >= ncol) break;
                     float dd[4] = {0.f, 0.f, 0.f, 0.f};
                     mma16816<true>(dd, a0[0], a1[0], a0[1], a1[1], hb[j][0], hb[j][1]);
                     mma16816<true>(dd, a0[2], a1[2], a0[3], a1[3], hb[j][2], hb[j][3]);
@@ -913,6 +914,13 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                         pc[r0 + 8] = dd[3];
                     }
                 }
+            };
+            if (MT == 16) {            // H = 2048: all sixteen tiles unrolled
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) tile(tt);
+            } else {
+#pragma unroll 4
+                for (int tt = 0; tt < MT; ++tt) tile(tt);
             }
         }
         __syncwarp();
