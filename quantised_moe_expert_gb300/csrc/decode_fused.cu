@@ -1105,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t dyn_raw[];
     uint8_t *dyn = align_smem_1024(dyn_raw);
     uint8_t *ring = dyn;
-    uint16_t *s_x = reinterpret_cast<uint16_t *>(dyn + geo.x_off);    // [T][G * 72 + 8] bf16 x', k order
+    uint16_t *s_x = reinterpret_cast<uint16_t *>(dyn + geo.x_off);    // [T][G * 72 + 8] fp16 x', k order
     float *s_xs = reinterpret_cast<float *>(dyn + geo.xs_off);         // [T][G] group sums of x'
     float *s_red = reinterpret_cast<float *>(dyn + geo.red_off);       // [2][4][NC][32]
     uint16_t *s_h = reinterpret_cast<uint16_t *>(dyn + geo.h_off);     // [NC][32] fp16 h', k order
