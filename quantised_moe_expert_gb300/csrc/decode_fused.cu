@@ -302,8 +302,9 @@ __device__ __forceinline__ void convert_row(FSmem &S, const FusedDecodeArgs &a, 
 // shared expert last) and each expert's column count by block-wide scans, and the column of pick
 // (t, j): the expert's first column plus the number of earlier tokens that picked the same expert.
 // logits: the caller's fp32 logits, or null for the logits this launch publishes (tagged with its epoch).
+template <class AfterTopk>
 __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, const float *logits,
-                                               const uint16_t *s_xr, uint16_t *s_x, float *s_xs)
+                                               const uint16_t *s_xr, uint16_t *s_x, float *s_xs, AfterTopk after_topk)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, E = a.E, k = a.k;
@@ -429,9 +430,13 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
         }
     }
     if (a.ids_in || logits) stamp(a, kStLogitsSeen);
+    // the raw rows in the ring area are read for the last time above: ordered before the copies that
+    // after_topk may issue into it
+    fence_proxy_async_smem();
     __syncthreads();                 // ids, the pick bitmap and token sets, and x' of every token complete
     stamp(a, kStXStaged);
     stamp(a, kStTopk);
+    after_topk();
     // the list of picked experts in increasing id (the shared expert last), each one's column count and
     // first column: thread e < E, two block-wide exclusive scans (picked flags, column counts)
     {
@@ -564,35 +569,118 @@ __device__ __forceinline__ void token_weights(FSmem &S, const FusedDecodeArgs &a
 // lanes arrive.  Down chunk: the slice's 16-byte column of all H rows.  From the packed layout it
 // is one contiguous block (one bulk copy); from the MLX layout it is 16 bytes of every 256-byte
 // row, which the 32 lanes take in turn with 16-byte cp.async, each arriving (without a count
-// increment) once its own copies have landed.
+// increment) once its own copies have landed.  The first unit's chunks go out right after top-k,
+// before the expert list is built (issue_first_unit); the loop issues the rest.
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, const FusedDecodeArgs &a,
-                                            const FusedGeom &geo, uint8_t *ring, int U)
+// Chunk c (0 gate, 1 up, 2 down) of unit (expert e, slice s) into ring slot `slot`, by the producer
+// warp; the slot is free.  The issuing lane (0) sets the expected bytes and issues the copies; the other
+// lanes arrive (the MLX down layout: each lane's 16-byte cp.async pieces, arriving once they land).
+__device__ __forceinline__ void issue_chunk(const FusedMaps &maps, const FusedDecodeArgs &a, const FusedGeom &geo,
+                                            uint8_t *ring, uint64_t *full, int slot, int e, int s, int c, uint64_t pol)
 {
     const int lane = threadIdx.x & 31;
-    // every argument read once into registers (each copy instruction is a compiler memory barrier)
-    const int H = a.H, I = a.I, E = a.E, G = H / kGroup, SL = I / kSlice, R = geo.R;
-    const uint32_t slot_bytes = geo.slot, codes1 = geo.codes1, sc1 = geo.sc1;
-    const size_t drow = (size_t)I / 2;
+    const int H = a.H, I = a.I, E = a.E, G = H / kGroup, SL = I / kSlice;
+    const bool shr = e == E;
+    uint8_t *base = ring + (size_t)slot * geo.slot;
+    const uint32_t fb = smem_u32(&full[slot]);
+    const int row0 = (shr ? 0 : e * I) + s * kSlice;
+    if (c < 2) {
+        // gate or up chunk: one 3D copy of the 32 code rows (each 128-byte box in the 128-byte swizzle) and
+        // two bulk copies of their scales and biases
+        if (lane == 0) {
+            const size_t so = (size_t)row0 * G;
+            const QMatDev &m = c == 0 ? (shr ? a.s_gate : a.gate) : (shr ? a.s_up : a.up);
+            mbar_arrive_expect_tx(fb, geo.codes1 + 2 * geo.sc1);
+            tma_load_3d_hint(smem_u32(base), c == 0 ? (shr ? &maps.sg : &maps.g) : (shr ? &maps.su : &maps.u), 0, row0, 0,
+                             fb, pol);
+            bulk_load_hint(smem_u32(base + geo.codes1), m.scales + so, geo.sc1, fb, pol);
+            bulk_load_hint(smem_u32(base + geo.codes1 + geo.sc1), m.biases + so, geo.sc1, fb, pol);
+        } else {
+            mbar_arrive(fb);
+        }
+    } else if (a.down_packed != nullptr && (!shr || a.s_down_packed != nullptr)) {
+        // the slice's down codes are one contiguous block of the packed layout: one bulk copy
+        if (lane == 0) {
+            const uint8_t *src = shr ? a.s_down_packed + (size_t)s * H * 16 : a.down_packed + ((size_t)e * SL + s) * H * 16;
+            mbar_arrive_expect_tx(fb, (uint32_t)H * 16);
+            bulk_load_hint(smem_u32(base), src, (uint32_t)H * 16, fb, pol);
+        } else {
+            mbar_arrive(fb);
+        }
+    } else {
+        const uint8_t *src = (shr ? a.s_down.codes : a.down.codes) + (size_t)(shr ? 0 : e) * H * ((size_t)I / 2) + s * 16;
+        const uint32_t dst = smem_u32(base);
+#pragma unroll 4
+        for (int r = lane; r < H; r += 32) cp_async16(dst + r * 16, src + (size_t)r * (I / 2));
+        cp_async_mbar_arrive_noinc(fb);
+    }
+}
+
+// Issued right after top-k, by the producer warp, before the expert list is built: the three chunks of this
+// CTA's first unit.  The list holds the picked experts in increasing id (the shared expert last), so list
+// entry d is the (d+1)-th set bit of the pick bitmap.  Returns the number of chunks issued (0 or 3).
+__device__ __forceinline__ int issue_first_unit(FSmem &S, const FusedMaps &maps, const FusedDecodeArgs &a,
+                                                const FusedGeom &geo, uint8_t *ring)
+{
+    const int lane = threadIdx.x & 31, SL = a.I / kSlice;
+    constexpr int NW = kMaxExperts / 32;
+    const uint32_t wbits = lane < NW ? S.pickmap[lane] : 0u;
+    const int cnt = __popc(wbits);
+    int pre = cnt;                                   // inclusive prefix count over the bitmap words
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, pre, o);
+        if (lane >= o) pre += v;
+    }
+    const int npick = __shfl_sync(0xffffffffu, pre, 31);
+    const int nlist = npick + (a.has_shared ? 1 : 0);
+    const int u = blockIdx.x, d = u / SL, s = u - d * SL;
+    if (d >= nlist) return 0;
+    int e = a.E;                                     // the shared expert, last
+    if (d < npick) {
+        const int wl = __ffs(__ballot_sync(0xffffffffu, pre > d)) - 1;
+        const uint32_t w = __shfl_sync(0xffffffffu, wbits, wl);
+        const int before = __shfl_sync(0xffffffffu, pre - cnt, wl);
+        e = wl * 32 + (int)__fns(w, 0, d - before + 1);
+    }
+    const uint64_t pol = l2_evict_first_policy();
+#pragma unroll 1
+    for (int c = 0; c < 3; ++c) issue_chunk(maps, a, geo, ring, S.full, c, e, s, c, pol);
+    return 3;
+}
+
+// Every issued copy lands before the CTA may leave: a slot is refilled only after the warps that read it
+// saw its previous copy land, so the copies still in flight are among the last R issued.
+__device__ __forceinline__ void producer_drain(FSmem &S, const FusedGeom &geo, int issued)
+{
+    const int R = geo.R;
+    if ((threadIdx.x & 31) == 0)
+#pragma unroll 1
+        for (int q = issued > R ? issued - R : 0; q < issued; ++q)
+            mbar_wait(smem_u32(&S.full[q % R]), (q / R) & 1, kDrainLimit, nullptr);
+    __syncwarp();
+}
+
+// The producer loop: units blockIdx.x, + grid, ...; the first unit's chunks may already be in flight
+// (`issued` of them, from issue_first_unit).
+__device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, const FusedDecodeArgs &a,
+                                            const FusedGeom &geo, uint8_t *ring, int U, int issued)
+{
+    const int lane = threadIdx.x & 31;
+    const int E = a.E, SL = a.I / kSlice, R = geo.R;
     const long long limit = kRingLimit;
-    const uint16_t *gsc = a.gate.scales, *gbi = a.gate.biases, *usc = a.up.scales, *ubi = a.up.biases;
-    const uint16_t *sgsc = a.s_gate.scales, *sgbi = a.s_gate.biases, *susc = a.s_up.scales, *subi = a.s_up.biases;
-    const uint8_t *dcodes = a.down.codes, *sdcodes = a.s_down.codes;
-    const uint8_t *packed = a.down_packed, *spacked = a.s_down_packed;
-    const CUtensorMap *mg = &maps.g, *mu = &maps.u, *msg = &maps.sg, *msu = &maps.su;
-    int issued = 0;
     bool stop = false;
     // every weight byte is read once per launch: evict-first in L2, so the per-slice partial sums that
     // the combine reads back stay there
     const uint64_t pol = l2_evict_first_policy();
+    const int i0 = issued / 3;
 #pragma unroll 1
-    for (int u = blockIdx.x, i = 0; u < U && !stop; u += gridDim.x, ++i) {
+    for (int u = blockIdx.x + i0 * (int)gridDim.x, i = i0; u < U && !stop; u += gridDim.x, ++i) {
         const int d = u / SL, s = u - d * SL, e = S.list[d];
-        const bool shr = e == E;
         if (e < 0 || e > E || d >= S.nlist) {           // a list entry out of range: report, issue nothing
             if (lane == 0) {
                 S.abort = 1;
@@ -615,49 +703,11 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
                 stop = true;
                 break;
             }
-            uint8_t *base = ring + (size_t)slot * slot_bytes;
-            const uint32_t fb = smem_u32(&S.full[slot]);
-            const int row0 = (shr ? 0 : e * I) + s * kSlice;
-            if (c < 2) {
-                // gate or up chunk: one 3D copy of the 32 code rows (each 128-byte box in the 128-byte
-                // swizzle) and two bulk copies of their scales and biases
-                if (lane == 0) {
-                    const size_t so = (size_t)row0 * G;
-                    const uint16_t *sc = c == 0 ? (shr ? sgsc : gsc) : (shr ? susc : usc);
-                    const uint16_t *bi = c == 0 ? (shr ? sgbi : gbi) : (shr ? subi : ubi);
-                    mbar_arrive_expect_tx(fb, codes1 + 2 * sc1);
-                    tma_load_3d_hint(smem_u32(base), c == 0 ? (shr ? msg : mg) : (shr ? msu : mu), 0, row0, 0, fb, pol);
-                    bulk_load_hint(smem_u32(base + codes1), sc + so, sc1, fb, pol);
-                    bulk_load_hint(smem_u32(base + codes1 + sc1), bi + so, sc1, fb, pol);
-                } else {
-                    mbar_arrive(fb);
-                }
-            } else if (packed != nullptr && (!shr || spacked != nullptr)) {
-                // the slice's down codes are one contiguous block of the packed layout: one bulk copy
-                if (lane == 0) {
-                    const uint8_t *src = shr ? spacked + (size_t)s * H * 16 : packed + ((size_t)e * SL + s) * H * 16;
-                    mbar_arrive_expect_tx(fb, (uint32_t)H * 16);
-                    bulk_load_hint(smem_u32(base), src, (uint32_t)H * 16, fb, pol);
-                } else {
-                    mbar_arrive(fb);
-                }
-            } else {
-                const uint8_t *src = (shr ? sdcodes : dcodes) + (size_t)(shr ? 0 : e) * H * drow + s * 16;
-                const uint32_t dst = smem_u32(base);
-#pragma unroll 4
-                for (int r = lane; r < H; r += 32) cp_async16(dst + r * 16, src + (size_t)r * drow);
-                cp_async_mbar_arrive_noinc(fb);
-            }
+            issue_chunk(maps, a, geo, ring, S.full, slot, e, s, c, pol);
             issued = q + 1;
         }
     }
-    // every issued copy lands before the CTA may leave: a slot is refilled only after the warps that
-    // read it saw its previous copy land, so the copies still in flight are among the last R issued
-    if (lane == 0)
-#pragma unroll 1
-        for (int q = issued > R ? issued - R : 0; q < issued; ++q)
-            mbar_wait(smem_u32(&S.full[q % R]), (q / R) & 1, kDrainLimit, nullptr);
-    __syncwarp();
+    producer_drain(S, geo, issued);
 }
 
 // ------------------------------------------------------------------ consumers (warps 0-7)
@@ -1225,9 +1275,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     stamp(a, kStRouterPub);
 
     // ---- routing, and x' for the expert units from the raw rows in the ring area (route_and_list)
-    int U = 0;
+    int U = 0, early = 0;
     if (!S.abort) {
-        route_and_list(S, a, a.logits_in, s_xr, s_x, s_xs);
+        // the producer sends the first unit's chunks as soon as the picks are known
+        route_and_list(S, a, a.logits_in, s_xr, s_x, s_xs, [&]() {
+            if (warp == kWarpProd && !S.abort) early = issue_first_unit(S, maps, a, geo, ring);
+        });
         U = S.nlist * SL;
     }
     stamp(a, kStRouted);
@@ -1237,9 +1290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     __syncthreads();
 
+    if (!go && warp == kWarpProd) producer_drain(S, geo, early);   // copies already in flight land first
     if (go) {
         if (warp == kWarpProd) {
-            fused_producer(S, maps, a, geo, ring, U);
+            fused_producer(S, maps, a, geo, ring, U, early);
         } else if (warp == kWarpAux) {
             prefetch_combine_scales(S, a, geo);
             token_weights(S, a);
