@@ -46,6 +46,7 @@
 // Every wait is bounded (a status code is recorded instead of hanging): the waits on other CTAs by
 // the caller's limit, a CTA's waits on its own copies by a fixed one (kRingLimit).
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.cuh"
 #include "tc_ptx.cuh"
@@ -620,6 +621,27 @@ __device__ __forceinline__ void issue_chunk(const FusedMaps &maps, const FusedDe
     }
 }
 
+// List entry d and slice s of unit u.  Units go round-robin over the CTAs (CTA b takes u = b, b + grid,
+// ...), so the CTAs b < U mod grid take one unit more than the others.  The shared expert's units (a
+// column per token: the heaviest) take the positions of the last full round's final CTAs, which take no
+// extra unit; the routed experts' units fill the other positions in list order.
+__device__ __forceinline__ void unit_at(int u, int U, int SL, int nlist, int has_shared, int &d, int &s)
+{
+    int v = u;
+    if (has_shared) {
+        const int grid = (int)gridDim.x;
+        const int P = max(0, min(U - SL, (U / grid) * grid - SL));
+        if (u >= P && u < P + SL) {
+            d = nlist - 1;
+            s = u - P;
+            return;
+        }
+        if (u >= P + SL) v = u - SL;
+    }
+    d = v / SL;
+    s = v - d * SL;
+}
+
 // Issued right after top-k, by the producer warp, before the expert list is built: the three chunks of this
 // CTA's first unit.  The list holds the picked experts in increasing id (the shared expert last), so list
 // entry d is the (d+1)-th set bit of the pick bitmap.  Returns the number of chunks issued (0 or 3).
@@ -638,8 +660,10 @@ __device__ __forceinline__ int issue_first_unit(FSmem &S, const FusedMaps &maps,
     }
     const int npick = __shfl_sync(0xffffffffu, pre, 31);
     const int nlist = npick + (a.has_shared ? 1 : 0);
-    const int u = blockIdx.x, d = u / SL, s = u - d * SL;
-    if (d >= nlist) return 0;
+    const int u = blockIdx.x;
+    if (u >= nlist * SL) return 0;
+    int d, s;
+    unit_at(u, nlist * SL, SL, nlist, a.has_shared, d, s);
     int e = a.E;                                     // the shared expert, last
     if (d < npick) {
         const int wl = __ffs(__ballot_sync(0xffffffffu, pre > d)) - 1;
@@ -680,7 +704,9 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
     const int i0 = issued / 3;
 #pragma unroll 1
     for (int u = blockIdx.x + i0 * (int)gridDim.x, i = i0; u < U && !stop; u += gridDim.x, ++i) {
-        const int d = u / SL, s = u - d * SL, e = S.list[d];
+        int d, s;
+        unit_at(u, U, SL, S.nlist, a.has_shared, d, s);
+        const int e = S.list[d];
         if (e < 0 || e > E || d >= S.nlist) {           // a list entry out of range: report, issue nothing
             if (lane == 0) {
                 S.abort = 1;
@@ -741,7 +767,8 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
     bool fail_d = false;
 #pragma unroll 1
     for (int u = blockIdx.x, i = 0; u < U; u += gridDim.x, ++i) {
-        const int d = u / SL, s = u - d * SL;
+        int d, s;
+        unit_at(u, U, SL, S.nlist, a.has_shared, d, s);
         const int ncol = min(S.ncols[d], T), colbase = S.colptr[d];
         // the x' row and the group-sum rows of the lane's B column (c) and D columns (cA, cA + 1); a lane
         // whose column is past the expert's reads the first column's token instead (those MMA columns and
@@ -763,15 +790,18 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
         bool ok = !fail_d && warp_wait(&S.full[slotg], (qg / R) & 1, limit, &S.abort);
         if (i == 0) stamp(a, kStFirstGate);
         ok = ok && warp_wait(&S.full[slotu], (qu / R) & 1, limit, &S.abort);
-        if (ok) {
+        // the unit's token columns in one 8-column MMA tile (every routed expert at these sizes) or two
+        // (ncol > 8): each a separate straight-line path, no per-step branch on the column count
+        auto gateup = [&](auto ntu) {
+            constexpr int NTU = decltype(ntu)::value;
             const uint8_t *chg = ring + (size_t)slotg * geo.slot, *chu = ring + (size_t)slotu * geo.slot;
             const uint8_t *cbg = chg + (mt * 16 + g) * 128, *cbu = chu + (mt * 16 + g) * 128;   // row mt 16 + g of every 4 KB box
             const uint16_t *scg = reinterpret_cast<const uint16_t *>(chg + geo.codes1) + (mt * 16 + g) * G;
             const uint16_t *scu = reinterpret_cast<const uint16_t *>(chu + geo.codes1) + (mt * 16 + g) * G;
             const uint16_t *big = scg + kSlice * G, *biu = scu + kSlice * G;
-            float accg[NT][4], accu[NT][4];
+            float accg[NTU][4], accu[NTU][4];
 #pragma unroll
-            for (int j = 0; j < NT; ++j)
+            for (int j = 0; j < NTU; ++j)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) accg[j][v] = accu[j][v] = 0.f;
             // one group: the code words of rows g, g + 8 of both matrices, the x' fragment at element xo of
@@ -789,8 +819,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                 nib8_signed(cu1.x, au1, dq);
                 nib8_signed(cu1.y, au1 + 4, dq);
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    if (j > 0 && j * 8 >= ncol) break;        // every expert has a first column
+                for (int j = 0; j < NTU; ++j) {
                     const uint4 *xr = reinterpret_cast<const uint4 *>(xq[j] + xo);
                     const uint4 lo = xr[0], hi = xr[1];
                     const uint32_t bp[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
@@ -864,7 +893,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
             float *redg = s_red + (size_t)(0 * 4 + kq) * NC * kSlice + mt * 16;
             float *redu = s_red + (size_t)(1 * 4 + kq) * NC * kSlice + mt * 16;
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
+            for (int j = 0; j < NTU; ++j) {
                 const int c0 = j * 8 + 2 * t4;
                 redg[c0 * kSlice + g] = accg[j][0];
                 redg[(c0 + 1) * kSlice + g] = accg[j][1];
@@ -875,6 +904,12 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                 redu[c0 * kSlice + g + 8] = accu[j][2];
                 redu[(c0 + 1) * kSlice + g + 8] = accu[j][3];
             }
+        };
+        if (ok) {
+            if (NT == 2 && ncol > 8)
+                gateup(std::integral_constant<int, NT>{});
+            else
+                gateup(std::integral_constant<int, 1>{});
         }
         // a warp releases the chunks only once both have landed (its waits succeeded): otherwise the
         // producer could issue the next copy into a slot whose copy is still in flight
@@ -921,11 +956,12 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
         const int q2 = 3 * i + 2, slot2 = q2 % R;
         const bool okd = warp_wait(&S.full[slot2], (q2 / R) & 1, limit, &S.abort);
         if (i == 0) stamp(a, kStFirstDown);
-        if (okd) {
+        auto down = [&](auto ntu) {
+            constexpr int NTU = decltype(ntu)::value;
             const uint8_t *dch = ring + (size_t)slot2 * geo.slot;
-            uint32_t hb[NT][4];
+            uint32_t hb[NTU][4];
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
+            for (int j = 0; j < NTU; ++j) {
                 const int c = j * 8 + g;
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 if (c < ncol) v = *reinterpret_cast<const uint4 *>(s_h + c * kSlice + 8 * t4);
@@ -947,8 +983,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                 nib8_signed(w0, a0, dq);
                 nib8_signed(w1, a1, dq);
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    if (j > 0 && j * 8 >= ncol) break;
+                for (int j = 0; j < NTU; ++j) {
                     float dd[4] = {0.f, 0.f, 0.f, 0.f};
                     mma16816<true>(dd, a0[0], a1[0], a0[1], a1[1], hb[j][0], hb[j][1]);
                     mma16816<true>(dd, a0[2], a1[2], a0[3], a1[3], hb[j][2], hb[j][3]);
@@ -972,6 +1007,12 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
 #pragma unroll 4
                 for (int tt = 0; tt < MT; ++tt) tile(tt);
             }
+        };
+        if (okd) {
+            if (NT == 2 && ncol > 8)
+                down(std::integral_constant<int, NT>{});
+            else
+                down(std::integral_constant<int, 1>{});
         }
         __syncwarp();
         if (i == 0) stamp(a, kStFirstDownDone);
