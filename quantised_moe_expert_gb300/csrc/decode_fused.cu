@@ -305,7 +305,8 @@ __device__ __forceinline__ void convert_row(FSmem &S, const FusedDecodeArgs &a, 
 // logits: the caller's fp32 logits, or null for the logits this launch publishes (tagged with its epoch).
 template <class AfterTopk>
 __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &a, const float *logits,
-                                               const uint16_t *s_xr, uint16_t *s_x, float *s_xs, AfterTopk after_topk)
+                                               const uint16_t *s_xr, uint16_t *s_x, float *s_xs, uint32_t *s_key,
+                                               AfterTopk after_topk)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, E = a.E, k = a.k;
@@ -327,51 +328,61 @@ __device__ __forceinline__ void route_and_list(FSmem &S, const FusedDecodeArgs &
         }
     } else {
         constexpr int RW = kMaxExperts / 32;
-#pragma unroll 1
-        for (int t = warp; t < T; t += kW) {
-            uint32_t key[RW];
-            if (logits) {
-#pragma unroll
-                for (int r = 0; r < RW; ++r) {
-                    const int e = lane + 32 * r;
-                    key[r] = e < E ? logit_key(__ldcg(logits + (size_t)t * E + e)) : 0u;   // 0: below every logit
-                }
-            } else {
-                // logits published by the CTAs of this launch, each tagged with the launch's epoch: poll
-                // the row until every entry carries it (bounded)
-                const unsigned long long *row = a.logits64 + (size_t)t * E;
+        if (!logits) {
+            // logits published by the CTAs of this launch, each tagged with the launch's epoch: every thread
+            // polls its entries of all T rows at once (entry tid + j kThreads) until every entry of every
+            // row carries the epoch (bounded), leaving the order keys in shared memory
+            const unsigned long long *lg = a.logits64;
+            const int n = T * E;
+            const uint32_t ep = S.epoch;
+            // bit j: entry tid + j kThreads still stale; each pass issues all of the thread's loads before it
+            // looks at any, so the round trips overlap
+            constexpr int kPoll = (kDecodeMaxTok * kMaxExperts + kThreads - 1) / kThreads;
+            auto poll_all = [&](auto np) {               // np: entries per thread, at most
+                constexpr int NP = decltype(np)::value;
                 uint32_t pend = 0;
 #pragma unroll
-                for (int r = 0; r < RW; ++r) {
-                    const int e = lane + 32 * r;
-                    key[r] = 0u;
-                    if (e < E) {
-                        const unsigned long long v = ld_relaxed_u64(row + e);
-                        if ((uint32_t)(v >> 32) == S.epoch) key[r] = logit_key(__uint_as_float((uint32_t)v));
-                        else pend |= 1u << r;
-                    }
-                }
+                for (int j = 0; j < NP; ++j)
+                    if (tid + j * kThreads < n) pend |= 1u << j;
+                auto pass = [&]() {
+                    unsigned long long v[NP];
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) v[j] = (pend >> j) & 1u ? ld_relaxed_u64(lg + tid + j * kThreads) : 0ull;
+#pragma unroll
+                    for (int j = 0; j < NP; ++j)
+                        if (((pend >> j) & 1u) && (uint32_t)(v[j] >> 32) == ep) {
+                            s_key[tid + j * kThreads] = logit_key(__uint_as_float((uint32_t)v[j]));
+                            pend &= ~(1u << j);
+                        }
+                };
+                pass();
                 long long polls = 1;
-                while (__any_sync(0xffffffffu, pend != 0)) {
+                while (__syncthreads_or(pend != 0)) {
                     if (polls++ >= a.wait_limit) {
-                        if (lane == 0) {
+                        if (tid == 0) {
                             S.abort = 1;
                             record_status(a.status, MOE_ERR_TIMEOUT);
                         }
                         break;
                     }
                     __nanosleep(32);
-#pragma unroll
-                    for (int r = 0; r < RW; ++r)
-                        if (pend & (1u << r)) {
-                            const unsigned long long v = ld_relaxed_u64(row + lane + 32 * r);
-                            if ((uint32_t)(v >> 32) == S.epoch) {
-                                key[r] = logit_key(__uint_as_float((uint32_t)v));
-                                pend &= ~(1u << r);
-                            }
-                        }
+                    pass();
                 }
-                if (t == 0) stamp(a, kStLogitsSeen);
+            };
+            if (n <= kThreads)
+                poll_all(std::integral_constant<int, 1>{});
+            else
+                poll_all(std::integral_constant<int, kPoll>{});
+            __syncthreads();                           // every key written (also after a timeout)
+            stamp(a, kStLogitsSeen);
+        }
+#pragma unroll 1
+        for (int t = warp; t < T; t += kW) {
+            uint32_t key[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int e = lane + 32 * r;
+                key[r] = e < E ? (logits ? logit_key(__ldcg(logits + (size_t)t * E + e)) : s_key[t * E + e]) : 0u;   // 0: below every logit
             }
             // the lane's RW (key, id) pairs sorted once, largest first (the key, then the lower id:
             // hi = 0xFFFF - e orders equal keys), by an 8-input sorting network; then each round takes
@@ -1319,7 +1330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int U = 0, early = 0;
     if (!S.abort) {
         // the producer sends the first unit's chunks as soon as the picks are known
-        route_and_list(S, a, a.logits_in, s_xr, s_x, s_xs, [&]() {
+        uint32_t *s_key = reinterpret_cast<uint32_t *>(ring + ((size_t)T * XS * 2 + 15) / 16 * 16);   // after raw x
+        route_and_list(S, a, a.logits_in, s_xr, s_x, s_xs, s_key, [&]() {
             if (warp == kWarpProd && !S.abort) early = issue_first_unit(S, maps, a, geo, ring);
         });
         U = S.nlist * SL;
@@ -1408,7 +1420,7 @@ bool dev_info(int dev, DevInfo *out)
     return true;
 }
 
-bool fused_geometry(int T, int H, int I, int k, int has_shared, int grid, int optin, FusedGeom *out)
+bool fused_geometry(int T, int H, int I, int E, int k, int has_shared, int grid, int optin, FusedGeom *out)
 {
     if (T < 1 || T > kDecodeMaxTok || H % 256 || H > 2048 || I % 64 || I > 4096 || grid < 1) return false;
     FusedGeom g{};
@@ -1430,7 +1442,8 @@ bool fused_geometry(int T, int H, int I, int k, int has_shared, int grid, int op
     g.RB = 4 * ((H + 4 * grid - 1) / (4 * grid));
     const int NS = k + (has_shared ? 1 : 0);
     if ((size_t)T * (g.RB / 4) * NS * 16 > (size_t)g.R * g.slot) return false;   // combine terms in the ring
-    if ((size_t)T * (G * kXG + 8) * 2 > (size_t)g.R * g.slot) return false;       // raw x in the ring
+    // raw x, then the order keys of the polled logits, in the ring area
+    if (((size_t)T * (G * kXG + 8) * 2 + 15) / 16 * 16 + (size_t)T * E * 4 > (size_t)g.R * g.slot) return false;
     size_t o = (size_t)g.R * g.slot;
     g.x_off = (uint32_t)o;
     o += xb;
@@ -1466,7 +1479,7 @@ bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared)
     if (cudaGetDevice(&dev) != cudaSuccess || !dev_info(dev, &di)) return false;
     if (E > kCW * di.sms || di.sms > kTraceMaxCtas) return false;   // at most eight router experts per CTA
     FusedGeom g;
-    return fused_geometry(T, H, I, k, has_shared, di.sms, di.optin, &g);
+    return fused_geometry(T, H, I, E, k, has_shared, di.sms, di.optin, &g);
 }
 
 size_t decode_fused_trace_ctas()
@@ -1485,7 +1498,7 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs &a, cudaStream_t st)
     DevInfo di;
     if (!dev_info(dev, &di)) return cudaErrorInvalidDevice;
     FusedGeom geo;
-    if (!fused_geometry(a.T, a.H, a.I, a.k, a.has_shared, di.sms, di.optin, &geo)) return cudaErrorInvalidValue;
+    if (!fused_geometry(a.T, a.H, a.I, a.E, a.k, a.has_shared, di.sms, di.optin, &geo)) return cudaErrorInvalidValue;
     FusedMaps maps;
     const uint64_t E = (uint64_t)a.E;
     bool ok = code_map_rows(&maps.g, a.gate.codes, a.H / 2, E * a.I, kSlice) &&
