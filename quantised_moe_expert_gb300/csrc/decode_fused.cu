@@ -853,7 +853,9 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                     accu[j][3] = fmaf(su1, du[3], fmaf(ku1, xB, accu[j][3]));
                 }
             };
-            if ((gq & 7) == 0) {
+            // the two-tile path (the shared expert's units at T > 8, a few per launch) takes the compact
+            // loop: a second fully unrolled copy would crowd the instruction cache of the hot path
+            if ((gq & 7) == 0 && NTU == 1) {
                 // blocks of eight groups (g0 a multiple of 8): the lane's four code offsets inside a box row
                 // (group position q = 0..3) are fixed, so every load of the block is a base plus a constant.
                 // Scales and biases of the eight groups per 16-byte load: rows g and g + 8 sit 64 bytes
@@ -1011,7 +1013,7 @@ __device__ __forceinline__ void fused_consumers(FSmem &S, const FusedDecodeArgs 
                     }
                 }
             };
-            if (MT == 16) {            // H = 2048: all sixteen tiles unrolled
+            if (MT == 16 && NTU == 1) {   // H = 2048: all sixteen tiles unrolled (the two-tile path stays compact)
 #pragma unroll
                 for (int tt = 0; tt < 16; ++tt) tile(tt);
             } else {
