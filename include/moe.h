@@ -50,7 +50,9 @@
  *   - Values: x and the weights are finite.  Each token's x is scaled by a
  *     power of two before the 16-bit intermediate steps and the scale is
  *     undone after them (exact), so rows far above the fp16 range or entirely
- *     below its normal range keep their precision; only an output beyond the
+ *     below its normal range keep their precision (within a row, elements
+ *     below 2^-17 of its largest are held to fp16's subnormal spacing, an
+ *     error of at most 2^-25 of that largest); only an output beyond the
  *     bf16 range overflows.
  *
  * Storage formats (MLX layout, [out, in] with quantisation along `in`)
