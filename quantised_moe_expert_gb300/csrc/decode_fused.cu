@@ -11,9 +11,11 @@
 //      ...) are loaded into registers before the wait for the preceding kernel; then x is
 //      staged in shared memory, the CTA's logits go to global memory tagged with the
 //      launch's epoch, and x is pre-scaled per token by a power of two (x' = x 2^-e, max |x'|
-//      in [1, 2): exact, and it keeps h inside the fp16 range, see below).  Every CTA then
-//      polls the tagged logits until all carry the epoch, runs the same top-k (warp max /
-//      min reductions, ties to the lower id) and builds the same expert list: no counter.
+//      in [1, 2), held as fp16: it keeps h inside the fp16 range, see below).  Every CTA then
+//      polls the tagged logits of all tokens (all threads at once) until all carry the epoch,
+//      runs the same top-k (warp max reductions, ties to the lower id), and its producer sends
+//      its first unit's chunks at once, before the expert list (the same in every CTA: no
+//      counter) is built.
 //   2. Units.  A unit is (expert, 32-row slice s of the intermediate dimension): the
 //      slice's gate and up rows (all of H) and the slice's 32 columns of the down matrix
 //      (all H rows).  Because the affine rule holds for any subset of a group,
