@@ -732,7 +732,7 @@ __device__ __forceinline__ void fused_producer(FSmem &S, const FusedMaps &maps, 
             const int q = 3 * i + c, slot = q % R;
             bool ok = true;
             if (lane == 0 && q >= R &&
-                !mbar_wait_sleepy(smem_u32(&S.empty[slot]), ((q / R) - 1) & 1, limit, &S.abort)) {
+                !mbar_wait(smem_u32(&S.empty[slot]), ((q / R) - 1) & 1, limit, &S.abort)) {
                 S.abort = 1;
                 record_status(a.status, MOE_ERR_TIMEOUT);
                 ok = false;
