@@ -84,19 +84,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
     }
 }
 
-// The same wait for a thread whose wait does not hold up others' work (a producer
-// waiting for a free slot): the polls are spaced by a short sleep, so the waiting
-// thread takes neither issue slots nor shared-memory bandwidth from the SM.
-__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, long long limit, volatile int *abort)
-{
-    if (mbar_test(bar, parity)) return true;
-    for (long long i = 1;; ++i) {
-        if (i >= limit || (abort != nullptr && *abort)) return false;
-        __nanosleep(128);
-        if (mbar_test(bar, parity)) return true;
-    }
-}
-
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
