@@ -117,6 +117,7 @@ struct FSmem {
     int scanp[kThreads / 32], scanc[kThreads / 32];   // per-warp sums of the list scans
     int nlist;
     int abort;
+    int cnt_state;                          // unit counter: 0 polling, 1 complete, 2 a poll ran out
     uint32_t epoch;                         // this launch's tag on the published logits
     uint64_t full[kMaxSlots], empty[kMaxSlots];
 };
@@ -193,17 +194,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
 {
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Bounded poll until *p >= target: one poll, then at most limit - 1 more, spaced by a short sleep.
-__device__ __noinline__ bool poll_geq(const int *p, int target, long long limit)
-{
-    if (ld_acquire_gpu(p) >= target) return true;
-    for (long long n = 1; n < limit; ++n) {
-        __nanosleep(32);
-        if (ld_acquire_gpu(p) >= target) return true;
-    }
-    return false;
 }
 
 // Called by whole warps; thread 0 writes the stamp and the warp is brought back together.
@@ -1365,15 +1355,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     stamp(a, kStUnitsDone);
-    if (tid == 0 && !S.abort) {
-        __threadfence();            // this CTA's partial sums and published weights, before the count
-        const int old = atomicAdd(cnt_units, 1);
-        if (old < 0 || old >= grid) {
-            record_status(a.status, MOE_ERR_WORKSPACE);
-            S.abort = 1;
-        } else if (!poll_geq(cnt_units, grid, limit)) {
-            record_status(a.status, MOE_ERR_TIMEOUT);
-            S.abort = 1;
+    // the unit counter: thread 0 adds this CTA; then lane 0 of every warp polls it, their first polls spread
+    // over about one L2 round trip, so the count is seen soon after it reaches L2; the first poller to see it
+    // (with an acquire load) tells the others through shared memory, and the barrier orders every thread's
+    // reads of the other CTAs' partial sums after that acquire
+    if (tid == 0) {
+        S.cnt_state = 0;
+        if (!S.abort) {
+            __threadfence();        // this CTA's partial sums and published weights, before the count
+            const int old = atomicAdd(cnt_units, 1);
+            if (old < 0 || old >= grid) {
+                record_status(a.status, MOE_ERR_WORKSPACE);
+                S.abort = 1;
+            }
+        }
+    }
+    __syncthreads();
+    if (!S.abort && lane == 0) {
+        volatile int *st = &S.cnt_state;
+        __nanosleep(96 * warp);
+        for (long long n = 1; *st == 0; ++n) {
+            if (ld_acquire_gpu(cnt_units) >= grid) {
+                *st = 1;
+                break;
+            }
+            if (n >= limit) {
+                if (atomicCAS(&S.cnt_state, 0, 2) == 0) {
+                    record_status(a.status, MOE_ERR_TIMEOUT);
+                    S.abort = 1;
+                }
+                break;
+            }
+            __nanosleep(32);
         }
     }
     __syncthreads();
