@@ -1048,15 +1048,12 @@ __device__ __forceinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a
         return;
     }
     const int nq = nrows / 4;
-#pragma unroll 1
-    for (int i = tid; i < T * k; i += kThreads)
-        S.p[i / k][i % k] = bf16_bits_to_float(a.ids_in ? a.p_in[i] : __ldcg(a.p_glob + i));
-#pragma unroll 1
-    for (int t = tid; t < T; t += kThreads) {
-        uint16_t wb = 0;
-        if (a.has_shared) wb = a.ids_in ? (a.ws_in ? a.ws_in[t] : (uint16_t)0) : __ldcg(a.ws_glob + t);
-        S.ws[t] = bf16_bits_to_float(wb);
-    }
+    // the pick and shared weights (published by other CTAs): loaded now, one per thread, and stored to shared
+    // memory only after the items' loads are out, so the two sets of loads share one round trip
+    static_assert(kDecodeMaxTok * kMaxTopK <= kThreads, "one pick weight per thread");
+    uint16_t pb = 0, wb = 0;
+    if (tid < T * k) pb = a.ids_in ? a.p_in[tid] : __ldcg(a.p_glob + tid);
+    if (tid < T && a.has_shared) wb = a.ids_in ? (a.ws_in ? a.ws_in[tid] : (uint16_t)0) : __ldcg(a.ws_glob + tid);
     const int nitem = T * nq * NS;
     // item it: the quad q varies fastest, so the threads of one (token, slot) read the 4 nq consecutive
     // rows of each slice's partial sums (and of the scale and bias rows) as one contiguous block
@@ -1132,6 +1129,8 @@ __device__ __forceinline__ void fused_combine(FSmem &S, const FusedDecodeArgs &a
             *reinterpret_cast<float4 *>(a.yslot_out + (size_t)f * H + r) = v;
         }
     }
+    if (tid < T * k) S.p[tid / k][tid % k] = bf16_bits_to_float(pb);
+    if (tid < T) S.ws[tid] = bf16_bits_to_float(wb);
     __syncthreads();
     stamp(a, kStCombineLoads);
     if (a.stages_only) return;
