@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(RouteArgs a)
 // One warp per token, 8 tokens per block.  Lane l holds logits e = l + 32 r.
 // A logit maps to an order-preserving unsigned key (+0 and -0 map to the same
 // key); the pair (key, 0xFFFF - id) is maximised, so equal logits resolve to
-// the lower id.  k rounds of a warp max give the ids in rank order.  Weights
+// the lower id: each lane sorts its pairs once, then k rounds of two warp
+// reductions give the ids in rank order.  Weights
 // are computed in fp64 and rounded once to bf16 (fp64 is scarce on this GPU,
 // hence few tokens per block so the work spreads over every SM).  Each pick
 // is counted into the histogram row of its 128-token block (global atomics).
@@ -157,47 +158,58 @@ __global__ void __launch_bounds__(256) topk_kernel(TopkArgs a)
         if (t >= a.T) return;
         const float *lrow = a.logits + (size_t)t * E;
         uint32_t key[kMaxExperts / 32];
-        float val[kMaxExperts / 32];
 #pragma unroll
         for (int r = 0; r < kMaxExperts / 32; ++r) {
             const int e = lane + 32 * r;
-            if (r < R && e < E) {
-                val[r] = lrow[e];
-                key[r] = logit_key(val[r]);
-            } else {
-                val[r] = 0.f;
-                key[r] = 0;     // below every real key
-            }
+            key[r] = r < R && e < E ? logit_key(lrow[e]) : 0u;   // 0: below every real key
         }
-        unsigned taken = 0;     // bit r: logit lane+32r already picked
+        // the lane's eight (key, id) pairs sorted once, largest first (the key, then the lower id: hi =
+        // 0xFFFF - e orders equal keys), by an 8-input sorting network; then each round takes the warp's
+        // largest head (the key by one reduction, the id among equal keys by another) and its lane pops it
+        static_assert(kMaxExperts / 32 == 8, "the sorting network below is for eight keys per lane");
+        uint32_t hk[8], hi[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            hk[r] = key[r];
+            hi[r] = 0xFFFFu - (uint32_t)(lane + 32 * r);
+        }
+        auto cx = [&](int a0, int b0) {           // (hk, hi)[a0] >= (hk, hi)[b0] afterwards
+            const bool sw = hk[b0] > hk[a0] || (hk[b0] == hk[a0] && hi[b0] > hi[a0]);
+            const uint32_t ka = hk[a0], ia = hi[a0];
+            hk[a0] = sw ? hk[b0] : ka;
+            hi[a0] = sw ? hi[b0] : ia;
+            hk[b0] = sw ? ka : hk[b0];
+            hi[b0] = sw ? ia : hi[b0];
+        };
+        cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+        cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+        cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+        cx(2, 4); cx(3, 5);
+        cx(1, 4); cx(3, 6);
+        cx(1, 2); cx(3, 4); cx(5, 6);
         int my_id = -1;         // lane j < k ends with the id of rank j
         float my_l = 0.f;
         float top_l = 0.f;
+#pragma unroll 1
         for (int j = 0; j < k; ++j) {
-            unsigned long long best = 0;
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, hk[0]);
+            const uint32_t mi = __reduce_max_sync(0xffffffffu, hk[0] == mk ? hi[0] : 0u);
+            if (hk[0] == mk && hi[0] == mi) {   // this lane's head is the pick: pop it
 #pragma unroll
-            for (int r = 0; r < kMaxExperts / 32; ++r) {
-                const int e = lane + 32 * r;
-                if (r < R && e < E && !(taken & (1u << r))) {
-                    unsigned long long c = ((unsigned long long)key[r] << 32) | (unsigned)(0xFFFF - e);
-                    best = c > best ? c : best;
+                for (int r = 0; r < 7; ++r) {
+                    hk[r] = hk[r + 1];
+                    hi[r] = hi[r + 1];
                 }
+                hk[7] = 0u;
+                hi[7] = 0u;
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-                best = other > best ? other : best;
-            }
-            const int id = 0xFFFF - (int)(best & 0xFFFFu);
-            if ((id & 31) == lane) taken |= 1u << (id >> 5);
-            // logit value of the winner, broadcast from its owner lane
-            float v = 0.f;
-#pragma unroll
-            for (int r = 0; r < kMaxExperts / 32; ++r)
-                if ((id >> 5) == r) v = val[r];
-            v = __shfl_sync(0xffffffffu, v, id & 31);
+            // the winner's logit from its key (the key map is one to one but for -0, which reads as +0)
+            const float v = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7FFFFFFFu) : ~mk);
             if (j == 0) top_l = v;
-            if (lane == j) { my_id = id; my_l = v; }
+            if (lane == j) {
+                my_id = 0xFFFF - (int)mi;
+                my_l = v;
+            }
         }
         // pick weights p_j = exp(l_j - l_top) / sum_i exp(l_i - l_top), rounded once to bf16.  In fp32
         // first (the difference split exactly into hi + lo by Knuth's two-sum, exp(hi) (1 + lo), the sum in
