@@ -38,11 +38,12 @@ def build(force: bool = False) -> str:
 
 class _Cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
-                ("hidden", "inter", "n_experts", "top_k", "group", "bits", "router_bits", "has_shared")]
+                ("hidden", "inter", "n_experts", "top_k", "group", "bits", "router_bits", "has_shared", "format")]
 
 
 class _QMat(ctypes.Structure):
-    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p)]
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("bscales", ctypes.c_void_p), ("gscale", ctypes.c_void_p)]
 
 
 class _Weights(ctypes.Structure):
@@ -62,6 +63,9 @@ def lib():
             _lib.oracle_f32_rne.restype = ctypes.c_float
             _lib.oracle_f32_rne.argtypes = [ctypes.c_double]
             _lib.oracle_num_threads.restype = ctypes.c_int
+            for f in ("oracle_e2m1_to_double", "oracle_e4m3_to_double"):
+                getattr(_lib, f).restype = ctypes.c_double
+                getattr(_lib, f).argtypes = [ctypes.c_int]
         return _lib
 
 
@@ -75,7 +79,11 @@ def _c(a, dtype):
 
 def _cfg(shape) -> _Cfg:
     return _Cfg(shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.group, shape.bits,
-                shape.router_bits, shape.has_shared)
+                shape.router_bits, shape.has_shared, 1 if is_nvfp4(shape) else 0)
+
+
+def is_nvfp4(shape) -> bool:
+    return getattr(shape, "fmt", "affine") == "nvfp4"
 
 
 def num_threads() -> int:
@@ -99,6 +107,22 @@ def dequant_row(codes_row, scales_row, biases_row, bits: int, in_dim: int, group
     codes_row, scales_row, biases_row = _c(codes_row, np.uint8), _c(scales_row, np.uint16), _c(biases_row, np.uint16)
     lib().oracle_dequant_row(_p(codes_row), _p(scales_row), _p(biases_row), ctypes.c_int(bits),
                              ctypes.c_int(in_dim), ctypes.c_int(group), _p(out))
+    return out
+
+
+def e2m1_to_f64(code: int) -> float:
+    return lib().oracle_e2m1_to_double(int(code))
+
+
+def e4m3_to_f64(code: int) -> float:
+    return lib().oracle_e4m3_to_double(int(code))
+
+
+def dequant_row_nvfp4(codes_row, bscales_row, gscale: float, in_dim: int) -> np.ndarray:
+    out = np.empty(in_dim, dtype=np.float64)
+    codes_row, bscales_row = _c(codes_row, np.uint8), _c(bscales_row, np.uint8)
+    lib().oracle_dequant_row_nvfp4(_p(codes_row), _p(bscales_row), ctypes.c_float(gscale), ctypes.c_int(in_dim),
+                                   _p(out))
     return out
 
 
@@ -149,43 +173,56 @@ def shared_weight(x, v):
     return gamma, ws
 
 
-def _expert_arrays(weights, e):
-    """(gate, up, down) QMats of expert e; e == -1 selects the shared expert."""
-    if e < 0:
-        return tuple((m.codes[0], m.scales[0], m.biases[0]) for m in (weights.s_gate, weights.s_up, weights.s_down))
-    return tuple((m.codes[e], m.scales[e], m.biases[e]) for m in (weights.gate, weights.up, weights.down))
+def _qmat_struct(m, keep, e=None, nvfp4=False):
+    """ctypes view of a stacked QMat (or of its expert e): affine codes/scales/biases, or NVFP4
+    codes, E4M3 block scales (stored in ``scales``) and the fp32 per-matrix scales."""
+    sel = (lambda a: a) if e is None else (lambda a: a[e:e + 1])
+    if nvfp4:
+        arrs = (_c(sel(m.codes), np.uint8), _c(sel(m.scales), np.uint8), _c(sel(m.gscale), np.float32))
+        keep.extend(arrs)
+        return _QMat(arrs[0].ctypes.data, None, None, arrs[1].ctypes.data, arrs[2].ctypes.data)
+    arrs = (_c(sel(m.codes), np.uint8), _c(sel(m.scales), np.uint16), _c(sel(m.biases), np.uint16))
+    keep.extend(arrs)
+    return _QMat(arrs[0].ctypes.data, arrs[1].ctypes.data, arrs[2].ctypes.data, None, None)
+
+
+def _expert_mats(shape, weights, e, keep):
+    """(gate, up, down) structs of expert e; e == -1 selects the shared expert."""
+    mats = (weights.s_gate, weights.s_up, weights.s_down) if e < 0 else (weights.gate, weights.up, weights.down)
+    return tuple(_qmat_struct(m, keep, 0 if e < 0 else e, is_nvfp4(shape)) for m in mats)
 
 
 def expert_ffn(shape, weights, e: int, x_f64):
     """One expert (e == -1: shared) on one token given as fp64 [H]; returns (h [I], y [H])."""
-    arrs = [tuple(_c(a, np.uint8 if i == 0 else np.uint16) for i, a in enumerate(m)) for m in _expert_arrays(weights, e)]
+    keep = []
+    mg, mu, md = _expert_mats(shape, weights, e, keep)
     x_f64 = _c(x_f64, np.float64)
     h = np.empty(shape.inter, dtype=np.float64)
     y = np.empty(shape.hidden, dtype=np.float64)
     cfg = _cfg(shape)
-    flat = [_p(a) for m in arrs for a in m]
-    lib().oracle_expert_ffn(ctypes.byref(cfg), *flat, _p(x_f64), _p(h), _p(y))
+    lib().oracle_expert_ffn_m(ctypes.byref(cfg), ctypes.byref(mg), ctypes.byref(mu), ctypes.byref(md), _p(x_f64),
+                              _p(h), _p(y))
     return h, y
 
 
 def expert_down(shape, weights, e: int, h_f64):
-    d = _expert_arrays(weights, e)[2]
-    d = (_c(d[0], np.uint8), _c(d[1], np.uint16), _c(d[2], np.uint16))
+    keep = []
+    md = _expert_mats(shape, weights, e, keep)[2]
     h_f64 = _c(h_f64, np.float64)
     y = np.empty(shape.hidden, dtype=np.float64)
     cfg = _cfg(shape)
-    lib().oracle_expert_down(ctypes.byref(cfg), _p(d[0]), _p(d[1]), _p(d[2]), _p(h_f64), _p(y))
+    lib().oracle_expert_down_m(ctypes.byref(cfg), ctypes.byref(md), _p(h_f64), _p(y))
     return y
 
 
 def _weights_struct(weights, keep):
-    def q(m):
-        arrs = (_c(m.codes, np.uint8), _c(m.scales, np.uint16), _c(m.biases, np.uint16))
-        keep.extend(arrs)
-        return _QMat(*(a.ctypes.data for a in arrs))
+    nv = is_nvfp4(weights.shape)
+
+    def q(m, expert=True):
+        return _qmat_struct(m, keep, None, nv and expert)
     v = _c(weights.shared_gate_vec, np.uint16)
     keep.append(v)
-    return _Weights(q(weights.router), q(weights.gate), q(weights.up), q(weights.down),
+    return _Weights(q(weights.router, False), q(weights.gate), q(weights.up), q(weights.down),
                     q(weights.s_gate), q(weights.s_up), q(weights.s_down), v.ctypes.data)
 
 

@@ -17,7 +17,13 @@
  *   - the shared expert is one more slot weighted bf16(sigmoid(bf16(gate)));
  *   - the weighted sum is rounded once to bf16;
  *   - experts are MLX affine 4-bit in groups of 64, the router 8-bit:
- *     w = scale * q + bias per group of 64 inputs of one output row.
+ *     w = scale * q + bias per group of 64 inputs of one output row;
+ *   - or, the block-scaled variant: experts in NVFP4 (the checkpoint format of
+ *     the page "Qwen-3.6-35B-A3B-SIQ-K6-K4K3" model card, served there by a
+ *     fused FP4 MoE backend; the router stays 8-bit affine).  The pages name the
+ *     format only; its definition is the public one: 4-bit E2M1 elements, one
+ *     E4M3 scale per block of 16 consecutive inputs of a row, one fp32 scale
+ *     per matrix, w = e2m1(q) * e4m3(s) * g.
  * The expert FFN is SwiGLU: down(silu(gate x) * up x) ("expert gate/up pair,
  * expert down" in the Gate section).
  *
@@ -42,7 +48,10 @@
 
 typedef struct {
     int hidden, inter, n_experts, top_k, group, bits, router_bits, has_shared;
+    int format;   /* 0: MLX affine experts (bits 4 or 8), 1: NVFP4 experts */
 } oracle_cfg;
+
+#define ORACLE_NVFP4_BLOCK 16
 
 /* ---------------------------------------------------------------- numbers */
 
@@ -107,6 +116,45 @@ void oracle_dequant_row(const uint8_t *codes_row, const uint16_t *s_row, const u
 }
 
 static size_t row_bytes(int in_dim, int bits) { return (size_t)in_dim * (size_t)bits / 8; }
+
+/* E2M1, the 4-bit float of NVFP4 elements: bit 3 sign, bits 2..1 exponent
+ * (bias 1), bit 0 mantissa.  Exponent 0 is subnormal: m * 2^-1.  Otherwise
+ * 2^(e-1) * (1 + m/2).  No infinities, no NaN. */
+double oracle_e2m1_to_double(int code)
+{
+    int sgn = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double mag = e == 0 ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return sgn ? -mag : mag;
+}
+
+/* E4M3 (the variant without infinities), the 8-bit float of NVFP4 block
+ * scales: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0 mantissa.
+ * Exponent 0 is subnormal: (m/8) * 2^-6.  Otherwise 2^(e-7) * (1 + m/8).
+ * Exponent 15 with mantissa 7 is NaN. */
+double oracle_e4m3_to_double(int code)
+{
+    int sgn = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -mag : mag;
+}
+
+/* Dequantise one row of an NVFP4 matrix into fp64.
+ * codes_row: in_dim/2 bytes, element j in byte j/2, low nibble for even j
+ * (the packing of the 4-bit affine codes); s_row: in_dim/16 E4M3 bytes, one
+ * per block of 16 consecutive inputs; gscale: the matrix's fp32 scale.
+ * w_j = e2m1(q_j) * e4m3(s_{j/16}) * gscale, each factor exact in fp64 and
+ * the product too (2 + 4 + 24 significant bits). */
+void oracle_dequant_row_nvfp4(const uint8_t *codes_row, const uint8_t *s_row, float gscale, int in_dim,
+                              double *out)
+{
+    for (int j = 0; j < in_dim; ++j) {
+        uint8_t byte = codes_row[j / 2];
+        int q = (j % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+        out[j] = oracle_e2m1_to_double(q) * oracle_e4m3_to_double(s_row[j / ORACLE_NVFP4_BLOCK]) *
+                 (double)gscale;
+    }
+}
 
 /* --------------------------------------------------------------- router */
 
@@ -198,29 +246,44 @@ void oracle_shared_weight(const uint16_t *x, const uint16_t *v, int T, int H, fl
 
 /* ---------------------------------------------------------------- expert FFN */
 
+/* One expert matrix.  Affine: codes, scales, biases (bf16 [rows, cols/group]).
+ * NVFP4: codes, bscales (E4M3 [rows, cols/16]) and gscale (fp32, one value). */
 typedef struct {
     const uint8_t *codes;
     const uint16_t *scales;
     const uint16_t *biases;
+    const uint8_t *bscales;
+    const float *gscale;
 } oracle_qmat;
 
 /* Pointers to expert e's block of a stacked [n, rows, cols] matrix. */
-static oracle_qmat qmat_expert(oracle_qmat m, int e, int rows, int cols, int bits, int G)
+static oracle_qmat qmat_expert(const oracle_cfg *c, oracle_qmat m, int e, int rows, int cols)
 {
-    oracle_qmat r;
-    r.codes = m.codes + (size_t)e * rows * row_bytes(cols, bits);
-    r.scales = m.scales + (size_t)e * rows * (cols / G);
-    r.biases = m.biases + (size_t)e * rows * (cols / G);
+    oracle_qmat r = m;
+    if (c->format == 1) {
+        r.codes = m.codes + (size_t)e * rows * row_bytes(cols, 4);
+        r.bscales = m.bscales + (size_t)e * rows * (cols / ORACLE_NVFP4_BLOCK);
+        r.gscale = m.gscale + e;
+    } else {
+        r.codes = m.codes + (size_t)e * rows * row_bytes(cols, c->bits);
+        r.scales = m.scales + (size_t)e * rows * (cols / c->group);
+        r.biases = m.biases + (size_t)e * rows * (cols / c->group);
+    }
     return r;
 }
 
-/* y = W v for one dequantised [rows, cols] matrix; scratch holds cols doubles. */
-static void qmat_matvec(oracle_qmat m, int rows, int cols, int bits, int G, const double *v,
-                        double *y, double *scratch)
+/* y = W v for one dequantised [rows, cols] expert matrix; scratch holds cols doubles. */
+static void qmat_matvec(const oracle_cfg *c, oracle_qmat m, int rows, int cols, const double *v, double *y,
+                        double *scratch)
 {
+    const int G = c->group, bits = c->bits;
     for (int r = 0; r < rows; ++r) {
-        oracle_dequant_row(m.codes + (size_t)r * row_bytes(cols, bits), m.scales + (size_t)r * (cols / G),
-                           m.biases + (size_t)r * (cols / G), bits, cols, G, scratch);
+        if (c->format == 1)
+            oracle_dequant_row_nvfp4(m.codes + (size_t)r * row_bytes(cols, 4),
+                                     m.bscales + (size_t)r * (cols / ORACLE_NVFP4_BLOCK), *m.gscale, cols, scratch);
+        else
+            oracle_dequant_row(m.codes + (size_t)r * row_bytes(cols, bits), m.scales + (size_t)r * (cols / G),
+                               m.biases + (size_t)r * (cols / G), bits, cols, G, scratch);
         double acc = 0.0;
         for (int j = 0; j < cols; ++j) acc += scratch[j] * v[j];
         y[r] = acc;
@@ -231,34 +294,47 @@ static void qmat_matvec(oracle_qmat m, int rows, int cols, int bits, int G, cons
  *   g = Wg x, u = Wu x   ([I]),  h = silu(g) * u = g / (1 + exp(-g)) * u,
  *   y = Wd h             ([H]).
  * h_out (optional) receives h.  gate/up are [I, H], down is [H, I]. */
-void oracle_expert_ffn(const oracle_cfg *c, const uint8_t *g_codes, const uint16_t *g_s,
-                       const uint16_t *g_b, const uint8_t *u_codes, const uint16_t *u_s,
-                       const uint16_t *u_b, const uint8_t *d_codes, const uint16_t *d_s,
-                       const uint16_t *d_b, const double *x, double *h_out, double *y)
+void oracle_expert_ffn_m(const oracle_cfg *c, const oracle_qmat *mg, const oracle_qmat *mu,
+                         const oracle_qmat *md, const double *x, double *h_out, double *y)
 {
-    const int H = c->hidden, I = c->inter, G = c->group, bits = c->bits;
+    const int H = c->hidden, I = c->inter;
     double *scratch = (double *)malloc(sizeof(double) * (size_t)(H > I ? H : I));
     double *g = (double *)malloc(sizeof(double) * (size_t)I);
     double *u = (double *)malloc(sizeof(double) * (size_t)I);
-    oracle_qmat mg = {g_codes, g_s, g_b}, mu = {u_codes, u_s, u_b}, md = {d_codes, d_s, d_b};
-    qmat_matvec(mg, I, H, bits, G, x, g, scratch);
-    qmat_matvec(mu, I, H, bits, G, x, u, scratch);
+    qmat_matvec(c, *mg, I, H, x, g, scratch);
+    qmat_matvec(c, *mu, I, H, x, u, scratch);
     for (int i = 0; i < I; ++i) g[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
     if (h_out) memcpy(h_out, g, sizeof(double) * (size_t)I);
-    qmat_matvec(md, H, I, bits, G, g, y, scratch);
+    qmat_matvec(c, *md, H, I, g, y, scratch);
     free(scratch);
     free(g);
     free(u);
 }
 
+/* The same with the affine matrices given by their arrays. */
+void oracle_expert_ffn(const oracle_cfg *c, const uint8_t *g_codes, const uint16_t *g_s,
+                       const uint16_t *g_b, const uint8_t *u_codes, const uint16_t *u_s,
+                       const uint16_t *u_b, const uint8_t *d_codes, const uint16_t *d_s,
+                       const uint16_t *d_b, const double *x, double *h_out, double *y)
+{
+    oracle_qmat mg = {g_codes, g_s, g_b, NULL, NULL}, mu = {u_codes, u_s, u_b, NULL, NULL},
+                md = {d_codes, d_s, d_b, NULL, NULL};
+    oracle_expert_ffn_m(c, &mg, &mu, &md, x, h_out, y);
+}
+
 /* Down projection alone, for staged checks: y = Wd h with h given. */
+void oracle_expert_down_m(const oracle_cfg *c, const oracle_qmat *md, const double *h, double *y)
+{
+    double *scratch = (double *)malloc(sizeof(double) * (size_t)c->inter);
+    qmat_matvec(c, *md, c->hidden, c->inter, h, y, scratch);
+    free(scratch);
+}
+
 void oracle_expert_down(const oracle_cfg *c, const uint8_t *d_codes, const uint16_t *d_s,
                         const uint16_t *d_b, const double *h, double *y)
 {
-    double *scratch = (double *)malloc(sizeof(double) * (size_t)c->inter);
-    oracle_qmat md = {d_codes, d_s, d_b};
-    qmat_matvec(md, c->hidden, c->inter, c->bits, c->group, h, y, scratch);
-    free(scratch);
+    oracle_qmat md = {d_codes, d_s, d_b, NULL, NULL};
+    oracle_expert_down_m(c, &md, h, y);
 }
 
 /* ---------------------------------------------------------------- layer */
@@ -277,7 +353,7 @@ int oracle_forward(const oracle_cfg *c, const oracle_weights *w, const uint16_t 
                    const float *bias, const float *logits_in, uint16_t *y, double *y_exact,
                    int32_t *ids_out, uint16_t *p_out, uint16_t *ws_out, float *logits_out)
 {
-    const int H = c->hidden, I = c->inter, E = c->n_experts, k = c->top_k, G = c->group;
+    const int H = c->hidden, I = c->inter, E = c->n_experts, k = c->top_k;
     if (T <= 0) return 0;
     float *logits = (float *)malloc(sizeof(float) * (size_t)T * E);
     int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k);
@@ -306,9 +382,9 @@ int oracle_forward(const oracle_cfg *c, const oracle_weights *w, const uint16_t 
                 double weight;
                 if (j < k) {
                     int e = ids[(size_t)t * k + j];
-                    mg = qmat_expert(w->gate, e, I, H, c->bits, G);
-                    mu = qmat_expert(w->up, e, I, H, c->bits, G);
-                    md = qmat_expert(w->down, e, H, I, c->bits, G);
+                    mg = qmat_expert(c, w->gate, e, I, H);
+                    mu = qmat_expert(c, w->up, e, I, H);
+                    md = qmat_expert(c, w->down, e, H, I);
                     weight = oracle_bf16_to_double(p[(size_t)t * k + j]);
                 } else {
                     mg = w->s_gate;
@@ -316,8 +392,7 @@ int oracle_forward(const oracle_cfg *c, const oracle_weights *w, const uint16_t 
                     md = w->s_down;
                     weight = oracle_bf16_to_double(ws[t]);
                 }
-                oracle_expert_ffn(c, mg.codes, mg.scales, mg.biases, mu.codes, mu.scales, mu.biases,
-                                  md.codes, md.scales, md.biases, xd, NULL, ye);
+                oracle_expert_ffn_m(c, &mg, &mu, &md, xd, NULL, ye);
                 for (int h = 0; h < H; ++h) acc[h] += weight * ye[h];
             }
             for (int h = 0; h < H; ++h) {

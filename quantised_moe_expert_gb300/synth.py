@@ -13,7 +13,10 @@ storage format is the MLX affine rule quoted in the same proposal (experts at
 4 bits in groups of 64, router at 8 bits): a group of 64 consecutive inputs of
 one output row shares one bf16 scale and one bf16 bias.  The same page's slice
 "8-bit experts" names the variant with 8-bit expert codes (same rule, q in
-0..255); the WORKLOADS_B8 list draws it.
+0..255); the WORKLOADS_B8 list draws it.  WORKLOADS_NVFP4 draws the
+block-scaled variant: experts in NVFP4, the checkpoint format named on the
+"Qwen-3.6-35B-A3B-SIQ-K6-K4K3" model card (4-bit E2M1 codes, one E4M3 scale
+per 16 inputs of a row, one fp32 scale per matrix; router unchanged).
 
 Storage layout (all little-endian, rows dense):
   x        bf16 bits, uint16 [T, H]
@@ -24,6 +27,9 @@ Storage layout (all little-endian, rows dense):
            scales/biases uint16 [E, I, H/64]
   down     codes uint8 [E, H, I/2] (8-bit: [E, H, I]), scales/biases uint16 [E, H, I/64]
   s_gate, s_up, s_down: the shared expert, same layouts with a leading dim of 1
+  NVFP4 experts: codes as the 4-bit codes (E2M1: bit 3 sign, bits 2-1 exponent,
+           bit 0 mantissa), scales uint8 E4M3 [E, rows, in/16], no biases (an
+           empty array), gscale float32 [E] (one per matrix)
 """
 from __future__ import annotations
 
@@ -45,6 +51,7 @@ class LayerShape:
     bits: int = 4
     router_bits: int = 8
     group: int = GROUP
+    fmt: str = "affine"        # "affine" (MLX, bits 4 or 8) or "nvfp4" (bits 4)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -60,6 +67,7 @@ class Workload:
 
 QWEN_SHAPE = LayerShape(hidden=2048, inter=512, n_experts=256, top_k=8)
 QWEN_SHAPE_B8 = dataclasses.replace(QWEN_SHAPE, bits=8)
+QWEN_SHAPE_NVFP4 = dataclasses.replace(QWEN_SHAPE, fmt="nvfp4")
 TINY_SHAPE = LayerShape(hidden=256, inter=64, n_experts=16, top_k=2)
 
 WORKLOADS = [
@@ -76,6 +84,14 @@ WORKLOADS_B8 = [
     Workload("decode_T1_H2048_E256_k8_b8", QWEN_SHAPE_B8, 1, seed=11),
     Workload("decode_T16_H2048_E256_k8_b8", QWEN_SHAPE_B8, 16, seed=12),
     Workload("prefill_T512_H2048_E256_k8_b8", QWEN_SHAPE_B8, 512, seed=13),
+]
+
+
+# The same layer with NVFP4 experts (router unchanged).
+WORKLOADS_NVFP4 = [
+    Workload("decode_T1_H2048_E256_k8_nvfp4", QWEN_SHAPE_NVFP4, 1, seed=21),
+    Workload("decode_T16_H2048_E256_k8_nvfp4", QWEN_SHAPE_NVFP4, 16, seed=22),
+    Workload("prefill_T512_H2048_E256_k8_nvfp4", QWEN_SHAPE_NVFP4, 512, seed=23),
 ]
 
 
@@ -96,7 +112,8 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 class QMat:
     codes: np.ndarray    # uint8 [..., rows, in*bits/8]
     scales: np.ndarray   # uint16 [..., rows, in/64]
-    biases: np.ndarray   # uint16 [..., rows, in/64]
+    biases: np.ndarray   # uint16 [..., rows, in/64] (NVFP4: empty)
+    gscale: np.ndarray | None = None   # NVFP4: float32 [...], one per matrix
 
 
 @dataclasses.dataclass
@@ -114,7 +131,7 @@ class LayerWeights:
     def nbytes(self) -> int:
         tot = self.shared_gate_vec.nbytes
         for m in (self.router, self.gate, self.up, self.down, self.s_gate, self.s_up, self.s_down):
-            tot += m.codes.nbytes + m.scales.nbytes + m.biases.nbytes
+            tot += m.codes.nbytes + m.scales.nbytes + m.biases.nbytes + (0 if m.gscale is None else m.gscale.nbytes)
         return tot
 
 
@@ -137,6 +154,18 @@ def _expert_qmat8(rng: np.random.Generator, n: int, rows: int, cols: int) -> QMa
     # -128 * s is exact in bf16 (power-of-two scaling of a bf16 value).
     b = f32_to_bf16_bits(-128.0 * bf16_bits_to_f32(s))
     return QMat(codes, s, b)
+
+
+def _expert_qmat_nvfp4(rng: np.random.Generator, n: int, rows: int, cols: int) -> QMat:
+    """NVFP4: E2M1 codes uniform over all 16 (so -0 too); E4M3 block scales with exponent field
+    uniform in 9..13 and mantissa uniform (values 4 to 120, never NaN); per-matrix fp32 scale
+    ~ U(3e-4, 6e-4).  |w| up to about 0.4, mean about 0.04, near the affine draws' spread."""
+    codes = rng.integers(0, 256, size=(n, rows, cols // 2), dtype=np.uint8)
+    e = rng.integers(9, 14, size=(n, rows, cols // 16), dtype=np.uint8)
+    m = rng.integers(0, 8, size=(n, rows, cols // 16), dtype=np.uint8)
+    scales = ((e << 3) | m).astype(np.uint8)
+    g = rng.uniform(3e-4, 6e-4, size=(n,)).astype(np.float32)
+    return QMat(codes, scales, np.zeros((n, rows, 0), dtype=np.uint16), g)
 
 
 def _quantise_8bit(w: np.ndarray) -> QMat:
@@ -163,11 +192,12 @@ def _quantise_8bit(w: np.ndarray) -> QMat:
 def make_weights(shape: LayerShape, seed: int) -> LayerWeights:
     """Draw one layer's weights.  Draw order: router, v, gate, up, down, shared gate/up/down."""
     assert shape.bits in (4, 8) and shape.router_bits == 8 and shape.group == GROUP
+    assert shape.fmt in ("affine", "nvfp4") and (shape.fmt == "affine" or shape.bits == 4)
     H, I, E = shape.hidden, shape.inter, shape.n_experts
     rng = np.random.default_rng([seed, 1])
     router = _quantise_8bit(rng.normal(0.0, 0.02, size=(E, H)).astype(np.float32))
     v = f32_to_bf16_bits(rng.normal(0.0, 0.02, size=(H,)).astype(np.float32))
-    qmat = _expert_qmat8 if shape.bits == 8 else _expert_qmat
+    qmat = _expert_qmat_nvfp4 if shape.fmt == "nvfp4" else _expert_qmat8 if shape.bits == 8 else _expert_qmat
     gate = qmat(rng, E, I, H)
     up = qmat(rng, E, I, H)
     down = qmat(rng, E, H, I)
@@ -216,9 +246,13 @@ def workload_inputs(wl: Workload, stream: int = 0):
 
 
 def active_expert_bytes(shape: LayerShape) -> int:
-    """Bytes of one expert's gate+up+down codes, scales and biases."""
+    """Bytes of one expert's gate+up+down codes, scales and biases (NVFP4: codes, block scales and
+    the per-matrix scale)."""
     H, I = shape.hidden, shape.inter
-    per = lambda rows, cols: rows * cols * shape.bits // 8 + 2 * 2 * rows * (cols // GROUP)
+    if shape.fmt == "nvfp4":
+        per = lambda rows, cols: rows * cols // 2 + rows * (cols // 16) + 4
+    else:
+        per = lambda rows, cols: rows * cols * shape.bits // 8 + 2 * 2 * rows * (cols // GROUP)
     return 2 * per(I, H) + per(H, I)
 
 
@@ -238,6 +272,6 @@ def nominal_tokens_per_expert(wl: Workload) -> float:
 
 
 if __name__ == "__main__":
-    for wl in WORKLOADS + WORKLOADS_B8:
+    for wl in WORKLOADS + WORKLOADS_B8 + WORKLOADS_NVFP4:
         print(wl.name, active_expert_bytes(wl.shape), router_bytes(wl.shape),
               expert_flops_per_token(wl.shape), math.ceil(nominal_tokens_per_expert(wl)))
