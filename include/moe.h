@@ -22,6 +22,13 @@
  * Code layout: a row of n inputs holds n * bits / 8 bytes; at 4 bits input j
  * is the low nibble of byte j / 2 for even j and the high nibble for odd j,
  * at 8 bits input j is byte j.
+ * Block-scaled experts (moe_config.format = MOE_FORMAT_NVFP4): every expert
+ * matrix, shared included, in NVFP4, the checkpoint format named on the model
+ * card "Qwen-3.6-35B-A3B-SIQ-K6-K4K3" (served there by a fused FP4 MoE
+ * backend); the router stays 8-bit affine.  w_j = e2m1(q_j) * e4m3(s_b) * g
+ * with q_j a 4-bit E2M1 code (bit 3 sign, bits 2..1 exponent with bias 1,
+ * bit 0 mantissa; packed as the 4-bit affine codes), s_b the E4M3 scale of
+ * the block of 16 consecutive inputs holding j, g the matrix's fp32 scale.
  *
  * Conventions shared by every entry point
  *   - Every function returns an int status (enum moe_status).  Argument,
@@ -59,6 +66,10 @@
  *   codes   4-bit: uint8 [rows, in/2], element j of a row in byte j/2, low
  *           nibble for even j.  8-bit: uint8 [rows, in].
  *   scales, biases: bf16 [rows, in/group].
+ *   NVFP4 experts: codes as the 4-bit codes; scales holds E4M3 bytes
+ *           [rows, in/16] (passed through the scales pointer); biases unused
+ *           (may be NULL); gscale fp32, one per matrix ([E] for a stack).
+ *           A NaN scale code (0x7F, 0xFF) makes the rows it scales undefined.
  *   Stacked expert matrices add a leading expert dimension:
  *     gate, up   [E, inter, hidden]     down  [E, hidden, inter]
  *     s_gate, s_up [inter, hidden]      s_down [hidden, inter]   (shared expert)
@@ -97,8 +108,8 @@ enum moe_path {
     MOE_PATH_PREFILL = 2   /* tcgen05 grouped GEMM kernels (any T >= 1) */
 };
 
-/* Layer shape and per-call options.  Supported: group == 64, bits == 4 or 8,
- * router_bits == 8, hidden and inter multiples of 64 (hidden <= 8192,
+/* Layer shape and per-call options.  Supported: group == 64, bits == 4 or 8
+ * (4 with format == MOE_FORMAT_NVFP4), router_bits == 8, hidden and inter multiples of 64 (hidden <= 8192,
  * inter <= 4096), 1 <= top_k <= min(n_experts, 16), 1 <= n_experts <= 256,
  * has_shared in {0,1}.  Anything else returns MOE_ERR_UNSUPPORTED.
  * wait_polls bounds the in-kernel waits of the call: a wait polls at most
@@ -112,8 +123,15 @@ enum moe_path {
  * limit never leaves the copy ring in mid-flight.
  * With bits == 8 the decode path runs the weight-streaming gate/up, down and
  * reduce kernels after the routing kernels (the fused decode kernel and the
- * packed down layout are for 4-bit codes), and the prefill path runs every
- * expert on the tensor-memory GEMMs. */
+ * packed down layout are for 4-bit affine codes), and the prefill path runs
+ * every expert on the tensor-memory GEMMs.  NVFP4 experts take the prefill
+ * path at every T (MOE_PATH_DECODE and MOE_PATH_AUTO select it too). */
+/* Expert storage formats (moe_config.format). */
+enum moe_format {
+    MOE_FORMAT_AFFINE = 0,  /* MLX affine, bits 4 or 8, groups of 64 */
+    MOE_FORMAT_NVFP4 = 1    /* E2M1 codes, E4M3 scale per 16 inputs, fp32 per matrix; bits == 4 */
+};
+
 typedef struct moe_config {
     int hidden;       /* H */
     int inter;        /* I, intermediate size of every expert, shared included */
@@ -124,13 +142,16 @@ typedef struct moe_config {
     int router_bits;  /* router code width */
     int has_shared;   /* 1: the layer has a shared expert slot */
     int wait_polls;   /* bound on the in-kernel waits of the call; 0 = default */
+    int format;       /* expert storage format, enum moe_format (0 = affine) */
 } moe_config;
 
-/* One affine-quantised matrix (or a stack of them), device pointers. */
+/* One quantised matrix (or a stack of them), device pointers, 16-byte aligned
+ * (gscale: 4-byte aligned). */
 typedef struct moe_qmat {
     const uint8_t *codes;
-    const uint16_t *scales;  /* bf16 */
-    const uint16_t *biases;  /* bf16 */
+    const uint16_t *scales;  /* affine: bf16; NVFP4: E4M3 bytes */
+    const uint16_t *biases;  /* affine: bf16; NVFP4: unused */
+    const float *gscale;     /* NVFP4: fp32 scale per matrix; affine: unused */
 } moe_qmat;
 
 /* All weights of one layer, device pointers.  s_* and shared_gate_vec may be

@@ -30,6 +30,9 @@ MOE_PATH_AUTO = 0
 MOE_PATH_DECODE = 1
 MOE_PATH_PREFILL = 2
 
+MOE_FORMAT_AFFINE = 0
+MOE_FORMAT_NVFP4 = 1
+
 EXPORTED = ("moe_status_string", "moe_check_config", "moe_workspace_size", "moe_route", "moe_permute",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status", "moe_pack_down",
             "moe_expert_stages",
@@ -45,11 +48,12 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("hidden", "inter", "n_experts", "top_k", "group", "bits", "router_bits", "has_shared",
-                 "wait_polls")]
+                 "wait_polls", "format")]
 
 
 class moe_qmat(ctypes.Structure):
-    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p)]
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("gscale", ctypes.c_void_p)]
 
 
 class moe_weights(ctypes.Structure):
@@ -132,8 +136,13 @@ def _check(fn: str, rc: int):
 
 def config_of(shape, wait_polls: int = 0) -> moe_config:
     """moe_config from any object with the layer-shape attributes (e.g. synth.LayerShape)."""
+    fmt = MOE_FORMAT_NVFP4 if getattr(shape, "fmt", "affine") == "nvfp4" else MOE_FORMAT_AFFINE
     return moe_config(shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.group, shape.bits,
-                      shape.router_bits, shape.has_shared, wait_polls)
+                      shape.router_bits, shape.has_shared, wait_polls, fmt)
+
+
+def _ptr(t):
+    return None if t is None or t.numel() == 0 else t.data_ptr()
 
 
 class DeviceLayer:
@@ -160,12 +169,13 @@ class DeviceLayer:
             c = up(name + ".codes", m.codes)
             s = up(name + ".scales", m.scales)
             b = up(name + ".biases", m.biases)
-            return moe_qmat(c.data_ptr(), s.data_ptr(), b.data_ptr())
+            g = None if m.gscale is None else up(name + ".gscale", m.gscale)
+            return moe_qmat(c.data_ptr(), s.data_ptr(), _ptr(b), _ptr(g))
 
         self.w = moe_weights(q("router", host.router), q("gate", host.gate), q("up", host.up),
                              q("down", host.down), q("s_gate", host.s_gate), q("s_up", host.s_up),
                              q("s_down", host.s_down), up("v", host.shared_gate_vec).data_ptr(), None, None)
-        if pack and host.shape.bits == 4:
+        if pack and host.shape.bits == 4 and getattr(host.shape, "fmt", "affine") == "affine":
             self.pack()
 
     def pack(self):
@@ -195,7 +205,7 @@ class DeviceLayer:
 
         def q(name):
             return moe_qmat(tensors[name + ".codes"].data_ptr(), tensors[name + ".scales"].data_ptr(),
-                            tensors[name + ".biases"].data_ptr())
+                            _ptr(tensors[name + ".biases"]), _ptr(tensors.get(name + ".gscale")))
         opt = lambda name: tensors[name].data_ptr() if name in tensors else None
         obj.w = moe_weights(q("router"), q("gate"), q("up"), q("down"), q("s_gate"), q("s_up"), q("s_down"),
                             tensors["v"].data_ptr(), opt("down.packed"), opt("s_down.packed"))

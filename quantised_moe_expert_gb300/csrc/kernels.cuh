@@ -78,9 +78,14 @@ struct WorklistArgs {
 // One expert matrix stack as the expert kernels see it.
 struct QMatDev {
     const uint8_t *codes;
-    const uint16_t *scales;
+    const uint16_t *scales;       // NVFP4: E4M3 block scales, read as bytes
     const uint16_t *biases;
+    const float *gscale;          // NVFP4: fp32 scale per matrix
 };
+
+// Value of the args' `bits` field for NVFP4 experts (4-bit E2M1 codes, E4M3 scale per 16 inputs,
+// fp32 scale per matrix); 4 and 8 are the affine code widths.
+constexpr int kNvfp4 = 5;
 
 struct ExpertArgs {
     const uint16_t *x;            // bf16 [T, H]
@@ -98,7 +103,7 @@ struct ExpertArgs {
     float *acc;                   // f32 [T, H]
     int *status;
     int T, H, I, E, k, has_shared;
-    int bits;                     // expert code width: 4 or 8
+    int bits;                     // expert codes: 4 or 8 (affine), kNvfp4
     int max_items;
 };
 
@@ -128,7 +133,7 @@ struct PrefillArgs {
                                   // expert-sorted position order (every element of the slots present written once)
     int *status;
     int T, H, I, E, k, has_shared, max_w1, max_w2;
-    int bits;                     // expert code width: 4 or 8
+    int bits;                     // expert codes: 4 or 8 (affine), kNvfp4
     long long wait_limit;
 };
 

@@ -14,15 +14,21 @@ long long wait_limit_of(const moe_config &c) { return c.wait_polls > 0 ? (long l
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned16_or_null(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool qmat_ok(const moe_qmat &m)
+bool qmat_ok(const moe_qmat &m, bool nvfp4 = false)
 {
+    if (nvfp4)
+        return aligned16(m.codes) && aligned16(m.scales) && m.gscale &&
+               (reinterpret_cast<uintptr_t>(m.gscale) & 3u) == 0;
     return aligned16(m.codes) && aligned16(m.scales) && aligned16(m.biases);
 }
+
+// The args' code field: the affine code width, or kNvfp4.
+int qcode(const moe_config &c) { return c.format == MOE_FORMAT_NVFP4 ? kNvfp4 : c.bits; }
 
 template <typename T>
 T *ws_at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
 
-QMatDev dev(const moe_qmat &m) { return QMatDev{m.codes, m.scales, m.biases}; }
+QMatDev dev(const moe_qmat &m) { return QMatDev{m.codes, m.scales, m.biases, m.gscale}; }
 
 int check_common(const moe_config *cfg, int T)
 {
@@ -43,8 +49,11 @@ int check_ws(const moe_config *cfg, int T, void *ws, size_t ws_bytes, WsLayout *
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-int resolve_path(int path, int T)
+// NVFP4 experts run on the tensor-memory GEMMs at every T (the weight-streaming decode kernels take
+// affine codes).
+int resolve_path(const moe_config &c, int path, int T)
 {
+    if (c.format == MOE_FORMAT_NVFP4) return MOE_PATH_PREFILL;
     if (path == MOE_PATH_AUTO) return T <= kDecodeMaxTok ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
     return path;
 }
@@ -134,7 +143,7 @@ PermuteArgs permute_args(const moe_config &c, const int32_t *ids, int T, int32_t
     pa.nblk = L.nblk;
     pa.has_shared = c.has_shared;
     pa.build_work = 1;
-    pa.small_tiles = prefill_small_fits(c.hidden, c.inter, c.bits) ? 1 : 0;
+    pa.small_tiles = prefill_small_fits(c.hidden, c.inter, qcode(c)) ? 1 : 0;
     pa.max_items[0] = L.max_wd;
     pa.max_items[1] = L.max_w1;
     pa.max_items[2] = L.max_w2;
@@ -171,7 +180,7 @@ ExpertArgs expert_args(const moe_config &c, const moe_weights &w, const uint16_t
     ea.E = c.n_experts;
     ea.k = c.top_k;
     ea.has_shared = c.has_shared;
-    ea.bits = c.bits;
+    ea.bits = qcode(c);
     return ea;
 }
 
@@ -246,7 +255,7 @@ int enqueue_prefill_experts(const moe_config &c, const ExpertArgs &ea, const WsL
     a.has_shared = c.has_shared;
     a.max_w1 = L.max_w1;
     a.max_w2 = L.max_w2;
-    a.bits = c.bits;
+    a.bits = qcode(c);
     a.wait_limit = wait_limit_of(c);
     const int rc = cuda_rc(launch_prefill_experts(a, st));
     if (rc) return rc;
@@ -297,7 +306,7 @@ FusedDecodeArgs fused_args(const moe_config &c, const moe_weights &w, const uint
 
 bool fused_fits(const moe_config &c, int T)
 {
-    return c.bits == 4 && T >= 1 && T <= kDecodeMaxTok &&
+    return c.bits == 4 && c.format == MOE_FORMAT_AFFINE && T >= 1 && T <= kDecodeMaxTok &&
            decode_fused_fits(T, c.hidden, c.inter, c.n_experts, c.top_k, c.has_shared);
 }
 
@@ -307,8 +316,10 @@ bool weights_ok(const moe_config &c, const moe_weights *w, bool need_router, boo
     if (!aligned16_or_null(w->down_packed) || !aligned16_or_null(w->s_down_packed)) return false;
     if (need_router && !qmat_ok(w->router)) return false;
     if (need_experts) {
-        if (!qmat_ok(w->gate) || !qmat_ok(w->up) || !qmat_ok(w->down)) return false;
-        if (c.has_shared && (!qmat_ok(w->s_gate) || !qmat_ok(w->s_up) || !qmat_ok(w->s_down))) return false;
+        const bool nv = c.format == MOE_FORMAT_NVFP4;
+        if (!qmat_ok(w->gate, nv) || !qmat_ok(w->up, nv) || !qmat_ok(w->down, nv)) return false;
+        if (c.has_shared && (!qmat_ok(w->s_gate, nv) || !qmat_ok(w->s_up, nv) || !qmat_ok(w->s_down, nv)))
+            return false;
     }
     return true;
 }
@@ -336,6 +347,7 @@ int moe_check_config(const moe_config *c)
     if (!c) return MOE_ERR_INVALID_ARG;
     if (c->hidden <= 0 || c->inter <= 0 || c->n_experts <= 0 || c->top_k <= 0) return MOE_ERR_INVALID_ARG;
     if (c->group != kGroup || (c->bits != 4 && c->bits != 8) || c->router_bits != 8) return MOE_ERR_UNSUPPORTED;
+    if (c->format != MOE_FORMAT_AFFINE && !(c->format == MOE_FORMAT_NVFP4 && c->bits == 4)) return MOE_ERR_UNSUPPORTED;
     if (c->hidden % 64 || c->inter % 64 || c->hidden > 8192 || c->inter > 4096) return MOE_ERR_UNSUPPORTED;
     if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->top_k > c->n_experts) return MOE_ERR_UNSUPPORTED;
     if (c->has_shared != 0 && c->has_shared != 1) return MOE_ERR_UNSUPPORTED;
@@ -423,11 +435,11 @@ int moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const uint16_t *
     wa.T = T;
     wa.E = cfg->n_experts;
     wa.has_shared = cfg->has_shared;
-    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter, cfg->bits) ? 1 : 0;
+    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter, qcode(*cfg)) ? 1 : 0;
     wa.max_items[0] = L.max_wd;
     wa.max_items[1] = L.max_w1;
     wa.max_items[2] = L.max_w2;
-    const int rp = resolve_path(path, T);
+    const int rp = resolve_path(*cfg, path, T);
     if (rp == MOE_PATH_DECODE && fused_fits(*cfg, T)) {
         FusedDecodeArgs fa = fused_args(*cfg, *w, x, T, L, ws);
         fa.ids_in = ids;
@@ -468,7 +480,7 @@ int moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x, 
     WsLayout L;
     if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
     if (T == 0) return MOE_OK;
-    const int rp = resolve_path(path, T);
+    const int rp = resolve_path(*cfg, path, T);
     auto st = static_cast<cudaStream_t>(stream);
     if (rp == MOE_PATH_DECODE && fused_fits(*cfg, T)) {
         // the whole layer in one cooperative launch
@@ -524,7 +536,7 @@ int moe_pack_down(const moe_config *cfg, const moe_weights *w, uint8_t *down_pac
     if (rc) return rc;
     if (!w || !aligned16(w->down.codes) || !aligned16(down_packed) || !aligned16_or_null(s_down_packed))
         return MOE_ERR_INVALID_ARG;
-    if (cfg->inter % kDecodeSlice || cfg->bits != 4) return MOE_ERR_UNSUPPORTED;
+    if (cfg->inter % kDecodeSlice || cfg->bits != 4 || cfg->format != MOE_FORMAT_AFFINE) return MOE_ERR_UNSUPPORTED;
     auto st = static_cast<cudaStream_t>(stream);
     rc = cuda_rc(launch_pack_down(w->down.codes, down_packed, cfg->n_experts, cfg->hidden, cfg->inter, st));
     if (rc || !cfg->has_shared || !s_down_packed) return rc;
@@ -546,7 +558,7 @@ int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_
     if ((rc = check_ws(cfg, T, ws, ws_bytes, &L))) return rc;
     if (T == 0 || (!h_out && !yslot_out)) return MOE_OK;
     auto st = static_cast<cudaStream_t>(stream);
-    const int rp = resolve_path(path, T);
+    const int rp = resolve_path(*cfg, path, T);
     if (rp == MOE_PATH_DECODE && fused_fits(*cfg, T)) {
         FusedDecodeArgs fa = fused_args(*cfg, *w, x, T, L, ws);
         fa.ids_in = ids;
@@ -571,7 +583,7 @@ int moe_expert_stages(const moe_config *cfg, const moe_weights *w, const uint16_
     wa.T = T;
     wa.E = cfg->n_experts;
     wa.has_shared = cfg->has_shared;
-    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter, cfg->bits) ? 1 : 0;
+    wa.small_tiles = prefill_small_fits(cfg->hidden, cfg->inter, qcode(*cfg)) ? 1 : 0;
     wa.max_items[0] = L.max_wd;
     wa.max_items[1] = L.max_w1;
     wa.max_items[2] = L.max_w2;

@@ -36,6 +36,14 @@
 // a 32-bit word of 8 nibbles into four fp16 pairs.  x16 and h are written in
 // the same order, so every product still pairs w_j with x_j.
 //
+// NVFP4 experts (E2M1 codes, an E4M3 scale per 16 inputs, an fp32 scale per
+// matrix).  The code tiles are those of the 4-bit codes.  A K-step's four block
+// scales of a row arrive through the same private scale buffer (4 bytes a group
+// in place of the bf16 scale and bias), each code word is expanded by the
+// hardware E2M1 -> fp16 conversion and multiplied by its block's scale in fp16
+// (exact: at most 6 significant bits in [2^-10, 2688]), and the matrix scale is
+// applied to the fp32 accumulators in the epilogues.
+//
 // Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT, the
 // CTA drains its in-flight copies and MMAs, frees its TMEM and returns.
 #include <algorithm>
@@ -59,7 +67,8 @@ constexpr int kStagesA2 = 3, kStagesB2 = 3, kCodeStages2 = 6;   // down:    16 K
 constexpr int kCodeStages1B8 = 3, kCodeStages2B8 = 3;           // 8-bit codes: 16 KB / 8 KB per stage
 
 // Bytes of one row's codes per K-step, and of one code stage of each GEMM (gate | up; down).
-constexpr int code_row_bytes(int bits) { return 8 * bits; }
+constexpr int cbits(int bits) { return bits == kNvfp4 ? 4 : bits; }   // code width of the args' code field
+constexpr int code_row_bytes(int bits) { return 8 * cbits(bits); }
 constexpr int code_stage1(int bits) { return 2 * 128 * code_row_bytes(bits); }
 constexpr int code_stage2(int bits) { return 128 * code_row_bytes(bits); }
 constexpr int kRedCols = 16, kRedBufs = 2;   // down epilogue: columns per store chunk, chunk buffers per team
@@ -93,6 +102,7 @@ struct G1Params {
     const uint8_t *gc, *uc, *sgc, *suc;    // int4 codes (routed [E, I, H/2], shared [I, H/2]), for L2 prefetch
     const uint16_t *gs, *gb, *us, *ub;     // routed gate/up scales, biases [E, I, H/64]
     const uint16_t *sgs, *sgb, *sus, *sub; // shared expert [I, H/64]
+    const float *ggs, *ugs, *sggs, *sugs;  // NVFP4: matrix scales (routed [E], shared [1])
     int *status;
     int T, H, I, E, k;
     int async_scales;                  // 1: scale rows are 16-byte aligned (H % 512 == 0), fetched with cp.async
@@ -110,6 +120,7 @@ struct G2Params {
     const uint8_t *dc, *sdc;           // int4 codes (routed [E, H, I/2], shared [H, I/2]), for L2 prefetch
     const uint16_t *ds, *db;           // routed down scales, biases [E, H, I/64]
     const uint16_t *sds, *sdb;         // shared [H, I/64]
+    const float *dgs, *sdgs;           // NVFP4: matrix scales (routed [E], shared [1])
     int *status;
     int T, H, I, E, k;
     int async_scales;                  // 1: scale rows are 16-byte aligned (I % 512 == 0), fetched with cp.async
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
 {
     const int H = P.H, I = P.I, G = H / kGroup, nk = G, MB = (I + 127) / 128, Tk = P.T * P.k;
     constexpr int CB = code_row_bytes(BITS), CST = code_stage1(BITS);
-    const size_t crow = (size_t)H * BITS / 8;            // bytes of one weight row's codes
+    const size_t crow = (size_t)H * cbits(BITS) / 8;     // bytes of one weight row's codes
     const int ntiles = __ldg(P.nwork + 3) * MB;          // the big items lead the list
     // This grid may start while the small-tile gate/up GEMM still runs (programmatic
     // dependent launch): it reads nothing that grid writes, and every CTA waits for that
@@ -475,8 +486,13 @@ __global__ void __launch_bounds__(kThreads1, 1)
         const int nchunk = (G + kScaleChunk1 - 1) / kScaleChunk1;
         auto row_src = [&](const TileInfo &t, int c, const uint16_t *&ps, const uint16_t *&pb) -> size_t {
             ps = m == 0 ? (t.shared_e ? P.sgs : P.gs) : (t.shared_e ? P.sus : P.us);
+            const size_t row = (size_t)(t.shared_e ? 0 : t.expert) * I + (size_t)(t.mb * 128 + r);
+            if constexpr (BITS == kNvfp4) {            // 4 E4M3 bytes a group: groups 0-3 | 4-7 of the chunk
+                pb = ps + 8;
+                return row * (2 * G) + (size_t)c * 2 * kScaleChunk1;
+            }
             pb = m == 0 ? (t.shared_e ? P.sgb : P.gb) : (t.shared_e ? P.sub : P.ub);
-            return ((size_t)(t.shared_e ? 0 : t.expert) * I + (size_t)(t.mb * 128 + r)) * G + (size_t)c * kScaleChunk1;
+            return row * G + (size_t)c * kScaleChunk1;
         };
         auto fetch_chunk = [&](const TileInfo &t, int c, int buf) {     // one commit group per call
             if (t.mb * 128 + r < I) {
@@ -495,9 +511,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
             uint16_t v[2][kScaleChunk1];
 #pragma unroll
             for (int g = 0; g < kScaleChunk1; ++g) {
-                const bool in = row_ok && c * kScaleChunk1 + g < G;
-                v[0][g] = in ? ps[off + g] : (uint16_t)0;
-                v[1][g] = in ? pb[off + g] : (uint16_t)0;
+                // NVFP4: 16-bit slot g of a half holds bytes of group (4 half + g / 2) of the chunk
+                const bool in0 = row_ok && c * kScaleChunk1 + (BITS == kNvfp4 ? g / 2 : g) < G;
+                const bool in1 = row_ok && c * kScaleChunk1 + (BITS == kNvfp4 ? 4 + g / 2 : g) < G;
+                v[0][g] = in0 ? ps[off + g] : (uint16_t)0;
+                v[1][g] = in1 ? pb[off + g] : (uint16_t)0;
             }
             uint16_t *d = mysc + buf * 2 * kScaleChunk1;
 #pragma unroll
@@ -537,9 +555,18 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     const int gi = s & 7;
                     const uint32_t sw = gi < 4 ? (gi < 2 ? sreg.x : sreg.y) : (gi < 6 ? sreg.z : sreg.w);
                     const uint32_t bw = gi < 4 ? (gi < 2 ? breg.x : breg.y) : (gi < 6 ? breg.z : breg.w);
-                    const __half2 sc = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
-                    const __half2 sc16 = __hmul2(sc, __float2half2_rn(0.0625f));
-                    const __half2 bc = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
+                    __half2 sc, sc16, bc;
+                    uint32_t nvs[2];                   // NVFP4: block scales 0,1 | 2,3 of the group (fp16x2)
+                    if constexpr (BITS == kNvfp4) {
+                        const uint32_t w4 = gi < 4 ? (gi < 2 ? (gi == 0 ? sreg.x : sreg.y) : (gi == 2 ? sreg.z : sreg.w))
+                                                   : (gi < 6 ? (gi == 4 ? breg.x : breg.y) : (gi == 6 ? breg.z : breg.w));
+                        nvs[0] = nv_e4m3x2_f16(w4);
+                        nvs[1] = nv_e4m3x2_f16(w4 >> 16);
+                    } else {
+                        sc = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
+                        sc16 = __hmul2(sc, __float2half2_rn(0.0625f));
+                        bc = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
+                    }
                     const uint8_t *cbase = sC + cs * CST + m * (CST / 2);
                     // tcgen05.st / wait::st are warp-collective: the lanes left the polling loops
                     // above at different iterations, so reconverge first
@@ -548,7 +575,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     for (int hh = 0; hh < 2; ++hh) {           // inputs 32 hh .. 32 hh + 31
                         uint32_t av[16];
                         if (w_ok) {
-                            uint32_t cw[BITS];                 // the 32 inputs' codes
+                            uint32_t cw[cbits(BITS)];          // the 32 inputs' codes
                             if constexpr (BITS == 8) {
                                 const uint4 w0 = *reinterpret_cast<const uint4 *>(cbase + swz64(r, 2 * hh));
                                 const uint4 w1 = *reinterpret_cast<const uint4 *>(cbase + swz64(r, 2 * hh + 1));
@@ -562,6 +589,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
                             for (int cc = 0; cc < 4; ++cc) {
                                 uint4 d;
                                 if constexpr (BITS == 8) d = dequant8_b8(cw[2 * cc], cw[2 * cc + 1], sc, bc);
+                                else if constexpr (BITS == kNvfp4) d = nv_dequant8(cw[cc], nv_bcast(nvs[hh], cc >= 2));
                                 else d = dequant8(cw[cc], sc, sc16, bc);
                                 av[4 * cc] = d.x;
                                 av[4 * cc + 1] = d.y;
@@ -638,6 +666,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
             const int erow = ti.mb * 128 + quad * 32 + lane;
             const int hcol = kperm_pos(erow);
             const uint32_t d0 = tmem + lane_base;
+            float fg = 1.f, fu = 1.f;                     // NVFP4: the matrices' scales
+            if constexpr (BITS == kNvfp4) {
+                fg = __ldg(ti.shared_e ? P.sggs : P.ggs + ti.expert);
+                fu = __ldg(ti.shared_e ? P.sugs : P.ugs + ti.expert);
+            }
             if (16 * half >= N) {                             // no chunk of this parity: nothing to read
                 tc_fence_before();
                 mbar_arrive(smem_u32(tempty));
@@ -656,7 +689,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
                     for (int j = 0; j < 16; ++j) {
                         const int n = n0 + j;
                         if (n < ti.ntok) {
-                            const float g = __uint_as_float(gv[j]), u = __uint_as_float(uv[j]);
+                            const float g = __uint_as_float(gv[j]) * fg, u = __uint_as_float(uv[j]) * fu;
                             const int e = ce[n];
                             const __half hq = __float2half_rn(__fdividef(g * u, 1.f + __expf(-g * pow2f(e))));
                             P.hs[(size_t)(ti.pbase + n) * I + hcol] = __half_as_ushort(hq);
@@ -692,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     const int H = P.H, I = P.I, GI = I / kGroup, nk = GI, MB = (H + 127) / 128, Tk = P.T * P.k;
     constexpr int CB = code_row_bytes(BITS), CST = code_stage2(BITS);
-    const size_t crow = (size_t)I * BITS / 8;            // bytes of one weight row's codes
+    const size_t crow = (size_t)I * cbits(BITS) / 8;     // bytes of one weight row's codes
     const int ntiles = __ldg(P.nwork + 4) * MB;          // the big items lead the list
     // may start while the small-tile down GEMM still runs; waits for it before exiting
     if ((int)blockIdx.x >= ntiles) {
@@ -855,15 +888,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = tid & 127, half = tid >> 7;
         uint16_t *mysc = sScale + (size_t)tid * (4 * kScaleChunk1);   // [buffer][scale | bias][kScaleChunk1]
         const int nchunk = (GI + kScaleChunk1 - 1) / kScaleChunk1;
+        // NVFP4: 4 E4M3 bytes a group, groups 0-3 of a chunk in the scale half, 4-7 in the bias half
+        constexpr int kCw = BITS == kNvfp4 ? 2 : 1;    // 16-bit words a group
         auto src_of = [&](const TileInfo &t, const uint16_t *&ps, const uint16_t *&pb) -> size_t {
             ps = t.shared_e ? P.sds : P.ds;
-            pb = t.shared_e ? P.sdb : P.db;
-            return ((size_t)(t.shared_e ? 0 : t.expert) * H + (size_t)(t.mb * 128 + r)) * GI;
+            pb = BITS == kNvfp4 ? ps + 8 : (t.shared_e ? P.sdb : P.db);
+            return ((size_t)(t.shared_e ? 0 : t.expert) * H + (size_t)(t.mb * 128 + r)) * GI * kCw;
         };
         auto fetch_chunk = [&](const TileInfo &t, int c, int buf) {     // one commit group per call
             if (t.mb * 128 + r < H) {
                 const uint16_t *ps, *pb;
-                const size_t off = src_of(t, ps, pb) + (size_t)c * kScaleChunk1;
+                const size_t off = src_of(t, ps, pb) + (size_t)c * kScaleChunk1 * kCw;
                 uint16_t *d = mysc + buf * 2 * kScaleChunk1;
                 cp_async16(smem_u32(d), ps + off);
                 cp_async16(smem_u32(d + kScaleChunk1), pb + off);
@@ -873,13 +908,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load_chunk = [&](const TileInfo &t, int c, int buf) {      // the same with plain loads
             const bool row_ok = t.mb * 128 + r < H;
             const uint16_t *ps, *pb;
-            const size_t off = src_of(t, ps, pb) + (size_t)c * kScaleChunk1;
+            const size_t off = src_of(t, ps, pb) + (size_t)c * kScaleChunk1 * kCw;
             uint16_t *d = mysc + buf * 2 * kScaleChunk1;
 #pragma unroll
             for (int g = 0; g < kScaleChunk1; ++g) {
-                const bool in = row_ok && c * kScaleChunk1 + g < GI;
-                d[g] = in ? ps[off + g] : (uint16_t)0;
-                d[kScaleChunk1 + g] = in ? pb[off + g] : (uint16_t)0;
+                const bool in0 = row_ok && c * kScaleChunk1 + (BITS == kNvfp4 ? g / 2 : g) < GI;
+                const bool in1 = row_ok && c * kScaleChunk1 + (BITS == kNvfp4 ? 4 + g / 2 : g) < GI;
+                d[g] = in0 ? ps[off + g] : (uint16_t)0;
+                d[kScaleChunk1 + g] = in1 ? pb[off + g] : (uint16_t)0;
             }
         };
         int q = 0, j = 0;                                  // j: scale chunks started by this thread
@@ -920,11 +956,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int gi = s & 7;
                 const uint32_t sw = gi < 4 ? (gi < 2 ? sreg.x : sreg.y) : (gi < 6 ? sreg.z : sreg.w);
                 const uint32_t bw = gi < 4 ? (gi < 2 ? breg.x : breg.y) : (gi < 6 ? breg.z : breg.w);
-                const __half2 sd = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
-                const __half2 sd16 = __hmul2(sd, __float2half2_rn(0.0625f));
-                const __half2 bd = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
                 uint8_t *aa = sA + st * 16384;
-                if constexpr (BITS == 8) {                 // inputs 32 half .. + 31: code chunks 2 half, 2 half + 1
+                if constexpr (BITS == kNvfp4) {            // inputs 32 half .. + 31: blocks 2 half, 2 half + 1
+                    const uint32_t w4 = gi < 4 ? (gi < 2 ? (gi == 0 ? sreg.x : sreg.y) : (gi == 2 ? sreg.z : sreg.w))
+                                               : (gi < 6 ? (gi == 4 ? breg.x : breg.y) : (gi == 6 ? breg.z : breg.w));
+                    const uint32_t sb = nv_e4m3x2_f16(half ? w4 >> 16 : w4);
+                    const uint4 w = *reinterpret_cast<const uint4 *>(sC + cs * CST + r * CB + half * 16);
+                    const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(aa + swz128(r, half * 4 + c)) = nv_dequant8(cw[c], nv_bcast(sb, c >= 2));
+                } else if constexpr (BITS == 8) {                 // inputs 32 half .. + 31: code chunks 2 half, 2 half + 1
+                    const __half2 sd = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
+                    const __half2 bd = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
                     const uint4 w0 = *reinterpret_cast<const uint4 *>(sC + cs * CST + swz64(r, 2 * half));
                     const uint4 w1 = *reinterpret_cast<const uint4 *>(sC + cs * CST + swz64(r, 2 * half + 1));
                     const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -932,6 +976,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 4; ++c)
                         *reinterpret_cast<uint4 *>(aa + swz128(r, half * 4 + c)) = dequant8_b8(cw[2 * c], cw[2 * c + 1], sd, bd);
                 } else {
+                    const __half2 sd = bf16_to_h2((uint16_t)(gi & 1 ? sw >> 16 : sw));
+                    const __half2 sd16 = __hmul2(sd, __float2half2_rn(0.0625f));
+                    const __half2 bd = bf16_to_h2((uint16_t)(gi & 1 ? bw >> 16 : bw));
                     const uint4 w = *reinterpret_cast<const uint4 *>(sC + cs * CST + r * CB + half * 16);
                     const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -960,7 +1007,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = i & 1;
             float *wv = s_w + buf * 256;
             // factor 2^2e of each column (one per epilogue thread): the h tile holds h 2^-2e, the factor
-            // undoes it (exact)
+            // undoes it (exact); NVFP4: times the matrix scale
+            float fd = 1.f;
+            if constexpr (BITS == kNvfp4) fd = __ldg(ti.shared_e ? P.sdgs : P.dgs + ti.expert);
             for (int n = et; n < 256; n += kEpiThreads) {
                 float wgt = 0.f;
                 if (n < ti.ntok) {
@@ -975,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (t >= 0) {
                         const float up = pow2f(__ldg(P.xe + t));
-                        wgt = up * up;
+                        wgt = up * up * fd;
                     }
                 }
                 wv[n] = wgt;
@@ -1141,14 +1190,14 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     }
     cudaError_t e = cudaSuccess;
 
-    if (a.bits != 4 && a.bits != 8) return cudaErrorInvalidValue;
-    const bool b8 = a.bits == 8;
+    if (a.bits != 4 && a.bits != 8 && a.bits != kNvfp4) return cudaErrorInvalidValue;
+    const bool b8 = a.bits == 8, nv = a.bits == kNvfp4;
     CUtensorMap mgc, muc, msgc, msuc, mdc, msdc, mh, my;
     const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
     // code boxes: 32 bytes (4-bit, unswizzled) or 64 bytes with the 64-byte swizzle (8-bit) of 128 rows
     const CUtensorMapSwizzle csw = b8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
     const uint32_t cbox = (uint32_t)code_row_bytes(a.bits);
-    const uint64_t hrow = (uint64_t)H * a.bits / 8, irow = (uint64_t)I * a.bits / 8;   // code bytes per row
+    const uint64_t hrow = (uint64_t)H * cbits(a.bits) / 8, irow = (uint64_t)I * cbits(a.bits) / 8;   // code bytes per row
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int ns = a.has_shared ? 1 : 0;
     bool ok = make_map_2d(&mgc, a.gate.codes, u8, 1, hrow, (uint64_t)E * I, cbox, 128, csw) &&
@@ -1189,6 +1238,10 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p1.sgb = a.s_gate.biases;
     p1.sus = a.s_up.scales;
     p1.sub = a.s_up.biases;
+    p1.ggs = a.gate.gscale;
+    p1.ugs = a.up.gscale;
+    p1.sggs = a.has_shared ? a.s_gate.gscale : a.gate.gscale;
+    p1.sugs = a.has_shared ? a.s_up.gscale : a.up.gscale;
     p1.status = a.status;
     p1.T = T;
     p1.H = H;
@@ -1204,7 +1257,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p1.wait_limit = a.wait_limit;
     const size_t s1 = b8 ? g1_smem(kCodeStages1B8, 8) : g1_smem(kCodeStages1, 4);
     auto k1 = b8 ? gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1B8, 8>
-                 : gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1, 4>;
+                 : nv ? gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1, kNvfp4>
+                      : gemm_gateup_kernel<kStagesA1, kStagesB1, kCodeStages1, 4>;
     cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     const int tiles1 = a.max_w1 * ((I + 127) / 128);
     const bool small = prefill_small_fits(H, I, a.bits);   // items of small experts: mma.sync tiles (nwork[3] on)
@@ -1227,6 +1281,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p2.db = a.down.biases;
     p2.sds = a.s_down.scales;
     p2.sdb = a.s_down.biases;
+    p2.dgs = a.down.gscale;
+    p2.sdgs = a.has_shared ? a.s_down.gscale : a.down.gscale;
     p2.status = a.status;
     p2.T = T;
     p2.H = H;
@@ -1242,7 +1298,8 @@ cudaError_t launch_prefill_experts(const PrefillArgs &a, cudaStream_t st)
     p2.wait_limit = a.wait_limit;
     const size_t s2 = b8 ? g2_smem(kCodeStages2B8, 8) : g2_smem(kCodeStages2, 4);
     auto k2 = b8 ? gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2B8, 8>
-                 : gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2, 4>;
+                 : nv ? gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2, kNvfp4>
+                      : gemm_down_kernel<kStagesA2, kStagesB2, kCodeStages2, 4>;
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
     const int tiles2 = a.max_w2 * ((H + 127) / 128);
     if (small && (e = launch_small_down(a, st)) != cudaSuccess) return e;

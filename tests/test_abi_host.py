@@ -70,6 +70,10 @@ def cfg_from(**kw):
     (dict(top_k=17), qm.MOE_ERR_UNSUPPORTED),
     (dict(n_experts=4, top_k=5), qm.MOE_ERR_UNSUPPORTED),
     (dict(has_shared=2), qm.MOE_ERR_UNSUPPORTED),
+    (dict(format=qm.MOE_FORMAT_NVFP4), qm.MOE_OK),
+    (dict(format=qm.MOE_FORMAT_NVFP4, bits=8), qm.MOE_ERR_UNSUPPORTED),
+    (dict(format=2), qm.MOE_ERR_UNSUPPORTED),
+    (dict(format=-1), qm.MOE_ERR_UNSUPPORTED),
     (dict(hidden=0), qm.MOE_ERR_INVALID_ARG),
     (dict(top_k=-1), qm.MOE_ERR_INVALID_ARG),
 ])
@@ -118,6 +122,23 @@ def test_forward_rejects_bad_arguments(lib):
     # the router is not needed when logits are supplied
     assert forward(lib, cfg, fake_weights("router"), T=0, logits_in=FAKE) == qm.MOE_OK
     assert forward(lib, cfg_from(bits=3), w) == qm.MOE_ERR_UNSUPPORTED
+
+
+def test_nvfp4_weights_need_the_matrix_scales(lib):
+    """NVFP4 expert matrices carry a 4-byte aligned fp32 scale per matrix; biases may be NULL."""
+    cfg = cfg_from(format=qm.MOE_FORMAT_NVFP4)
+    q = lambda g: qm.moe_qmat(FAKE, FAKE, None, g)
+    w = qm.moe_weights(qm.moe_qmat(FAKE, FAKE, FAKE), q(FAKE), q(FAKE), q(FAKE), q(FAKE), q(FAKE), q(FAKE), FAKE)
+    assert forward(lib, cfg, w, T=0) == qm.MOE_OK                          # checks pass, nothing enqueued
+    for m in ("gate", "up", "down", "s_gate", "s_up", "s_down"):
+        bad = qm.moe_weights(*[getattr(w, n) for n in ("router", "gate", "up", "down", "s_gate", "s_up", "s_down")],
+                             FAKE)
+        getattr(bad, m).gscale = None
+        assert forward(lib, cfg, bad, T=0) == qm.MOE_ERR_INVALID_ARG, m
+        getattr(bad, m).gscale = FAKE + 2
+        assert forward(lib, cfg, bad, T=0) == qm.MOE_ERR_INVALID_ARG, m
+    # the affine rule still wants its biases
+    assert forward(lib, cfg_from(), w, T=0) == qm.MOE_ERR_INVALID_ARG
 
 
 def test_forward_workspace_too_small(lib):
@@ -178,7 +199,7 @@ def test_other_entry_points_reject_bad_arguments(lib):
 def test_wait_limit_is_a_field_of_the_call_config(lib):
     """The bound on in-kernel waits travels with each call (no process-wide setting)."""
     names = [f[0] for f in qm.moe_config._fields_]
-    assert names[-1] == "wait_polls"
+    assert "wait_polls" in names
     assert lib.moe_check_config(ctypes.byref(cfg_from(wait_polls=1))) == qm.MOE_OK
     assert lib.moe_check_config(ctypes.byref(cfg_from(wait_polls=-5))) == qm.MOE_OK
     assert "moe_set_wait_limit" not in open(HEADER).read()
