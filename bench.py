@@ -8,7 +8,8 @@ expert FFNs, combine) over one batch of T tokens, through the C ABI.  The
 default workload is the T = 1 decode layer (hidden 2048, 256 experts, top-8 +
 shared, intermediate 512, int4 g64 experts, 8-bit router); --config picks
 another of the named workloads in quantised_moe_expert_gb300.synth.WORKLOADS,
---workload any workload by name (the 8-bit expert layers of WORKLOADS_B8 too).
+--workload any workload by name (the 8-bit and NVFP4 expert layers of WORKLOADS_B8 and
+WORKLOADS_NVFP4 too).
 
 Timing: W warm-up steps, then exactly K steps replayed from one CUDA graph,
 bracketed by a barrier and a device synchronize, timed with CUDA events on
@@ -54,7 +55,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--workload", default=None,
-                    help="a workload by name (any of synth.WORKLOADS or synth.WORKLOADS_B8); overrides --config")
+                    help="a workload by name (any of synth.WORKLOADS, WORKLOADS_B8 or WORKLOADS_NVFP4); overrides --config")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -231,13 +232,18 @@ class Workload:
                             None, None, self.qm.MOE_PATH_AUTO, self.ws[c], stream)
 
     def path(self):
+        # NVFP4 experts take the grouped GEMMs at every T (the library resolves the decode path to them)
         return self.qm.MOE_PATH_DECODE if self.wl.tokens <= 16 else self.qm.MOE_PATH_PREFILL
 
     def kernels_per_step(self):
         # decode: the one fused kernel (8-bit experts: router GEMV, top-k, permute, gate/up, down,
         # slot sum); prefill: router GEMV (gamma), router MMA, top-k, permute, x conversion, two
         # small-tile (4-bit experts only) and two tensor-memory GEMMs, slot sum
+        # NVFP4 experts (grouped GEMMs at every T): router GEMV (logits at T <= 16, and gamma), router MMA
+        # (T > 16), top-k, permute, x conversion, two tensor-memory GEMMs, slot sum
         b8 = self.wl.shape.bits == 8
+        if self.wl.shape.fmt == "nvfp4":
+            return 7 if self.wl.tokens <= 16 else 8
         if self.wl.tokens <= 16:
             return 6 if b8 else 1
         return 8 if b8 else 10
@@ -573,7 +579,8 @@ def stage_roofline(wl, st, hbm, tc, peak_src):
         ach = st["expert_bytes"] / (st["ms"] / 1e3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                 "traffic": traffic_for("decode_expert_ffn", wl.name),
-                "kernel": ("expert-FFN stage (decode gate/up, down and reduce kernels)" if wl.shape.bits == 8
+                "kernel": ("expert-FFN stage (tensor-memory GEMMs and slot sum)" if wl.shape.fmt == "nvfp4"
+                           else "expert-FFN stage (decode gate/up, down and reduce kernels)" if wl.shape.bits == 8
                            else "expert-FFN stage (fused decode kernel: units + combine)"),
                 "kernel_us": st["ms"] * 1e3, "algorithmic_bytes_per_launch": st["expert_bytes"],
                 "peak_source": peak_src}
@@ -609,7 +616,7 @@ def traffic_for(kernel_key, workload):
 
 
 def workload_named(name):
-    for wl in synth.WORKLOADS + synth.WORKLOADS_B8:
+    for wl in synth.WORKLOADS + synth.WORKLOADS_B8 + synth.WORKLOADS_NVFP4:
         if wl.name == name:
             return wl
     raise SystemExit(f"unknown workload {name!r}")
@@ -644,10 +651,12 @@ def main():
     roof = stage_roofline(wl, r["stage"], hbm, tc, peak_src)
     line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": steps,
             "warmup": warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": f"int{wl.shape.bits}-affine/bf16 in, fp32 accumulate", "data": "synthetic",
+            "vs_baseline": None, "data": "synthetic",
+            "dtype": ("nvfp4 (e2m1 codes, e4m3 block scales)/bf16 in, fp32 accumulate" if wl.shape.fmt == "nvfp4"
+                      else f"int{wl.shape.bits}-affine/bf16 in, fp32 accumulate"),
             "config": {"workload": wl.name, "tokens": wl.tokens, "hidden": wl.shape.hidden,
                        "inter": wl.shape.inter, "experts": wl.shape.n_experts, "top_k": wl.shape.top_k,
-                       "shared": wl.shape.has_shared, "expert_bits": wl.shape.bits,
+                       "shared": wl.shape.has_shared, "expert_bits": wl.shape.bits, "expert_format": wl.shape.fmt,
                        "parallelism": f"replicas x{world}",
                        "l2": f"{r['copies']} rotating weight copies and inputs: no step finds its weights in L2"},
             "roofline": roof,
@@ -670,7 +679,8 @@ def main():
         line["cpu_baseline"] = cb
     if not args.no_sweep and rank == 0:
         sweep = {}
-        others = [o for o in synth.WORKLOADS[1:] + synth.WORKLOADS_B8 if o.name != wl.name]   # not the tiny layer
+        others = [o for o in synth.WORKLOADS[1:] + synth.WORKLOADS_B8 + synth.WORKLOADS_NVFP4
+                  if o.name != wl.name]                                              # not the tiny layer
         for other in others:
             try:
                 rr = run_ours(args, other, 0, 1, None, default_steps(other) // 2, 3, want_extras=False)
