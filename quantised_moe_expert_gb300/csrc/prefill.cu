@@ -49,6 +49,7 @@
 #include <algorithm>
 
 #include "kernels.cuh"
+#include "nvfp4.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.cuh"
 
@@ -397,11 +398,16 @@ __global__ void __launch_bounds__(kThreads1, 1)
                 const size_t wrow = (size_t)(t2.shared_e ? 0 : t2.expert * I) + t2.mb * 128;
                 prefetch_rows((t2.shared_e ? P.sgc : P.gc) + wrow * crow, (uint32_t)(rows * crow));
                 prefetch_rows((t2.shared_e ? P.suc : P.uc) + wrow * crow, (uint32_t)(rows * crow));
-                const uint32_t sb = (uint32_t)rows * G * 2;
-                prefetch_rows((t2.shared_e ? P.sgs : P.gs) + wrow * G, sb);
-                prefetch_rows((t2.shared_e ? P.sgb : P.gb) + wrow * G, sb);
-                prefetch_rows((t2.shared_e ? P.sus : P.us) + wrow * G, sb);
-                prefetch_rows((t2.shared_e ? P.sub : P.ub) + wrow * G, sb);
+                // scale bytes of a row: bf16 scale (and bias) per group, or NVFP4's 4 E4M3 bytes per group
+                constexpr int kSb = BITS == kNvfp4 ? 4 : 2;
+                const uint32_t sb = (uint32_t)rows * G * kSb;
+                const size_t so = wrow * G * kSb;
+                prefetch_rows(reinterpret_cast<const uint8_t *>(t2.shared_e ? P.sgs : P.gs) + so, sb);
+                prefetch_rows(reinterpret_cast<const uint8_t *>(t2.shared_e ? P.sus : P.us) + so, sb);
+                if constexpr (BITS != kNvfp4) {           // NVFP4 has no biases
+                    prefetch_rows((t2.shared_e ? P.sgb : P.gb) + wrow * G, sb);
+                    prefetch_rows((t2.shared_e ? P.sub : P.ub) + wrow * G, sb);
+                }
             };
             prefetch_tile(blockIdx.x);
             int q = 0;
@@ -790,9 +796,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rows = min(128, H - t2.mb * 128);
                 const size_t wrow = (size_t)(t2.shared_e ? 0 : t2.expert * H) + t2.mb * 128;
                 prefetch_rows((t2.shared_e ? P.sdc : P.dc) + wrow * crow, (uint32_t)(rows * crow));
-                const uint32_t sb = (uint32_t)rows * GI * 2;
-                prefetch_rows((t2.shared_e ? P.sds : P.ds) + wrow * GI, sb);
-                prefetch_rows((t2.shared_e ? P.sdb : P.db) + wrow * GI, sb);
+                constexpr int kSb = BITS == kNvfp4 ? 4 : 2;
+                const uint32_t sb = (uint32_t)rows * GI * kSb;
+                prefetch_rows(reinterpret_cast<const uint8_t *>(t2.shared_e ? P.sds : P.ds) + wrow * GI * kSb, sb);
+                if constexpr (BITS != kNvfp4) prefetch_rows((t2.shared_e ? P.sdb : P.db) + wrow * GI, sb);
             };
             prefetch_tile(blockIdx.x);
             int q = 0;
